@@ -1,0 +1,162 @@
+"""Seeded synthetic inputs for exact training attention.
+
+This module is shared by the parity tests, the benchmark and the CPU oracle runs. It holds no
+attention arithmetic: only random draws, the round-to-nearest-even narrowing of those draws to
+bf16, and the shapes of the five workloads. Both the CUDA path and the oracle receive the very
+same bf16 bit patterns from here.
+
+Conventions taken from the mlx-native training tests (page "mlx-native
+tests/test_flash_attn_train.rs", section "Test helpers" and `oracle_for_bf16`):
+
+* inputs are drawn in f32 and rounded once to bf16; the oracle widens those bf16 values exactly;
+* the seed constant 0x5452_4149_4E30_3031 ("TRAIN001") is the base of every seed.
+
+The draws themselves are N(0, 1) from NumPy's PCG64 generator, as the workload list asks; the
+page's own LCG is not reused (it yields only negative values).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+
+SEED_BASE = 0x5452_4149_4E30_3031
+
+# tensor_idx part of a seed: seed = SEED_BASE + 16 * workload_index + tensor_idx
+T_Q, T_K, T_V, T_DO, T_MASK = 0, 1, 2, 3, 4
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One attention problem: sizes, scale, causal flag and how its inputs are drawn."""
+
+    name: str
+    batch: int
+    n_heads: int
+    n_kv_heads: int
+    ql: int
+    kl: int
+    head_dim: int
+    scale: float
+    causal: bool
+    masked: bool = False  # additive f32 mask [batch, n_heads, ql, kl]
+    do_std: float = 1.0  # dO ~ N(0, 1) * do_std
+
+    @property
+    def group(self) -> int:
+        return self.n_heads // self.n_kv_heads
+
+    def q_shape(self):
+        return (self.batch, self.n_heads, self.ql, self.head_dim)
+
+    def kv_shape(self):
+        return (self.batch, self.n_kv_heads, self.kl, self.head_dim)
+
+    def lse_shape(self):
+        return (self.batch, self.n_heads, self.ql)
+
+    def mask_shape(self):
+        return (self.batch, self.n_heads, self.ql, self.kl)
+
+    def visible_pairs(self) -> int:
+        """Number of (query, key) pairs a causal bottom-right mask leaves visible (per b, h)."""
+        if not self.causal:
+            return self.ql * self.kl
+        off = self.kl - self.ql
+        tot = 0
+        for i in range(self.ql):
+            tot += max(0, min(self.kl, off + i + 1))
+        return tot
+
+    def flops(self, exact: bool = False):
+        """(fwd, bwd) FLOPs: 4*B*H*ql*kl*d*f and 10*B*H*ql*kl*d*f.
+
+        f = 0.5 for causal (the headline counting rule), 1 otherwise; with exact=True f is the
+        visible fraction of (query, key) pairs.
+        """
+        if exact:
+            f = self.visible_pairs() / (self.ql * self.kl)
+        else:
+            f = 0.5 if self.causal else 1.0
+        base = self.batch * self.n_heads * self.ql * self.kl * self.head_dim * f
+        return 4.0 * base, 10.0 * base
+
+
+# The five workloads, in order (index = workload_index in the seed formula).
+WORKLOADS = [
+    Workload("tiny_gqa_d64", 1, 2, 1, 64, 64, 64, 1.0 / 8.0, True),
+    Workload("masked_d256", 2, 4, 2, 128, 128, 256, 1.0 / 16.0, False, masked=True),
+    Workload("train_d64", 4, 16, 16, 2048, 2048, 64, 1.0 / 8.0, True, do_std=0.1),
+    Workload("gqa_d128_4k", 2, 32, 8, 4096, 4096, 128, 1.0 / math.sqrt(128.0), True, do_std=0.1),
+    Workload("rect_d256", 1, 16, 4, 1024, 8192, 256, 1.0 / 16.0, True, do_std=0.1),
+]
+BY_NAME = {w.name: w for w in WORKLOADS}
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round f32 values to bf16 bit patterns, round-to-nearest-even (NaN-free inputs only).
+
+    Same bit trick as the page "tang src/compute/cuda.rs", `f32_to_bf16`.
+    """
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (b >> np.uint64(16)) & np.uint64(1)
+    return ((b + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns to f32 exactly."""
+    return (np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(
+        np.float32
+    )
+
+
+def normal_bf16(seed: int, shape, std: float = 1.0) -> np.ndarray:
+    """N(0,1)*std drawn in f32 from PCG64(seed), rounded to bf16; returned as bf16 bits."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        x = x * np.float32(std)
+    return f32_to_bf16_bits(x)
+
+
+def additive_mask(seed: int, shape, p_neg_inf: float = 0.1, full_rows: int = 2) -> np.ndarray:
+    """f32 natural-log additive mask: U[-2, 0], then each entry -inf with probability p_neg_inf,
+    then `full_rows` distinct rows per (b, h) set entirely to -inf."""
+    rng = np.random.default_rng(seed)
+    m = rng.uniform(-2.0, 0.0, size=shape).astype(np.float32)
+    m[rng.random(size=shape) < p_neg_inf] = -np.inf
+    b_, h_, ql, _ = shape
+    for b in range(b_):
+        for h in range(h_):
+            rows = rng.choice(ql, size=min(full_rows, ql), replace=False)
+            m[b, h, rows, :] = -np.inf
+    return m
+
+
+@dataclass
+class Inputs:
+    """bf16 bit patterns of q, k, v, dO (uint16) and an optional f32 mask."""
+
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    do: np.ndarray
+    mask: np.ndarray | None
+
+    def widened(self):
+        """(q, k, v, dO) as f32 arrays holding the exact bf16 values."""
+        return tuple(bf16_bits_to_f32(t) for t in (self.q, self.k, self.v, self.do))
+
+
+def make_inputs(w: Workload, index: int | None = None, seed_base: int | None = None) -> Inputs:
+    """Seeded inputs of workload `w` (index = its position in WORKLOADS unless given)."""
+    if index is None:
+        index = WORKLOADS.index(w) if w in WORKLOADS else 15
+    base = (SEED_BASE if seed_base is None else seed_base) + 16 * index
+    q = normal_bf16(base + T_Q, w.q_shape())
+    k = normal_bf16(base + T_K, w.kv_shape())
+    v = normal_bf16(base + T_V, w.kv_shape())
+    do = normal_bf16(base + T_DO, w.q_shape(), w.do_std)
+    mask = additive_mask(base + T_MASK, w.mask_shape()) if w.masked else None
+    return Inputs(q, k, v, do, mask)

@@ -1,0 +1,187 @@
+"""CPU oracle for exact training attention -- TEST INFRASTRUCTURE.
+
+Only `tests/`, `__graft_entry__.smoke()` and the benchmark's CPU-baseline leg may import this
+package. The product path (`flash_attention_gb300`) never imports, links or calls it, and the
+oracle imports nothing from the product.
+
+The arithmetic lives in `fa_oracle.c` (plain C, f64). This module compiles it with gcc and
+marshals numpy arrays through ctypes. Inputs are f32 arrays that hold exact bf16 values
+(`fa_inputs.bf16_bits_to_f32`); outputs are f64.
+
+What each function computes, and the passages it follows, is written at the top of
+`fa_oracle.c`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libfa_oracle.so")
+_lib = None
+_lock = threading.Lock()
+
+# Planted-mistake codes understood by fa_oracle_set_mutation (tests only).
+MUTATIONS = {
+    "no_scale": 1,
+    "top_left_causal": 2,
+    "gqa_modulo": 3,
+    "no_normalise": 4,
+    "mask_sign": 5,
+    "lse_no_max": 6,
+    "ds_no_d": 7,
+    "dk_uses_k": 8,
+    "dv_uses_ds": 9,
+    "causal_off_by_one": 10,
+    "dq_no_scale": 11,
+    "d_from_do_only": 12,
+}
+
+
+def build(force: bool = False) -> str:
+    """Compile fa_oracle.c into libfa_oracle.so next to it (gcc, no fast-math, no FMA
+    contraction, so that x86 and Arm give the same bits)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
+           "-fno-fast-math", "-Wall", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            f = ctypes.c_void_p
+            i = ctypes.c_int
+            d = ctypes.c_double
+            lib.fa_oracle_fwd_rows.argtypes = [f, f, f, f, i, i, i, i, i, i, d, i, f,
+                                               ctypes.c_long, i, f, f, i]
+            lib.fa_oracle_bwd_q_rows.argtypes = [f, f, f, f, f, i, i, i, i, i, i, d, i, f,
+                                                 ctypes.c_long, f, i]
+            lib.fa_oracle_bwd_kv_rows.argtypes = [f, f, f, f, f, i, i, i, i, i, i, d, i, i, i,
+                                                  f, i, f, f, i]
+            lib.fa_oracle_bwd.argtypes = [f, f, f, f, f, i, i, i, i, i, i, d, i, f, f, f, i]
+            lib.fa_oracle_set_mutation.argtypes = [i]
+            lib.fa_oracle_get_mutation.restype = i
+            for fn in (lib.fa_oracle_fwd_rows, lib.fa_oracle_bwd_q_rows,
+                       lib.fa_oracle_bwd_kv_rows, lib.fa_oracle_bwd):
+                fn.restype = i
+            _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def _f32(x):
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    return a
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _shape(q, k):
+    B, H, ql, d = q.shape
+    Bk, Hk, kl, dk = k.shape
+    if B != Bk or d != dk:
+        raise ValueError("q and k disagree on batch or head_dim")
+    if H % Hk:
+        raise ValueError("n_heads must be a multiple of n_kv_heads")
+    return B, H, Hk, ql, kl, d
+
+
+def set_mutation(name_or_code) -> None:
+    """Plant one known mistake in the oracle (tests only); 0 or None removes it."""
+    code = MUTATIONS.get(name_or_code, name_or_code) if name_or_code else 0
+    _load().fa_oracle_set_mutation(int(code))
+
+
+def fwd(q, k, v, mask=None, *, scale, causal, base2=False, nthreads=None):
+    """Full forward: (O [B,H,ql,d] f64, L [B,H,ql] f64)."""
+    return fwd_rows(q, k, v, mask, scale=scale, causal=causal, rows=None, base2=base2,
+                    nthreads=nthreads)
+
+
+def fwd_rows(q, k, v, mask=None, *, scale, causal, rows=None, base2=False, nthreads=None):
+    """O and L of the flat rows (b*H + h)*ql + i listed in `rows` (None: every row, returned
+    in [B,H,ql,(d)] shape)."""
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    mask = None if mask is None else _f32(mask)
+    B, H, Hk, ql, kl, d = _shape(q, k)
+    full = rows is None
+    r = None if full else np.ascontiguousarray(rows, dtype=np.int64)
+    n = B * H * ql if full else len(r)
+    o = np.empty((n, d), np.float64)
+    lse = np.empty((n,), np.float64)
+    rc = _load().fa_oracle_fwd_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), B, H, Hk, ql, kl, d,
+                                    float(scale), int(bool(causal)), _ptr(r), n, int(bool(base2)),
+                                    _ptr(o), _ptr(lse), nthreads or default_threads())
+    if rc:
+        raise ValueError(f"oracle fwd failed ({rc})")
+    if full:
+        return o.reshape(B, H, ql, d), lse.reshape(B, H, ql)
+    return o, lse
+
+
+def bwd_q_rows(q, k, v, mask, do, *, scale, causal, rows=None, nthreads=None):
+    """dQ of the listed flat query rows (None: all rows, shaped [B,H,ql,d])."""
+    q, k, v, do = _f32(q), _f32(k), _f32(v), _f32(do)
+    mask = None if mask is None else _f32(mask)
+    B, H, Hk, ql, kl, d = _shape(q, k)
+    full = rows is None
+    r = None if full else np.ascontiguousarray(rows, dtype=np.int64)
+    n = B * H * ql if full else len(r)
+    dq = np.empty((n, d), np.float64)
+    rc = _load().fa_oracle_bwd_q_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(do), B, H, Hk,
+                                      ql, kl, d, float(scale), int(bool(causal)), _ptr(r), n,
+                                      _ptr(dq), nthreads or default_threads())
+    if rc:
+        raise ValueError(f"oracle bwd_q_rows failed ({rc})")
+    return dq.reshape(B, H, ql, d) if full else dq
+
+
+def bwd_kv_rows(q, k, v, mask, do, *, scale, causal, b, kh, js, nthreads=None):
+    """dK and dV rows js of kv head kh in batch b: two arrays [len(js), d]."""
+    q, k, v, do = _f32(q), _f32(k), _f32(v), _f32(do)
+    mask = None if mask is None else _f32(mask)
+    B, H, Hk, ql, kl, d = _shape(q, k)
+    jarr = np.ascontiguousarray(js, dtype=np.int32)
+    dk = np.empty((len(jarr), d), np.float64)
+    dv = np.empty((len(jarr), d), np.float64)
+    rc = _load().fa_oracle_bwd_kv_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(do), B, H,
+                                       Hk, ql, kl, d, float(scale), int(bool(causal)), int(b),
+                                       int(kh), _ptr(jarr), len(jarr), _ptr(dk), _ptr(dv),
+                                       nthreads or default_threads())
+    if rc:
+        raise ValueError(f"oracle bwd_kv_rows failed ({rc})")
+    return dk, dv
+
+
+def bwd(q, k, v, mask, do, *, scale, causal, nthreads=None):
+    """Full backward: (dQ [B,H,ql,d], dK [B,Hk,kl,d], dV [B,Hk,kl,d]) in f64."""
+    q, k, v, do = _f32(q), _f32(k), _f32(v), _f32(do)
+    mask = None if mask is None else _f32(mask)
+    B, H, Hk, ql, kl, d = _shape(q, k)
+    dq = np.empty((B, H, ql, d), np.float64)
+    dk = np.empty((B, Hk, kl, d), np.float64)
+    dv = np.empty((B, Hk, kl, d), np.float64)
+    rc = _load().fa_oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(do), B, H, Hk, ql, kl,
+                               d, float(scale), int(bool(causal)), _ptr(dq), _ptr(dk), _ptr(dv),
+                               nthreads or default_threads())
+    if rc:
+        raise ValueError(f"oracle bwd failed ({rc})")
+    return dq, dk, dv

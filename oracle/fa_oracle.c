@@ -1,0 +1,436 @@
+/*
+ * fa_oracle.c -- plain, slow CPU oracle for exact training attention (forward O, L and
+ * backward dQ, dK, dV).
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product path may call, link or load this file;
+ * only the tests, the smoke check and the benchmark's CPU-baseline leg use it. It shares no
+ * code, header or constant with the CUDA path.
+ *
+ * What it computes (the plain definition, in f64 over inputs that hold exact bf16 values):
+ * for batch b, query head h, query row i, with G = n_heads / n_kv_heads and kv head
+ * kh = h / G (page "mlx-native tests/test_flash_attn_train.rs", `sdpa_reference_with_logsumexp`,
+ * the `kv_h = h / heads_per_kv` head map):
+ *
+ *   visible(i, j) = !causal || j <= kl - ql + i            (bottom-right causal alignment)
+ *   s_ij  = scale * <q_i, k_j> + mask_ij   if visible, else -inf
+ *   L_i   = log sum_j exp(s_ij)            (-inf when no s_ij is finite)
+ *   O_i   = sum_j exp(s_ij - L_i) v_j      (0 when L_i = -inf)
+ *
+ * Backward (same page, `sdpa_backward_reference_f32`, the FlashAttention-2 backward
+ * equations), with dO the upstream gradient of O:
+ *
+ *   P_ij  = exp(s_ij - L_i)     (0 where s_ij = -inf or L_i = -inf)
+ *   D_i   = <dO_i, O_i>         (O the oracle's own f64 output)
+ *   dP_ij = <dO_i, v_j>,   dS_ij = P_ij (dP_ij - D_i)
+ *   dQ_i  = scale * sum_j dS_ij k_j
+ *   dK_j  = scale * sum_{h in group(kh)} sum_i dS_ij q_i
+ *   dV_j  =         sum_{h in group(kh)} sum_i P_ij dO_i
+ *
+ * Readings where the pages are silent or disagree:
+ *   - causal alignment is bottom-right in BOTH passes (the backward oracle on the mlx-native
+ *     page uses top-left `k_j > q_i`, which agrees only when ql == kl; the forward oracle on
+ *     that page and the nuvec-core direct formula `visible = i + lk - lq + 1` are bottom-right);
+ *   - kl - ql + i is signed: with causal and ql > kl the first ql - kl rows see no key and are
+ *     fully masked (the mlx-native forward clamps with saturating_sub instead; parity of that
+ *     corner is unpinned by the pages because the two disagree);
+ *   - the mask is natural-log additive, shape [B, H, ql, kl], an entry -inf hides the key.
+ *
+ * A second forward mode (base2 = 1) takes the mlx-native forward oracle's own steps: the score
+ * is multiplied by scale*log2(e), the mask by log2(e), the row max starts at the finite
+ * sentinel -FLT_MAX/2, p = exp2(s - max), L = max*ln(2) + ln(sum p), O = sum (p / safe_sum) v
+ * with safe_sum = 1 when the sum is 0. Both modes must agree to rounding on any input.
+ *
+ * Layouts (all contiguous, row-major): q, dO, O, dQ [B, H, ql, d]; k, v, dK, dV [B, Hk, kl, d];
+ * L [B, H, ql]; mask [B, H, ql, kl] or NULL.
+ *
+ * A mutation switch (fa_oracle_set_mutation) plants one known mistake at a time. It is off (0)
+ * by default and exists only so that the tests can show that each planted mistake fails one
+ * of the oracle's pins.
+ */
+#include <float.h>
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+  int B, H, Hk, ql, kl, d;
+  double scale;
+  int causal;
+  const float *q, *k, *v, *mask, *dO;
+} prob_t;
+
+/* Planted mistakes (tests only). 0 = none. */
+enum {
+  MUT_NONE = 0,
+  MUT_NO_SCALE = 1,        /* score without the scale factor */
+  MUT_TOP_LEFT = 2,        /* causal aligned top-left instead of bottom-right */
+  MUT_GQA_MODULO = 3,      /* kv head = h % Hk instead of h / G */
+  MUT_NO_NORMALISE = 4,    /* O not divided by the row sum */
+  MUT_MASK_SIGN = 5,       /* mask subtracted instead of added */
+  MUT_L_NO_MAX = 6,        /* L = log(sum exp(s - m)), max dropped */
+  MUT_DS_NO_D = 7,         /* dS = P * dP (the -D term dropped) */
+  MUT_DK_USES_K = 8,       /* dK accumulates dS * k_j instead of dS * q_i */
+  MUT_DV_USES_DS = 9,      /* dV accumulates dS instead of P */
+  MUT_CAUSAL_OFF_BY_ONE = 10, /* visible iff j < kl - ql + i */
+  MUT_DQ_NO_SCALE = 11,    /* dQ without the scale factor */
+  MUT_D_FROM_DO_ONLY = 12, /* D_i = sum dO (O dropped) */
+};
+static int g_mutation = 0;
+
+void fa_oracle_set_mutation(int m) { g_mutation = m; }
+int fa_oracle_get_mutation(void) { return g_mutation; }
+
+static inline size_t q_index(const prob_t *p, int b, int h, int i) {
+  return (((size_t)b * p->H + h) * p->ql + i) * (size_t)p->d;
+}
+static inline size_t kv_index(const prob_t *p, int b, int kh, int j) {
+  return (((size_t)b * p->Hk + kh) * p->kl + j) * (size_t)p->d;
+}
+static inline int kv_head(const prob_t *p, int h) {
+  if (g_mutation == MUT_GQA_MODULO) return h % p->Hk;
+  return h / (p->H / p->Hk);
+}
+static inline int visible(const prob_t *p, int i, int j) {
+  if (!p->causal) return 1;
+  long off = (long)p->kl - (long)p->ql;
+  if (g_mutation == MUT_TOP_LEFT) off = 0;
+  if (g_mutation == MUT_CAUSAL_OFF_BY_ONE) return (long)j < off + (long)i;
+  return (long)j <= off + (long)i;
+}
+
+/* Scores of row (b, h, i) into s[kl]: natural-log domain, -inf where hidden. */
+static void row_scores(const prob_t *p, int b, int h, int i, double *s) {
+  const int kh = kv_head(p, h);
+  const float *qi = p->q + q_index(p, b, h, i);
+  const double sc = (g_mutation == MUT_NO_SCALE) ? 1.0 : p->scale;
+  for (int j = 0; j < p->kl; ++j) {
+    if (!visible(p, i, j)) { s[j] = -INFINITY; continue; }
+    const float *kj = p->k + kv_index(p, b, kh, j);
+    double dot = 0.0;
+    for (int c = 0; c < p->d; ++c) dot += (double)qi[c] * (double)kj[c];
+    double v = sc * dot;
+    if (p->mask) {
+      double m = (double)p->mask[(((size_t)b * p->H + h) * p->ql + i) * (size_t)p->kl + j];
+      if (g_mutation == MUT_MASK_SIGN) m = -m;
+      v += m; /* an entry of -inf gives -inf */
+    }
+    s[j] = v;
+  }
+}
+
+/* Forward of one row, natural-log mode: L and O[d] from the scores. */
+static double row_forward_nat(const prob_t *p, int b, int h, int i, const double *s, double *o) {
+  const int kh = kv_head(p, h);
+  double m = -INFINITY;
+  for (int j = 0; j < p->kl; ++j) if (s[j] > m) m = s[j];
+  for (int c = 0; c < p->d; ++c) o[c] = 0.0;
+  if (m == -INFINITY) return -INFINITY; /* fully masked row: O = 0, L = -inf */
+  double z = 0.0;
+  for (int j = 0; j < p->kl; ++j) z += exp(s[j] - m);
+  for (int j = 0; j < p->kl; ++j) {
+    if (s[j] == -INFINITY) continue;
+    double w = exp(s[j] - m);
+    if (g_mutation != MUT_NO_NORMALISE) w /= z;
+    const float *vj = p->v + kv_index(p, b, kh, j);
+    for (int c = 0; c < p->d; ++c) o[c] += w * (double)vj[c];
+  }
+  if (g_mutation == MUT_L_NO_MAX) return log(z);
+  return m + log(z);
+}
+
+/* Forward of one row in the mlx-native base-2 form (steps of `sdpa_reference_with_logsumexp`,
+ * carried out in f64). Recomputes its own scores so that it owns every step. */
+static double row_forward_base2(const prob_t *p, int b, int h, int i, double *o) {
+  const double LOG2E = 1.4426950408889634074;
+  const double LN2 = 0.69314718055994530942;
+  const int kh = kv_head(p, h);
+  const float *qi = p->q + q_index(p, b, h, i);
+  const double sc = ((g_mutation == MUT_NO_SCALE) ? 1.0 : p->scale) * LOG2E; /* q pre-scale */
+  double *s2 = (double *)malloc(sizeof(double) * (size_t)p->kl);
+  for (int j = 0; j < p->kl; ++j) {
+    const float *kj = p->k + kv_index(p, b, kh, j);
+    double dot = 0.0;
+    for (int c = 0; c < p->d; ++c) dot += (double)qi[c] * (double)kj[c];
+    s2[j] = dot * sc;
+    if (p->mask) {
+      double m = (double)p->mask[(((size_t)b * p->H + h) * p->ql + i) * (size_t)p->kl + j];
+      if (g_mutation == MUT_MASK_SIGN) m = -m;
+      s2[j] += LOG2E * m;
+    }
+    if (!visible(p, i, j)) s2[j] = -INFINITY;
+  }
+  double mx = -(double)FLT_MAX / 2.0; /* finite sentinel */
+  for (int j = 0; j < p->kl; ++j) if (s2[j] > mx) mx = s2[j];
+  double sum = 0.0;
+  for (int j = 0; j < p->kl; ++j) { s2[j] = exp2(s2[j] - mx); sum += s2[j]; }
+  double lse = (g_mutation == MUT_L_NO_MAX) ? log(sum) : mx * LN2 + log(sum);
+  double safe = (sum == 0.0) ? 1.0 : sum;
+  if (g_mutation == MUT_NO_NORMALISE) safe = 1.0;
+  for (int c = 0; c < p->d; ++c) o[c] = 0.0;
+  for (int j = 0; j < p->kl; ++j) {
+    const float *vj = p->v + kv_index(p, b, kh, j);
+    double w = s2[j] / safe;
+    for (int c = 0; c < p->d; ++c) o[c] += w * (double)vj[c];
+  }
+  free(s2);
+  return lse;
+}
+
+/* ------------------------------------------------------------------ tiny thread pool */
+typedef struct {
+  void (*fn)(void *ctx, long task, int worker);
+  void *ctx;
+  long ntasks;
+  long next;
+  pthread_mutex_t mu;
+  int worker_seq;
+} pool_t;
+
+static void *pool_main(void *arg) {
+  pool_t *pl = (pool_t *)arg;
+  pthread_mutex_lock(&pl->mu);
+  int me = pl->worker_seq++;
+  pthread_mutex_unlock(&pl->mu);
+  for (;;) {
+    pthread_mutex_lock(&pl->mu);
+    long t = pl->next++;
+    pthread_mutex_unlock(&pl->mu);
+    if (t >= pl->ntasks) break;
+    pl->fn(pl->ctx, t, me);
+  }
+  return NULL;
+}
+
+static void parallel_for(long ntasks, int nthreads, void (*fn)(void *, long, int), void *ctx) {
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > ntasks) nthreads = (int)(ntasks > 0 ? ntasks : 1);
+  pool_t pl;
+  pl.fn = fn; pl.ctx = ctx; pl.ntasks = ntasks; pl.next = 0; pl.worker_seq = 0;
+  pthread_mutex_init(&pl.mu, NULL);
+  if (nthreads == 1) {
+    pool_main(&pl);
+  } else {
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    for (int t = 0; t < nthreads; ++t) pthread_create(&th[t], NULL, pool_main, &pl);
+    for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+    free(th);
+  }
+  pthread_mutex_destroy(&pl.mu);
+}
+
+static prob_t make_prob(const float *q, const float *k, const float *v, const float *mask,
+                        const float *dO, int B, int H, int Hk, int ql, int kl, int d,
+                        double scale, int causal) {
+  prob_t p;
+  p.B = B; p.H = H; p.Hk = Hk; p.ql = ql; p.kl = kl; p.d = d;
+  p.scale = scale; p.causal = causal;
+  p.q = q; p.k = k; p.v = v; p.mask = mask; p.dO = dO;
+  return p;
+}
+
+/* ------------------------------------------------------------------ forward, by rows */
+typedef struct {
+  const prob_t *p;
+  const int64_t *rows; /* flat (b*H + h)*ql + i */
+  double *o, *lse;
+  int base2;
+} fwd_ctx;
+
+static void fwd_task(void *vctx, long t, int worker) {
+  (void)worker;
+  fwd_ctx *c = (fwd_ctx *)vctx;
+  const prob_t *p = c->p;
+  int64_t r = c->rows ? c->rows[t] : (int64_t)t;
+  int i = (int)(r % p->ql);
+  int h = (int)((r / p->ql) % p->H);
+  int b = (int)(r / ((int64_t)p->ql * p->H));
+  double *o = c->o + (size_t)t * p->d;
+  if (c->base2) {
+    c->lse[t] = row_forward_base2(p, b, h, i, o);
+  } else {
+    double *s = (double *)malloc(sizeof(double) * (size_t)p->kl);
+    row_scores(p, b, h, i, s);
+    c->lse[t] = row_forward_nat(p, b, h, i, s, o);
+    free(s);
+  }
+}
+
+/* O and L of the listed rows (rows == NULL: all B*H*ql rows in order). Output o[nrows*d],
+ * lse[nrows]. Returns 0, or -1 on bad sizes. */
+int fa_oracle_fwd_rows(const float *q, const float *k, const float *v, const float *mask,
+                       int B, int H, int Hk, int ql, int kl, int d, double scale, int causal,
+                       const int64_t *rows, long nrows, int base2, double *o, double *lse,
+                       int nthreads) {
+  if (B <= 0 || H <= 0 || Hk <= 0 || ql <= 0 || kl <= 0 || d <= 0 || H % Hk) return -1;
+  prob_t p = make_prob(q, k, v, mask, NULL, B, H, Hk, ql, kl, d, scale, causal);
+  fwd_ctx c = {&p, rows, o, lse, base2};
+  parallel_for(nrows, nthreads, fwd_task, &c);
+  return 0;
+}
+
+/* ------------------------------------------------------------------ backward pieces */
+
+/* Everything the backward needs about one query row: P row (kl), dP row (kl), D. */
+typedef struct {
+  double *s, *o, *pr, *ds; /* scores, O row, P row, dS row */
+} rowbuf;
+
+static rowbuf rowbuf_new(const prob_t *p) {
+  rowbuf r;
+  r.s = (double *)malloc(sizeof(double) * (size_t)p->kl);
+  r.pr = (double *)malloc(sizeof(double) * (size_t)p->kl);
+  r.ds = (double *)malloc(sizeof(double) * (size_t)p->kl);
+  r.o = (double *)malloc(sizeof(double) * (size_t)p->d);
+  return r;
+}
+static void rowbuf_free(rowbuf *r) { free(r->s); free(r->pr); free(r->ds); free(r->o); }
+
+/* Fills r.pr with the P row and r.ds with the dS row of query row (b, h, i). */
+static void row_backward_prep(const prob_t *p, int b, int h, int i, rowbuf *r) {
+  const int kh = kv_head(p, h);
+  row_scores(p, b, h, i, r->s);
+  double L = row_forward_nat(p, b, h, i, r->s, r->o);
+  const float *doi = p->dO + q_index(p, b, h, i);
+  double D = 0.0;
+  for (int c = 0; c < p->d; ++c)
+    D += (double)doi[c] * ((g_mutation == MUT_D_FROM_DO_ONLY) ? 1.0 : r->o[c]);
+  for (int j = 0; j < p->kl; ++j) {
+    double P = (r->s[j] == -INFINITY || L == -INFINITY) ? 0.0 : exp(r->s[j] - L);
+    const float *vj = p->v + kv_index(p, b, kh, j);
+    double dP = 0.0;
+    for (int c = 0; c < p->d; ++c) dP += (double)doi[c] * (double)vj[c];
+    r->pr[j] = P;
+    r->ds[j] = (g_mutation == MUT_DS_NO_D) ? P * dP : P * (dP - D);
+  }
+}
+
+typedef struct {
+  const prob_t *p;
+  const int64_t *rows;
+  double *dq;
+} dq_ctx;
+
+static void dq_task(void *vctx, long t, int worker) {
+  (void)worker;
+  dq_ctx *c = (dq_ctx *)vctx;
+  const prob_t *p = c->p;
+  int64_t r = c->rows ? c->rows[t] : (int64_t)t;
+  int i = (int)(r % p->ql);
+  int h = (int)((r / p->ql) % p->H);
+  int b = (int)(r / ((int64_t)p->ql * p->H));
+  const int kh = kv_head(p, h);
+  rowbuf rb = rowbuf_new(p);
+  row_backward_prep(p, b, h, i, &rb);
+  double *dq = c->dq + (size_t)t * p->d;
+  const double sc = (g_mutation == MUT_DQ_NO_SCALE) ? 1.0 : p->scale;
+  for (int cc = 0; cc < p->d; ++cc) dq[cc] = 0.0;
+  for (int j = 0; j < p->kl; ++j) {
+    double ds = rb.ds[j];
+    if (ds == 0.0) continue;
+    const float *kj = p->k + kv_index(p, b, kh, j);
+    for (int cc = 0; cc < p->d; ++cc) dq[cc] += sc * ds * (double)kj[cc];
+  }
+  rowbuf_free(&rb);
+}
+
+/* dQ of the listed query rows (rows == NULL: all). Output dq[nrows*d]. */
+int fa_oracle_bwd_q_rows(const float *q, const float *k, const float *v, const float *mask,
+                         const float *dO, int B, int H, int Hk, int ql, int kl, int d,
+                         double scale, int causal, const int64_t *rows, long nrows, double *dq,
+                         int nthreads) {
+  if (B <= 0 || H <= 0 || Hk <= 0 || ql <= 0 || kl <= 0 || d <= 0 || H % Hk) return -1;
+  prob_t p = make_prob(q, k, v, mask, dO, B, H, Hk, ql, kl, d, scale, causal);
+  dq_ctx c = {&p, rows, dq};
+  parallel_for(nrows, nthreads, dq_task, &c);
+  return 0;
+}
+
+/* dK, dV rows of one (b, kh): tasks run over (h in group, i), each worker owning a private
+ * accumulator that is summed at the end (the sum order over workers is fixed). */
+typedef struct {
+  const prob_t *p;
+  int b, kh;
+  const int32_t *js;
+  int nj;
+  double *acc; /* [nworkers][2][nj][d] */
+  int nworkers;
+} dkv_ctx;
+
+static void dkv_task(void *vctx, long t, int worker) {
+  dkv_ctx *c = (dkv_ctx *)vctx;
+  const prob_t *p = c->p;
+  const int G = p->H / p->Hk;
+  int gh = (int)(t / p->ql), i = (int)(t % p->ql);
+  int h = c->kh * G + gh;
+  if (g_mutation == MUT_GQA_MODULO) h = c->kh + gh * p->Hk; /* heads with h % Hk == kh */
+  rowbuf rb = rowbuf_new(p);
+  row_backward_prep(p, c->b, h, i, &rb);
+  const float *qi = p->q + q_index(p, c->b, h, i);
+  const float *doi = p->dO + q_index(p, c->b, h, i);
+  double *dk = c->acc + (size_t)worker * 2 * c->nj * p->d;
+  double *dv = dk + (size_t)c->nj * p->d;
+  for (int n = 0; n < c->nj; ++n) {
+    int j = c->js[n];
+    double P = rb.pr[j], ds = rb.ds[j];
+    if (P == 0.0 && ds == 0.0) continue;
+    const float *kj = p->k + kv_index(p, c->b, c->kh, j);
+    const float *src = (g_mutation == MUT_DK_USES_K) ? kj : qi;
+    const double pv = (g_mutation == MUT_DV_USES_DS) ? ds : P;
+    for (int cc = 0; cc < p->d; ++cc) {
+      dk[(size_t)n * p->d + cc] += p->scale * ds * (double)src[cc];
+      dv[(size_t)n * p->d + cc] += pv * (double)doi[cc];
+    }
+  }
+  rowbuf_free(&rb);
+}
+
+/* dK and dV rows js[0..nj) of kv head kh in batch b. Outputs dk[nj*d], dv[nj*d]. */
+int fa_oracle_bwd_kv_rows(const float *q, const float *k, const float *v, const float *mask,
+                          const float *dO, int B, int H, int Hk, int ql, int kl, int d,
+                          double scale, int causal, int b, int kh, const int32_t *js, int nj,
+                          double *dk, double *dv, int nthreads) {
+  if (B <= 0 || H <= 0 || Hk <= 0 || ql <= 0 || kl <= 0 || d <= 0 || H % Hk) return -1;
+  if (b < 0 || b >= B || kh < 0 || kh >= Hk) return -1;
+  for (int n = 0; n < nj; ++n) if (js[n] < 0 || js[n] >= kl) return -1;
+  prob_t p = make_prob(q, k, v, mask, dO, B, H, Hk, ql, kl, d, scale, causal);
+  const int G = H / Hk;
+  long ntasks = (long)G * ql;
+  int nw = nthreads < 1 ? 1 : nthreads;
+  if (nw > ntasks) nw = (int)ntasks;
+  dkv_ctx c;
+  c.p = &p; c.b = b; c.kh = kh; c.js = js; c.nj = nj; c.nworkers = nw;
+  c.acc = (double *)calloc((size_t)nw * 2 * nj * d, sizeof(double));
+  if (!c.acc) return -2;
+  parallel_for(ntasks, nw, dkv_task, &c);
+  for (size_t e = 0; e < (size_t)nj * d; ++e) { dk[e] = 0.0; dv[e] = 0.0; }
+  for (int w = 0; w < nw; ++w) {
+    const double *a = c.acc + (size_t)w * 2 * nj * d;
+    for (size_t e = 0; e < (size_t)nj * d; ++e) {
+      dk[e] += a[e];
+      dv[e] += a[(size_t)nj * d + e];
+    }
+  }
+  free(c.acc);
+  return 0;
+}
+
+/* Full backward: dq [B,H,ql,d], dk and dv [B,Hk,kl,d]. */
+int fa_oracle_bwd(const float *q, const float *k, const float *v, const float *mask,
+                  const float *dO, int B, int H, int Hk, int ql, int kl, int d, double scale,
+                  int causal, double *dq, double *dk, double *dv, int nthreads) {
+  int rc = fa_oracle_bwd_q_rows(q, k, v, mask, dO, B, H, Hk, ql, kl, d, scale, causal, NULL,
+                                (long)B * H * ql, dq, nthreads);
+  if (rc) return rc;
+  int32_t *js = (int32_t *)malloc(sizeof(int32_t) * (size_t)kl);
+  for (int j = 0; j < kl; ++j) js[j] = j;
+  for (int b = 0; b < B && !rc; ++b)
+    for (int kh = 0; kh < Hk && !rc; ++kh) {
+      size_t off = (((size_t)b * Hk + kh) * kl) * (size_t)d;
+      rc = fa_oracle_bwd_kv_rows(q, k, v, mask, dO, B, H, Hk, ql, kl, d, scale, causal, b, kh,
+                                 js, kl, dk + off, dv + off, nthreads);
+    }
+  free(js);
+  return rc;
+}

@@ -1,0 +1,344 @@
+"""Pins of the CPU oracle: checks against things other than the oracle itself.
+
+Each `pin_*` function returns a list of failure strings (empty = pass). They are called by
+`test_oracle_pins.py` one by one, and all together by the planted-mistake test, which shows
+that each mistake planted in the oracle fails at least one of them.
+
+Sources of truth used here (none of them is the oracle's own formula retyped):
+  * torch's CPU library kernels in f64: `_scaled_dot_product_flash_attention_for_cpu`
+    (O and logsumexp) and autograd through `scaled_dot_product_attention` (dQ, dK, dV), with
+    bottom-right causal taken from torch's own `causal_lower_right` bias;
+  * f64 central finite differences (with Richardson extrapolation) of the oracle's forward;
+  * closed forms and invariants of softmax attention (constant V, a single visible key, Q = 0,
+    mask shifts, rows of P summing to one, zero column sums of dK, ...);
+  * structural facts from the mlx-native training tests (page "mlx-native
+    tests/test_flash_attn_train.rs": the causal sentinel-K test of section 6 and the GQA
+    accumulation test of section 16) and the nuvec-core direct formula (page "nuvec-core
+    tests/fast.rs", `attention_fallback_matches_a_direct_formula`: bottom-right causal).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+from torch.nn.attention.bias import causal_lower_right
+
+import oracle
+
+TOL = 1e-10
+
+
+def _rand(rng, shape, lo=None):
+    return rng.standard_normal(shape).astype(np.float32)
+
+
+def _bf16_exact(x):
+    # values with at most 8 significant bits, like the bf16 inputs the oracle always receives
+    from fa_inputs import bf16_bits_to_f32, f32_to_bf16_bits
+
+    return bf16_bits_to_f32(f32_to_bf16_bits(x))
+
+
+def _problem(seed, B, H, Hk, ql, kl, d, mask=False, neg_inf_frac=0.0):
+    rng = np.random.default_rng(seed)
+    q = _bf16_exact(_rand(rng, (B, H, ql, d)))
+    k = _bf16_exact(_rand(rng, (B, Hk, kl, d)))
+    v = _bf16_exact(_rand(rng, (B, Hk, kl, d)))
+    do = _bf16_exact(_rand(rng, (B, H, ql, d)))
+    m = None
+    if mask:
+        m = rng.uniform(-2, 0, size=(B, H, ql, kl)).astype(np.float32)
+        if neg_inf_frac:
+            m[rng.random(m.shape) < neg_inf_frac] = -np.inf
+    return q, k, v, do, m
+
+
+def _torch_bias(ql, kl, causal, mask, H, B):
+    """Additive f64 bias [B,H,ql,kl] from torch's own lower-right causal bias and the mask."""
+    bias = torch.zeros(B, H, ql, kl, dtype=torch.float64)
+    if causal:
+        allowed = causal_lower_right(ql, kl)._materialize(device="cpu")
+        bias = bias.masked_fill(~allowed, float("-inf"))
+    if mask is not None:
+        bias = bias + torch.from_numpy(mask).double()
+    return bias
+
+
+def _torch_fwd(q, k, v, mask, scale, causal):
+    B, H, ql, d = q.shape
+    G = H // k.shape[1]
+    kt = torch.from_numpy(k).double().repeat_interleave(G, dim=1)
+    vt = torch.from_numpy(v).double().repeat_interleave(G, dim=1)
+    qt = torch.from_numpy(q).double()
+    bias = _torch_bias(ql, k.shape[2], causal, mask, H, B)
+    o, lse = torch.ops.aten._scaled_dot_product_flash_attention_for_cpu(
+        qt, kt, vt, 0.0, False, attn_mask=bias, scale=scale)
+    return o.numpy(), lse.numpy()
+
+
+def _torch_grads(q, k, v, mask, do, scale, causal):
+    B, H, ql, d = q.shape
+    qt = torch.from_numpy(q).double().requires_grad_()
+    kt = torch.from_numpy(k).double().requires_grad_()
+    vt = torch.from_numpy(v).double().requires_grad_()
+    if causal and mask is None:
+        bias = causal_lower_right(ql, k.shape[2])
+    else:
+        bias = _torch_bias(ql, k.shape[2], causal, mask, H, B)
+    with torch.nn.attention.sdpa_kernel(torch.nn.attention.SDPBackend.MATH):
+        o = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=bias, scale=scale,
+                                           enable_gqa=True)
+    (o * torch.from_numpy(do).double()).sum().backward()
+    return qt.grad.numpy(), kt.grad.numpy(), vt.grad.numpy()
+
+
+def _cmp(name, got, want, tol=TOL, out=None):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    if got.shape != want.shape:
+        out.append(f"{name}: shape {got.shape} vs {want.shape}")
+        return
+    same_inf = np.isinf(want) & (got == want)
+    with np.errstate(invalid="ignore"):
+        err = np.where(same_inf, 0.0, np.abs(got - want))
+    scale = np.maximum(1.0, np.where(np.isfinite(want), np.abs(want), 1.0))
+    bad = ~(err <= tol * scale)
+    if bad.any():
+        idx = np.unravel_index(np.argmax(np.where(bad, err, -1)), err.shape)
+        out.append(f"{name}: {int(bad.sum())} bad, worst at {idx}: got {got[idx]!r} want {want[idx]!r}")
+
+
+# Shapes for the library pins: (B, H, Hk, ql, kl, d, causal, mask)
+LIB_CASES = [
+    (1, 1, 1, 5, 7, 4, False, False),
+    (2, 4, 2, 6, 6, 8, True, False),
+    (1, 2, 1, 3, 9, 4, True, False),     # bottom-right rectangle, kl > ql
+    (1, 2, 2, 4, 5, 8, False, True),     # additive mask
+    (1, 4, 1, 5, 8, 4, True, True),      # causal + mask + GQA 4:1
+]
+
+
+def pin_fwd_vs_torch_cpu_flash():
+    fails = []
+    for n, (B, H, Hk, ql, kl, d, causal, mask) in enumerate(LIB_CASES):
+        q, k, v, do, m = _problem(100 + n, B, H, Hk, ql, kl, d, mask)
+        scale = 0.37
+        o, lse = oracle.fwd(q, k, v, m, scale=scale, causal=causal)
+        to, tl = _torch_fwd(q, k, v, m, scale, causal)
+        _cmp(f"case{n} O", o, to, out=fails)
+        _cmp(f"case{n} L", lse, tl, out=fails)
+    return fails
+
+
+def pin_bwd_vs_torch_autograd():
+    fails = []
+    for n, (B, H, Hk, ql, kl, d, causal, mask) in enumerate(LIB_CASES):
+        q, k, v, do, m = _problem(200 + n, B, H, Hk, ql, kl, d, mask)
+        scale = 0.41
+        dq, dk, dv = oracle.bwd(q, k, v, m, do, scale=scale, causal=causal)
+        tq, tk, tv = _torch_grads(q, k, v, m, do, scale, causal)
+        _cmp(f"case{n} dQ", dq, tq, out=fails)
+        _cmp(f"case{n} dK", dk, tk, out=fails)
+        _cmp(f"case{n} dV", dv, tv, out=fails)
+    return fails
+
+
+def pin_bwd_vs_finite_differences():
+    """loss = sum(O * dO); Richardson-extrapolated central differences with steps 2^-8, 2^-9,
+    which are exact in f32 for bf16-valued inputs of magnitude < 8."""
+    fails = []
+    B, H, Hk, ql, kl, d = 1, 2, 1, 3, 5, 4
+    q, k, v, do, m = _problem(300, B, H, Hk, ql, kl, d, mask=True, neg_inf_frac=0.15)
+    scale, causal = 0.6, True
+    dq, dk, dv = oracle.bwd(q, k, v, m, do, scale=scale, causal=causal)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.fwd(qq, kk, vv, m, scale=scale, causal=causal, nthreads=1)
+        return float((o * do.astype(np.float64)).sum())
+
+    for name, arr, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros(arr.shape)
+        for idx in np.ndindex(arr.shape):
+            ests = []
+            for h in (2.0 ** -8, 2.0 ** -9):
+                plus, minus = arr.copy(), arr.copy()
+                plus[idx] += np.float32(h)
+                minus[idx] -= np.float32(h)
+                args_p = {"q": (plus, k, v), "k": (q, plus, v), "v": (q, k, plus)}[name]
+                args_m = {"q": (minus, k, v), "k": (q, minus, v), "v": (q, k, minus)}[name]
+                ests.append((loss(*args_p) - loss(*args_m)) / (2 * h))
+            num[idx] = (4 * ests[1] - ests[0]) / 3
+        _cmp(f"FD d{name}", grad, num, tol=2e-7, out=fails)
+    return fails
+
+
+def pin_closed_forms():
+    fails = []
+    rng = np.random.default_rng(7)
+    B, H, Hk, ql, kl, d = 1, 2, 1, 4, 6, 8
+    q, k, v, do, _ = _problem(400, B, H, Hk, ql, kl, d)
+    scale = 0.5
+    # constant V along keys -> O = that constant row (every row has a visible key)
+    vc = np.broadcast_to(v[:, :, :1, :], v.shape).copy()
+    o, _ = oracle.fwd(q, k, vc, None, scale=scale, causal=True)
+    _cmp("constant V", o, np.broadcast_to(vc[:, :1, :1, :].repeat(H, 1), o.shape), out=fails)
+    # Q = 0 -> uniform weights over the visible keys: O = mean of visible V, L = log(#visible)
+    qz = np.zeros_like(q)
+    o, lse = oracle.fwd(qz, k, v, None, scale=scale, causal=True)
+    off = kl - ql
+    for i in range(ql):
+        n_vis = off + i + 1
+        want = v[0, 0, :n_vis, :].astype(np.float64).mean(axis=0)
+        for h in range(H):
+            _cmp(f"Q=0 O row {i}", o[0, h, i], want, out=fails)
+            _cmp(f"Q=0 L row {i}", lse[0, h, i], np.log(n_vis), out=fails)
+    # a single key -> O = V_0 and L = s_00 = scale * <q, k_0>
+    o, lse = oracle.fwd(q, k[:, :, :1], v[:, :, :1], None, scale=scale, causal=False)
+    _cmp("single key O", o, np.broadcast_to(v[:, :, :1], o.shape), out=fails)
+    want_l = scale * np.einsum("bhid,bd->bhi", q.astype(np.float64), k[:, 0, 0].astype(np.float64))
+    _cmp("single key L", lse, want_l, out=fails)
+    # square causal: row 0 sees only key 0
+    o, lse = oracle.fwd(q, k[:, :, :ql], v[:, :, :ql], None, scale=scale, causal=True)
+    _cmp("causal row 0 O", o[:, :, 0], np.broadcast_to(v[:, 0, 0], o[:, :, 0].shape), out=fails)
+    # adding c to a whole mask row shifts L by c and leaves O unchanged
+    m = _bf16_exact(rng.uniform(-1, 0, size=(B, H, ql, kl)).astype(np.float32))  # + 0.75 exact
+    o1, l1 = oracle.fwd(q, k, v, m, scale=scale, causal=False)
+    o2, l2 = oracle.fwd(q, k, v, m + np.float32(0.75), scale=scale, causal=False)
+    _cmp("mask shift O", o2, o1, tol=1e-12, out=fails)
+    _cmp("mask shift L", l2, l1 + 0.75, tol=1e-12, out=fails)
+    # V = identity (d = kl) makes O = P: each row is a distribution, hidden keys get 0
+    kk = k[:, :, :, :]
+    eye = np.broadcast_to(np.eye(kl, dtype=np.float32), (B, Hk, kl, kl)).copy()
+    qq = q[..., :kl] if d >= kl else np.concatenate([q, q], -1)[..., :kl]
+    kk = kk[..., :kl] if d >= kl else np.concatenate([kk, kk], -1)[..., :kl]
+    p, _ = oracle.fwd(np.ascontiguousarray(qq), np.ascontiguousarray(kk), eye, None, scale=scale,
+                      causal=True)
+    _cmp("P rows sum to 1", p.sum(-1), np.ones(p.shape[:-1]), out=fails)
+    for i in range(ql):
+        if (p[..., i, off + i + 1:] != 0).any():
+            fails.append(f"P row {i} puts weight on a hidden key")
+    return fails
+
+
+def pin_causal_structure():
+    fails = []
+    # bottom-right rectangle == last ql rows of the square causal problem over kl queries
+    B, H, Hk, ql, kl, d = 1, 2, 1, 3, 7, 4
+    q, k, v, do, _ = _problem(500, B, H, Hk, ql, kl, d)
+    rng = np.random.default_rng(501)
+    top = _bf16_exact(_rand(rng, (B, H, kl - ql, d)))
+    qs = np.concatenate([top, q], axis=2)
+    dos = np.concatenate([np.zeros_like(top), do], axis=2)
+    scale = 0.45
+    o, lse = oracle.fwd(q, k, v, None, scale=scale, causal=True)
+    os_, ls = oracle.fwd(qs, k, v, None, scale=scale, causal=True)
+    _cmp("rect O = square tail", o, os_[:, :, kl - ql:], tol=1e-13, out=fails)
+    _cmp("rect L = square tail", lse, ls[:, :, kl - ql:], tol=1e-13, out=fails)
+    dq, dk, dv = oracle.bwd(q, k, v, None, do, scale=scale, causal=True)
+    dqs, dks, dvs = oracle.bwd(qs, k, v, None, dos, scale=scale, causal=True)
+    _cmp("rect dQ = square tail", dq, dqs[:, :, kl - ql:], tol=1e-13, out=fails)
+    _cmp("rect dK = square (zero dO on top rows)", dk, dks, tol=1e-13, out=fails)
+    _cmp("rect dV = square (zero dO on top rows)", dv, dvs, tol=1e-13, out=fails)
+    # mlx-native sentinel test: K rows after the target set to 128 leave O[0..=target] unchanged
+    ql = kl = 16
+    target = 7
+    q, k, v, do, _ = _problem(502, 1, 1, 1, ql, kl, 8)
+    kp = k.copy()
+    kp[:, :, target + 1:, :] = 128.0
+    o1, _ = oracle.fwd(q, k, v, None, scale=0.35, causal=True)
+    o2, _ = oracle.fwd(q, kp, v, None, scale=0.35, causal=True)
+    _cmp("sentinel K prefix", o2[:, :, :target + 1], o1[:, :, :target + 1], tol=0, out=fails)
+    if np.allclose(o2[:, :, target + 1:], o1[:, :, target + 1:]):
+        fails.append("sentinel K did not change the rows that may see it")
+    return fails
+
+
+def pin_gqa_equals_repeated_mha():
+    fails = []
+    B, H, Hk, ql, kl, d = 2, 6, 2, 5, 5, 4
+    q, k, v, do, m = _problem(600, B, H, Hk, ql, kl, d, mask=True)
+    G = H // Hk
+    kr, vr = np.repeat(k, G, axis=1), np.repeat(v, G, axis=1)
+    scale = 0.3
+    o, lse = oracle.fwd(q, k, v, m, scale=scale, causal=True)
+    o2, l2 = oracle.fwd(q, kr, vr, m, scale=scale, causal=True)
+    _cmp("GQA O", o, o2, tol=0, out=fails)
+    _cmp("GQA L", lse, l2, tol=0, out=fails)
+    dq, dk, dv = oracle.bwd(q, k, v, m, do, scale=scale, causal=True)
+    dq2, dk2, dv2 = oracle.bwd(q, kr, vr, m, do, scale=scale, causal=True)
+    _cmp("GQA dQ", dq, dq2, tol=1e-13, out=fails)
+    _cmp("GQA dK = sum over repeats", dk, dk2.reshape(B, Hk, G, kl, d).sum(2), tol=1e-13, out=fails)
+    _cmp("GQA dV = sum over repeats", dv, dv2.reshape(B, Hk, G, kl, d).sum(2), tol=1e-13, out=fails)
+    return fails
+
+
+def pin_bwd_invariants():
+    fails = []
+    B, H, Hk, ql, kl, d = 1, 4, 2, 6, 8, 4
+    q, k, v, do, m = _problem(700, B, H, Hk, ql, kl, d, mask=True, neg_inf_frac=0.2)
+    m[0, 1, 2, :] = -np.inf  # one fully masked row
+    scale = 0.5
+    o, lse = oracle.fwd(q, k, v, m, scale=scale, causal=True)
+    dq, dk, dv = oracle.bwd(q, k, v, m, do, scale=scale, causal=True)
+    # sum_j dS_ij = 0  =>  sum_j dK_j = 0 for every kv head
+    _cmp("sum_j dK = 0", dk.sum(axis=2), np.zeros((B, Hk, d)), tol=1e-12, out=fails)
+    # sum_j dV_j = sum of dO over the group's rows that see at least one key
+    G = H // Hk
+    live = np.isfinite(lse)
+    want = (do.astype(np.float64) * live[..., None]).reshape(B, Hk, G, ql, d).sum(axis=(2, 3))
+    _cmp("sum_j dV = sum dO of live rows", dv.sum(axis=2), want, tol=1e-12, out=fails)
+    # the fully masked row: O = 0, L = -inf, dQ = 0 exactly, and nothing is NaN
+    if not (o[0, 1, 2] == 0).all() or lse[0, 1, 2] != -np.inf or not (dq[0, 1, 2] == 0).all():
+        fails.append("fully masked row is not O=0, L=-inf, dQ=0")
+    for name, a in (("O", o), ("dQ", dq), ("dK", dk), ("dV", dv)):
+        if np.isnan(a).any():
+            fails.append(f"NaN in {name}")
+    # all keys equal -> constant scores per row -> dQ = 0
+    ke = np.broadcast_to(k[:, :, :1], k.shape).copy()
+    dq0, _, _ = oracle.bwd(q, ke, v, None, do, scale=scale, causal=False)
+    _cmp("equal keys -> dQ = 0", dq0, np.zeros_like(dq0), tol=1e-12, out=fails)
+    return fails
+
+
+def pin_base2_mode_agrees():
+    fails = []
+    q, k, v, do, m = _problem(800, 2, 4, 2, 9, 13, 16, mask=True, neg_inf_frac=0.1)
+    m[1, 3, 4, :] = -np.inf
+    for causal in (False, True):
+        o1, l1 = oracle.fwd(q, k, v, m, scale=0.25, causal=causal)
+        o2, l2 = oracle.fwd(q, k, v, m, scale=0.25, causal=causal, base2=True)
+        _cmp(f"base2 O causal={causal}", o2, o1, tol=1e-12, out=fails)
+        _cmp(f"base2 L causal={causal}", l2, l1, tol=1e-12, out=fails)
+    return fails
+
+
+def pin_sampled_entry_points_agree():
+    fails = []
+    B, H, Hk, ql, kl, d = 2, 4, 2, 7, 9, 8
+    q, k, v, do, m = _problem(900, B, H, Hk, ql, kl, d, mask=True)
+    scale = 0.3
+    o, lse = oracle.fwd(q, k, v, m, scale=scale, causal=True)
+    dq, dk, dv = oracle.bwd(q, k, v, m, do, scale=scale, causal=True)
+    rows = np.array([0, 5, 13, 40, B * H * ql - 1])
+    o_r, l_r = oracle.fwd_rows(q, k, v, m, scale=scale, causal=True, rows=rows)
+    _cmp("fwd_rows O", o_r, o.reshape(-1, d)[rows], tol=0, out=fails)
+    _cmp("fwd_rows L", l_r, lse.reshape(-1)[rows], tol=0, out=fails)
+    dq_r = oracle.bwd_q_rows(q, k, v, m, do, scale=scale, causal=True, rows=rows)
+    _cmp("bwd_q_rows", dq_r, dq.reshape(-1, d)[rows], tol=0, out=fails)
+    js = [0, 4, 8]
+    dk_r, dv_r = oracle.bwd_kv_rows(q, k, v, m, do, scale=scale, causal=True, b=1, kh=1, js=js)
+    _cmp("bwd_kv_rows dK", dk_r, dk[1, 1, js], tol=1e-14, out=fails)
+    _cmp("bwd_kv_rows dV", dv_r, dv[1, 1, js], tol=1e-14, out=fails)
+    return fails
+
+
+ALL_PINS = [
+    pin_fwd_vs_torch_cpu_flash,
+    pin_bwd_vs_torch_autograd,
+    pin_bwd_vs_finite_differences,
+    pin_closed_forms,
+    pin_causal_structure,
+    pin_gqa_equals_repeated_mha,
+    pin_bwd_invariants,
+    pin_base2_mode_agrees,
+]
