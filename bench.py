@@ -1,0 +1,431 @@
+"""Benchmark: exact training attention, forward + backward, bf16, on GB300.
+
+One step = one pass of the whole path over one batch of synthetic inputs: the forward
+(O, L) and the backward (dQ, dK, dV) through the C ABI on the current stream.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline]
+
+Prints ONE JSON line (rank 0). `value` is whole-job fwd+bwd TFLOP/s with inputs resident in
+HBM (device CUDA events, max over ranks; causal FLOPs counted as half: fwd 4*B*H*ql*kl*d*f,
+bwd 10*B*H*ql*kl*d*f, f = 0.5). `e2e` repeats the measurement through the same C calls with
+the step's inputs copied from pinned host memory and the gradients read back inside the timed
+region. `roofline` is for the kernel with the largest device time, timed live with CUDA events
+on its launch stream by the library's timing facility. `cpu_baseline` times the CPU oracle on a
+bounded sample of the same workload (rank 0, N = 1 only).
+
+--impl reference times the CPU oracle (the only reference implementation this project has) on
+the host cores, on the same workload, metric and unit, each step a bounded sample.
+
+Several GPUs (torchrun, one process per GPU): every rank runs the full workload on its own GPU
+(independent problems, no collective on the data path): "scaling": "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import fa_inputs  # noqa: E402
+
+METRIC = "attention fwd+bwd TFLOP/s (bf16, causal) at 1 GB300; % of dense bf16 tensor peak"
+DEFAULT_WORKLOAD = "gqa_d128_4k"
+KERNEL_SOURCES = {
+    "fwd_kernel": ["flash_attention_gb300/csrc/fa_fwd.cu", "flash_attention_gb300/csrc/fa_common.cuh"],
+    "bwd_main_kernel": ["flash_attention_gb300/csrc/fa_bwd.cu",
+                        "flash_attention_gb300/csrc/fa_common.cuh"],
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(fa_inputs.BY_NAME))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return {"bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
+                "hbm_gbs": float(pk["hbm_gbs"]), "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+            "source": "fallback"}
+
+
+def source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
+    source of that kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    e = rec.get(kernel, {}).get(workload)
+    if not e or e.get("source_hash") != source_hash(KERNEL_SOURCES.get(kernel, [])):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"fa_bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx = max(mx, float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[3:7]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle sample
+def oracle_head_sample(w, inp, heads, nthreads=None):
+    """Full forward + backward of single query heads (with their kv head) by the CPU oracle:
+    each is 1/(B*H) of the workload's units. Returns (flops counted by the rule, seconds)."""
+    import numpy as np
+
+    import oracle
+
+    q, k, v, do = inp.widened()
+    G = w.n_heads // w.n_kv_heads
+    fwd_f, bwd_f = w.flops()
+    per_head = (fwd_f + bwd_f) / (w.batch * w.n_heads)
+    t0 = time.perf_counter()
+    for (b, h) in heads:
+        kh = h // G
+        qs = np.ascontiguousarray(q[b:b + 1, h:h + 1])
+        ks = np.ascontiguousarray(k[b:b + 1, kh:kh + 1])
+        vs = np.ascontiguousarray(v[b:b + 1, kh:kh + 1])
+        dos = np.ascontiguousarray(do[b:b + 1, h:h + 1])
+        ms = None if inp.mask is None else np.ascontiguousarray(inp.mask[b:b + 1, h:h + 1])
+        oracle.fwd(qs, ks, vs, ms, scale=w.scale, causal=w.causal, nthreads=nthreads)
+        oracle.bwd(qs, ks, vs, ms, dos, scale=w.scale, causal=w.causal, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return per_head * len(heads), dt
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    inp = fa_inputs.make_inputs(w)
+    cores = cpu_cores()
+    B, H = w.batch, w.n_heads
+    order = [(b, h) for b in range(B) for h in range(H)]
+    for s in range(args.warmup):
+        oracle_head_sample(w, inp, [order[s % len(order)]], nthreads=cores)
+    times, flops = [], []
+    for s in range(args.steps):
+        f, dt = oracle_head_sample(w, inp, [order[(args.warmup + s) % len(order)]], nthreads=cores)
+        times.append(dt)
+        flops.append(f)
+    tot_t = sum(times)
+    value = sum(flops) / tot_t / 1e12
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, args.gpus),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"per step: full fwd+bwd of one query head (1/{B * H} of the "
+                                   f"workload) on the CPU oracle, heads taken in turn"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def config_of(w, n):
+    return {"workload": w.name, "batch": w.batch, "n_heads": w.n_heads,
+            "n_kv_heads": w.n_kv_heads, "ql": w.ql, "kl": w.kl, "head_dim": w.head_dim,
+            "scale": w.scale, "causal": w.causal, "mask": w.masked,
+            "flop_rule": "fwd 4*B*H*ql*kl*d*f, bwd 10*B*H*ql*kl*d*f, f=0.5 causal",
+            "l2": "inputs larger than L2 (no flush): a step touches "
+                  f"{step_bytes(w) / 1e6:.0f} MB",
+            "parallelism": "replicas" if n == 1 else f"{n} independent replicas"}
+
+
+def step_bytes(w):
+    qb = w.batch * w.n_heads * w.ql * w.head_dim * 2
+    kb = w.batch * w.n_kv_heads * w.kl * w.head_dim * 2
+    # q k v o dO dq dk dv + the f32 dQ accumulator
+    return 5 * qb + 4 * kb + 2 * qb
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, w):
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import flash_attention_gb300 as fa
+
+    fa.build()
+    fa.load_library()
+
+    inp = fa_inputs.make_inputs(w)
+
+    def bf(bits):
+        return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16)
+
+    h_q, h_k, h_v, h_do = (bf(t).pin_memory() for t in (inp.q, inp.k, inp.v, inp.do))
+    q, k, v, do = (t.to(dev) for t in (h_q, h_k, h_v, h_do))
+    mask = None if inp.mask is None else torch.from_numpy(inp.mask).to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.lse_shape(), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    params = fa.FaParams(w.batch, w.n_heads, w.n_kv_heads, w.ql, w.kl, w.head_dim, w.scale,
+                         int(w.causal))
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.fa_train_fwd(q, k, v, mask, o, lse, params, stream)
+        fa.fa_train_bwd(q, k, v, o, lse, do, mask, dq, dk, dv, params, stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if fa.fa_device_status(True) != fa.FA_OK:
+        raise RuntimeError("a kernel gave up a bounded wait during warm-up")
+
+    # ---------------- device-timed steps (inputs resident)
+    clocks = ClockSampler(local)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    fa.fa_profile_read()  # clear
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    fa.fa_profile_enable(True)
+    for s in range(args.steps):
+        ev[s][0].record(stream)
+        fa.fa_train_fwd(q, k, v, mask, o, lse, params, stream)
+        ev[s][1].record(stream)
+        fa.fa_train_bwd(q, k, v, o, lse, do, mask, dq, dk, dv, params, stream)
+        ev[s][2].record(stream)
+    torch.cuda.synchronize()
+    fa.fa_profile_enable(False)
+    clk = clocks.stop()
+    barrier()
+    fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
+    tot_ms = ev[0][0].elapsed_time(ev[-1][2]) / args.steps
+    prof = fa.fa_profile_read()
+    if fa.fa_device_status(True) != fa.FA_OK:
+        raise RuntimeError("a kernel gave up a bounded wait during the timed steps")
+
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([tot_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms = float(t.item())
+
+    fwd_f, bwd_f = w.flops()
+    fwd_ex, bwd_ex = w.flops(exact=True)
+    value = world * (fwd_f + bwd_f) / (tot_ms * 1e-3) / 1e12
+    peaks = load_peaks()
+    peak = peaks["bf16_tflops"]
+
+    # ---------------- roofline of the dominant kernel (live CUDA-event timing)
+    launches_per_step = sum(n for _, n in prof.values()) / args.steps
+    dom = max(prof.items(), key=lambda kv: kv[1][0])
+    dom_name, (dom_ms, dom_n) = dom
+    algo = {"fwd_kernel": fwd_f, "bwd_main_kernel": bwd_f}.get(dom_name, 0.0)
+    dom_avg = dom_ms / max(dom_n, 1)
+    achieved = algo / (dom_avg * 1e-3) / 1e12
+    traffic = recorded_traffic(dom_name, w.name)
+    roofline = {"bound": "tensor", "kernel": dom_name, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"bf16_tflops burst, {peaks['source']}",
+                "per_kernel_ms": {n: (t / max(c, 1)) for n, (t, c) in prof.items()}}
+
+    # ---------------- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        h_dq = torch.empty(dq.shape, dtype=dq.dtype).pin_memory()
+        h_dk = torch.empty(dk.shape, dtype=dk.dtype).pin_memory()
+        h_dv = torch.empty(dv.shape, dtype=dv.dtype).pin_memory()
+
+        def e2e_step():
+            q.copy_(h_q, non_blocking=True)
+            k.copy_(h_k, non_blocking=True)
+            v.copy_(h_v, non_blocking=True)
+            do.copy_(h_do, non_blocking=True)
+            step()
+            h_dq.copy_(dq, non_blocking=True)
+            h_dk.copy_(dk, non_blocking=True)
+            h_dv.copy_(dv, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / args.steps
+        if world > 1:
+            import torch.distributed as dist
+
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_do))
+        d2h = sum(t.numel() * t.element_size() for t in (h_dq, h_dk, h_dv))
+        e2e = {"value": world * (fwd_f + bwd_f) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    # ---------------- CPU oracle baseline (rank 0, N = 1)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cores = cpu_cores()
+        heads, spent, fl = [], 0.0, 0.0
+        order = [(b, h) for b in range(w.batch) for h in range(w.n_heads)]
+        n = 0
+        while spent < 10.0 and n < len(order):
+            f, dt = oracle_head_sample(w, inp, [order[n]], nthreads=cores)
+            heads.append(order[n])
+            spent += dt
+            fl += f
+            n += 1
+        cpu = {"value": fl / spent / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"full fwd+bwd of {len(heads)} query head(s) with their kv head "
+                         f"({len(heads)}/{w.batch * w.n_heads} of the workload), f64, "
+                         f"{spent:.1f} s"}
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": config_of(w, world),
+            "pct_of_peak": 100.0 * value / (world * peak),
+            "fwd_tflops": (fwd_f / (statistics.median(fwd_ms) * 1e-3)) / 1e12,
+            "bwd_tflops": (bwd_f / (statistics.median(bwd_ms) * 1e-3)) / 1e12,
+            "fwd_ms_median": statistics.median(fwd_ms), "bwd_ms_median": statistics.median(bwd_ms),
+            "exact_visible_tflops": world * (fwd_ex + bwd_ex) / (tot_ms * 1e-3) / 1e12,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": int(round(launches_per_step * args.steps)),
+            "clocks": clk,
+        }
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    w = fa_inputs.BY_NAME[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,330 @@
+// fa_api.cu -- the C ABI declared in include/fa_train.h: argument checks, TMA tensor-map
+// encoding, workspace management and kernel dispatch on the caller's stream.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "../../include/fa_train.h"
+#include "fa_launch.h"
+
+namespace {
+
+thread_local char g_last_cuda_error[256] = "";
+
+int cuda_fail(cudaError_t e, const char* where) {
+  snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s (%d)", where,
+           cudaGetErrorString(e), (int)e);
+  return FA_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- driver entry point (TMA)
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+cudaError_t get_encoder() {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess) {
+      g_encode_err = e;
+    } else if (q != cudaDriverEntryPointSuccess || fn == nullptr) {
+      g_encode_err = cudaErrorSymbolNotFound;
+    } else {
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  });
+  return g_encode_err;
+}
+
+// 3-D bf16 tensor map over a contiguous [bh, rows, d] tensor, box (64, box_rows, 1), 128-byte
+// swizzle; reads outside [0, rows) fill with zeros.
+bool encode_bf16_3d(CUtensorMap* m, const void* base, int bh, int rows, int d, int box_rows) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)bh};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * (cuuint64_t)d * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- per-device status word
+constexpr int kMaxDevices = 64;
+int* g_status[kMaxDevices] = {nullptr};
+std::mutex g_status_mu;
+
+cudaError_t device_status_word(int dev, int** out) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_status_mu);
+  if (!g_status[dev]) {
+    int* p = nullptr;
+    cudaError_t e = cudaMalloc(&p, sizeof(int));
+    if (e != cudaSuccess) return e;
+    e = cudaMemset(p, 0, sizeof(int));
+    if (e != cudaSuccess) return e;
+    g_status[dev] = p;
+  }
+  *out = g_status[dev];
+  return cudaSuccess;
+}
+
+// ---------------------------------------------------------------- argument checks
+constexpr int kMaxLen = 1 << 22;  // keeps every grid dimension within its limit
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_params(const fa_params* p) {
+  if (!p) return FA_ERR_INVALID;
+  if (p->batch <= 0 || p->n_heads <= 0 || p->n_kv_heads <= 0 || p->ql <= 0 || p->kl <= 0)
+    return FA_ERR_INVALID;
+  if (p->n_heads % p->n_kv_heads != 0) return FA_ERR_INVALID;
+  if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256) return FA_ERR_INVALID;
+  if (!(isfinite(p->scale) && p->scale > 0.0f)) return FA_ERR_INVALID;
+  if (p->causal != 0 && p->causal != 1) return FA_ERR_INVALID;
+  if (p->ql > kMaxLen || p->kl > kMaxLen) return FA_ERR_INVALID;
+  if ((int64_t)p->batch * p->n_heads > INT32_MAX / 2) return FA_ERR_INVALID;
+  return FA_OK;
+}
+
+int check_bf16(const void* ptr) { return (ptr && aligned(ptr, 16)) ? FA_OK : FA_ERR_INVALID; }
+int check_f32(const void* ptr) { return (ptr && aligned(ptr, 16)) ? FA_OK : FA_ERR_INVALID; }
+
+int check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int major = 0;
+  e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  if (major != 10) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+// ---------------------------------------------------------------- kernel timing
+struct ProfRec {
+  int kernel;
+  cudaEvent_t start, stop;
+};
+std::atomic<int> g_prof_on{0};
+std::mutex g_prof_mu;
+std::vector<ProfRec> g_prof_recs;
+std::vector<cudaEvent_t> g_prof_pool;
+ProfRec g_prof_open[fa::kNumKernels];
+bool g_prof_is_open[fa::kNumKernels] = {false, false, false, false};
+
+cudaEvent_t prof_event() {
+  if (!g_prof_pool.empty()) {
+    cudaEvent_t e = g_prof_pool.back();
+    g_prof_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+}  // namespace
+
+namespace fa {
+void profile_mark(int kernel, int end, cudaStream_t s) {
+  if (!g_prof_on.load(std::memory_order_relaxed)) return;
+  if (kernel < 0 || kernel >= kNumKernels) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!end) {
+    ProfRec r;
+    r.kernel = kernel;
+    r.start = prof_event();
+    r.stop = prof_event();
+    cudaEventRecord(r.start, s);
+    g_prof_open[kernel] = r;
+    g_prof_is_open[kernel] = true;
+  } else if (g_prof_is_open[kernel]) {
+    ProfRec r = g_prof_open[kernel];
+    cudaEventRecord(r.stop, s);
+    g_prof_recs.push_back(r);
+    g_prof_is_open[kernel] = false;
+  }
+}
+}  // namespace fa
+
+extern "C" {
+
+int fa_profile_enable(int on) {
+  g_prof_on.store(on ? 1 : 0);
+  return FA_OK;
+}
+
+int fa_profile_read(double* total_ms, int64_t* launches) {
+  if (!total_ms || !launches) return FA_ERR_INVALID;
+  for (int k = 0; k < fa::kNumKernels; ++k) {
+    total_ms[k] = 0.0;
+    launches[k] = 0;
+  }
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  int rc = FA_OK;
+  for (const ProfRec& r : g_prof_recs) {
+    float ms = 0.0f;
+    cudaError_t e = cudaEventSynchronize(r.stop);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.start, r.stop);
+    if (e != cudaSuccess) {
+      rc = cuda_fail(e, "fa_profile_read");
+    } else {
+      total_ms[r.kernel] += ms;
+      launches[r.kernel] += 1;
+    }
+    g_prof_pool.push_back(r.start);
+    g_prof_pool.push_back(r.stop);
+  }
+  g_prof_recs.clear();
+  return rc;
+}
+
+const char* fa_kernel_name(int id) {
+  switch (id) {
+    case FA_KERNEL_FWD: return "fwd_kernel";
+    case FA_KERNEL_BWD_PREP: return "bwd_prep_kernel";
+    case FA_KERNEL_BWD_MAIN: return "bwd_main_kernel";
+    case FA_KERNEL_BWD_DQ: return "bwd_dq_kernel";
+    default: return "unknown";
+  }
+}
+
+int fa_train_fwd(const void* q, const void* k, const void* v, const float* mask, void* o,
+                 float* lse, const fa_params* p, void* stream) {
+  int rc = check_params(p);
+  if (rc) return rc;
+  if ((rc = check_bf16(q)) || (rc = check_bf16(k)) || (rc = check_bf16(v)) ||
+      (rc = check_bf16(o)) || (rc = check_f32(lse)))
+    return rc;
+  if (mask && !aligned(mask, 16)) return FA_ERR_INVALID;
+  if ((rc = check_device())) return rc;
+  cudaError_t e = get_encoder();
+  if (e != cudaSuccess) return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
+  int dev = 0;
+  cudaGetDevice(&dev);
+  fa::FwdArgs a;
+  a.mask = mask;
+  a.o = o;
+  a.lse = lse;
+  if ((e = device_status_word(dev, &a.status)) != cudaSuccess) return cuda_fail(e, "status word");
+  a.B = p->batch;
+  a.H = p->n_heads;
+  a.Hk = p->n_kv_heads;
+  a.ql = p->ql;
+  a.kl = p->kl;
+  a.d = p->head_dim;
+  a.scale = p->scale;
+  a.causal = p->causal;
+  fa::FwdMaps m;
+  const int qrows = fa::fwd_q_box_rows(a.d), kvrows = fa::fwd_kv_box_rows(a.d);
+  if (!encode_bf16_3d(&m.q, q, a.B * a.H, a.ql, a.d, qrows) ||
+      !encode_bf16_3d(&m.k, k, a.B * a.Hk, a.kl, a.d, kvrows) ||
+      !encode_bf16_3d(&m.v, v, a.B * a.Hk, a.kl, a.d, kvrows))
+    return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+  e = fa::launch_fwd(a, m, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  return FA_OK;
+}
+
+int fa_train_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dO, const float* mask, void* dq, void* dk, void* dv,
+                 const fa_params* p, void* stream) {
+  int rc = check_params(p);
+  if (rc) return rc;
+  if ((rc = check_bf16(q)) || (rc = check_bf16(k)) || (rc = check_bf16(v)) ||
+      (rc = check_bf16(o)) || (rc = check_f32(lse)) || (rc = check_bf16(dO)) ||
+      (rc = check_bf16(dq)) || (rc = check_bf16(dk)) || (rc = check_bf16(dv)))
+    return rc;
+  if (mask && !aligned(mask, 16)) return FA_ERR_INVALID;
+  if ((rc = check_device())) return rc;
+  cudaError_t e = get_encoder();
+  if (e != cudaSuccess) return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  fa::BwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.dO = dO;
+  a.mask = mask;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.B = p->batch;
+  a.H = p->n_heads;
+  a.Hk = p->n_kv_heads;
+  a.ql = p->ql;
+  a.kl = p->kl;
+  a.d = p->head_dim;
+  a.ql_pad = fa::bwd_ql_pad(a.ql);
+  a.scale = p->scale;
+  a.causal = p->causal;
+  if ((e = device_status_word(dev, &a.status)) != cudaSuccess) return cuda_fail(e, "status word");
+
+  fa::BwdMaps m;
+  const int qrows = fa::bwd_q_box_rows(a.d), kvrows = fa::bwd_kv_box_rows(a.d);
+  if (!encode_bf16_3d(&m.q, q, a.B * a.H, a.ql, a.d, qrows) ||
+      !encode_bf16_3d(&m.dO, dO, a.B * a.H, a.ql, a.d, qrows) ||
+      !encode_bf16_3d(&m.k, k, a.B * a.Hk, a.kl, a.d, kvrows) ||
+      !encode_bf16_3d(&m.v, v, a.B * a.Hk, a.kl, a.d, kvrows))
+    return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+
+  const size_t ws_bytes = fa::bwd_workspace_bytes(a.B, a.H, a.ql, a.d);
+  void* ws = nullptr;
+  e = cudaMallocAsync(&ws, ws_bytes, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync (backward workspace)");
+  fa::bwd_carve_workspace(ws, a.B, a.H, a.ql, a.d, &a.lse2, &a.dvec, &a.dqacc);
+  e = fa::launch_bwd(a, m, s);
+  cudaError_t e2 = cudaFreeAsync(ws, s);
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync (backward workspace)");
+  return FA_OK;
+}
+
+int fa_device_status(int clear) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int* w = nullptr;
+  if ((e = device_status_word(dev, &w)) != cudaSuccess) return cuda_fail(e, "status word");
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  int v = 0;
+  if ((e = cudaMemcpy(&v, w, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "cudaMemcpy (status)");
+  if (clear && v) {
+    if ((e = cudaMemset(w, 0, sizeof(int))) != cudaSuccess) return cuda_fail(e, "cudaMemset");
+  }
+  return v ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
+}
+
+const char* fa_error_string(int code) {
+  switch (code) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID: return "invalid argument (parameter, null or misaligned pointer)";
+    case FA_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case FA_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait on the device";
+    case FA_ERR_UNSUPPORTED: return "device is not an sm_100-family GPU (needs sm_103a)";
+    default: return "unknown error code";
+  }
+}
+
+const char* fa_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* fa_version(void) { return "fa_gb300 0.1 (sm_103a, tcgen05)"; }
+
+}  // extern "C"

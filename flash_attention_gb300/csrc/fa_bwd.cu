@@ -1,0 +1,646 @@
+// fa_bwd.cu -- backward of exact attention: dQ, dK, dV from Q, K, V, O, L and dO (sm_103a).
+//
+// Method: the FlashAttention-2 backward equations of page "mlx-native
+// tests/test_flash_attn_train.rs" (`sdpa_backward_reference_f32`):
+//   P = exp(S - L),  dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),  dQ = scale dS K,
+//   dK = scale dS^T Q,
+// with D_i = rowsum(dO_i o O_i) taken from the stored forward output, and the split into
+// kernels of the flash backward on page "tang src/compute/cuda.rs" (`causal_attention_backward`):
+// a D pre-pass, a kv-tile-major main pass in which each CTA owns one kv tile and walks every
+// query head that shares its kv head (so dK and dV are reduced in the CTA, without atomics),
+// and dQ accumulated in f32 across CTAs. P is recomputed from L with base-2 exponentials:
+// P = exp2(S * scale * log2(e) + mask * log2(e) - L * log2(e)); a row with L = -inf (no
+// visible key) gets +inf in place of L * log2(e), which makes its P exactly 0.
+//
+// Kernels:
+//   bwd_prep_kernel  D_i, L_i * log2(e), and zeroes the dQ accumulator (bandwidth bound)
+//   bwd_main_kernel  per kv tile of 128 rows (and, for head_dim 256, per half of the head
+//                    dimension): S^T = K Q^T and dP^T = V dO^T into TMEM; P^T and dS^T
+//                    computed by one warpgroup (thread = kv row = TMEM lane) and written back
+//                    to TMEM as bf16; dV += P^T dO and dK += dS^T Q with the A operand read
+//                    from TMEM; dQ^T = K^T dS^T (head_dim >= 128) or dQ = dS K (head_dim 64)
+//                    with dS^T staged in swizzled shared memory; a second warpgroup drains dQ
+//                    from TMEM into the f32 accumulator with global reductions, and writes
+//                    dK, dV at the end
+//   bwd_dq_kernel    dQ = bf16(scale * accumulator)
+#include <float.h>
+#include "fa_common.cuh"
+#include "fa_launch.h"
+
+namespace fa {
+
+namespace {
+constexpr float kLog2eB = 1.4426950408889634f;
+}
+
+// ------------------------------------------------------------------------ traits / layout
+template <int HD>
+struct BwdTraits;
+template <>
+struct BwdTraits<64> {
+  static constexpr int BM = 128, DSPLIT = 1, STAGES = 2;
+  static constexpr bool DQT = false;  // dQ = dS K (M = BM)
+};
+template <>
+struct BwdTraits<128> {
+  static constexpr int BM = 64, DSPLIT = 1, STAGES = 2;
+  static constexpr bool DQT = true;  // dQ^T = K^T dS^T (M = head-dim slice)
+};
+template <>
+struct BwdTraits<256> {
+  static constexpr int BM = 64, DSPLIT = 2, STAGES = 1;
+  static constexpr bool DQT = true;
+};
+
+constexpr int kBN = 128;  // kv rows per CTA (the M of the kv-major MMAs)
+
+template <int HD>
+struct BwdLayout {
+  using T = BwdTraits<HD>;
+  static constexpr int BM = T::BM;
+  static constexpr int DH = HD / T::DSPLIT;  // head-dim slice this CTA produces
+  static constexpr int KCH = HD / 64;
+  static constexpr int KV_BYTES = kBN * HD * 2;
+  static constexpr int QT_BYTES = BM * HD * 2;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + KV_BYTES;
+  static constexpr int OFF_Q = OFF_V + KV_BYTES;                    // STAGES x Q tile
+  static constexpr int OFF_DO = OFF_Q + T::STAGES * QT_BYTES;       // STAGES x dO tile
+  static constexpr int OFF_DS = OFF_DO + T::STAGES * QT_BYTES;      // dS^T [kv][q] swizzled
+  static constexpr int DS_BYTES = kBN * BM * 2;
+  static constexpr int OFF_L = OFF_DS + DS_BYTES;                   // STAGES x BM f32
+  static constexpr int OFF_D = OFF_L + T::STAGES * BM * 4;          // STAGES x BM f32
+  static constexpr int OFF_END = OFF_D + T::STAGES * BM * 4;
+  static constexpr int SMEM_BYTES = OFF_END + 1024;
+  // TMEM columns
+  static constexpr int COL_S = 0;
+  static constexpr int COL_DP = BM;
+  static constexpr int COL_DV = 2 * BM;
+  static constexpr int COL_DK = 2 * BM + DH;
+  static constexpr int COL_DQ = 2 * BM + 2 * DH;
+  static constexpr int DQ_COLS = T::DQT ? BM : HD;
+  static constexpr int TMEM_USED = COL_DQ + DQ_COLS;
+  static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
+  static constexpr int THREADS = 320;  // WG0 dS, WG1 dQ drain + epilogue, TMA warp, MMA warp
+  static constexpr int TMA_WARP = 8, MMA_WARP = 9;
+  static_assert(TMEM_USED <= 512, "TMEM budget");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static_assert(T::DQT ? DH == 128 : BM == 128, "every MMA has M = 128");
+};
+
+struct BwdKParams {
+  const float* mask;
+  const float* lse2;
+  const float* dvec;
+  float* dqacc;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int* status;
+  int H, Hk, ql, kl, ql_pad;
+  float scale, scale_log2;
+};
+
+// ------------------------------------------------------------------------ prep kernel
+// One warp per (bh, row < ql_pad).
+template <int HD>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
+                                                       const __nv_bfloat16* __restrict__ dO,
+                                                       const float* __restrict__ lse,
+                                                       float* __restrict__ lse2,
+                                                       float* __restrict__ dvec,
+                                                       float* __restrict__ dqacc, int BH, int ql,
+                                                       int ql_pad) {
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= (long long)BH * ql_pad) return;
+  const int bh = (int)(row / ql_pad), i = (int)(row % ql_pad);
+  constexpr int PER = HD / 32;  // elements per lane
+  float acc = 0.0f;
+  if (i < ql) {
+    const size_t base = ((size_t)bh * ql + i) * HD + lane * PER;
+    if constexpr (PER == 2) {
+      __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + base);
+      __nv_bfloat162 g = *reinterpret_cast<const __nv_bfloat162*>(dO + base);
+      acc = __low2float(a) * __low2float(g) + __high2float(a) * __high2float(g);
+    } else {
+      constexpr int NV = PER / 4;  // uint2 (4 bf16) chunks
+#pragma unroll
+      for (int u = 0; u < NV; ++u) {
+        uint2 a = *reinterpret_cast<const uint2*>(o + base + 4 * u);
+        uint2 g = *reinterpret_cast<const uint2*>(dO + base + 4 * u);
+        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+        const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          acc += __low2float(a2[e]) * __low2float(g2[e]) + __high2float(a2[e]) * __high2float(g2[e]);
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) {
+    float l2 = INFINITY;  // padding rows and fully masked rows: P = exp2(s - inf) = 0
+    if (i < ql) {
+      const float L = lse[(size_t)bh * ql + i];
+      if (L != -INFINITY) l2 = L * kLog2eB;
+    }
+    lse2[(size_t)bh * ql_pad + i] = l2;
+    dvec[(size_t)bh * ql_pad + i] = acc;
+  }
+  float4* z = reinterpret_cast<float4*>(dqacc + ((size_t)bh * ql_pad + i) * HD);
+#pragma unroll
+  for (int c = lane; c < HD / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// ------------------------------------------------------------------------ dQ convert
+template <int HD>
+__global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ dqacc,
+                                                     __nv_bfloat16* __restrict__ dq, int BH,
+                                                     int ql, int ql_pad, float scale) {
+  const long long n4 = (long long)BH * ql * HD / 4;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n4;
+       e += (long long)gridDim.x * blockDim.x) {
+    const long long flat = e * 4;
+    const long long row = flat / HD;
+    const int c = (int)(flat % HD);
+    const int bh = (int)(row / ql), i = (int)(row % ql);
+    const float4 v =
+        *reinterpret_cast<const float4*>(dqacc + ((size_t)bh * ql_pad + i) * HD + c);
+    uint2 out;
+    out.x = pack_bf16(v.x * scale, v.y * scale);
+    out.y = pack_bf16(v.z * scale, v.w * scale);
+    *reinterpret_cast<uint2*>(dq + flat) = out;
+  }
+}
+
+// ------------------------------------------------------------------------ main kernel
+template <int HD, bool CAUSAL>
+__device__ __forceinline__ int bwd_first_mtile(int n0, int ql, int kl) {
+  if (!CAUSAL) return 0;
+  constexpr int BM = BwdTraits<HD>::BM;
+  const int first_row = n0 - (kl - ql);  // key n0 is visible to rows >= first_row
+  return first_row <= 0 ? 0 : first_row / BM;
+}
+
+// Writes 8 bf16 (one 16-byte granule g of row j) into a 128-byte-swizzled tile chunk.
+__device__ __forceinline__ void st_swizzled(uint8_t* chunk, int j, int g, uint4 val) {
+  *reinterpret_cast<uint4*>(chunk + j * 128 + ((g ^ (j & 7)) << 4)) = val;
+}
+
+template <int HD, bool CAUSAL, bool HAS_MASK>
+__global__ void __launch_bounds__(320, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                    const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mDO,
+                    const BwdKParams p) {
+  using T = BwdTraits<HD>;
+  using LY = BwdLayout<HD>;
+  constexpr int BM = T::BM, DH = LY::DH, KCH = LY::KCH, ST = T::STAGES;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  __shared__ uint64_t kv_full, qdo_full[ST], qdo_empty[ST];
+  __shared__ uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free, acc_full, mma_drain;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_flag;
+
+  const int warp = warp_id(), lane = lane_id();
+  const int dh = (int)blockIdx.x % T::DSPLIT;
+  const int bkh = (int)blockIdx.x / T::DSPLIT;  // b * Hk + kh
+  const int b = bkh / p.Hk, kh = bkh % p.Hk;
+  const int G = p.H / p.Hk;
+  const int n0 = (int)blockIdx.y * kBN;
+  const int n_mt = (p.ql + BM - 1) / BM;
+  const int m_first = min(bwd_first_mtile<HD, CAUSAL>(n0, p.ql, p.kl), n_mt);
+  const int nm = n_mt - m_first;      // query tiles per head
+  const int n_iter = G * nm;          // (head, query tile) pairs this CTA visits
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&kv_full, 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&qdo_full[s], 1);
+      mbar_init(&qdo_empty[s], 1);
+    }
+    mbar_init(&s_full, 1);
+    mbar_init(&dp_full, 1);
+    mbar_init(&p_ready, 128);
+    mbar_init(&ds_ready, 128);
+    mbar_init(&dq_full, 1);
+    mbar_init(&dq_free, 128);
+    mbar_init(&acc_full, 1);
+    mbar_init(&mma_drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == LY::MMA_WARP) {
+    tmem_alloc(&tmem_base_s, LY::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base_s;
+
+  if (warp == LY::TMA_WARP) {
+    // ------------------------------------------------------------------ TMA producer
+    if (elect_one()) {
+      tma_prefetch_desc(&mQ);
+      tma_prefetch_desc(&mK);
+      tma_prefetch_desc(&mV);
+      tma_prefetch_desc(&mDO);
+      int last_use[ST];
+      for (int s = 0; s < ST; ++s) last_use[s] = -1;
+      mbar_arrive_expect_tx(&kv_full, 2 * LY::KV_BYTES);
+      for (int c = 0; c < KCH; ++c) {
+        tma_load_3d(smem + LY::OFF_K + c * kBN * 128, &mK, &kv_full, c * 64, n0, bkh);
+        tma_load_3d(smem + LY::OFF_V + c * kBN * 128, &mV, &kv_full, c * 64, n0, bkh);
+      }
+      for (int it = 0; it < n_iter; ++it) {
+        const int st = it % ST;
+        const uint32_t use = it / ST;
+        if (it >= ST && !mbar_wait(&qdo_empty[st], (use - 1) & 1, &abort_flag)) break;
+        const int h = kh * G + it / nm;
+        const int q0 = (m_first + it % nm) * BM;
+        const int bh = b * p.H + h;
+        mbar_arrive_expect_tx(&qdo_full[st], 2 * LY::QT_BYTES + 2 * BM * 4);
+        for (int c = 0; c < KCH; ++c) {
+          tma_load_3d(smem + LY::OFF_Q + st * LY::QT_BYTES + c * BM * 128, &mQ, &qdo_full[st],
+                      c * 64, q0, bh);
+          tma_load_3d(smem + LY::OFF_DO + st * LY::QT_BYTES + c * BM * 128, &mDO,
+                      &qdo_full[st], c * 64, q0, bh);
+        }
+        bulk_load(smem + LY::OFF_L + st * BM * 4, p.lse2 + (size_t)bh * p.ql_pad + q0, BM * 4,
+                  &qdo_full[st]);
+        bulk_load(smem + LY::OFF_D + st * BM * 4, p.dvec + (size_t)bh * p.ql_pad + q0, BM * 4,
+                  &qdo_full[st]);
+        last_use[st] = it;
+      }
+      mbar_wait_drain(&kv_full, 0);
+      for (int s = 0; s < ST; ++s)
+        if (last_use[s] >= 0) mbar_wait_drain(&qdo_full[s], (last_use[s] / ST) & 1);
+    }
+  } else if (warp == LY::MMA_WARP) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      const uint32_t sK = smem_u32(smem + LY::OFF_K), sV = smem_u32(smem + LY::OFF_V);
+      const uint32_t sDS = smem_u32(smem + LY::OFF_DS);
+      const uint32_t id_s = idesc_bf16(128, BM, 0, 0);      // S^T, dP^T: [kv x q]
+      const uint32_t id_acc = idesc_bf16(128, DH, 0, 1);    // dV, dK: A tmem, B MN-major
+      const uint32_t id_dq = T::DQT ? idesc_bf16(DH, BM, 1, 1) : idesc_bf16(BM, HD, 1, 1);
+      const uint32_t tS = tbase + LY::COL_S, tDP = tbase + LY::COL_DP;
+      const uint32_t tDV = tbase + LY::COL_DV, tDK = tbase + LY::COL_DK;
+      const uint32_t tDQ = tbase + LY::COL_DQ;
+      bool ok = mbar_wait(&kv_full, 0, &abort_flag);
+
+      auto issue_s_dp = [&](int it) {
+        const int st = it % ST;
+        ok = ok && mbar_wait(&qdo_full[st], (it / ST) & 1, &abort_flag);
+        if (!ok) return;
+        tc_fence_after();
+        const uint32_t sQ = smem_u32(smem + LY::OFF_Q + st * LY::QT_BYTES);
+        const uint32_t sDO = smem_u32(smem + LY::OFF_DO + st * LY::QT_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks) {
+          const uint32_t ko = (ks / 4) * (kBN * 128) + (ks % 4) * 32;
+          const uint32_t qo = (ks / 4) * (BM * 128) + (ks % 4) * 32;
+          mma_ss(tS, smem_desc(sK + ko, 16, 1024), smem_desc(sQ + qo, 16, 1024), id_s,
+                 ks > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full);
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks) {
+          const uint32_t ko = (ks / 4) * (kBN * 128) + (ks % 4) * 32;
+          const uint32_t qo = (ks / 4) * (BM * 128) + (ks % 4) * 32;
+          mma_ss(tDP, smem_desc(sV + ko, 16, 1024), smem_desc(sDO + qo, 16, 1024), id_s,
+                 ks > 0 ? 1u : 0u);
+        }
+        mma_commit(&dp_full);
+      };
+
+      if (n_iter > 0) issue_s_dp(0);
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const int st = it % ST;
+        const uint32_t sQ = smem_u32(smem + LY::OFF_Q + st * LY::QT_BYTES);
+        const uint32_t sDO = smem_u32(smem + LY::OFF_DO + st * LY::QT_BYTES);
+        // head-dim slice of Q / dO used as the B operand (MN-major, N = DH)
+        const uint32_t slice = (dh * DH / 64) * (BM * 128);
+        // dV += P^T dO
+        ok = mbar_wait(&p_ready, it & 1, &abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < BM / 16; ++ks)
+          mma_ts(tDV, tS + ks * 8, smem_desc(sDO + slice + ks * 2048, BM * 128, 1024), id_acc,
+                 (it > 0 || ks > 0) ? 1u : 0u);
+        // dK += dS^T Q
+        ok = mbar_wait(&ds_ready, it & 1, &abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < BM / 16; ++ks)
+          mma_ts(tDK, tDP + ks * 8, smem_desc(sQ + slice + ks * 2048, BM * 128, 1024), id_acc,
+                 (it > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(&qdo_empty[st]);
+        // next scores while this tile's dQ is formed
+        if (it + 1 < n_iter) issue_s_dp(it + 1);
+        if (!ok) break;
+        // dQ for this tile
+        if (it > 0) {
+          ok = mbar_wait(&dq_free, (it - 1) & 1, &abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        if constexpr (T::DQT) {
+          // dQ^T[d, q] = sum_kv K[kv, d] dS^T[kv, q]: A = K slice (MN-major), B = dS^T
+          const uint32_t kslice = (dh * DH / 64) * (kBN * 128);
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks)
+            mma_ss(tDQ, smem_desc(sK + kslice + ks * 2048, kBN * 128, 1024),
+                   smem_desc(sDS + ks * 2048, kBN * 128, 1024), id_dq, ks > 0 ? 1u : 0u);
+        } else {
+          // dQ[q, d] = sum_kv dS^T[kv, q] K[kv, d]: A = dS^T (MN-major), B = K (MN-major)
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks)
+            mma_ss(tDQ, smem_desc(sDS + ks * 2048, kBN * 128, 1024),
+                   smem_desc(sK + ks * 2048, kBN * 128, 1024), id_dq, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(&dq_full);
+      }
+      mma_commit(&acc_full);
+      mma_commit(&mma_drain);
+      mbar_wait_drain(&mma_drain, 0);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------------ WG0: P^T and dS^T
+    const int j = warp * 32 + lane;  // kv row within the tile == TMEM lane
+    const int kv = n0 + j;
+    const bool kv_live = kv < p.kl;
+    const uint32_t lane_base = tbase + ((uint32_t)(warp * 32) << 16);
+    const float c2 = p.scale_log2;
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int st = it % ST;
+      const int h = kh * G + it / nm;
+      const int q0 = (m_first + it % nm) * BM;
+      const int bh = b * p.H + h;
+      const float* sL = reinterpret_cast<const float*>(smem + LY::OFF_L + st * BM * 4);
+      const float* sD = reinterpret_cast<const float*>(smem + LY::OFF_D + st * BM * 4);
+      // query q (column) sees this key iff q0 + q >= kv - (kl - ql)
+      const int qmin = kv - (p.kl - p.ql) - q0;  // columns < qmin are hidden (causal)
+      const bool edge = CAUSAL && (n0 + kBN - 1 - (p.kl - p.ql) > q0);
+      const float* mcol = nullptr;
+      if (HAS_MASK && kv_live) mcol = p.mask + ((size_t)bh * p.ql + q0) * (size_t)p.kl + kv;
+
+      ok = mbar_wait(&s_full, it & 1, &abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      float pv[BM];
+#pragma unroll
+      for (int c32 = 0; c32 < BM / 32; ++c32) {
+        uint32_t r[32];
+        tmem_ld32(lane_base + LY::COL_S + c32 * 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int q = c32 * 32 + e;
+          float x = __uint_as_float(r[e]);
+          float mterm = 0.0f;
+          if (HAS_MASK) mterm = (mcol != nullptr && q0 + q < p.ql) ? mcol[(size_t)q * p.kl] : 0.0f;
+          float s2 = fmaf(x, c2, fmaf(mterm, kLog2eB, -sL[q]));
+          float pr = ex2(s2);
+          if (!kv_live || (edge && q < qmin)) pr = 0.0f;
+          pv[q] = pr;
+        }
+      }
+      // P^T as bf16 into the S columns (A operand of dV += P^T dO)
+#pragma unroll
+      for (int c32 = 0; c32 < BM / 32; ++c32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(pv[c32 * 32 + 2 * e], pv[c32 * 32 + 2 * e + 1]);
+        tmem_st16(lane_base + LY::COL_S + c32 * 16, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&p_ready);
+
+      ok = mbar_wait(&dp_full, it & 1, &abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      // the previous tile's dQ MMA must be done reading the shared dS^T buffer
+      if (it > 0) {
+        ok = mbar_wait(&dq_full, (it - 1) & 1, &abort_flag);
+        if (!ok) break;
+      }
+#pragma unroll
+      for (int c32 = 0; c32 < BM / 32; ++c32) {
+        uint32_t r[32];
+        tmem_ld32(lane_base + LY::COL_DP + c32 * 32, r);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int q = c32 * 32 + 2 * e;
+          const float d0 = pv[q] * (__uint_as_float(r[2 * e]) - sD[q]);
+          const float d1 = pv[q + 1] * (__uint_as_float(r[2 * e + 1]) - sD[q + 1]);
+          pk[e] = pack_bf16(d0, d1);
+        }
+        tmem_st16(lane_base + LY::COL_DP + c32 * 16, pk);
+        // dS^T row j, columns c32*32 .. +31: 4 granules of the 64-column chunk c32/2
+        uint8_t* chunk = smem + LY::OFF_DS + (c32 / 2) * (kBN * 128);
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+          st_swizzled(chunk, j, (c32 % 2) * 4 + g,
+                      make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]));
+      }
+      fence_proxy_async();  // generic-proxy writes of dS^T -> visible to the tensor core
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&ds_ready);
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------------ WG1: dQ drain
+    const int wl = warp - 4;
+    const uint32_t lane_base = tbase + ((uint32_t)(wl * 32) << 16);
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int h = kh * G + it / nm;
+      const int q0 = (m_first + it % nm) * BM;
+      const int bh = b * p.H + h;
+      ok = mbar_wait(&dq_full, it & 1, &abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      if constexpr (T::DQT) {
+        // lane = head-dim index within the slice, column = query row
+        const int dc = dh * DH + wl * 32 + lane;
+        float* dst = p.dqacc + ((size_t)bh * p.ql_pad + q0) * HD + dc;
+#pragma unroll
+        for (int c32 = 0; c32 < BM / 32; ++c32) {
+          uint32_t r[32];
+          tmem_ld32(lane_base + LY::COL_DQ + c32 * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) atomicAdd(dst + (size_t)(c32 * 32 + e) * HD, __uint_as_float(r[e]));
+        }
+      } else {
+        // lane = query row, column = head-dim index
+        const int q = wl * 32 + lane;
+        float4* dst = reinterpret_cast<float4*>(p.dqacc + ((size_t)bh * p.ql_pad + q0 + q) * HD);
+#pragma unroll
+        for (int c32 = 0; c32 < HD / 32; ++c32) {
+          uint32_t r[32];
+          tmem_ld32(lane_base + LY::COL_DQ + c32 * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            atomicAdd(dst + c32 * 8 + e,
+                      make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
+                                  __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3])));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&dq_free);
+    }
+    // ---------------------------------------------------------------- dK, dV epilogue
+    const int j = wl * 32 + lane;
+    const int kv = n0 + j;
+    bool have = false;
+    if (ok) {
+      ok = mbar_wait(&acc_full, 0, &abort_flag);
+      tc_fence_after();
+      have = ok && n_iter > 0;
+    }
+    const size_t rowoff = ((size_t)bkh * p.kl + (kv < p.kl ? kv : 0)) * HD + dh * DH;
+#pragma unroll 1
+    for (int which = 0; which < 2; ++which) {
+      const uint32_t col = which == 0 ? LY::COL_DV : LY::COL_DK;
+      const float mul = which == 0 ? 1.0f : p.scale;
+      __nv_bfloat16* out = (which == 0 ? p.dv : p.dk) + rowoff;
+#pragma unroll 1
+      for (int c = 0; c < DH; c += 32) {
+        uint32_t r[32];
+        if (have) {
+          tmem_ld32(lane_base + col + c, r);
+          tmem_wait_ld();
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = have ? pack_bf16(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul)
+                       : 0u;
+        if (kv < p.kl) {
+          uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == LY::MMA_WARP) tmem_dealloc(tbase, LY::TMEM_COLS);
+  if (threadIdx.x == 0) report_abort(&abort_flag, p.status);
+}
+
+// ------------------------------------------------------------------------ host side
+int bwd_q_box_rows(int d) {
+  return d == 64 ? BwdTraits<64>::BM : d == 128 ? BwdTraits<128>::BM : BwdTraits<256>::BM;
+}
+int bwd_kv_box_rows(int) { return kBN; }
+int bwd_ql_pad(int ql) { return (ql + 127) / 128 * 128; }
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t bwd_workspace_bytes(int B, int H, int ql, int d) {
+  const size_t rows = (size_t)B * H * bwd_ql_pad(ql);
+  return align256(rows * 4) * 2 + align256(rows * d * 4);
+}
+
+void bwd_carve_workspace(void* base, int B, int H, int ql, int d, float** lse2, float** dvec,
+                         float** dqacc) {
+  const size_t rows = (size_t)B * H * bwd_ql_pad(ql);
+  uint8_t* p = static_cast<uint8_t*>(base);
+  *lse2 = reinterpret_cast<float*>(p);
+  *dvec = reinterpret_cast<float*>(p + align256(rows * 4));
+  *dqacc = reinterpret_cast<float*>(p + 2 * align256(rows * 4));
+  (void)d;
+}
+
+template <int HD, bool CAUSAL, bool HAS_MASK>
+static cudaError_t launch_main_t(const BwdArgs& a, const BwdMaps& m, cudaStream_t s) {
+  using LY = BwdLayout<HD>;
+  auto kern = bwd_main_kernel<HD, CAUSAL, HAS_MASK>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  BwdKParams kp;
+  kp.mask = a.mask;
+  kp.lse2 = a.lse2;
+  kp.dvec = a.dvec;
+  kp.dqacc = a.dqacc;
+  kp.dk = reinterpret_cast<__nv_bfloat16*>(a.dk);
+  kp.dv = reinterpret_cast<__nv_bfloat16*>(a.dv);
+  kp.status = a.status;
+  kp.H = a.H;
+  kp.Hk = a.Hk;
+  kp.ql = a.ql;
+  kp.kl = a.kl;
+  kp.ql_pad = a.ql_pad;
+  kp.scale = a.scale;
+  kp.scale_log2 = a.scale * kLog2eB;
+  dim3 grid(a.B * a.Hk * BwdTraits<HD>::DSPLIT, (a.kl + kBN - 1) / kBN);
+  profile_mark(kKernBwdMain, 0, s);
+  kern<<<grid, LY::THREADS, LY::SMEM_BYTES, s>>>(m.q, m.k, m.v, m.dO, kp);
+  cudaError_t e = cudaGetLastError();
+  profile_mark(kKernBwdMain, 1, s);
+  return e;
+}
+
+template <int HD>
+static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t s) {
+  const int BH = a.B * a.H;
+  {
+    const long long rows = (long long)BH * a.ql_pad;
+    profile_mark(kKernBwdPrep, 0, s);
+    bwd_prep_kernel<HD><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
+        reinterpret_cast<const __nv_bfloat16*>(a.o), reinterpret_cast<const __nv_bfloat16*>(a.dO),
+        a.lse, a.lse2, a.dvec, a.dqacc, BH, a.ql, a.ql_pad);
+    cudaError_t e = cudaGetLastError();
+    profile_mark(kKernBwdPrep, 1, s);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e;
+  if (a.causal) {
+    e = a.mask ? launch_main_t<HD, true, true>(a, m, s) : launch_main_t<HD, true, false>(a, m, s);
+  } else {
+    e = a.mask ? launch_main_t<HD, false, true>(a, m, s) : launch_main_t<HD, false, false>(a, m, s);
+  }
+  if (e != cudaSuccess) return e;
+  {
+    const long long n4 = (long long)BH * a.ql * HD / 4;
+    long long blocks = (n4 + 255) / 256;
+    if (blocks > 152 * 32) blocks = 152 * 32;
+    profile_mark(kKernBwdDq, 0, s);
+    bwd_dq_kernel<HD><<<(unsigned)blocks, 256, 0, s>>>(
+        a.dqacc, reinterpret_cast<__nv_bfloat16*>(a.dq), BH, a.ql, a.ql_pad, a.scale);
+    profile_mark(kKernBwdDq, 1, s);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(const BwdArgs& a, const BwdMaps& m, cudaStream_t stream) {
+  switch (a.d) {
+    case 64: return launch_bwd_d<64>(a, m, stream);
+    case 128: return launch_bwd_d<128>(a, m, stream);
+    case 256: return launch_bwd_d<256>(a, m, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fa

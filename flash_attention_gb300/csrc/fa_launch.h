@@ -1,0 +1,78 @@
+// fa_launch.h -- internal interface between the C-ABI layer (fa_api.cu) and the kernel
+// translation units. Host-side only; not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa {
+
+// Kernel ids of the timing facility (same values as FA_KERNEL_* in the public header).
+enum KernelId { kKernFwd = 0, kKernBwdPrep = 1, kKernBwdMain = 2, kKernBwdDq = 3, kNumKernels = 4 };
+
+// Records a timing event before (end = 0) or after (end = 1) a launch on `s` when timing is
+// enabled; does nothing otherwise. Defined in fa_api.cu.
+void profile_mark(int kernel, int end, cudaStream_t s);
+
+// Everything a forward launch needs besides the tensor maps.
+struct FwdArgs {
+  const float* mask;  // [B, H, ql, kl] or nullptr
+  void* o;            // bf16 [B, H, ql, d]
+  float* lse;         // [B, H, ql]
+  int* status;        // device status word (nullable)
+  int B, H, Hk, ql, kl, d;
+  float scale;
+  int causal;
+};
+
+// Tensor maps of a forward launch (3-D, innermost first: d, rows, batch*heads; 128-byte
+// swizzle; box of 64 columns).
+struct FwdMaps {
+  CUtensorMap q, k, v;
+};
+
+// Rows per query tile and keys per kv tile the forward kernel of head_dim d uses (the tensor
+// map boxes must match).
+int fwd_q_box_rows(int d);
+int fwd_kv_box_rows(int d);
+
+cudaError_t launch_fwd(const FwdArgs& a, const FwdMaps& m, cudaStream_t stream);
+
+// Backward.
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const float* lse;
+  const void* dO;
+  const float* mask;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* lse2;   // workspace [B*H, ql_pad]: L * log2(e), +inf for fully masked rows
+  float* dvec;   // workspace [B*H, ql_pad]: D = rowsum(dO * O)
+  float* dqacc;  // workspace [B*H, ql_pad, d] f32 dQ accumulator
+  int* status;
+  int B, H, Hk, ql, kl, d, ql_pad;
+  float scale;
+  int causal;
+};
+
+struct BwdMaps {
+  CUtensorMap q, k, v, dO;
+};
+
+int bwd_q_box_rows(int d);
+int bwd_kv_box_rows(int d);
+int bwd_ql_pad(int ql);
+
+// Workspace bytes of a backward call (lse2 + dvec + dqacc, each 256-byte aligned).
+size_t bwd_workspace_bytes(int B, int H, int ql, int d);
+void bwd_carve_workspace(void* base, int B, int H, int ql, int d, float** lse2, float** dvec,
+                         float** dqacc);
+
+cudaError_t launch_bwd(const BwdArgs& a, const BwdMaps& m, cudaStream_t stream);
+
+}  // namespace fa

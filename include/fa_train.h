@@ -1,0 +1,137 @@
+/*
+ * fa_train.h -- C ABI of libfa_gb300: exact scaled-dot-product attention for training on one
+ * NVIDIA GB300 (sm_103a), forward and backward.
+ *
+ * The operation (page "mlx-native tests/test_flash_attn_train.rs", functions
+ * `sdpa_reference_with_logsumexp` and `sdpa_backward_reference_f32`; causal alignment as in the
+ * nuvec-core direct formula, page "nuvec-core tests/fast.rs",
+ * `attention_fallback_matches_a_direct_formula`):
+ *
+ *   for batch b, query head h, query row i, kv head kh = h / (n_heads / n_kv_heads):
+ *     visible(i, j) = !causal || j <= kl - ql + i          (bottom-right alignment, signed)
+ *     s_ij = scale * <q_i, k_j> + mask[b,h,i,j]             (-inf where not visible)
+ *     L_i  = log sum_j exp(s_ij)                            (natural log; -inf if no key)
+ *     O_i  = sum_j exp(s_ij - L_i) v_j                      (0 if L_i = -inf)
+ *
+ *   backward, with dO the gradient of O and P_ij = exp(s_ij - L_i), D_i = <dO_i, O_i>:
+ *     dS_ij = P_ij (<dO_i, v_j> - D_i)
+ *     dQ_i  = scale * sum_j dS_ij k_j
+ *     dK_j  = scale * sum_{h sharing kh} sum_i dS_ij q_i
+ *     dV_j  =         sum_{h sharing kh} sum_i P_ij dO_i
+ *
+ * Internally the scores are taken to base 2: the f32 dot product is multiplied by
+ * scale*log2(e), the mask by log2(e), the running row maximum starts at -FLT_MAX/2, and
+ * L = max_2 * ln(2) + ln(sum) -- the conventions of the same mlx-native page.
+ *
+ * Layouts: every tensor is contiguous, row-major, on the current CUDA device.
+ *   q, o, dO, dq          [batch, n_heads,    ql, head_dim]  bf16 (raw 16-bit patterns)
+ *   k, v, dk, dv          [batch, n_kv_heads, kl, head_dim]  bf16
+ *   lse                   [batch, n_heads,    ql]            f32, natural-log logsumexp L
+ *   mask (optional)       [batch, n_heads,    ql, kl]        f32, natural-log additive; an
+ *                                                            entry of -inf hides that key
+ *
+ * Ownership: the caller owns every buffer. Outputs are overwritten completely, never
+ * accumulated into. The backward needs f32 scratch (a per-row D and a dQ accumulator); the
+ * library takes it with cudaMallocAsync on `stream` and frees it with cudaFreeAsync on the same
+ * stream inside the call.
+ *
+ * Streams: `stream` is a cudaStream_t (NULL = the legacy default stream). Calls are
+ * asynchronous: they return after the kernels are enqueued. Inputs must not be modified, and
+ * outputs not read, until the stream reaches that point.
+ *
+ * Errors: a synchronous return code. Arguments are checked before anything is enqueued, so an
+ * FA_ERR_INVALID call has no effect. FA_ERR_CUDA means a CUDA call or launch failed (the text
+ * of the last such error is kept per thread, see fa_last_cuda_error). Kernel-side pipeline
+ * stalls are bounded: a kernel that waited more than 2 s on one of its own barriers gives up,
+ * returns, and leaves FA_ERR_DEVICE_TIMEOUT for fa_device_status to report.
+ */
+#ifndef FA_TRAIN_H_
+#define FA_TRAIN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Problem description. Mirrors the parameter block of the mlx-native dispatch functions
+ * (`FlashAttnTrainParams` in the same test page, section "Run the training-forward kernel"). */
+typedef struct fa_params {
+  int32_t batch;      /* >= 1 */
+  int32_t n_heads;    /* query heads, >= 1, a multiple of n_kv_heads */
+  int32_t n_kv_heads; /* key/value heads, >= 1 */
+  int32_t ql;         /* query length, >= 1 */
+  int32_t kl;         /* key length, >= 1 */
+  int32_t head_dim;   /* 64, 128 or 256 */
+  float scale;        /* finite and > 0; a plain multiplier (not assumed to be 1/sqrt(d)) */
+  int32_t causal;     /* 0 or 1: bottom-right causal mask (q_abs = kl - ql + i) */
+} fa_params;
+
+/* Return codes. */
+#define FA_OK 0
+#define FA_ERR_INVALID 1        /* bad parameter, null or misaligned pointer */
+#define FA_ERR_CUDA 2           /* a CUDA runtime/driver call or a launch failed */
+#define FA_ERR_DEVICE_TIMEOUT 3 /* a kernel gave up a bounded wait (see fa_device_status) */
+#define FA_ERR_UNSUPPORTED 4    /* the device is not sm_103 or sm_100 family */
+
+/* Forward: O and L. Page "mlx-native tests/test_flash_attn_train.rs", sections 2-8 (forward
+ * parity), function `sdpa_reference_with_logsumexp`.
+ *   q, k, v : inputs (bf16, device, 16-byte aligned)
+ *   mask    : NULL, or the f32 additive mask (device, 16-byte aligned)
+ *   o       : output, bf16 [batch, n_heads, ql, head_dim]
+ *   lse     : output, f32  [batch, n_heads, ql]
+ *   p       : problem description (host pointer, read during the call only)
+ *   stream  : cudaStream_t
+ * A fully masked row gives O = 0 and L = -inf. */
+int fa_train_fwd(const void* q, const void* k, const void* v, const float* mask, void* o,
+                 float* lse, const fa_params* p, void* stream);
+
+/* Backward: dQ, dK, dV from the forward's O and L. Same page, sections 10-16 (backward parity),
+ * function `sdpa_backward_reference_f32`; the kernel decomposition (a D_i = rowsum(dO * O)
+ * pass, a kv-tile-major pass for dK/dV over the query heads that share a kv head, f32 dQ
+ * accumulation) follows the flash backward of page "tang src/compute/cuda.rs",
+ * `causal_attention_backward`.
+ *   q, k, v, o, dO : inputs, bf16 (o is this library's forward output for q, k, v, mask)
+ *   lse            : input, f32, the forward's L
+ *   mask           : NULL, or the same mask as in the forward
+ *   dq, dk, dv     : outputs, bf16, shapes of q, k, v
+ * Rows with L = -inf (fully masked) contribute nothing and get dQ = 0. */
+int fa_train_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dO, const float* mask, void* dq, void* dk, void* dv,
+                 const fa_params* p, void* stream);
+
+/* Kernel timing (a tracing aid). While enabled, each kernel launch of this library is
+ * bracketed by two CUDA events recorded on the launch's own stream; fa_profile_read waits for
+ * them, adds up the device time per kernel and clears the record. Kernel ids: */
+#define FA_KERNEL_FWD 0      /* forward (O, L) */
+#define FA_KERNEL_BWD_PREP 1 /* backward pre-pass: D = rowsum(dO * O), scratch zeroing */
+#define FA_KERNEL_BWD_MAIN 2 /* backward main pass: dK, dV, dQ accumulation */
+#define FA_KERNEL_BWD_DQ 3   /* backward dQ conversion to bf16 */
+#define FA_NUM_KERNELS 4
+
+/* Turns timing on (1) or off (0). Returns FA_OK. */
+int fa_profile_enable(int on);
+/* Fills total_ms[FA_NUM_KERNELS] and launches[FA_NUM_KERNELS] (host arrays) with the device
+ * time and number of launches recorded since the last read, then clears the record. */
+int fa_profile_read(double* total_ms, int64_t* launches);
+/* Name of a kernel id (static storage). */
+const char* fa_kernel_name(int id);
+
+/* Synchronises the current device, then returns FA_OK, or FA_ERR_DEVICE_TIMEOUT if any kernel
+ * of this library on it gave up a bounded wait since the last call with clear != 0. */
+int fa_device_status(int clear);
+
+/* Human-readable text of a return code (static storage). */
+const char* fa_error_string(int code);
+
+/* Text of the last CUDA error seen by this thread in a call that returned FA_ERR_CUDA. */
+const char* fa_last_cuda_error(void);
+
+/* Library version string (static storage). */
+const char* fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_TRAIN_H_ */

@@ -1,0 +1,113 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol include/fa_train.h declares,
+and rejects bad arguments with FA_ERR_INVALID before it touches the device or any pointer."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import flash_attention_gb300 as fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa_train.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa.build()
+    return fa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("fa_train_fwd", "fa_train_bwd", "fa_error_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/fa_train.h but not exported"
+
+
+def test_error_strings(lib):
+    for code in range(5):
+        assert fa.fa_error_string(code)
+    assert "unknown" in fa.fa_error_string(99)
+    assert "sm_103a" in fa.fa_version()
+
+
+def test_params_struct_layout():
+    assert ctypes.sizeof(fa.FaParams) == 32
+    assert fa.FaParams.scale.offset == 24 and fa.FaParams.causal.offset == 28
+
+
+GOOD = dict(batch=1, n_heads=4, n_kv_heads=2, ql=128, kl=128, head_dim=128, scale=0.125, causal=1)
+FAKE = 0x100000  # a 16-byte aligned address that is never dereferenced: checks come first
+
+
+def _fwd(lib, params, q=FAKE, k=FAKE, v=FAKE, mask=None, o=FAKE, lse=FAKE):
+    p = fa.FaParams(**params)
+    return lib.fa_train_fwd(q, k, v, mask, o, lse, ctypes.byref(p), None)
+
+
+def _bwd(lib, params, ptrs=None, mask=None):
+    p = fa.FaParams(**params)
+    a = [FAKE] * 9 if ptrs is None else ptrs
+    q, k, v, o, lse, dO, dq, dk, dv = a
+    return lib.fa_train_bwd(q, k, v, o, lse, dO, mask, dq, dk, dv, ctypes.byref(p), None)
+
+
+BAD_PARAMS = [
+    ("batch", 0), ("n_heads", 0), ("n_kv_heads", 0), ("ql", 0), ("kl", -3), ("head_dim", 96),
+    ("head_dim", 32), ("n_heads", 3), ("scale", 0.0), ("scale", -1.0), ("scale", float("inf")),
+    ("scale", float("nan")), ("causal", 2), ("ql", (1 << 22) + 1), ("kl", 1 << 23),
+]
+
+
+@pytest.mark.parametrize("field,value", BAD_PARAMS)
+def test_bad_params_rejected(lib, field, value):
+    bad = dict(GOOD, **{field: value})
+    assert _fwd(lib, bad) == fa.FA_ERR_INVALID
+    assert _bwd(lib, bad) == fa.FA_ERR_INVALID
+
+
+def test_null_params_rejected(lib):
+    assert lib.fa_train_fwd(FAKE, FAKE, FAKE, None, FAKE, FAKE, None, None) == fa.FA_ERR_INVALID
+
+
+@pytest.mark.parametrize("slot", range(5))
+def test_null_or_misaligned_pointer_rejected_fwd(lib, slot):
+    for bad in (None, FAKE + 2, FAKE + 8):
+        ptrs = [FAKE] * 5
+        ptrs[slot] = bad
+        q, k, v, o, lse = ptrs
+        assert _fwd(lib, GOOD, q, k, v, None, o, lse) == fa.FA_ERR_INVALID
+
+
+@pytest.mark.parametrize("slot", range(9))
+def test_null_or_misaligned_pointer_rejected_bwd(lib, slot):
+    for bad in (None, FAKE + 2):
+        ptrs = [FAKE] * 9
+        ptrs[slot] = bad
+        assert _bwd(lib, GOOD, ptrs) == fa.FA_ERR_INVALID
+
+
+def test_misaligned_mask_rejected(lib):
+    assert _fwd(lib, GOOD, mask=FAKE + 4) == fa.FA_ERR_INVALID
+    assert _bwd(lib, GOOD, mask=FAKE + 4) == fa.FA_ERR_INVALID
+
+
+def test_valid_call_without_gpu_fails_cleanly(lib):
+    """With no usable device the call reports a CUDA or device error; it never crashes."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc = _fwd(lib, GOOD)
+    assert rc in (fa.FA_ERR_CUDA, fa.FA_ERR_UNSUPPORTED)
