@@ -65,6 +65,25 @@ def dist_env():
     return rank, world, local
 
 
+def shard_inputs(w, rank):
+    """Inputs of this rank's shard: every rank draws its own batches (seed offset by rank),
+    so N ranks process N independent copies of the workload's shape (weak scaling)."""
+    base = fa_inputs.SEED_BASE + 1_000_003 * rank
+    return fa_inputs.make_inputs(w, seed_base=base)
+
+
+def reduce_max(x, world, device=None):
+    """Max of a float over ranks (identity for one rank). Timing only: no data-path traffic."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -255,7 +274,7 @@ def run_ours(args, w):
     fa.build()
     fa.load_library()
 
-    inp = fa_inputs.make_inputs(w)
+    inp = shard_inputs(w, rank)
 
     def bf(bits):
         return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16)
@@ -313,12 +332,7 @@ def run_ours(args, w):
     if fa.fa_device_status(True) != fa.FA_OK:
         raise RuntimeError("a kernel gave up a bounded wait during the timed steps")
 
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([tot_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms = float(t.item())
+    tot_ms = reduce_max(tot_ms, world, dev)
 
     fwd_f, bwd_f = w.flops()
     fwd_ex, bwd_ex = w.flops(exact=True)
@@ -366,13 +380,7 @@ def run_ours(args, w):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / args.steps
-        if world > 1:
-            import torch.distributed as dist
-
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = reduce_max(e0.elapsed_time(e1) / args.steps, world, dev)
         h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_do))
         d2h = sum(t.numel() * t.element_size() for t in (h_dq, h_dk, h_dv))
         e2e = {"value": world * (fwd_f + bwd_f) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",

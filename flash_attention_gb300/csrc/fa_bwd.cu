@@ -391,7 +391,10 @@ __global__ void __launch_bounds__(320, 1)
       const float* mcol = nullptr;
       if (HAS_MASK && kv_live) mcol = p.mask + ((size_t)bh * p.ql + q0) * (size_t)p.kl + kv;
 
-      ok = mbar_wait(&s_full, it & 1, &abort_flag);
+      // the stage's L and D rows came with the Q/dO copies; observe that barrier here too
+      // (its next phase needs this tile's dK MMA, so it cannot have moved on)
+      ok = __all_sync(0xffffffffu, mbar_wait(&qdo_full[st], (it / ST) & 1, &abort_flag));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full, it & 1, &abort_flag));
       if (!ok) break;
       tc_fence_after();
       float pv[BM];
@@ -424,12 +427,12 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       mbar_arrive(&p_ready);
 
-      ok = mbar_wait(&dp_full, it & 1, &abort_flag);
+      ok = __all_sync(0xffffffffu, mbar_wait(&dp_full, it & 1, &abort_flag));
       if (!ok) break;
       tc_fence_after();
       // the previous tile's dQ MMA must be done reading the shared dS^T buffer
       if (it > 0) {
-        ok = mbar_wait(&dq_full, (it - 1) & 1, &abort_flag);
+        ok = __all_sync(0xffffffffu, mbar_wait(&dq_full, (it - 1) & 1, &abort_flag));
         if (!ok) break;
       }
 #pragma unroll
@@ -467,7 +470,7 @@ __global__ void __launch_bounds__(320, 1)
       const int h = kh * G + it / nm;
       const int q0 = (m_first + it % nm) * BM;
       const int bh = b * p.H + h;
-      ok = mbar_wait(&dq_full, it & 1, &abort_flag);
+      ok = __all_sync(0xffffffffu, mbar_wait(&dq_full, it & 1, &abort_flag));
       if (!ok) break;
       tc_fence_after();
       if constexpr (T::DQT) {
@@ -506,7 +509,7 @@ __global__ void __launch_bounds__(320, 1)
     const int kv = n0 + j;
     bool have = false;
     if (ok) {
-      ok = mbar_wait(&acc_full, 0, &abort_flag);
+      ok = __all_sync(0xffffffffu, mbar_wait(&acc_full, 0, &abort_flag));
       tc_fence_after();
       have = ok && n_iter > 0;
     }

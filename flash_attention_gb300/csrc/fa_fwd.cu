@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
                                              ~uintptr_t(1023));
   __shared__ uint64_t q_full;
   __shared__ uint64_t k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
-  __shared__ uint64_t s_full[NQ][NS], p_full[NQ][NS], o_done[NQ];
+  __shared__ uint64_t s_full[NQ][NS], p_full[NQ][NS], o_done[NQ], o_final[NQ];
   __shared__ uint64_t mma_drain;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
         mbar_init(&p_full[t][s], 128);
       }
       mbar_init(&o_done[t], 1);
+      mbar_init(&o_final[t], 1);
     }
     mbar_init(&mma_drain, 1);
     fence_barrier_init();
@@ -255,6 +256,7 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
             mma_ts(o_tmem, p_tmem + ks * 8, bd, idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
           }
           mma_commit(&o_done[t]);
+          if (j == nt[t] - 1) mma_commit(&o_final[t]);  // every PV of tile t issued
           if (t == NQ - 1) mma_commit(&v_empty[st]);
           if (j + NS < nt[t]) issue_s(t, j + NS);
         }
@@ -284,7 +286,7 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
 
     for (int j = 0; j < ntt; ++j) {
       const int sb = j % NS;
-      ok = mbar_wait(&s_full[t][sb], (j / NS) & 1, &abort_flag);
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t][sb], (j / NS) & 1, &abort_flag));
       if (!ok) break;
       tc_fence_after();
       const uint32_t s_addr = lane_base + o_col + HD + sb * BN;
@@ -325,7 +327,7 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
           // O holds PV of tiles < j: wait for the last of them, then scale the row in place.
           // (S of tile j was committed after PV of tile j-NS, so at most NS-1 <= 1 phase of
           // o_done is outstanding here and the parity wait is exact.)
-          ok = mbar_wait(&o_done[t], (j - 1) & 1, &abort_flag);
+          ok = __all_sync(0xffffffffu, mbar_wait(&o_done[t], (j - 1) & 1, &abort_flag));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
@@ -371,12 +373,11 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
     }
 
     // ---------------------------------------------------------------- epilogue
-    // The commit of S for the last tile came after PV of tile ntt-1-NS, so o_done has
-    // completed at least ntt-NS phases; wait the remaining ones in order (a parity wait must
-    // never run two phases ahead of the barrier).
+    // o_final completes once, after the last PV of this tile (a single-phase barrier: o_done
+    // may be anywhere between NS phases behind and done here, which a parity wait cannot
+    // tell apart).
     if (ok && ntt > 0) {
-      for (int k = max(0, ntt - NS); k < ntt && ok; ++k)
-        ok = mbar_wait(&o_done[t], k & 1, &abort_flag);
+      ok = __all_sync(0xffffffffu, mbar_wait(&o_final[t], 0, &abort_flag));
       tc_fence_after();
     }
     const bool live = ok && ntt > 0 && l > 0.0f;
