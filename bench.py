@@ -49,12 +49,15 @@ KERNEL_SOURCES = {
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(fa_inputs.BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ncu", action="store_true",
+                    help="profiling mode: run exactly warmup + steps fwd+bwd steps, no timing, "
+                         "no e2e, no CPU baseline, no JSON line (for ncu captures)")
     return ap.parse_args()
 
 
@@ -134,7 +137,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -167,7 +170,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": "warm-up and timed steps, 20 ms sampling"}
 
 
 # ------------------------------------------------------------------ CPU oracle sample
@@ -299,21 +302,31 @@ def run_ours(args, w):
 
             dist.barrier()
 
+    if args.ncu:
+        for _ in range(args.warmup + args.steps):
+            step()
+        torch.cuda.synchronize()
+        rc = fa.fa_device_status(True)
+        print(f"ncu mode: {args.warmup + args.steps} steps of {w.name}, status {rc}", flush=True)
+        if rc != fa.FA_OK:
+            raise RuntimeError("a kernel gave up a bounded wait")
+        return
+
+    clocks = ClockSampler(local)
+    clocks.start()
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
     if fa.fa_device_status(True) != fa.FA_OK:
+        clocks.stop()
         raise RuntimeError("a kernel gave up a bounded wait during warm-up")
 
     # ---------------- device-timed steps (inputs resident)
-    clocks = ClockSampler(local)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     fa.fa_profile_read()  # clear
     barrier()
     torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
     fa.fa_profile_enable(True)
     for s in range(args.steps):
         ev[s][0].record(stream)

@@ -34,22 +34,28 @@ constexpr float kLog2eB = 1.4426950408889634f;
 }
 
 // ------------------------------------------------------------------------ traits / layout
+// BM query rows per tile; DSPLIT: slices of the head dimension (one CTA per slice);
+// ST: depth of the Q/dO ring; NSB: score buffers (S^T) in TMEM; DQT: dQ formed transposed.
+// Two dP^T buffers are always used; the dQ tile of iteration `it` is written into the dP^T
+// buffer of `it` once dK has consumed the dS^T stored there. LOOKAHEAD: issue the next tile's
+// dP^T before this tile's dK (needs ST >= 2), so the dS warpgroup is fed while the tensor core
+// forms dV, dK and dQ.
 template <int HD>
 struct BwdTraits;
 template <>
 struct BwdTraits<64> {
-  static constexpr int BM = 128, DSPLIT = 1, STAGES = 2;
-  static constexpr bool DQT = false;  // dQ = dS K (M = BM)
+  static constexpr int BM = 128, DSPLIT = 1, ST = 3, NSB = 1;
+  static constexpr bool DQT = false, LOOKAHEAD = true;  // dQ = dS K (M = BM)
 };
 template <>
 struct BwdTraits<128> {
-  static constexpr int BM = 64, DSPLIT = 1, STAGES = 2;
-  static constexpr bool DQT = true;  // dQ^T = K^T dS^T (M = head-dim slice)
+  static constexpr int BM = 64, DSPLIT = 1, ST = 3, NSB = 2;
+  static constexpr bool DQT = true, LOOKAHEAD = true;  // dQ^T = K^T dS^T (M = head-dim slice)
 };
 template <>
 struct BwdTraits<256> {
-  static constexpr int BM = 64, DSPLIT = 2, STAGES = 1;
-  static constexpr bool DQT = true;
+  static constexpr int BM = 64, DSPLIT = 2, ST = 1, NSB = 2;
+  static constexpr bool DQT = true, LOOKAHEAD = false;
 };
 
 constexpr int kBN = 128;  // kv rows per CTA (the M of the kv-major MMAs)
@@ -62,30 +68,31 @@ struct BwdLayout {
   static constexpr int KCH = HD / 64;
   static constexpr int KV_BYTES = kBN * HD * 2;
   static constexpr int QT_BYTES = BM * HD * 2;
+  static constexpr int DS_BYTES = kBN * BM * 2;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_BYTES;
-  static constexpr int OFF_Q = OFF_V + KV_BYTES;                    // STAGES x Q tile
-  static constexpr int OFF_DO = OFF_Q + T::STAGES * QT_BYTES;       // STAGES x dO tile
-  static constexpr int OFF_DS = OFF_DO + T::STAGES * QT_BYTES;      // dS^T [kv][q] swizzled
-  static constexpr int DS_BYTES = kBN * BM * 2;
-  static constexpr int OFF_L = OFF_DS + DS_BYTES;                   // STAGES x BM f32
-  static constexpr int OFF_D = OFF_L + T::STAGES * BM * 4;          // STAGES x BM f32
-  static constexpr int OFF_END = OFF_D + T::STAGES * BM * 4;
+  static constexpr int OFF_Q = OFF_V + KV_BYTES;                // ST x Q tile
+  static constexpr int OFF_DO = OFF_Q + T::ST * QT_BYTES;       // ST x dO tile
+  static constexpr int OFF_DS = OFF_DO + T::ST * QT_BYTES;      // 2 x dS^T [kv][q] swizzled
+  static constexpr int OFF_L = OFF_DS + 2 * DS_BYTES;           // ST x BM f32
+  static constexpr int OFF_D = OFF_L + T::ST * BM * 4;          // ST x BM f32
+  static constexpr int OFF_END = OFF_D + T::ST * BM * 4;
   static constexpr int SMEM_BYTES = OFF_END + 1024;
-  // TMEM columns
-  static constexpr int COL_S = 0;
-  static constexpr int COL_DP = BM;
-  static constexpr int COL_DV = 2 * BM;
-  static constexpr int COL_DK = 2 * BM + DH;
-  static constexpr int COL_DQ = 2 * BM + 2 * DH;
-  static constexpr int DQ_COLS = T::DQT ? BM : HD;
-  static constexpr int TMEM_USED = COL_DQ + DQ_COLS;
+  // TMEM columns: S^T buffers, dP^T buffers (also holding dQ), dV, dK
+  static constexpr int COL_S0 = 0;
+  static constexpr int COL_DP0 = T::NSB * BM;
+  static constexpr int COL_DV = (T::NSB + 2) * BM;
+  static constexpr int COL_DK = COL_DV + DH;
+  static constexpr int TMEM_USED = COL_DK + DH;
   static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
+  static constexpr int DQ_COLS = T::DQT ? BM : HD;
   static constexpr int THREADS = 320;  // WG0 dS, WG1 dQ drain + epilogue, TMA warp, MMA warp
   static constexpr int TMA_WARP = 8, MMA_WARP = 9;
   static_assert(TMEM_USED <= 512, "TMEM budget");
+  static_assert(DQ_COLS <= BM, "dQ tile must fit in a dP^T buffer");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(T::DQT ? DH == 128 : BM == 128, "every MMA has M = 128");
+  static_assert(T::LOOKAHEAD ? T::ST >= (T::NSB == 2 ? 3 : 2) : true, "ring too shallow");
 };
 
 struct BwdKParams {
@@ -194,13 +201,15 @@ __global__ void __launch_bounds__(320, 1)
                     const BwdKParams p) {
   using T = BwdTraits<HD>;
   using LY = BwdLayout<HD>;
-  constexpr int BM = T::BM, DH = LY::DH, KCH = LY::KCH, ST = T::STAGES;
+  constexpr int BM = T::BM, DH = LY::DH, KCH = LY::KCH, ST = T::ST, NSB = T::NSB;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   __shared__ uint64_t kv_full, qdo_full[ST], qdo_empty[ST];
-  __shared__ uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free, acc_full, mma_drain;
+  __shared__ uint64_t s_full[NSB], p_ready[NSB];
+  __shared__ uint64_t dp_full[2], ds_ready[2], dq_full[2], dq_free[2];
+  __shared__ uint64_t acc_full, mma_drain;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
 
@@ -222,12 +231,16 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&qdo_full[s], 1);
       mbar_init(&qdo_empty[s], 1);
     }
-    mbar_init(&s_full, 1);
-    mbar_init(&dp_full, 1);
-    mbar_init(&p_ready, 128);
-    mbar_init(&ds_ready, 128);
-    mbar_init(&dq_full, 1);
-    mbar_init(&dq_free, 128);
+    for (int s = 0; s < NSB; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_ready[s], 128);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&dp_full[s], 1);
+      mbar_init(&ds_ready[s], 128);
+      mbar_init(&dq_full[s], 1);
+      mbar_init(&dq_free[s], 128);
+    }
     mbar_init(&acc_full, 1);
     mbar_init(&mma_drain, 1);
     fence_barrier_init();
@@ -283,22 +296,27 @@ __global__ void __launch_bounds__(320, 1)
     // ------------------------------------------------------------------ MMA issuer
     if (elect_one()) {
       const uint32_t sK = smem_u32(smem + LY::OFF_K), sV = smem_u32(smem + LY::OFF_V);
-      const uint32_t sDS = smem_u32(smem + LY::OFF_DS);
       const uint32_t id_s = idesc_bf16(128, BM, 0, 0);      // S^T, dP^T: [kv x q]
       const uint32_t id_acc = idesc_bf16(128, DH, 0, 1);    // dV, dK: A tmem, B MN-major
       const uint32_t id_dq = T::DQT ? idesc_bf16(DH, BM, 1, 1) : idesc_bf16(BM, HD, 1, 1);
-      const uint32_t tS = tbase + LY::COL_S, tDP = tbase + LY::COL_DP;
       const uint32_t tDV = tbase + LY::COL_DV, tDK = tbase + LY::COL_DK;
-      const uint32_t tDQ = tbase + LY::COL_DQ;
+      // head-dim slice of Q / dO used as the B operand of dV, dK (MN-major, N = DH)
+      const uint32_t slice = (dh * DH / 64) * (BM * 128);
       bool ok = mbar_wait(&kv_full, 0, &abort_flag);
+      int q_ready = -1;  // highest iteration whose Q/dO stage wait is done
 
-      auto issue_s_dp = [&](int it) {
-        const int st = it % ST;
-        ok = ok && mbar_wait(&qdo_full[st], (it / ST) & 1, &abort_flag);
+      auto stage_ready = [&](int it) {
+        if (it > q_ready) {
+          ok = ok && mbar_wait(&qdo_full[it % ST], (it / ST) & 1, &abort_flag);
+          q_ready = it;
+          tc_fence_after();
+        }
+      };
+      auto issue_s = [&](int it) {  // S^T(it) = K Q^T
+        stage_ready(it);
         if (!ok) return;
-        tc_fence_after();
-        const uint32_t sQ = smem_u32(smem + LY::OFF_Q + st * LY::QT_BYTES);
-        const uint32_t sDO = smem_u32(smem + LY::OFF_DO + st * LY::QT_BYTES);
+        const uint32_t sQ = smem_u32(smem + LY::OFF_Q + (it % ST) * LY::QT_BYTES);
+        const uint32_t tS = tbase + LY::COL_S0 + (it % NSB) * BM;
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks) {
           const uint32_t ko = (ks / 4) * (kBN * 128) + (ks % 4) * 32;
@@ -306,7 +324,17 @@ __global__ void __launch_bounds__(320, 1)
           mma_ss(tS, smem_desc(sK + ko, 16, 1024), smem_desc(sQ + qo, 16, 1024), id_s,
                  ks > 0 ? 1u : 0u);
         }
-        mma_commit(&s_full);
+        mma_commit(&s_full[it % NSB]);
+      };
+      auto issue_dp = [&](int it) {  // dP^T(it) = V dO^T, into the buffer dQ(it-2) used
+        stage_ready(it);
+        if (ok && it >= 2) {
+          ok = mbar_wait(&dq_free[it % 2], ((it - 2) / 2) & 1, &abort_flag);
+          tc_fence_after();
+        }
+        if (!ok) return;
+        const uint32_t sDO = smem_u32(smem + LY::OFF_DO + (it % ST) * LY::QT_BYTES);
+        const uint32_t tDP = tbase + LY::COL_DP0 + (it % 2) * BM;
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks) {
           const uint32_t ko = (ks / 4) * (kBN * 128) + (ks % 4) * 32;
@@ -314,26 +342,38 @@ __global__ void __launch_bounds__(320, 1)
           mma_ss(tDP, smem_desc(sV + ko, 16, 1024), smem_desc(sDO + qo, 16, 1024), id_s,
                  ks > 0 ? 1u : 0u);
         }
-        mma_commit(&dp_full);
+        mma_commit(&dp_full[it % 2]);
       };
 
-      if (n_iter > 0) issue_s_dp(0);
+      if (n_iter > 0 && ok) {
+        issue_s(0);
+        issue_dp(0);
+        if (NSB == 2 && T::LOOKAHEAD && n_iter > 1) issue_s(1);
+      }
       for (int it = 0; it < n_iter && ok; ++it) {
         const int st = it % ST;
         const uint32_t sQ = smem_u32(smem + LY::OFF_Q + st * LY::QT_BYTES);
         const uint32_t sDO = smem_u32(smem + LY::OFF_DO + st * LY::QT_BYTES);
-        // head-dim slice of Q / dO used as the B operand (MN-major, N = DH)
-        const uint32_t slice = (dh * DH / 64) * (BM * 128);
+        const uint32_t tS = tbase + LY::COL_S0 + (it % NSB) * BM;
+        const uint32_t tDP = tbase + LY::COL_DP0 + (it % 2) * BM;
+        const uint32_t sDS = smem_u32(smem + LY::OFF_DS + (it % 2) * LY::DS_BYTES);
         // dV += P^T dO
-        ok = mbar_wait(&p_ready, it & 1, &abort_flag);
+        ok = mbar_wait(&p_ready[it % NSB], (it / NSB) & 1, &abort_flag);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < BM / 16; ++ks)
           mma_ts(tDV, tS + ks * 8, smem_desc(sDO + slice + ks * 2048, BM * 128, 1024), id_acc,
                  (it > 0 || ks > 0) ? 1u : 0u);
+        if constexpr (T::LOOKAHEAD) {
+          if (it + 1 < n_iter) {
+            if (NSB == 1) issue_s(it + 1);  // its buffer held P^T(it), now read by dV(it)
+            issue_dp(it + 1);
+            if (!ok) break;
+          }
+        }
         // dK += dS^T Q
-        ok = mbar_wait(&ds_ready, it & 1, &abort_flag);
+        ok = mbar_wait(&ds_ready[it % 2], (it / 2) & 1, &abort_flag);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -341,30 +381,32 @@ __global__ void __launch_bounds__(320, 1)
           mma_ts(tDK, tDP + ks * 8, smem_desc(sQ + slice + ks * 2048, BM * 128, 1024), id_acc,
                  (it > 0 || ks > 0) ? 1u : 0u);
         mma_commit(&qdo_empty[st]);
-        // next scores while this tile's dQ is formed
-        if (it + 1 < n_iter) issue_s_dp(it + 1);
-        if (!ok) break;
-        // dQ for this tile
-        if (it > 0) {
-          ok = mbar_wait(&dq_free, (it - 1) & 1, &abort_flag);
-          if (!ok) break;
-          tc_fence_after();
+        if constexpr (!T::LOOKAHEAD) {
+          if (it + 1 < n_iter) {
+            issue_s(it + 1);
+            issue_dp(it + 1);
+            if (!ok) break;
+          }
         }
+        // dQ of this tile, into the dP^T buffer (its dS^T has just been read by dK)
         if constexpr (T::DQT) {
           // dQ^T[d, q] = sum_kv K[kv, d] dS^T[kv, q]: A = K slice (MN-major), B = dS^T
           const uint32_t kslice = (dh * DH / 64) * (kBN * 128);
 #pragma unroll
           for (int ks = 0; ks < kBN / 16; ++ks)
-            mma_ss(tDQ, smem_desc(sK + kslice + ks * 2048, kBN * 128, 1024),
+            mma_ss(tDP, smem_desc(sK + kslice + ks * 2048, kBN * 128, 1024),
                    smem_desc(sDS + ks * 2048, kBN * 128, 1024), id_dq, ks > 0 ? 1u : 0u);
         } else {
           // dQ[q, d] = sum_kv dS^T[kv, q] K[kv, d]: A = dS^T (MN-major), B = K (MN-major)
 #pragma unroll
           for (int ks = 0; ks < kBN / 16; ++ks)
-            mma_ss(tDQ, smem_desc(sDS + ks * 2048, kBN * 128, 1024),
+            mma_ss(tDP, smem_desc(sDS + ks * 2048, kBN * 128, 1024),
                    smem_desc(sK + ks * 2048, kBN * 128, 1024), id_dq, ks > 0 ? 1u : 0u);
         }
-        mma_commit(&dq_full);
+        mma_commit(&dq_full[it % 2]);
+        if constexpr (T::LOOKAHEAD && NSB == 2) {
+          if (it + 2 < n_iter) issue_s(it + 2);  // its buffer held P^T(it), read by dV(it)
+        }
       }
       mma_commit(&acc_full);
       mma_commit(&mma_drain);
@@ -385,6 +427,8 @@ __global__ void __launch_bounds__(320, 1)
       const int bh = b * p.H + h;
       const float* sL = reinterpret_cast<const float*>(smem + LY::OFF_L + st * BM * 4);
       const float* sD = reinterpret_cast<const float*>(smem + LY::OFF_D + st * BM * 4);
+      const uint32_t colS = LY::COL_S0 + (it % NSB) * BM;
+      const uint32_t colDP = LY::COL_DP0 + (it % 2) * BM;
       // query q (column) sees this key iff q0 + q >= kv - (kl - ql)
       const int qmin = kv - (p.kl - p.ql) - q0;  // columns < qmin are hidden (causal)
       const bool edge = CAUSAL && (n0 + kBN - 1 - (p.kl - p.ql) > q0);
@@ -394,14 +438,14 @@ __global__ void __launch_bounds__(320, 1)
       // the stage's L and D rows came with the Q/dO copies; observe that barrier here too
       // (its next phase needs this tile's dK MMA, so it cannot have moved on)
       ok = __all_sync(0xffffffffu, mbar_wait(&qdo_full[st], (it / ST) & 1, &abort_flag));
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full, it & 1, &abort_flag));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[it % NSB], (it / NSB) & 1, &abort_flag));
       if (!ok) break;
       tc_fence_after();
       float pv[BM];
 #pragma unroll
       for (int c32 = 0; c32 < BM / 32; ++c32) {
         uint32_t r[32];
-        tmem_ld32(lane_base + LY::COL_S + c32 * 32, r);
+        tmem_ld32(lane_base + colS + c32 * 32, r);
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
@@ -421,24 +465,25 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(pv[c32 * 32 + 2 * e], pv[c32 * 32 + 2 * e + 1]);
-        tmem_st16(lane_base + LY::COL_S + c32 * 16, pk);
+        tmem_st16(lane_base + colS + c32 * 16, pk);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_ready);
+      mbar_arrive(&p_ready[it % NSB]);
 
-      ok = __all_sync(0xffffffffu, mbar_wait(&dp_full, it & 1, &abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(&dp_full[it % 2], (it / 2) & 1, &abort_flag));
       if (!ok) break;
       tc_fence_after();
-      // the previous tile's dQ MMA must be done reading the shared dS^T buffer
-      if (it > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&dq_full, (it - 1) & 1, &abort_flag));
+      // the dQ MMA of iteration it-2 must be done reading this dS^T buffer
+      if (it >= 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[it % 2], ((it - 2) / 2) & 1, &abort_flag));
         if (!ok) break;
       }
+      uint8_t* sds = smem + LY::OFF_DS + (it % 2) * LY::DS_BYTES;
 #pragma unroll
       for (int c32 = 0; c32 < BM / 32; ++c32) {
         uint32_t r[32];
-        tmem_ld32(lane_base + LY::COL_DP + c32 * 32, r);
+        tmem_ld32(lane_base + colDP + c32 * 32, r);
         tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
@@ -448,9 +493,9 @@ __global__ void __launch_bounds__(320, 1)
           const float d1 = pv[q + 1] * (__uint_as_float(r[2 * e + 1]) - sD[q + 1]);
           pk[e] = pack_bf16(d0, d1);
         }
-        tmem_st16(lane_base + LY::COL_DP + c32 * 16, pk);
+        tmem_st16(lane_base + colDP + c32 * 16, pk);
         // dS^T row j, columns c32*32 .. +31: 4 granules of the 64-column chunk c32/2
-        uint8_t* chunk = smem + LY::OFF_DS + (c32 / 2) * (kBN * 128);
+        uint8_t* chunk = sds + (c32 / 2) * (kBN * 128);
 #pragma unroll
         for (int g = 0; g < 4; ++g)
           st_swizzled(chunk, j, (c32 % 2) * 4 + g,
@@ -459,7 +504,7 @@ __global__ void __launch_bounds__(320, 1)
       fence_proxy_async();  // generic-proxy writes of dS^T -> visible to the tensor core
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&ds_ready);
+      mbar_arrive(&ds_ready[it % 2]);
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------------ WG1: dQ drain
@@ -470,7 +515,8 @@ __global__ void __launch_bounds__(320, 1)
       const int h = kh * G + it / nm;
       const int q0 = (m_first + it % nm) * BM;
       const int bh = b * p.H + h;
-      ok = __all_sync(0xffffffffu, mbar_wait(&dq_full, it & 1, &abort_flag));
+      const uint32_t colDQ = LY::COL_DP0 + (it % 2) * BM;
+      ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[it % 2], (it / 2) & 1, &abort_flag));
       if (!ok) break;
       tc_fence_after();
       if constexpr (T::DQT) {
@@ -480,7 +526,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int c32 = 0; c32 < BM / 32; ++c32) {
           uint32_t r[32];
-          tmem_ld32(lane_base + LY::COL_DQ + c32 * 32, r);
+          tmem_ld32(lane_base + colDQ + c32 * 32, r);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) atomicAdd(dst + (size_t)(c32 * 32 + e) * HD, __uint_as_float(r[e]));
@@ -492,7 +538,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int c32 = 0; c32 < HD / 32; ++c32) {
           uint32_t r[32];
-          tmem_ld32(lane_base + LY::COL_DQ + c32 * 32, r);
+          tmem_ld32(lane_base + colDQ + c32 * 32, r);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 8; ++e)
@@ -502,7 +548,7 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&dq_free);
+      mbar_arrive(&dq_free[it % 2]);
     }
     // ---------------------------------------------------------------- dK, dV epilogue
     const int j = wl * 32 + lane;

@@ -306,6 +306,52 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Three-input maximum (sm_100 family).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Packed pairs of f32 (one 64-bit register) for the sm_100-family f32x2 instructions.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// 2^x on the FMA pipe, for a share of the softmax exponentials (the MUFU unit does the rest).
+// Method: Cody-Waite range reduction x = n + f with n = round(x) obtained by the 1.5 * 2^23
+// magic-number addition, f in [-0.5, 0.5]; 2^f by a degree-3 polynomial whose coefficients are
+// this project's own relative-error minimax (Remez) fit on [-0.5, 0.5] (max relative error
+// 7.5e-5, far below the 2^-9 half-ulp of the bf16 P it feeds); 2^n is added to the exponent
+// field. Inputs below -126 return 0 (the softmax never needs values under 2^-126).
+__device__ __forceinline__ float ex2_poly(float x) {
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  constexpr float c0 = 0.99992806f, c1 = 0.69326097f, c2 = 0.24261113f, c3 = 0.05517167f;
+  const float xc = fmaxf(x, -126.0f);
+  const float t = xc + kMagic;
+  const float n = t - kMagic;
+  const float f = xc - n;
+  float p = fmaf(fmaf(fmaf(c3, f, c2), f, c1), f, c0);
+  const int e = __float_as_int(t) << 23;  // n << 23 (the mantissa bits of t hold n)
+  const float r = __int_as_float(__float_as_int(p) + e);
+  return x < -126.0f ? 0.0f : r;
+}
+
 // Pack two floats into bf16x2 (round to nearest even): `lo` in bits 0-15, `hi` in 16-31.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;

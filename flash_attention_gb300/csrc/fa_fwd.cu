@@ -38,17 +38,21 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest p before O is 
 
 template <int HD>
 struct FwdTraits;
+// NQ query tiles per CTA, BN keys per kv tile, NS score buffers per query tile, STAGES-deep
+// K/V ring. POLY: one pair of exponentials in every POLY goes to the FMA-pipe polynomial
+// (0 = all on MUFU); the MUFU unit (16 exp2 per clock per SM) would otherwise be as slow as
+// the tensor core at head_dim 128 and the bottleneck at 64.
 template <>
 struct FwdTraits<64> {
-  static constexpr int NQ = 2, BN = 128, NS = 1, STAGES = 3;
+  static constexpr int NQ = 2, BN = 128, NS = 1, STAGES = 3, POLY = 2;
 };
 template <>
 struct FwdTraits<128> {
-  static constexpr int NQ = 2, BN = 128, NS = 1, STAGES = 2;
+  static constexpr int NQ = 2, BN = 128, NS = 1, STAGES = 2, POLY = 4;
 };
 template <>
 struct FwdTraits<256> {
-  static constexpr int NQ = 1, BN = 64, NS = 2, STAGES = 2;
+  static constexpr int NQ = 1, BN = 64, NS = 2, STAGES = 2, POLY = 0;
 };
 
 template <int HD>
@@ -300,7 +304,6 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
       const bool edge = (n0 + BN > p.kl) || (CAUSAL && n0 + BN - 1 > p.kl - p.ql + tile_row0);
       const int lim = kmax_row - n0;  // element c visible iff c <= lim
       float x[BN];
-      float mx = -INFINITY;
 #pragma unroll
       for (int c32 = 0; c32 < BN / 32; ++c32) {
 #pragma unroll
@@ -313,9 +316,11 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
           }
           if (edge && c > lim) v = -INFINITY;
           x[c] = v;
-          mx = fmaxf(mx, v);
         }
       }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN; c += 2) mx = fmax3(mx, x[c], x[c + 1]);
       // row maximum in base-2 units
       const float m_tile = HAS_MASK ? mx : mx * c2;
       const float m_new = fmaxf(m_used, m_tile);
@@ -344,28 +349,36 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
         }
         m_used = m_new;
       }
-      // p = exp2(x - m_used), packed to bf16 pairs in place of S, 32 columns at a time
-      const float neg_m = -m_used;
-      float rs = 0.0f;
+      // p = exp2(x - m_used) on pairs, packed to bf16 in place of S, 32 columns at a time
+      const uint64_t negm = f2_pack(-m_used, -m_used);
+      const uint64_t c2v = f2_pack(c2, c2);
+      uint64_t acc = f2_pack(0.0f, 0.0f);
 #pragma unroll
       for (int c32 = 0; c32 < BN / 32; ++c32) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int c = c32 * 32 + 2 * e;
+          const uint64_t xv = f2_pack(x[c], x[c + 1]);
+          const uint64_t sv = HAS_MASK ? f2_add(xv, negm) : f2_fma(xv, c2v, negm);
+          float s0, s1;
+          f2_unpack(sv, s0, s1);
           float p0, p1;
-          if (HAS_MASK) {
-            p0 = ex2(x[c] + neg_m);
-            p1 = ex2(x[c + 1] + neg_m);
+          if (T::POLY > 0 && (e % (T::POLY > 0 ? T::POLY : 1)) == 0) {
+            p0 = ex2_poly(s0);
+            p1 = ex2_poly(s1);
           } else {
-            p0 = ex2(fmaf(x[c], c2, neg_m));
-            p1 = ex2(fmaf(x[c + 1], c2, neg_m));
+            p0 = ex2(s0);
+            p1 = ex2(s1);
           }
-          rs += p0 + p1;
+          acc = f2_add(acc, f2_pack(p0, p1));
           pk[e] = pack_bf16(p0, p1);
         }
         tmem_st16(s_addr + c32 * 16, pk);
       }
+      float rs0, rs1;
+      f2_unpack(acc, rs0, rs1);
+      const float rs = rs0 + rs1;
       l += rs;
       tmem_wait_st();
       tc_fence_before();
