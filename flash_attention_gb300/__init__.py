@@ -17,6 +17,7 @@ __all__ = [
     "FaParams", "fa_train_fwd", "fa_train_bwd", "fa_device_status", "fa_error_string",
     "fa_version", "fa_profile_enable", "fa_profile_read", "attention_fwd", "attention_bwd", "load_library", "build", "LIB_PATH",
     "FA_OK", "FA_ERR_INVALID", "FA_ERR_CUDA", "FA_ERR_DEVICE_TIMEOUT", "FA_ERR_UNSUPPORTED",
+    "FA_ERR_TOO_LARGE",
 ]
 
 FA_OK = 0
@@ -24,6 +25,7 @@ FA_ERR_INVALID = 1
 FA_ERR_CUDA = 2
 FA_ERR_DEVICE_TIMEOUT = 3
 FA_ERR_UNSUPPORTED = 4
+FA_ERR_TOO_LARGE = 5
 
 
 class FaParams(ctypes.Structure):

@@ -296,6 +296,65 @@ int fa_train_bwd(const void* q, const void* k, const void* v, const void* o, con
   return FA_OK;
 }
 
+int fa_train_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO, const float* mask, void* dq, void* dk,
+                         void* dv, const fa_params* p, void* stream) {
+  int rc = check_params(p);
+  if (rc) return rc;
+  if ((rc = check_bf16(q)) || (rc = check_bf16(k)) || (rc = check_bf16(v)) ||
+      (rc = check_bf16(o)) || (rc = check_f32(lse)) || (rc = check_bf16(dO)) ||
+      (rc = check_bf16(dq)) || (rc = check_bf16(dk)) || (rc = check_bf16(dv)))
+    return rc;
+  if (mask && !aligned(mask, 16)) return FA_ERR_INVALID;
+  const size_t ws_bytes = fa::bwd_workspace_bytes(p->batch, p->n_heads, p->ql, p->head_dim);
+  if (ws_bytes > fa::kNoAllocScratchBytes) {
+    snprintf(g_last_cuda_error, sizeof(g_last_cuda_error),
+             "fa_train_bwd_noalloc: needs %zu bytes of scratch, the fixed array holds %zu",
+             ws_bytes, fa::kNoAllocScratchBytes);
+    return FA_ERR_TOO_LARGE;
+  }
+  if ((rc = check_device())) return rc;
+  cudaError_t e = get_encoder();
+  if (e != cudaSuccess) return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
+  void* ws = nullptr;
+  if ((e = fa::noalloc_scratch(&ws)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+
+  fa::BwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.dO = dO;
+  a.mask = mask;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.B = p->batch;
+  a.H = p->n_heads;
+  a.Hk = p->n_kv_heads;
+  a.ql = p->ql;
+  a.kl = p->kl;
+  a.d = p->head_dim;
+  a.ql_pad = fa::bwd_ql_pad(a.ql);
+  a.scale = p->scale;
+  a.causal = p->causal;
+  a.status = nullptr;  // the status word is allocated; this path records no timeout
+  fa::BwdMaps m;
+  const int qrows = fa::bwd_q_box_rows(a.d), kvrows = fa::bwd_kv_box_rows(a.d);
+  if (!encode_bf16_3d(&m.q, q, a.B * a.H, a.ql, a.d, qrows) ||
+      !encode_bf16_3d(&m.dO, dO, a.B * a.H, a.ql, a.d, qrows) ||
+      !encode_bf16_3d(&m.k, k, a.B * a.Hk, a.kl, a.d, kvrows) ||
+      !encode_bf16_3d(&m.v, v, a.B * a.Hk, a.kl, a.d, kvrows))
+    return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+  // the pre-pass rewrites L*log2(e) and D and zeroes the dQ accumulator for every row the
+  // main pass reads, so the array's previous contents never reach a result
+  fa::bwd_carve_workspace(ws, a.B, a.H, a.ql, a.d, &a.lse2, &a.dvec, &a.dqacc);
+  e = fa::launch_bwd(a, m, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  return FA_OK;
+}
+
 int fa_device_status(int clear) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -319,6 +378,7 @@ const char* fa_error_string(int code) {
     case FA_ERR_CUDA: return "CUDA call or kernel launch failed";
     case FA_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait on the device";
     case FA_ERR_UNSUPPORTED: return "device is not an sm_100-family GPU (needs sm_103a)";
+    case FA_ERR_TOO_LARGE: return "problem needs more scratch than the fixed no-allocation array holds";
     default: return "unknown error code";
   }
 }

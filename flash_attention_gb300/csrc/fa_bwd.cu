@@ -24,6 +24,9 @@
 //                    dK, dV at the end
 //   bwd_dq_kernel    dQ = bf16(scale * accumulator)
 #include <float.h>
+
+#include <mutex>
+
 #include "fa_common.cuh"
 #include "fa_launch.h"
 
@@ -681,6 +684,35 @@ static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t
     profile_mark(kKernBwdDq, 1, s);
   }
   return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------ fixed scratch
+// Backward scratch for callers that must not allocate device memory (fa_train_bwd_noalloc).
+// A file-scope device array: every GPU that loads this library holds these bytes until the
+// process exits. Host code cannot use the array's name as a device address, so its address
+// is looked up once per device with cudaGetSymbolAddress (below) and passed to the kernels.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kMaxNoAllocDevices = 64;
+void* g_noalloc_ptr[kMaxNoAllocDevices] = {nullptr};
+std::mutex g_noalloc_mu;
+}  // namespace
+
+cudaError_t noalloc_scratch(void** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxNoAllocDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // with `dev` current
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return cudaSuccess;
 }
 
 cudaError_t launch_bwd(const BwdArgs& a, const BwdMaps& m, cudaStream_t stream) {

@@ -75,4 +75,9 @@ void bwd_carve_workspace(void* base, int B, int H, int ql, int d, float** lse2, 
 
 cudaError_t launch_bwd(const BwdArgs& a, const BwdMaps& m, cudaStream_t stream);
 
+// Fixed-size device scratch of fa_train_bwd_noalloc (defined in fa_bwd.cu). The first call on a
+// device looks up the array's device address; later calls return the cached address.
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
+cudaError_t noalloc_scratch(void** ptr);
+
 }  // namespace fa

@@ -73,6 +73,7 @@ typedef struct fa_params {
 #define FA_ERR_CUDA 2           /* a CUDA runtime/driver call or a launch failed */
 #define FA_ERR_DEVICE_TIMEOUT 3 /* a kernel gave up a bounded wait (see fa_device_status) */
 #define FA_ERR_UNSUPPORTED 4    /* the device is not sm_103 or sm_100 family */
+#define FA_ERR_TOO_LARGE 5      /* the problem needs more scratch than fa_train_bwd_noalloc has */
 
 /* Forward: O and L. Page "mlx-native tests/test_flash_attn_train.rs", sections 2-8 (forward
  * parity), function `sdpa_reference_with_logsumexp`.
@@ -116,6 +117,33 @@ int fa_profile_enable(int on);
 int fa_profile_read(double* total_ms, int64_t* launches);
 /* Name of a kernel id (static storage). */
 const char* fa_kernel_name(int id);
+
+/* Backward without any device allocation. The pages have no counterpart of this entry point.
+ *
+ * Some callers cannot let a library allocate device memory: processes whose GPU memory is
+ * owned by a pool allocator that has already reserved the device (an allocation made behind
+ * its back can fail or be invisible to its accounting), and step loops where an allocation is
+ * not allowed because it may block or fail at an unpredictable moment. For them this call does
+ * what fa_train_bwd does, with the same arguments, layouts and results, but takes its scratch
+ * (the per-row D, L*log2(e) and the f32 dQ accumulator) from a fixed array compiled into the
+ * library instead of cudaMallocAsync. It calls no cudaMalloc, cudaFree or other allocating
+ * routine; the caller still provides every input and output.
+ *
+ * Limits and rules:
+ *  - the scratch holds 64 MiB per GPU, held from the moment the library is loaded on that GPU
+ *    until the process exits; a problem whose scratch, 4*B*H*ceil128(ql)*(head_dim + 2) bytes
+ *    plus alignment, exceeds it returns FA_ERR_TOO_LARGE without touching the device;
+ *  - every call on a GPU shares that one array, and the array keeps the previous call's
+ *    contents (each call rewrites what it reads, so that does not leak into results); calls
+ *    that overlap on the GPU (for example on two streams) race on it and give wrong results:
+ *    serialise them;
+ *  - the first call on each GPU looks up the array's device address (one runtime call, made
+ *    with that GPU current); make that first call before any stream capture;
+ *  - a bounded wait that runs out in one of its kernels is not recorded for fa_device_status
+ *    (the kernel still ends). */
+int fa_train_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO, const float* mask, void* dq, void* dk,
+                         void* dv, const fa_params* p, void* stream);
 
 /* Synchronises the current device, then returns FA_OK, or FA_ERR_DEVICE_TIMEOUT if any kernel
  * of this library on it gave up a bounded wait since the last call with clear != 0. */
