@@ -10,10 +10,10 @@
 // query head that shares its kv head (so dK and dV are reduced in the CTA, without atomics),
 // and dQ accumulated in f32 across CTAs. P is recomputed from L with base-2 exponentials:
 // P = exp2(S * scale * log2(e) + mask * log2(e) - L * log2(e)); a row with L = -inf (no
-// visible key) gets +inf in place of L * log2(e), which makes its P exactly 0.
+// visible key) gets -inf in place of -L * log2(e), which makes its P exactly 0.
 //
 // Kernels:
-//   bwd_prep_kernel  D_i, L_i * log2(e), and zeroes the dQ accumulator (bandwidth bound)
+//   bwd_prep_kernel  D_i, -L_i * log2(e), and zeroes the dQ accumulator (bandwidth bound)
 //   bwd_main_kernel  per kv tile of 128 rows (and, for head_dim 256, per half of the head
 //                    dimension): S^T = K Q^T and dP^T = V dO^T into TMEM; P^T and dS^T
 //                    computed by one warpgroup (thread = kv row = TMEM lane) and written back
@@ -45,20 +45,24 @@ constexpr float kLog2eB = 1.4426950408889634f;
 // forms dV, dK and dQ.
 template <int HD>
 struct BwdTraits;
+// DQ_BULK: the dQ tile is staged in shared memory ([q][d] f32, contiguous in the accumulator)
+// and added to the accumulator by one bulk reduction; otherwise each thread adds its values
+// with global reductions.
 template <>
 struct BwdTraits<64> {
   static constexpr int BM = 128, DSPLIT = 1, ST = 3, NSB = 1;
-  static constexpr bool DQT = false, LOOKAHEAD = true;  // dQ = dS K (M = BM)
+  static constexpr bool DQT = false, LOOKAHEAD = true, DQ_BULK = false;  // dQ = dS K (M = BM)
 };
 template <>
 struct BwdTraits<128> {
   static constexpr int BM = 64, DSPLIT = 1, ST = 3, NSB = 2;
-  static constexpr bool DQT = true, LOOKAHEAD = true;  // dQ^T = K^T dS^T (M = head-dim slice)
+  // dQ^T = K^T dS^T (M = head-dim slice)
+  static constexpr bool DQT = true, LOOKAHEAD = true, DQ_BULK = true;
 };
 template <>
 struct BwdTraits<256> {
   static constexpr int BM = 64, DSPLIT = 2, ST = 1, NSB = 2;
-  static constexpr bool DQT = true, LOOKAHEAD = false;
+  static constexpr bool DQT = true, LOOKAHEAD = false, DQ_BULK = false;
 };
 
 constexpr int kBN = 128;  // kv rows per CTA (the M of the kv-major MMAs)
@@ -79,7 +83,9 @@ struct BwdLayout {
   static constexpr int OFF_DS = OFF_DO + T::ST * QT_BYTES;      // 2 x dS^T [kv][q] swizzled
   static constexpr int OFF_L = OFF_DS + 2 * DS_BYTES;           // ST x BM f32
   static constexpr int OFF_D = OFF_L + T::ST * BM * 4;          // ST x BM f32
-  static constexpr int OFF_END = OFF_D + T::ST * BM * 4;
+  static constexpr int OFF_STG = OFF_D + T::ST * BM * 4;            // dQ staging [BM][HD] f32
+  static constexpr int STG_BYTES = T::DQ_BULK ? BM * HD * 4 : 0;
+  static constexpr int OFF_END = OFF_STG + STG_BYTES;
   static constexpr int SMEM_BYTES = OFF_END + 1024;
   // TMEM columns: S^T buffers, dP^T buffers (also holding dQ), dV, dK
   static constexpr int COL_S0 = 0;
@@ -89,13 +95,16 @@ struct BwdLayout {
   static constexpr int TMEM_USED = COL_DK + DH;
   static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
   static constexpr int DQ_COLS = T::DQT ? BM : HD;
-  static constexpr int THREADS = 320;  // WG0 dS, WG1 dQ drain + epilogue, TMA warp, MMA warp
-  static constexpr int TMA_WARP = 8, MMA_WARP = 9;
+  // WG0 (warps 0-3): P^T and the dQ drain; WG1 (warps 4-7): dS^T and the dK/dV epilogue;
+  // warp 8: TMA; warp 9: MMA; warp 10: issues the bulk dQ reductions; warp 11: idle.
+  static constexpr int THREADS = 384;
+  static constexpr int TMA_WARP = 8, MMA_WARP = 9, BULK_WARP = 10;
   static_assert(TMEM_USED <= 512, "TMEM budget");
   static_assert(DQ_COLS <= BM, "dQ tile must fit in a dP^T buffer");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(T::DQT ? DH == 128 : BM == 128, "every MMA has M = 128");
   static_assert(T::LOOKAHEAD ? T::ST >= (T::NSB == 2 ? 3 : 2) : true, "ring too shallow");
+  static_assert(!T::DQ_BULK || (T::DQT && T::DSPLIT == 1), "bulk dQ needs whole [q][d] rows");
 };
 
 struct BwdKParams {
@@ -149,12 +158,12 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (lane == 0) {
-    float l2 = INFINITY;  // padding rows and fully masked rows: P = exp2(s - inf) = 0
+    float nl2 = -INFINITY;  // padding rows and fully masked rows: P = exp2(s - inf) = 0
     if (i < ql) {
       const float L = lse[(size_t)bh * ql + i];
-      if (L != -INFINITY) l2 = L * kLog2eB;
+      if (L != -INFINITY) nl2 = -L * kLog2eB;
     }
-    lse2[(size_t)bh * ql_pad + i] = l2;
+    lse2[(size_t)bh * ql_pad + i] = nl2;
     dvec[(size_t)bh * ql_pad + i] = acc;
   }
   float4* z = reinterpret_cast<float4*>(dqacc + ((size_t)bh * ql_pad + i) * HD);
@@ -198,7 +207,7 @@ __device__ __forceinline__ void st_swizzled(uint8_t* chunk, int j, int g, uint4 
 }
 
 template <int HD, bool CAUSAL, bool HAS_MASK>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                     const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mDO,
                     const BwdKParams p) {
@@ -213,6 +222,7 @@ __global__ void __launch_bounds__(320, 1)
   __shared__ uint64_t s_full[NSB], p_ready[NSB];
   __shared__ uint64_t dp_full[2], ds_ready[2], dq_full[2], dq_free[2];
   __shared__ uint64_t acc_full, mma_drain;
+  __shared__ uint64_t stg_full, stg_free;  // dQ staging handshake of the bulk drain
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
 
@@ -246,6 +256,8 @@ __global__ void __launch_bounds__(320, 1)
     }
     mbar_init(&acc_full, 1);
     mbar_init(&mma_drain, 1);
+    mbar_init(&stg_full, 128);
+    mbar_init(&stg_free, 1);
     fence_barrier_init();
   }
   if (warp == LY::MMA_WARP) {
@@ -370,7 +382,6 @@ __global__ void __launch_bounds__(320, 1)
                  (it > 0 || ks > 0) ? 1u : 0u);
         if constexpr (T::LOOKAHEAD) {
           if (it + 1 < n_iter) {
-            if (NSB == 1) issue_s(it + 1);  // its buffer held P^T(it), now read by dV(it)
             issue_dp(it + 1);
             if (!ok) break;
           }
@@ -384,6 +395,14 @@ __global__ void __launch_bounds__(320, 1)
           mma_ts(tDK, tDP + ks * 8, smem_desc(sQ + slice + ks * 2048, BM * 128, 1024), id_acc,
                  (it > 0 || ks > 0) ? 1u : 0u);
         mma_commit(&qdo_empty[st]);
+        if constexpr (T::LOOKAHEAD && NSB == 1) {
+          // one score buffer: S^T(it+1) overwrites P^T(it), which dV(it) and the dS warpgroup
+          // read; dK(it) was issued after that warpgroup signalled ds_ready(it)
+          if (it + 1 < n_iter) {
+            issue_s(it + 1);
+            if (!ok) break;
+          }
+        }
         if constexpr (!T::LOOKAHEAD) {
           if (it + 1 < n_iter) {
             issue_s(it + 1);
@@ -415,147 +434,252 @@ __global__ void __launch_bounds__(320, 1)
       mma_commit(&mma_drain);
       mbar_wait_drain(&mma_drain, 0);
     }
+  } else if (warp == LY::BULK_WARP) {
+    // ------------------------------------------------------------------ bulk dQ reductions
+    if constexpr (T::DQ_BULK) {
+      if (elect_one()) {
+        const float* stg = reinterpret_cast<const float*>(smem + LY::OFF_STG);
+        for (int it = 0; it < n_iter; ++it) {
+          if (!mbar_wait(&stg_full, it & 1, &abort_flag)) break;
+          const int h = kh * G + it / nm;
+          const int q0 = (m_first + it % nm) * BM;
+          const int bh = b * p.H + h;
+          bulk_reduce_add_f32(p.dqacc + ((size_t)bh * p.ql_pad + q0) * HD, stg, BM * HD * 4);
+          bulk_commit();
+          bulk_wait_read<0>();  // the staging buffer has been read
+          mbar_arrive(&stg_free);
+        }
+        bulk_wait<0>();  // every reduction has landed before the CTA exits
+      }
+    }
   } else if (warp < 4) {
-    // ------------------------------------------------------------------ WG0: P^T and dS^T
+    // ------------------------------------------------------------------ WG0: P^T, dQ drain
     const int j = warp * 32 + lane;  // kv row within the tile == TMEM lane
     const int kv = n0 + j;
     const bool kv_live = kv < p.kl;
     const uint32_t lane_base = tbase + ((uint32_t)(warp * 32) << 16);
     const float c2 = p.scale_log2;
+    const uint64_t c2v = f2_pack(c2, c2);
     bool ok = true;
-    for (int it = 0; it < n_iter; ++it) {
+
+    // dQ of iteration `it` into the f32 accumulator
+    auto drain = [&](int it) {
+      const int h = kh * G + it / nm;
+      const int q0 = (m_first + it % nm) * BM;
+      const int bh = b * p.H + h;
+      const uint32_t colDQ = LY::COL_DP0 + (it % 2) * BM;
+      ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[it % 2], (it / 2) & 1, &abort_flag));
+      if (!ok) return;
+      tc_fence_after();
+      if constexpr (T::DQ_BULK) {
+        // lane = head-dim index, column = query row: stage as [q][d] f32 (contiguous in the
+        // accumulator); the bulk warp adds the tile with one reduction. The staging buffer is
+        // handed over with mbarriers: stg_full once written, stg_free once read.
+        float* stg = reinterpret_cast<float*>(smem + LY::OFF_STG);
+        uint32_t rq[BM / 32][32];
+#pragma unroll
+        for (int c32 = 0; c32 < BM / 32; ++c32) tmem_ld32(lane_base + colDQ + c32 * 32, rq[c32]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&dq_free[it % 2]);
+        if (it > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&stg_free, (it - 1) & 1, &abort_flag));
+          if (!ok) return;
+        }
+#pragma unroll
+        for (int c32 = 0; c32 < BM / 32; ++c32)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) stg[(c32 * 32 + e) * HD + j] = __uint_as_float(rq[c32][e]);
+        fence_proxy_async();  // staging writes -> visible to the bulk copy
+        mbar_arrive(&stg_full);
+      } else if constexpr (T::DQT) {
+        // lane = head-dim index within the slice, column = query row
+        float* dst = p.dqacc + ((size_t)bh * p.ql_pad + q0) * HD + dh * DH + j;
+        uint32_t rq[BM / 32][32];
+#pragma unroll
+        for (int c32 = 0; c32 < BM / 32; ++c32) tmem_ld32(lane_base + colDQ + c32 * 32, rq[c32]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&dq_free[it % 2]);
+#pragma unroll
+        for (int c32 = 0; c32 < BM / 32; ++c32)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            atomicAdd(dst + (size_t)(c32 * 32 + e) * HD, __uint_as_float(rq[c32][e]));
+      } else {
+        // lane = query row, column = head-dim index
+        float4* dst = reinterpret_cast<float4*>(p.dqacc + ((size_t)bh * p.ql_pad + q0 + j) * HD);
+        uint32_t rq[HD / 32][32];
+#pragma unroll
+        for (int c32 = 0; c32 < HD / 32; ++c32) tmem_ld32(lane_base + colDQ + c32 * 32, rq[c32]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&dq_free[it % 2]);
+#pragma unroll
+        for (int c32 = 0; c32 < HD / 32; ++c32)
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            atomicAdd(dst + c32 * 8 + e,
+                      make_float4(__uint_as_float(rq[c32][4 * e]), __uint_as_float(rq[c32][4 * e + 1]),
+                                  __uint_as_float(rq[c32][4 * e + 2]),
+                                  __uint_as_float(rq[c32][4 * e + 3])));
+      }
+    };
+
+    for (int it = 0; it < n_iter && ok; ++it) {
       const int st = it % ST;
       const int h = kh * G + it / nm;
       const int q0 = (m_first + it % nm) * BM;
       const int bh = b * p.H + h;
       const float* sL = reinterpret_cast<const float*>(smem + LY::OFF_L + st * BM * 4);
-      const float* sD = reinterpret_cast<const float*>(smem + LY::OFF_D + st * BM * 4);
       const uint32_t colS = LY::COL_S0 + (it % NSB) * BM;
-      const uint32_t colDP = LY::COL_DP0 + (it % 2) * BM;
       // query q (column) sees this key iff q0 + q >= kv - (kl - ql)
       const int qmin = kv - (p.kl - p.ql) - q0;  // columns < qmin are hidden (causal)
       const bool edge = CAUSAL && (n0 + kBN - 1 - (p.kl - p.ql) > q0);
+      // columns below qcut get P = 0: the causal bound on edge tiles, every column for kv rows
+      // past the end
+      const bool need_mask = edge || !kv_live;
+      const int qcut = !kv_live ? BM : (edge ? qmin : 0);
       const float* mcol = nullptr;
       if (HAS_MASK && kv_live) mcol = p.mask + ((size_t)bh * p.ql + q0) * (size_t)p.kl + kv;
 
-      // the stage's L and D rows came with the Q/dO copies; observe that barrier here too
-      // (its next phase needs this tile's dK MMA, so it cannot have moved on)
+      // the stage's L rows came with the Q/dO copies; observe that barrier here too (its
+      // next phase needs this tile's dK MMA, so it cannot have moved on)
       ok = __all_sync(0xffffffffu, mbar_wait(&qdo_full[st], (it / ST) & 1, &abort_flag));
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[it % NSB], (it / NSB) & 1, &abort_flag));
       if (!ok) break;
       tc_fence_after();
-      float pv[BM];
+      const float4* sL4 = reinterpret_cast<const float4*>(sL);  // -L*log2(e) per query
+      constexpr int GRP = BM / 32 < 2 ? BM / 32 : 2;  // 32-column chunks loaded per wait
 #pragma unroll
-      for (int c32 = 0; c32 < BM / 32; ++c32) {
-        uint32_t r[32];
-        tmem_ld32(lane_base + colS + c32 * 32, r);
+      for (int g0 = 0; g0 < BM / 32; g0 += GRP) {
+        uint32_t rs[GRP][32];
+#pragma unroll
+        for (int g = 0; g < GRP; ++g) tmem_ld32(lane_base + colS + (g0 + g) * 32, rs[g]);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int q = c32 * 32 + e;
-          float x = __uint_as_float(r[e]);
-          float mterm = 0.0f;
-          if (HAS_MASK) mterm = (mcol != nullptr && q0 + q < p.ql) ? mcol[(size_t)q * p.kl] : 0.0f;
-          float s2 = fmaf(x, c2, fmaf(mterm, kLog2eB, -sL[q]));
-          float pr = ex2(s2);
-          if (!kv_live || (edge && q < qmin)) pr = 0.0f;
-          pv[q] = pr;
+        for (int g = 0; g < GRP; ++g) {
+          const int c32 = g0 + g;
+          uint32_t pk[16];
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 nl = sL4[c32 * 8 + e4];
+            const int q = c32 * 32 + e4 * 4;
+            uint64_t b01 = f2_pack(nl.x, nl.y), b23 = f2_pack(nl.z, nl.w);
+            if (HAS_MASK) {
+              float m4[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                m4[k] = (mcol != nullptr && q0 + q + k < p.ql) ? mcol[(size_t)(q + k) * p.kl] * kLog2eB
+                                                               : 0.0f;
+              b01 = f2_add(b01, f2_pack(m4[0], m4[1]));
+              b23 = f2_add(b23, f2_pack(m4[2], m4[3]));
+            }
+            const uint32_t* r = rs[g];
+            const uint64_t s01 = f2_fma(f2_pack(__uint_as_float(r[4 * e4]), __uint_as_float(r[4 * e4 + 1])), c2v, b01);
+            const uint64_t s23 = f2_fma(f2_pack(__uint_as_float(r[4 * e4 + 2]), __uint_as_float(r[4 * e4 + 3])), c2v, b23);
+            float a0, a1, a2, a3;
+            f2_unpack(s01, a0, a1);
+            f2_unpack(s23, a2, a3);
+            float p0 = ex2(a0), p1 = ex2(a1), p2 = ex2(a2), p3 = ex2(a3);
+            if (need_mask) {  // hidden columns (causal) and kv rows past the end
+              p0 = q >= qcut ? p0 : 0.0f;
+              p1 = q + 1 >= qcut ? p1 : 0.0f;
+              p2 = q + 2 >= qcut ? p2 : 0.0f;
+              p3 = q + 3 >= qcut ? p3 : 0.0f;
+            }
+            pk[2 * e4] = pack_bf16(p0, p1);
+            pk[2 * e4 + 1] = pack_bf16(p2, p3);
+          }
+          // P^T as bf16 into the S columns (A operand of dV += P^T dO; read again by WG1)
+          tmem_st16(lane_base + colS + c32 * 16, pk);
         }
-      }
-      // P^T as bf16 into the S columns (A operand of dV += P^T dO)
-#pragma unroll
-      for (int c32 = 0; c32 < BM / 32; ++c32) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(pv[c32 * 32 + 2 * e], pv[c32 * 32 + 2 * e + 1]);
-        tmem_st16(lane_base + colS + c32 * 16, pk);
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&p_ready[it % NSB]);
-
+      // dQ of the previous tile (its MMA followed that tile's dK)
+      if (it > 0) drain(it - 1);
+    }
+    if (ok && n_iter > 0) drain(n_iter - 1);
+  } else if (warp < 8) {
+    // ------------------------------------------------------------------ WG1: dS^T, epilogue
+    const int wl = warp - 4;
+    const int j = wl * 32 + lane;
+    const int kv = n0 + j;
+    const uint32_t lane_base = tbase + ((uint32_t)(wl * 32) << 16);
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int st = it % ST;
+      const float* sD = reinterpret_cast<const float*>(smem + LY::OFF_D + st * BM * 4);
+      const uint32_t colS = LY::COL_S0 + (it % NSB) * BM;
+      const uint32_t colDP = LY::COL_DP0 + (it % 2) * BM;
       ok = __all_sync(0xffffffffu, mbar_wait(&dp_full[it % 2], (it / 2) & 1, &abort_flag));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&p_ready[it % NSB], (it / NSB) & 1, &abort_flag));
+      // the stage's D rows came with the Q/dO copies (that phase cannot have moved on: its
+      // next one needs this tile's dK MMA)
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&qdo_full[st], (it / ST) & 1, &abort_flag));
+      // the dQ MMA of tile it-2 must be done reading this dS^T buffer
+      if (ok && it >= 2)
+        ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[it % 2], ((it - 2) / 2) & 1, &abort_flag));
       if (!ok) break;
       tc_fence_after();
-      // the dQ MMA of iteration it-2 must be done reading this dS^T buffer
-      if (it >= 2) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[it % 2], ((it - 2) / 2) & 1, &abort_flag));
-        if (!ok) break;
-      }
       uint8_t* sds = smem + LY::OFF_DS + (it % 2) * LY::DS_BYTES;
+      const float4* sD4 = reinterpret_cast<const float4*>(sD);
+      constexpr int GRP = BM / 32 < 2 ? BM / 32 : 2;  // 32-column chunks loaded per wait
 #pragma unroll
-      for (int c32 = 0; c32 < BM / 32; ++c32) {
-        uint32_t r[32];
-        tmem_ld32(lane_base + colDP + c32 * 32, r);
-        tmem_wait_ld();
-        uint32_t pk[16];
+      for (int g0 = 0; g0 < BM / 32; g0 += GRP) {
+        uint32_t rd[GRP][32];
+        uint32_t rp[32];  // P^T bf16 pairs of these 2 x 32 columns (first 16 or 32 used)
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int q = c32 * 32 + 2 * e;
-          const float d0 = pv[q] * (__uint_as_float(r[2 * e]) - sD[q]);
-          const float d1 = pv[q + 1] * (__uint_as_float(r[2 * e + 1]) - sD[q + 1]);
-          pk[e] = pack_bf16(d0, d1);
+        for (int g = 0; g < GRP; ++g) tmem_ld32(lane_base + colDP + (g0 + g) * 32, rd[g]);
+        if (GRP == 2) {
+          tmem_ld32(lane_base + colS + g0 * 16, rp);
+        } else {
+          tmem_ld16(lane_base + colS + g0 * 16, *reinterpret_cast<uint32_t(*)[16]>(rp));
         }
-        tmem_st16(lane_base + colDP + c32 * 16, pk);
-        // dS^T row j, columns c32*32 .. +31: 4 granules of the 64-column chunk c32/2
-        uint8_t* chunk = sds + (c32 / 2) * (kBN * 128);
+        tmem_wait_ld();
 #pragma unroll
-        for (int g = 0; g < 4; ++g)
-          st_swizzled(chunk, j, (c32 % 2) * 4 + g,
-                      make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]));
+        for (int g = 0; g < GRP; ++g) {
+          const int c32 = g0 + g;
+          const uint32_t* r = rd[g];
+          uint32_t pk[16];
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 dd = sD4[c32 * 8 + e4];
+            // P of columns q .. q+3 from the packed pairs (bf16 -> f32 is a shift)
+            const uint32_t pp0 = rp[g * 16 + 2 * e4];
+            const uint32_t pp1 = rp[g * 16 + 2 * e4 + 1];
+            const uint64_t pv01 = f2_pack(__uint_as_float(pp0 << 16), __uint_as_float(pp0 & 0xffff0000u));
+            const uint64_t pv23 = f2_pack(__uint_as_float(pp1 << 16), __uint_as_float(pp1 & 0xffff0000u));
+            const uint64_t t01 = f2_add(f2_pack(__uint_as_float(r[4 * e4]), __uint_as_float(r[4 * e4 + 1])),
+                                        f2_pack(-dd.x, -dd.y));
+            const uint64_t t23 = f2_add(f2_pack(__uint_as_float(r[4 * e4 + 2]), __uint_as_float(r[4 * e4 + 3])),
+                                        f2_pack(-dd.z, -dd.w));
+            const uint64_t u01 = f2_mul(t01, pv01);
+            const uint64_t u23 = f2_mul(t23, pv23);
+            float d0, d1, d2, d3;
+            f2_unpack(u01, d0, d1);
+            f2_unpack(u23, d2, d3);
+            pk[2 * e4] = pack_bf16(d0, d1);
+            pk[2 * e4 + 1] = pack_bf16(d2, d3);
+          }
+          tmem_st16(lane_base + colDP + c32 * 16, pk);
+          // dS^T row j, columns c32*32 .. +31: 4 granules of the 64-column chunk c32/2
+          uint8_t* chunk = sds + (c32 / 2) * (kBN * 128);
+#pragma unroll
+          for (int gg = 0; gg < 4; ++gg)
+            st_swizzled(chunk, j, (c32 % 2) * 4 + gg,
+                        make_uint4(pk[4 * gg], pk[4 * gg + 1], pk[4 * gg + 2], pk[4 * gg + 3]));
+        }
       }
       fence_proxy_async();  // generic-proxy writes of dS^T -> visible to the tensor core
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&ds_ready[it % 2]);
     }
-  } else if (warp < 8) {
-    // ------------------------------------------------------------------ WG1: dQ drain
-    const int wl = warp - 4;
-    const uint32_t lane_base = tbase + ((uint32_t)(wl * 32) << 16);
-    bool ok = true;
-    for (int it = 0; it < n_iter; ++it) {
-      const int h = kh * G + it / nm;
-      const int q0 = (m_first + it % nm) * BM;
-      const int bh = b * p.H + h;
-      const uint32_t colDQ = LY::COL_DP0 + (it % 2) * BM;
-      ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[it % 2], (it / 2) & 1, &abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      if constexpr (T::DQT) {
-        // lane = head-dim index within the slice, column = query row
-        const int dc = dh * DH + wl * 32 + lane;
-        float* dst = p.dqacc + ((size_t)bh * p.ql_pad + q0) * HD + dc;
-#pragma unroll
-        for (int c32 = 0; c32 < BM / 32; ++c32) {
-          uint32_t r[32];
-          tmem_ld32(lane_base + colDQ + c32 * 32, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) atomicAdd(dst + (size_t)(c32 * 32 + e) * HD, __uint_as_float(r[e]));
-        }
-      } else {
-        // lane = query row, column = head-dim index
-        const int q = wl * 32 + lane;
-        float4* dst = reinterpret_cast<float4*>(p.dqacc + ((size_t)bh * p.ql_pad + q0 + q) * HD);
-#pragma unroll
-        for (int c32 = 0; c32 < HD / 32; ++c32) {
-          uint32_t r[32];
-          tmem_ld32(lane_base + colDQ + c32 * 32, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            atomicAdd(dst + c32 * 8 + e,
-                      make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
-                                  __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3])));
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&dq_free[it % 2]);
-    }
+
     // ---------------------------------------------------------------- dK, dV epilogue
-    const int j = wl * 32 + lane;
-    const int kv = n0 + j;
     bool have = false;
     if (ok) {
       ok = __all_sync(0xffffffffu, mbar_wait(&acc_full, 0, &abort_flag));

@@ -44,11 +44,11 @@ struct FwdTraits;
 // the tensor core at head_dim 128 and the bottleneck at 64.
 template <>
 struct FwdTraits<64> {
-  static constexpr int NQ = 2, BN = 128, NS = 1, STAGES = 3, POLY = 2;
+  static constexpr int NQ = 2, BN = 128, NS = 1, STAGES = 3, POLY = 4;
 };
 template <>
 struct FwdTraits<128> {
-  static constexpr int NQ = 2, BN = 128, NS = 1, STAGES = 2, POLY = 4;
+  static constexpr int NQ = 2, BN = 128, NS = 1, STAGES = 2, POLY = 8;
 };
 template <>
 struct FwdTraits<256> {
@@ -70,7 +70,7 @@ struct FwdLayout {
   static constexpr int TILE_COLS = HD + T::NS * T::BN;
   static constexpr int TMEM_COLS_USED = T::NQ * TILE_COLS;
   static constexpr int TMEM_COLS = TMEM_COLS_USED <= 256 ? 256 : 512;
-  static constexpr int THREADS = T::NQ * 128 + 64;
+  static constexpr int THREADS = T::NQ * 128 + 64;  // softmax warpgroups + TMA + MMA warps
   static constexpr int TMA_WARP = T::NQ * 4;
   static constexpr int MMA_WARP = T::NQ * 4 + 1;
   static_assert(TMEM_COLS_USED <= 512, "TMEM budget");
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
       mma_commit(&mma_drain);
       mbar_wait_drain(&mma_drain, 0);
     }
-  } else {
+  } else if (warp < 4 * NQ) {
     // ------------------------------------------------------------------ softmax warpgroups
     const int t = warp / 4;
     const int wl = warp % 4;
@@ -303,24 +303,30 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
       // does any element of this tile need masking (uniform over the warpgroup)?
       const bool edge = (n0 + BN > p.kl) || (CAUSAL && n0 + BN - 1 > p.kl - p.ql + tile_row0);
       const int lim = kmax_row - n0;  // element c visible iff c <= lim
-      float x[BN];
+      // scores in place of the loaded row: raw S, or (with a mask) the base-2 score; -inf
+      // where the key is hidden. Tiles away from the diagonal and the key tail skip this.
+      if (HAS_MASK || edge) {
 #pragma unroll
-      for (int c32 = 0; c32 < BN / 32; ++c32) {
+        for (int c32 = 0; c32 < BN / 32; ++c32) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int c = c32 * 32 + e;
-          float v = __uint_as_float(sr[c32][e]);
-          if (HAS_MASK) {
-            float mv = (mrow != nullptr && n0 + c < p.kl) ? mrow[n0 + c] : 0.0f;
-            v = fmaf(v, c2, mv * kLog2e);
+          for (int e = 0; e < 32; ++e) {
+            const int c = c32 * 32 + e;
+            float v = __uint_as_float(sr[c32][e]);
+            if (HAS_MASK) {
+              float mv = (mrow != nullptr && n0 + c < p.kl) ? mrow[n0 + c] : 0.0f;
+              v = fmaf(v, c2, mv * kLog2e);
+            }
+            if (c > lim) v = -INFINITY;
+            sr[c32][e] = __float_as_uint(v);
           }
-          if (edge && c > lim) v = -INFINITY;
-          x[c] = v;
         }
       }
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < BN; c += 2) mx = fmax3(mx, x[c], x[c + 1]);
+      for (int c32 = 0; c32 < BN / 32; ++c32)
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          mx = fmax3(mx, __uint_as_float(sr[c32][e]), __uint_as_float(sr[c32][e + 1]));
       // row maximum in base-2 units
       const float m_tile = HAS_MASK ? mx : mx * c2;
       const float m_new = fmaxf(m_used, m_tile);
@@ -352,14 +358,14 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
       // p = exp2(x - m_used) on pairs, packed to bf16 in place of S, 32 columns at a time
       const uint64_t negm = f2_pack(-m_used, -m_used);
       const uint64_t c2v = f2_pack(c2, c2);
-      uint64_t acc = f2_pack(0.0f, 0.0f);
+      float rs0 = 0.0f, rs1 = 0.0f;
 #pragma unroll
       for (int c32 = 0; c32 < BN / 32; ++c32) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int c = c32 * 32 + 2 * e;
-          const uint64_t xv = f2_pack(x[c], x[c + 1]);
+          const uint64_t xv = f2_pack(__uint_as_float(sr[c32][2 * e]),
+                                      __uint_as_float(sr[c32][2 * e + 1]));
           const uint64_t sv = HAS_MASK ? f2_add(xv, negm) : f2_fma(xv, c2v, negm);
           float s0, s1;
           f2_unpack(sv, s0, s1);
@@ -371,13 +377,12 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
             p0 = ex2(s0);
             p1 = ex2(s1);
           }
-          acc = f2_add(acc, f2_pack(p0, p1));
+          rs0 += p0;
+          rs1 += p1;
           pk[e] = pack_bf16(p0, p1);
         }
         tmem_st16(s_addr + c32 * 16, pk);
       }
-      float rs0, rs1;
-      f2_unpack(acc, rs0, rs1);
       const float rs = rs0 + rs1;
       l += rs;
       tmem_wait_st();
