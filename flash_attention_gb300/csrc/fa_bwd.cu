@@ -95,10 +95,10 @@ struct BwdLayout {
   static constexpr int TMEM_USED = COL_DK + DH;
   static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
   static constexpr int DQ_COLS = T::DQT ? BM : HD;
-  // WG0 (warps 0-3): P^T and the dQ drain; WG1 (warps 4-7): dS^T and the dK/dV epilogue;
-  // warp 8: TMA; warp 9: MMA; warp 10: issues the bulk dQ reductions; warp 11: idle.
-  static constexpr int THREADS = 384;
-  static constexpr int TMA_WARP = 8, MMA_WARP = 9, BULK_WARP = 10;
+  // WG0 (warps 0-3): P^T; WG1 (warps 4-7): dS^T and the dK/dV epilogue; WG2 (warps 8-11):
+  // the dQ drain; warp 12: TMA; warp 13: MMA; warp 14: issues the bulk dQ reductions.
+  static constexpr int THREADS = 512;
+  static constexpr int TMA_WARP = 12, MMA_WARP = 13, BULK_WARP = 14;
   static_assert(TMEM_USED <= 512, "TMEM budget");
   static_assert(DQ_COLS <= BM, "dQ tile must fit in a dP^T buffer");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   __shared__ uint64_t kv_full, qdo_full[ST], qdo_empty[ST];
-  __shared__ uint64_t s_full[NSB], p_ready[NSB];
+  __shared__ uint64_t s_full[NSB], p_ready[NSB], p_consumed[NSB];
   __shared__ uint64_t dp_full[2], ds_ready[2], dq_full[2], dq_free[2];
   __shared__ uint64_t acc_full, mma_drain;
   __shared__ uint64_t stg_full, stg_free;  // dQ staging handshake of the bulk drain
@@ -247,6 +247,7 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
     for (int s = 0; s < NSB; ++s) {
       mbar_init(&s_full[s], 1);
       mbar_init(&p_ready[s], 128);
+      mbar_init(&p_consumed[s], 128);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&dp_full[s], 1);
@@ -311,6 +312,9 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
     // ------------------------------------------------------------------ MMA issuer
     if (elect_one()) {
       const uint32_t sK = smem_u32(smem + LY::OFF_K), sV = smem_u32(smem + LY::OFF_V);
+      const Desc kd = make_desc(sK, 16, 1024);          // K as a K-major operand
+      const Desc vd = make_desc(sV, 16, 1024);          // V as a K-major operand
+      const Desc kmn = make_desc(sK, kBN * 128, 1024);  // K as an MN-major operand
       const uint32_t id_s = idesc_bf16(128, BM, 0, 0);      // S^T, dP^T: [kv x q]
       const uint32_t id_acc = idesc_bf16(128, DH, 0, 1);    // dV, dK: A tmem, B MN-major
       const uint32_t id_dq = T::DQT ? idesc_bf16(DH, BM, 1, 1) : idesc_bf16(BM, HD, 1, 1);
@@ -330,14 +334,13 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
       auto issue_s = [&](int it) {  // S^T(it) = K Q^T
         stage_ready(it);
         if (!ok) return;
-        const uint32_t sQ = smem_u32(smem + LY::OFF_Q + (it % ST) * LY::QT_BYTES);
+        const Desc qd = make_desc(smem_u32(smem + LY::OFF_Q + (it % ST) * LY::QT_BYTES), 16, 1024);
         const uint32_t tS = tbase + LY::COL_S0 + (it % NSB) * BM;
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks) {
           const uint32_t ko = (ks / 4) * (kBN * 128) + (ks % 4) * 32;
           const uint32_t qo = (ks / 4) * (BM * 128) + (ks % 4) * 32;
-          mma_ss(tS, smem_desc(sK + ko, 16, 1024), smem_desc(sQ + qo, 16, 1024), id_s,
-                 ks > 0 ? 1u : 0u);
+          mma_ss2(tS, kd.at(ko), kd.hi, qd.at(qo), qd.hi, id_s, ks > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[it % NSB]);
       };
@@ -348,14 +351,13 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
           tc_fence_after();
         }
         if (!ok) return;
-        const uint32_t sDO = smem_u32(smem + LY::OFF_DO + (it % ST) * LY::QT_BYTES);
+        const Desc dod = make_desc(smem_u32(smem + LY::OFF_DO + (it % ST) * LY::QT_BYTES), 16, 1024);
         const uint32_t tDP = tbase + LY::COL_DP0 + (it % 2) * BM;
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks) {
           const uint32_t ko = (ks / 4) * (kBN * 128) + (ks % 4) * 32;
           const uint32_t qo = (ks / 4) * (BM * 128) + (ks % 4) * 32;
-          mma_ss(tDP, smem_desc(sV + ko, 16, 1024), smem_desc(sDO + qo, 16, 1024), id_s,
-                 ks > 0 ? 1u : 0u);
+          mma_ss2(tDP, vd.at(ko), vd.hi, dod.at(qo), dod.hi, id_s, ks > 0 ? 1u : 0u);
         }
         mma_commit(&dp_full[it % 2]);
       };
@@ -367,22 +369,31 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
       }
       for (int it = 0; it < n_iter && ok; ++it) {
         const int st = it % ST;
-        const uint32_t sQ = smem_u32(smem + LY::OFF_Q + st * LY::QT_BYTES);
-        const uint32_t sDO = smem_u32(smem + LY::OFF_DO + st * LY::QT_BYTES);
+        const Desc qmn = make_desc(smem_u32(smem + LY::OFF_Q + st * LY::QT_BYTES), BM * 128, 1024);
+        const Desc domn = make_desc(smem_u32(smem + LY::OFF_DO + st * LY::QT_BYTES), BM * 128, 1024);
         const uint32_t tS = tbase + LY::COL_S0 + (it % NSB) * BM;
         const uint32_t tDP = tbase + LY::COL_DP0 + (it % 2) * BM;
-        const uint32_t sDS = smem_u32(smem + LY::OFF_DS + (it % 2) * LY::DS_BYTES);
+        const Desc dsd = make_desc(smem_u32(smem + LY::OFF_DS + (it % 2) * LY::DS_BYTES), kBN * 128, 1024);
         // dV += P^T dO
         ok = mbar_wait(&p_ready[it % NSB], (it / NSB) & 1, &abort_flag);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < BM / 16; ++ks)
-          mma_ts(tDV, tS + ks * 8, smem_desc(sDO + slice + ks * 2048, BM * 128, 1024), id_acc,
-                 (it > 0 || ks > 0) ? 1u : 0u);
+          mma_ts2(tDV, tS + ks * 8, domn.at(slice + ks * 2048), domn.hi, id_acc,
+                  (it > 0 || ks > 0) ? 1u : 0u);
         if constexpr (T::LOOKAHEAD) {
           if (it + 1 < n_iter) {
             issue_dp(it + 1);
+            if (!ok) break;
+          }
+          // the next S^T into this tile's score buffer, as soon as the dS warpgroup has read
+          // P^T(it) from it (dV(it), issued above, reads it first: same-thread MMAs run in order)
+          if (it + NSB < n_iter) {
+            ok = mbar_wait(&p_consumed[it % NSB], (it / NSB) & 1, &abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(it + NSB);
             if (!ok) break;
           }
         }
@@ -392,17 +403,9 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < BM / 16; ++ks)
-          mma_ts(tDK, tDP + ks * 8, smem_desc(sQ + slice + ks * 2048, BM * 128, 1024), id_acc,
-                 (it > 0 || ks > 0) ? 1u : 0u);
+          mma_ts2(tDK, tDP + ks * 8, qmn.at(slice + ks * 2048), qmn.hi, id_acc,
+                  (it > 0 || ks > 0) ? 1u : 0u);
         mma_commit(&qdo_empty[st]);
-        if constexpr (T::LOOKAHEAD && NSB == 1) {
-          // one score buffer: S^T(it+1) overwrites P^T(it), which dV(it) and the dS warpgroup
-          // read; dK(it) was issued after that warpgroup signalled ds_ready(it)
-          if (it + 1 < n_iter) {
-            issue_s(it + 1);
-            if (!ok) break;
-          }
-        }
         if constexpr (!T::LOOKAHEAD) {
           if (it + 1 < n_iter) {
             issue_s(it + 1);
@@ -416,19 +419,16 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
           const uint32_t kslice = (dh * DH / 64) * (kBN * 128);
 #pragma unroll
           for (int ks = 0; ks < kBN / 16; ++ks)
-            mma_ss(tDP, smem_desc(sK + kslice + ks * 2048, kBN * 128, 1024),
-                   smem_desc(sDS + ks * 2048, kBN * 128, 1024), id_dq, ks > 0 ? 1u : 0u);
+            mma_ss2(tDP, kmn.at(kslice + ks * 2048), kmn.hi, dsd.at(ks * 2048), dsd.hi, id_dq,
+                    ks > 0 ? 1u : 0u);
         } else {
           // dQ[q, d] = sum_kv dS^T[kv, q] K[kv, d]: A = dS^T (MN-major), B = K (MN-major)
 #pragma unroll
           for (int ks = 0; ks < kBN / 16; ++ks)
-            mma_ss(tDP, smem_desc(sDS + ks * 2048, kBN * 128, 1024),
-                   smem_desc(sK + ks * 2048, kBN * 128, 1024), id_dq, ks > 0 ? 1u : 0u);
+            mma_ss2(tDP, dsd.at(ks * 2048), dsd.hi, kmn.at(ks * 2048), kmn.hi, id_dq,
+                    ks > 0 ? 1u : 0u);
         }
         mma_commit(&dq_full[it % 2]);
-        if constexpr (T::LOOKAHEAD && NSB == 2) {
-          if (it + 2 < n_iter) issue_s(it + 2);  // its buffer held P^T(it), read by dV(it)
-        }
       }
       mma_commit(&acc_full);
       mma_commit(&mma_drain);
@@ -461,70 +461,6 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
     const float c2 = p.scale_log2;
     const uint64_t c2v = f2_pack(c2, c2);
     bool ok = true;
-
-    // dQ of iteration `it` into the f32 accumulator
-    auto drain = [&](int it) {
-      const int h = kh * G + it / nm;
-      const int q0 = (m_first + it % nm) * BM;
-      const int bh = b * p.H + h;
-      const uint32_t colDQ = LY::COL_DP0 + (it % 2) * BM;
-      ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[it % 2], (it / 2) & 1, &abort_flag));
-      if (!ok) return;
-      tc_fence_after();
-      if constexpr (T::DQ_BULK) {
-        // lane = head-dim index, column = query row: stage as [q][d] f32 (contiguous in the
-        // accumulator); the bulk warp adds the tile with one reduction. The staging buffer is
-        // handed over with mbarriers: stg_full once written, stg_free once read.
-        float* stg = reinterpret_cast<float*>(smem + LY::OFF_STG);
-        uint32_t rq[BM / 32][32];
-#pragma unroll
-        for (int c32 = 0; c32 < BM / 32; ++c32) tmem_ld32(lane_base + colDQ + c32 * 32, rq[c32]);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&dq_free[it % 2]);
-        if (it > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&stg_free, (it - 1) & 1, &abort_flag));
-          if (!ok) return;
-        }
-#pragma unroll
-        for (int c32 = 0; c32 < BM / 32; ++c32)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) stg[(c32 * 32 + e) * HD + j] = __uint_as_float(rq[c32][e]);
-        fence_proxy_async();  // staging writes -> visible to the bulk copy
-        mbar_arrive(&stg_full);
-      } else if constexpr (T::DQT) {
-        // lane = head-dim index within the slice, column = query row
-        float* dst = p.dqacc + ((size_t)bh * p.ql_pad + q0) * HD + dh * DH + j;
-        uint32_t rq[BM / 32][32];
-#pragma unroll
-        for (int c32 = 0; c32 < BM / 32; ++c32) tmem_ld32(lane_base + colDQ + c32 * 32, rq[c32]);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&dq_free[it % 2]);
-#pragma unroll
-        for (int c32 = 0; c32 < BM / 32; ++c32)
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            atomicAdd(dst + (size_t)(c32 * 32 + e) * HD, __uint_as_float(rq[c32][e]));
-      } else {
-        // lane = query row, column = head-dim index
-        float4* dst = reinterpret_cast<float4*>(p.dqacc + ((size_t)bh * p.ql_pad + q0 + j) * HD);
-        uint32_t rq[HD / 32][32];
-#pragma unroll
-        for (int c32 = 0; c32 < HD / 32; ++c32) tmem_ld32(lane_base + colDQ + c32 * 32, rq[c32]);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&dq_free[it % 2]);
-#pragma unroll
-        for (int c32 = 0; c32 < HD / 32; ++c32)
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            atomicAdd(dst + c32 * 8 + e,
-                      make_float4(__uint_as_float(rq[c32][4 * e]), __uint_as_float(rq[c32][4 * e + 1]),
-                                  __uint_as_float(rq[c32][4 * e + 2]),
-                                  __uint_as_float(rq[c32][4 * e + 3])));
-      }
-    };
 
     for (int it = 0; it < n_iter && ok; ++it) {
       const int st = it % ST;
@@ -598,10 +534,77 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&p_ready[it % NSB]);
-      // dQ of the previous tile (its MMA followed that tile's dK)
-      if (it > 0) drain(it - 1);
     }
-    if (ok && n_iter > 0) drain(n_iter - 1);
+  } else if (warp >= 8 && warp < 12) {
+    // ------------------------------------------------------------------ WG2: dQ drain
+    const int j = (warp - 8) * 32 + lane;  // TMEM lane (head-dim row of dQ^T, or query row)
+    const uint32_t lane_base = tbase + ((uint32_t)((warp - 8) * 32) << 16);
+    bool ok = true;
+    // dQ of iteration `it` into the f32 accumulator (its MMA followed that tile's dK)
+    auto drain = [&](int it) {
+      const int h = kh * G + it / nm;
+      const int q0 = (m_first + it % nm) * BM;
+      const int bh = b * p.H + h;
+      const uint32_t colDQ = LY::COL_DP0 + (it % 2) * BM;
+      ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[it % 2], (it / 2) & 1, &abort_flag));
+      if (!ok) return;
+      tc_fence_after();
+      if constexpr (T::DQ_BULK) {
+        // lane = head-dim index, column = query row: stage as [q][d] f32 (contiguous in the
+        // accumulator); the bulk warp adds the tile with one reduction. The staging buffer is
+        // handed over with mbarriers: stg_full once written, stg_free once read.
+        float* stg = reinterpret_cast<float*>(smem + LY::OFF_STG);
+        uint32_t rq[BM / 32][32];
+#pragma unroll
+        for (int c32 = 0; c32 < BM / 32; ++c32) tmem_ld32(lane_base + colDQ + c32 * 32, rq[c32]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&dq_free[it % 2]);
+        if (it > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&stg_free, (it - 1) & 1, &abort_flag));
+          if (!ok) return;
+        }
+#pragma unroll
+        for (int c32 = 0; c32 < BM / 32; ++c32)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) stg[(c32 * 32 + e) * HD + j] = __uint_as_float(rq[c32][e]);
+        fence_proxy_async();  // staging writes -> visible to the bulk copy
+        mbar_arrive(&stg_full);
+      } else if constexpr (T::DQT) {
+        // lane = head-dim index within the slice, column = query row
+        float* dst = p.dqacc + ((size_t)bh * p.ql_pad + q0) * HD + dh * DH + j;
+        uint32_t rq[BM / 32][32];
+#pragma unroll
+        for (int c32 = 0; c32 < BM / 32; ++c32) tmem_ld32(lane_base + colDQ + c32 * 32, rq[c32]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&dq_free[it % 2]);
+#pragma unroll
+        for (int c32 = 0; c32 < BM / 32; ++c32)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            atomicAdd(dst + (size_t)(c32 * 32 + e) * HD, __uint_as_float(rq[c32][e]));
+      } else {
+        // lane = query row, column = head-dim index
+        float4* dst = reinterpret_cast<float4*>(p.dqacc + ((size_t)bh * p.ql_pad + q0 + j) * HD);
+        uint32_t rq[HD / 32][32];
+#pragma unroll
+        for (int c32 = 0; c32 < HD / 32; ++c32) tmem_ld32(lane_base + colDQ + c32 * 32, rq[c32]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&dq_free[it % 2]);
+#pragma unroll
+        for (int c32 = 0; c32 < HD / 32; ++c32)
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            atomicAdd(dst + c32 * 8 + e,
+                      make_float4(__uint_as_float(rq[c32][4 * e]), __uint_as_float(rq[c32][4 * e + 1]),
+                                  __uint_as_float(rq[c32][4 * e + 2]),
+                                  __uint_as_float(rq[c32][4 * e + 3])));
+      }
+    };
+
+    for (int it = 0; it < n_iter && ok; ++it) drain(it);
   } else if (warp < 8) {
     // ------------------------------------------------------------------ WG1: dS^T, epilogue
     const int wl = warp - 4;
@@ -615,10 +618,9 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
       const uint32_t colS = LY::COL_S0 + (it % NSB) * BM;
       const uint32_t colDP = LY::COL_DP0 + (it % 2) * BM;
       ok = __all_sync(0xffffffffu, mbar_wait(&dp_full[it % 2], (it / 2) & 1, &abort_flag));
+      // (p_ready also makes the stage's D rows visible: the P warpgroup observed the Q/dO stage
+      // barrier before it arrived on p_ready)
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&p_ready[it % NSB], (it / NSB) & 1, &abort_flag));
-      // the stage's D rows came with the Q/dO copies (that phase cannot have moved on: its
-      // next one needs this tile's dK MMA)
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&qdo_full[st], (it / ST) & 1, &abort_flag));
       // the dQ MMA of tile it-2 must be done reading this dS^T buffer
       if (ok && it >= 2)
         ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[it % 2], ((it - 2) / 2) & 1, &abort_flag));
@@ -639,6 +641,10 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
           tmem_ld16(lane_base + colS + g0 * 16, *reinterpret_cast<uint32_t(*)[16]>(rp));
         }
         tmem_wait_ld();
+        if (g0 + GRP >= BM / 32) {  // every column of P^T(it) is in registers: free its buffer
+          tc_fence_before();
+          mbar_arrive(&p_consumed[it % NSB]);
+        }
 #pragma unroll
         for (int g = 0; g < GRP; ++g) {
           const int c32 = g0 + g;

@@ -303,6 +303,40 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
+// A descriptor split into its two 32-bit words. The start address lives in the low 14 bits
+// (address >> 4, at most 227 KB / 16 < 2^14), so moving the operand by `bytes` within shared
+// memory is one 32-bit add on the low word: at(bytes).
+struct Desc {
+  uint32_t lo, hi;
+  __device__ __forceinline__ uint32_t at(uint32_t bytes) const { return lo + (bytes >> 4); }
+};
+__device__ __forceinline__ Desc make_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  const uint64_t d = smem_desc(saddr, lbo, sbo);
+  return Desc{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
+}
+
+// D(tmem) (+)= A(smem) * B(smem), descriptors given as (low word, high word) pairs
+__device__ __forceinline__ void mma_ss2(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                        uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 ad, bd;\n setp.ne.b32 p, %6, 0;\n"
+      " mov.b64 ad, {%1, %2};\n mov.b64 bd, {%3, %4};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D(tmem) (+)= A(tmem) * B(smem)
+__device__ __forceinline__ void mma_ts2(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                        uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 bd;\n setp.ne.b32 p, %5, 0;\n"
+      " mov.b64 bd, {%2, %3};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D(tmem) (+)= A(smem) * B(smem)
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                        uint32_t idesc, uint32_t accumulate) {

@@ -221,14 +221,12 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
           tc_fence_after();
         }
         const uint32_t d_tmem = tbase + t * LY::TILE_COLS + HD + (j % NS) * BN;
-        const uint32_t qa = sq + t * LY::Q_TILE_BYTES;
-        const uint32_t kb = sk + st * LY::KV_TILE_BYTES;
+        const Desc qa = make_desc(sq + t * LY::Q_TILE_BYTES, 16, 1024);
+        const Desc kb = make_desc(sk + st * LY::KV_TILE_BYTES, 16, 1024);
 #pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks) {
-          const uint64_t ad = smem_desc(qa + (ks / 4) * (kBM * 128) + (ks % 4) * 32, 16, 1024);
-          const uint64_t bd = smem_desc(kb + (ks / 4) * (BN * 128) + (ks % 4) * 32, 16, 1024);
-          mma_ss(d_tmem, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
-        }
+        for (int ks = 0; ks < HD / 16; ++ks)
+          mma_ss2(d_tmem, qa.at((ks / 4) * (kBM * 128) + (ks % 4) * 32), qa.hi,
+                  kb.at((ks / 4) * (BN * 128) + (ks % 4) * 32), kb.hi, idesc_s, ks > 0 ? 1u : 0u);
         mma_commit(&s_full[t][j % NS]);
         if (t == NQ - 1) mma_commit(&k_empty[st]);
       };
@@ -253,12 +251,11 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
           tc_fence_after();
           const uint32_t o_tmem = tbase + t * LY::TILE_COLS;
           const uint32_t p_tmem = o_tmem + HD + sb * BN;
-          const uint32_t vb = sv + st * LY::KV_TILE_BYTES;
+          const Desc vb = make_desc(sv + st * LY::KV_TILE_BYTES, BN * 128, 1024);
 #pragma unroll
-          for (int ks = 0; ks < BN / 16; ++ks) {
-            const uint64_t bd = smem_desc(vb + ks * 2048, BN * 128, 1024);
-            mma_ts(o_tmem, p_tmem + ks * 8, bd, idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
-          }
+          for (int ks = 0; ks < BN / 16; ++ks)
+            mma_ts2(o_tmem, p_tmem + ks * 8, vb.at(ks * 2048), vb.hi, idesc_o,
+                    (j > 0 || ks > 0) ? 1u : 0u);
           mma_commit(&o_done[t]);
           if (j == nt[t] - 1) mma_commit(&o_final[t]);  // every PV of tile t issued
           if (t == NQ - 1) mma_commit(&v_empty[st]);
