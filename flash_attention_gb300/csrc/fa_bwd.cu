@@ -120,7 +120,11 @@ struct BwdKParams {
 };
 
 // ------------------------------------------------------------------------ prep kernel
-// One warp per (bh, row < ql_pad).
+// D_i = <dO_i, O_i>, -L_i * log2(e) (-inf for padding rows and rows with L = -inf), and the
+// dQ accumulator zeroed. Grid: x = chunk of RPB*ROWS rows within a head, y = head (strided).
+// A group of HD/8 threads owns one row (16-byte loads of O and dO); each thread walks ROWS
+// rows so that many loads are in flight; the chunk's accumulator rows are then zeroed with
+// coalesced float4 stores.
 template <int HD>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
                                                        const __nv_bfloat16* __restrict__ dO,
@@ -129,66 +133,71 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
                                                        float* __restrict__ dvec,
                                                        float* __restrict__ dqacc, int BH, int ql,
                                                        int ql_pad) {
-  const int lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (row >= (long long)BH * ql_pad) return;
-  const int bh = (int)(row / ql_pad), i = (int)(row % ql_pad);
-  constexpr int PER = HD / 32;  // elements per lane
-  float acc = 0.0f;
-  if (i < ql) {
-    const size_t base = ((size_t)bh * ql + i) * HD + lane * PER;
-    if constexpr (PER == 2) {
-      __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + base);
-      __nv_bfloat162 g = *reinterpret_cast<const __nv_bfloat162*>(dO + base);
-      acc = __low2float(a) * __low2float(g) + __high2float(a) * __high2float(g);
-    } else {
-      constexpr int NV = PER / 4;  // uint2 (4 bf16) chunks
+  constexpr int TPR = HD / 8;            // threads per row (8 bf16 = 16 bytes each)
+  constexpr int RPB = 256 / TPR;         // rows per pass of the block
+  constexpr int ROWS = 4;                // passes per block
+  const int sub = threadIdx.x % TPR;
+  const int i0 = blockIdx.x * RPB * ROWS;  // first row of the chunk (ql_pad is a multiple)
+  for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
+    uint4 a[ROWS], g[ROWS];
 #pragma unroll
-      for (int u = 0; u < NV; ++u) {
-        uint2 a = *reinterpret_cast<const uint2*>(o + base + 4 * u);
-        uint2 g = *reinterpret_cast<const uint2*>(dO + base + 4 * u);
-        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-        const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-          acc += __low2float(a2[e]) * __low2float(g2[e]) + __high2float(a2[e]) * __high2float(g2[e]);
+    for (int r = 0; r < ROWS; ++r) {
+      const int i = i0 + r * RPB + threadIdx.x / TPR;
+      a[r] = make_uint4(0, 0, 0, 0);
+      g[r] = make_uint4(0, 0, 0, 0);
+      if (i < ql) {
+        const size_t base = ((size_t)bh * ql + i) * HD + sub * 8;
+        a[r] = *reinterpret_cast<const uint4*>(o + base);
+        g[r] = *reinterpret_cast<const uint4*>(dO + base);
       }
     }
-  }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
-    float nl2 = -INFINITY;  // padding rows and fully masked rows: P = exp2(s - inf) = 0
-    if (i < ql) {
-      const float L = lse[(size_t)bh * ql + i];
-      if (L != -INFINITY) nl2 = -L * kLog2eB;
+    for (int r = 0; r < ROWS; ++r) {
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[r]);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g[r]);
+      float acc = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        acc += __low2float(a2[e]) * __low2float(g2[e]) + __high2float(a2[e]) * __high2float(g2[e]);
+#pragma unroll
+      for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      const int i = i0 + r * RPB + threadIdx.x / TPR;
+      if (sub == 0) {
+        float nl2 = -INFINITY;  // padding rows and fully masked rows: P = exp2(s - inf) = 0
+        if (i < ql) {
+          const float L = lse[(size_t)bh * ql + i];
+          if (L != -INFINITY) nl2 = -L * kLog2eB;
+        }
+        lse2[(size_t)bh * ql_pad + i] = nl2;
+        dvec[(size_t)bh * ql_pad + i] = i < ql ? acc : 0.0f;
+      }
     }
-    lse2[(size_t)bh * ql_pad + i] = nl2;
-    dvec[(size_t)bh * ql_pad + i] = acc;
+    float4* z = reinterpret_cast<float4*>(dqacc + ((size_t)bh * ql_pad + i0) * HD);
+#pragma unroll 4
+    for (int c = threadIdx.x; c < RPB * ROWS * HD / 4; c += 256) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  float4* z = reinterpret_cast<float4*>(dqacc + ((size_t)bh * ql_pad + i) * HD);
-#pragma unroll
-  for (int c = lane; c < HD / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ------------------------------------------------------------------------ dQ convert
+// dQ = bf16(scale * accumulator). Grid: x = chunk of 256 groups of 8 values within a head,
+// y = head (strided). Each thread converts 8 consecutive values (two float4 loads, one 16-byte
+// store).
 template <int HD>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ dqacc,
                                                      __nv_bfloat16* __restrict__ dq, int BH,
                                                      int ql, int ql_pad, float scale) {
-  const long long n4 = (long long)BH * ql * HD / 4;
-  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n4;
-       e += (long long)gridDim.x * blockDim.x) {
-    const long long flat = e * 4;
-    const long long row = flat / HD;
-    const int c = (int)(flat % HD);
-    const int bh = (int)(row / ql), i = (int)(row % ql);
-    const float4 v =
-        *reinterpret_cast<const float4*>(dqacc + ((size_t)bh * ql_pad + i) * HD + c);
-    uint2 out;
-    out.x = pack_bf16(v.x * scale, v.y * scale);
-    out.y = pack_bf16(v.z * scale, v.w * scale);
-    *reinterpret_cast<uint2*>(dq + flat) = out;
+  const int e = blockIdx.x * 256 + threadIdx.x;  // index of the 8-value group within a head
+  const int i = e / (HD / 8), c = (e % (HD / 8)) * 8;
+  if (i >= ql) return;
+  for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
+    const float4* src = reinterpret_cast<const float4*>(dqacc + ((size_t)bh * ql_pad + i) * HD + c);
+    const float4 v0 = src[0], v1 = src[1];
+    uint4 out;
+    out.x = pack_bf16(v0.x * scale, v0.y * scale);
+    out.y = pack_bf16(v0.z * scale, v0.w * scale);
+    out.z = pack_bf16(v1.x * scale, v1.y * scale);
+    out.w = pack_bf16(v1.z * scale, v1.w * scale);
+    *reinterpret_cast<uint4*>(dq + ((size_t)bh * ql + i) * HD + c) = out;
   }
 }
 
@@ -788,9 +797,10 @@ template <int HD>
 static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t s) {
   const int BH = a.B * a.H;
   {
-    const long long rows = (long long)BH * a.ql_pad;
+    constexpr int rows_per_block = (256 / (HD / 8)) * 4;  // divides 128, hence ql_pad
+    dim3 grid(a.ql_pad / rows_per_block, BH < 65535 ? BH : 65535);
     profile_mark(kKernBwdPrep, 0, s);
-    bwd_prep_kernel<HD><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
+    bwd_prep_kernel<HD><<<grid, 256, 0, s>>>(
         reinterpret_cast<const __nv_bfloat16*>(a.o), reinterpret_cast<const __nv_bfloat16*>(a.dO),
         a.lse, a.lse2, a.dvec, a.dqacc, BH, a.ql, a.ql_pad);
     cudaError_t e = cudaGetLastError();
@@ -805,12 +815,11 @@ static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t
   }
   if (e != cudaSuccess) return e;
   {
-    const long long n4 = (long long)BH * a.ql * HD / 4;
-    long long blocks = (n4 + 255) / 256;
-    if (blocks > 152 * 32) blocks = 152 * 32;
+    const long long groups = (long long)a.ql * (HD / 8);  // 8-value groups per head
+    dim3 grid((unsigned)((groups + 255) / 256), BH < 65535 ? BH : 65535);
     profile_mark(kKernBwdDq, 0, s);
-    bwd_dq_kernel<HD><<<(unsigned)blocks, 256, 0, s>>>(
-        a.dqacc, reinterpret_cast<__nv_bfloat16*>(a.dq), BH, a.ql, a.ql_pad, a.scale);
+    bwd_dq_kernel<HD><<<grid, 256, 0, s>>>(a.dqacc, reinterpret_cast<__nv_bfloat16*>(a.dq), BH,
+                                           a.ql, a.ql_pad, a.scale);
     profile_mark(kKernBwdDq, 1, s);
   }
   return cudaGetLastError();
