@@ -40,6 +40,7 @@ MUTATIONS = {
     "causal_off_by_one": 10,
     "dq_no_scale": 11,
     "d_from_do_only": 12,
+    "window_off_by_one": 13,
 }
 
 
@@ -73,6 +74,7 @@ def _load():
                                                   f, i, f, f, i]
             lib.fa_oracle_bwd.argtypes = [f, f, f, f, f, i, i, i, i, i, i, d, i, f, f, f, i]
             lib.fa_oracle_set_mutation.argtypes = [i]
+            lib.fa_oracle_set_window.argtypes = [i, i]
             lib.fa_oracle_get_mutation.restype = i
             for fn in (lib.fa_oracle_fwd_rows, lib.fa_oracle_bwd_q_rows,
                        lib.fa_oracle_bwd_kv_rows, lib.fa_oracle_bwd):
@@ -102,6 +104,36 @@ def _shape(q, k):
     if H % Hk:
         raise ValueError("n_heads must be a multiple of n_kv_heads")
     return B, H, Hk, ql, kl, d
+
+
+class window:
+    """Context manager: local attention window (left, right) for the oracle calls inside it;
+    -1 leaves a side unbounded. Key j is hidden when j < q_abs - left or j > q_abs + right,
+    with q_abs = kl - ql + i."""
+
+    def __init__(self, left=-1, right=-1):
+        self.left, self.right = int(left), int(right)
+
+    def __enter__(self):
+        _load().fa_oracle_set_window(self.left, self.right)
+        return self
+
+    def __exit__(self, *exc):
+        _load().fa_oracle_set_window(-1, -1)
+        return False
+
+
+def dense_mask(mask, shape):
+    """Any mask form the CUDA path accepts, as the oracle's dense f32 additive mask [B,H,ql,kl]:
+    bool masks (True = visible) become 0 / -inf, bf16 and f32 masks their f32 values, and
+    broadcast shapes ([ql,kl], [1,H,ql,kl], [B,1,ql,kl], ...) are expanded."""
+    if mask is None:
+        return None
+    m = np.asarray(mask)
+    if m.dtype == np.bool_ or m.dtype == np.uint8:
+        m = np.where(m != 0, np.float32(0.0), np.float32(-np.inf))
+    m = np.broadcast_to(m.astype(np.float32), shape)
+    return np.ascontiguousarray(m)
 
 
 def set_mutation(name_or_code) -> None:

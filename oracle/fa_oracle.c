@@ -35,6 +35,11 @@
  *     corner is unpinned by the pages because the two disagree);
  *   - the mask is natural-log additive, shape [B, H, ql, kl], an entry -inf hides the key.
  *
+ * Local (sliding-window) attention, the windowed form of the mlx-native SWA tests (sections 7
+ * and 15, which build it as an additive mask): with window_left = wl >= 0 a key j is hidden
+ * when j < q_abs - wl, with window_right = wr >= 0 when j > q_abs + wr; -1 leaves that side
+ * unbounded. It composes with causal (which hides j > q_abs) and with the mask.
+ *
  * A second forward mode (base2 = 1) takes the mlx-native forward oracle's own steps: the score
  * is multiplied by scale*log2(e), the mask by log2(e), the row max starts at the finite
  * sentinel -FLT_MAX/2, p = exp2(s - max), L = max*ln(2) + ln(sum p), O = sum (p / safe_sum) v
@@ -58,6 +63,7 @@ typedef struct {
   int B, H, Hk, ql, kl, d;
   double scale;
   int causal;
+  int wl, wr; /* local window around q_abs = kl - ql + i: -1 = unbounded on that side */
   const float *q, *k, *v, *mask, *dO;
 } prob_t;
 
@@ -76,6 +82,7 @@ enum {
   MUT_CAUSAL_OFF_BY_ONE = 10, /* visible iff j < kl - ql + i */
   MUT_DQ_NO_SCALE = 11,    /* dQ without the scale factor */
   MUT_D_FROM_DO_ONLY = 12, /* D_i = sum dO (O dropped) */
+  MUT_WINDOW_OFF_BY_ONE = 13, /* left window bound one key too narrow */
 };
 static int g_mutation = 0;
 
@@ -93,11 +100,14 @@ static inline int kv_head(const prob_t *p, int h) {
   return h / (p->H / p->Hk);
 }
 static inline int visible(const prob_t *p, int i, int j) {
-  if (!p->causal) return 1;
   long off = (long)p->kl - (long)p->ql;
   if (g_mutation == MUT_TOP_LEFT) off = 0;
-  if (g_mutation == MUT_CAUSAL_OFF_BY_ONE) return (long)j < off + (long)i;
-  return (long)j <= off + (long)i;
+  const long qa = off + (long)i; /* query position aligned to the end of the keys */
+  if (p->wl >= 0 && (long)j < qa - p->wl + (g_mutation == MUT_WINDOW_OFF_BY_ONE ? 1 : 0)) return 0;
+  if (p->wr >= 0 && (long)j > qa + p->wr) return 0;
+  if (!p->causal) return 1;
+  if (g_mutation == MUT_CAUSAL_OFF_BY_ONE) return (long)j < qa;
+  return (long)j <= qa;
 }
 
 /* Scores of row (b, h, i) into s[kl]: natural-log domain, -inf where hidden. */
@@ -220,12 +230,17 @@ static void parallel_for(long ntasks, int nthreads, void (*fn)(void *, long, int
   pthread_mutex_destroy(&pl.mu);
 }
 
+static int g_wl = -1, g_wr = -1; /* window of the next calls (fa_oracle_set_window) */
+
+void fa_oracle_set_window(int wl, int wr) { g_wl = wl; g_wr = wr; }
+
 static prob_t make_prob(const float *q, const float *k, const float *v, const float *mask,
                         const float *dO, int B, int H, int Hk, int ql, int kl, int d,
                         double scale, int causal) {
   prob_t p;
   p.B = B; p.H = H; p.Hk = Hk; p.ql = ql; p.kl = kl; p.d = d;
   p.scale = scale; p.causal = causal;
+  p.wl = g_wl; p.wr = g_wr;
   p.q = q; p.k = k; p.v = v; p.mask = mask; p.dO = dO;
   return p;
 }

@@ -53,38 +53,48 @@ def _problem(seed, B, H, Hk, ql, kl, d, mask=False, neg_inf_frac=0.0):
     return q, k, v, do, m
 
 
-def _torch_bias(ql, kl, causal, mask, H, B):
-    """Additive f64 bias [B,H,ql,kl] from torch's own lower-right causal bias and the mask."""
+def _torch_bias(ql, kl, causal, mask, H, B, window=None):
+    """Additive f64 bias [B,H,ql,kl] from torch's own lower-right causal bias, a local window
+    band built with torch.tril / torch.triu around the same diagonal, and the mask."""
     bias = torch.zeros(B, H, ql, kl, dtype=torch.float64)
     if causal:
         allowed = causal_lower_right(ql, kl)._materialize(device="cpu")
         bias = bias.masked_fill(~allowed, float("-inf"))
+    if window is not None:
+        wl, wr = window
+        band = torch.ones(ql, kl, dtype=torch.bool)
+        off = kl - ql
+        if wr >= 0:
+            band = band.tril(diagonal=off + wr)
+        if wl >= 0:
+            band = band.triu(diagonal=off - wl)
+        bias = bias.masked_fill(~band, float("-inf"))
     if mask is not None:
         bias = bias + torch.from_numpy(mask).double()
     return bias
 
 
-def _torch_fwd(q, k, v, mask, scale, causal):
+def _torch_fwd(q, k, v, mask, scale, causal, window=None):
     B, H, ql, d = q.shape
     G = H // k.shape[1]
     kt = torch.from_numpy(k).double().repeat_interleave(G, dim=1)
     vt = torch.from_numpy(v).double().repeat_interleave(G, dim=1)
     qt = torch.from_numpy(q).double()
-    bias = _torch_bias(ql, k.shape[2], causal, mask, H, B)
+    bias = _torch_bias(ql, k.shape[2], causal, mask, H, B, window)
     o, lse = torch.ops.aten._scaled_dot_product_flash_attention_for_cpu(
         qt, kt, vt, 0.0, False, attn_mask=bias, scale=scale)
     return o.numpy(), lse.numpy()
 
 
-def _torch_grads(q, k, v, mask, do, scale, causal):
+def _torch_grads(q, k, v, mask, do, scale, causal, window=None):
     B, H, ql, d = q.shape
     qt = torch.from_numpy(q).double().requires_grad_()
     kt = torch.from_numpy(k).double().requires_grad_()
     vt = torch.from_numpy(v).double().requires_grad_()
-    if causal and mask is None:
+    if causal and mask is None and window is None:
         bias = causal_lower_right(ql, k.shape[2])
     else:
-        bias = _torch_bias(ql, k.shape[2], causal, mask, H, B)
+        bias = _torch_bias(ql, k.shape[2], causal, mask, H, B, window)
     with torch.nn.attention.sdpa_kernel(torch.nn.attention.SDPBackend.MATH):
         o = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=bias, scale=scale,
                                            enable_gqa=True)
@@ -332,6 +342,72 @@ def pin_sampled_entry_points_agree():
     return fails
 
 
+# Local-window cases: (B, H, Hk, ql, kl, d, causal, mask, (window_left, window_right))
+WINDOW_CASES = [
+    (1, 2, 1, 9, 9, 4, True, False, (3, -1)),
+    (1, 2, 2, 6, 11, 8, False, False, (2, 1)),
+    (2, 4, 2, 7, 7, 4, True, True, (0, -1)),
+    (1, 2, 1, 5, 12, 4, False, True, (-1, 2)),
+]
+
+
+def pin_window_vs_torch():
+    """The oracle's local window against torch's CPU kernels with a tril/triu band."""
+    fails = []
+    for n, (B, H, Hk, ql, kl, d, causal, mask, win) in enumerate(WINDOW_CASES):
+        q, k, v, do, m = _problem(1000 + n, B, H, Hk, ql, kl, d, mask)
+        scale = 0.43
+        with oracle.window(*win):
+            o, lse = oracle.fwd(q, k, v, m, scale=scale, causal=causal)
+            dq, dk, dv = oracle.bwd(q, k, v, m, do, scale=scale, causal=causal)
+        to, tl = _torch_fwd(q, k, v, m, scale, causal, win)
+        live = np.isfinite(tl)
+        _cmp(f"win{n} O", o[live], to[live], out=fails)
+        _cmp(f"win{n} L", lse, tl, out=fails)
+        if live.all():
+            tq, tk, tv = _torch_grads(q, k, v, m, do, scale, causal, win)
+            _cmp(f"win{n} dQ", dq, tq, out=fails)
+            _cmp(f"win{n} dK", dk, tk, out=fails)
+            _cmp(f"win{n} dV", dv, tv, out=fails)
+    return fails
+
+
+def pin_window_closed_forms():
+    fails = []
+    B, H, Hk, ql, kl, d = 1, 2, 1, 6, 10, 4
+    q, k, v, do, _ = _problem(1100, B, H, Hk, ql, kl, d)
+    off = kl - ql
+    # causal with a zero-width left window: row i sees only key off + i, so O = V[off + i]
+    with oracle.window(0, -1):
+        o, lse = oracle.fwd(q, k, v, None, scale=0.5, causal=True)
+    want = np.broadcast_to(v[:, :, off:off + ql, :], o.shape)
+    _cmp("window 0: O = diagonal V", o, want, tol=0, out=fails)
+    want_l = 0.5 * np.einsum("bhid,bhid->bhi", q.astype(np.float64),
+                             np.broadcast_to(k[:, :, off:off + ql, :], q.shape).astype(np.float64))
+    _cmp("window 0: L = diagonal score", lse, want_l, out=fails)
+    # a window wider than the keys changes nothing
+    o0, l0 = oracle.fwd(q, k, v, None, scale=0.5, causal=True)
+    with oracle.window(kl + 5, kl + 5):
+        o1, l1 = oracle.fwd(q, k, v, None, scale=0.5, causal=True)
+    _cmp("wide window O", o1, o0, tol=0, out=fails)
+    _cmp("wide window L", l1, l0, tol=0, out=fails)
+    # the window equals the same band given as an additive -inf mask (the pages' SWA form)
+    ii = np.arange(ql)[:, None] + off
+    jj = np.arange(kl)[None, :]
+    band = np.where((jj >= ii - 3) & (jj <= ii + 1), 0.0, -np.inf).astype(np.float32)
+    mband = np.broadcast_to(band, (B, H, ql, kl)).copy()
+    with oracle.window(3, 1):
+        ow, lw = oracle.fwd(q, k, v, None, scale=0.5, causal=False)
+        gw = oracle.bwd(q, k, v, None, do, scale=0.5, causal=False)
+    om, lm = oracle.fwd(q, k, v, mband, scale=0.5, causal=False)
+    gm = oracle.bwd(q, k, v, mband, do, scale=0.5, causal=False)
+    _cmp("window = band mask O", ow, om, tol=0, out=fails)
+    _cmp("window = band mask L", lw, lm, tol=0, out=fails)
+    for a, b_, n in zip(gw, gm, ("dQ", "dK", "dV")):
+        _cmp(f"window = band mask {n}", a, b_, tol=1e-15, out=fails)
+    return fails
+
+
 ALL_PINS = [
     pin_fwd_vs_torch_cpu_flash,
     pin_bwd_vs_torch_autograd,
@@ -341,4 +417,6 @@ ALL_PINS = [
     pin_gqa_equals_repeated_mha,
     pin_bwd_invariants,
     pin_base2_mode_agrees,
+    pin_window_vs_torch,
+    pin_window_closed_forms,
 ]
