@@ -186,6 +186,8 @@ def oracle_head_sample(w, inp, heads, nthreads=None):
     fwd_f, bwd_f = w.flops()
     per_head = (fwd_f + bwd_f) / (w.batch * w.n_heads)
     t0 = time.perf_counter()
+    win = oracle.window(w.window_left, w.window_right)
+    win.__enter__()
     for (b, h) in heads:
         kh = h // G
         qs = np.ascontiguousarray(q[b:b + 1, h:h + 1])
@@ -195,6 +197,7 @@ def oracle_head_sample(w, inp, heads, nthreads=None):
         ms = None if inp.mask is None else np.ascontiguousarray(inp.mask[b:b + 1, h:h + 1])
         oracle.fwd(qs, ks, vs, ms, scale=w.scale, causal=w.causal, nthreads=nthreads)
         oracle.bwd(qs, ks, vs, ms, dos, scale=w.scale, causal=w.causal, nthreads=nthreads)
+    win.__exit__(None, None, None)
     dt = time.perf_counter() - t0
     return per_head * len(heads), dt
 
@@ -246,7 +249,10 @@ def config_of(w, n):
     return {"workload": w.name, "batch": w.batch, "n_heads": w.n_heads,
             "n_kv_heads": w.n_kv_heads, "ql": w.ql, "kl": w.kl, "head_dim": w.head_dim,
             "scale": w.scale, "causal": w.causal, "mask": w.masked,
-            "flop_rule": "fwd 4*B*H*ql*kl*d*f, bwd 10*B*H*ql*kl*d*f, f=0.5 causal",
+            **({"window": [w.window_left, w.window_right]} if w.windowed else {}),
+            "flop_rule": "fwd 4*B*H*ql*kl*d*f, bwd 10*B*H*ql*kl*d*f, "
+                         + ("f = visible fraction of (query, key) pairs under the window"
+                            if w.windowed else "f=0.5 causal"),
             "l2": "inputs larger than L2 (no flush): a step touches "
                   f"{step_bytes(w) / 1e6:.0f} MB",
             "parallelism": "replicas" if n == 1 else f"{n} independent replicas"}
@@ -290,11 +296,12 @@ def run_ours(args, w):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     params = fa.FaParams(w.batch, w.n_heads, w.n_kv_heads, w.ql, w.kl, w.head_dim, w.scale,
                          int(w.causal))
+    opts = fa.make_options(q, k, mask, (w.window_left, w.window_right))
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        fa.fa_train_fwd(q, k, v, mask, o, lse, params, stream)
-        fa.fa_train_bwd(q, k, v, o, lse, do, mask, dq, dk, dv, params, stream)
+        fa.fa_train_fwd_ex(q, k, v, mask, o, lse, params, opts, stream)
+        fa.fa_train_bwd_ex(q, k, v, o, lse, do, mask, dq, dk, dv, params, opts, stream)
 
     def barrier():
         if world > 1:
@@ -330,9 +337,9 @@ def run_ours(args, w):
     fa.fa_profile_enable(True)
     for s in range(args.steps):
         ev[s][0].record(stream)
-        fa.fa_train_fwd(q, k, v, mask, o, lse, params, stream)
+        fa.fa_train_fwd_ex(q, k, v, mask, o, lse, params, opts, stream)
         ev[s][1].record(stream)
-        fa.fa_train_bwd(q, k, v, o, lse, do, mask, dq, dk, dv, params, stream)
+        fa.fa_train_bwd_ex(q, k, v, o, lse, do, mask, dq, dk, dv, params, opts, stream)
         ev[s][2].record(stream)
     torch.cuda.synchronize()
     fa.fa_profile_enable(False)

@@ -42,6 +42,14 @@ class Workload:
     causal: bool
     masked: bool = False  # additive f32 mask [batch, n_heads, ql, kl]
     do_std: float = 1.0  # dO ~ N(0, 1) * do_std
+    # local attention window: key j is hidden from row i when j < q_abs - window_left or
+    # j > q_abs + window_right (q_abs = kl - ql + i); -1 leaves that side unbounded
+    window_left: int = -1
+    window_right: int = -1
+
+    @property
+    def windowed(self) -> bool:
+        return self.window_left >= 0 or self.window_right >= 0
 
     @property
     def group(self) -> int:
@@ -60,22 +68,26 @@ class Workload:
         return (self.batch, self.n_heads, self.ql, self.kl)
 
     def visible_pairs(self) -> int:
-        """Number of (query, key) pairs a causal bottom-right mask leaves visible (per b, h)."""
-        if not self.causal:
-            return self.ql * self.kl
-        off = self.kl - self.ql
-        tot = 0
-        for i in range(self.ql):
-            tot += max(0, min(self.kl, off + i + 1))
-        return tot
+        """Number of (query, key) pairs the causal bottom-right mask and the window leave
+        visible (per b, h); the additive mask is not counted."""
+        q_abs = np.arange(self.ql, dtype=np.int64) + (self.kl - self.ql)
+        lo = np.zeros_like(q_abs)
+        hi = np.full_like(q_abs, self.kl - 1)
+        if self.window_left >= 0:
+            lo = np.maximum(lo, q_abs - self.window_left)
+        if self.causal:
+            hi = np.minimum(hi, q_abs)
+        if self.window_right >= 0:
+            hi = np.minimum(hi, q_abs + self.window_right)
+        return int(np.maximum(0, hi - lo + 1).sum())
 
     def flops(self, exact: bool = False):
         """(fwd, bwd) FLOPs: 4*B*H*ql*kl*d*f and 10*B*H*ql*kl*d*f.
 
-        f = 0.5 for causal (the headline counting rule), 1 otherwise; with exact=True f is the
-        visible fraction of (query, key) pairs.
+        f = 0.5 for causal (the headline counting rule), 1 otherwise; with exact=True, or with a
+        window (which has no such rule), f is the visible fraction of (query, key) pairs.
         """
-        if exact:
+        if exact or self.windowed:
             f = self.visible_pairs() / (self.ql * self.kl)
         else:
             f = 0.5 if self.causal else 1.0
@@ -83,13 +95,16 @@ class Workload:
         return 4.0 * base, 10.0 * base
 
 
-# The five workloads, in order (index = workload_index in the seed formula).
+# The workloads, in order (index = workload_index in the seed formula; new ones go last).
 WORKLOADS = [
     Workload("tiny_gqa_d64", 1, 2, 1, 64, 64, 64, 1.0 / 8.0, True),
     Workload("masked_d256", 2, 4, 2, 128, 128, 256, 1.0 / 16.0, False, masked=True),
     Workload("train_d64", 4, 16, 16, 2048, 2048, 64, 1.0 / 8.0, True, do_std=0.1),
     Workload("gqa_d128_4k", 2, 32, 8, 4096, 4096, 128, 1.0 / math.sqrt(128.0), True, do_std=0.1),
     Workload("rect_d256", 1, 16, 4, 1024, 8192, 256, 1.0 / 16.0, True, do_std=0.1),
+    # sliding-window causal attention: every row sees its last 4096 keys (itself included)
+    Workload("swa_d128_16k", 1, 32, 8, 16384, 16384, 128, 1.0 / math.sqrt(128.0), True,
+             do_std=0.1, window_left=4095),
 ]
 BY_NAME = {w.name: w for w in WORKLOADS}
 

@@ -17,7 +17,8 @@ __all__ = [
     "FaParams", "fa_train_fwd", "fa_train_bwd", "fa_device_status", "fa_error_string",
     "fa_version", "fa_profile_enable", "fa_profile_read", "attention_fwd", "attention_bwd", "load_library", "build", "LIB_PATH",
     "FA_OK", "FA_ERR_INVALID", "FA_ERR_CUDA", "FA_ERR_DEVICE_TIMEOUT", "FA_ERR_UNSUPPORTED",
-    "FA_ERR_TOO_LARGE",
+    "FA_ERR_TOO_LARGE", "FaOptions", "fa_train_fwd_ex", "fa_train_bwd_ex", "make_options",
+    "FA_MASK_F32", "FA_MASK_BF16", "FA_MASK_BOOL",
 ]
 
 FA_OK = 0
@@ -26,6 +27,25 @@ FA_ERR_CUDA = 2
 FA_ERR_DEVICE_TIMEOUT = 3
 FA_ERR_UNSUPPORTED = 4
 FA_ERR_TOO_LARGE = 5
+
+
+FA_MASK_F32 = 0
+FA_MASK_BF16 = 1
+FA_MASK_BOOL = 2
+
+
+class FaOptions(ctypes.Structure):
+    """Mirror of `fa_options` in include/fa_train.h."""
+
+    _fields_ = [
+        ("window_left", ctypes.c_int32),
+        ("window_right", ctypes.c_int32),
+        ("mask_type", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("mask_stride_b", ctypes.c_int64),
+        ("mask_stride_h", ctypes.c_int64),
+        ("mask_stride_q", ctypes.c_int64),
+    ]
 
 
 class FaParams(ctypes.Structure):
@@ -72,6 +92,11 @@ def load_library():
             lib.fa_train_fwd.restype = ctypes.c_int
             lib.fa_train_bwd.argtypes = [vp, vp, vp, vp, fp, vp, fp, vp, vp, vp, pp, vp]
             lib.fa_train_bwd.restype = ctypes.c_int
+            po = ctypes.POINTER(FaOptions)
+            lib.fa_train_fwd_ex.argtypes = [vp, vp, vp, vp, vp, fp, pp, po, vp]
+            lib.fa_train_fwd_ex.restype = ctypes.c_int
+            lib.fa_train_bwd_ex.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, vp, pp, po, vp]
+            lib.fa_train_bwd_ex.restype = ctypes.c_int
             lib.fa_device_status.argtypes = [ctypes.c_int]
             lib.fa_device_status.restype = ctypes.c_int
             lib.fa_error_string.argtypes = [ctypes.c_int]
@@ -149,6 +174,61 @@ def fa_train_bwd(q, k, v, o, lse, dO, mask, dq, dk, dv, params: FaParams, stream
         raise FaError(rc, "fa_train_bwd")
 
 
+def make_options(q, k, mask=None, window=(-1, -1)) -> FaOptions:
+    """fa_options for a mask tensor of any supported dtype (float32, bfloat16, bool) whose shape
+    broadcasts to [B, H, ql, kl] with the keys contiguous, and a (left, right) window."""
+    import torch
+
+    B, H, ql, _ = q.shape
+    kl = k.shape[2]
+    wl, wr = window if window is not None else (-1, -1)
+    opt = FaOptions(int(wl), int(wr), FA_MASK_F32, 0, 0, 0, 0)
+    if mask is not None:
+        types = {torch.float32: FA_MASK_F32, torch.bfloat16: FA_MASK_BF16, torch.bool: FA_MASK_BOOL,
+                 torch.uint8: FA_MASK_BOOL}
+        if mask.dtype not in types or not mask.is_cuda:
+            raise ValueError("mask must be a CUDA float32, bfloat16 or bool tensor")
+        e = mask.expand(B, H, ql, kl)
+        sb, sh, sq, sk = e.stride()
+        if kl > 1 and sk != 1:
+            raise ValueError("the mask's key dimension must be contiguous")
+        opt.mask_type = types[mask.dtype]
+        opt.mask_stride_b, opt.mask_stride_h, opt.mask_stride_q = sb, sh, sq
+    return opt
+
+
+def fa_train_fwd_ex(q, k, v, mask, o, lse, params: FaParams, options: FaOptions,
+                    stream=None) -> None:
+    """C call `fa_train_fwd_ex` (window, mask type and broadcast in `options`)."""
+    import torch
+
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _check(t, torch.bfloat16, n)
+    _check(lse, torch.float32, "lse")
+    rc = load_library().fa_train_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(o), _ptr(lse),
+                                        ctypes.byref(params), ctypes.byref(options),
+                                        _stream_handle(stream))
+    if rc:
+        raise FaError(rc, "fa_train_fwd_ex")
+
+
+def fa_train_bwd_ex(q, k, v, o, lse, dO, mask, dq, dk, dv, params: FaParams, options: FaOptions,
+                    stream=None) -> None:
+    """C call `fa_train_bwd_ex`."""
+    import torch
+
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO"), (dq, "dq"), (dk, "dk"),
+                 (dv, "dv")):
+        _check(t, torch.bfloat16, n)
+    _check(lse, torch.float32, "lse")
+    rc = load_library().fa_train_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
+                                        _ptr(mask), _ptr(dq), _ptr(dk), _ptr(dv),
+                                        ctypes.byref(params), ctypes.byref(options),
+                                        _stream_handle(stream))
+    if rc:
+        raise FaError(rc, "fa_train_bwd_ex")
+
+
 def fa_device_status(clear: bool = True) -> int:
     return load_library().fa_device_status(int(bool(clear)))
 
@@ -179,24 +259,40 @@ def fa_version() -> str:
     return load_library().fa_version().decode()
 
 
-def attention_fwd(q, k, v, *, scale, causal, mask=None, stream=None):
-    """Allocate O and L and run the forward: returns (o, lse)."""
+def attention_fwd(q, k, v, *, scale, causal, mask=None, window=None, stream=None):
+    """Allocate O and L and run the forward: returns (o, lse). `mask`: None, or a float32 /
+    bfloat16 additive or bool mask broadcastable to [B, H, ql, kl]; `window`: None or
+    (left, right) with -1 for an unbounded side."""
     import torch
 
     B, H, ql, d = q.shape
     o = torch.empty_like(q)
     lse = torch.empty((B, H, ql), dtype=torch.float32, device=q.device)
-    fa_train_fwd(q, k, v, mask, o, lse, make_params(q, k, scale=scale, causal=causal), stream)
+    params = make_params(q, k, scale=scale, causal=causal)
+    if window is None and (mask is None or (mask.dtype == torch.float32 and mask.dim() == 4
+                                            and mask.is_contiguous()
+                                            and tuple(mask.shape) == (B, H, ql, k.shape[2]))):
+        fa_train_fwd(q, k, v, mask, o, lse, params, stream)
+    else:
+        fa_train_fwd_ex(q, k, v, mask, o, lse, params, make_options(q, k, mask, window), stream)
     return o, lse
 
 
-def attention_bwd(q, k, v, o, lse, dO, *, scale, causal, mask=None, stream=None):
-    """Allocate dQ, dK, dV and run the backward: returns (dq, dk, dv)."""
+def attention_bwd(q, k, v, o, lse, dO, *, scale, causal, mask=None, window=None, stream=None):
+    """Allocate dQ, dK, dV and run the backward: returns (dq, dk, dv). `mask` and `window` as
+    given to attention_fwd."""
     import torch
 
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
-    fa_train_bwd(q, k, v, o, lse, dO, mask, dq, dk, dv,
-                 make_params(q, k, scale=scale, causal=causal), stream)
+    params = make_params(q, k, scale=scale, causal=causal)
+    B, H, ql, _ = q.shape
+    if window is None and (mask is None or (mask.dtype == torch.float32 and mask.dim() == 4
+                                            and mask.is_contiguous()
+                                            and tuple(mask.shape) == (B, H, ql, k.shape[2]))):
+        fa_train_bwd(q, k, v, o, lse, dO, mask, dq, dk, dv, params, stream)
+    else:
+        fa_train_bwd_ex(q, k, v, o, lse, dO, mask, dq, dk, dv, params,
+                        make_options(q, k, mask, window), stream)
     return dq, dk, dv

@@ -100,6 +100,32 @@ int check_params(const fa_params* p) {
 int check_bf16(const void* ptr) { return (ptr && aligned(ptr, 16)) ? FA_OK : FA_ERR_INVALID; }
 int check_f32(const void* ptr) { return (ptr && aligned(ptr, 16)) ? FA_OK : FA_ERR_INVALID; }
 
+// Options with the base entry points' meaning: no window, dense [B, H, ql, kl] f32 mask.
+fa_options default_options(const fa_params* p) {
+  fa_options o;
+  o.window_left = -1;
+  o.window_right = -1;
+  o.mask_type = FA_MASK_F32;
+  o.reserved = 0;
+  o.mask_stride_q = p->kl;
+  o.mask_stride_h = (int64_t)p->ql * p->kl;
+  o.mask_stride_b = (int64_t)p->n_heads * p->ql * p->kl;
+  return o;
+}
+
+int check_options(const fa_options* o, const void* mask) {
+  if (o->window_left < -1 || o->window_right < -1) return FA_ERR_INVALID;
+  if (o->reserved != 0) return FA_ERR_INVALID;
+  if (o->mask_type != FA_MASK_F32 && o->mask_type != FA_MASK_BF16 && o->mask_type != FA_MASK_BOOL)
+    return FA_ERR_INVALID;
+  if (o->mask_stride_b < 0 || o->mask_stride_h < 0 || o->mask_stride_q < 0) return FA_ERR_INVALID;
+  if (mask) {
+    const uintptr_t es = o->mask_type == FA_MASK_F32 ? 4 : o->mask_type == FA_MASK_BF16 ? 2 : 1;
+    if (!aligned(mask, es)) return FA_ERR_INVALID;
+  }
+  return FA_OK;
+}
+
 int check_device() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -200,14 +226,16 @@ const char* fa_kernel_name(int id) {
   }
 }
 
-int fa_train_fwd(const void* q, const void* k, const void* v, const float* mask, void* o,
-                 float* lse, const fa_params* p, void* stream) {
+int fa_train_fwd_ex(const void* q, const void* k, const void* v, const void* mask, void* o,
+                    float* lse, const fa_params* p, const fa_options* opt, void* stream) {
   int rc = check_params(p);
   if (rc) return rc;
   if ((rc = check_bf16(q)) || (rc = check_bf16(k)) || (rc = check_bf16(v)) ||
       (rc = check_bf16(o)) || (rc = check_f32(lse)))
     return rc;
-  if (mask && !aligned(mask, 16)) return FA_ERR_INVALID;
+  const fa_options o_def = default_options(p);
+  const fa_options* op = opt ? opt : &o_def;
+  if ((rc = check_options(op, mask))) return rc;
   if ((rc = check_device())) return rc;
   cudaError_t e = get_encoder();
   if (e != cudaSuccess) return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
@@ -215,6 +243,10 @@ int fa_train_fwd(const void* q, const void* k, const void* v, const float* mask,
   cudaGetDevice(&dev);
   fa::FwdArgs a;
   a.mask = mask;
+  a.mask_type = op->mask_type;
+  a.mask_stride_b = op->mask_stride_b;
+  a.mask_stride_h = op->mask_stride_h;
+  a.mask_stride_q = op->mask_stride_q;
   a.o = o;
   a.lse = lse;
   if ((e = device_status_word(dev, &a.status)) != cudaSuccess) return cuda_fail(e, "status word");
@@ -225,7 +257,10 @@ int fa_train_fwd(const void* q, const void* k, const void* v, const float* mask,
   a.kl = p->kl;
   a.d = p->head_dim;
   a.scale = p->scale;
-  a.causal = p->causal;
+  const fa::Band band = fa::make_band(p->causal, op->window_left, op->window_right);
+  a.lo_off = band.lo_off;
+  a.hi_off = band.hi_off;
+  a.band = band.mode;
   fa::FwdMaps m;
   const int qrows = fa::fwd_q_box_rows(a.d), kvrows = fa::fwd_kv_box_rows(a.d);
   if (!encode_bf16_3d(&m.q, q, a.B * a.H, a.ql, a.d, qrows) ||
@@ -237,52 +272,82 @@ int fa_train_fwd(const void* q, const void* k, const void* v, const float* mask,
   return FA_OK;
 }
 
-int fa_train_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                 const void* dO, const float* mask, void* dq, void* dk, void* dv,
-                 const fa_params* p, void* stream) {
+int fa_train_fwd(const void* q, const void* k, const void* v, const float* mask, void* o,
+                 float* lse, const fa_params* p, void* stream) {
+  if (mask && !aligned(mask, 16)) return FA_ERR_INVALID;
+  return fa_train_fwd_ex(q, k, v, mask, o, lse, p, nullptr, stream);
+}
+
+// Fills the backward arguments shared by the allocating and the no-allocation entry points.
+static int prepare_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dO, const void* mask, void* dq, void* dk,
+                       void* dv, const fa_params* p, const fa_options* opt, fa::BwdArgs* a,
+                       fa::BwdMaps* m) {
   int rc = check_params(p);
   if (rc) return rc;
   if ((rc = check_bf16(q)) || (rc = check_bf16(k)) || (rc = check_bf16(v)) ||
       (rc = check_bf16(o)) || (rc = check_f32(lse)) || (rc = check_bf16(dO)) ||
       (rc = check_bf16(dq)) || (rc = check_bf16(dk)) || (rc = check_bf16(dv)))
     return rc;
-  if (mask && !aligned(mask, 16)) return FA_ERR_INVALID;
+  const fa_options o_def = default_options(p);
+  const fa_options* op = opt ? opt : &o_def;
+  if ((rc = check_options(op, mask))) return rc;
+  a->q = q;
+  a->k = k;
+  a->v = v;
+  a->o = o;
+  a->lse = lse;
+  a->dO = dO;
+  a->mask = mask;
+  a->mask_type = op->mask_type;
+  a->mask_stride_b = op->mask_stride_b;
+  a->mask_stride_h = op->mask_stride_h;
+  a->mask_stride_q = op->mask_stride_q;
+  a->dq = dq;
+  a->dk = dk;
+  a->dv = dv;
+  a->B = p->batch;
+  a->H = p->n_heads;
+  a->Hk = p->n_kv_heads;
+  a->ql = p->ql;
+  a->kl = p->kl;
+  a->d = p->head_dim;
+  a->ql_pad = fa::bwd_ql_pad(a->ql);
+  a->scale = p->scale;
+  const fa::Band band = fa::make_band(p->causal, op->window_left, op->window_right);
+  a->lo_off = band.lo_off;
+  a->hi_off = band.hi_off;
+  a->band = band.mode;
+  a->status = nullptr;
+  (void)m;
+  return FA_OK;
+}
+
+static int encode_bwd_maps(const fa::BwdArgs& a, fa::BwdMaps* m) {
+  const int qrows = fa::bwd_q_box_rows(a.d), kvrows = fa::bwd_kv_box_rows(a.d);
+  if (!encode_bf16_3d(&m->q, a.q, a.B * a.H, a.ql, a.d, qrows) ||
+      !encode_bf16_3d(&m->dO, a.dO, a.B * a.H, a.ql, a.d, qrows) ||
+      !encode_bf16_3d(&m->k, a.k, a.B * a.Hk, a.kl, a.d, kvrows) ||
+      !encode_bf16_3d(&m->v, a.v, a.B * a.Hk, a.kl, a.d, kvrows))
+    return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+  return FA_OK;
+}
+
+int fa_train_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, const void* mask, void* dq, void* dk, void* dv,
+                    const fa_params* p, const fa_options* opt, void* stream) {
+  fa::BwdArgs a;
+  fa::BwdMaps m;
+  int rc = prepare_bwd(q, k, v, o, lse, dO, mask, dq, dk, dv, p, opt, &a, &m);
+  if (rc) return rc;
   if ((rc = check_device())) return rc;
   cudaError_t e = get_encoder();
   if (e != cudaSuccess) return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
   int dev = 0;
   cudaGetDevice(&dev);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-  fa::BwdArgs a;
-  a.q = q;
-  a.k = k;
-  a.v = v;
-  a.o = o;
-  a.lse = lse;
-  a.dO = dO;
-  a.mask = mask;
-  a.dq = dq;
-  a.dk = dk;
-  a.dv = dv;
-  a.B = p->batch;
-  a.H = p->n_heads;
-  a.Hk = p->n_kv_heads;
-  a.ql = p->ql;
-  a.kl = p->kl;
-  a.d = p->head_dim;
-  a.ql_pad = fa::bwd_ql_pad(a.ql);
-  a.scale = p->scale;
-  a.causal = p->causal;
   if ((e = device_status_word(dev, &a.status)) != cudaSuccess) return cuda_fail(e, "status word");
-
-  fa::BwdMaps m;
-  const int qrows = fa::bwd_q_box_rows(a.d), kvrows = fa::bwd_kv_box_rows(a.d);
-  if (!encode_bf16_3d(&m.q, q, a.B * a.H, a.ql, a.d, qrows) ||
-      !encode_bf16_3d(&m.dO, dO, a.B * a.H, a.ql, a.d, qrows) ||
-      !encode_bf16_3d(&m.k, k, a.B * a.Hk, a.kl, a.d, kvrows) ||
-      !encode_bf16_3d(&m.v, v, a.B * a.Hk, a.kl, a.d, kvrows))
-    return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+  if ((rc = encode_bwd_maps(a, &m))) return rc;
 
   const size_t ws_bytes = fa::bwd_workspace_bytes(a.B, a.H, a.ql, a.d);
   void* ws = nullptr;
@@ -296,17 +361,22 @@ int fa_train_bwd(const void* q, const void* k, const void* v, const void* o, con
   return FA_OK;
 }
 
+int fa_train_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dO, const float* mask, void* dq, void* dk, void* dv,
+                 const fa_params* p, void* stream) {
+  if (mask && !aligned(mask, 16)) return FA_ERR_INVALID;
+  return fa_train_bwd_ex(q, k, v, o, lse, dO, mask, dq, dk, dv, p, nullptr, stream);
+}
+
 int fa_train_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                          const float* lse, const void* dO, const float* mask, void* dq, void* dk,
                          void* dv, const fa_params* p, void* stream) {
-  int rc = check_params(p);
-  if (rc) return rc;
-  if ((rc = check_bf16(q)) || (rc = check_bf16(k)) || (rc = check_bf16(v)) ||
-      (rc = check_bf16(o)) || (rc = check_f32(lse)) || (rc = check_bf16(dO)) ||
-      (rc = check_bf16(dq)) || (rc = check_bf16(dk)) || (rc = check_bf16(dv)))
-    return rc;
   if (mask && !aligned(mask, 16)) return FA_ERR_INVALID;
-  const size_t ws_bytes = fa::bwd_workspace_bytes(p->batch, p->n_heads, p->ql, p->head_dim);
+  fa::BwdArgs a;
+  fa::BwdMaps m;
+  int rc = prepare_bwd(q, k, v, o, lse, dO, mask, dq, dk, dv, p, nullptr, &a, &m);
+  if (rc) return rc;
+  const size_t ws_bytes = fa::bwd_workspace_bytes(a.B, a.H, a.ql, a.d);
   if (ws_bytes > fa::kNoAllocScratchBytes) {
     snprintf(g_last_cuda_error, sizeof(g_last_cuda_error),
              "fa_train_bwd_noalloc: needs %zu bytes of scratch, the fixed array holds %zu",
@@ -318,35 +388,8 @@ int fa_train_bwd_noalloc(const void* q, const void* k, const void* v, const void
   if (e != cudaSuccess) return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
   void* ws = nullptr;
   if ((e = fa::noalloc_scratch(&ws)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
-
-  fa::BwdArgs a;
-  a.q = q;
-  a.k = k;
-  a.v = v;
-  a.o = o;
-  a.lse = lse;
-  a.dO = dO;
-  a.mask = mask;
-  a.dq = dq;
-  a.dk = dk;
-  a.dv = dv;
-  a.B = p->batch;
-  a.H = p->n_heads;
-  a.Hk = p->n_kv_heads;
-  a.ql = p->ql;
-  a.kl = p->kl;
-  a.d = p->head_dim;
-  a.ql_pad = fa::bwd_ql_pad(a.ql);
-  a.scale = p->scale;
-  a.causal = p->causal;
   a.status = nullptr;  // the status word is allocated; this path records no timeout
-  fa::BwdMaps m;
-  const int qrows = fa::bwd_q_box_rows(a.d), kvrows = fa::bwd_kv_box_rows(a.d);
-  if (!encode_bf16_3d(&m.q, q, a.B * a.H, a.ql, a.d, qrows) ||
-      !encode_bf16_3d(&m.dO, dO, a.B * a.H, a.ql, a.d, qrows) ||
-      !encode_bf16_3d(&m.k, k, a.B * a.Hk, a.kl, a.d, kvrows) ||
-      !encode_bf16_3d(&m.v, v, a.B * a.Hk, a.kl, a.d, kvrows))
-    return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+  if ((rc = encode_bwd_maps(a, &m))) return rc;
   // the pre-pass rewrites L*log2(e) and D and zeroes the dQ accumulator for every row the
   // main pass reads, so the array's previous contents never reach a result
   fa::bwd_carve_workspace(ws, a.B, a.H, a.ql, a.d, &a.lse2, &a.dvec, &a.dqacc);

@@ -108,7 +108,8 @@ struct BwdLayout {
 };
 
 struct BwdKParams {
-  const float* mask;
+  const void* mask;         // additive f32 / bf16, or bool (uint8), addressed with the strides
+  long long msb, msh, msq;  // mask strides (elements) of batch, head, query row
   const float* lse2;
   const float* dvec;
   float* dqacc;
@@ -116,6 +117,7 @@ struct BwdKParams {
   __nv_bfloat16* dv;
   int* status;
   int H, Hk, ql, kl, ql_pad;
+  int lo_off, hi_off;  // key j is visible to query row i iff q_abs + lo_off <= j <= q_abs + hi_off
   float scale, scale_log2;
 };
 
@@ -202,12 +204,44 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
 }
 
 // ------------------------------------------------------------------------ main kernel
-template <int HD, bool CAUSAL>
-__device__ __forceinline__ int bwd_first_mtile(int n0, int ql, int kl) {
-  if (!CAUSAL) return 0;
+// Query tiles [first, last] whose rows see some key of the kv tile starting at n0: rows i with
+// q_abs + lo_off <= j <= q_abs + hi_off for some j in the tile (q_abs = kl - ql + i). Under the
+// causal band alone, key n0 is visible to the rows from n0 - (kl - ql) on, and to the last row.
+template <int HD, int BAND>
+__device__ __forceinline__ void bwd_mtile_range(int n0, const BwdKParams& p, int& first,
+                                                int& last) {
   constexpr int BM = BwdTraits<HD>::BM;
-  const int first_row = n0 - (kl - ql);  // key n0 is visible to rows >= first_row
-  return first_row <= 0 ? 0 : first_row / BM;
+  const int n_mt = (p.ql + BM - 1) / BM;
+  if (BAND != kBandWindow) {
+    first = 0;
+    if (BAND == kBandCausal) {
+      const int first_row = n0 - (p.kl - p.ql);
+      first = first_row <= 0 ? 0 : first_row / BM;
+    }
+    last = n_mt - 1;
+    return;
+  }
+  const long long off = (long long)p.kl - p.ql;
+  const long long n1 = min(n0 + kBN, p.kl) - 1;
+  const long long imin = max(0LL, (long long)n0 - off - p.hi_off);
+  const long long imax = min((long long)p.ql - 1, n1 - off - p.lo_off);
+  if (imax < imin) {
+    first = 0;
+    last = -1;
+    return;
+  }
+  first = (int)(imin / BM);
+  last = (int)(imax / BM);
+}
+
+// Mask value at element offset `e` from `base`, as a base-2 additive term.
+template <int MASKT>
+__device__ __forceinline__ float mask_log2_b(const void* base, long long e) {
+  if constexpr (MASKT == 1) return reinterpret_cast<const float*>(base)[e] * kLog2eB;
+  if constexpr (MASKT == 2)
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[e]) * kLog2eB;
+  if constexpr (MASKT == 3) return reinterpret_cast<const uint8_t*>(base)[e] ? 0.0f : -INFINITY;
+  return 0.0f;
 }
 
 // Writes 8 bf16 (one 16-byte granule g of row j) into a 128-byte-swizzled tile chunk.
@@ -215,7 +249,7 @@ __device__ __forceinline__ void st_swizzled(uint8_t* chunk, int j, int g, uint4 
   *reinterpret_cast<uint4*>(chunk + j * 128 + ((g ^ (j & 7)) << 4)) = val;
 }
 
-template <int HD, bool CAUSAL, bool HAS_MASK>
+template <int HD, int BAND, int MASKT>
 __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                     const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mDO,
@@ -241,9 +275,10 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
   const int b = bkh / p.Hk, kh = bkh % p.Hk;
   const int G = p.H / p.Hk;
   const int n0 = (int)blockIdx.y * kBN;
-  const int n_mt = (p.ql + BM - 1) / BM;
-  const int m_first = min(bwd_first_mtile<HD, CAUSAL>(n0, p.ql, p.kl), n_mt);
-  const int nm = n_mt - m_first;      // query tiles per head
+  int m_first, m_last;
+  constexpr bool WIN = BAND == kBandWindow;
+  bwd_mtile_range<HD, BAND>(n0, p, m_first, m_last);
+  const int nm = m_last - m_first + 1;  // query tiles per head (0 if none)
   const int n_iter = G * nm;          // (head, query tile) pairs this CTA visits
 
   if (threadIdx.x == 0) {
@@ -478,15 +513,27 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
       const int bh = b * p.H + h;
       const float* sL = reinterpret_cast<const float*>(smem + LY::OFF_L + st * BM * 4);
       const uint32_t colS = LY::COL_S0 + (it % NSB) * BM;
-      // query q (column) sees this key iff q0 + q >= kv - (kl - ql)
-      const int qmin = kv - (p.kl - p.ql) - q0;  // columns < qmin are hidden (causal)
-      const bool edge = CAUSAL && (n0 + kBN - 1 - (p.kl - p.ql) > q0);
-      // columns below qcut get P = 0: the causal bound on edge tiles, every column for kv rows
-      // past the end
+      // column q (row q0 + q) sees this key iff qlo <= q <= qhi (no upper limit without a
+      // window)
+      const int off = p.kl - p.ql;
+      const int hi_off = WIN ? p.hi_off : 0;
+      const int qlo = kv - off - hi_off - q0;
+      const int qhi = WIN ? kv - off - p.lo_off - q0 : BM;
+      // interior pair: the first query row sees the tile's last key and the last query row its
+      // first key; otherwise some element is hidden (uniform over the warpgroup)
+      const bool edge = BAND != kBandNone && !(q0 >= n0 + kBN - 1 - off - hi_off &&
+                                               (!WIN || q0 + BM - 1 <= n0 - off - p.lo_off));
+      // columns outside [qcut_lo, qcut_hi] get P = 0: the band on edge tiles, every column for
+      // kv rows past the end (qcut_lo = BM)
       const bool need_mask = edge || !kv_live;
-      const int qcut = !kv_live ? BM : (edge ? qmin : 0);
-      const float* mcol = nullptr;
-      if (HAS_MASK && kv_live) mcol = p.mask + ((size_t)bh * p.ql + q0) * (size_t)p.kl + kv;
+      const int qcut_lo = !kv_live ? BM : (edge ? qlo : 0);
+      const int qcut_hi = edge ? qhi : BM;
+      const void* mcol = nullptr;
+      if (MASKT != 0 && kv_live) {
+        const size_t es = MASKT == 1 ? 4 : MASKT == 2 ? 2 : 1;
+        mcol = reinterpret_cast<const uint8_t*>(p.mask) +
+               (b * p.msb + (long long)h * p.msh + (long long)q0 * p.msq + kv) * es;
+      }
 
       // the stage's L rows came with the Q/dO copies; observe that barrier here too (its
       // next phase needs this tile's dK MMA, so it cannot have moved on)
@@ -511,12 +558,13 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
             const float4 nl = sL4[c32 * 8 + e4];
             const int q = c32 * 32 + e4 * 4;
             uint64_t b01 = f2_pack(nl.x, nl.y), b23 = f2_pack(nl.z, nl.w);
-            if (HAS_MASK) {
+            if (MASKT != 0) {
               float m4[4];
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                m4[k] = (mcol != nullptr && q0 + q + k < p.ql) ? mcol[(size_t)(q + k) * p.kl] * kLog2eB
-                                                               : 0.0f;
+                m4[k] = (mcol != nullptr && q0 + q + k < p.ql)
+                            ? mask_log2_b<MASKT>(mcol, (long long)(q + k) * p.msq)
+                            : 0.0f;
               b01 = f2_add(b01, f2_pack(m4[0], m4[1]));
               b23 = f2_add(b23, f2_pack(m4[2], m4[3]));
             }
@@ -527,11 +575,11 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
             f2_unpack(s01, a0, a1);
             f2_unpack(s23, a2, a3);
             float p0 = ex2(a0), p1 = ex2(a1), p2 = ex2(a2), p3 = ex2(a3);
-            if (need_mask) {  // hidden columns (causal) and kv rows past the end
-              p0 = q >= qcut ? p0 : 0.0f;
-              p1 = q + 1 >= qcut ? p1 : 0.0f;
-              p2 = q + 2 >= qcut ? p2 : 0.0f;
-              p3 = q + 3 >= qcut ? p3 : 0.0f;
+            if (need_mask) {  // hidden columns (band) and kv rows past the end
+              p0 = (q >= qcut_lo && (!WIN || q <= qcut_hi)) ? p0 : 0.0f;
+              p1 = (q + 1 >= qcut_lo && (!WIN || q + 1 <= qcut_hi)) ? p1 : 0.0f;
+              p2 = (q + 2 >= qcut_lo && (!WIN || q + 2 <= qcut_hi)) ? p2 : 0.0f;
+              p3 = (q + 3 >= qcut_lo && (!WIN || q + 3 <= qcut_hi)) ? p3 : 0.0f;
             }
             pk[2 * e4] = pack_bf16(p0, p1);
             pk[2 * e4 + 1] = pack_bf16(p2, p3);
@@ -759,10 +807,10 @@ void bwd_carve_workspace(void* base, int B, int H, int ql, int d, float** lse2, 
   (void)d;
 }
 
-template <int HD, bool CAUSAL, bool HAS_MASK>
+template <int HD, int BAND, int MASKT>
 static cudaError_t launch_main_t(const BwdArgs& a, const BwdMaps& m, cudaStream_t s) {
   using LY = BwdLayout<HD>;
-  auto kern = bwd_main_kernel<HD, CAUSAL, HAS_MASK>;
+  auto kern = bwd_main_kernel<HD, BAND, MASKT>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
@@ -772,6 +820,11 @@ static cudaError_t launch_main_t(const BwdArgs& a, const BwdMaps& m, cudaStream_
   }
   BwdKParams kp;
   kp.mask = a.mask;
+  kp.msb = a.mask_stride_b;
+  kp.msh = a.mask_stride_h;
+  kp.msq = a.mask_stride_q;
+  kp.lo_off = a.lo_off;
+  kp.hi_off = a.hi_off;
   kp.lse2 = a.lse2;
   kp.dvec = a.dvec;
   kp.dqacc = a.dqacc;
@@ -793,6 +846,16 @@ static cudaError_t launch_main_t(const BwdArgs& a, const BwdMaps& m, cudaStream_
   return e;
 }
 
+template <int HD, int BAND>
+static cudaError_t launch_main_m(const BwdArgs& a, const BwdMaps& m, cudaStream_t s) {
+  if (!a.mask) return launch_main_t<HD, BAND, 0>(a, m, s);
+  switch (a.mask_type) {
+    case 0: return launch_main_t<HD, BAND, 1>(a, m, s);
+    case 1: return launch_main_t<HD, BAND, 2>(a, m, s);
+    default: return launch_main_t<HD, BAND, 3>(a, m, s);
+  }
+}
+
 template <int HD>
 static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t s) {
   const int BH = a.B * a.H;
@@ -807,12 +870,9 @@ static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t
     profile_mark(kKernBwdPrep, 1, s);
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e;
-  if (a.causal) {
-    e = a.mask ? launch_main_t<HD, true, true>(a, m, s) : launch_main_t<HD, true, false>(a, m, s);
-  } else {
-    e = a.mask ? launch_main_t<HD, false, true>(a, m, s) : launch_main_t<HD, false, false>(a, m, s);
-  }
+  cudaError_t e = a.band == kBandNone     ? launch_main_m<HD, kBandNone>(a, m, s)
+                  : a.band == kBandCausal ? launch_main_m<HD, kBandCausal>(a, m, s)
+                                          : launch_main_m<HD, kBandWindow>(a, m, s);
   if (e != cudaSuccess) return e;
   {
     const long long groups = (long long)a.ql * (HD / 8);  // 8-value groups per head

@@ -78,30 +78,58 @@ struct FwdLayout {
 };
 
 struct FwdKParams {
-  const float* mask;
+  const void* mask;  // additive f32 / bf16, or bool (uint8), addressed with the strides below
+  long long msb, msh, msq;  // mask strides (elements) of batch, head, query row; keys contiguous
   __nv_bfloat16* o;
   float* lse;
   int* status;
   int H, Hk, ql, kl, n_mblk;
-  float scale_log2;  // scale * log2(e)
+  int lo_off, hi_off;  // key j is visible to row i iff q_abs + lo_off <= j <= q_abs + hi_off
+  float scale_log2;    // scale * log2(e)
 };
 
-// Number of kv tiles query tile t of the CTA at row m0 must visit.
-template <int HD, bool CAUSAL>
-__device__ __forceinline__ int fwd_tiles_for(int m0, int t, int ql, int kl) {
-  constexpr int BN = FwdTraits<HD>::BN;
-  int kend = kl;
-  if (CAUSAL) {
-    // last row of the tile is m0 + (t+1)*BM - 1 (clamped to ql-1); it sees keys <= off + row
-    int last_row = min(m0 + (t + 1) * kBM, ql) - 1;
-    int lim = kl - ql + last_row + 1;  // exclusive key bound
-    kend = min(kend, lim);
-  }
-  if (kend <= 0) return 0;
-  return (kend + BN - 1) / BN;
+// Mask value of key column `j` for the row whose mask row starts at `mrow`, as a base-2
+// additive term (0 or -inf for bool masks).
+template <int MASKT>
+__device__ __forceinline__ float mask_log2(const void* mrow, long long j) {
+  if constexpr (MASKT == 1) return reinterpret_cast<const float*>(mrow)[j] * kLog2e;
+  if constexpr (MASKT == 2)
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(mrow)[j]) * kLog2e;
+  if constexpr (MASKT == 3) return reinterpret_cast<const uint8_t*>(mrow)[j] ? 0.0f : -INFINITY;
+  return 0.0f;
 }
 
-template <int HD, bool CAUSAL, bool HAS_MASK>
+// Kv tiles [first, last) that query tile t of the CTA at row m0 must visit: the tiles holding a
+// key inside the row band [q_abs + lo_off, q_abs + hi_off] of any of its rows (q_abs = kl - ql +
+// row). Without a window every range starts at tile 0 (an empty range is [0, 0)). With one, a
+// tile wholly past the last query row, or whose band misses every key, gets first = last = -1
+// and the caller places it at the end of the previous tile's range, so that the ranges of a
+// CTA's tiles stay ordered.
+template <int HD, int BAND>
+__device__ __forceinline__ void fwd_tile_range(int m0, int t, const FwdKParams& p, int& first,
+                                               int& last) {
+  constexpr int BN = FwdTraits<HD>::BN;
+  const int r1 = min(m0 + (t + 1) * kBM, p.ql) - 1;  // last row of the tile (clamped)
+  const int off = p.kl - p.ql;
+  if (BAND != kBandWindow) {
+    int kend = p.kl;
+    if (BAND == kBandCausal) kend = min(kend, off + r1 + 1);  // exclusive key bound
+    first = 0;
+    last = kend <= 0 ? 0 : (kend + BN - 1) / BN;
+    return;
+  }
+  const int r0 = m0 + t * kBM;
+  const long long klo = max(0LL, (long long)off + r0 + p.lo_off);
+  const long long khi = min((long long)p.kl, (long long)off + r1 + p.hi_off + 1);  // exclusive
+  if (r0 >= p.ql || khi <= klo) {
+    first = last = -1;
+    return;
+  }
+  first = (int)(klo / BN);
+  last = (int)((khi + BN - 1) / BN);
+}
+
+template <int HD, int BAND, int MASKT>
 __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                const __grid_constant__ CUtensorMap mV, const FwdKParams p) {
@@ -127,12 +155,30 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
   const int b = bh / p.H, h = bh % p.H;
   const int bkh = b * p.Hk + h / (p.H / p.Hk);
 
-  int nt[NQ];
-  int nt_max = 0;
+  // kv tile ranges of the query tiles, and their union [J0, J1)
+  constexpr bool WIN = BAND == kBandWindow;
+  int jt0[NQ], jt1[NQ];
 #pragma unroll
-  for (int t = 0; t < NQ; ++t) {
-    nt[t] = fwd_tiles_for<HD, CAUSAL>(m0, t, p.ql, p.kl);
-    nt_max = max(nt_max, nt[t]);
+  for (int t = 0; t < NQ; ++t) fwd_tile_range<HD, BAND>(m0, t, p, jt0[t], jt1[t]);
+  int J0 = 0, J1 = 0;
+  if (!WIN) {
+#pragma unroll
+    for (int t = 0; t < NQ; ++t) {
+      jt0[t] = 0;
+      J1 = max(J1, jt1[t]);
+    }
+  } else {
+    bool any = false;
+#pragma unroll
+    for (int t = 0; t < NQ; ++t) {
+      if (jt0[t] < 0) continue;
+      J0 = any ? min(J0, jt0[t]) : jt0[t];
+      J1 = any ? max(J1, jt1[t]) : jt1[t];
+      any = true;
+    }
+#pragma unroll
+    for (int t = 0; t < NQ; ++t)
+      if (jt0[t] < 0) jt0[t] = jt1[t] = (t > 0 ? jt1[t - 1] : J0);  // empty, in order
   }
 
   if (threadIdx.x == 0) {
@@ -178,21 +224,21 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
         for (int c = 0; c < KCH; ++c)
           tma_load_3d(smem + LY::OFF_Q + t * LY::Q_TILE_BYTES + c * kBM * 128, &mQ, &q_full,
                       c * 64, m0 + t * kBM, bh);
-      for (int j = 0; j < nt_max; ++j) {
-        const int st = j % STAGES;
-        const uint32_t use = j / STAGES;
-        if (j >= STAGES && !mbar_wait(&k_empty[st], (use - 1) & 1, &abort_flag)) break;
+      for (int j = J0; j < J1; ++j) {
+        const int st = (j - J0) % STAGES;
+        const uint32_t use = (j - J0) / STAGES;
+        if (use > 0 && !mbar_wait(&k_empty[st], (use - 1) & 1, &abort_flag)) break;
         mbar_arrive_expect_tx(&k_full[st], LY::KV_TILE_BYTES);
         for (int c = 0; c < KCH; ++c)
           tma_load_3d_hint(smem + LY::OFF_K + st * LY::KV_TILE_BYTES + c * BN * 128, &mK,
                            &k_full[st], c * 64, j * BN, bkh, pol_kv);
-        last_k[st] = j;
-        if (j >= STAGES && !mbar_wait(&v_empty[st], (use - 1) & 1, &abort_flag)) break;
+        last_k[st] = j - J0;
+        if (use > 0 && !mbar_wait(&v_empty[st], (use - 1) & 1, &abort_flag)) break;
         mbar_arrive_expect_tx(&v_full[st], LY::KV_TILE_BYTES);
         for (int c = 0; c < KCH; ++c)
           tma_load_3d_hint(smem + LY::OFF_V + st * LY::KV_TILE_BYTES + c * BN * 128, &mV,
                            &v_full[st], c * 64, j * BN, bkh, pol_kv);
-        last_v[st] = j;
+        last_v[st] = j - J0;
       }
       // Let every copy this thread started land before the CTA can exit.
       mbar_wait_drain(&q_full, 0);
@@ -209,43 +255,65 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
       const uint32_t sq = smem_u32(smem + LY::OFF_Q);
       const uint32_t sk = smem_u32(smem + LY::OFF_K);
       const uint32_t sv = smem_u32(smem + LY::OFF_V);
-      int k_ready = -1, v_ready = -1;  // highest kv tile whose K / V wait is done
+      // K / V of kv tile j sit in stage (j - J0) % STAGES. A stage is released once every query
+      // tile that uses the kv tile has issued its MMA on it. Without a window the last query
+      // tile uses every kv tile of the CTA (its range is the widest and all start at 0), so it
+      // releases; with one, kleft / vleft count the users still to come (set when the tile's
+      // full barrier is waited, in kv order).
+      int k_ready = J0 - 1, v_ready = J0 - 1;  // highest kv tile whose K / V wait is done
+      int kleft[STAGES], vleft[STAGES];
+      auto users = [&](int j) {
+        int n = 0;
+#pragma unroll
+        for (int t = 0; t < NQ; ++t) n += (j >= jt0[t] && j < jt1[t]) ? 1 : 0;
+        return n;
+      };
       bool ok = mbar_wait(&q_full, 0, &abort_flag);
       tc_fence_after();
 
       auto issue_s = [&](int t, int j) {
-        const int st = j % STAGES;
-        if (j > k_ready) {
-          ok = ok && mbar_wait(&k_full[st], (j / STAGES) & 1, &abort_flag);
-          k_ready = j;
+        const int st = (j - J0) % STAGES;
+        // wait the K tiles in order (without a window the next one is always j itself)
+        while (ok && j > k_ready) {
+          const int jw = WIN ? k_ready + 1 : j;
+          ok = mbar_wait(&k_full[(jw - J0) % STAGES], ((jw - J0) / STAGES) & 1, &abort_flag);
+          if (WIN) kleft[(jw - J0) % STAGES] = users(jw);
+          k_ready = jw;
           tc_fence_after();
         }
-        const uint32_t d_tmem = tbase + t * LY::TILE_COLS + HD + (j % NS) * BN;
+        if (!ok) return;
+        const int jj = j - jt0[t];  // == j without a window
+        const uint32_t d_tmem = tbase + t * LY::TILE_COLS + HD + (jj % NS) * BN;
         const Desc qa = make_desc(sq + t * LY::Q_TILE_BYTES, 16, 1024);
         const Desc kb = make_desc(sk + st * LY::KV_TILE_BYTES, 16, 1024);
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks)
           mma_ss2(d_tmem, qa.at((ks / 4) * (kBM * 128) + (ks % 4) * 32), qa.hi,
                   kb.at((ks / 4) * (BN * 128) + (ks % 4) * 32), kb.hi, idesc_s, ks > 0 ? 1u : 0u);
-        mma_commit(&s_full[t][j % NS]);
-        if (t == NQ - 1) mma_commit(&k_empty[st]);
+        mma_commit(&s_full[t][jj % NS]);
+        if (WIN ? --kleft[st] == 0 : t == NQ - 1) mma_commit(&k_empty[st]);
       };
 
       // prologue: the first NS score tiles of every query tile
-      for (int j = 0; j < NS && ok; ++j)
+      for (int s0 = 0; s0 < NS && ok; ++s0)
+#pragma unroll
         for (int t = 0; t < NQ; ++t)
-          if (j < nt[t]) issue_s(t, j);
+          if (jt0[t] + s0 < jt1[t]) issue_s(t, jt0[t] + s0);
 
-      for (int j = 0; j < nt_max && ok; ++j) {
-        const int st = j % STAGES;
-        for (int t = 0; t < NQ && ok; ++t) {
-          if (j >= nt[t]) continue;
-          const int sb = j % NS;
-          ok = mbar_wait(&p_full[t][sb], (j / NS) & 1, &abort_flag);
+      for (int j = J0; j < J1 && ok; ++j) {
+        const int st = (j - J0) % STAGES;
+#pragma unroll
+        for (int t = 0; t < NQ; ++t) {
+          if (!ok) break;
+          if (j < jt0[t] || j >= jt1[t]) continue;
+          const int jj = j - jt0[t];  // iteration of this query tile
+          const int sb = jj % NS;
+          ok = mbar_wait(&p_full[t][sb], (jj / NS) & 1, &abort_flag);
           if (!ok) break;
           if (j > v_ready) {
-            ok = mbar_wait(&v_full[st], (j / STAGES) & 1, &abort_flag);
+            ok = mbar_wait(&v_full[st], ((j - J0) / STAGES) & 1, &abort_flag);
             if (!ok) break;
+            if (WIN) vleft[st] = users(j);
             v_ready = j;
           }
           tc_fence_after();
@@ -255,11 +323,11 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
 #pragma unroll
           for (int ks = 0; ks < BN / 16; ++ks)
             mma_ts2(o_tmem, p_tmem + ks * 8, vb.at(ks * 2048), vb.hi, idesc_o,
-                    (j > 0 || ks > 0) ? 1u : 0u);
+                    (jj > 0 || ks > 0) ? 1u : 0u);
           mma_commit(&o_done[t]);
-          if (j == nt[t] - 1) mma_commit(&o_final[t]);  // every PV of tile t issued
-          if (t == NQ - 1) mma_commit(&v_empty[st]);
-          if (j + NS < nt[t]) issue_s(t, j + NS);
+          if (j == jt1[t] - 1) mma_commit(&o_final[t]);  // every PV of tile t issued
+          if (WIN ? --vleft[st] == 0 : t == NQ - 1) mma_commit(&v_empty[st]);
+          if (j + NS < jt1[t]) issue_s(t, j + NS);
         }
       }
       // all MMAs complete before TMEM can be released
@@ -272,20 +340,37 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
     const int wl = warp % 4;
     const int r = wl * 32 + lane;  // row within the tile == TMEM lane
     const int i = m0 + t * kBM + r;
-    const int ntt = nt[t];
-    const int kmax_row = CAUSAL ? min(p.kl - 1, p.kl - p.ql + i) : p.kl - 1;  // last visible key
+    // kv tiles [kt0, kt0 + ntt) of this query tile (an empty window range gives ntt = 0)
+    int kt0, kt1;
+    fwd_tile_range<HD, BAND>(m0, t, p, kt0, kt1);
+    const int ntt = kt1 - kt0;
+    const int off = p.kl - p.ql;
+    // visible keys of this row: [klo_row, khi_row] (the row band, clipped to the keys)
+    const int hi_off = WIN ? p.hi_off : 0;
+    const int klo_row = WIN ? off + i + p.lo_off : 0;
+    const int khi_row = BAND != kBandNone ? min(p.kl - 1, off + i + hi_off) : p.kl - 1;
+    // the same bounds at the tile's first and last rows decide whether a kv tile is interior
     const int tile_row0 = m0 + t * kBM;
+    const int tile_row1 = min(tile_row0 + kBM, p.ql) - 1;
+    const int klo_tile = WIN ? off + tile_row1 + p.lo_off : 0;  // largest lo
+    const int khi_tile =
+        BAND != kBandNone ? min(p.kl - 1, off + tile_row0 + hi_off) : p.kl - 1;  // smallest hi
     const float c2 = p.scale_log2;
     const uint32_t lane_base = tbase + ((uint32_t)(wl * 32) << 16);
     const uint32_t o_col = t * LY::TILE_COLS;
-    const float* mrow = nullptr;
-    if (HAS_MASK && i < p.ql) mrow = p.mask + ((size_t)bh * p.ql + i) * (size_t)p.kl;
+    const void* mrow = nullptr;
+    if (MASKT != 0 && i < p.ql) {
+      const int b_ = bh / p.H, h_ = bh % p.H;
+      const size_t es = MASKT == 1 ? 4 : MASKT == 2 ? 2 : 1;
+      mrow = reinterpret_cast<const uint8_t*>(p.mask) +
+             (b_ * p.msb + h_ * p.msh + (long long)i * p.msq) * es;
+    }
 
     float m_used = -FLT_MAX / 2.0f;  // finite sentinel
     float l = 0.0f;
     bool ok = true;
 
-    for (int j = 0; j < ntt; ++j) {
+    for (int j = 0; j < ntt; ++j) {  // j: iteration of this query tile (kv tile kt0 + j)
       const int sb = j % NS;
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t][sb], (j / NS) & 1, &abort_flag));
       if (!ok) break;
@@ -296,24 +381,24 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
       for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
       tmem_wait_ld();
 
-      const int n0 = j * BN;
+      const int n0 = (kt0 + j) * BN;
       // does any element of this tile need masking (uniform over the warpgroup)?
-      const bool edge = (n0 + BN > p.kl) || (CAUSAL && n0 + BN - 1 > p.kl - p.ql + tile_row0);
-      const int lim = kmax_row - n0;  // element c visible iff c <= lim
+      const bool edge = (n0 + BN - 1 > khi_tile) || (WIN && n0 < klo_tile);
+      const int lim_lo = klo_row - n0, lim_hi = khi_row - n0;  // c visible iff lo <= c <= hi
       // scores in place of the loaded row: raw S, or (with a mask) the base-2 score; -inf
-      // where the key is hidden. Tiles away from the diagonal and the key tail skip this.
-      if (HAS_MASK || edge) {
+      // where the key is hidden. Tiles inside every row's band skip this.
+      if (MASKT != 0 || edge) {
 #pragma unroll
         for (int c32 = 0; c32 < BN / 32; ++c32) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int c = c32 * 32 + e;
             float v = __uint_as_float(sr[c32][e]);
-            if (HAS_MASK) {
-              float mv = (mrow != nullptr && n0 + c < p.kl) ? mrow[n0 + c] : 0.0f;
-              v = fmaf(v, c2, mv * kLog2e);
+            if (MASKT != 0) {
+              const float mv = (mrow != nullptr && n0 + c < p.kl) ? mask_log2<MASKT>(mrow, n0 + c) : 0.0f;
+              v = fmaf(v, c2, mv);
             }
-            if (c > lim) v = -INFINITY;
+            if ((WIN && c < lim_lo) || c > lim_hi) v = -INFINITY;
             sr[c32][e] = __float_as_uint(v);
           }
         }
@@ -325,7 +410,7 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
         for (int e = 0; e < 32; e += 2)
           mx = fmax3(mx, __uint_as_float(sr[c32][e]), __uint_as_float(sr[c32][e + 1]));
       // row maximum in base-2 units
-      const float m_tile = HAS_MASK ? mx : mx * c2;
+      const float m_tile = MASKT != 0 ? mx : mx * c2;
       const float m_new = fmaxf(m_used, m_tile);
       const bool need = m_new > m_used + kRescaleThreshold;
       if (__any_sync(0xffffffffu, need)) {
@@ -363,7 +448,7 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
         for (int e = 0; e < 16; ++e) {
           const uint64_t xv = f2_pack(__uint_as_float(sr[c32][2 * e]),
                                       __uint_as_float(sr[c32][2 * e + 1]));
-          const uint64_t sv = HAS_MASK ? f2_add(xv, negm) : f2_fma(xv, c2v, negm);
+          const uint64_t sv = MASKT != 0 ? f2_add(xv, negm) : f2_fma(xv, c2v, negm);
           float s0, s1;
           f2_unpack(sv, s0, s1);
           float p0, p1;
@@ -434,10 +519,10 @@ int fwd_kv_box_rows(int d) {
   return d == 64 ? FwdTraits<64>::BN : d == 128 ? FwdTraits<128>::BN : FwdTraits<256>::BN;
 }
 
-template <int HD, bool CAUSAL, bool HAS_MASK>
+template <int HD, int BAND, int MASKT>
 static cudaError_t launch_fwd_t(const FwdArgs& a, const FwdMaps& m, cudaStream_t stream) {
   using LY = FwdLayout<HD>;
-  auto kern = fwd_kernel<HD, CAUSAL, HAS_MASK>;
+  auto kern = fwd_kernel<HD, BAND, MASKT>;
   static bool attr_set = false;  // per instantiation; the attribute is per device function
   if (!attr_set) {
     cudaError_t e =
@@ -447,6 +532,9 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, const FwdMaps& m, cudaStream_t
   }
   FwdKParams kp;
   kp.mask = a.mask;
+  kp.msb = a.mask_stride_b;
+  kp.msh = a.mask_stride_h;
+  kp.msq = a.mask_stride_q;
   kp.o = reinterpret_cast<__nv_bfloat16*>(a.o);
   kp.lse = a.lse;
   kp.status = a.status;
@@ -454,6 +542,8 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, const FwdMaps& m, cudaStream_t
   kp.Hk = a.Hk;
   kp.ql = a.ql;
   kp.kl = a.kl;
+  kp.lo_off = a.lo_off;
+  kp.hi_off = a.hi_off;
   kp.n_mblk = (a.ql + FwdTraits<HD>::NQ * kBM - 1) / (FwdTraits<HD>::NQ * kBM);
   kp.scale_log2 = a.scale * kLog2e;
   dim3 grid(a.B * a.H, kp.n_mblk);
@@ -464,12 +554,23 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, const FwdMaps& m, cudaStream_t
   return e;
 }
 
+template <int HD, int BAND>
+static cudaError_t launch_fwd_m(const FwdArgs& a, const FwdMaps& m, cudaStream_t s) {
+  if (!a.mask) return launch_fwd_t<HD, BAND, 0>(a, m, s);
+  switch (a.mask_type) {
+    case 0: return launch_fwd_t<HD, BAND, 1>(a, m, s);
+    case 1: return launch_fwd_t<HD, BAND, 2>(a, m, s);
+    default: return launch_fwd_t<HD, BAND, 3>(a, m, s);
+  }
+}
+
 template <int HD>
 static cudaError_t launch_fwd_d(const FwdArgs& a, const FwdMaps& m, cudaStream_t s) {
-  if (a.causal) {
-    return a.mask ? launch_fwd_t<HD, true, true>(a, m, s) : launch_fwd_t<HD, true, false>(a, m, s);
+  switch (a.band) {
+    case kBandNone: return launch_fwd_m<HD, kBandNone>(a, m, s);
+    case kBandCausal: return launch_fwd_m<HD, kBandCausal>(a, m, s);
+    default: return launch_fwd_m<HD, kBandWindow>(a, m, s);
   }
-  return a.mask ? launch_fwd_t<HD, false, true>(a, m, s) : launch_fwd_t<HD, false, false>(a, m, s);
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, const FwdMaps& m, cudaStream_t stream) {

@@ -15,15 +15,44 @@ enum KernelId { kKernFwd = 0, kKernBwdPrep = 1, kKernBwdMain = 2, kKernBwdDq = 3
 // enabled; does nothing otherwise. Defined in fa_api.cu.
 void profile_mark(int kernel, int end, cudaStream_t s);
 
+// Visibility band of a row: key j is visible to query row i iff
+//   q_abs + lo_off <= j <= q_abs + hi_off,  q_abs = kl - ql + i
+// (plus j < kl). The kernels are compiled per band mode: kBandNone (no causal mask, no window:
+// no per-element test), kBandCausal (the causal diagonal alone: hi_off = 0, lo unbounded) and
+// kBandWindow (any other band; both bounds are runtime values and the kv ranges of the query
+// tiles of one CTA may start at different tiles).
+enum BandMode : int { kBandNone = 0, kBandCausal = 1, kBandWindow = 2 };
+struct Band {
+  int lo_off, hi_off;
+  int mode;
+};
+constexpr int kUnbounded = 1 << 30;
+inline Band make_band(int causal, int window_left, int window_right) {
+  Band b;
+  b.lo_off = window_left >= 0 ? -window_left : -kUnbounded;
+  b.hi_off = window_right >= 0 ? window_right : kUnbounded;
+  if (causal && b.hi_off > 0) b.hi_off = 0;
+  if (!causal && window_left < 0 && window_right < 0)
+    b.mode = kBandNone;
+  else if (causal && window_left < 0)
+    b.mode = kBandCausal;  // hi_off == 0 here
+  else
+    b.mode = kBandWindow;
+  return b;
+}
+
 // Everything a forward launch needs besides the tensor maps.
 struct FwdArgs {
-  const float* mask;  // [B, H, ql, kl] or nullptr
+  const void* mask;   // nullptr, or the mask in mask_type's element type
+  int mask_type;      // 0 f32 additive, 1 bf16 additive, 2 bool (uint8, nonzero = visible)
+  long long mask_stride_b, mask_stride_h, mask_stride_q;  // elements; keys contiguous
   void* o;            // bf16 [B, H, ql, d]
   float* lse;         // [B, H, ql]
   int* status;        // device status word (nullable)
   int B, H, Hk, ql, kl, d;
   float scale;
-  int causal;
+  int lo_off, hi_off;
+  int band;  // BandMode
 };
 
 // Tensor maps of a forward launch (3-D, innermost first: d, rows, batch*heads; 128-byte
@@ -47,17 +76,20 @@ struct BwdArgs {
   const void* o;
   const float* lse;
   const void* dO;
-  const float* mask;
+  const void* mask;
+  int mask_type;
+  long long mask_stride_b, mask_stride_h, mask_stride_q;
   void* dq;
   void* dk;
   void* dv;
-  float* lse2;   // workspace [B*H, ql_pad]: L * log2(e), +inf for fully masked rows
+  float* lse2;   // workspace [B*H, ql_pad]: -L * log2(e), -inf for fully masked rows
   float* dvec;   // workspace [B*H, ql_pad]: D = rowsum(dO * O)
   float* dqacc;  // workspace [B*H, ql_pad, d] f32 dQ accumulator
   int* status;
   int B, H, Hk, ql, kl, d, ql_pad;
   float scale;
-  int causal;
+  int lo_off, hi_off;
+  int band;  // BandMode
 };
 
 struct BwdMaps {

@@ -75,6 +75,37 @@ typedef struct fa_params {
 #define FA_ERR_UNSUPPORTED 4    /* the device is not sm_103 or sm_100 family */
 #define FA_ERR_TOO_LARGE 5      /* the problem needs more scratch than fa_train_bwd_noalloc has */
 
+/* Mask element types of fa_options.mask_type. */
+#define FA_MASK_F32 0  /* additive, natural log, float (an entry -inf hides the key) */
+#define FA_MASK_BF16 1 /* additive, natural log, bf16 */
+#define FA_MASK_BOOL 2 /* uint8: nonzero = the key is visible, 0 = hidden */
+
+/* Options beyond the pages' parameter block, for the *_ex entry points.
+ *
+ * Local (sliding-window) attention, the windowed form of the mlx-native SWA tests (sections 7
+ * and 15 of the same page, which build it as an additive -inf mask): with
+ * q_abs = kl - ql + i, key j is hidden from query row i when
+ *   window_left  >= 0 and j < q_abs - window_left, or
+ *   window_right >= 0 and j > q_abs + window_right
+ * (-1 = unbounded on that side). It combines with `causal` (j > q_abs hidden) and the mask.
+ * Kv tiles outside every row's window are neither loaded nor multiplied.
+ *
+ * Masks may be given in any of the FA_MASK_* element types and broadcast over batch, heads
+ * and/or query rows: element (b, h, i, j) is read at
+ *   mask + b*mask_stride_b + h*mask_stride_h + i*mask_stride_q + j      (in elements)
+ * (keys contiguous; a zero stride broadcasts). The dense [B, H, ql, kl] f32 mask of the base
+ * entry points is mask_type FA_MASK_F32 with strides (H*ql*kl, ql*kl, kl). The mask pointer
+ * must be aligned to its element size. */
+typedef struct fa_options {
+  int32_t window_left;   /* -1, or >= 0 */
+  int32_t window_right;  /* -1, or >= 0 */
+  int32_t mask_type;     /* FA_MASK_* (ignored when the mask pointer is NULL) */
+  int32_t reserved;      /* must be 0 */
+  int64_t mask_stride_b; /* >= 0 */
+  int64_t mask_stride_h; /* >= 0 */
+  int64_t mask_stride_q; /* >= 0 */
+} fa_options;
+
 /* Forward: O and L. Page "mlx-native tests/test_flash_attn_train.rs", sections 2-8 (forward
  * parity), function `sdpa_reference_with_logsumexp`.
  *   q, k, v : inputs (bf16, device, 16-byte aligned)
@@ -86,6 +117,14 @@ typedef struct fa_params {
  * A fully masked row gives O = 0 and L = -inf. */
 int fa_train_fwd(const void* q, const void* k, const void* v, const float* mask, void* o,
                  float* lse, const fa_params* p, void* stream);
+
+/* Forward with options (window, mask type and broadcast). opt == NULL gives the base
+ * behaviour (no window; a mask, if any, dense [B, H, ql, kl] f32). Rows whose window and mask
+ * leave no key give O = 0 and L = -inf. Errors as fa_train_fwd; FA_ERR_INVALID also for
+ * window values below -1, an unknown mask type, a nonzero `reserved`, negative strides or a
+ * mask not aligned to its element size. */
+int fa_train_fwd_ex(const void* q, const void* k, const void* v, const void* mask, void* o,
+                    float* lse, const fa_params* p, const fa_options* opt, void* stream);
 
 /* Backward: dQ, dK, dV from the forward's O and L. Same page, sections 10-16 (backward parity),
  * function `sdpa_backward_reference_f32`; the kernel decomposition (a D_i = rowsum(dO * O)
@@ -117,6 +156,12 @@ int fa_profile_enable(int on);
 int fa_profile_read(double* total_ms, int64_t* launches);
 /* Name of a kernel id (static storage). */
 const char* fa_kernel_name(int id);
+
+/* Backward with options; `opt` and `mask` must be those given to the forward that produced
+ * o and lse. opt == NULL gives the base behaviour. */
+int fa_train_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, const void* mask, void* dq, void* dk, void* dv,
+                    const fa_params* p, const fa_options* opt, void* stream);
 
 /* Backward without any device allocation. The pages have no counterpart of this entry point.
  *

@@ -8,7 +8,11 @@ Tolerances (written here, used by every parity test):
         value (7.8e-3 already at |O| in [2, 4)), so that half ulp is added on top. The strict
         mlx-native rule (|O_gpu - bf16(O_ref)| <= 5e-3) is also evaluated and the number of
         elements that miss it by one bf16 ulp is reported, not hidden;
-  * dQ, dK, dV: max |g_gpu - g_ref| <= 2e-2 * max |g_ref| per tensor.
+  * dQ, dK, dV: max |g_gpu - g_ref| <= 2e-2 * max |g_ref| + 1e-4 per tensor. The absolute
+        1e-4 only matters where a gradient vanishes in exact arithmetic: a row whose only
+        visible key is its own (window 0) has P = 1, O = V and dS = dP - D = 0, so the oracle's
+        dQ is exactly 0 while the kernel's dP and D, two f32 dot products of length d, leave a
+        cancellation residue of order d * 2^-24 * |dO| |V| (about 1e-6 at d = 64).
 References are the oracle's unrounded f64 values.
 """
 from __future__ import annotations
@@ -21,6 +25,7 @@ import oracle
 O_ATOL = 5e-3
 L_ATOL = 3e-3
 G_REL = 2e-2
+G_ABS = 1e-4
 
 
 def bf16_ulp(x):
@@ -69,9 +74,9 @@ def check_grad(g_gpu, g_ref, name, label="", scale_ref=None):
     assert not np.isnan(g_gpu).any(), f"{label}: NaN in {name}"
     gmax = float(np.abs(g_ref).max(initial=0.0)) if scale_ref is None else scale_ref
     err = float(np.abs(g_gpu - g_ref).max(initial=0.0))
-    bound = G_REL * gmax
-    assert err <= bound or (gmax == 0.0 and err == 0.0), (
-        f"{label}: {name} max error {err:.3e} > {G_REL} * max|{name}| = {bound:.3e}")
+    bound = G_REL * gmax + G_ABS
+    assert err <= bound, (
+        f"{label}: {name} max error {err:.3e} > {G_REL} * max|{name}| + {G_ABS} = {bound:.3e}")
     return {f"{name}_max_err": err, f"{name}_max_abs": gmax}
 
 
@@ -94,12 +99,13 @@ def run_gpu(w: fa_inputs.Workload, inp: fa_inputs.Inputs, bwd=True):
     import flash_attention_gb300 as fa
 
     d = to_device(inp)
+    win = (w.window_left, w.window_right) if w.windowed else None
     o, lse = fa.attention_fwd(d["q"], d["k"], d["v"], scale=w.scale, causal=w.causal,
-                              mask=d["mask"])
+                              mask=d["mask"], window=win)
     out = {"o": o, "lse": lse}
     if bwd:
         dq, dk, dv = fa.attention_bwd(d["q"], d["k"], d["v"], o, lse, d["do"], scale=w.scale,
-                                      causal=w.causal, mask=d["mask"])
+                                      causal=w.causal, mask=d["mask"], window=win)
         out.update(dq=dq, dk=dk, dv=dv)
     torch.cuda.synchronize()
     assert fa.fa_device_status(True) == fa.FA_OK, "a kernel gave up a bounded wait"
@@ -108,11 +114,12 @@ def run_gpu(w: fa_inputs.Workload, inp: fa_inputs.Inputs, bwd=True):
 
 def oracle_full(w: fa_inputs.Workload, inp: fa_inputs.Inputs, bwd=True):
     q, k, v, do = inp.widened()
-    o, lse = oracle.fwd(q, k, v, inp.mask, scale=w.scale, causal=w.causal)
-    res = {"o": o, "lse": lse}
-    if bwd:
-        dq, dk, dv = oracle.bwd(q, k, v, inp.mask, do, scale=w.scale, causal=w.causal)
-        res.update(dq=dq, dk=dk, dv=dv)
+    with oracle.window(w.window_left, w.window_right):
+        o, lse = oracle.fwd(q, k, v, inp.mask, scale=w.scale, causal=w.causal)
+        res = {"o": o, "lse": lse}
+        if bwd:
+            dq, dk, dv = oracle.bwd(q, k, v, inp.mask, do, scale=w.scale, causal=w.causal)
+            res.update(dq=dq, dk=dk, dv=dv)
     return res
 
 

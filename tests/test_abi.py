@@ -111,3 +111,54 @@ def test_valid_call_without_gpu_fails_cleanly(lib):
         pytest.skip("a GPU is present")
     rc = _fwd(lib, GOOD)
     assert rc in (fa.FA_ERR_CUDA, fa.FA_ERR_UNSUPPORTED)
+
+
+def _fwd_ex(lib, params, opts, mask=None):
+    p = fa.FaParams(**params)
+    return lib.fa_train_fwd_ex(FAKE, FAKE, FAKE, mask, FAKE, FAKE, ctypes.byref(p),
+                               ctypes.byref(opts) if opts is not None else None, None)
+
+
+def _bwd_ex(lib, params, opts, mask=None):
+    p = fa.FaParams(**params)
+    return lib.fa_train_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, mask, FAKE, FAKE, FAKE,
+                               ctypes.byref(p), ctypes.byref(opts) if opts is not None else None,
+                               None)
+
+
+def _opts(**kw):
+    base = dict(window_left=-1, window_right=-1, mask_type=0, reserved=0, mask_stride_b=0,
+                mask_stride_h=0, mask_stride_q=128)
+    base.update(kw)
+    return fa.FaOptions(**base)
+
+
+BAD_OPTIONS = [
+    dict(window_left=-2), dict(window_right=-5), dict(mask_type=3), dict(mask_type=-1),
+    dict(reserved=1), dict(mask_stride_b=-1), dict(mask_stride_h=-4), dict(mask_stride_q=-128),
+]
+
+
+@pytest.mark.parametrize("kw", BAD_OPTIONS, ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()))
+def test_bad_options_rejected(lib, kw):
+    assert _fwd_ex(lib, GOOD, _opts(**kw), mask=FAKE) == fa.FA_ERR_INVALID
+    assert _bwd_ex(lib, GOOD, _opts(**kw), mask=FAKE) == fa.FA_ERR_INVALID
+
+
+def test_mask_alignment_follows_its_element_type(lib):
+    # f32 needs 4-byte alignment, bf16 2, bool 1
+    assert _fwd_ex(lib, GOOD, _opts(mask_type=0), mask=FAKE + 2) == fa.FA_ERR_INVALID
+    assert _fwd_ex(lib, GOOD, _opts(mask_type=1), mask=FAKE + 1) == fa.FA_ERR_INVALID
+    import torch
+
+    if not torch.cuda.is_available():
+        # checks pass, then the device check fails cleanly
+        assert _fwd_ex(lib, GOOD, _opts(mask_type=2), mask=FAKE + 1) in (fa.FA_ERR_CUDA,
+                                                                          fa.FA_ERR_UNSUPPORTED)
+        assert _fwd_ex(lib, GOOD, _opts(window_left=0, window_right=0)) in (
+            fa.FA_ERR_CUDA, fa.FA_ERR_UNSUPPORTED)
+
+
+def test_options_struct_layout():
+    assert ctypes.sizeof(fa.FaOptions) == 40
+    assert fa.FaOptions.mask_stride_b.offset == 16

@@ -91,14 +91,23 @@ def _sample_rows(w, rng, n=48):
     return np.array(sorted(rows), np.int64)
 
 
-@pytest.mark.parametrize("idx", [2, 3, 4], ids=["train_d64", "gqa_d128_4k", "rect_d256"])
-def test_full_size_sampled(idx):
-    w = fa_inputs.WORKLOADS[idx]
+FULL_SIZE = ["train_d64", "gqa_d128_4k", "rect_d256", "swa_d128_16k"]
+
+
+@pytest.mark.parametrize("name", FULL_SIZE)
+def test_full_size_sampled(name):
+    w = fa_inputs.BY_NAME[name]
+    idx = fa_inputs.WORKLOADS.index(w)
     inp = fa_inputs.make_inputs(w)
     gpu = parity.run_gpu(w, inp)
     q, k, v, do = inp.widened()
     rng = np.random.default_rng(1234 + idx)
     rows = _sample_rows(w, rng)
+    with oracle.window(w.window_left, w.window_right):
+        _check_sampled(w, inp, gpu, q, k, v, do, rows, rng)
+
+
+def _check_sampled(w, inp, gpu, q, k, v, do, rows, rng):
     o_r, l_r = oracle.fwd_rows(q, k, v, inp.mask, scale=w.scale, causal=w.causal, rows=rows)
     d = w.head_dim
     parity.check_o(gpu["o"].reshape(-1, d)[rows], o_r, w.name)

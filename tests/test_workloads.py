@@ -1,0 +1,52 @@
+"""Host-side workload bookkeeping: visible (query, key) pair counts and the FLOP rule."""
+import itertools
+
+import pytest
+
+import fa_inputs
+
+
+def brute_visible(w):
+    off = w.kl - w.ql
+    n = 0
+    for i, j in itertools.product(range(w.ql), range(w.kl)):
+        qa = off + i
+        if w.causal and j > qa:
+            continue
+        if w.window_left >= 0 and j < qa - w.window_left:
+            continue
+        if w.window_right >= 0 and j > qa + w.window_right:
+            continue
+        n += 1
+    return n
+
+
+SHAPES = [(17, 17), (9, 30), (30, 9), (1, 40), (40, 1)]
+WINDOWS = [(-1, -1), (0, -1), (3, -1), (-1, 0), (-1, 4), (2, 5), (0, 0), (100, 100)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("ql,kl", SHAPES)
+@pytest.mark.parametrize("wl,wr", WINDOWS)
+def test_visible_pairs_brute_force(causal, ql, kl, wl, wr):
+    w = fa_inputs.Workload("t", 1, 1, 1, ql, kl, 64, 0.125, causal, window_left=wl,
+                           window_right=wr)
+    assert w.visible_pairs() == brute_visible(w)
+
+
+def test_flop_rule():
+    w = fa_inputs.BY_NAME["gqa_d128_4k"]
+    base = w.batch * w.n_heads * w.ql * w.kl * w.head_dim
+    assert w.flops() == (4.0 * base * 0.5, 10.0 * base * 0.5)  # causal counted as half
+    s = fa_inputs.BY_NAME["swa_d128_16k"]
+    # a window has no halving rule: the exact visible fraction is counted
+    assert s.flops() == s.flops(exact=True)
+    rows_full = s.kl - s.window_left  # rows that see a full 4096-key window
+    pairs = rows_full * (s.window_left + 1) + sum(range(1, s.window_left + 1))
+    assert s.visible_pairs() == pairs
+
+
+def test_existing_seeds_unchanged():
+    # appending workloads must not move the seeds of the existing ones
+    names = [w.name for w in fa_inputs.WORKLOADS[:5]]
+    assert names == ["tiny_gqa_d64", "masked_d256", "train_d64", "gqa_d128_4k", "rect_d256"]
