@@ -41,6 +41,9 @@ MUTATIONS = {
     "dq_no_scale": 11,
     "d_from_do_only": 12,
     "window_off_by_one": 13,
+    "sink_scaled": 14,
+    "dsink_sign": 15,
+    "v_stride_d": 16,
 }
 
 
@@ -66,18 +69,20 @@ def _load():
             f = ctypes.c_void_p
             i = ctypes.c_int
             d = ctypes.c_double
-            lib.fa_oracle_fwd_rows.argtypes = [f, f, f, f, i, i, i, i, i, i, d, i, f,
+            lib.fa_oracle_fwd_rows.argtypes = [f, f, f, f, i, i, i, i, i, i, i, d, i, f,
                                                ctypes.c_long, i, f, f, i]
-            lib.fa_oracle_bwd_q_rows.argtypes = [f, f, f, f, f, i, i, i, i, i, i, d, i, f,
+            lib.fa_oracle_bwd_q_rows.argtypes = [f, f, f, f, f, i, i, i, i, i, i, i, d, i, f,
                                                  ctypes.c_long, f, i]
-            lib.fa_oracle_bwd_kv_rows.argtypes = [f, f, f, f, f, i, i, i, i, i, i, d, i, i, i,
-                                                  f, i, f, f, i]
-            lib.fa_oracle_bwd.argtypes = [f, f, f, f, f, i, i, i, i, i, i, d, i, f, f, f, i]
+            lib.fa_oracle_bwd_kv_rows.argtypes = [f, f, f, f, f, i, i, i, i, i, i, i, d, i, i,
+                                                  i, f, i, f, f, i]
+            lib.fa_oracle_bwd.argtypes = [f, f, f, f, f, i, i, i, i, i, i, i, d, i, f, f, f, i]
+            lib.fa_oracle_dsinks.argtypes = [f, f, f, f, f, i, i, i, i, i, i, i, d, i, f, i]
             lib.fa_oracle_set_mutation.argtypes = [i]
             lib.fa_oracle_set_window.argtypes = [i, i]
+            lib.fa_oracle_set_sinks.argtypes = [f]
             lib.fa_oracle_get_mutation.restype = i
             for fn in (lib.fa_oracle_fwd_rows, lib.fa_oracle_bwd_q_rows,
-                       lib.fa_oracle_bwd_kv_rows, lib.fa_oracle_bwd):
+                       lib.fa_oracle_bwd_kv_rows, lib.fa_oracle_bwd, lib.fa_oracle_dsinks):
                 fn.restype = i
             _lib = lib
     return _lib
@@ -96,14 +101,17 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
-def _shape(q, k):
+def _shape(q, k, v):
+    """(B, H, Hk, ql, kl, d, dv): d from q/k, dv (the value head dim) from v."""
     B, H, ql, d = q.shape
     Bk, Hk, kl, dk = k.shape
     if B != Bk or d != dk:
         raise ValueError("q and k disagree on batch or head_dim")
+    if tuple(v.shape[:3]) != (B, Hk, kl):
+        raise ValueError("v must be [B, Hk, kl, dv]")
     if H % Hk:
         raise ValueError("n_heads must be a multiple of n_kv_heads")
-    return B, H, Hk, ql, kl, d
+    return B, H, Hk, ql, kl, d, int(v.shape[3])
 
 
 class window:
@@ -120,6 +128,23 @@ class window:
 
     def __exit__(self, *exc):
         _load().fa_oracle_set_window(-1, -1)
+        return False
+
+
+class sinks:
+    """Context manager: per-head sink logits (natural-log units, shape [H]) for the oracle calls
+    inside it; None means no sinks. The row normaliser gains exp(sink_h); the sink carries no
+    value."""
+
+    def __init__(self, values):
+        self.values = None if values is None else np.ascontiguousarray(values, np.float32)
+
+    def __enter__(self):
+        _load().fa_oracle_set_sinks(_ptr(self.values))
+        return self
+
+    def __exit__(self, *exc):
+        _load().fa_oracle_set_sinks(None)
         return False
 
 
@@ -153,19 +178,20 @@ def fwd_rows(q, k, v, mask=None, *, scale, causal, rows=None, base2=False, nthre
     in [B,H,ql,(d)] shape)."""
     q, k, v = _f32(q), _f32(k), _f32(v)
     mask = None if mask is None else _f32(mask)
-    B, H, Hk, ql, kl, d = _shape(q, k)
+    B, H, Hk, ql, kl, d, dv = _shape(q, k, v)
     full = rows is None
     r = None if full else np.ascontiguousarray(rows, dtype=np.int64)
     n = B * H * ql if full else len(r)
-    o = np.empty((n, d), np.float64)
+    o = np.empty((n, dv), np.float64)
     lse = np.empty((n,), np.float64)
     rc = _load().fa_oracle_fwd_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), B, H, Hk, ql, kl, d,
-                                    float(scale), int(bool(causal)), _ptr(r), n, int(bool(base2)),
-                                    _ptr(o), _ptr(lse), nthreads or default_threads())
+                                    dv, float(scale), int(bool(causal)), _ptr(r), n,
+                                    int(bool(base2)), _ptr(o), _ptr(lse),
+                                    nthreads or default_threads())
     if rc:
         raise ValueError(f"oracle fwd failed ({rc})")
     if full:
-        return o.reshape(B, H, ql, d), lse.reshape(B, H, ql)
+        return o.reshape(B, H, ql, dv), lse.reshape(B, H, ql)
     return o, lse
 
 
@@ -173,13 +199,13 @@ def bwd_q_rows(q, k, v, mask, do, *, scale, causal, rows=None, nthreads=None):
     """dQ of the listed flat query rows (None: all rows, shaped [B,H,ql,d])."""
     q, k, v, do = _f32(q), _f32(k), _f32(v), _f32(do)
     mask = None if mask is None else _f32(mask)
-    B, H, Hk, ql, kl, d = _shape(q, k)
+    B, H, Hk, ql, kl, d, dv = _shape(q, k, v)
     full = rows is None
     r = None if full else np.ascontiguousarray(rows, dtype=np.int64)
     n = B * H * ql if full else len(r)
     dq = np.empty((n, d), np.float64)
     rc = _load().fa_oracle_bwd_q_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(do), B, H, Hk,
-                                      ql, kl, d, float(scale), int(bool(causal)), _ptr(r), n,
+                                      ql, kl, d, dv, float(scale), int(bool(causal)), _ptr(r), n,
                                       _ptr(dq), nthreads or default_threads())
     if rc:
         raise ValueError(f"oracle bwd_q_rows failed ({rc})")
@@ -187,33 +213,48 @@ def bwd_q_rows(q, k, v, mask, do, *, scale, causal, rows=None, nthreads=None):
 
 
 def bwd_kv_rows(q, k, v, mask, do, *, scale, causal, b, kh, js, nthreads=None):
-    """dK and dV rows js of kv head kh in batch b: two arrays [len(js), d]."""
+    """dK and dV rows js of kv head kh in batch b: arrays [len(js), d] and [len(js), dv]."""
     q, k, v, do = _f32(q), _f32(k), _f32(v), _f32(do)
     mask = None if mask is None else _f32(mask)
-    B, H, Hk, ql, kl, d = _shape(q, k)
+    B, H, Hk, ql, kl, d, dvd = _shape(q, k, v)
     jarr = np.ascontiguousarray(js, dtype=np.int32)
     dk = np.empty((len(jarr), d), np.float64)
-    dv = np.empty((len(jarr), d), np.float64)
+    dv = np.empty((len(jarr), dvd), np.float64)
     rc = _load().fa_oracle_bwd_kv_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(do), B, H,
-                                       Hk, ql, kl, d, float(scale), int(bool(causal)), int(b),
-                                       int(kh), _ptr(jarr), len(jarr), _ptr(dk), _ptr(dv),
-                                       nthreads or default_threads())
+                                       Hk, ql, kl, d, dvd, float(scale), int(bool(causal)),
+                                       int(b), int(kh), _ptr(jarr), len(jarr), _ptr(dk),
+                                       _ptr(dv), nthreads or default_threads())
     if rc:
         raise ValueError(f"oracle bwd_kv_rows failed ({rc})")
     return dk, dv
 
 
 def bwd(q, k, v, mask, do, *, scale, causal, nthreads=None):
-    """Full backward: (dQ [B,H,ql,d], dK [B,Hk,kl,d], dV [B,Hk,kl,d]) in f64."""
+    """Full backward: (dQ [B,H,ql,d], dK [B,Hk,kl,d], dV [B,Hk,kl,dv]) in f64."""
     q, k, v, do = _f32(q), _f32(k), _f32(v), _f32(do)
     mask = None if mask is None else _f32(mask)
-    B, H, Hk, ql, kl, d = _shape(q, k)
+    B, H, Hk, ql, kl, d, dvd = _shape(q, k, v)
     dq = np.empty((B, H, ql, d), np.float64)
     dk = np.empty((B, Hk, kl, d), np.float64)
-    dv = np.empty((B, Hk, kl, d), np.float64)
+    dv = np.empty((B, Hk, kl, dvd), np.float64)
     rc = _load().fa_oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(do), B, H, Hk, ql, kl,
-                               d, float(scale), int(bool(causal)), _ptr(dq), _ptr(dk), _ptr(dv),
-                               nthreads or default_threads())
+                               d, dvd, float(scale), int(bool(causal)), _ptr(dq), _ptr(dk),
+                               _ptr(dv), nthreads or default_threads())
     if rc:
         raise ValueError(f"oracle bwd failed ({rc})")
     return dq, dk, dv
+
+
+def dsinks(q, k, v, mask, do, *, scale, causal, nthreads=None):
+    """Gradient of sum(O * dO) with respect to the sink logits of the enclosing `sinks(...)`
+    block: [H] f64, dsink_h = -sum over batch and rows of exp(sink_h - L) * D."""
+    q, k, v, do = _f32(q), _f32(k), _f32(v), _f32(do)
+    mask = None if mask is None else _f32(mask)
+    B, H, Hk, ql, kl, d, dvd = _shape(q, k, v)
+    out = np.empty((H,), np.float64)
+    rc = _load().fa_oracle_dsinks(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(do), B, H, Hk, ql,
+                                  kl, d, dvd, float(scale), int(bool(causal)), _ptr(out),
+                                  nthreads or default_threads())
+    if rc:
+        raise ValueError(f"oracle dsinks failed ({rc}); is a sinks(...) block active?")
+    return out

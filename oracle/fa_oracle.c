@@ -35,6 +35,24 @@
  *     corner is unpinned by the pages because the two disagree);
  *   - the mask is natural-log additive, shape [B, H, ql, kl], an entry -inf hides the key.
  *
+ * Attention sinks (page "nuvec-core tests/fast.rs", `attention_kernels_match_the_fallback`,
+ * where the fused attention takes an optional `sinks` array of shape [n_heads]): the page
+ * shows only the shape, so the plainest reading is taken: sink_h is one extra natural-log
+ * logit of every row of query head h that enters the softmax normaliser but carries no
+ * value and is not scaled, i.e.
+ *
+ *   L_i = log( exp(sink_h) + sum_j exp(s_ij) ),   O_i = sum_j exp(s_ij - L_i) v_j
+ *
+ * so a row that sees no key has O = 0 and L = sink_h. The backward formulas above hold as
+ * written (L carries the sink), and the sink's own gradient follows from the definition
+ * (its score has no value, so its dP is 0 and dS_sink = P_sink (0 - D_i)):
+ *
+ *   dsink_h = - sum_b sum_i exp(sink_h - L_i) D_i
+ *
+ * Value head dimension (same page: its shapes list (D, Dv) pairs with Dv != D): q and k have
+ * d columns, v, O, dO, dV have dv columns; every formula above is unchanged, the QK dot
+ * products run over d and the dO.v, dO.O dot products over dv.
+ *
  * Local (sliding-window) attention, the windowed form of the mlx-native SWA tests (sections 7
  * and 15, which build it as an additive mask): with window_left = wl >= 0 a key j is hidden
  * when j < q_abs - wl, with window_right = wr >= 0 when j > q_abs + wr; -1 leaves that side
@@ -45,8 +63,9 @@
  * sentinel -FLT_MAX/2, p = exp2(s - max), L = max*ln(2) + ln(sum p), O = sum (p / safe_sum) v
  * with safe_sum = 1 when the sum is 0. Both modes must agree to rounding on any input.
  *
- * Layouts (all contiguous, row-major): q, dO, O, dQ [B, H, ql, d]; k, v, dK, dV [B, Hk, kl, d];
- * L [B, H, ql]; mask [B, H, ql, kl] or NULL.
+ * Layouts (all contiguous, row-major): q, dQ [B, H, ql, d]; O, dO [B, H, ql, dv];
+ * k, dK [B, Hk, kl, d]; v, dV [B, Hk, kl, dv]; L [B, H, ql]; mask [B, H, ql, kl] or NULL;
+ * sinks [H] or NULL (set with fa_oracle_set_sinks).
  *
  * A mutation switch (fa_oracle_set_mutation) plants one known mistake at a time. It is off (0)
  * by default and exists only so that the tests can show that each planted mistake fails one
@@ -60,11 +79,12 @@
 #include <string.h>
 
 typedef struct {
-  int B, H, Hk, ql, kl, d;
+  int B, H, Hk, ql, kl, d, dv; /* d: q/k head dim; dv: v/O/dO head dim */
   double scale;
   int causal;
   int wl, wr; /* local window around q_abs = kl - ql + i: -1 = unbounded on that side */
   const float *q, *k, *v, *mask, *dO;
+  const float *sinks; /* [H] natural-log sink logits, or NULL */
 } prob_t;
 
 /* Planted mistakes (tests only). 0 = none. */
@@ -83,6 +103,9 @@ enum {
   MUT_DQ_NO_SCALE = 11,    /* dQ without the scale factor */
   MUT_D_FROM_DO_ONLY = 12, /* D_i = sum dO (O dropped) */
   MUT_WINDOW_OFF_BY_ONE = 13, /* left window bound one key too narrow */
+  MUT_SINK_SCALED = 14,    /* sink logit multiplied by the score scale */
+  MUT_DSINK_SIGN = 15,     /* dsink without its minus sign */
+  MUT_V_STRIDE_D = 16,     /* v rows addressed with the q/k head dim */
 };
 static int g_mutation = 0;
 
@@ -94,6 +117,21 @@ static inline size_t q_index(const prob_t *p, int b, int h, int i) {
 }
 static inline size_t kv_index(const prob_t *p, int b, int kh, int j) {
   return (((size_t)b * p->Hk + kh) * p->kl + j) * (size_t)p->d;
+}
+/* row j of v (dv columns), and row i of O / dO (dv columns) */
+static inline size_t v_index(const prob_t *p, int b, int kh, int j) {
+  const size_t w = (g_mutation == MUT_V_STRIDE_D) ? (size_t)p->d : (size_t)p->dv;
+  return (((size_t)b * p->Hk + kh) * p->kl + j) * w;
+}
+static inline size_t o_index(const prob_t *p, int b, int h, int i) {
+  return (((size_t)b * p->H + h) * p->ql + i) * (size_t)p->dv;
+}
+/* the sink logit of head h in natural-log units, or -inf without sinks */
+static inline double sink_logit(const prob_t *p, int h) {
+  if (!p->sinks) return -INFINITY;
+  double s = (double)p->sinks[h];
+  if (g_mutation == MUT_SINK_SCALED) s *= p->scale;
+  return s;
 }
 static inline int kv_head(const prob_t *p, int h) {
   if (g_mutation == MUT_GQA_MODULO) return h % p->Hk;
@@ -130,21 +168,23 @@ static void row_scores(const prob_t *p, int b, int h, int i, double *s) {
   }
 }
 
-/* Forward of one row, natural-log mode: L and O[d] from the scores. */
+/* Forward of one row, natural-log mode: L and O[dv] from the scores (and the head's sink). */
 static double row_forward_nat(const prob_t *p, int b, int h, int i, const double *s, double *o) {
+  (void)i;
   const int kh = kv_head(p, h);
-  double m = -INFINITY;
+  const double sink = sink_logit(p, h);
+  double m = sink;
   for (int j = 0; j < p->kl; ++j) if (s[j] > m) m = s[j];
-  for (int c = 0; c < p->d; ++c) o[c] = 0.0;
-  if (m == -INFINITY) return -INFINITY; /* fully masked row: O = 0, L = -inf */
-  double z = 0.0;
+  for (int c = 0; c < p->dv; ++c) o[c] = 0.0;
+  if (m == -INFINITY) return -INFINITY; /* fully masked row, no sink: O = 0, L = -inf */
+  double z = exp(sink - m);             /* the sink's share of the normaliser (0 without) */
   for (int j = 0; j < p->kl; ++j) z += exp(s[j] - m);
   for (int j = 0; j < p->kl; ++j) {
     if (s[j] == -INFINITY) continue;
     double w = exp(s[j] - m);
     if (g_mutation != MUT_NO_NORMALISE) w /= z;
-    const float *vj = p->v + kv_index(p, b, kh, j);
-    for (int c = 0; c < p->d; ++c) o[c] += w * (double)vj[c];
+    const float *vj = p->v + v_index(p, b, kh, j);
+    for (int c = 0; c < p->dv; ++c) o[c] += w * (double)vj[c];
   }
   if (g_mutation == MUT_L_NO_MAX) return log(z);
   return m + log(z);
@@ -172,17 +212,19 @@ static double row_forward_base2(const prob_t *p, int b, int h, int i, double *o)
     if (!visible(p, i, j)) s2[j] = -INFINITY;
   }
   double mx = -(double)FLT_MAX / 2.0; /* finite sentinel */
+  const double sink2 = sink_logit(p, h) * LOG2E; /* -inf without sinks */
+  if (sink2 > mx) mx = sink2;
   for (int j = 0; j < p->kl; ++j) if (s2[j] > mx) mx = s2[j];
-  double sum = 0.0;
+  double sum = exp2(sink2 - mx);
   for (int j = 0; j < p->kl; ++j) { s2[j] = exp2(s2[j] - mx); sum += s2[j]; }
   double lse = (g_mutation == MUT_L_NO_MAX) ? log(sum) : mx * LN2 + log(sum);
   double safe = (sum == 0.0) ? 1.0 : sum;
   if (g_mutation == MUT_NO_NORMALISE) safe = 1.0;
-  for (int c = 0; c < p->d; ++c) o[c] = 0.0;
+  for (int c = 0; c < p->dv; ++c) o[c] = 0.0;
   for (int j = 0; j < p->kl; ++j) {
-    const float *vj = p->v + kv_index(p, b, kh, j);
+    const float *vj = p->v + v_index(p, b, kh, j);
     double w = s2[j] / safe;
-    for (int c = 0; c < p->d; ++c) o[c] += w * (double)vj[c];
+    for (int c = 0; c < p->dv; ++c) o[c] += w * (double)vj[c];
   }
   free(s2);
   return lse;
@@ -231,18 +273,26 @@ static void parallel_for(long ntasks, int nthreads, void (*fn)(void *, long, int
 }
 
 static int g_wl = -1, g_wr = -1; /* window of the next calls (fa_oracle_set_window) */
+static const float *g_sinks = NULL; /* sinks of the next calls (fa_oracle_set_sinks) */
 
 void fa_oracle_set_window(int wl, int wr) { g_wl = wl; g_wr = wr; }
+/* [H] sink logits read by the following calls (the caller keeps the array alive), or NULL. */
+void fa_oracle_set_sinks(const float *sinks) { g_sinks = sinks; }
 
 static prob_t make_prob(const float *q, const float *k, const float *v, const float *mask,
-                        const float *dO, int B, int H, int Hk, int ql, int kl, int d,
+                        const float *dO, int B, int H, int Hk, int ql, int kl, int d, int dv,
                         double scale, int causal) {
   prob_t p;
-  p.B = B; p.H = H; p.Hk = Hk; p.ql = ql; p.kl = kl; p.d = d;
+  p.B = B; p.H = H; p.Hk = Hk; p.ql = ql; p.kl = kl; p.d = d; p.dv = dv;
   p.scale = scale; p.causal = causal;
   p.wl = g_wl; p.wr = g_wr;
   p.q = q; p.k = k; p.v = v; p.mask = mask; p.dO = dO;
+  p.sinks = g_sinks;
   return p;
+}
+
+static int bad_sizes(int B, int H, int Hk, int ql, int kl, int d, int dv) {
+  return B <= 0 || H <= 0 || Hk <= 0 || ql <= 0 || kl <= 0 || d <= 0 || dv <= 0 || H % Hk;
 }
 
 /* ------------------------------------------------------------------ forward, by rows */
@@ -261,7 +311,7 @@ static void fwd_task(void *vctx, long t, int worker) {
   int i = (int)(r % p->ql);
   int h = (int)((r / p->ql) % p->H);
   int b = (int)(r / ((int64_t)p->ql * p->H));
-  double *o = c->o + (size_t)t * p->d;
+  double *o = c->o + (size_t)t * p->dv;
   if (c->base2) {
     c->lse[t] = row_forward_base2(p, b, h, i, o);
   } else {
@@ -272,14 +322,14 @@ static void fwd_task(void *vctx, long t, int worker) {
   }
 }
 
-/* O and L of the listed rows (rows == NULL: all B*H*ql rows in order). Output o[nrows*d],
+/* O and L of the listed rows (rows == NULL: all B*H*ql rows in order). Output o[nrows*dv],
  * lse[nrows]. Returns 0, or -1 on bad sizes. */
 int fa_oracle_fwd_rows(const float *q, const float *k, const float *v, const float *mask,
-                       int B, int H, int Hk, int ql, int kl, int d, double scale, int causal,
-                       const int64_t *rows, long nrows, int base2, double *o, double *lse,
-                       int nthreads) {
-  if (B <= 0 || H <= 0 || Hk <= 0 || ql <= 0 || kl <= 0 || d <= 0 || H % Hk) return -1;
-  prob_t p = make_prob(q, k, v, mask, NULL, B, H, Hk, ql, kl, d, scale, causal);
+                       int B, int H, int Hk, int ql, int kl, int d, int dv, double scale,
+                       int causal, const int64_t *rows, long nrows, int base2, double *o,
+                       double *lse, int nthreads) {
+  if (bad_sizes(B, H, Hk, ql, kl, d, dv)) return -1;
+  prob_t p = make_prob(q, k, v, mask, NULL, B, H, Hk, ql, kl, d, dv, scale, causal);
   fwd_ctx c = {&p, rows, o, lse, base2};
   parallel_for(nrows, nthreads, fwd_task, &c);
   return 0;
@@ -287,9 +337,10 @@ int fa_oracle_fwd_rows(const float *q, const float *k, const float *v, const flo
 
 /* ------------------------------------------------------------------ backward pieces */
 
-/* Everything the backward needs about one query row: P row (kl), dP row (kl), D. */
+/* Everything the backward needs about one query row: P row (kl), dS row (kl), O, L and D. */
 typedef struct {
-  double *s, *o, *pr, *ds; /* scores, O row, P row, dS row */
+  double *s, *o, *pr, *ds; /* scores, O row (dv), P row, dS row */
+  double L, D;
 } rowbuf;
 
 static rowbuf rowbuf_new(const prob_t *p) {
@@ -297,28 +348,32 @@ static rowbuf rowbuf_new(const prob_t *p) {
   r.s = (double *)malloc(sizeof(double) * (size_t)p->kl);
   r.pr = (double *)malloc(sizeof(double) * (size_t)p->kl);
   r.ds = (double *)malloc(sizeof(double) * (size_t)p->kl);
-  r.o = (double *)malloc(sizeof(double) * (size_t)p->d);
+  r.o = (double *)malloc(sizeof(double) * (size_t)p->dv);
+  r.L = 0.0;
+  r.D = 0.0;
   return r;
 }
 static void rowbuf_free(rowbuf *r) { free(r->s); free(r->pr); free(r->ds); free(r->o); }
 
-/* Fills r.pr with the P row and r.ds with the dS row of query row (b, h, i). */
+/* Fills r.pr with the P row, r.ds with the dS row, r.L and r.D of query row (b, h, i). */
 static void row_backward_prep(const prob_t *p, int b, int h, int i, rowbuf *r) {
   const int kh = kv_head(p, h);
   row_scores(p, b, h, i, r->s);
   double L = row_forward_nat(p, b, h, i, r->s, r->o);
-  const float *doi = p->dO + q_index(p, b, h, i);
+  const float *doi = p->dO + o_index(p, b, h, i);
   double D = 0.0;
-  for (int c = 0; c < p->d; ++c)
+  for (int c = 0; c < p->dv; ++c)
     D += (double)doi[c] * ((g_mutation == MUT_D_FROM_DO_ONLY) ? 1.0 : r->o[c]);
   for (int j = 0; j < p->kl; ++j) {
     double P = (r->s[j] == -INFINITY || L == -INFINITY) ? 0.0 : exp(r->s[j] - L);
-    const float *vj = p->v + kv_index(p, b, kh, j);
+    const float *vj = p->v + v_index(p, b, kh, j);
     double dP = 0.0;
-    for (int c = 0; c < p->d; ++c) dP += (double)doi[c] * (double)vj[c];
+    for (int c = 0; c < p->dv; ++c) dP += (double)doi[c] * (double)vj[c];
     r->pr[j] = P;
     r->ds[j] = (g_mutation == MUT_DS_NO_D) ? P * dP : P * (dP - D);
   }
+  r->L = L;
+  r->D = D;
 }
 
 typedef struct {
@@ -352,11 +407,11 @@ static void dq_task(void *vctx, long t, int worker) {
 
 /* dQ of the listed query rows (rows == NULL: all). Output dq[nrows*d]. */
 int fa_oracle_bwd_q_rows(const float *q, const float *k, const float *v, const float *mask,
-                         const float *dO, int B, int H, int Hk, int ql, int kl, int d,
+                         const float *dO, int B, int H, int Hk, int ql, int kl, int d, int dv,
                          double scale, int causal, const int64_t *rows, long nrows, double *dq,
                          int nthreads) {
-  if (B <= 0 || H <= 0 || Hk <= 0 || ql <= 0 || kl <= 0 || d <= 0 || H % Hk) return -1;
-  prob_t p = make_prob(q, k, v, mask, dO, B, H, Hk, ql, kl, d, scale, causal);
+  if (bad_sizes(B, H, Hk, ql, kl, d, dv)) return -1;
+  prob_t p = make_prob(q, k, v, mask, dO, B, H, Hk, ql, kl, d, dv, scale, causal);
   dq_ctx c = {&p, rows, dq};
   parallel_for(nrows, nthreads, dq_task, &c);
   return 0;
@@ -369,7 +424,7 @@ typedef struct {
   int b, kh;
   const int32_t *js;
   int nj;
-  double *acc; /* [nworkers][2][nj][d] */
+  double *acc; /* [nworkers][nj * (d + dv)]: dK rows, then dV rows */
   int nworkers;
 } dkv_ctx;
 
@@ -383,8 +438,8 @@ static void dkv_task(void *vctx, long t, int worker) {
   rowbuf rb = rowbuf_new(p);
   row_backward_prep(p, c->b, h, i, &rb);
   const float *qi = p->q + q_index(p, c->b, h, i);
-  const float *doi = p->dO + q_index(p, c->b, h, i);
-  double *dk = c->acc + (size_t)worker * 2 * c->nj * p->d;
+  const float *doi = p->dO + o_index(p, c->b, h, i);
+  double *dk = c->acc + (size_t)worker * c->nj * (p->d + p->dv);
   double *dv = dk + (size_t)c->nj * p->d;
   for (int n = 0; n < c->nj; ++n) {
     int j = c->js[n];
@@ -393,59 +448,96 @@ static void dkv_task(void *vctx, long t, int worker) {
     const float *kj = p->k + kv_index(p, c->b, c->kh, j);
     const float *src = (g_mutation == MUT_DK_USES_K) ? kj : qi;
     const double pv = (g_mutation == MUT_DV_USES_DS) ? ds : P;
-    for (int cc = 0; cc < p->d; ++cc) {
-      dk[(size_t)n * p->d + cc] += p->scale * ds * (double)src[cc];
-      dv[(size_t)n * p->d + cc] += pv * (double)doi[cc];
-    }
+    for (int cc = 0; cc < p->d; ++cc) dk[(size_t)n * p->d + cc] += p->scale * ds * (double)src[cc];
+    for (int cc = 0; cc < p->dv; ++cc) dv[(size_t)n * p->dv + cc] += pv * (double)doi[cc];
   }
   rowbuf_free(&rb);
 }
 
-/* dK and dV rows js[0..nj) of kv head kh in batch b. Outputs dk[nj*d], dv[nj*d]. */
+/* dK and dV rows js[0..nj) of kv head kh in batch b. Outputs dk[nj*d], dv[nj*dv]. */
 int fa_oracle_bwd_kv_rows(const float *q, const float *k, const float *v, const float *mask,
-                          const float *dO, int B, int H, int Hk, int ql, int kl, int d,
+                          const float *dO, int B, int H, int Hk, int ql, int kl, int d, int dv,
                           double scale, int causal, int b, int kh, const int32_t *js, int nj,
-                          double *dk, double *dv, int nthreads) {
-  if (B <= 0 || H <= 0 || Hk <= 0 || ql <= 0 || kl <= 0 || d <= 0 || H % Hk) return -1;
+                          double *dk, double *dvo, int nthreads) {
+  if (bad_sizes(B, H, Hk, ql, kl, d, dv)) return -1;
   if (b < 0 || b >= B || kh < 0 || kh >= Hk) return -1;
   for (int n = 0; n < nj; ++n) if (js[n] < 0 || js[n] >= kl) return -1;
-  prob_t p = make_prob(q, k, v, mask, dO, B, H, Hk, ql, kl, d, scale, causal);
+  prob_t p = make_prob(q, k, v, mask, dO, B, H, Hk, ql, kl, d, dv, scale, causal);
   const int G = H / Hk;
   long ntasks = (long)G * ql;
   int nw = nthreads < 1 ? 1 : nthreads;
   if (nw > ntasks) nw = (int)ntasks;
+  const size_t per = (size_t)nj * (d + dv);
   dkv_ctx c;
   c.p = &p; c.b = b; c.kh = kh; c.js = js; c.nj = nj; c.nworkers = nw;
-  c.acc = (double *)calloc((size_t)nw * 2 * nj * d, sizeof(double));
+  c.acc = (double *)calloc((size_t)nw * per, sizeof(double));
   if (!c.acc) return -2;
   parallel_for(ntasks, nw, dkv_task, &c);
-  for (size_t e = 0; e < (size_t)nj * d; ++e) { dk[e] = 0.0; dv[e] = 0.0; }
+  for (size_t e = 0; e < (size_t)nj * d; ++e) dk[e] = 0.0;
+  for (size_t e = 0; e < (size_t)nj * dv; ++e) dvo[e] = 0.0;
   for (int w = 0; w < nw; ++w) {
-    const double *a = c.acc + (size_t)w * 2 * nj * d;
-    for (size_t e = 0; e < (size_t)nj * d; ++e) {
-      dk[e] += a[e];
-      dv[e] += a[(size_t)nj * d + e];
-    }
+    const double *a = c.acc + (size_t)w * per;
+    for (size_t e = 0; e < (size_t)nj * d; ++e) dk[e] += a[e];
+    for (size_t e = 0; e < (size_t)nj * dv; ++e) dvo[e] += a[(size_t)nj * d + e];
   }
   free(c.acc);
   return 0;
 }
 
-/* Full backward: dq [B,H,ql,d], dk and dv [B,Hk,kl,d]. */
+/* Full backward: dq [B,H,ql,d], dk [B,Hk,kl,d] and dv [B,Hk,kl,dv]. */
 int fa_oracle_bwd(const float *q, const float *k, const float *v, const float *mask,
-                  const float *dO, int B, int H, int Hk, int ql, int kl, int d, double scale,
-                  int causal, double *dq, double *dk, double *dv, int nthreads) {
-  int rc = fa_oracle_bwd_q_rows(q, k, v, mask, dO, B, H, Hk, ql, kl, d, scale, causal, NULL,
+                  const float *dO, int B, int H, int Hk, int ql, int kl, int d, int dv,
+                  double scale, int causal, double *dq, double *dk, double *dvo, int nthreads) {
+  int rc = fa_oracle_bwd_q_rows(q, k, v, mask, dO, B, H, Hk, ql, kl, d, dv, scale, causal, NULL,
                                 (long)B * H * ql, dq, nthreads);
   if (rc) return rc;
   int32_t *js = (int32_t *)malloc(sizeof(int32_t) * (size_t)kl);
   for (int j = 0; j < kl; ++j) js[j] = j;
   for (int b = 0; b < B && !rc; ++b)
     for (int kh = 0; kh < Hk && !rc; ++kh) {
-      size_t off = (((size_t)b * Hk + kh) * kl) * (size_t)d;
-      rc = fa_oracle_bwd_kv_rows(q, k, v, mask, dO, B, H, Hk, ql, kl, d, scale, causal, b, kh,
-                                 js, kl, dk + off, dv + off, nthreads);
+      const size_t row0 = ((size_t)b * Hk + kh) * kl;
+      rc = fa_oracle_bwd_kv_rows(q, k, v, mask, dO, B, H, Hk, ql, kl, d, dv, scale, causal, b,
+                                 kh, js, kl, dk + row0 * d, dvo + row0 * dv, nthreads);
     }
   free(js);
   return rc;
+}
+
+/* ------------------------------------------------------------------ sink gradient */
+typedef struct {
+  const prob_t *p;
+  double *term; /* [B*H*ql]: -exp(sink_h - L_i) D_i of every row */
+} dsink_ctx;
+
+static void dsink_task(void *vctx, long t, int worker) {
+  (void)worker;
+  dsink_ctx *c = (dsink_ctx *)vctx;
+  const prob_t *p = c->p;
+  int i = (int)(t % p->ql);
+  int h = (int)((t / p->ql) % p->H);
+  int b = (int)(t / ((int64_t)p->ql * p->H));
+  rowbuf rb = rowbuf_new(p);
+  row_backward_prep(p, b, h, i, &rb);
+  const double sink = sink_logit(p, h);
+  const double psink = (rb.L == -INFINITY) ? 0.0 : exp(sink - rb.L); /* the sink's P */
+  c->term[t] = (g_mutation == MUT_DSINK_SIGN) ? psink * rb.D : -psink * rb.D;
+  rowbuf_free(&rb);
+}
+
+/* Gradient of sum(O * dO) with respect to the sink logits set by fa_oracle_set_sinks:
+ * dsinks[h] = -sum_b sum_i exp(sink_h - L_bhi) D_bhi. Returns -1 on bad sizes or when no
+ * sinks are set. */
+int fa_oracle_dsinks(const float *q, const float *k, const float *v, const float *mask,
+                     const float *dO, int B, int H, int Hk, int ql, int kl, int d, int dv,
+                     double scale, int causal, double *dsinks, int nthreads) {
+  if (bad_sizes(B, H, Hk, ql, kl, d, dv) || !g_sinks) return -1;
+  prob_t p = make_prob(q, k, v, mask, dO, B, H, Hk, ql, kl, d, dv, scale, causal);
+  const long n = (long)B * H * ql;
+  dsink_ctx c = {&p, (double *)malloc(sizeof(double) * (size_t)n)};
+  if (!c.term) return -2;
+  parallel_for(n, nthreads, dsink_task, &c);
+  for (int h = 0; h < H; ++h) dsinks[h] = 0.0;
+  for (long t = 0; t < n; ++t) dsinks[(t / ql) % H] += c.term[t]; /* fixed order */
+  free(c.term);
+  return 0;
 }

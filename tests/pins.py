@@ -408,6 +408,183 @@ def pin_window_closed_forms():
     return fails
 
 
+# ------------------------------------------------------------------ attention sinks
+# A sink is one extra logit per query head that joins the softmax normaliser and carries no
+# value. torch has no sink argument, so the pin builds the equivalent problem for torch: one
+# extra key with k = 0 and v = 0 whose additive bias column is sink_h. torch's own kernels
+# then compute O and L, and autograd through that bias column gives d(sinks).
+SINK_CASES = [
+    # (B, H, Hk, ql, kl, d, causal, mask, window)
+    (1, 2, 1, 4, 6, 8, False, False, None),
+    (2, 4, 2, 5, 5, 4, True, False, None),
+    (1, 2, 2, 3, 7, 8, True, True, None),       # rectangle + mask
+    (1, 4, 1, 6, 6, 4, True, False, (2, -1)),   # causal sliding window
+]
+
+
+def _sink_aug(k, v, sinks_t, bias, B, ql):
+    """k, v with a zero key/value prepended, and the bias with the sink column in front."""
+    Bk, Hk, kl, d = k.shape
+    kz = np.concatenate([np.zeros((Bk, Hk, 1, d), np.float32), k], axis=2)
+    vz = np.concatenate([np.zeros((Bk, Hk, 1, v.shape[3]), np.float32), v], axis=2)
+    H = sinks_t.shape[0]
+    col = sinks_t.view(1, H, 1, 1).expand(B, H, ql, 1)
+    return kz, vz, torch.cat([col, bias], dim=-1)
+
+
+def pin_sinks_vs_torch():
+    fails = []
+    for n, (B, H, Hk, ql, kl, d, causal, mask, win) in enumerate(SINK_CASES):
+        q, k, v, do, m = _problem(800 + n, B, H, Hk, ql, kl, d, mask)
+        if mask:  # one fully masked row: with a sink it has O = 0 and L = sink
+            m[0, 0, 1, :] = -np.inf
+        rng = np.random.default_rng(850 + n)
+        sinks = _bf16_exact((2.0 * rng.standard_normal(H)).astype(np.float32))
+        scale = 0.45
+        with oracle.window(*(win or (-1, -1))), oracle.sinks(sinks):
+            o, lse = oracle.fwd(q, k, v, m, scale=scale, causal=causal)
+            dq, dk, dv = oracle.bwd(q, k, v, m, do, scale=scale, causal=causal)
+            ds = oracle.dsinks(q, k, v, m, do, scale=scale, causal=causal)
+        bias = _torch_bias(ql, kl, causal, m, H, B, win)
+        # forward: torch's CPU flash kernel on the augmented problem
+        st = torch.from_numpy(sinks).double()
+        kz, vz, bz = _sink_aug(k, v, st, bias, B, ql)
+        G = H // Hk
+        to, tl = torch.ops.aten._scaled_dot_product_flash_attention_for_cpu(
+            torch.from_numpy(q).double(), torch.from_numpy(kz).double().repeat_interleave(G, 1),
+            torch.from_numpy(vz).double().repeat_interleave(G, 1), 0.0, False, attn_mask=bz,
+            scale=scale)
+        _cmp(f"sink case{n} O", o, to.numpy(), out=fails)
+        _cmp(f"sink case{n} L", lse, tl.numpy(), out=fails)
+        # backward: autograd through the math backend, sinks as a leaf
+        st = torch.from_numpy(sinks).double().requires_grad_()
+        qt = torch.from_numpy(q).double().requires_grad_()
+        kt = torch.from_numpy(kz).double().requires_grad_()
+        vt = torch.from_numpy(vz).double().requires_grad_()
+        _, _, bz = _sink_aug(k, v, st, bias, B, ql)
+        with torch.nn.attention.sdpa_kernel(torch.nn.attention.SDPBackend.MATH):
+            ot = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=bz, scale=scale,
+                                                enable_gqa=True)
+        (ot * torch.from_numpy(do).double()).sum().backward()
+        _cmp(f"sink case{n} dQ", dq, qt.grad.numpy(), out=fails)
+        _cmp(f"sink case{n} dK", dk, kt.grad.numpy()[:, :, 1:], out=fails)
+        _cmp(f"sink case{n} dV", dv, vt.grad.numpy()[:, :, 1:], out=fails)
+        _cmp(f"sink case{n} dsinks", ds, st.grad.numpy(), out=fails)
+    return fails
+
+
+def pin_sinks_closed_forms():
+    """Q = 0 with no mask: every visible score is 0, so O = sum(v) / (n + e^sink) and
+    L = log(n + e^sink); a row that sees nothing has O = 0, L = sink; a very negative sink is
+    no sink; and d(sinks) against central differences of the oracle's forward."""
+    fails = []
+    B, H, Hk, ql, kl, d = 1, 2, 1, 3, 5, 4
+    _, k, v, do, _ = _problem(870, B, H, Hk, ql, kl, d)
+    q0 = np.zeros((B, H, ql, d), np.float32)
+    sinks = np.array([0.5, -1.25], np.float32)
+    with oracle.sinks(sinks):
+        o, lse = oracle.fwd(q0, k, v, None, scale=0.5, causal=False)
+    z = kl + np.exp(sinks.astype(np.float64))
+    want_o = np.broadcast_to(v.astype(np.float64).sum(axis=2, keepdims=True), (B, Hk, 1, d))
+    want_o = np.repeat(want_o, H // Hk, axis=1) / z[None, :, None, None]
+    _cmp("sink Q=0 O", o, np.broadcast_to(want_o, o.shape), tol=1e-13, out=fails)
+    _cmp("sink Q=0 L", lse, np.broadcast_to(np.log(z)[None, :, None], lse.shape), tol=1e-13,
+         out=fails)
+    # a fully masked row (causal with ql > kl: the first ql - kl rows see no key)
+    q, k2, v2, do2, _ = _problem(871, 1, 2, 1, 6, 4, 4)
+    with oracle.sinks(sinks):
+        o, lse = oracle.fwd(q, k2, v2, None, scale=0.5, causal=True)
+        dq, _, _ = oracle.bwd(q, k2, v2, None, do2, scale=0.5, causal=True)
+    _cmp("sink dead row O", o[:, :, :2], np.zeros_like(o[:, :, :2]), tol=0, out=fails)
+    _cmp("sink dead row L", lse[:, :, :2],
+         np.broadcast_to(sinks.astype(np.float64)[None, :, None], (1, 2, 2)), tol=0, out=fails)
+    _cmp("sink dead row dQ", dq[:, :, :2], np.zeros_like(dq[:, :, :2]), tol=0, out=fails)
+    # a sink far below every score changes nothing
+    q, k3, v3, do3, m3 = _problem(872, 1, 2, 2, 4, 5, 4, mask=True)
+    o_ref, l_ref = oracle.fwd(q, k3, v3, m3, scale=0.5, causal=True)
+    with oracle.sinks(np.full(2, -200.0, np.float32)):
+        o_s, l_s = oracle.fwd(q, k3, v3, m3, scale=0.5, causal=True)
+    _cmp("sink -200 O", o_s, o_ref, tol=1e-15, out=fails)
+    _cmp("sink -200 L", l_s, l_ref, tol=1e-15, out=fails)
+    # dsinks against central differences of sum(O * dO)
+    q, k4, v4, do4, m4 = _problem(873, 1, 2, 1, 4, 6, 4, mask=True, neg_inf_frac=0.2)
+    base = np.array([0.75, -0.5], np.float32)
+    with oracle.sinks(base):
+        ds = oracle.dsinks(q, k4, v4, m4, do4, scale=0.6, causal=True)
+    num = np.zeros(2)
+    for h in range(2):
+        ests = []
+        for step in (2.0 ** -8, 2.0 ** -9):
+            vals = []
+            for sgn in (1, -1):
+                sk = base.copy()
+                sk[h] += np.float32(sgn * step)
+                with oracle.sinks(sk):
+                    o4, _ = oracle.fwd(q, k4, v4, m4, scale=0.6, causal=True, nthreads=1)
+                vals.append(float((o4 * do4.astype(np.float64)).sum()))
+            ests.append((vals[0] - vals[1]) / (2 * step))
+        num[h] = (4 * ests[1] - ests[0]) / 3
+    _cmp("FD dsinks", ds, num, tol=2e-7, out=fails)
+    return fails
+
+
+# ------------------------------------------------------------------ value head dim != d
+DV_CASES = [
+    # (B, H, Hk, ql, kl, d, dv, causal, mask)
+    (1, 2, 1, 4, 6, 8, 4, False, False),
+    (2, 4, 2, 5, 5, 4, 8, True, False),
+    (1, 2, 2, 3, 7, 8, 12, True, True),
+]
+
+
+def pin_value_dim_vs_torch():
+    """dv != d: L does not depend on V, so torch's CPU flash kernel with a d-wide V gives it;
+    O and the gradients come from torch's math backend, which takes any value width."""
+    fails = []
+    for n, (B, H, Hk, ql, kl, d, dvd, causal, mask) in enumerate(DV_CASES):
+        q, k, v_d, do_d, m = _problem(900 + n, B, H, Hk, ql, kl, d, mask)
+        rng = np.random.default_rng(950 + n)
+        v = _bf16_exact(rng.standard_normal((B, Hk, kl, dvd)).astype(np.float32))
+        do = _bf16_exact(rng.standard_normal((B, H, ql, dvd)).astype(np.float32))
+        scale = 0.39
+        o, lse = oracle.fwd(q, k, v, m, scale=scale, causal=causal)
+        dq, dk, dv = oracle.bwd(q, k, v, m, do, scale=scale, causal=causal)
+        _, tl = _torch_fwd(q, k, v_d, m, scale, causal)
+        _cmp(f"dv case{n} L", lse, tl, out=fails)
+        bias = _torch_bias(ql, kl, causal, m, H, B)
+        qt = torch.from_numpy(q).double().requires_grad_()
+        kt = torch.from_numpy(k).double().requires_grad_()
+        vt = torch.from_numpy(v).double().requires_grad_()
+        with torch.nn.attention.sdpa_kernel(torch.nn.attention.SDPBackend.MATH):
+            ot = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=bias, scale=scale,
+                                                enable_gqa=True)
+        (ot * torch.from_numpy(do).double()).sum().backward()
+        _cmp(f"dv case{n} O", o, ot.detach().numpy(), out=fails)
+        _cmp(f"dv case{n} dQ", dq, qt.grad.numpy(), out=fails)
+        _cmp(f"dv case{n} dK", dk, kt.grad.numpy(), out=fails)
+        _cmp(f"dv case{n} dV", dv, vt.grad.numpy(), out=fails)
+    return fails
+
+
+def pin_value_dim_identity():
+    """dv = kl and V = I (per kv head): O is the P matrix itself, so each live row of O sums to
+    one, hidden keys get exactly 0, and O_ij = exp(s_ij - L_i) with the scores from torch."""
+    fails = []
+    B, H, Hk, ql, kl, d = 1, 2, 1, 4, 6, 8
+    q, k, _, _, _ = _problem(960, B, H, Hk, ql, kl, d)
+    v = np.broadcast_to(np.eye(kl, dtype=np.float32), (B, Hk, kl, kl)).copy()
+    o, lse = oracle.fwd(q, k, v, None, scale=0.3, causal=True)
+    _cmp("V=I rows sum to 1", o.sum(axis=-1), np.ones((B, H, ql)), tol=1e-14, out=fails)
+    allowed = causal_lower_right(ql, kl)._materialize(device="cpu").numpy()
+    hidden = np.broadcast_to(~allowed, o.shape)
+    _cmp("V=I hidden keys", np.where(hidden, o, 0.0), np.zeros_like(o), tol=0, out=fails)
+    s = torch.from_numpy(q).double() @ torch.from_numpy(k).double().repeat_interleave(
+        H // Hk, 1).transpose(-1, -2) * 0.3
+    want = np.where(hidden, 0.0, np.exp(s.numpy() - lse[..., None]))
+    _cmp("V=I O = P", o, want, tol=1e-13, out=fails)
+    return fails
+
+
 ALL_PINS = [
     pin_fwd_vs_torch_cpu_flash,
     pin_bwd_vs_torch_autograd,
@@ -419,4 +596,8 @@ ALL_PINS = [
     pin_base2_mode_agrees,
     pin_window_vs_torch,
     pin_window_closed_forms,
+    pin_sinks_vs_torch,
+    pin_sinks_closed_forms,
+    pin_value_dim_vs_torch,
+    pin_value_dim_identity,
 ]
