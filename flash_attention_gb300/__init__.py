@@ -41,10 +41,12 @@ class FaOptions(ctypes.Structure):
         ("window_left", ctypes.c_int32),
         ("window_right", ctypes.c_int32),
         ("mask_type", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("value_dim", ctypes.c_int32),
         ("mask_stride_b", ctypes.c_int64),
         ("mask_stride_h", ctypes.c_int64),
         ("mask_stride_q", ctypes.c_int64),
+        ("sinks", ctypes.c_void_p),
+        ("dsinks", ctypes.c_void_p),
     ]
 
 
@@ -174,15 +176,18 @@ def fa_train_bwd(q, k, v, o, lse, dO, mask, dq, dk, dv, params: FaParams, stream
         raise FaError(rc, "fa_train_bwd")
 
 
-def make_options(q, k, mask=None, window=(-1, -1)) -> FaOptions:
+def make_options(q, k, mask=None, window=(-1, -1), v=None, sinks=None, dsinks=None) -> FaOptions:
     """fa_options for a mask tensor of any supported dtype (float32, bfloat16, bool) whose shape
-    broadcasts to [B, H, ql, kl] with the keys contiguous, and a (left, right) window."""
+    broadcasts to [B, H, ql, kl] with the keys contiguous, a (left, right) window, the value
+    head dim of `v` (when it differs from q's), and float32 [H] sinks / dsinks tensors."""
     import torch
 
-    B, H, ql, _ = q.shape
+    B, H, ql, d = q.shape
     kl = k.shape[2]
     wl, wr = window if window is not None else (-1, -1)
-    opt = FaOptions(int(wl), int(wr), FA_MASK_F32, 0, 0, 0, 0)
+    opt = FaOptions(int(wl), int(wr), FA_MASK_F32, 0, 0, 0, 0, None, None)
+    if v is not None and v.shape[-1] != d:
+        opt.value_dim = int(v.shape[-1])
     if mask is not None:
         types = {torch.float32: FA_MASK_F32, torch.bfloat16: FA_MASK_BF16, torch.bool: FA_MASK_BOOL,
                  torch.uint8: FA_MASK_BOOL}
@@ -194,6 +199,13 @@ def make_options(q, k, mask=None, window=(-1, -1)) -> FaOptions:
             raise ValueError("the mask's key dimension must be contiguous")
         opt.mask_type = types[mask.dtype]
         opt.mask_stride_b, opt.mask_stride_h, opt.mask_stride_q = sb, sh, sq
+    for name, t in (("sinks", sinks), ("dsinks", dsinks)):
+        if t is None:
+            continue
+        if t.dtype != torch.float32 or not t.is_cuda or tuple(t.shape) != (H,) or \
+                not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA float32 tensor of shape [{H}]")
+        setattr(opt, name, t.data_ptr())
     return opt
 
 
@@ -259,40 +271,51 @@ def fa_version() -> str:
     return load_library().fa_version().decode()
 
 
-def attention_fwd(q, k, v, *, scale, causal, mask=None, window=None, stream=None):
-    """Allocate O and L and run the forward: returns (o, lse). `mask`: None, or a float32 /
-    bfloat16 additive or bool mask broadcastable to [B, H, ql, kl]; `window`: None or
-    (left, right) with -1 for an unbounded side."""
+def _plain_call(q, k, v, mask, window, sinks):
+    """True when the base entry point covers the call (dense f32 mask or none, no window, no
+    sinks, value head dim = head dim)."""
     import torch
 
     B, H, ql, d = q.shape
-    o = torch.empty_like(q)
+    dense = mask is None or (mask.dtype == torch.float32 and mask.dim() == 4
+                             and mask.is_contiguous()
+                             and tuple(mask.shape) == (B, H, ql, k.shape[2]))
+    return dense and window is None and sinks is None and v.shape[-1] == d
+
+
+def attention_fwd(q, k, v, *, scale, causal, mask=None, window=None, sinks=None, stream=None):
+    """Allocate O and L and run the forward: returns (o, lse). `mask`: None, or a float32 /
+    bfloat16 additive or bool mask broadcastable to [B, H, ql, kl]; `window`: None or
+    (left, right) with -1 for an unbounded side; `sinks`: None or float32 [H] logits. v may
+    have its own head dim (o then has it too)."""
+    import torch
+
+    B, H, ql, d = q.shape
+    o = torch.empty((B, H, ql, v.shape[-1]), dtype=q.dtype, device=q.device)
     lse = torch.empty((B, H, ql), dtype=torch.float32, device=q.device)
     params = make_params(q, k, scale=scale, causal=causal)
-    if window is None and (mask is None or (mask.dtype == torch.float32 and mask.dim() == 4
-                                            and mask.is_contiguous()
-                                            and tuple(mask.shape) == (B, H, ql, k.shape[2]))):
+    if _plain_call(q, k, v, mask, window, sinks):
         fa_train_fwd(q, k, v, mask, o, lse, params, stream)
     else:
-        fa_train_fwd_ex(q, k, v, mask, o, lse, params, make_options(q, k, mask, window), stream)
+        fa_train_fwd_ex(q, k, v, mask, o, lse, params,
+                        make_options(q, k, mask, window, v=v, sinks=sinks), stream)
     return o, lse
 
 
-def attention_bwd(q, k, v, o, lse, dO, *, scale, causal, mask=None, window=None, stream=None):
-    """Allocate dQ, dK, dV and run the backward: returns (dq, dk, dv). `mask` and `window` as
-    given to attention_fwd."""
+def attention_bwd(q, k, v, o, lse, dO, *, scale, causal, mask=None, window=None, sinks=None,
+                  stream=None):
+    """Allocate dQ, dK, dV and run the backward: returns (dq, dk, dv), or (dq, dk, dv, dsinks)
+    when `sinks` is given. `mask`, `window` and `sinks` as given to attention_fwd."""
     import torch
 
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
     params = make_params(q, k, scale=scale, causal=causal)
-    B, H, ql, _ = q.shape
-    if window is None and (mask is None or (mask.dtype == torch.float32 and mask.dim() == 4
-                                            and mask.is_contiguous()
-                                            and tuple(mask.shape) == (B, H, ql, k.shape[2]))):
+    if _plain_call(q, k, v, mask, window, sinks):
         fa_train_bwd(q, k, v, o, lse, dO, mask, dq, dk, dv, params, stream)
-    else:
-        fa_train_bwd_ex(q, k, v, o, lse, dO, mask, dq, dk, dv, params,
-                        make_options(q, k, mask, window), stream)
-    return dq, dk, dv
+        return dq, dk, dv
+    dsinks = None if sinks is None else torch.empty_like(sinks)
+    fa_train_bwd_ex(q, k, v, o, lse, dO, mask, dq, dk, dv, params,
+                    make_options(q, k, mask, window, v=v, sinks=sinks, dsinks=dsinks), stream)
+    return (dq, dk, dv) if sinks is None else (dq, dk, dv, dsinks)

@@ -106,16 +106,22 @@ fa_options default_options(const fa_params* p) {
   o.window_left = -1;
   o.window_right = -1;
   o.mask_type = FA_MASK_F32;
-  o.reserved = 0;
+  o.value_dim = 0;
+  o.sinks = nullptr;
+  o.dsinks = nullptr;
   o.mask_stride_q = p->kl;
   o.mask_stride_h = (int64_t)p->ql * p->kl;
   o.mask_stride_b = (int64_t)p->n_heads * p->ql * p->kl;
   return o;
 }
 
-int check_options(const fa_options* o, const void* mask) {
+// Option checks shared by both passes; `bwd` adds the dsinks rules. FA_ERR_INVALID comes before
+// FA_ERR_UNSUPPORTED (a value head dim without kernels).
+int check_options(const fa_options* o, const void* mask, const fa_params* p, bool bwd) {
   if (o->window_left < -1 || o->window_right < -1) return FA_ERR_INVALID;
-  if (o->reserved != 0) return FA_ERR_INVALID;
+  if (o->value_dim < 0) return FA_ERR_INVALID;
+  if (o->sinks && !aligned(o->sinks, 4)) return FA_ERR_INVALID;
+  if (bwd && o->dsinks && (!o->sinks || !aligned(o->dsinks, 4))) return FA_ERR_INVALID;
   if (o->mask_type != FA_MASK_F32 && o->mask_type != FA_MASK_BF16 && o->mask_type != FA_MASK_BOOL)
     return FA_ERR_INVALID;
   if (o->mask_stride_b < 0 || o->mask_stride_h < 0 || o->mask_stride_q < 0) return FA_ERR_INVALID;
@@ -123,6 +129,8 @@ int check_options(const fa_options* o, const void* mask) {
     const uintptr_t es = o->mask_type == FA_MASK_F32 ? 4 : o->mask_type == FA_MASK_BF16 ? 2 : 1;
     if (!aligned(mask, es)) return FA_ERR_INVALID;
   }
+  if (!fa_value_dim_supported(p->head_dim, o->value_dim ? o->value_dim : p->head_dim))
+    return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 
@@ -235,7 +243,7 @@ int fa_train_fwd_ex(const void* q, const void* k, const void* v, const void* mas
     return rc;
   const fa_options o_def = default_options(p);
   const fa_options* op = opt ? opt : &o_def;
-  if ((rc = check_options(op, mask))) return rc;
+  if ((rc = check_options(op, mask, p, false))) return rc;
   if ((rc = check_device())) return rc;
   cudaError_t e = get_encoder();
   if (e != cudaSuccess) return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
@@ -247,6 +255,7 @@ int fa_train_fwd_ex(const void* q, const void* k, const void* v, const void* mas
   a.mask_stride_b = op->mask_stride_b;
   a.mask_stride_h = op->mask_stride_h;
   a.mask_stride_q = op->mask_stride_q;
+  a.sinks = op->sinks;
   a.o = o;
   a.lse = lse;
   if ((e = device_status_word(dev, &a.status)) != cudaSuccess) return cuda_fail(e, "status word");
@@ -291,7 +300,7 @@ static int prepare_bwd(const void* q, const void* k, const void* v, const void* 
     return rc;
   const fa_options o_def = default_options(p);
   const fa_options* op = opt ? opt : &o_def;
-  if ((rc = check_options(op, mask))) return rc;
+  if ((rc = check_options(op, mask, p, true))) return rc;
   a->q = q;
   a->k = k;
   a->v = v;
@@ -303,6 +312,9 @@ static int prepare_bwd(const void* q, const void* k, const void* v, const void* 
   a->mask_stride_b = op->mask_stride_b;
   a->mask_stride_h = op->mask_stride_h;
   a->mask_stride_q = op->mask_stride_q;
+  a->sinks = op->sinks;
+  a->dsinks = op->dsinks;
+  a->dsink_part = nullptr;  // set with the workspace
   a->dq = dq;
   a->dk = dk;
   a->dv = dv;
@@ -353,7 +365,8 @@ int fa_train_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
   void* ws = nullptr;
   e = cudaMallocAsync(&ws, ws_bytes, s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync (backward workspace)");
-  fa::bwd_carve_workspace(ws, a.B, a.H, a.ql, a.d, &a.lse2, &a.dvec, &a.dqacc);
+  fa::bwd_carve_workspace(ws, a.B, a.H, a.ql, a.d, &a.lse2, &a.dvec, &a.dqacc,
+                          &a.dsink_part);
   e = fa::launch_bwd(a, m, s);
   cudaError_t e2 = cudaFreeAsync(ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
@@ -392,7 +405,8 @@ int fa_train_bwd_noalloc(const void* q, const void* k, const void* v, const void
   if ((rc = encode_bwd_maps(a, &m))) return rc;
   // the pre-pass rewrites L*log2(e) and D and zeroes the dQ accumulator for every row the
   // main pass reads, so the array's previous contents never reach a result
-  fa::bwd_carve_workspace(ws, a.B, a.H, a.ql, a.d, &a.lse2, &a.dvec, &a.dqacc);
+  fa::bwd_carve_workspace(ws, a.B, a.H, a.ql, a.d, &a.lse2, &a.dvec, &a.dqacc,
+                          &a.dsink_part);
   e = fa::launch_bwd(a, m, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   return FA_OK;
@@ -429,5 +443,9 @@ const char* fa_error_string(int code) {
 const char* fa_last_cuda_error(void) { return g_last_cuda_error; }
 
 const char* fa_version(void) { return "fa_gb300 0.1 (sm_103a, tcgen05)"; }
+
+int fa_value_dim_supported(int head_dim, int value_dim) {
+  return (head_dim == 64 || head_dim == 128 || head_dim == 256) && value_dim == head_dim;
+}
 
 }  // extern "C"

@@ -127,19 +127,34 @@ struct BwdKParams {
 // A group of HD/8 threads owns one row (16-byte loads of O and dO); each thread walks ROWS
 // rows so that many loads are in flight; the chunk's accumulator rows are then zeroed with
 // coalesced float4 stores.
+// With sinks and a dsinks output, each block also sums the rows' sink-gradient terms
+// -exp(sink_h - L_i) * D_i of its chunk in a fixed order into dsink_part[bh, chunk]; the dQ
+// kernel adds those partials up per head (also in a fixed order).
+constexpr int kPrepRowsMin = 32;  // fewest rows per prep block (head_dim 256): sizes the partials
+template <int HD>
+__host__ __device__ constexpr int prep_rows_per_block() {
+  return (256 / (HD / 8)) * 4;
+}
+
 template <int HD>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
                                                        const __nv_bfloat16* __restrict__ dO,
                                                        const float* __restrict__ lse,
                                                        float* __restrict__ lse2,
                                                        float* __restrict__ dvec,
-                                                       float* __restrict__ dqacc, int BH, int ql,
-                                                       int ql_pad) {
+                                                       float* __restrict__ dqacc,
+                                                       const float* __restrict__ sinks,
+                                                       float* __restrict__ dsink_part, int BH,
+                                                       int H, int ql, int ql_pad) {
   constexpr int TPR = HD / 8;            // threads per row (8 bf16 = 16 bytes each)
   constexpr int RPB = 256 / TPR;         // rows per pass of the block
   constexpr int ROWS = 4;                // passes per block
+  static_assert(RPB * ROWS == prep_rows_per_block<HD>(), "prep chunk");
+  static_assert(RPB * ROWS >= kPrepRowsMin && RPB * ROWS <= 256, "sink partial layout");
+  __shared__ float sink_terms[RPB * ROWS];
   const int sub = threadIdx.x % TPR;
   const int i0 = blockIdx.x * RPB * ROWS;  // first row of the chunk (ql_pad is a multiple)
+  const bool want_dsink = dsink_part != nullptr;
   for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
     uint4 a[ROWS], g[ROWS];
 #pragma unroll
@@ -166,17 +181,33 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
       const int i = i0 + r * RPB + threadIdx.x / TPR;
       if (sub == 0) {
         float nl2 = -INFINITY;  // padding rows and fully masked rows: P = exp2(s - inf) = 0
+        float term = 0.0f;      // this row's share of dsinks[h]
         if (i < ql) {
           const float L = lse[(size_t)bh * ql + i];
-          if (L != -INFINITY) nl2 = -L * kLog2eB;
+          if (L != -INFINITY) {
+            nl2 = -L * kLog2eB;
+            if (want_dsink) term = -expf(__ldg(sinks + bh % H) - L) * acc;
+          }
         }
         lse2[(size_t)bh * ql_pad + i] = nl2;
         dvec[(size_t)bh * ql_pad + i] = i < ql ? acc : 0.0f;
+        if (want_dsink) sink_terms[r * RPB + threadIdx.x / TPR] = term;
       }
     }
     float4* z = reinterpret_cast<float4*>(dqacc + ((size_t)bh * ql_pad + i0) * HD);
 #pragma unroll 4
     for (int c = threadIdx.x; c < RPB * ROWS * HD / 4; c += 256) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (want_dsink) {  // block-uniform
+      __syncthreads();
+      if (threadIdx.x < 32) {
+        float s = 0.0f;
+        for (int k = threadIdx.x; k < RPB * ROWS; k += 32) s += sink_terms[k];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        if (threadIdx.x == 0) dsink_part[(size_t)bh * gridDim.x + blockIdx.x] = s;
+      }
+      __syncthreads();  // sink_terms is rewritten by the next head
+    }
   }
 }
 
@@ -184,10 +215,33 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
 // dQ = bf16(scale * accumulator). Grid: x = chunk of 256 groups of 8 values within a head,
 // y = head (strided). Each thread converts 8 consecutive values (two float4 loads, one 16-byte
 // store).
+// Blocks with x == 0 also finish dsinks[h] for h = y, y + gridDim.y, ...: the sum, in a fixed
+// order, of the prep kernel's partials of every batch entry of head h.
 template <int HD>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ dqacc,
                                                      __nv_bfloat16* __restrict__ dq, int BH,
-                                                     int ql, int ql_pad, float scale) {
+                                                     int ql, int ql_pad, float scale,
+                                                     const float* __restrict__ dsink_part,
+                                                     float* __restrict__ dsinks, int B, int H,
+                                                     int sink_chunks) {
+  if (dsinks != nullptr && blockIdx.x == 0) {  // block-uniform
+    __shared__ float red[256];
+    const int n = B * sink_chunks;
+    for (int h = blockIdx.y; h < H; h += gridDim.y) {
+      float s = 0.0f;
+      for (int k = threadIdx.x; k < n; k += 256)
+        s += dsink_part[((size_t)(k / sink_chunks) * H + h) * sink_chunks + k % sink_chunks];
+      red[threadIdx.x] = s;
+      __syncthreads();
+#pragma unroll
+      for (int w = 128; w > 0; w >>= 1) {
+        if ((int)threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
+      }
+      if (threadIdx.x == 0) dsinks[h] = red[0];
+      __syncthreads();  // red is reused by the next head
+    }
+  }
   const int e = blockIdx.x * 256 + threadIdx.x;  // index of the 8-value group within a head
   const int i = e / (HD / 8), c = (e % (HD / 8)) * 8;
   if (i >= ql) return;
@@ -510,7 +564,6 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
       const int st = it % ST;
       const int h = kh * G + it / nm;
       const int q0 = (m_first + it % nm) * BM;
-      const int bh = b * p.H + h;
       const float* sL = reinterpret_cast<const float*>(smem + LY::OFF_L + st * BM * 4);
       const uint32_t colS = LY::COL_S0 + (it % NSB) * BM;
       // column q (row q0 + q) sees this key iff qlo <= q <= qhi (no upper limit without a
@@ -794,17 +847,17 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 size_t bwd_workspace_bytes(int B, int H, int ql, int d) {
   const size_t rows = (size_t)B * H * bwd_ql_pad(ql);
-  return align256(rows * 4) * 2 + align256(rows * d * 4);
+  return align256(rows * 4) * 2 + align256(rows * d * 4) + align256(rows / kPrepRowsMin * 4);
 }
 
 void bwd_carve_workspace(void* base, int B, int H, int ql, int d, float** lse2, float** dvec,
-                         float** dqacc) {
+                         float** dqacc, float** dsink_part) {
   const size_t rows = (size_t)B * H * bwd_ql_pad(ql);
   uint8_t* p = static_cast<uint8_t*>(base);
   *lse2 = reinterpret_cast<float*>(p);
   *dvec = reinterpret_cast<float*>(p + align256(rows * 4));
   *dqacc = reinterpret_cast<float*>(p + 2 * align256(rows * 4));
-  (void)d;
+  *dsink_part = reinterpret_cast<float*>(p + 2 * align256(rows * 4) + align256(rows * d * 4));
 }
 
 template <int HD, int BAND, int MASKT>
@@ -859,13 +912,15 @@ static cudaError_t launch_main_m(const BwdArgs& a, const BwdMaps& m, cudaStream_
 template <int HD>
 static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t s) {
   const int BH = a.B * a.H;
+  constexpr int rows_per_block = prep_rows_per_block<HD>();  // divides 128, hence ql_pad
+  const int sink_chunks = a.ql_pad / rows_per_block;
+  float* dsink_part = a.dsinks != nullptr ? a.dsink_part : nullptr;
   {
-    constexpr int rows_per_block = (256 / (HD / 8)) * 4;  // divides 128, hence ql_pad
-    dim3 grid(a.ql_pad / rows_per_block, BH < 65535 ? BH : 65535);
+    dim3 grid(sink_chunks, BH < 65535 ? BH : 65535);
     profile_mark(kKernBwdPrep, 0, s);
     bwd_prep_kernel<HD><<<grid, 256, 0, s>>>(
         reinterpret_cast<const __nv_bfloat16*>(a.o), reinterpret_cast<const __nv_bfloat16*>(a.dO),
-        a.lse, a.lse2, a.dvec, a.dqacc, BH, a.ql, a.ql_pad);
+        a.lse, a.lse2, a.dvec, a.dqacc, a.sinks, dsink_part, BH, a.H, a.ql, a.ql_pad);
     cudaError_t e = cudaGetLastError();
     profile_mark(kKernBwdPrep, 1, s);
     if (e != cudaSuccess) return e;
@@ -879,7 +934,8 @@ static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t
     dim3 grid((unsigned)((groups + 255) / 256), BH < 65535 ? BH : 65535);
     profile_mark(kKernBwdDq, 0, s);
     bwd_dq_kernel<HD><<<grid, 256, 0, s>>>(a.dqacc, reinterpret_cast<__nv_bfloat16*>(a.dq), BH,
-                                           a.ql, a.ql_pad, a.scale);
+                                           a.ql, a.ql_pad, a.scale, dsink_part, a.dsinks, a.B,
+                                           a.H, sink_chunks);
     profile_mark(kKernBwdDq, 1, s);
   }
   return cudaGetLastError();

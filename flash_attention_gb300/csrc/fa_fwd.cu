@@ -82,6 +82,7 @@ struct FwdKParams {
   long long msb, msh, msq;  // mask strides (elements) of batch, head, query row; keys contiguous
   __nv_bfloat16* o;
   float* lse;
+  const float* sinks;  // [H] natural-log sink logits, or nullptr
   int* status;
   int H, Hk, ql, kl, n_mblk;
   int lo_off, hi_off;  // key j is visible to row i iff q_abs + lo_off <= j <= q_abs + hi_off
@@ -366,8 +367,15 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
              (b_ * p.msb + h_ * p.msh + (long long)i * p.msq) * es;
     }
 
-    float m_used = -FLT_MAX / 2.0f;  // finite sentinel
+    // Running max (base 2) starts at the finite sentinel and the row sum at 0; a sink starts
+    // them at the sink's logit and its exp2 share (1, or 0 for a sink of -inf).
+    float m_used = -FLT_MAX / 2.0f;
     float l = 0.0f;
+    if (p.sinks != nullptr) {
+      const float s2 = __ldg(p.sinks + bh % p.H) * kLog2e;
+      m_used = fmaxf(s2, m_used);
+      l = ex2(s2 - m_used);
+    }
     bool ok = true;
 
     for (int j = 0; j < ntt; ++j) {  // j: iteration of this query tile (kv tile kt0 + j)
@@ -480,8 +488,11 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&o_final[t], 0, &abort_flag));
       tc_fence_after();
     }
-    const bool live = ok && ntt > 0 && l > 0.0f;
-    const float inv = live ? 1.0f / l : 0.0f;
+    // L is finite whenever the normaliser is positive (keys seen, or a sink); O exists in TMEM
+    // only when some kv tile was visited.
+    const bool live = ok && l > 0.0f;
+    const bool have_o = live && ntt > 0;
+    const float inv = have_o ? 1.0f / l : 0.0f;
     __nv_bfloat16* orow = p.o + ((size_t)bh * p.ql + (i < p.ql ? i : 0)) * HD;
 #pragma unroll 1
     for (int c = 0; c < HD; c += 32) {
@@ -493,8 +504,8 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
       uint32_t packed[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        float a0 = live ? __uint_as_float(orr[2 * e]) * inv : 0.0f;
-        float a1 = live ? __uint_as_float(orr[2 * e + 1]) * inv : 0.0f;
+        float a0 = have_o ? __uint_as_float(orr[2 * e]) * inv : 0.0f;
+        float a1 = have_o ? __uint_as_float(orr[2 * e + 1]) * inv : 0.0f;
         packed[e] = pack_bf16(a0, a1);
       }
       if (i < p.ql) {
@@ -537,6 +548,7 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, const FwdMaps& m, cudaStream_t
   kp.msq = a.mask_stride_q;
   kp.o = reinterpret_cast<__nv_bfloat16*>(a.o);
   kp.lse = a.lse;
+  kp.sinks = a.sinks;
   kp.status = a.status;
   kp.H = a.H;
   kp.Hk = a.Hk;

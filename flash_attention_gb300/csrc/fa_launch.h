@@ -48,6 +48,7 @@ struct FwdArgs {
   long long mask_stride_b, mask_stride_h, mask_stride_q;  // elements; keys contiguous
   void* o;            // bf16 [B, H, ql, d]
   float* lse;         // [B, H, ql]
+  const float* sinks; // [H] natural-log sink logits, or nullptr
   int* status;        // device status word (nullable)
   int B, H, Hk, ql, kl, d;
   float scale;
@@ -85,6 +86,9 @@ struct BwdArgs {
   float* lse2;   // workspace [B*H, ql_pad]: -L * log2(e), -inf for fully masked rows
   float* dvec;   // workspace [B*H, ql_pad]: D = rowsum(dO * O)
   float* dqacc;  // workspace [B*H, ql_pad, d] f32 dQ accumulator
+  const float* sinks;  // [H] sink logits, or nullptr
+  float* dsinks;       // [H] sink gradient output, or nullptr (then no sink partials)
+  float* dsink_part;   // workspace [B*H, sink_chunks]: per-block partial sums of dsinks
   int* status;
   int B, H, Hk, ql, kl, d, ql_pad;
   float scale;
@@ -100,10 +104,11 @@ int bwd_q_box_rows(int d);
 int bwd_kv_box_rows(int d);
 int bwd_ql_pad(int ql);
 
-// Workspace bytes of a backward call (lse2 + dvec + dqacc, each 256-byte aligned).
+// Workspace bytes of a backward call (lse2 + dvec + dqacc + the dsinks partials, each 256-byte
+// aligned).
 size_t bwd_workspace_bytes(int B, int H, int ql, int d);
 void bwd_carve_workspace(void* base, int B, int H, int ql, int d, float** lse2, float** dvec,
-                         float** dqacc);
+                         float** dqacc, float** dsink_part);
 
 cudaError_t launch_bwd(const BwdArgs& a, const BwdMaps& m, cudaStream_t stream);
 

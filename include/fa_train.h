@@ -95,16 +95,38 @@ typedef struct fa_params {
  *   mask + b*mask_stride_b + h*mask_stride_h + i*mask_stride_q + j      (in elements)
  * (keys contiguous; a zero stride broadcasts). The dense [B, H, ql, kl] f32 mask of the base
  * entry points is mask_type FA_MASK_F32 with strides (H*ql*kl, ql*kl, kl). The mask pointer
- * must be aligned to its element size. */
+ * must be aligned to its element size.
+ *
+ * Attention sinks (page "nuvec-core tests/fast.rs", the per-head `sinks` input of the fused
+ * attention in `attention_kernels_match_the_fallback`; the page gives only the shape, and the
+ * reading taken is an extra logit with no value): sinks is NULL or a device array of n_heads
+ * f32 natural-log logits, not scaled. sink_h joins the softmax normaliser of every row of
+ * head h:  L = log(exp(sink_h) + sum_j exp(s_ij)),  O = sum_j exp(s_ij - L) v_j.
+ * A row that sees no key then gives O = 0 and L = sink_h; a sink of -inf is no sink (values
+ * must be finite or -inf). dsinks (backward only) is NULL or a device array of n_heads f32
+ * that receives the gradient with respect to the sinks,
+ *   dsinks[h] = -sum_b sum_i exp(sink_h - L_bhi) * D_bhi,   D = rowsum(dO * O),
+ * overwritten (not accumulated) and summed in a fixed order, so it is bitwise reproducible.
+ * dsinks requires sinks. The forward and the backward must be given the same sinks.
+ *
+ * Value head dim (same page: its shapes list (D, Dv) pairs with Dv != D): value_dim = 0 means
+ * head_dim; otherwise v, dV are [B, Hk, kl, value_dim] and o, dO are [B, H, ql, value_dim]
+ * while q, k, dQ, dK keep head_dim. Supported pairs (head_dim, value_dim) are listed by
+ * fa_value_dim_supported; others give FA_ERR_UNSUPPORTED. */
 typedef struct fa_options {
   int32_t window_left;   /* -1, or >= 0 */
   int32_t window_right;  /* -1, or >= 0 */
   int32_t mask_type;     /* FA_MASK_* (ignored when the mask pointer is NULL) */
-  int32_t reserved;      /* must be 0 */
+  int32_t value_dim;     /* 0 (= head_dim), or a supported value head dim */
   int64_t mask_stride_b; /* >= 0 */
   int64_t mask_stride_h; /* >= 0 */
   int64_t mask_stride_q; /* >= 0 */
+  const float* sinks;    /* NULL, or [n_heads] f32 on the device, 4-byte aligned */
+  float* dsinks;         /* backward only: NULL, or [n_heads] f32 output on the device */
 } fa_options;
+
+/* 1 if this build has kernels for the (head_dim, value_dim) pair, else 0. */
+int fa_value_dim_supported(int head_dim, int value_dim);
 
 /* Forward: O and L. Page "mlx-native tests/test_flash_attn_train.rs", sections 2-8 (forward
  * parity), function `sdpa_reference_with_logsumexp`.
@@ -121,8 +143,9 @@ int fa_train_fwd(const void* q, const void* k, const void* v, const float* mask,
 /* Forward with options (window, mask type and broadcast). opt == NULL gives the base
  * behaviour (no window; a mask, if any, dense [B, H, ql, kl] f32). Rows whose window and mask
  * leave no key give O = 0 and L = -inf. Errors as fa_train_fwd; FA_ERR_INVALID also for
- * window values below -1, an unknown mask type, a nonzero `reserved`, negative strides or a
- * mask not aligned to its element size. */
+ * window values below -1, an unknown mask type, a negative value_dim, negative strides, a
+ * mask not aligned to its element size or a misaligned sinks pointer; FA_ERR_UNSUPPORTED for
+ * a (head_dim, value_dim) pair without kernels. The forward ignores dsinks. */
 int fa_train_fwd_ex(const void* q, const void* k, const void* v, const void* mask, void* o,
                     float* lse, const fa_params* p, const fa_options* opt, void* stream);
 
@@ -157,8 +180,10 @@ int fa_profile_read(double* total_ms, int64_t* launches);
 /* Name of a kernel id (static storage). */
 const char* fa_kernel_name(int id);
 
-/* Backward with options; `opt` and `mask` must be those given to the forward that produced
- * o and lse. opt == NULL gives the base behaviour. */
+/* Backward with options; `opt` (window, mask, value_dim, sinks) and `mask` must be those
+ * given to the forward that produced o and lse. opt == NULL gives the base behaviour. With
+ * opt->dsinks non-NULL the sink gradient is written too (FA_ERR_INVALID if opt->sinks is
+ * NULL or either pointer is not 4-byte aligned). */
 int fa_train_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
                     const void* dO, const void* mask, void* dq, void* dk, void* dv,
                     const fa_params* p, const fa_options* opt, void* stream);

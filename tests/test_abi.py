@@ -127,15 +127,16 @@ def _bwd_ex(lib, params, opts, mask=None):
 
 
 def _opts(**kw):
-    base = dict(window_left=-1, window_right=-1, mask_type=0, reserved=0, mask_stride_b=0,
-                mask_stride_h=0, mask_stride_q=128)
+    base = dict(window_left=-1, window_right=-1, mask_type=0, value_dim=0, mask_stride_b=0,
+                mask_stride_h=0, mask_stride_q=128, sinks=None, dsinks=None)
     base.update(kw)
     return fa.FaOptions(**base)
 
 
 BAD_OPTIONS = [
     dict(window_left=-2), dict(window_right=-5), dict(mask_type=3), dict(mask_type=-1),
-    dict(reserved=1), dict(mask_stride_b=-1), dict(mask_stride_h=-4), dict(mask_stride_q=-128),
+    dict(value_dim=-1), dict(mask_stride_b=-1), dict(mask_stride_h=-4),
+    dict(mask_stride_q=-128), dict(sinks=FAKE + 2),
 ]
 
 
@@ -159,6 +160,26 @@ def test_mask_alignment_follows_its_element_type(lib):
             fa.FA_ERR_CUDA, fa.FA_ERR_UNSUPPORTED)
 
 
+def test_dsinks_rules_in_the_backward(lib):
+    # dsinks needs sinks, and 4-byte alignment; the forward ignores dsinks
+    assert _bwd_ex(lib, GOOD, _opts(dsinks=FAKE)) == fa.FA_ERR_INVALID
+    assert _bwd_ex(lib, GOOD, _opts(sinks=FAKE, dsinks=FAKE + 2)) == fa.FA_ERR_INVALID
+    import torch
+
+    if not torch.cuda.is_available():
+        assert _fwd_ex(lib, GOOD, _opts(dsinks=FAKE)) in (fa.FA_ERR_CUDA, fa.FA_ERR_UNSUPPORTED)
+        assert _bwd_ex(lib, GOOD, _opts(sinks=FAKE, dsinks=FAKE)) in (fa.FA_ERR_CUDA,
+                                                                       fa.FA_ERR_UNSUPPORTED)
+
+
+def test_value_dim_without_kernels_is_unsupported(lib):
+    assert not lib.fa_value_dim_supported(128, 96)
+    assert lib.fa_value_dim_supported(128, 128)
+    assert _fwd_ex(lib, GOOD, _opts(value_dim=96)) == fa.FA_ERR_UNSUPPORTED
+    assert _bwd_ex(lib, GOOD, _opts(value_dim=96)) == fa.FA_ERR_UNSUPPORTED
+
+
 def test_options_struct_layout():
-    assert ctypes.sizeof(fa.FaOptions) == 40
+    assert ctypes.sizeof(fa.FaOptions) == 56
     assert fa.FaOptions.mask_stride_b.offset == 16
+    assert fa.FaOptions.sinks.offset == 40 and fa.FaOptions.dsinks.offset == 48
