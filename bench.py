@@ -189,6 +189,8 @@ def oracle_head_sample(w, inp, heads, nthreads=None):
     win = oracle.window(w.window_left, w.window_right)
     win.__enter__()
     for (b, h) in heads:
+        sk = oracle.sinks(None if inp.sinks is None else inp.sinks[h:h + 1])
+        sk.__enter__()
         kh = h // G
         qs = np.ascontiguousarray(q[b:b + 1, h:h + 1])
         ks = np.ascontiguousarray(k[b:b + 1, kh:kh + 1])
@@ -197,6 +199,9 @@ def oracle_head_sample(w, inp, heads, nthreads=None):
         ms = None if inp.mask is None else np.ascontiguousarray(inp.mask[b:b + 1, h:h + 1])
         oracle.fwd(qs, ks, vs, ms, scale=w.scale, causal=w.causal, nthreads=nthreads)
         oracle.bwd(qs, ks, vs, ms, dos, scale=w.scale, causal=w.causal, nthreads=nthreads)
+        if inp.sinks is not None:
+            oracle.dsinks(qs, ks, vs, ms, dos, scale=w.scale, causal=w.causal, nthreads=nthreads)
+        sk.__exit__(None, None, None)
     win.__exit__(None, None, None)
     dt = time.perf_counter() - t0
     return per_head * len(heads), dt
@@ -250,6 +255,8 @@ def config_of(w, n):
             "n_kv_heads": w.n_kv_heads, "ql": w.ql, "kl": w.kl, "head_dim": w.head_dim,
             "scale": w.scale, "causal": w.causal, "mask": w.masked,
             **({"window": [w.window_left, w.window_right]} if w.windowed else {}),
+            **({"value_dim": w.dv} if w.dv != w.head_dim else {}),
+            **({"sinks": True} if w.sinks else {}),
             "flop_rule": "fwd 4*B*H*ql*kl*d*f, bwd 10*B*H*ql*kl*d*f, "
                          + ("f = visible fraction of (query, key) pairs under the window"
                             if w.windowed else "f=0.5 causal"),
@@ -260,9 +267,11 @@ def config_of(w, n):
 
 def step_bytes(w):
     qb = w.batch * w.n_heads * w.ql * w.head_dim * 2
+    ob = w.batch * w.n_heads * w.ql * w.dv * 2
     kb = w.batch * w.n_kv_heads * w.kl * w.head_dim * 2
-    # q k v o dO dq dk dv + the f32 dQ accumulator
-    return 5 * qb + 4 * kb + 2 * qb
+    vb = w.batch * w.n_kv_heads * w.kl * w.dv * 2
+    # q, dq, o (twice), dO + k, dk + v, dv + the f32 dQ accumulator (read and written)
+    return 2 * qb + 3 * ob + 2 * kb + 2 * vb + 4 * qb
 
 
 # ------------------------------------------------------------------ our arm
@@ -291,12 +300,15 @@ def run_ours(args, w):
     h_q, h_k, h_v, h_do = (bf(t).pin_memory() for t in (inp.q, inp.k, inp.v, inp.do))
     q, k, v, do = (t.to(dev) for t in (h_q, h_k, h_v, h_do))
     mask = None if inp.mask is None else torch.from_numpy(inp.mask).to(dev)
-    o = torch.empty_like(q)
+    o = torch.empty(w.o_shape(), dtype=q.dtype, device=dev)
     lse = torch.empty(w.lse_shape(), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     params = fa.FaParams(w.batch, w.n_heads, w.n_kv_heads, w.ql, w.kl, w.head_dim, w.scale,
                          int(w.causal))
-    opts = fa.make_options(q, k, mask, (w.window_left, w.window_right))
+    sinks = None if inp.sinks is None else torch.from_numpy(inp.sinks).to(dev)
+    dsinks = None if sinks is None else torch.empty_like(sinks)
+    opts = fa.make_options(q, k, mask, (w.window_left, w.window_right), v=v, sinks=sinks,
+                           dsinks=dsinks)
     stream = torch.cuda.current_stream(dev)
 
     def step():

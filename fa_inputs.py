@@ -24,7 +24,7 @@ import numpy as np
 SEED_BASE = 0x5452_4149_4E30_3031
 
 # tensor_idx part of a seed: seed = SEED_BASE + 16 * workload_index + tensor_idx
-T_Q, T_K, T_V, T_DO, T_MASK = 0, 1, 2, 3, 4
+T_Q, T_K, T_V, T_DO, T_MASK, T_SINK = 0, 1, 2, 3, 4, 5
 
 
 @dataclass(frozen=True)
@@ -46,6 +46,8 @@ class Workload:
     # j > q_abs + window_right (q_abs = kl - ql + i); -1 leaves that side unbounded
     window_left: int = -1
     window_right: int = -1
+    value_dim: int = 0  # head dim of v, O, dO (0 = head_dim)
+    sinks: bool = False  # one sink logit per query head, N(0, 1) in natural-log units
 
     @property
     def windowed(self) -> bool:
@@ -60,6 +62,16 @@ class Workload:
 
     def kv_shape(self):
         return (self.batch, self.n_kv_heads, self.kl, self.head_dim)
+
+    @property
+    def dv(self) -> int:
+        return self.value_dim or self.head_dim
+
+    def v_shape(self):
+        return (self.batch, self.n_kv_heads, self.kl, self.dv)
+
+    def o_shape(self):
+        return (self.batch, self.n_heads, self.ql, self.dv)
 
     def lse_shape(self):
         return (self.batch, self.n_heads, self.ql)
@@ -82,7 +94,8 @@ class Workload:
         return int(np.maximum(0, hi - lo + 1).sum())
 
     def flops(self, exact: bool = False):
-        """(fwd, bwd) FLOPs: 4*B*H*ql*kl*d*f and 10*B*H*ql*kl*d*f.
+        """(fwd, bwd) FLOPs: 4*B*H*ql*kl*d*f and 10*B*H*ql*kl*d*f, or with a value head dim
+        dv != d: 2*(d + dv) (QK^T, PV) and 2*(3d + 2dv) (S, dP, dV, dK, dQ) per pair.
 
         f = 0.5 for causal (the headline counting rule), 1 otherwise; with exact=True, or with a
         window (which has no such rule), f is the visible fraction of (query, key) pairs.
@@ -91,8 +104,9 @@ class Workload:
             f = self.visible_pairs() / (self.ql * self.kl)
         else:
             f = 0.5 if self.causal else 1.0
-        base = self.batch * self.n_heads * self.ql * self.kl * self.head_dim * f
-        return 4.0 * base, 10.0 * base
+        pairs = self.batch * self.n_heads * self.ql * self.kl * f
+        d, dv = self.head_dim, self.dv
+        return 2.0 * (d + dv) * pairs, 2.0 * (3 * d + 2 * dv) * pairs
 
 
 # The workloads, in order (index = workload_index in the seed formula; new ones go last).
@@ -105,6 +119,12 @@ WORKLOADS = [
     # sliding-window causal attention: every row sees its last 4096 keys (itself included)
     Workload("swa_d128_16k", 1, 32, 8, 16384, 16384, 128, 1.0 / math.sqrt(128.0), True,
              do_std=0.1, window_left=4095),
+    # the headline shape with a sink logit per query head
+    Workload("gqa_d128_4k_sinks", 2, 32, 8, 4096, 4096, 128, 1.0 / math.sqrt(128.0), True,
+             do_std=0.1, sinks=True),
+    # the headline shape with a value head dim of 64 (q, k keep 128)
+    Workload("gqa_d128_dv64_4k", 2, 32, 8, 4096, 4096, 128, 1.0 / math.sqrt(128.0), True,
+             do_std=0.1, value_dim=64),
 ]
 BY_NAME = {w.name: w for w in WORKLOADS}
 
@@ -158,6 +178,7 @@ class Inputs:
     v: np.ndarray
     do: np.ndarray
     mask: np.ndarray | None
+    sinks: np.ndarray | None = None  # f32 [H] holding exact bf16 values
 
     def widened(self):
         """(q, k, v, dO) as f32 arrays holding the exact bf16 values."""
@@ -171,7 +192,8 @@ def make_inputs(w: Workload, index: int | None = None, seed_base: int | None = N
     base = (SEED_BASE if seed_base is None else seed_base) + 16 * index
     q = normal_bf16(base + T_Q, w.q_shape())
     k = normal_bf16(base + T_K, w.kv_shape())
-    v = normal_bf16(base + T_V, w.kv_shape())
-    do = normal_bf16(base + T_DO, w.q_shape(), w.do_std)
+    v = normal_bf16(base + T_V, w.v_shape())
+    do = normal_bf16(base + T_DO, w.o_shape(), w.do_std)
     mask = additive_mask(base + T_MASK, w.mask_shape()) if w.masked else None
-    return Inputs(q, k, v, do, mask)
+    sinks = bf16_bits_to_f32(normal_bf16(base + T_SINK, (w.n_heads,))) if w.sinks else None
+    return Inputs(q, k, v, do, mask, sinks)

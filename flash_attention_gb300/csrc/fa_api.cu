@@ -265,6 +265,7 @@ int fa_train_fwd_ex(const void* q, const void* k, const void* v, const void* mas
   a.ql = p->ql;
   a.kl = p->kl;
   a.d = p->head_dim;
+  a.dval = op->value_dim ? op->value_dim : p->head_dim;
   a.scale = p->scale;
   const fa::Band band = fa::make_band(p->causal, op->window_left, op->window_right);
   a.lo_off = band.lo_off;
@@ -274,7 +275,7 @@ int fa_train_fwd_ex(const void* q, const void* k, const void* v, const void* mas
   const int qrows = fa::fwd_q_box_rows(a.d), kvrows = fa::fwd_kv_box_rows(a.d);
   if (!encode_bf16_3d(&m.q, q, a.B * a.H, a.ql, a.d, qrows) ||
       !encode_bf16_3d(&m.k, k, a.B * a.Hk, a.kl, a.d, kvrows) ||
-      !encode_bf16_3d(&m.v, v, a.B * a.Hk, a.kl, a.d, kvrows))
+      !encode_bf16_3d(&m.v, v, a.B * a.Hk, a.kl, a.dval, kvrows))
     return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
   e = fa::launch_fwd(a, m, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
@@ -324,6 +325,7 @@ static int prepare_bwd(const void* q, const void* k, const void* v, const void* 
   a->ql = p->ql;
   a->kl = p->kl;
   a->d = p->head_dim;
+  a->dval = op->value_dim ? op->value_dim : p->head_dim;
   a->ql_pad = fa::bwd_ql_pad(a->ql);
   a->scale = p->scale;
   const fa::Band band = fa::make_band(p->causal, op->window_left, op->window_right);
@@ -338,9 +340,9 @@ static int prepare_bwd(const void* q, const void* k, const void* v, const void* 
 static int encode_bwd_maps(const fa::BwdArgs& a, fa::BwdMaps* m) {
   const int qrows = fa::bwd_q_box_rows(a.d), kvrows = fa::bwd_kv_box_rows(a.d);
   if (!encode_bf16_3d(&m->q, a.q, a.B * a.H, a.ql, a.d, qrows) ||
-      !encode_bf16_3d(&m->dO, a.dO, a.B * a.H, a.ql, a.d, qrows) ||
+      !encode_bf16_3d(&m->dO, a.dO, a.B * a.H, a.ql, a.dval, qrows) ||
       !encode_bf16_3d(&m->k, a.k, a.B * a.Hk, a.kl, a.d, kvrows) ||
-      !encode_bf16_3d(&m->v, a.v, a.B * a.Hk, a.kl, a.d, kvrows))
+      !encode_bf16_3d(&m->v, a.v, a.B * a.Hk, a.kl, a.dval, kvrows))
     return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
   return FA_OK;
 }
@@ -445,7 +447,8 @@ const char* fa_last_cuda_error(void) { return g_last_cuda_error; }
 const char* fa_version(void) { return "fa_gb300 0.1 (sm_103a, tcgen05)"; }
 
 int fa_value_dim_supported(int head_dim, int value_dim) {
-  return (head_dim == 64 || head_dim == 128 || head_dim == 256) && value_dim == head_dim;
+  if (value_dim == head_dim) return head_dim == 64 || head_dim == 128 || head_dim == 256;
+  return head_dim == 128 && value_dim == 64;
 }
 
 }  // extern "C"

@@ -67,20 +67,25 @@ struct BwdTraits<256> {
 
 constexpr int kBN = 128;  // kv rows per CTA (the M of the kv-major MMAs)
 
-template <int HD>
+// HD: head dim of Q, K (and dQ, dK); DV: head dim of V, O, dO (and dV).
+template <int HD, int DV>
 struct BwdLayout {
   using T = BwdTraits<HD>;
   static constexpr int BM = T::BM;
-  static constexpr int DH = HD / T::DSPLIT;  // head-dim slice this CTA produces
+  static constexpr int DH = HD / T::DSPLIT;   // head-dim slice of dK this CTA produces
+  static constexpr int DVH = DV / T::DSPLIT;  // ... of dV
   static constexpr int KCH = HD / 64;
-  static constexpr int KV_BYTES = kBN * HD * 2;
+  static constexpr int VCH = DV / 64;
+  static constexpr int K_BYTES = kBN * HD * 2;
+  static constexpr int V_BYTES = kBN * DV * 2;
   static constexpr int QT_BYTES = BM * HD * 2;
+  static constexpr int DOT_BYTES = BM * DV * 2;
   static constexpr int DS_BYTES = kBN * BM * 2;
   static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = OFF_K + KV_BYTES;
-  static constexpr int OFF_Q = OFF_V + KV_BYTES;                // ST x Q tile
+  static constexpr int OFF_V = OFF_K + K_BYTES;
+  static constexpr int OFF_Q = OFF_V + V_BYTES;                 // ST x Q tile
   static constexpr int OFF_DO = OFF_Q + T::ST * QT_BYTES;       // ST x dO tile
-  static constexpr int OFF_DS = OFF_DO + T::ST * QT_BYTES;      // 2 x dS^T [kv][q] swizzled
+  static constexpr int OFF_DS = OFF_DO + T::ST * DOT_BYTES;     // 2 x dS^T [kv][q] swizzled
   static constexpr int OFF_L = OFF_DS + 2 * DS_BYTES;           // ST x BM f32
   static constexpr int OFF_D = OFF_L + T::ST * BM * 4;          // ST x BM f32
   static constexpr int OFF_STG = OFF_D + T::ST * BM * 4;            // dQ staging [BM][HD] f32
@@ -91,7 +96,7 @@ struct BwdLayout {
   static constexpr int COL_S0 = 0;
   static constexpr int COL_DP0 = T::NSB * BM;
   static constexpr int COL_DV = (T::NSB + 2) * BM;
-  static constexpr int COL_DK = COL_DV + DH;
+  static constexpr int COL_DK = COL_DV + DVH;
   static constexpr int TMEM_USED = COL_DK + DH;
   static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
   static constexpr int DQ_COLS = T::DQT ? BM : HD;
@@ -105,6 +110,8 @@ struct BwdLayout {
   static_assert(T::DQT ? DH == 128 : BM == 128, "every MMA has M = 128");
   static_assert(T::LOOKAHEAD ? T::ST >= (T::NSB == 2 ? 3 : 2) : true, "ring too shallow");
   static_assert(!T::DQ_BULK || (T::DQT && T::DSPLIT == 1), "bulk dQ needs whole [q][d] rows");
+  static_assert(T::DSPLIT == 1 || DV == HD, "a split head dim needs DV == HD");
+  static_assert(DVH % 16 == 0 && DVH >= 16 && DVH <= 256, "dV MMA N");
 };
 
 struct BwdKParams {
@@ -136,7 +143,7 @@ __host__ __device__ constexpr int prep_rows_per_block() {
   return (256 / (HD / 8)) * 4;
 }
 
-template <int HD>
+template <int HD, int DV>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
                                                        const __nv_bfloat16* __restrict__ dO,
                                                        const float* __restrict__ lse,
@@ -146,10 +153,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
                                                        const float* __restrict__ sinks,
                                                        float* __restrict__ dsink_part, int BH,
                                                        int H, int ql, int ql_pad) {
-  constexpr int TPR = HD / 8;            // threads per row (8 bf16 = 16 bytes each)
+  constexpr int TPR = DV / 8;            // threads per O / dO row (8 bf16 = 16 bytes each)
   constexpr int RPB = 256 / TPR;         // rows per pass of the block
   constexpr int ROWS = 4;                // passes per block
-  static_assert(RPB * ROWS == prep_rows_per_block<HD>(), "prep chunk");
+  static_assert(RPB * ROWS == prep_rows_per_block<DV>(), "prep chunk");
   static_assert(RPB * ROWS >= kPrepRowsMin && RPB * ROWS <= 256, "sink partial layout");
   __shared__ float sink_terms[RPB * ROWS];
   const int sub = threadIdx.x % TPR;
@@ -163,7 +170,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
       a[r] = make_uint4(0, 0, 0, 0);
       g[r] = make_uint4(0, 0, 0, 0);
       if (i < ql) {
-        const size_t base = ((size_t)bh * ql + i) * HD + sub * 8;
+        const size_t base = ((size_t)bh * ql + i) * DV + sub * 8;
         a[r] = *reinterpret_cast<const uint4*>(o + base);
         g[r] = *reinterpret_cast<const uint4*>(dO + base);
       }
@@ -303,14 +310,15 @@ __device__ __forceinline__ void st_swizzled(uint8_t* chunk, int j, int g, uint4 
   *reinterpret_cast<uint4*>(chunk + j * 128 + ((g ^ (j & 7)) << 4)) = val;
 }
 
-template <int HD, int BAND, int MASKT>
-__global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
+template <int HD, int DV, int BAND, int MASKT>
+__global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                     const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mDO,
                     const BwdKParams p) {
   using T = BwdTraits<HD>;
-  using LY = BwdLayout<HD>;
+  using LY = BwdLayout<HD, DV>;
   constexpr int BM = T::BM, DH = LY::DH, KCH = LY::KCH, ST = T::ST, NSB = T::NSB;
+  constexpr int DVH = LY::DVH, VCH = LY::VCH;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -377,11 +385,11 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
       tma_prefetch_desc(&mDO);
       int last_use[ST];
       for (int s = 0; s < ST; ++s) last_use[s] = -1;
-      mbar_arrive_expect_tx(&kv_full, 2 * LY::KV_BYTES);
-      for (int c = 0; c < KCH; ++c) {
+      mbar_arrive_expect_tx(&kv_full, LY::K_BYTES + LY::V_BYTES);
+      for (int c = 0; c < KCH; ++c)
         tma_load_3d(smem + LY::OFF_K + c * kBN * 128, &mK, &kv_full, c * 64, n0, bkh);
+      for (int c = 0; c < VCH; ++c)
         tma_load_3d(smem + LY::OFF_V + c * kBN * 128, &mV, &kv_full, c * 64, n0, bkh);
-      }
       for (int it = 0; it < n_iter; ++it) {
         const int st = it % ST;
         const uint32_t use = it / ST;
@@ -389,13 +397,13 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
         const int h = kh * G + it / nm;
         const int q0 = (m_first + it % nm) * BM;
         const int bh = b * p.H + h;
-        mbar_arrive_expect_tx(&qdo_full[st], 2 * LY::QT_BYTES + 2 * BM * 4);
-        for (int c = 0; c < KCH; ++c) {
+        mbar_arrive_expect_tx(&qdo_full[st], LY::QT_BYTES + LY::DOT_BYTES + 2 * BM * 4);
+        for (int c = 0; c < KCH; ++c)
           tma_load_3d(smem + LY::OFF_Q + st * LY::QT_BYTES + c * BM * 128, &mQ, &qdo_full[st],
                       c * 64, q0, bh);
-          tma_load_3d(smem + LY::OFF_DO + st * LY::QT_BYTES + c * BM * 128, &mDO,
+        for (int c = 0; c < VCH; ++c)
+          tma_load_3d(smem + LY::OFF_DO + st * LY::DOT_BYTES + c * BM * 128, &mDO,
                       &qdo_full[st], c * 64, q0, bh);
-        }
         bulk_load(smem + LY::OFF_L + st * BM * 4, p.lse2 + (size_t)bh * p.ql_pad + q0, BM * 4,
                   &qdo_full[st]);
         bulk_load(smem + LY::OFF_D + st * BM * 4, p.dvec + (size_t)bh * p.ql_pad + q0, BM * 4,
@@ -414,11 +422,13 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
       const Desc vd = make_desc(sV, 16, 1024);          // V as a K-major operand
       const Desc kmn = make_desc(sK, kBN * 128, 1024);  // K as an MN-major operand
       const uint32_t id_s = idesc_bf16(128, BM, 0, 0);      // S^T, dP^T: [kv x q]
-      const uint32_t id_acc = idesc_bf16(128, DH, 0, 1);    // dV, dK: A tmem, B MN-major
+      const uint32_t id_dv = idesc_bf16(128, DVH, 0, 1);    // dV: A tmem, B MN-major
+      const uint32_t id_dk = idesc_bf16(128, DH, 0, 1);     // dK: A tmem, B MN-major
       const uint32_t id_dq = T::DQT ? idesc_bf16(DH, BM, 1, 1) : idesc_bf16(BM, HD, 1, 1);
       const uint32_t tDV = tbase + LY::COL_DV, tDK = tbase + LY::COL_DK;
-      // head-dim slice of Q / dO used as the B operand of dV, dK (MN-major, N = DH)
+      // head-dim slices of Q (for dK, N = DH) and dO (for dV, N = DVH): MN-major B operands
       const uint32_t slice = (dh * DH / 64) * (BM * 128);
+      const uint32_t vslice = (dh * DVH / 64) * (BM * 128);
       bool ok = mbar_wait(&kv_full, 0, &abort_flag);
       int q_ready = -1;  // highest iteration whose Q/dO stage wait is done
 
@@ -449,10 +459,10 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
           tc_fence_after();
         }
         if (!ok) return;
-        const Desc dod = make_desc(smem_u32(smem + LY::OFF_DO + (it % ST) * LY::QT_BYTES), 16, 1024);
+        const Desc dod = make_desc(smem_u32(smem + LY::OFF_DO + (it % ST) * LY::DOT_BYTES), 16, 1024);
         const uint32_t tDP = tbase + LY::COL_DP0 + (it % 2) * BM;
 #pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks) {
+        for (int ks = 0; ks < DV / 16; ++ks) {  // contraction over the value head dim
           const uint32_t ko = (ks / 4) * (kBN * 128) + (ks % 4) * 32;
           const uint32_t qo = (ks / 4) * (BM * 128) + (ks % 4) * 32;
           mma_ss2(tDP, vd.at(ko), vd.hi, dod.at(qo), dod.hi, id_s, ks > 0 ? 1u : 0u);
@@ -468,7 +478,7 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
       for (int it = 0; it < n_iter && ok; ++it) {
         const int st = it % ST;
         const Desc qmn = make_desc(smem_u32(smem + LY::OFF_Q + st * LY::QT_BYTES), BM * 128, 1024);
-        const Desc domn = make_desc(smem_u32(smem + LY::OFF_DO + st * LY::QT_BYTES), BM * 128, 1024);
+        const Desc domn = make_desc(smem_u32(smem + LY::OFF_DO + st * LY::DOT_BYTES), BM * 128, 1024);
         const uint32_t tS = tbase + LY::COL_S0 + (it % NSB) * BM;
         const uint32_t tDP = tbase + LY::COL_DP0 + (it % 2) * BM;
         const Desc dsd = make_desc(smem_u32(smem + LY::OFF_DS + (it % 2) * LY::DS_BYTES), kBN * 128, 1024);
@@ -478,7 +488,7 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < BM / 16; ++ks)
-          mma_ts2(tDV, tS + ks * 8, domn.at(slice + ks * 2048), domn.hi, id_acc,
+          mma_ts2(tDV, tS + ks * 8, domn.at(vslice + ks * 2048), domn.hi, id_dv,
                   (it > 0 || ks > 0) ? 1u : 0u);
         if constexpr (T::LOOKAHEAD) {
           if (it + 1 < n_iter) {
@@ -501,7 +511,7 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < BM / 16; ++ks)
-          mma_ts2(tDK, tDP + ks * 8, qmn.at(slice + ks * 2048), qmn.hi, id_acc,
+          mma_ts2(tDK, tDP + ks * 8, qmn.at(slice + ks * 2048), qmn.hi, id_dk,
                   (it > 0 || ks > 0) ? 1u : 0u);
         mma_commit(&qdo_empty[st]);
         if constexpr (!T::LOOKAHEAD) {
@@ -802,14 +812,15 @@ __global__ void __launch_bounds__(BwdLayout<HD>::THREADS, 1)
       tc_fence_after();
       have = ok && n_iter > 0;
     }
-    const size_t rowoff = ((size_t)bkh * p.kl + (kv < p.kl ? kv : 0)) * HD + dh * DH;
+    const size_t kvrow = (size_t)bkh * p.kl + (kv < p.kl ? kv : 0);
 #pragma unroll 1
     for (int which = 0; which < 2; ++which) {
       const uint32_t col = which == 0 ? LY::COL_DV : LY::COL_DK;
       const float mul = which == 0 ? 1.0f : p.scale;
-      __nv_bfloat16* out = (which == 0 ? p.dv : p.dk) + rowoff;
+      const int width = which == 0 ? DVH : DH;  // columns of the slice this CTA owns
+      __nv_bfloat16* out = which == 0 ? p.dv + kvrow * DV + dh * DVH : p.dk + kvrow * HD + dh * DH;
 #pragma unroll 1
-      for (int c = 0; c < DH; c += 32) {
+      for (int c = 0; c < width; c += 32) {
         uint32_t r[32];
         if (have) {
           tmem_ld32(lane_base + col + c, r);
@@ -860,10 +871,10 @@ void bwd_carve_workspace(void* base, int B, int H, int ql, int d, float** lse2, 
   *dsink_part = reinterpret_cast<float*>(p + 2 * align256(rows * 4) + align256(rows * d * 4));
 }
 
-template <int HD, int BAND, int MASKT>
+template <int HD, int DV, int BAND, int MASKT>
 static cudaError_t launch_main_t(const BwdArgs& a, const BwdMaps& m, cudaStream_t s) {
-  using LY = BwdLayout<HD>;
-  auto kern = bwd_main_kernel<HD, BAND, MASKT>;
+  using LY = BwdLayout<HD, DV>;
+  auto kern = bwd_main_kernel<HD, DV, BAND, MASKT>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
@@ -899,35 +910,35 @@ static cudaError_t launch_main_t(const BwdArgs& a, const BwdMaps& m, cudaStream_
   return e;
 }
 
-template <int HD, int BAND>
+template <int HD, int DV, int BAND>
 static cudaError_t launch_main_m(const BwdArgs& a, const BwdMaps& m, cudaStream_t s) {
-  if (!a.mask) return launch_main_t<HD, BAND, 0>(a, m, s);
+  if (!a.mask) return launch_main_t<HD, DV, BAND, 0>(a, m, s);
   switch (a.mask_type) {
-    case 0: return launch_main_t<HD, BAND, 1>(a, m, s);
-    case 1: return launch_main_t<HD, BAND, 2>(a, m, s);
-    default: return launch_main_t<HD, BAND, 3>(a, m, s);
+    case 0: return launch_main_t<HD, DV, BAND, 1>(a, m, s);
+    case 1: return launch_main_t<HD, DV, BAND, 2>(a, m, s);
+    default: return launch_main_t<HD, DV, BAND, 3>(a, m, s);
   }
 }
 
-template <int HD>
+template <int HD, int DV>
 static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t s) {
   const int BH = a.B * a.H;
-  constexpr int rows_per_block = prep_rows_per_block<HD>();  // divides 128, hence ql_pad
+  constexpr int rows_per_block = prep_rows_per_block<DV>();  // divides 128, hence ql_pad
   const int sink_chunks = a.ql_pad / rows_per_block;
   float* dsink_part = a.dsinks != nullptr ? a.dsink_part : nullptr;
   {
     dim3 grid(sink_chunks, BH < 65535 ? BH : 65535);
     profile_mark(kKernBwdPrep, 0, s);
-    bwd_prep_kernel<HD><<<grid, 256, 0, s>>>(
+    bwd_prep_kernel<HD, DV><<<grid, 256, 0, s>>>(
         reinterpret_cast<const __nv_bfloat16*>(a.o), reinterpret_cast<const __nv_bfloat16*>(a.dO),
         a.lse, a.lse2, a.dvec, a.dqacc, a.sinks, dsink_part, BH, a.H, a.ql, a.ql_pad);
     cudaError_t e = cudaGetLastError();
     profile_mark(kKernBwdPrep, 1, s);
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = a.band == kBandNone     ? launch_main_m<HD, kBandNone>(a, m, s)
-                  : a.band == kBandCausal ? launch_main_m<HD, kBandCausal>(a, m, s)
-                                          : launch_main_m<HD, kBandWindow>(a, m, s);
+  cudaError_t e = a.band == kBandNone     ? launch_main_m<HD, DV, kBandNone>(a, m, s)
+                  : a.band == kBandCausal ? launch_main_m<HD, DV, kBandCausal>(a, m, s)
+                                          : launch_main_m<HD, DV, kBandWindow>(a, m, s);
   if (e != cudaSuccess) return e;
   {
     const long long groups = (long long)a.ql * (HD / 8);  // 8-value groups per head
@@ -971,12 +982,11 @@ cudaError_t noalloc_scratch(void** ptr) {
 }
 
 cudaError_t launch_bwd(const BwdArgs& a, const BwdMaps& m, cudaStream_t stream) {
-  switch (a.d) {
-    case 64: return launch_bwd_d<64>(a, m, stream);
-    case 128: return launch_bwd_d<128>(a, m, stream);
-    case 256: return launch_bwd_d<256>(a, m, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  if (a.d == 64 && a.dval == 64) return launch_bwd_d<64, 64>(a, m, stream);
+  if (a.d == 128 && a.dval == 128) return launch_bwd_d<128, 128>(a, m, stream);
+  if (a.d == 256 && a.dval == 256) return launch_bwd_d<256, 256>(a, m, stream);
+  if (a.d == 128 && a.dval == 64) return launch_bwd_d<128, 64>(a, m, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace fa

@@ -55,19 +55,22 @@ struct FwdTraits<256> {
   static constexpr int NQ = 1, BN = 64, NS = 2, STAGES = 2, POLY = 0;
 };
 
-template <int HD>
+// HD: head dim of Q and K; DV: head dim of V and O (the value head dim).
+template <int HD, int DV>
 struct FwdLayout {
   using T = FwdTraits<HD>;
-  static constexpr int KCH = HD / 64;                         // 128-byte column chunks
+  static constexpr int KCH = HD / 64;                         // 128-byte column chunks of Q, K
+  static constexpr int VCH = DV / 64;                         // ... of V
   static constexpr int Q_TILE_BYTES = kBM * HD * 2;
-  static constexpr int KV_TILE_BYTES = T::BN * HD * 2;
+  static constexpr int K_TILE_BYTES = T::BN * HD * 2;
+  static constexpr int V_TILE_BYTES = T::BN * DV * 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + T::NQ * Q_TILE_BYTES;
-  static constexpr int OFF_V = OFF_K + T::STAGES * KV_TILE_BYTES;
-  static constexpr int OFF_END = OFF_V + T::STAGES * KV_TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + T::STAGES * K_TILE_BYTES;
+  static constexpr int OFF_END = OFF_V + T::STAGES * V_TILE_BYTES;
   static constexpr int SMEM_BYTES = OFF_END + 1024;  // + alignment slack
-  // TMEM columns of tile t: O at t*TILE_COLS, S buffer s at t*TILE_COLS + HD + s*BN.
-  static constexpr int TILE_COLS = HD + T::NS * T::BN;
+  // TMEM columns of tile t: O at t*TILE_COLS, S buffer s at t*TILE_COLS + DV + s*BN.
+  static constexpr int TILE_COLS = DV + T::NS * T::BN;
   static constexpr int TMEM_COLS_USED = T::NQ * TILE_COLS;
   static constexpr int TMEM_COLS = TMEM_COLS_USED <= 256 ? 256 : 512;
   static constexpr int THREADS = T::NQ * 128 + 64;  // softmax warpgroups + TMA + MMA warps
@@ -130,13 +133,14 @@ __device__ __forceinline__ void fwd_tile_range(int m0, int t, const FwdKParams& 
   last = (int)((khi + BN - 1) / BN);
 }
 
-template <int HD, int BAND, int MASKT>
-__global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
+template <int HD, int DV, int BAND, int MASKT>
+__global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                const __grid_constant__ CUtensorMap mV, const FwdKParams p) {
   using T = FwdTraits<HD>;
-  using LY = FwdLayout<HD>;
+  using LY = FwdLayout<HD, DV>;
   constexpr int NQ = T::NQ, BN = T::BN, NS = T::NS, STAGES = T::STAGES, KCH = LY::KCH;
+  constexpr int VCH = LY::VCH;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -229,15 +233,15 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
         const int st = (j - J0) % STAGES;
         const uint32_t use = (j - J0) / STAGES;
         if (use > 0 && !mbar_wait(&k_empty[st], (use - 1) & 1, &abort_flag)) break;
-        mbar_arrive_expect_tx(&k_full[st], LY::KV_TILE_BYTES);
+        mbar_arrive_expect_tx(&k_full[st], LY::K_TILE_BYTES);
         for (int c = 0; c < KCH; ++c)
-          tma_load_3d_hint(smem + LY::OFF_K + st * LY::KV_TILE_BYTES + c * BN * 128, &mK,
+          tma_load_3d_hint(smem + LY::OFF_K + st * LY::K_TILE_BYTES + c * BN * 128, &mK,
                            &k_full[st], c * 64, j * BN, bkh, pol_kv);
         last_k[st] = j - J0;
         if (use > 0 && !mbar_wait(&v_empty[st], (use - 1) & 1, &abort_flag)) break;
-        mbar_arrive_expect_tx(&v_full[st], LY::KV_TILE_BYTES);
-        for (int c = 0; c < KCH; ++c)
-          tma_load_3d_hint(smem + LY::OFF_V + st * LY::KV_TILE_BYTES + c * BN * 128, &mV,
+        mbar_arrive_expect_tx(&v_full[st], LY::V_TILE_BYTES);
+        for (int c = 0; c < VCH; ++c)
+          tma_load_3d_hint(smem + LY::OFF_V + st * LY::V_TILE_BYTES + c * BN * 128, &mV,
                            &v_full[st], c * 64, j * BN, bkh, pol_kv);
         last_v[st] = j - J0;
       }
@@ -252,7 +256,7 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
     // ------------------------------------------------------------------ MMA issuer
     if (elect_one()) {
       const uint32_t idesc_s = idesc_bf16(kBM, BN, 0, 0);
-      const uint32_t idesc_o = idesc_bf16(kBM, HD, 0, 1);
+      const uint32_t idesc_o = idesc_bf16(kBM, DV, 0, 1);
       const uint32_t sq = smem_u32(smem + LY::OFF_Q);
       const uint32_t sk = smem_u32(smem + LY::OFF_K);
       const uint32_t sv = smem_u32(smem + LY::OFF_V);
@@ -284,9 +288,9 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
         }
         if (!ok) return;
         const int jj = j - jt0[t];  // == j without a window
-        const uint32_t d_tmem = tbase + t * LY::TILE_COLS + HD + (jj % NS) * BN;
+        const uint32_t d_tmem = tbase + t * LY::TILE_COLS + DV + (jj % NS) * BN;
         const Desc qa = make_desc(sq + t * LY::Q_TILE_BYTES, 16, 1024);
-        const Desc kb = make_desc(sk + st * LY::KV_TILE_BYTES, 16, 1024);
+        const Desc kb = make_desc(sk + st * LY::K_TILE_BYTES, 16, 1024);
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks)
           mma_ss2(d_tmem, qa.at((ks / 4) * (kBM * 128) + (ks % 4) * 32), qa.hi,
@@ -319,8 +323,8 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
           }
           tc_fence_after();
           const uint32_t o_tmem = tbase + t * LY::TILE_COLS;
-          const uint32_t p_tmem = o_tmem + HD + sb * BN;
-          const Desc vb = make_desc(sv + st * LY::KV_TILE_BYTES, BN * 128, 1024);
+          const uint32_t p_tmem = o_tmem + DV + sb * BN;
+          const Desc vb = make_desc(sv + st * LY::V_TILE_BYTES, BN * 128, 1024);
 #pragma unroll
           for (int ks = 0; ks < BN / 16; ++ks)
             mma_ts2(o_tmem, p_tmem + ks * 8, vb.at(ks * 2048), vb.hi, idesc_o,
@@ -383,7 +387,7 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t][sb], (j / NS) & 1, &abort_flag));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t s_addr = lane_base + o_col + HD + sb * BN;
+      const uint32_t s_addr = lane_base + o_col + DV + sb * BN;
       uint32_t sr[BN / 32][32];
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
@@ -432,7 +436,7 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < HD; c += 32) {
+          for (int c = 0; c < DV; c += 32) {
             uint32_t orr[32];
             tmem_ld32(lane_base + o_col + c, orr);
             tmem_wait_ld();
@@ -493,9 +497,9 @@ __global__ void __launch_bounds__(FwdLayout<HD>::THREADS, 1)
     const bool live = ok && l > 0.0f;
     const bool have_o = live && ntt > 0;
     const float inv = have_o ? 1.0f / l : 0.0f;
-    __nv_bfloat16* orow = p.o + ((size_t)bh * p.ql + (i < p.ql ? i : 0)) * HD;
+    __nv_bfloat16* orow = p.o + ((size_t)bh * p.ql + (i < p.ql ? i : 0)) * DV;
 #pragma unroll 1
-    for (int c = 0; c < HD; c += 32) {
+    for (int c = 0; c < DV; c += 32) {
       uint32_t orr[32];
       if (ok && ntt > 0) {
         tmem_ld32(lane_base + o_col + c, orr);
@@ -530,10 +534,10 @@ int fwd_kv_box_rows(int d) {
   return d == 64 ? FwdTraits<64>::BN : d == 128 ? FwdTraits<128>::BN : FwdTraits<256>::BN;
 }
 
-template <int HD, int BAND, int MASKT>
+template <int HD, int DV, int BAND, int MASKT>
 static cudaError_t launch_fwd_t(const FwdArgs& a, const FwdMaps& m, cudaStream_t stream) {
-  using LY = FwdLayout<HD>;
-  auto kern = fwd_kernel<HD, BAND, MASKT>;
+  using LY = FwdLayout<HD, DV>;
+  auto kern = fwd_kernel<HD, DV, BAND, MASKT>;
   static bool attr_set = false;  // per instantiation; the attribute is per device function
   if (!attr_set) {
     cudaError_t e =
@@ -566,32 +570,31 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, const FwdMaps& m, cudaStream_t
   return e;
 }
 
-template <int HD, int BAND>
+template <int HD, int DV, int BAND>
 static cudaError_t launch_fwd_m(const FwdArgs& a, const FwdMaps& m, cudaStream_t s) {
-  if (!a.mask) return launch_fwd_t<HD, BAND, 0>(a, m, s);
+  if (!a.mask) return launch_fwd_t<HD, DV, BAND, 0>(a, m, s);
   switch (a.mask_type) {
-    case 0: return launch_fwd_t<HD, BAND, 1>(a, m, s);
-    case 1: return launch_fwd_t<HD, BAND, 2>(a, m, s);
-    default: return launch_fwd_t<HD, BAND, 3>(a, m, s);
+    case 0: return launch_fwd_t<HD, DV, BAND, 1>(a, m, s);
+    case 1: return launch_fwd_t<HD, DV, BAND, 2>(a, m, s);
+    default: return launch_fwd_t<HD, DV, BAND, 3>(a, m, s);
   }
 }
 
-template <int HD>
+template <int HD, int DV>
 static cudaError_t launch_fwd_d(const FwdArgs& a, const FwdMaps& m, cudaStream_t s) {
   switch (a.band) {
-    case kBandNone: return launch_fwd_m<HD, kBandNone>(a, m, s);
-    case kBandCausal: return launch_fwd_m<HD, kBandCausal>(a, m, s);
-    default: return launch_fwd_m<HD, kBandWindow>(a, m, s);
+    case kBandNone: return launch_fwd_m<HD, DV, kBandNone>(a, m, s);
+    case kBandCausal: return launch_fwd_m<HD, DV, kBandCausal>(a, m, s);
+    default: return launch_fwd_m<HD, DV, kBandWindow>(a, m, s);
   }
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, const FwdMaps& m, cudaStream_t stream) {
-  switch (a.d) {
-    case 64: return launch_fwd_d<64>(a, m, stream);
-    case 128: return launch_fwd_d<128>(a, m, stream);
-    case 256: return launch_fwd_d<256>(a, m, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  if (a.d == 64 && a.dval == 64) return launch_fwd_d<64, 64>(a, m, stream);
+  if (a.d == 128 && a.dval == 128) return launch_fwd_d<128, 128>(a, m, stream);
+  if (a.d == 256 && a.dval == 256) return launch_fwd_d<256, 256>(a, m, stream);
+  if (a.d == 128 && a.dval == 64) return launch_fwd_d<128, 64>(a, m, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace fa

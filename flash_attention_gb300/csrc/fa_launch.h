@@ -51,6 +51,7 @@ struct FwdArgs {
   const float* sinks; // [H] natural-log sink logits, or nullptr
   int* status;        // device status word (nullable)
   int B, H, Hk, ql, kl, d;
+  int dval;           // value head dim (of v and o)
   float scale;
   int lo_off, hi_off;
   int band;  // BandMode
@@ -91,6 +92,7 @@ struct BwdArgs {
   float* dsink_part;   // workspace [B*H, sink_chunks]: per-block partial sums of dsinks
   int* status;
   int B, H, Hk, ql, kl, d, ql_pad;
+  int dval;  // value head dim (of v, o, dO, dV)
   float scale;
   int lo_off, hi_off;
   int band;  // BandMode

@@ -89,6 +89,7 @@ def to_device(inp: fa_inputs.Inputs):
 
     dev = {"q": bf(inp.q), "k": bf(inp.k), "v": bf(inp.v), "do": bf(inp.do)}
     dev["mask"] = None if inp.mask is None else torch.from_numpy(inp.mask).cuda()
+    dev["sinks"] = None if inp.sinks is None else torch.from_numpy(inp.sinks).cuda()
     return dev
 
 
@@ -101,12 +102,14 @@ def run_gpu(w: fa_inputs.Workload, inp: fa_inputs.Inputs, bwd=True):
     d = to_device(inp)
     win = (w.window_left, w.window_right) if w.windowed else None
     o, lse = fa.attention_fwd(d["q"], d["k"], d["v"], scale=w.scale, causal=w.causal,
-                              mask=d["mask"], window=win)
+                              mask=d["mask"], window=win, sinks=d["sinks"])
     out = {"o": o, "lse": lse}
     if bwd:
-        dq, dk, dv = fa.attention_bwd(d["q"], d["k"], d["v"], o, lse, d["do"], scale=w.scale,
-                                      causal=w.causal, mask=d["mask"], window=win)
-        out.update(dq=dq, dk=dk, dv=dv)
+        g = fa.attention_bwd(d["q"], d["k"], d["v"], o, lse, d["do"], scale=w.scale,
+                             causal=w.causal, mask=d["mask"], window=win, sinks=d["sinks"])
+        out.update(dq=g[0], dk=g[1], dv=g[2])
+        if d["sinks"] is not None:
+            out["dsinks"] = g[3]
     torch.cuda.synchronize()
     assert fa.fa_device_status(True) == fa.FA_OK, "a kernel gave up a bounded wait"
     return {k: v.float().cpu().numpy().astype(np.float64) for k, v in out.items()}
@@ -114,12 +117,15 @@ def run_gpu(w: fa_inputs.Workload, inp: fa_inputs.Inputs, bwd=True):
 
 def oracle_full(w: fa_inputs.Workload, inp: fa_inputs.Inputs, bwd=True):
     q, k, v, do = inp.widened()
-    with oracle.window(w.window_left, w.window_right):
+    with oracle.window(w.window_left, w.window_right), oracle.sinks(inp.sinks):
         o, lse = oracle.fwd(q, k, v, inp.mask, scale=w.scale, causal=w.causal)
         res = {"o": o, "lse": lse}
         if bwd:
             dq, dk, dv = oracle.bwd(q, k, v, inp.mask, do, scale=w.scale, causal=w.causal)
             res.update(dq=dq, dk=dk, dv=dv)
+            if inp.sinks is not None:
+                res["dsinks"] = oracle.dsinks(q, k, v, inp.mask, do, scale=w.scale,
+                                              causal=w.causal)
     return res
 
 
@@ -130,4 +136,6 @@ def compare_full(w, gpu, ref, label):
     if "dq" in gpu:
         for n in ("dq", "dk", "dv"):
             stats.update(check_grad(gpu[n], ref[n], n, label))
+    if "dsinks" in gpu:
+        stats.update(check_grad(gpu["dsinks"], ref["dsinks"], "dsinks", label))
     return stats

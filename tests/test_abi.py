@@ -174,7 +174,9 @@ def test_dsinks_rules_in_the_backward(lib):
 
 def test_value_dim_without_kernels_is_unsupported(lib):
     assert not lib.fa_value_dim_supported(128, 96)
+    assert not lib.fa_value_dim_supported(64, 128)
     assert lib.fa_value_dim_supported(128, 128)
+    assert lib.fa_value_dim_supported(128, 64)
     assert _fwd_ex(lib, GOOD, _opts(value_dim=96)) == fa.FA_ERR_UNSUPPORTED
     assert _bwd_ex(lib, GOOD, _opts(value_dim=96)) == fa.FA_ERR_UNSUPPORTED
 

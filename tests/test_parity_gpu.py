@@ -91,7 +91,8 @@ def _sample_rows(w, rng, n=48):
     return np.array(sorted(rows), np.int64)
 
 
-FULL_SIZE = ["train_d64", "gqa_d128_4k", "rect_d256", "swa_d128_16k"]
+FULL_SIZE = ["train_d64", "gqa_d128_4k", "rect_d256", "swa_d128_16k", "gqa_d128_4k_sinks",
+             "gqa_d128_dv64_4k"]
 
 
 @pytest.mark.parametrize("name", FULL_SIZE)
@@ -103,14 +104,21 @@ def test_full_size_sampled(name):
     q, k, v, do = inp.widened()
     rng = np.random.default_rng(1234 + idx)
     rows = _sample_rows(w, rng)
-    with oracle.window(w.window_left, w.window_right):
+    with oracle.window(w.window_left, w.window_right), oracle.sinks(inp.sinks):
         _check_sampled(w, inp, gpu, q, k, v, do, rows, rng)
 
 
 def _check_sampled(w, inp, gpu, q, k, v, do, rows, rng):
+    if inp.sinks is not None:
+        # dsinks over every row (too many for the oracle at this size): the definition
+        # -sum_{b,i} exp(sink_h - L) * rowsum(dO * O), evaluated in f64 from the GPU's own L
+        # and stored O, must match the kernel's fixed-order f32 sum
+        D = (gpu["o"] * do.astype(np.float64)).sum(-1)
+        want = -(np.exp(inp.sinks.astype(np.float64)[None, :, None] - gpu["lse"]) * D).sum((0, 2))
+        parity.check_grad(gpu["dsinks"], want, "dsinks (definition)", w.name)
     o_r, l_r = oracle.fwd_rows(q, k, v, inp.mask, scale=w.scale, causal=w.causal, rows=rows)
     d = w.head_dim
-    parity.check_o(gpu["o"].reshape(-1, d)[rows], o_r, w.name)
+    parity.check_o(gpu["o"].reshape(-1, w.dv)[rows], o_r, w.name)
     parity.check_l(gpu["lse"].reshape(-1)[rows], l_r, w.name)
     dq_r = oracle.bwd_q_rows(q, k, v, inp.mask, do, scale=w.scale, causal=w.causal, rows=rows)
     # the gradient bound scales with max|dQ| of the whole tensor, taken from the GPU result
