@@ -26,6 +26,7 @@
 //  * with causal masking, key tiles that lie wholly above a query tile's diagonal are never
 //    loaded or multiplied, and the CTAs with the most work are launched first.
 #include <float.h>
+#include "fa_band.cuh"
 #include "fa_common.cuh"
 #include "fa_launch.h"
 
@@ -112,25 +113,13 @@ __device__ __forceinline__ float mask_log2(const void* mrow, long long j) {
 template <int HD, int BAND>
 __device__ __forceinline__ void fwd_tile_range(int m0, int t, const FwdKParams& p, int& first,
                                                int& last) {
-  constexpr int BN = FwdTraits<HD>::BN;
-  const int r1 = min(m0 + (t + 1) * kBM, p.ql) - 1;  // last row of the tile (clamped)
-  const int off = p.kl - p.ql;
-  if (BAND != kBandWindow) {
-    int kend = p.kl;
-    if (BAND == kBandCausal) kend = min(kend, off + r1 + 1);  // exclusive key bound
-    first = 0;
-    last = kend <= 0 ? 0 : (kend + BN - 1) / BN;
-    return;
-  }
   const int r0 = m0 + t * kBM;
-  const long long klo = max(0LL, (long long)off + r0 + p.lo_off);
-  const long long khi = min((long long)p.kl, (long long)off + r1 + p.hi_off + 1);  // exclusive
-  if (r0 >= p.ql || khi <= klo) {
+  if (BAND == kBandWindow && r0 >= p.ql) {  // a tile wholly past the last query row
     first = last = -1;
     return;
   }
-  first = (int)(klo / BN);
-  last = (int)((khi + BN - 1) / BN);
+  const int r1 = min(m0 + (t + 1) * kBM, p.ql) - 1;  // last row of the tile (clamped)
+  band_kv_tiles<FwdTraits<HD>::BN, BAND>(r0, r1, p.ql, p.kl, p.lo_off, p.hi_off, first, last);
 }
 
 template <int HD, int DV, int BAND, int MASKT>
@@ -371,15 +360,10 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
              (b_ * p.msb + h_ * p.msh + (long long)i * p.msq) * es;
     }
 
-    // Running max (base 2) starts at the finite sentinel and the row sum at 0; a sink starts
-    // them at the sink's logit and its exp2 share (1, or 0 for a sink of -inf).
+    // running max (base 2, from the finite sentinel) and row sum over the keys; a sink joins
+    // only in the epilogue
     float m_used = -FLT_MAX / 2.0f;
     float l = 0.0f;
-    if (p.sinks != nullptr) {
-      const float s2 = __ldg(p.sinks + bh % p.H) * kLog2e;
-      m_used = fmaxf(s2, m_used);
-      l = ex2(s2 - m_used);
-    }
     bool ok = true;
 
     for (int j = 0; j < ntt; ++j) {  // j: iteration of this query tile (kv tile kt0 + j)
@@ -492,11 +476,26 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&o_final[t], 0, &abort_flag));
       tc_fence_after();
     }
-    // L is finite whenever the normaliser is positive (keys seen, or a sink); O exists in TMEM
-    // only when some kv tile was visited.
-    const bool live = ok && l > 0.0f;
-    const bool have_o = live && ntt > 0;
-    const float inv = have_o ? 1.0f / l : 0.0f;
+    // O = O_acc * inv and L from the keys' normaliser l * 2^m_used. A sink adds 2^s2 to the
+    // normaliser here, in log2 form so that nothing overflows: keeping it out of the running
+    // max leaves the largest key's weight at exactly 1, so the bf16 rounding of P costs a row
+    // dominated by one key no more than without a sink. O exists in TMEM only when some kv
+    // tile was visited.
+    const bool have_o = ok && ntt > 0 && l > 0.0f;
+    float inv = have_o ? 1.0f / l : 0.0f;
+    float L = (ok && l > 0.0f) ? m_used * kLn2 + logf(l) : -INFINITY;
+    if (p.sinks != nullptr && ok) {
+      const float s2 = __ldg(p.sinks + bh % p.H) * kLog2e;  // -inf: no sink
+      if (l > 0.0f) {
+        const float lm = m_used + log2f(l);
+        const float mx = fmaxf(lm, s2);
+        const float L2 = mx + log2f(exp2f(lm - mx) + exp2f(s2 - mx));
+        inv = exp2f(m_used - L2);
+        L = L2 * kLn2;
+      } else {
+        L = s2 * kLn2;  // a row that sees no key: O = 0, L = sink
+      }
+    }
     __nv_bfloat16* orow = p.o + ((size_t)bh * p.ql + (i < p.ql ? i : 0)) * DV;
 #pragma unroll 1
     for (int c = 0; c < DV; c += 32) {
@@ -520,7 +519,7 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
                                packed[4 * v4 + 3]);
       }
     }
-    if (i < p.ql) p.lse[(size_t)bh * p.ql + i] = live ? m_used * kLn2 + logf(l) : -INFINITY;
+    if (i < p.ql) p.lse[(size_t)bh * p.ql + i] = L;
   }
 
   tc_fence_before();

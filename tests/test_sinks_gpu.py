@@ -103,3 +103,32 @@ def test_sinks_fwd_bwd(idx):
     if dead.any():
         assert (gpu["o"][dead] == 0).all()
     print(_ids(CASES[idx]), stats)
+
+
+def test_sink_above_the_scores_keeps_single_key_rows_accurate():
+    """Sinks larger than every score. Causal row 0 sees one key, so O_0 = w * v_0 with
+    w = 1 / (1 + exp(sink - s_00)): the weight must be formed in f32, not by rounding the key's
+    P to bf16 relative to the sink (an error of up to 2^-9 |O|). Row 0 is held to half a bf16
+    ulp of the output plus 2e-4 relative; all rows to the usual O and L tolerances."""
+    import torch
+
+    import flash_attention_gb300 as fa
+
+    w = fa_inputs.Workload("sink_high", 1, 4, 2, 256, 256, 128, 128 ** -0.5, True)
+    inp = fa_inputs.make_inputs(w, index=50)
+    sinks = np.array([3.0, 5.0, 8.0, 2.5], np.float32)
+    dev = parity.to_device(inp)
+    s_t = torch.from_numpy(sinks).cuda()
+    o, lse = fa.attention_fwd(dev["q"], dev["k"], dev["v"], scale=w.scale, causal=True,
+                              sinks=s_t)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(True) == fa.FA_OK
+    q, k, v, _ = inp.widened()
+    with oracle.sinks(sinks):
+        o_r, l_r = oracle.fwd(q, k, v, None, scale=w.scale, causal=True)
+    o_g = o.float().cpu().numpy().astype(np.float64)
+    parity.check_o(o_g, o_r, "sink_high")
+    parity.check_l(lse.float().cpu().numpy(), l_r, "sink_high")
+    row0_err = np.abs(o_g[:, :, 0] - o_r[:, :, 0])
+    bound = 0.5 * parity.bf16_ulp(o_r[:, :, 0]) + 2e-4 * np.maximum(1.0, np.abs(o_r[:, :, 0]))
+    assert (row0_err <= bound).all(), f"single-key row: max error {row0_err.max():.3e}"
