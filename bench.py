@@ -40,10 +40,28 @@ import fa_inputs  # noqa: E402
 METRIC = "attention fwd+bwd TFLOP/s (bf16, causal) at 1 GB300; % of dense bf16 tensor peak"
 DEFAULT_WORKLOAD = "gqa_d128_4k"
 KERNEL_SOURCES = {
-    "fwd_kernel": ["flash_attention_gb300/csrc/fa_fwd.cu", "flash_attention_gb300/csrc/fa_common.cuh"],
+    "fwd_kernel": ["flash_attention_gb300/csrc/fa_fwd.cu", "flash_attention_gb300/csrc/fa_common.cuh",
+                   "flash_attention_gb300/csrc/fa_band.cuh"],
     "bwd_main_kernel": ["flash_attention_gb300/csrc/fa_bwd.cu",
                         "flash_attention_gb300/csrc/fa_common.cuh"],
+    "bwd_dq_det_kernel": ["flash_attention_gb300/csrc/fa_bwd_dq.cu",
+                          "flash_attention_gb300/csrc/fa_common.cuh",
+                          "flash_attention_gb300/csrc/fa_band.cuh"],
 }
+
+
+def kernel_flops(w):
+    """Algorithmic FLOPs of one launch of each tensor-core kernel, by the workload's counting
+    rule: the forward 2(d + dv) per pair; the backward main pass 2(3d + 2dv) (S, dP, dV, dK,
+    dQ), or 2(2d + 2dv) in deterministic mode, where the dQ kernel does 2(2d + dv) (S, dP, dQ)."""
+    fwd_f, bwd_f = w.flops()
+    d, dv = w.head_dim, w.dv
+    pairs = bwd_f / (2.0 * (3 * d + 2 * dv))
+    out = {"fwd_kernel": fwd_f, "bwd_main_kernel": bwd_f}
+    if w.deterministic:
+        out["bwd_main_kernel"] = pairs * 2.0 * (2 * d + 2 * dv)
+        out["bwd_dq_det_kernel"] = pairs * 2.0 * (2 * d + dv)
+    return out
 
 
 def parse():
@@ -257,6 +275,7 @@ def config_of(w, n):
             **({"window": [w.window_left, w.window_right]} if w.windowed else {}),
             **({"value_dim": w.dv} if w.dv != w.head_dim else {}),
             **({"sinks": True} if w.sinks else {}),
+            **({"deterministic": True} if w.deterministic else {}),
             "flop_rule": "fwd 4*B*H*ql*kl*d*f, bwd 10*B*H*ql*kl*d*f, "
                          + ("f = visible fraction of (query, key) pairs under the window"
                             if w.windowed else "f=0.5 causal"),
@@ -308,7 +327,7 @@ def run_ours(args, w):
     sinks = None if inp.sinks is None else torch.from_numpy(inp.sinks).to(dev)
     dsinks = None if sinks is None else torch.empty_like(sinks)
     opts = fa.make_options(q, k, mask, (w.window_left, w.window_right), v=v, sinks=sinks,
-                           dsinks=dsinks)
+                           dsinks=dsinks, deterministic=w.deterministic)
     stream = torch.cuda.current_stream(dev)
 
     def step():
@@ -376,7 +395,7 @@ def run_ours(args, w):
     launches_per_step = sum(n for _, n in prof.values()) / args.steps
     dom = max(prof.items(), key=lambda kv: kv[1][0])
     dom_name, (dom_ms, dom_n) = dom
-    algo = {"fwd_kernel": fwd_f, "bwd_main_kernel": bwd_f}.get(dom_name, 0.0)
+    algo = kernel_flops(w).get(dom_name, 0.0)
     dom_avg = dom_ms / max(dom_n, 1)
     achieved = algo / (dom_avg * 1e-3) / 1e12
     traffic = recorded_traffic(dom_name, w.name)

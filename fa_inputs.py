@@ -48,6 +48,7 @@ class Workload:
     window_right: int = -1
     value_dim: int = 0  # head dim of v, O, dO (0 = head_dim)
     sinks: bool = False  # one sink logit per query head, N(0, 1) in natural-log units
+    deterministic: bool = False  # the backward's bitwise-reproducible mode
 
     @property
     def windowed(self) -> bool:
@@ -125,6 +126,9 @@ WORKLOADS = [
     # the headline shape with a value head dim of 64 (q, k keep 128)
     Workload("gqa_d128_dv64_4k", 2, 32, 8, 4096, 4096, 128, 1.0 / math.sqrt(128.0), True,
              do_std=0.1, value_dim=64),
+    # the headline shape with the deterministic backward
+    Workload("gqa_d128_4k_det", 2, 32, 8, 4096, 4096, 128, 1.0 / math.sqrt(128.0), True,
+             do_std=0.1, deterministic=True),
 ]
 BY_NAME = {w.name: w for w in WORKLOADS}
 

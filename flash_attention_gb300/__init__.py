@@ -47,6 +47,8 @@ class FaOptions(ctypes.Structure):
         ("mask_stride_q", ctypes.c_int64),
         ("sinks", ctypes.c_void_p),
         ("dsinks", ctypes.c_void_p),
+        ("deterministic", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
     ]
 
 
@@ -176,16 +178,19 @@ def fa_train_bwd(q, k, v, o, lse, dO, mask, dq, dk, dv, params: FaParams, stream
         raise FaError(rc, "fa_train_bwd")
 
 
-def make_options(q, k, mask=None, window=(-1, -1), v=None, sinks=None, dsinks=None) -> FaOptions:
+def make_options(q, k, mask=None, window=(-1, -1), v=None, sinks=None, dsinks=None,
+                 deterministic=False) -> FaOptions:
     """fa_options for a mask tensor of any supported dtype (float32, bfloat16, bool) whose shape
     broadcasts to [B, H, ql, kl] with the keys contiguous, a (left, right) window, the value
-    head dim of `v` (when it differs from q's), and float32 [H] sinks / dsinks tensors."""
+    head dim of `v` (when it differs from q's), float32 [H] sinks / dsinks tensors, and the
+    deterministic backward."""
     import torch
 
     B, H, ql, d = q.shape
     kl = k.shape[2]
     wl, wr = window if window is not None else (-1, -1)
-    opt = FaOptions(int(wl), int(wr), FA_MASK_F32, 0, 0, 0, 0, None, None)
+    opt = FaOptions(int(wl), int(wr), FA_MASK_F32, 0, 0, 0, 0, None, None,
+                    1 if deterministic else 0, 0)
     if v is not None and v.shape[-1] != d:
         opt.value_dim = int(v.shape[-1])
     if mask is not None:
@@ -245,7 +250,7 @@ def fa_device_status(clear: bool = True) -> int:
     return load_library().fa_device_status(int(bool(clear)))
 
 
-FA_NUM_KERNELS = 4
+FA_NUM_KERNELS = 5
 
 
 def fa_profile_enable(on: bool) -> None:
@@ -303,19 +308,21 @@ def attention_fwd(q, k, v, *, scale, causal, mask=None, window=None, sinks=None,
 
 
 def attention_bwd(q, k, v, o, lse, dO, *, scale, causal, mask=None, window=None, sinks=None,
-                  stream=None):
+                  deterministic=False, stream=None):
     """Allocate dQ, dK, dV and run the backward: returns (dq, dk, dv), or (dq, dk, dv, dsinks)
-    when `sinks` is given. `mask`, `window` and `sinks` as given to attention_fwd."""
+    when `sinks` is given. `mask`, `window` and `sinks` as given to attention_fwd;
+    `deterministic` makes every output bitwise reproducible (dQ from its own kernel)."""
     import torch
 
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
     params = make_params(q, k, scale=scale, causal=causal)
-    if _plain_call(q, k, v, mask, window, sinks):
+    if _plain_call(q, k, v, mask, window, sinks) and not deterministic:
         fa_train_bwd(q, k, v, o, lse, dO, mask, dq, dk, dv, params, stream)
         return dq, dk, dv
     dsinks = None if sinks is None else torch.empty_like(sinks)
     fa_train_bwd_ex(q, k, v, o, lse, dO, mask, dq, dk, dv, params,
-                    make_options(q, k, mask, window, v=v, sinks=sinks, dsinks=dsinks), stream)
+                    make_options(q, k, mask, window, v=v, sinks=sinks, dsinks=dsinks,
+                                 deterministic=deterministic), stream)
     return (dq, dk, dv) if sinks is None else (dq, dk, dv, dsinks)

@@ -109,6 +109,8 @@ fa_options default_options(const fa_params* p) {
   o.value_dim = 0;
   o.sinks = nullptr;
   o.dsinks = nullptr;
+  o.deterministic = 0;
+  o.reserved = 0;
   o.mask_stride_q = p->kl;
   o.mask_stride_h = (int64_t)p->ql * p->kl;
   o.mask_stride_b = (int64_t)p->n_heads * p->ql * p->kl;
@@ -120,6 +122,7 @@ fa_options default_options(const fa_params* p) {
 int check_options(const fa_options* o, const void* mask, const fa_params* p, bool bwd) {
   if (o->window_left < -1 || o->window_right < -1) return FA_ERR_INVALID;
   if (o->value_dim < 0) return FA_ERR_INVALID;
+  if ((o->deterministic != 0 && o->deterministic != 1) || o->reserved != 0) return FA_ERR_INVALID;
   if (o->sinks && !aligned(o->sinks, 4)) return FA_ERR_INVALID;
   if (bwd && o->dsinks && (!o->sinks || !aligned(o->dsinks, 4))) return FA_ERR_INVALID;
   if (o->mask_type != FA_MASK_F32 && o->mask_type != FA_MASK_BF16 && o->mask_type != FA_MASK_BOOL)
@@ -155,7 +158,7 @@ std::mutex g_prof_mu;
 std::vector<ProfRec> g_prof_recs;
 std::vector<cudaEvent_t> g_prof_pool;
 ProfRec g_prof_open[fa::kNumKernels];
-bool g_prof_is_open[fa::kNumKernels] = {false, false, false, false};
+bool g_prof_is_open[fa::kNumKernels] = {};
 
 cudaEvent_t prof_event() {
   if (!g_prof_pool.empty()) {
@@ -228,6 +231,7 @@ const char* fa_kernel_name(int id) {
   switch (id) {
     case FA_KERNEL_FWD: return "fwd_kernel";
     case FA_KERNEL_BWD_PREP: return "bwd_prep_kernel";
+    case FA_KERNEL_BWD_DQ_DET: return "bwd_dq_det_kernel";
     case FA_KERNEL_BWD_MAIN: return "bwd_main_kernel";
     case FA_KERNEL_BWD_DQ: return "bwd_dq_kernel";
     default: return "unknown";
@@ -316,6 +320,7 @@ static int prepare_bwd(const void* q, const void* k, const void* v, const void* 
   a->sinks = op->sinks;
   a->dsinks = op->dsinks;
   a->dsink_part = nullptr;  // set with the workspace
+  a->deterministic = op->deterministic;
   a->dq = dq;
   a->dk = dk;
   a->dv = dv;
@@ -344,6 +349,14 @@ static int encode_bwd_maps(const fa::BwdArgs& a, fa::BwdMaps* m) {
       !encode_bf16_3d(&m->k, a.k, a.B * a.Hk, a.kl, a.d, kvrows) ||
       !encode_bf16_3d(&m->v, a.v, a.B * a.Hk, a.kl, a.dval, kvrows))
     return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+  if (a.deterministic) {
+    const int drows = fa::dq_det_box_rows();
+    if (!encode_bf16_3d(&m->det.q, a.q, a.B * a.H, a.ql, a.d, 128) ||
+        !encode_bf16_3d(&m->det.dO, a.dO, a.B * a.H, a.ql, a.dval, 128) ||
+        !encode_bf16_3d(&m->det.k, a.k, a.B * a.Hk, a.kl, a.d, drows) ||
+        !encode_bf16_3d(&m->det.v, a.v, a.B * a.Hk, a.kl, a.dval, drows))
+      return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+  }
   return FA_OK;
 }
 

@@ -125,6 +125,7 @@ struct BwdKParams {
   int* status;
   int H, Hk, ql, kl, ql_pad;
   int lo_off, hi_off;  // key j is visible to query row i iff q_abs + lo_off <= j <= q_abs + hi_off
+  int skip_dq;         // 1: dQ comes from the deterministic dQ kernel; no dQ work here
   float scale, scale_log2;
 };
 
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
                                                        float* __restrict__ dqacc,
                                                        const float* __restrict__ sinks,
                                                        float* __restrict__ dsink_part, int BH,
-                                                       int H, int ql, int ql_pad) {
+                                                       int H, int ql, int ql_pad, int zero_acc) {
   constexpr int TPR = DV / 8;            // threads per O / dO row (8 bf16 = 16 bytes each)
   constexpr int RPB = 256 / TPR;         // rows per pass of the block
   constexpr int ROWS = 4;                // passes per block
@@ -201,9 +202,12 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
         if (want_dsink) sink_terms[r * RPB + threadIdx.x / TPR] = term;
       }
     }
-    float4* z = reinterpret_cast<float4*>(dqacc + ((size_t)bh * ql_pad + i0) * HD);
+    if (zero_acc) {  // (the deterministic mode has no accumulator)
+      float4* z = reinterpret_cast<float4*>(dqacc + ((size_t)bh * ql_pad + i0) * HD);
 #pragma unroll 4
-    for (int c = threadIdx.x; c < RPB * ROWS * HD / 4; c += 256) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c = threadIdx.x; c < RPB * ROWS * HD / 4; c += 256)
+        z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     if (want_dsink) {  // block-uniform
       __syncthreads();
       if (threadIdx.x < 32) {
@@ -223,14 +227,15 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
 // y = head (strided). Each thread converts 8 consecutive values (two float4 loads, one 16-byte
 // store).
 // Blocks with x == 0 also finish dsinks[h] for h = y, y + gridDim.y, ...: the sum, in a fixed
-// order, of the prep kernel's partials of every batch entry of head h.
+// order, of the prep kernel's partials of every batch entry of head h. With convert = 0 (the
+// deterministic mode, where dQ is written by its own kernel) only that sum is done.
 template <int HD>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ dqacc,
                                                      __nv_bfloat16* __restrict__ dq, int BH,
                                                      int ql, int ql_pad, float scale,
                                                      const float* __restrict__ dsink_part,
                                                      float* __restrict__ dsinks, int B, int H,
-                                                     int sink_chunks) {
+                                                     int sink_chunks, int convert) {
   if (dsinks != nullptr && blockIdx.x == 0) {  // block-uniform
     __shared__ float red[256];
     const int n = B * sink_chunks;
@@ -249,6 +254,7 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
       __syncthreads();  // red is reused by the next head
     }
   }
+  if (!convert) return;
   const int e = blockIdx.x * 256 + threadIdx.x;  // index of the 8-value group within a head
   const int i = e / (HD / 8), c = (e % (HD / 8)) * 8;
   if (i >= ql) return;
@@ -521,8 +527,10 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
             if (!ok) break;
           }
         }
-        // dQ of this tile, into the dP^T buffer (its dS^T has just been read by dK)
-        if constexpr (T::DQT) {
+        // dQ of this tile, into the dP^T buffer (its dS^T has just been read by dK). With
+        // skip_dq the commit below still tells WG1 and WG2 that dK has read the buffers.
+        if (p.skip_dq) {
+        } else if constexpr (T::DQT) {
           // dQ^T[d, q] = sum_kv K[kv, d] dS^T[kv, q]: A = K slice (MN-major), B = dS^T
           const uint32_t kslice = (dh * DH / 64) * (kBN * 128);
 #pragma unroll
@@ -545,7 +553,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
   } else if (warp == LY::BULK_WARP) {
     // ------------------------------------------------------------------ bulk dQ reductions
     if constexpr (T::DQ_BULK) {
-      if (elect_one()) {
+      if (!p.skip_dq && elect_one()) {
         const float* stg = reinterpret_cast<const float*>(smem + LY::OFF_STG);
         for (int it = 0; it < n_iter; ++it) {
           if (!mbar_wait(&stg_full, it & 1, &abort_flag)) break;
@@ -669,6 +677,11 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[it % 2], (it / 2) & 1, &abort_flag));
       if (!ok) return;
       tc_fence_after();
+      if (p.skip_dq) {  // nothing to drain: hand the buffer straight back
+        tc_fence_before();
+        mbar_arrive(&dq_free[it % 2]);
+        return;
+      }
       if constexpr (T::DQ_BULK) {
         // lane = head-dim index, column = query row: stage as [q][d] f32 (contiguous in the
         // accumulator); the bulk warp adds the tile with one reduction. The staging buffer is
@@ -791,7 +804,8 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
             pk[2 * e4 + 1] = pack_bf16(d2, d3);
           }
           tmem_st16(lane_base + colDP + c32 * 16, pk);
-          // dS^T row j, columns c32*32 .. +31: 4 granules of the 64-column chunk c32/2
+          // dS^T row j, columns c32*32 .. +31: 4 granules of the 64-column chunk c32/2 (also
+          // written with skip_dq: a branch here costs the default path more than the stores)
           uint8_t* chunk = sds + (c32 / 2) * (kBN * 128);
 #pragma unroll
           for (int gg = 0; gg < 4; ++gg)
@@ -889,6 +903,7 @@ static cudaError_t launch_main_t(const BwdArgs& a, const BwdMaps& m, cudaStream_
   kp.msq = a.mask_stride_q;
   kp.lo_off = a.lo_off;
   kp.hi_off = a.hi_off;
+  kp.skip_dq = a.deterministic ? 1 : 0;
   kp.lse2 = a.lse2;
   kp.dvec = a.dvec;
   kp.dqacc = a.dqacc;
@@ -931,7 +946,8 @@ static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t
     profile_mark(kKernBwdPrep, 0, s);
     bwd_prep_kernel<HD, DV><<<grid, 256, 0, s>>>(
         reinterpret_cast<const __nv_bfloat16*>(a.o), reinterpret_cast<const __nv_bfloat16*>(a.dO),
-        a.lse, a.lse2, a.dvec, a.dqacc, a.sinks, dsink_part, BH, a.H, a.ql, a.ql_pad);
+        a.lse, a.lse2, a.dvec, a.dqacc, a.sinks, dsink_part, BH, a.H, a.ql, a.ql_pad,
+        a.deterministic ? 0 : 1);
     cudaError_t e = cudaGetLastError();
     profile_mark(kKernBwdPrep, 1, s);
     if (e != cudaSuccess) return e;
@@ -940,13 +956,25 @@ static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t
                   : a.band == kBandCausal ? launch_main_m<HD, DV, kBandCausal>(a, m, s)
                                           : launch_main_m<HD, DV, kBandWindow>(a, m, s);
   if (e != cudaSuccess) return e;
+  if (a.deterministic) {
+    e = launch_dq_det(a, m.det, s);
+    if (e != cudaSuccess) return e;
+    if (a.dsinks != nullptr) {  // the dsinks sum alone
+      profile_mark(kKernBwdDq, 0, s);
+      bwd_dq_kernel<HD><<<dim3(1, a.H < 65535 ? a.H : 65535), 256, 0, s>>>(
+          a.dqacc, reinterpret_cast<__nv_bfloat16*>(a.dq), BH, a.ql, a.ql_pad, a.scale,
+          dsink_part, a.dsinks, a.B, a.H, sink_chunks, 0);
+      profile_mark(kKernBwdDq, 1, s);
+    }
+    return cudaGetLastError();
+  }
   {
     const long long groups = (long long)a.ql * (HD / 8);  // 8-value groups per head
     dim3 grid((unsigned)((groups + 255) / 256), BH < 65535 ? BH : 65535);
     profile_mark(kKernBwdDq, 0, s);
     bwd_dq_kernel<HD><<<grid, 256, 0, s>>>(a.dqacc, reinterpret_cast<__nv_bfloat16*>(a.dq), BH,
                                            a.ql, a.ql_pad, a.scale, dsink_part, a.dsinks, a.B,
-                                           a.H, sink_chunks);
+                                           a.H, sink_chunks, 1);
     profile_mark(kKernBwdDq, 1, s);
   }
   return cudaGetLastError();

@@ -9,7 +9,14 @@
 namespace fa {
 
 // Kernel ids of the timing facility (same values as FA_KERNEL_* in the public header).
-enum KernelId { kKernFwd = 0, kKernBwdPrep = 1, kKernBwdMain = 2, kKernBwdDq = 3, kNumKernels = 4 };
+enum KernelId {
+  kKernFwd = 0,
+  kKernBwdPrep = 1,
+  kKernBwdMain = 2,
+  kKernBwdDq = 3,
+  kKernBwdDqDet = 4,
+  kNumKernels = 5
+};
 
 // Records a timing event before (end = 0) or after (end = 1) a launch on `s` when timing is
 // enabled; does nothing otherwise. Defined in fa_api.cu.
@@ -93,13 +100,20 @@ struct BwdArgs {
   int* status;
   int B, H, Hk, ql, kl, d, ql_pad;
   int dval;  // value head dim (of v, o, dO, dV)
+  int deterministic;  // 1: dQ from the query-tile-major kernel (no cross-CTA additions)
   float scale;
   int lo_off, hi_off;
   int band;  // BandMode
 };
 
+// Tensor maps of the deterministic dQ kernel (boxes: 128 query rows, dq_det_box_rows() keys).
+struct DqMaps {
+  CUtensorMap q, k, v, dO;
+};
+
 struct BwdMaps {
   CUtensorMap q, k, v, dO;
+  DqMaps det;  // encoded only in deterministic mode
 };
 
 int bwd_q_box_rows(int d);
@@ -113,6 +127,10 @@ void bwd_carve_workspace(void* base, int B, int H, int ql, int d, float** lse2, 
                          float** dqacc, float** dsink_part);
 
 cudaError_t launch_bwd(const BwdArgs& a, const BwdMaps& m, cudaStream_t stream);
+
+// Deterministic dQ (fa_bwd_dq.cu): needs lse2 and dvec from the pre-pass; writes a.dq (bf16).
+int dq_det_box_rows();
+cudaError_t launch_dq_det(const BwdArgs& a, const DqMaps& m, cudaStream_t stream);
 
 // Fixed-size device scratch of fa_train_bwd_noalloc (defined in fa_bwd.cu). The first call on a
 // device looks up the array's device address; later calls return the cached address.

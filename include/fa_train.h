@@ -112,7 +112,14 @@ typedef struct fa_params {
  * Value head dim (same page: its shapes list (D, Dv) pairs with Dv != D): value_dim = 0 means
  * head_dim; otherwise v, dV are [B, Hk, kl, value_dim] and o, dO are [B, H, ql, value_dim]
  * while q, k, dQ, dK keep head_dim. Supported pairs (head_dim, value_dim) are listed by
- * fa_value_dim_supported; others give FA_ERR_UNSUPPORTED. */
+ * fa_value_dim_supported; others give FA_ERR_UNSUPPORTED.
+ *
+ * Deterministic backward (the mlx-native page notes that its GPU backward reduces dQ in a
+ * nondeterministic order): with deterministic = 1, dQ is formed query-tile-major by a
+ * separate kernel that walks the kv tiles of each query tile in a fixed order, instead of
+ * being added into an f32 accumulator by many CTAs at once. dK, dV and dsinks are always
+ * reduced in a fixed order, so the whole backward then returns the same bits on every run.
+ * It recomputes S and dP once more, which costs time. Ignored by the forward. */
 typedef struct fa_options {
   int32_t window_left;   /* -1, or >= 0 */
   int32_t window_right;  /* -1, or >= 0 */
@@ -123,6 +130,8 @@ typedef struct fa_options {
   int64_t mask_stride_q; /* >= 0 */
   const float* sinks;    /* NULL, or [n_heads] f32 on the device, 4-byte aligned */
   float* dsinks;         /* backward only: NULL, or [n_heads] f32 output on the device */
+  int32_t deterministic; /* 0 or 1 (backward only) */
+  int32_t reserved;      /* must be 0 */
 } fa_options;
 
 /* 1 if this build has kernels for the (head_dim, value_dim) pair, else 0. */
@@ -169,8 +178,9 @@ int fa_train_bwd(const void* q, const void* k, const void* v, const void* o, con
 #define FA_KERNEL_FWD 0      /* forward (O, L) */
 #define FA_KERNEL_BWD_PREP 1 /* backward pre-pass: D = rowsum(dO * O), scratch zeroing */
 #define FA_KERNEL_BWD_MAIN 2 /* backward main pass: dK, dV, dQ accumulation */
-#define FA_KERNEL_BWD_DQ 3   /* backward dQ conversion to bf16 */
-#define FA_NUM_KERNELS 4
+#define FA_KERNEL_BWD_DQ 3   /* backward dQ conversion to bf16 (and the dsinks sum) */
+#define FA_KERNEL_BWD_DQ_DET 4 /* deterministic mode: query-tile-major dQ */
+#define FA_NUM_KERNELS 5
 
 /* Turns timing on (1) or off (0). Returns FA_OK. */
 int fa_profile_enable(int on);

@@ -38,6 +38,8 @@ def test_library_exports_every_declared_symbol(lib):
 def test_error_strings(lib):
     for code in range(5):
         assert fa.fa_error_string(code)
+    names = [fa.load_library().fa_kernel_name(k).decode() for k in range(fa.FA_NUM_KERNELS)]
+    assert names[-1] == "bwd_dq_det_kernel" and len(set(names)) == fa.FA_NUM_KERNELS
     assert "unknown" in fa.fa_error_string(99)
     assert "sm_103a" in fa.fa_version()
 
@@ -128,7 +130,8 @@ def _bwd_ex(lib, params, opts, mask=None):
 
 def _opts(**kw):
     base = dict(window_left=-1, window_right=-1, mask_type=0, value_dim=0, mask_stride_b=0,
-                mask_stride_h=0, mask_stride_q=128, sinks=None, dsinks=None)
+                mask_stride_h=0, mask_stride_q=128, sinks=None, dsinks=None, deterministic=0,
+                reserved=0)
     base.update(kw)
     return fa.FaOptions(**base)
 
@@ -136,7 +139,7 @@ def _opts(**kw):
 BAD_OPTIONS = [
     dict(window_left=-2), dict(window_right=-5), dict(mask_type=3), dict(mask_type=-1),
     dict(value_dim=-1), dict(mask_stride_b=-1), dict(mask_stride_h=-4),
-    dict(mask_stride_q=-128), dict(sinks=FAKE + 2),
+    dict(mask_stride_q=-128), dict(sinks=FAKE + 2), dict(deterministic=2), dict(reserved=1),
 ]
 
 
@@ -182,6 +185,7 @@ def test_value_dim_without_kernels_is_unsupported(lib):
 
 
 def test_options_struct_layout():
-    assert ctypes.sizeof(fa.FaOptions) == 56
+    assert ctypes.sizeof(fa.FaOptions) == 64
+    assert fa.FaOptions.deterministic.offset == 56
     assert fa.FaOptions.mask_stride_b.offset == 16
     assert fa.FaOptions.sinks.offset == 40 and fa.FaOptions.dsinks.offset == 48
