@@ -201,3 +201,76 @@ def make_inputs(w: Workload, index: int | None = None, seed_base: int | None = N
     mask = additive_mask(base + T_MASK, w.mask_shape()) if w.masked else None
     sinks = bf16_bits_to_f32(normal_bf16(base + T_SINK, (w.n_heads,))) if w.sinks else None
     return Inputs(q, k, v, do, mask, sinks)
+
+
+# ------------------------------------------------------------------ paged KV-cache inputs
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """Queries over a paged key/value cache: `q_len` new positions per sequence (1 = decode),
+    sequence lengths drawn in [min_len, max_len] (the last sequence gets max_len), caches in
+    pages of `page_size` positions placed in a shuffled order with `spare_pages` unused."""
+
+    name: str
+    batch: int
+    n_heads: int
+    n_kv_heads: int
+    q_len: int
+    head_dim: int
+    page_size: int
+    min_len: int
+    max_len: int
+    causal: bool = True
+    spare_pages: int = 3
+
+    @property
+    def scale(self) -> float:
+        return self.head_dim ** -0.5
+
+    @property
+    def max_pages(self) -> int:
+        return (self.max_len + self.page_size - 1) // self.page_size
+
+
+@dataclass
+class PagedInputs:
+    q: np.ndarray            # bf16 bits [B, H, lq, d]
+    k_cache: np.ndarray      # bf16 bits [num_pages, Hk, page_size, d]
+    v_cache: np.ndarray      # bf16 bits [num_pages, Hk, page_size, d]
+    block_table: np.ndarray  # int32 [B, max_pages]
+    lengths: np.ndarray      # int32 [B]
+
+    def widened(self):
+        """(q, k_cache, v_cache) as f32 arrays (NaN where the cache holds no key)."""
+        return tuple(bf16_bits_to_f32(t) for t in (self.q, self.k_cache, self.v_cache))
+
+
+BF16_NAN_BITS = 0x7FC0
+
+
+def make_paged_inputs(w: DecodeWorkload, index: int = 31, seed_base: int | None = None,
+                      poison: bool = True) -> PagedInputs:
+    """Seeded paged inputs. Every cache slot that holds no key of its sequence (past its
+    length, and the spare pages) is set to NaN when `poison` is on, so that a kernel that reads
+    past a sequence's end shows it."""
+    base = (SEED_BASE if seed_base is None else seed_base) + 16 * index
+    rng = np.random.default_rng(base + T_MASK)
+    B, Hk, bs, d = w.batch, w.n_kv_heads, w.page_size, w.head_dim
+    lens = rng.integers(w.min_len, w.max_len + 1, size=B).astype(np.int32)
+    lens[-1] = w.max_len
+    per = w.max_pages
+    n_pages = B * per + w.spare_pages
+    order = rng.permutation(n_pages).astype(np.int32)
+    table = order[:B * per].reshape(B, per).copy()
+    q = normal_bf16(base + T_Q, (B, w.n_heads, w.q_len, d))
+    caches = []
+    for tix in (T_K, T_V):
+        logical = normal_bf16(base + tix, (B, Hk, per * bs, d))  # position-major per sequence
+        if poison:
+            pos = np.arange(per * bs)[None, :] >= lens[:, None]      # [B, positions]
+            logical[np.broadcast_to(pos[:, None, :, None], logical.shape)] = BF16_NAN_BITS
+        cache = np.full((n_pages, Hk, bs, d), BF16_NAN_BITS if poison else 0, np.uint16)
+        # page p of sequence b holds positions p*bs .. p*bs + bs - 1
+        blocks = logical.reshape(B, Hk, per, bs, d).transpose(0, 2, 1, 3, 4)  # [B, per, Hk, bs, d]
+        cache[table.reshape(-1)] = blocks.reshape(B * per, Hk, bs, d)
+        caches.append(cache)
+    return PagedInputs(q, caches[0], caches[1], table, lens)

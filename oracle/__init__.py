@@ -44,6 +44,8 @@ MUTATIONS = {
     "sink_scaled": 14,
     "dsink_sign": 15,
     "v_stride_d": 16,
+    "table_stride": 17,
+    "decode_top_left": 18,
 }
 
 
@@ -77,6 +79,9 @@ def _load():
                                                   i, f, i, f, f, i]
             lib.fa_oracle_bwd.argtypes = [f, f, f, f, f, i, i, i, i, i, i, i, d, i, f, f, f, i]
             lib.fa_oracle_dsinks.argtypes = [f, f, f, f, f, i, i, i, i, i, i, i, d, i, f, i]
+            lib.fa_oracle_paged_fwd.argtypes = [f, f, f, f, f, i, i, i, i, i, i, i, i, d, i, f, f,
+                                                i]
+            lib.fa_oracle_paged_fwd.restype = i
             lib.fa_oracle_set_mutation.argtypes = [i]
             lib.fa_oracle_set_window.argtypes = [i, i]
             lib.fa_oracle_set_sinks.argtypes = [f]
@@ -258,3 +263,25 @@ def dsinks(q, k, v, mask, do, *, scale, causal, nthreads=None):
     if rc:
         raise ValueError(f"oracle dsinks failed ({rc}); is a sinks(...) block active?")
     return out
+
+
+def paged_fwd(q, k_cache, v_cache, block_table, lengths, *, scale, causal, nthreads=None):
+    """Attention of q [B, H, lq, d] over paged caches [num_pages, Hk, page_size, d] with block
+    table [B, max_pages] (int32) and lengths [B] (int32): (O [B, H, lq, d], L [B, H, lq]) in
+    f64. The lq queries are each sequence's last lq positions (bottom-right causal)."""
+    q, kc, vc = _f32(q), _f32(k_cache), _f32(v_cache)
+    table = np.ascontiguousarray(block_table, dtype=np.int32)
+    lens = np.ascontiguousarray(lengths, dtype=np.int32)
+    B, H, lq, d = q.shape
+    P, Hk, bs, dk = kc.shape
+    if dk != d or vc.shape != kc.shape or table.shape[0] != B or lens.shape != (B,):
+        raise ValueError("paged_fwd: inconsistent shapes")
+    o = np.empty((B, H, lq, d), np.float64)
+    lse = np.empty((B, H, lq), np.float64)
+    rc = _load().fa_oracle_paged_fwd(_ptr(q), _ptr(kc), _ptr(vc), _ptr(table), _ptr(lens), B, H,
+                                     Hk, lq, d, bs, table.shape[1], P, float(scale),
+                                     int(bool(causal)), _ptr(o), _ptr(lse),
+                                     nthreads or default_threads())
+    if rc:
+        raise ValueError(f"oracle paged_fwd failed ({rc})")
+    return o, lse

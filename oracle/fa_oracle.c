@@ -63,6 +63,16 @@
  * sentinel -FLT_MAX/2, p = exp2(s - max), L = max*ln(2) + ln(sum p), O = sum (p / safe_sum) v
  * with safe_sum = 1 when the sum is 0. Both modes must agree to rounding on any input.
  *
+ * Attention over a paged key/value cache (page "nuvec-core tests/fast.rs",
+ * `paged_attention_equals_contiguous_attention` and its `paged` helper; page "tang
+ * src/compute/cuda.rs", `kv_attention`, for single-query decode and the cached prefill with
+ * `cache_start`): the keys of sequence b are its first len_b cache positions; logical key j
+ * lives in physical page table[b][j / bs], slot j % bs, of caches shaped
+ * [num_pages, Hk, bs, d]. The lq queries of a sequence are its last lq positions, so with the
+ * causal mask query i sees key j iff j <= len_b - lq + i (the bottom-right alignment above,
+ * per sequence; tang's cached prefill is the case len_b = cache_start + lq). Then the same
+ * definition: s = scale <q, k_j>, L = log sum exp s, O = sum exp(s - L) v_j.
+ *
  * Layouts (all contiguous, row-major): q, dQ [B, H, ql, d]; O, dO [B, H, ql, dv];
  * k, dK [B, Hk, kl, d]; v, dV [B, Hk, kl, dv]; L [B, H, ql]; mask [B, H, ql, kl] or NULL;
  * sinks [H] or NULL (set with fa_oracle_set_sinks).
@@ -106,6 +116,8 @@ enum {
   MUT_SINK_SCALED = 14,    /* sink logit multiplied by the score scale */
   MUT_DSINK_SIGN = 15,     /* dsink without its minus sign */
   MUT_V_STRIDE_D = 16,     /* v rows addressed with the q/k head dim */
+  MUT_TABLE_STRIDE = 17,   /* block-table row stride = the pages a sequence uses, not its capacity */
+  MUT_DECODE_TOP_LEFT = 18, /* paged causal aligned to the first key (q_abs = i) */
 };
 static int g_mutation = 0;
 
@@ -539,5 +551,91 @@ int fa_oracle_dsinks(const float *q, const float *k, const float *v, const float
   for (int h = 0; h < H; ++h) dsinks[h] = 0.0;
   for (long t = 0; t < n; ++t) dsinks[(t / ql) % H] += c.term[t]; /* fixed order */
   free(c.term);
+  return 0;
+}
+
+/* ------------------------------------------------------------------ paged KV cache */
+typedef struct {
+  const float *q, *kc, *vc;
+  const int32_t *table, *lens;
+  int B, H, Hk, lq, d, bs, max_pages, num_pages, causal;
+  double scale;
+  double *o, *lse;
+} paged_ctx;
+
+/* physical (page, slot) of logical key j of sequence b */
+static void paged_locate(const paged_ctx *c, int b, int j, int *page, int *slot) {
+  long stride = c->max_pages;
+  if (g_mutation == MUT_TABLE_STRIDE) stride = (c->lens[b] + c->bs - 1) / c->bs;
+  *page = c->table[(long)b * stride + j / c->bs];
+  *slot = j % c->bs;
+}
+
+static void paged_task(void *vctx, long t, int worker) {
+  (void)worker;
+  const paged_ctx *c = (const paged_ctx *)vctx;
+  const int i = (int)(t % c->lq);
+  const int h = (int)((t / c->lq) % c->H);
+  const int b = (int)(t / ((long)c->lq * c->H));
+  const int kh = h / (c->H / c->Hk);
+  const int len = c->lens[b];
+  const float *qi = c->q + (size_t)t * c->d;
+  double *o = c->o + (size_t)t * c->d;
+  const long qa = (g_mutation == MUT_DECODE_TOP_LEFT) ? (long)i : (long)len - c->lq + i;
+  double *s = (double *)malloc(sizeof(double) * (size_t)(len > 0 ? len : 1));
+  double m = -INFINITY;
+  for (int j = 0; j < len; ++j) {
+    s[j] = -INFINITY;
+    if (c->causal && (long)j > qa) continue;
+    int page, slot;
+    paged_locate(c, b, j, &page, &slot);
+    const float *kj = c->kc + ((((size_t)page * c->Hk + kh) * c->bs + slot) * (size_t)c->d);
+    double dot = 0.0;
+    for (int e = 0; e < c->d; ++e) dot += (double)qi[e] * (double)kj[e];
+    s[j] = c->scale * dot;
+    if (s[j] > m) m = s[j];
+  }
+  for (int e = 0; e < c->d; ++e) o[e] = 0.0;
+  if (m == -INFINITY) {
+    c->lse[t] = -INFINITY; /* a query that sees no key: O = 0, L = -inf */
+    free(s);
+    return;
+  }
+  double z = 0.0;
+  for (int j = 0; j < len; ++j) z += exp(s[j] - m);
+  const double L = m + log(z);
+  for (int j = 0; j < len; ++j) {
+    if (s[j] == -INFINITY) continue;
+    int page, slot;
+    paged_locate(c, b, j, &page, &slot);
+    const float *vj = c->vc + ((((size_t)page * c->Hk + kh) * c->bs + slot) * (size_t)c->d);
+    const double w = exp(s[j] - L);
+    for (int e = 0; e < c->d; ++e) o[e] += w * (double)vj[e];
+  }
+  c->lse[t] = L;
+  free(s);
+}
+
+/* O [B, H, lq, d] and L [B, H, lq] of queries q [B, H, lq, d] over paged caches
+ * kc, vc [num_pages, Hk, bs, d] with block table [B, max_pages] and lengths [B]. Returns -1 on
+ * bad sizes, a length outside [0, max_pages * bs] or a used table entry outside
+ * [0, num_pages). */
+int fa_oracle_paged_fwd(const float *q, const float *kc, const float *vc, const int32_t *table,
+                        const int32_t *lens, int B, int H, int Hk, int lq, int d, int bs,
+                        int max_pages, int num_pages, double scale, int causal, double *o,
+                        double *lse, int nthreads) {
+  if (B <= 0 || H <= 0 || Hk <= 0 || lq <= 0 || d <= 0 || bs <= 0 || max_pages <= 0 ||
+      num_pages <= 0 || H % Hk)
+    return -1;
+  for (int b = 0; b < B; ++b) {
+    if (lens[b] < 0 || (long)lens[b] > (long)max_pages * bs) return -1;
+    for (int p = 0; p < (lens[b] + bs - 1) / bs; ++p) {
+      const int32_t e = table[(long)b * max_pages + p];
+      if (e < 0 || e >= num_pages) return -1;
+    }
+  }
+  paged_ctx c = {q, kc, vc, table, lens, B, H, Hk, lq, d, bs, max_pages, num_pages,
+                 causal ? 1 : 0, scale, o, lse};
+  parallel_for((long)B * H * lq, nthreads, paged_task, &c);
   return 0;
 }

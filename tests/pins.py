@@ -585,6 +585,99 @@ def pin_value_dim_identity():
     return fails
 
 
+# ------------------------------------------------------------------ paged key/value cache
+# (batch, query heads, kv heads, queries, head dim, page size, min len, max len, causal)
+PAGED_CASES = [
+    (1, 4, 4, 1, 16, 4, 9, 9, False),
+    (3, 4, 2, 1, 8, 4, 1, 13, True),
+    (2, 4, 1, 3, 8, 4, 3, 11, True),     # several queries: bottom-right causal per sequence
+    (2, 2, 2, 4, 8, 8, 2, 17, True),     # lq > len for a short sequence: rows with no key
+    (2, 4, 2, 2, 8, 4, 6, 10, False),
+]
+
+
+def _paged(n, case, poison=True):
+    import fa_inputs
+
+    B, H, Hk, lq, d, bs, lo, hi, causal = case
+    w = fa_inputs.DecodeWorkload(f"pin{n}", B, H, Hk, lq, d, bs, lo, hi, causal)
+    return w, fa_inputs.make_paged_inputs(w, index=100 + n, poison=poison)
+
+
+def _gather(cache, table, b, length, bs):
+    """Keys 0 .. length-1 of sequence b as [Hk, length, d] (numpy fancy indexing)."""
+    j = np.arange(length)
+    return cache[table[b, j // bs], :, j % bs, :].transpose(1, 0, 2)
+
+
+def pin_paged_vs_torch():
+    """Each sequence's keys gathered from the pages with numpy, then torch's CPU flash kernel
+    with its own bottom-right causal bias (the sequence's queries are its last positions)."""
+    fails = []
+    for n, case in enumerate(PAGED_CASES):
+        w, x = _paged(n, case)
+        q, kc, vc = x.widened()
+        o, lse = oracle.paged_fwd(q, kc, vc, x.block_table, x.lengths, scale=w.scale,
+                                  causal=w.causal)
+        G = w.n_heads // w.n_kv_heads
+        for b in range(w.batch):
+            L = int(x.lengths[b])
+            if L == 0:
+                continue
+            kb = torch.from_numpy(_gather(kc, x.block_table, b, L, w.page_size)).double()
+            vb = torch.from_numpy(_gather(vc, x.block_table, b, L, w.page_size)).double()
+            qb = torch.from_numpy(q[b:b + 1]).double()
+            bias = torch.zeros(1, w.n_heads, w.q_len, L, dtype=torch.float64)
+            if w.causal:
+                allowed = causal_lower_right(w.q_len, L)._materialize(device="cpu")
+                bias = bias.masked_fill(~allowed, float("-inf"))
+            to, tl = torch.ops.aten._scaled_dot_product_flash_attention_for_cpu(
+                qb, kb[None].repeat_interleave(G, 1), vb[None].repeat_interleave(G, 1), 0.0,
+                False, attn_mask=bias, scale=w.scale)
+            dead = torch.isinf(tl) | torch.isnan(tl)  # rows that see no key
+            to = torch.where(dead[..., None], torch.zeros_like(to), to)
+            tl = torch.where(dead, torch.full_like(tl, float("-inf")), tl)
+            _cmp(f"paged case{n} seq{b} O", o[b:b + 1], to.numpy(), out=fails)
+            _cmp(f"paged case{n} seq{b} L", lse[b:b + 1], tl.numpy(), out=fails)
+    return fails
+
+
+def pin_paged_layout_invariance():
+    """The physical placement of the pages is invisible: a different page order (table
+    updated), and NaN instead of zeros in every slot that holds no key, give identical bits;
+    and the result equals the contiguous oracle on each sequence's gathered keys."""
+    fails = []
+    for n, case in enumerate(PAGED_CASES):
+        w, x = _paged(n, case, poison=True)
+        _, xz = _paged(n, case, poison=False)
+        q, kc, vc = x.widened()
+        o1, l1 = oracle.paged_fwd(q, kc, vc, x.block_table, x.lengths, scale=w.scale,
+                                  causal=w.causal)
+        qz, kz, vz = xz.widened()
+        o0, l0 = oracle.paged_fwd(qz, kz, vz, xz.block_table, xz.lengths, scale=w.scale,
+                                  causal=w.causal)
+        _cmp(f"paged case{n} NaN-free O", o1, o0, tol=0, out=fails)
+        _cmp(f"paged case{n} NaN-free L", l1, l0, tol=0, out=fails)
+        # move every page to a new place
+        rng = np.random.default_rng(7 + n)
+        perm = rng.permutation(kc.shape[0])
+        inv = np.argsort(perm)
+        o2, l2 = oracle.paged_fwd(q, kc[perm], vc[perm], inv[x.block_table].astype(np.int32),
+                                  x.lengths, scale=w.scale, causal=w.causal)
+        _cmp(f"paged case{n} moved pages O", o2, o1, tol=0, out=fails)
+        _cmp(f"paged case{n} moved pages L", l2, l1, tol=0, out=fails)
+        for b in range(w.batch):
+            L = int(x.lengths[b])
+            if L == 0:
+                continue
+            kb = _gather(kc, x.block_table, b, L, w.page_size)[None]
+            vb = _gather(vc, x.block_table, b, L, w.page_size)[None]
+            oc, lc = oracle.fwd(q[b:b + 1], kb, vb, None, scale=w.scale, causal=w.causal)
+            _cmp(f"paged case{n} seq{b} = contiguous O", o1[b:b + 1], oc, tol=1e-15, out=fails)
+            _cmp(f"paged case{n} seq{b} = contiguous L", l1[b:b + 1], lc, tol=1e-15, out=fails)
+    return fails
+
+
 ALL_PINS = [
     pin_fwd_vs_torch_cpu_flash,
     pin_bwd_vs_torch_autograd,
@@ -600,4 +693,6 @@ ALL_PINS = [
     pin_sinks_closed_forms,
     pin_value_dim_vs_torch,
     pin_value_dim_identity,
+    pin_paged_vs_torch,
+    pin_paged_layout_invariance,
 ]
