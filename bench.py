@@ -32,6 +32,8 @@ import subprocess
 import sys
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -47,6 +49,8 @@ KERNEL_SOURCES = {
     "bwd_dq_det_kernel": ["flash_attention_gb300/csrc/fa_bwd_dq.cu",
                           "flash_attention_gb300/csrc/fa_common.cuh",
                           "flash_attention_gb300/csrc/fa_band.cuh"],
+    "paged_attn_kernel": ["flash_attention_gb300/csrc/fa_paged.cu",
+                          "flash_attention_gb300/csrc/fa_common.cuh"],
 }
 
 
@@ -70,7 +74,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(fa_inputs.BY_NAME))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(fa_inputs.BY_NAME) + sorted(fa_inputs.DECODE_BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ncu", action="store_true",
@@ -266,6 +271,209 @@ def run_reference(args, w):
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------------ paged key/value cache
+PAGED_METRIC = "paged attention: key/value bytes read per second (bf16 cache) at 1 GB300"
+
+
+def paged_bytes(w, x):
+    """Algorithmic bytes of one call: every key and value of every sequence once, q, o, lse,
+    the used block-table entries and the lengths."""
+    kv = int(x.lengths.astype(np.int64).sum()) * w.n_kv_heads * w.head_dim * 2 * 2
+    qo = 2 * w.batch * w.n_heads * w.q_len * w.head_dim * 2 + w.batch * w.n_heads * w.q_len * 4
+    pages = int(((x.lengths.astype(np.int64) + w.page_size - 1) // w.page_size).sum())
+    return kv + qo + 4 * pages + 4 * w.batch
+
+
+def paged_config(w, n):
+    return {"workload": w.name, "batch": w.batch, "n_heads": w.n_heads,
+            "n_kv_heads": w.n_kv_heads, "q_len": w.q_len, "head_dim": w.head_dim,
+            "page_size": w.page_size, "lengths": f"uniform in [{w.min_len}, {w.max_len}]",
+            "causal": w.causal, "pages": "shuffled, unused slots NaN",
+            "l2": "inputs larger than L2 (no flush)",
+            "parallelism": "replicas" if n == 1 else f"{n} independent replicas"}
+
+
+def paged_oracle_sample(w, x, budget_s=10.0, cores=None):
+    """The CPU oracle on whole sequences, taken in turn until ~budget_s: (bytes, seconds, n)."""
+    import oracle
+
+    q, kc, vc = x.widened()
+    spent, nbytes, n = 0.0, 0, 0
+    while spent < budget_s and n < w.batch:
+        t0 = time.perf_counter()
+        oracle.paged_fwd(q[n:n + 1], kc, vc, x.block_table[n:n + 1], x.lengths[n:n + 1],
+                         scale=w.scale, causal=w.causal, nthreads=cores)
+        spent += time.perf_counter() - t0
+        nbytes += int(x.lengths[n]) * w.n_kv_heads * w.head_dim * 4
+        n += 1
+    return nbytes, spent, n
+
+
+def run_paged_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    x = fa_inputs.make_paged_inputs(w)
+    cores = cpu_cores()
+    per_step = max(1.0, 120.0 / max(args.steps + args.warmup, 1))
+    for _ in range(args.warmup):
+        paged_oracle_sample(w, x, min(per_step, 2.0), cores)
+    tot_b, tot_s = 0, 0.0
+    for _ in range(args.steps):
+        b_, s_, _ = paged_oracle_sample(w, x, per_step, cores)
+        tot_b += b_
+        tot_s += s_
+    value = tot_b / tot_s / 1e9
+    out = {"impl": "reference", "metric": PAGED_METRIC, "value": value, "unit": "GB/s",
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": tot_s / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": paged_config(w, args.gpus),
+           "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                            "sample": "per step: whole sequences in turn for ~"
+                                      f"{per_step:.0f} s of the CPU oracle"},
+           "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def run_paged(args, w):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import flash_attention_gb300 as fa
+
+    fa.build()
+    fa.load_library()
+    x = fa_inputs.make_paged_inputs(w, seed_base=fa_inputs.SEED_BASE + 1_000_003 * rank)
+
+    def bf(bits):
+        return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16)
+
+    h_q = bf(x.q).pin_memory()
+    h_tb = torch.from_numpy(x.block_table).pin_memory()
+    h_ln = torch.from_numpy(x.lengths).pin_memory()
+    q, tb, ln = h_q.to(dev), h_tb.to(dev), h_ln.to(dev)
+    kc, vc = bf(x.k_cache).to(dev), bf(x.v_cache).to(dev)  # the cache stays on the GPU
+    o = torch.empty_like(q)
+    lse = torch.empty((w.batch, w.n_heads, w.q_len), dtype=torch.float32, device=dev)
+    params = fa.FaPagedParams(w.batch, w.n_heads, w.n_kv_heads, w.q_len, w.head_dim,
+                              w.page_size, x.block_table.shape[1], x.k_cache.shape[0],
+                              w.scale, int(w.causal), 0, 0)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.fa_paged_attention(q, kc, vc, tb, ln, o, lse, params, stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    if args.ncu:
+        for _ in range(args.warmup + args.steps):
+            step()
+        torch.cuda.synchronize()
+        rc = fa.fa_device_status(True)
+        print(f"ncu mode: {args.warmup + args.steps} steps of {w.name}, status {rc}", flush=True)
+        if rc != fa.FA_OK:
+            raise RuntimeError("paged kernel reported an error")
+        return
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if fa.fa_device_status(True) != fa.FA_OK:
+        clocks.stop()
+        raise RuntimeError("paged kernel reported an error during warm-up")
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fa.fa_profile_enable(True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    fa.fa_profile_enable(False)
+    clk = clocks.stop()
+    barrier()
+    prof = fa.fa_profile_read()
+    if fa.fa_device_status(True) != fa.FA_OK:
+        raise RuntimeError("paged kernel reported an error during the timed steps")
+    tot_ms = reduce_max(e0.elapsed_time(e1) / args.steps, world, dev)
+    nbytes = paged_bytes(w, x)
+    value = world * nbytes / (tot_ms * 1e-3) / 1e9
+    peaks = load_peaks()
+    hbm = peaks["hbm_gbs"]
+    ms, n = prof["paged_attn_kernel"]
+    kern_ms = ms / max(n, 1)
+    roofline = {"bound": "hbm", "kernel": "paged_attn_kernel",
+                "achieved": nbytes / (kern_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                "frac": nbytes / (kern_ms * 1e-3) / 1e9 / hbm,
+                "traffic": recorded_traffic("paged_attn_kernel", w.name),
+                "peak_source": f"hbm_gbs, {peaks['source']}",
+                "per_kernel_ms": {k: (t / max(c, 1)) for k, (t, c) in prof.items() if c}}
+    launches = sum(c for _, c in prof.values())
+
+    e2e = None
+    if not args.no_e2e:
+        h_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+
+        def e2e_step():  # new queries, table and lengths in; the attention output back
+            q.copy_(h_q, non_blocking=True)
+            tb.copy_(h_tb, non_blocking=True)
+            ln.copy_(h_ln, non_blocking=True)
+            step()
+            h_o.copy_(o, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        f1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max(f0.elapsed_time(f1) / args.steps, world, dev)
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_tb, h_ln))
+        e2e = {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": h_o.numel() * h_o.element_size(),
+               "note": "the key/value cache stays resident on the GPU, as in serving"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cores = cpu_cores()
+        b_, s_, n_ = paged_oracle_sample(w, x, 10.0, cores)
+        cpu = {"value": b_ / s_ / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n_} whole sequence(s) of {w.batch}, f64, {s_:.1f} s"}
+
+    if rank == 0:
+        out = {"metric": PAGED_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms,
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+               "dtype": "bf16", "data": "synthetic", "config": paged_config(w, world),
+               "bytes_per_step": nbytes, "roofline": roofline, "cpu_baseline": cpu,
+               "e2e": e2e, "gpu_launches": int(launches), "clocks": clk}
+        print(json.dumps(out), flush=True)
 
 
 def config_of(w, n):
@@ -479,6 +687,13 @@ def run_ours(args, w):
 
 def main():
     args = parse()
+    if args.workload in fa_inputs.DECODE_BY_NAME:
+        w = fa_inputs.DECODE_BY_NAME[args.workload]
+        if args.impl == "reference":
+            run_paged_reference(args, w)
+        else:
+            run_paged(args, w)
+        return
     w = fa_inputs.BY_NAME[args.workload]
     if args.impl == "reference":
         run_reference(args, w)

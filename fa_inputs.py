@@ -221,6 +221,7 @@ class DecodeWorkload:
     max_len: int
     causal: bool = True
     spare_pages: int = 3
+    lengths: tuple = ()  # fixed lengths instead of drawn ones
 
     @property
     def scale(self) -> float:
@@ -247,16 +248,21 @@ class PagedInputs:
 BF16_NAN_BITS = 0x7FC0
 
 
-def make_paged_inputs(w: DecodeWorkload, index: int = 31, seed_base: int | None = None,
-                      poison: bool = True) -> PagedInputs:
+def make_paged_inputs(w: DecodeWorkload, index: int | None = None,
+                      seed_base: int | None = None, poison: bool = True) -> PagedInputs:
     """Seeded paged inputs. Every cache slot that holds no key of its sequence (past its
     length, and the spare pages) is set to NaN when `poison` is on, so that a kernel that reads
     past a sequence's end shows it."""
+    if index is None:
+        index = 40 + DECODE_WORKLOADS.index(w) if w in DECODE_WORKLOADS else 31
     base = (SEED_BASE if seed_base is None else seed_base) + 16 * index
     rng = np.random.default_rng(base + T_MASK)
     B, Hk, bs, d = w.batch, w.n_kv_heads, w.page_size, w.head_dim
-    lens = rng.integers(w.min_len, w.max_len + 1, size=B).astype(np.int32)
-    lens[-1] = w.max_len
+    if w.lengths:
+        lens = np.array(w.lengths, np.int32)
+    else:
+        lens = rng.integers(w.min_len, w.max_len + 1, size=B).astype(np.int32)
+        lens[-1] = w.max_len
     per = w.max_pages
     n_pages = B * per + w.spare_pages
     order = rng.permutation(n_pages).astype(np.int32)
@@ -274,3 +280,13 @@ def make_paged_inputs(w: DecodeWorkload, index: int = 31, seed_base: int | None 
         cache[table.reshape(-1)] = blocks.reshape(B * per, Hk, bs, d)
         caches.append(cache)
     return PagedInputs(q, caches[0], caches[1], table, lens)
+
+
+# Paged-cache workloads of the benchmark (index = position + 40 in the seed formula).
+DECODE_WORKLOADS = [
+    # single-query decode: 16 sequences of 2k-16k keys, GQA 32:8, pages of 16 positions
+    DecodeWorkload("paged_decode_d128", 16, 32, 8, 1, 128, 16, 2048, 16384),
+    # four new positions per sequence (causal) against the same kind of cache
+    DecodeWorkload("paged_prefill4_d128", 16, 32, 8, 4, 128, 16, 2048, 16384),
+]
+DECODE_BY_NAME = {w.name: w for w in DECODE_WORKLOADS}

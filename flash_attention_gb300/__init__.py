@@ -17,7 +17,8 @@ __all__ = [
     "FaParams", "fa_train_fwd", "fa_train_bwd", "fa_device_status", "fa_error_string",
     "fa_version", "fa_profile_enable", "fa_profile_read", "attention_fwd", "attention_bwd", "load_library", "build", "LIB_PATH",
     "FA_OK", "FA_ERR_INVALID", "FA_ERR_CUDA", "FA_ERR_DEVICE_TIMEOUT", "FA_ERR_UNSUPPORTED",
-    "FA_ERR_TOO_LARGE", "FaOptions", "fa_train_fwd_ex", "fa_train_bwd_ex", "make_options",
+    "FA_ERR_TOO_LARGE", "FA_ERR_BAD_INPUT", "FaOptions", "FaPagedParams", "paged_attention",
+    "fa_paged_attention", "fa_train_fwd_ex", "fa_train_bwd_ex", "make_options",
     "FA_MASK_F32", "FA_MASK_BF16", "FA_MASK_BOOL",
 ]
 
@@ -27,6 +28,7 @@ FA_ERR_CUDA = 2
 FA_ERR_DEVICE_TIMEOUT = 3
 FA_ERR_UNSUPPORTED = 4
 FA_ERR_TOO_LARGE = 5
+FA_ERR_BAD_INPUT = 6
 
 
 FA_MASK_F32 = 0
@@ -48,6 +50,25 @@ class FaOptions(ctypes.Structure):
         ("sinks", ctypes.c_void_p),
         ("dsinks", ctypes.c_void_p),
         ("deterministic", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
+class FaPagedParams(ctypes.Structure):
+    """Mirror of `fa_paged_params` in include/fa_train.h."""
+
+    _fields_ = [
+        ("batch", ctypes.c_int32),
+        ("n_heads", ctypes.c_int32),
+        ("n_kv_heads", ctypes.c_int32),
+        ("q_len", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("max_pages", ctypes.c_int32),
+        ("num_pages", ctypes.c_int32),
+        ("scale", ctypes.c_float),
+        ("causal", ctypes.c_int32),
+        ("num_splits", ctypes.c_int32),
         ("reserved", ctypes.c_int32),
     ]
 
@@ -101,6 +122,8 @@ def load_library():
             lib.fa_train_fwd_ex.restype = ctypes.c_int
             lib.fa_train_bwd_ex.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, vp, pp, po, vp]
             lib.fa_train_bwd_ex.restype = ctypes.c_int
+            lib.fa_paged_attention.argtypes = [vp, vp, vp, vp, vp, vp, fp, vp, vp]
+            lib.fa_paged_attention.restype = ctypes.c_int
             lib.fa_device_status.argtypes = [ctypes.c_int]
             lib.fa_device_status.restype = ctypes.c_int
             lib.fa_error_string.argtypes = [ctypes.c_int]
@@ -250,7 +273,7 @@ def fa_device_status(clear: bool = True) -> int:
     return load_library().fa_device_status(int(bool(clear)))
 
 
-FA_NUM_KERNELS = 5
+FA_NUM_KERNELS = 7
 
 
 def fa_profile_enable(on: bool) -> None:
@@ -326,3 +349,39 @@ def attention_bwd(q, k, v, o, lse, dO, *, scale, causal, mask=None, window=None,
                     make_options(q, k, mask, window, v=v, sinks=sinks, dsinks=dsinks,
                                  deterministic=deterministic), stream)
     return (dq, dk, dv) if sinks is None else (dq, dk, dv, dsinks)
+
+
+def fa_paged_attention(q, k_cache, v_cache, block_table, lengths, o, lse, params: FaPagedParams,
+                       stream=None) -> None:
+    """C call `fa_paged_attention` (q, caches, o bf16; block_table, lengths int32; lse f32 or
+    None)."""
+    import torch
+
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (o, "o")):
+        _check(t, torch.bfloat16, n)
+    _check(block_table, torch.int32, "block_table")
+    _check(lengths, torch.int32, "lengths")
+    if lse is not None:
+        _check(lse, torch.float32, "lse")
+    rc = load_library().fa_paged_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                           _ptr(block_table), _ptr(lengths), _ptr(o), _ptr(lse),
+                                           ctypes.byref(params), _stream_handle(stream))
+    if rc:
+        raise FaError(rc, "fa_paged_attention")
+
+
+def paged_attention(q, k_cache, v_cache, block_table, lengths, *, scale, causal=True,
+                    num_splits=0, stream=None):
+    """Attention of q [B, H, q_len, d] over paged caches [num_pages, Hk, page_size, d] with a
+    block table [B, max_pages] and lengths [B] (int32, on the device): returns (o, lse). The
+    q_len queries are each sequence's last positions (causal: bottom-right per sequence)."""
+    import torch
+
+    B, H, lq, d = q.shape
+    P, Hk, bs, _ = k_cache.shape
+    params = FaPagedParams(B, H, Hk, lq, d, bs, block_table.shape[1], P, float(scale),
+                           int(bool(causal)), int(num_splits), 0)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, lq), dtype=torch.float32, device=q.device)
+    fa_paged_attention(q, k_cache, v_cache, block_table, lengths, o, lse, params, stream)
+    return o, lse

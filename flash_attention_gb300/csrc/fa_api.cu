@@ -4,6 +4,7 @@
 #include <math.h>
 #include <stdint.h>
 #include <stdio.h>
+#include <cmath>
 #include <string.h>
 
 #include <atomic>
@@ -81,6 +82,7 @@ cudaError_t device_status_word(int dev, int** out) {
 
 // ---------------------------------------------------------------- argument checks
 constexpr int kMaxLen = 1 << 22;  // keeps every grid dimension within its limit
+constexpr int kPagedMaxRows = 128 * 65535;  // query rows per kv head (grid z of 128-row tiles)
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -232,6 +234,8 @@ const char* fa_kernel_name(int id) {
     case FA_KERNEL_FWD: return "fwd_kernel";
     case FA_KERNEL_BWD_PREP: return "bwd_prep_kernel";
     case FA_KERNEL_BWD_DQ_DET: return "bwd_dq_det_kernel";
+    case FA_KERNEL_PAGED: return "paged_attn_kernel";
+    case FA_KERNEL_PAGED_COMBINE: return "paged_combine_kernel";
     case FA_KERNEL_BWD_MAIN: return "bwd_main_kernel";
     case FA_KERNEL_BWD_DQ: return "bwd_dq_kernel";
     default: return "unknown";
@@ -427,6 +431,75 @@ int fa_train_bwd_noalloc(const void* q, const void* k, const void* v, const void
   return FA_OK;
 }
 
+int fa_paged_attention(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_table, const int32_t* lengths, void* o, float* lse,
+                       const fa_paged_params* p, void* stream) {
+  if (!p) return FA_ERR_INVALID;
+  const int ps = p->page_size;
+  if (p->batch <= 0 || p->n_heads <= 0 || p->n_kv_heads <= 0 || p->q_len <= 0 ||
+      p->max_pages <= 0 || p->num_pages <= 0 || p->n_heads % p->n_kv_heads)
+    return FA_ERR_INVALID;
+  if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256) return FA_ERR_INVALID;
+  if (ps < 8 || ps > 256 || (ps & (ps - 1))) return FA_ERR_INVALID;
+  if (!(p->scale > 0.0f) || !std::isfinite(p->scale)) return FA_ERR_INVALID;
+  if ((p->causal != 0 && p->causal != 1) || p->reserved != 0) return FA_ERR_INVALID;
+  if (p->num_splits < 0 || p->num_splits > 1024) return FA_ERR_INVALID;
+  if ((int64_t)p->max_pages * ps > kMaxLen || p->q_len > kMaxLen) return FA_ERR_INVALID;
+  if ((int64_t)p->num_pages * p->n_kv_heads > INT32_MAX / 2) return FA_ERR_INVALID;
+  const int64_t G = p->n_heads / p->n_kv_heads;
+  if (G * p->q_len > (int64_t)kPagedMaxRows) return FA_ERR_INVALID;
+  if ((int64_t)p->batch * p->n_kv_heads > 65535) return FA_ERR_INVALID;  // grid y
+  int rc;
+  if ((rc = check_bf16(q)) || (rc = check_bf16(k_cache)) || (rc = check_bf16(v_cache)) ||
+      (rc = check_bf16(o)))
+    return rc;
+  if (!block_table || !lengths || !aligned(block_table, 4) || !aligned(lengths, 4))
+    return FA_ERR_INVALID;
+  if (lse && !aligned(lse, 4)) return FA_ERR_INVALID;
+  if ((rc = check_device())) return rc;
+  cudaError_t e = get_encoder();
+  if (e != cudaSuccess) return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  fa::PagedArgs a;
+  a.table = block_table;
+  a.lens = lengths;
+  a.o = o;
+  a.lse = lse;
+  if ((e = device_status_word(dev, &a.status)) != cudaSuccess) return cuda_fail(e, "status word");
+  a.B = p->batch;
+  a.H = p->n_heads;
+  a.Hk = p->n_kv_heads;
+  a.G = (int)G;
+  a.lq = p->q_len;
+  a.d = p->head_dim;
+  a.bs = ps;
+  a.max_pages = p->max_pages;
+  a.num_pages = p->num_pages;
+  a.causal = p->causal;
+  a.num_splits = p->num_splits;
+  a.scale = p->scale;
+  fa::PagedMaps m;
+  const int rows = a.G * a.lq, kvrows = fa::paged_key_box_rows(ps);
+  if (!encode_bf16_3d(&m.q, q, a.B * a.Hk, rows, a.d, fa::paged_query_box_rows()) ||
+      !encode_bf16_3d(&m.k, k_cache, a.num_pages * a.Hk, ps, a.d, kvrows) ||
+      !encode_bf16_3d(&m.v, v_cache, a.num_pages * a.Hk, ps, a.d, kvrows))
+    return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+  const int splits = fa::paged_splits(a);
+  const size_t ws_bytes = fa::paged_workspace_bytes(a, splits);
+  void* ws = nullptr;
+  if (ws_bytes) {
+    e = cudaMallocAsync(&ws, ws_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync (paged workspace)");
+  }
+  e = fa::launch_paged(a, m, splits, ws, s);
+  cudaError_t e2 = ws ? cudaFreeAsync(ws, s) : cudaSuccess;
+  if (e != cudaSuccess) return cuda_fail(e, "paged attention launch");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync (paged workspace)");
+  return FA_OK;
+}
+
 int fa_device_status(int clear) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -440,7 +513,8 @@ int fa_device_status(int clear) {
   if (clear && v) {
     if ((e = cudaMemset(w, 0, sizeof(int))) != cudaSuccess) return cuda_fail(e, "cudaMemset");
   }
-  return v ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
+  if (!v) return FA_OK;
+  return v == fa::kStatusBadInput ? FA_ERR_BAD_INPUT : FA_ERR_DEVICE_TIMEOUT;
 }
 
 const char* fa_error_string(int code) {
@@ -451,6 +525,8 @@ const char* fa_error_string(int code) {
     case FA_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait on the device";
     case FA_ERR_UNSUPPORTED: return "device is not an sm_100-family GPU (needs sm_103a)";
     case FA_ERR_TOO_LARGE: return "problem needs more scratch than the fixed no-allocation array holds";
+    case FA_ERR_BAD_INPUT:
+      return "a paged call met a sequence length or block-table entry out of range";
     default: return "unknown error code";
   }
 }

@@ -11,12 +11,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-namespace fa {
+#include "fa_launch.h"  // status codes
 
-// ----------------------------------------------------------------------------- status word
-// Device-side status codes. A kernel whose bounded wait gave up writes kStatusTimeout into the
-// status word it was given (a device int owned by the library) before it exits.
-enum : int { kStatusOk = 0, kStatusTimeout = 1 };
+namespace fa {
 
 // Limit of one mbarrier wait, in ns of %globaltimer. A legitimate wait in these kernels lasts
 // microseconds; reaching this means a pipeline bug, and the kernel then winds down instead of

@@ -8,6 +8,12 @@
 
 namespace fa {
 
+// Device-side status codes, written into the per-device status word the kernels are given (a
+// device int owned by the library): kStatusTimeout when a bounded wait gave up (the kernel then
+// winds down), kStatusBadInput when a paged kernel met a length or block-table entry out of
+// range.
+enum : int { kStatusOk = 0, kStatusTimeout = 1, kStatusBadInput = 2 };
+
 // Kernel ids of the timing facility (same values as FA_KERNEL_* in the public header).
 enum KernelId {
   kKernFwd = 0,
@@ -15,7 +21,9 @@ enum KernelId {
   kKernBwdMain = 2,
   kKernBwdDq = 3,
   kKernBwdDqDet = 4,
-  kNumKernels = 5
+  kKernPaged = 5,
+  kKernPagedCombine = 6,
+  kNumKernels = 7
 };
 
 // Records a timing event before (end = 0) or after (end = 1) a launch on `s` when timing is
@@ -136,5 +144,25 @@ cudaError_t launch_dq_det(const BwdArgs& a, const DqMaps& m, cudaStream_t stream
 // device looks up the array's device address; later calls return the cached address.
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
 cudaError_t noalloc_scratch(void** ptr);
+
+// Paged key/value cache attention (fa_paged.cu).
+struct PagedArgs {
+  const int32_t* table;  // [B, max_pages] device
+  const int32_t* lens;   // [B] device
+  void* o;               // bf16 [B, H, lq, d]
+  float* lse;            // [B, H, lq] or nullptr
+  int* status;
+  int B, H, Hk, G, lq, d, bs, max_pages, num_pages, causal, num_splits;
+  float scale;
+};
+struct PagedMaps {
+  CUtensorMap q, k, v;  // q as [B*Hk, G*lq, d]; caches as [num_pages*Hk, page_size, d]
+};
+int paged_key_box_rows(int page_size);
+int paged_query_box_rows();
+int paged_splits(const PagedArgs& a);
+size_t paged_workspace_bytes(const PagedArgs& a, int splits);
+cudaError_t launch_paged(const PagedArgs& a, const PagedMaps& m, int splits, void* ws,
+                         cudaStream_t stream);
 
 }  // namespace fa

@@ -74,6 +74,8 @@ typedef struct fa_params {
 #define FA_ERR_DEVICE_TIMEOUT 3 /* a kernel gave up a bounded wait (see fa_device_status) */
 #define FA_ERR_UNSUPPORTED 4    /* the device is not sm_103 or sm_100 family */
 #define FA_ERR_TOO_LARGE 5      /* the problem needs more scratch than fa_train_bwd_noalloc has */
+#define FA_ERR_BAD_INPUT 6      /* (fa_device_status) a paged call met a sequence length or a
+                                   block-table entry out of range; those keys were read as 0 */
 
 /* Mask element types of fa_options.mask_type. */
 #define FA_MASK_F32 0  /* additive, natural log, float (an entry -inf hides the key) */
@@ -180,7 +182,9 @@ int fa_train_bwd(const void* q, const void* k, const void* v, const void* o, con
 #define FA_KERNEL_BWD_MAIN 2 /* backward main pass: dK, dV, dQ accumulation */
 #define FA_KERNEL_BWD_DQ 3   /* backward dQ conversion to bf16 (and the dsinks sum) */
 #define FA_KERNEL_BWD_DQ_DET 4 /* deterministic mode: query-tile-major dQ */
-#define FA_NUM_KERNELS 5
+#define FA_KERNEL_PAGED 5      /* paged key/value cache attention */
+#define FA_KERNEL_PAGED_COMBINE 6 /* merge of the key splits of fa_paged_attention */
+#define FA_NUM_KERNELS 7
 
 /* Turns timing on (1) or off (0). Returns FA_OK. */
 int fa_profile_enable(int on);
@@ -225,8 +229,55 @@ int fa_train_bwd_noalloc(const void* q, const void* k, const void* v, const void
                          const float* lse, const void* dO, const float* mask, void* dq, void* dk,
                          void* dv, const fa_params* p, void* stream);
 
-/* Synchronises the current device, then returns FA_OK, or FA_ERR_DEVICE_TIMEOUT if any kernel
- * of this library on it gave up a bounded wait since the last call with clear != 0. */
+/* ------------------------------------------------------------------ paged key/value cache
+ * Attention of a few new queries per sequence over a paged cache, for inference: single-query
+ * decode (q_len = 1) and a causal prefill of q_len positions against a cache. Page
+ * "nuvec-core tests/fast.rs", `paged_attention_equals_contiguous_attention` (layout, block
+ * table, lengths; one pass below about 1024 keys, two above), and page "tang
+ * src/compute/cuda.rs", `kv_attention` (decode, and the prefill with cache_start = len - q_len).
+ *
+ * The keys of sequence b are its first lengths[b] cache positions; logical key j is in page
+ * block_table[b * max_pages + j / page_size], slot j % page_size. The q_len queries are the
+ * sequence's last positions: with causal = 1, query i sees key j iff
+ * j <= lengths[b] - q_len + i. O = softmax(scale * q k^T) v; L = natural-log logsumexp. A query
+ * that sees no key gets O = 0 and L = -inf. Forward only (no gradient). */
+typedef struct fa_paged_params {
+  int32_t batch;       /* sequences, >= 1 */
+  int32_t n_heads;     /* query heads, a multiple of n_kv_heads */
+  int32_t n_kv_heads;  /* >= 1 */
+  int32_t q_len;       /* new positions per sequence, >= 1 */
+  int32_t head_dim;    /* 64, 128 or 256 */
+  int32_t page_size;   /* positions per page: a power of two in [8, 256] */
+  int32_t max_pages;   /* columns of the block table; max_pages * page_size <= 2^22 */
+  int32_t num_pages;   /* pages in each cache */
+  float scale;         /* finite and > 0 */
+  int32_t causal;      /* 0 or 1 */
+  int32_t num_splits;  /* 0: chosen by the library; otherwise the key range is cut into this
+                          many parts, each part one CTA, merged by a second kernel */
+  int32_t reserved;    /* must be 0 */
+} fa_paged_params;
+
+/*   q            bf16 [batch, n_heads, q_len, head_dim] (device, 16-byte aligned)
+ *   k_cache      bf16 [num_pages, n_kv_heads, page_size, head_dim] (device, 16-byte aligned)
+ *   v_cache      same layout as k_cache
+ *   block_table  int32 [batch, max_pages] (device, 4-byte aligned): page of each block of
+ *                page_size positions; only the first ceil(lengths[b] / page_size) are read
+ *   lengths      int32 [batch] (device): keys of each sequence, 0 .. max_pages * page_size
+ *   o            output, bf16 [batch, n_heads, q_len, head_dim] (device, 16-byte aligned)
+ *   lse          output or NULL: f32 [batch, n_heads, q_len]
+ * The lengths and the table live on the device, so they are checked there: a length outside
+ * [0, max_pages * page_size] is clamped and a table entry outside [0, num_pages) reads as zero
+ * keys, and either makes fa_device_status return FA_ERR_BAD_INPUT. With more than one split
+ * the call takes a small scratch buffer (splits * batch * n_heads * q_len * (head_dim + 1) f32)
+ * with cudaMallocAsync on `stream`. Returns FA_OK, FA_ERR_INVALID (parameters, pointers),
+ * FA_ERR_UNSUPPORTED or FA_ERR_CUDA. */
+int fa_paged_attention(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_table, const int32_t* lengths, void* o, float* lse,
+                       const fa_paged_params* p, void* stream);
+
+/* Synchronises the current device, then returns FA_OK, FA_ERR_DEVICE_TIMEOUT if any kernel of
+ * this library on it gave up a bounded wait, or FA_ERR_BAD_INPUT if a paged call met a length
+ * or block-table entry out of range, since the last call with clear != 0. */
 int fa_device_status(int clear);
 
 /* Human-readable text of a return code (static storage). */

@@ -36,10 +36,12 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_error_strings(lib):
-    for code in range(5):
+    for code in range(7):
         assert fa.fa_error_string(code)
     names = [fa.load_library().fa_kernel_name(k).decode() for k in range(fa.FA_NUM_KERNELS)]
-    assert names[-1] == "bwd_dq_det_kernel" and len(set(names)) == fa.FA_NUM_KERNELS
+    assert len(set(names)) == fa.FA_NUM_KERNELS and "unknown" not in " ".join(names)
+    assert {"bwd_dq_det_kernel", "paged_attn_kernel", "paged_combine_kernel"} <= set(names)
+    assert "paged" in fa.fa_error_string(fa.FA_ERR_BAD_INPUT)
     assert "unknown" in fa.fa_error_string(99)
     assert "sm_103a" in fa.fa_version()
 
@@ -189,3 +191,38 @@ def test_options_struct_layout():
     assert fa.FaOptions.deterministic.offset == 56
     assert fa.FaOptions.mask_stride_b.offset == 16
     assert fa.FaOptions.sinks.offset == 40 and fa.FaOptions.dsinks.offset == 48
+
+
+PAGED_GOOD = dict(batch=2, n_heads=8, n_kv_heads=2, q_len=1, head_dim=128, page_size=16,
+                  max_pages=4, num_pages=10, scale=0.1, causal=1, num_splits=0, reserved=0)
+
+
+def _paged(lib, params, table=FAKE, lens=FAKE, lse=None, q=FAKE):
+    p = fa.FaPagedParams(**params)
+    return lib.fa_paged_attention(q, FAKE, FAKE, table, lens, FAKE, lse, ctypes.byref(p), None)
+
+
+BAD_PAGED = [
+    ("batch", 0), ("n_heads", 7), ("q_len", 0), ("head_dim", 96), ("page_size", 12),
+    ("page_size", 4), ("page_size", 512), ("max_pages", 0), ("num_pages", 0), ("scale", 0.0),
+    ("causal", 3), ("num_splits", -1), ("reserved", 2), ("max_pages", 1 << 19),
+]
+
+
+@pytest.mark.parametrize("field,value", BAD_PAGED)
+def test_paged_bad_params_rejected(lib, field, value):
+    assert _paged(lib, dict(PAGED_GOOD, **{field: value})) == fa.FA_ERR_INVALID
+
+
+def test_paged_bad_pointers_rejected(lib):
+    assert lib.fa_paged_attention(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None) == \
+        fa.FA_ERR_INVALID
+    assert _paged(lib, PAGED_GOOD, table=None) == fa.FA_ERR_INVALID
+    assert _paged(lib, PAGED_GOOD, lens=FAKE + 2) == fa.FA_ERR_INVALID
+    assert _paged(lib, PAGED_GOOD, lse=FAKE + 1) == fa.FA_ERR_INVALID
+    assert _paged(lib, PAGED_GOOD, q=FAKE + 8) == fa.FA_ERR_INVALID
+
+
+def test_paged_params_struct_layout():
+    assert ctypes.sizeof(fa.FaPagedParams) == 48
+    assert fa.FaPagedParams.scale.offset == 32
