@@ -15,12 +15,16 @@
 //  * one CTA owns one (split, sequence, kv head) and up to 128 query rows: the G query heads
 //    of the kv head times q_len queries are packed into the M = 128 rows of one tcgen05 tile
 //    (Q viewed as [B * Hk, G * q_len, d]), so each K/V page is read once for all of them;
-//  * one warp streams the pages with TMA (boxes of min(page_size, 64) rows, 128-byte swizzle)
-//    through a ring; a page the table does not name, or positions past the sequence's end,
-//    are read as out-of-bounds boxes, which TMA fills with zeros;
-//  * one warp issues S = Q K^T into double-buffered TMEM and O += P V with P read from TMEM;
-//    before the last tile's P V it zeroes the V rows past the sequence's end, so that whatever
-//    the cache holds there (NaN included) cannot reach O;
+//  * one warp streams the pages with TMA through K and V rings (boxes of min(page_size, 64)
+//    rows, 128-byte swizzle), the block-table entries staged in shared memory a chunk at a
+//    time, and the box copies of a tile issued by all 32 lanes (small boxes issued by one
+//    thread queue behind each other); a page the table does not name, or positions past the
+//    sequence's end in a later page, are read as out-of-bounds boxes, which TMA fills with
+//    zeros; before the last tile's P V the V rows past the sequence's end are zeroed, so
+//    that whatever the cache holds there (NaN included) cannot reach O;
+//  * one warp issues S = Q K^T into double-buffered TMEM as soon as its K tile has landed
+//    (and frees that K stage when S is done); another issues O += P V with P read from TMEM
+//    (and frees the V stage), so neither kind of MMA waits for the other's operands;
 //  * one warpgroup (thread = query row = TMEM lane) runs the online softmax with the lazy
 //    rescale of the training forward;
 //  * with more than one split, each CTA writes its normalised partial O and its L, and a
@@ -40,11 +44,14 @@ constexpr int kPN = 64;   // keys per tile
 constexpr float kLog2eP = 1.4426950408889634f;
 constexpr float kLn2P = 0.6931471805599453f;
 constexpr float kRescaleP = 8.0f;
+constexpr int kPageChunk = 512;  // block-table entries staged in shared memory at a time
 }  // namespace
 
 template <int HD>
 struct PagedLayout {
-  static constexpr int STAGES = HD == 64 ? 6 : HD == 128 ? 4 : 2;
+  // K/V ring depth; at head_dim <= 128 two CTAs fit on an SM (one streams while the other
+  // starts or finishes)
+  static constexpr int STAGES = HD == 64 ? 4 : 2;
   static constexpr int KCH = HD / 64;
   static constexpr int Q_BYTES = kPM * HD * 2;
   static constexpr int KV_BYTES = kPN * HD * 2;
@@ -58,8 +65,9 @@ struct PagedLayout {
   static constexpr int COL_S0 = HD;
   static constexpr int TMEM_USED = HD + 2 * kPN;
   static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
-  static constexpr int THREADS = 192;  // warps 0-3 softmax, warp 4 TMA, warp 5 MMA
-  static constexpr int TMA_WARP = 4, MMA_WARP = 5;
+  // warps 0-3 softmax, warp 4 TMA, warp 5 issues S = Q K^T, warp 6 issues O += P V
+  static constexpr int THREADS = 224;
+  static constexpr int TMA_WARP = 4, S_WARP = 5, PV_WARP = 6;
   static_assert(TMEM_USED <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
@@ -86,10 +94,11 @@ __global__ void __launch_bounds__(PagedLayout<HD>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  __shared__ uint64_t q_full, k_full[ST], v_full[ST], kv_empty[ST];
-  __shared__ uint64_t s_full[2], p_full[2], o_done, o_final, mma_drain;
+  __shared__ uint64_t q_full, k_full[ST], v_full[ST], k_empty[ST], v_empty[ST];
+  __shared__ uint64_t s_full[2], p_full[2], pv_done[2], o_done, o_final, drain_s, drain_pv;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag, bad_input;
+  __shared__ int page_s[kPageChunk];  // block-table entries [chunk_base, chunk_base + 512)
 
   const int warp = warp_id(), lane = lane_id();
   const int split = blockIdx.x;
@@ -102,6 +111,9 @@ __global__ void __launch_bounds__(PagedLayout<HD>::THREADS, 1)
   const int k0 = split * p.kps;
   const int k1 = min(k0 + p.kps, len);
   const int ntt = k1 > k0 ? (k1 - k0 + kPN - 1) / kPN : 0;  // key tiles of this CTA
+  // softmax warps that own at least one real query row (rows past G * q_len are padding of
+  // the M = 128 tile: their P and O rows are never used, so their warps skip the work)
+  const int live_warps = min(4, (min(p.rows - r0, kPM) + 31) / 32);
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -110,18 +122,21 @@ __global__ void __launch_bounds__(PagedLayout<HD>::THREADS, 1)
     for (int s = 0; s < ST; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 128);
+      mbar_init(&p_full[s], 32 * live_warps);
+      mbar_init(&pv_done[s], 1);
     }
     mbar_init(&o_done, 1);
     mbar_init(&o_final, 1);
-    mbar_init(&mma_drain, 1);
+    mbar_init(&drain_s, 1);
+    mbar_init(&drain_pv, 1);
     fence_barrier_init();
   }
-  if (warp == LY::MMA_WARP) {
+  if (warp == LY::S_WARP) {
     tmem_alloc(&tmem_base_s, LY::TMEM_COLS);
     tmem_relinquish();
   }
@@ -131,8 +146,11 @@ __global__ void __launch_bounds__(PagedLayout<HD>::THREADS, 1)
   const uint32_t tbase = tmem_base_s;
 
   if (warp == LY::TMA_WARP) {
-    // ------------------------------------------------------------------ TMA producer
-    if (elect_one()) {
+    // ------------------------------------------------------------------ TMA producer: the
+    // warp stages the block-table entries in shared memory (coalesced, a chunk at a time),
+    // lane 0 issues the copies
+    const bool leader = lane == 0;
+    if (leader) {
       tma_prefetch_desc(&mQ);
       tma_prefetch_desc(&mK);
       tma_prefetch_desc(&mV);
@@ -141,70 +159,103 @@ __global__ void __launch_bounds__(PagedLayout<HD>::THREADS, 1)
         for (int c = 0; c < KCH; ++c)
           tma_load_3d(smem + LY::OFF_Q + c * kPM * 128, &mQ, &q_full, c * 64, r0, bkh);
       }
-      const int box = p.bs < kPN ? p.bs : kPN;  // rows per TMA box
-      const int nsub = kPN / box;                // boxes per key tile (<= 8)
-      const int z_oob = p.num_pages * p.Hk;      // a page index past the cache: zero fill
-      int last[ST];
-      for (int s = 0; s < ST; ++s) last[s] = -1;
-      for (int jj = 0; jj < ntt; ++jj) {
-        const int st = jj % ST;
-        const uint32_t use = jj / ST;
-        if (use > 0 && !mbar_wait(&kv_empty[st], (use - 1) & 1, &abort_flag)) break;
-        const int n0 = k0 + jj * kPN;
-        int zs[8], ys[8];
-        for (int sub = 0; sub < nsub; ++sub) {
-          const int key = n0 + sub * box;
-          zs[sub] = z_oob;
-          ys[sub] = 0;
-          if (key < len) {  // key / bs < max_pages because len <= max_pages * bs
-            const int page = p.table[(size_t)b * p.max_pages + key / p.bs];
-            if (page >= 0 && page < p.num_pages) {
-              zs[sub] = page * p.Hk + kh;
-              ys[sub] = key % p.bs;
-            } else {
-              bad_input = 1;
-            }
+    }
+    const int box = p.bs < kPN ? p.bs : kPN;  // rows per TMA box
+    const int nsub = kPN / box;                // boxes per key tile (<= 8)
+    const int z_oob = p.num_pages * p.Hk;      // a page index past the cache: zero fill
+    const int used_pages = (len + p.bs - 1) / p.bs;  // table entries of this sequence
+    const int32_t* trow = p.table + (size_t)b * p.max_pages;
+    int chunk_base = -1;  // first table entry held in page_s (-1: none)
+    int last_k[ST], last_v[ST];
+    for (int s = 0; s < ST; ++s) last_k[s] = last_v[s] = -1;
+    // Makes page_s hold the table entries of tiles jt .. jt + 1 (warp-wide).
+    auto stage_pages = [&](int jt) {
+      const int p_first = (k0 + jt * kPN) / p.bs;
+      const int p_last = min(used_pages - 1, (k0 + (jt + 2) * kPN - 1) / p.bs);
+      if (chunk_base >= 0 && p_first >= chunk_base && p_last < chunk_base + kPageChunk) return;
+      chunk_base = p_first;
+      __syncwarp();  // the old chunk is no longer read
+      for (int e = lane; e < kPageChunk; e += 32) {
+        const int idx = chunk_base + e;
+        int pg = -1;
+        if (idx < used_pages) {  // < max_pages because len <= max_pages * page_size
+          pg = trow[idx];
+          if (pg < 0 || pg >= p.num_pages) {
+            pg = -1;
+            bad_input = 1;
           }
         }
-        mbar_arrive_expect_tx(&k_full[st], LY::KV_BYTES);
-        for (int sub = 0; sub < nsub; ++sub)
-          for (int c = 0; c < KCH; ++c)
-            tma_load_3d(smem + LY::OFF_K + st * LY::KV_BYTES + c * kPN * 128 + sub * box * 128,
-                        &mK, &k_full[st], c * 64, ys[sub], zs[sub]);
-        mbar_arrive_expect_tx(&v_full[st], LY::KV_BYTES);
-        for (int sub = 0; sub < nsub; ++sub)
-          for (int c = 0; c < KCH; ++c)
-            tma_load_3d(smem + LY::OFF_V + st * LY::KV_BYTES + c * kPN * 128 + sub * box * 128,
-                        &mV, &v_full[st], c * 64, ys[sub], zs[sub]);
-        last[st] = jj;
+        page_s[e] = pg;
       }
-      if (ntt > 0) mbar_wait_drain(&q_full, 0);
-      for (int s = 0; s < ST; ++s)
-        if (last[s] >= 0) {
-          mbar_wait_drain(&k_full[s], (last[s] / ST) & 1);
-          mbar_wait_drain(&v_full[s], (last[s] / ST) & 1);
-        }
-    }
-  } else if (warp == LY::MMA_WARP) {
-    // ------------------------------------------------------------------ MMA issuer (lane 0;
-    // the whole warp zeroes the tail of the last V tile)
-    const bool leader = lane == 0;
-    const uint32_t sq = smem_u32(smem + LY::OFF_Q);
-    const uint32_t sk = smem_u32(smem + LY::OFF_K), sv = smem_u32(smem + LY::OFF_V);
-    const uint32_t id_s = idesc_bf16(kPM, kPN, 0, 0);
-    const uint32_t id_o = idesc_bf16(kPM, HD, 0, 1);
-    const uint32_t tO = tbase + LY::COL_O;
-    const Desc qa = make_desc(sq, 16, 1024);
-    bool ok = true;
-    if (ntt > 0) ok = __all_sync(0xffffffffu, mbar_wait(&q_full, 0, &abort_flag));
-    tc_fence_after();
-
-    auto issue_s = [&](int jj) {
-      const int st = jj % ST;
-      ok = ok && __all_sync(0xffffffffu, mbar_wait(&k_full[st], (jj / ST) & 1, &abort_flag));
-      if (!ok) return;
-      tc_fence_after();
+      __syncwarp();
+    };
+    // The copies of tile jt into stage jt % ST of the K (which = 0) or V ring (warp-wide): lane
+    // 0 waits for the stage and sets the byte count, then the lanes issue the nsub * KCH box
+    // copies in parallel (issued by one thread, small boxes queue behind each other).
+    auto issue = [&](int jt, int which) -> bool {
+      const int st = jt % ST;
+      const uint32_t use = jt / ST;
+      uint64_t* empty = which == 0 ? &k_empty[st] : &v_empty[st];
+      uint64_t* full = which == 0 ? &k_full[st] : &v_full[st];
+      bool ok = true;
       if (leader) {
+        if (use > 0) ok = mbar_wait(empty, (use - 1) & 1, &abort_flag);
+        if (ok) mbar_arrive_expect_tx(full, LY::KV_BYTES);
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+      const int n0 = k0 + jt * kPN;
+      uint8_t* dst = smem + (which == 0 ? LY::OFF_K : LY::OFF_V) + st * LY::KV_BYTES;
+      const CUtensorMap* map = which == 0 ? &mK : &mV;
+      for (int e = lane; e < nsub * KCH; e += 32) {
+        const int sub = e / KCH, c = e % KCH;
+        const int key = n0 + sub * box;
+        int z = z_oob, y = 0;
+        if (key < len) {
+          const int pg = page_s[key / p.bs - chunk_base];
+          if (pg >= 0) {
+            z = pg * p.Hk + kh;
+            y = key % p.bs;
+          }
+        }
+        tma_load_3d(dst + c * kPN * 128 + sub * box * 128, map, full, c * 64, y, z);
+      }
+      if (leader) (which == 0 ? last_k : last_v)[st] = jt;
+      return true;
+    };
+    // K runs one tile ahead of V: S needs K earlier than P V needs V
+    bool ok = true;
+    if (ntt > 0) {
+      stage_pages(0);
+      ok = issue(0, 0);
+    }
+    for (int jj = 0; jj < ntt && ok; ++jj) {
+      stage_pages(jj);
+      if (jj + 1 < ntt) ok = issue(jj + 1, 0);
+      if (ok) ok = issue(jj, 1);
+    }
+    if (leader) {
+      if (ntt > 0) mbar_wait_drain(&q_full, 0);
+      for (int s = 0; s < ST; ++s) {
+        if (last_k[s] >= 0) mbar_wait_drain(&k_full[s], (last_k[s] / ST) & 1);
+        if (last_v[s] >= 0) mbar_wait_drain(&v_full[s], (last_v[s] / ST) & 1);
+      }
+    }
+  } else if (warp == LY::S_WARP) {
+    // ------------------------------------------------------------------ S = Q K^T issuer: S(jj)
+    // into buffer jj % 2 once K(jj) has landed and P V(jj - 2) has read that buffer; the K
+    // stage is released as soon as S(jj) is done, so K loads run ahead of P V
+    if (elect_one()) {
+      const uint32_t sq = smem_u32(smem + LY::OFF_Q), sk = smem_u32(smem + LY::OFF_K);
+      const uint32_t id_s = idesc_bf16(kPM, kPN, 0, 0);
+      const Desc qa = make_desc(sq, 16, 1024);
+      bool ok = ntt == 0 || mbar_wait(&q_full, 0, &abort_flag);
+      tc_fence_after();
+      for (int jj = 0; jj < ntt && ok; ++jj) {
+        const int st = jj % ST;
+        ok = mbar_wait(&k_full[st], (jj / ST) & 1, &abort_flag);
+        if (ok && jj >= 2) ok = mbar_wait(&pv_done[jj % 2], ((jj - 2) / 2) & 1, &abort_flag);
+        if (!ok) break;
+        tc_fence_after();
         const uint32_t tS = tbase + LY::COL_S0 + (jj % 2) * kPN;
         const Desc kb = make_desc(sk + st * LY::KV_BYTES, 16, 1024);
 #pragma unroll
@@ -212,12 +263,19 @@ __global__ void __launch_bounds__(PagedLayout<HD>::THREADS, 1)
           mma_ss2(tS, qa.at((ks / 4) * (kPM * 128) + (ks % 4) * 32), qa.hi,
                   kb.at((ks / 4) * (kPN * 128) + (ks % 4) * 32), kb.hi, id_s, ks > 0 ? 1u : 0u);
         mma_commit(&s_full[jj % 2]);
+        mma_commit(&k_empty[st]);
       }
-      __syncwarp();
-    };
-
-    if (ntt > 0) issue_s(0);
-    if (ntt > 1) issue_s(1);
+      mma_commit(&drain_s);
+      mbar_wait_drain(&drain_s, 0);
+    }
+  } else if (warp == LY::PV_WARP) {
+    // ------------------------------------------------------------------ O += P V issuer (lane 0;
+    // the whole warp zeroes the tail of the last V tile)
+    const bool leader = lane == 0;
+    const uint32_t sv = smem_u32(smem + LY::OFF_V);
+    const uint32_t id_o = idesc_bf16(kPM, HD, 0, 1);
+    const uint32_t tO = tbase + LY::COL_O;
+    bool ok = true;
     for (int jj = 0; jj < ntt && ok; ++jj) {
       const int st = jj % ST;
       const int n0 = k0 + jj * kPN;
@@ -225,7 +283,8 @@ __global__ void __launch_bounds__(PagedLayout<HD>::THREADS, 1)
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&v_full[st], (jj / ST) & 1, &abort_flag));
       if (!ok) break;
       if (n0 + kPN > len) {
-        // rows len - n0 .. kPN - 1 of this V tile hold no key: zero all of their 128-byte rows
+        // rows len - n0 .. kPN - 1 of this V tile hold no key of the sequence (the rest of the
+        // page): zero all of their 128-byte rows
         uint8_t* vt = smem + LY::OFF_V + st * LY::KV_BYTES;
         const int r_first = len - n0;
         const int items = (kPN - r_first) * KCH * 8;  // 16-byte granules
@@ -245,18 +304,18 @@ __global__ void __launch_bounds__(PagedLayout<HD>::THREADS, 1)
         for (int ks = 0; ks < kPN / 16; ++ks)
           mma_ts2(tO, tP + ks * 8, vb.at(ks * 2048), vb.hi, id_o, (jj > 0 || ks > 0) ? 1u : 0u);
         mma_commit(&o_done);
+        mma_commit(&pv_done[jj % 2]);
         if (jj == ntt - 1) mma_commit(&o_final);
-        mma_commit(&kv_empty[st]);
+        mma_commit(&v_empty[st]);
       }
       __syncwarp();
-      if (jj + 2 < ntt) issue_s(jj + 2);  // into the buffer P(jj) was read from (in order)
     }
     if (leader) {
-      mma_commit(&mma_drain);
-      mbar_wait_drain(&mma_drain, 0);
+      mma_commit(&drain_pv);
+      mbar_wait_drain(&drain_pv, 0);
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < live_warps) {
     // ------------------------------------------------------------------ softmax warpgroup
     const int r = warp * 32 + lane;
     const int R = r0 + r;  // row of the (sequence, kv head) group: g * lq + i
@@ -390,7 +449,7 @@ __global__ void __launch_bounds__(PagedLayout<HD>::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == LY::MMA_WARP) tmem_dealloc(tbase, LY::TMEM_COLS);
+  if (warp == LY::S_WARP) tmem_dealloc(tbase, LY::TMEM_COLS);
   if (threadIdx.x == 0) {
     report_abort(&abort_flag, p.status);
     if (bad_input && p.status) atomicCAS(p.status, kStatusOk, kStatusBadInput);
@@ -451,8 +510,11 @@ int paged_splits(const PagedArgs& a) {
   const long long cap = (long long)a.max_pages * a.bs;
   if (a.num_splits > 0) return (int)std::min<long long>(a.num_splits, (cap + kPN - 1) / kPN);
   if (cap <= 1024) return 1;  // one pass
+  // about 2048 keys per split (short enough to balance sequences of mixed lengths over the
+  // SMs, long enough to amortise a CTA's start), and enough CTAs to fill the GPU
   const long long ctas = (long long)a.B * a.Hk * ((a.G * a.lq + kPM - 1) / kPM);
-  long long s = std::max<long long>(2, (2 * 152 + ctas - 1) / ctas);
+  long long s = std::max<long long>(2, (cap + 2047) / 2048);
+  s = std::max<long long>(s, (2 * 152 + ctas - 1) / ctas);
   s = std::min<long long>(s, (cap + 255) / 256);  // at least 256 keys per split
   return (int)std::max<long long>(1, s);
 }
