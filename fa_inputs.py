@@ -290,3 +290,69 @@ DECODE_WORKLOADS = [
     DecodeWorkload("paged_prefill4_d128", 16, 32, 8, 4, 128, 16, 2048, 16384),
 ]
 DECODE_BY_NAME = {w.name: w for w in DECODE_WORKLOADS}
+
+
+# ------------------------------------------------------------------ variable-length batches
+@dataclass(frozen=True)
+class VarlenWorkload:
+    """Independent sequences packed without padding, head-major: q [H, total_q, d], k and v
+    [Hk, total_k, d]; sequence b has q_lens[b] queries and k_lens[b] keys."""
+
+    name: str
+    n_heads: int
+    n_kv_heads: int
+    head_dim: int
+    q_lens: tuple
+    k_lens: tuple
+    causal: bool = True
+    window_left: int = -1
+    window_right: int = -1
+    do_std: float = 1.0
+
+    @property
+    def scale(self) -> float:
+        return self.head_dim ** -0.5
+
+    @property
+    def batch(self) -> int:
+        return len(self.q_lens)
+
+    def cu(self, lens):
+        return np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+
+    @property
+    def windowed(self) -> bool:
+        return self.window_left >= 0 or self.window_right >= 0
+
+    def flops(self):
+        """(fwd, bwd) FLOPs over the visible pairs of every sequence (4d and 10d per pair)."""
+        pairs = 0
+        for ql, kl in zip(self.q_lens, self.k_lens):
+            w = Workload("s", 1, 1, 1, max(ql, 1), max(kl, 1), self.head_dim, 1.0, self.causal,
+                         window_left=self.window_left, window_right=self.window_right)
+            pairs += w.visible_pairs() if ql > 0 and kl > 0 else 0
+        return 4.0 * self.head_dim * pairs * self.n_heads, 10.0 * self.head_dim * pairs * self.n_heads
+
+
+@dataclass
+class VarlenInputs:
+    q: np.ndarray    # bf16 bits [H, total_q, d]
+    k: np.ndarray    # bf16 bits [Hk, total_k, d]
+    v: np.ndarray
+    do: np.ndarray   # bf16 bits [H, total_q, d]
+    cu_q: np.ndarray  # int32 [B + 1]
+    cu_k: np.ndarray
+
+    def widened(self):
+        return tuple(bf16_bits_to_f32(t) for t in (self.q, self.k, self.v, self.do))
+
+
+def make_varlen_inputs(w: VarlenWorkload, index: int = 33, seed_base: int | None = None):
+    base = (SEED_BASE if seed_base is None else seed_base) + 16 * index
+    cu_q, cu_k = w.cu(w.q_lens), w.cu(w.k_lens)
+    tq, tk = max(int(cu_q[-1]), 1), max(int(cu_k[-1]), 1)
+    q = normal_bf16(base + T_Q, (w.n_heads, tq, w.head_dim))
+    k = normal_bf16(base + T_K, (w.n_kv_heads, tk, w.head_dim))
+    v = normal_bf16(base + T_V, (w.n_kv_heads, tk, w.head_dim))
+    do = normal_bf16(base + T_DO, (w.n_heads, tq, w.head_dim), w.do_std)
+    return VarlenInputs(q, k, v, do, cu_q, cu_k)

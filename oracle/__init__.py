@@ -25,6 +25,7 @@ _SRC = os.path.join(_HERE, "fa_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "libfa_oracle.so")
 _lib = None
 _lock = threading.Lock()
+_active_sinks = None  # the values of the enclosing sinks(...) block
 
 # Planted-mistake codes understood by fa_oracle_set_mutation (tests only).
 MUTATIONS = {
@@ -145,11 +146,15 @@ class sinks:
         self.values = None if values is None else np.ascontiguousarray(values, np.float32)
 
     def __enter__(self):
+        global _active_sinks
         _load().fa_oracle_set_sinks(_ptr(self.values))
+        _active_sinks = self.values
         return self
 
     def __exit__(self, *exc):
+        global _active_sinks
         _load().fa_oracle_set_sinks(None)
+        _active_sinks = None
         return False
 
 
@@ -285,3 +290,53 @@ def paged_fwd(q, k_cache, v_cache, block_table, lengths, *, scale, causal, nthre
     if rc:
         raise ValueError(f"oracle paged_fwd failed ({rc})")
     return o, lse
+
+
+# ------------------------------------------------------------------ variable-length batches
+def _seq_bounds(cu, b):
+    return int(cu[b]), int(cu[b + 1])
+
+
+def varlen_fwd(q, k, v, cu_q, cu_k, *, scale, causal, nthreads=None):
+    """A batch of independent sequences packed without padding: q [H, total_q, d], k and v
+    [Hk, total_k, d(v)], sequence b owning rows cu_q[b] .. cu_q[b+1] of q and cu_k[b] ..
+    cu_k[b+1] of k, v. Each sequence is the fixed-length problem on its own rows (causal
+    bottom-right within the sequence). Returns (O [H, total_q, dv], L [H, total_q]) in f64;
+    a query of a sequence with no keys gets O = 0 and L = -inf. Window and sinks come from the
+    enclosing `window(...)` / `sinks(...)` blocks."""
+    H, Tq, d = q.shape
+    dvd = v.shape[2]
+    o = np.zeros((H, Tq, dvd), np.float64)
+    lse = np.full((H, Tq), -np.inf, np.float64)
+    for b in range(len(cu_q) - 1):
+        qs, qe = _seq_bounds(cu_q, b)
+        ks, ke = _seq_bounds(cu_k, b)
+        if qe == qs:
+            continue
+        if ke == ks:  # no keys: O = 0; L = -inf, or the head's sink where sinks are set
+            if _active_sinks is not None:
+                lse[:, qs:qe] = np.asarray(_active_sinks, np.float64)[:, None]
+            continue
+        ob, lb = fwd(q[None, :, qs:qe], k[None, :, ks:ke], v[None, :, ks:ke], None,
+                     scale=scale, causal=causal, nthreads=nthreads)
+        o[:, qs:qe] = ob[0]
+        lse[:, qs:qe] = lb[0]
+    return o, lse
+
+
+def varlen_bwd(q, k, v, do, cu_q, cu_k, *, scale, causal, nthreads=None):
+    """dQ [H, total_q, d], dK [Hk, total_k, d], dV [Hk, total_k, dv] of `varlen_fwd` (f64)."""
+    dq = np.zeros(q.shape, np.float64)
+    dk = np.zeros(k.shape, np.float64)
+    dv = np.zeros(v.shape, np.float64)
+    for b in range(len(cu_q) - 1):
+        qs, qe = _seq_bounds(cu_q, b)
+        ks, ke = _seq_bounds(cu_k, b)
+        if qe == qs or ke == ks:
+            continue
+        g = bwd(q[None, :, qs:qe], k[None, :, ks:ke], v[None, :, ks:ke], None,
+                do[None, :, qs:qe], scale=scale, causal=causal, nthreads=nthreads)
+        dq[:, qs:qe] = g[0][0]
+        dk[:, ks:ke] = g[1][0]
+        dv[:, ks:ke] = g[2][0]
+    return dq, dk, dv

@@ -678,6 +678,59 @@ def pin_paged_layout_invariance():
     return fails
 
 
+# ------------------------------------------------------------------ variable-length batches
+VARLEN_CASES = [
+    # (H, Hk, d, q_lens, k_lens, causal)
+    (4, 2, 8, (3, 5, 1), (3, 7, 4), True),
+    (2, 2, 4, (4, 0, 6), (9, 3, 2), False),     # an empty query sequence
+    (4, 1, 8, (2, 5), (0, 5), True),            # a sequence with no keys
+    (2, 1, 8, (6, 3, 4), (6, 2, 9), True),      # ql > kl: rows that see no key
+]
+
+
+def pin_varlen_vs_torch():
+    """Each packed sequence against torch's CPU flash kernel (O, L) and autograd (dQ, dK, dV)
+    on that sequence alone, with torch's bottom-right causal bias."""
+    import fa_inputs
+
+    fails = []
+    for n, (H, Hk, d, ql, kl, causal) in enumerate(VARLEN_CASES):
+        w = fa_inputs.VarlenWorkload(f"pin{n}", H, Hk, d, ql, kl, causal)
+        x = fa_inputs.make_varlen_inputs(w, index=140 + n)
+        q, k, v, do = x.widened()
+        o, lse = oracle.varlen_fwd(q, k, v, x.cu_q, x.cu_k, scale=0.4, causal=causal)
+        dq, dk, dv = oracle.varlen_bwd(q, k, v, do, x.cu_q, x.cu_k, scale=0.4, causal=causal)
+        for b in range(w.batch):
+            qs, qe, ks, ke = x.cu_q[b], x.cu_q[b + 1], x.cu_k[b], x.cu_k[b + 1]
+            if qe == qs:
+                continue
+            tag = f"varlen case{n} seq{b}"
+            if ke == ks:
+                _cmp(tag + " O (no keys)", o[:, qs:qe], np.zeros_like(o[:, qs:qe]), tol=0, out=fails)
+                _cmp(tag + " L (no keys)", lse[:, qs:qe], np.full_like(lse[:, qs:qe], -np.inf),
+                     tol=0, out=fails)
+                continue
+            qb, kb, vb, dob = (t[None, :, a:e] for t, (a, e) in
+                               ((q, (qs, qe)), (k, (ks, ke)), (v, (ks, ke)), (do, (qs, qe))))
+            to, tl = _torch_fwd(qb, kb, vb, None, 0.4, causal)
+            # rows that see no key (causal, query position before the first key): O = 0 and
+            # L = -inf by the definition; torch reports another L there
+            rows = np.arange(qe - qs)
+            dead = np.broadcast_to(causal & ((ke - ks) - (qe - qs) + rows < 0), tl.shape)
+            to = np.where(dead[..., None], 0.0, to)
+            tl = np.where(dead, -np.inf, tl)
+            _cmp(tag + " O", o[None, :, qs:qe], to, out=fails)
+            _cmp(tag + " L", lse[None, :, qs:qe], tl, out=fails)
+            tq, tk, tv = _torch_grads(qb, kb, vb, None, dob, 0.4, causal)
+            tq = np.nan_to_num(tq)
+            _cmp(tag + " dQ", dq[None, :, qs:qe], tq, out=fails)
+            _cmp(tag + " dK", dk[None, :, ks:ke], np.nan_to_num(tk), out=fails)
+            _cmp(tag + " dV", dv[None, :, ks:ke], np.nan_to_num(tv), out=fails)
+        # keys and values of other sequences are untouched: their gradients stay 0 outside
+        # every sequence's rows, and equal lengths give the batched problem
+    return fails
+
+
 ALL_PINS = [
     pin_fwd_vs_torch_cpu_flash,
     pin_bwd_vs_torch_autograd,
@@ -695,4 +748,5 @@ ALL_PINS = [
     pin_value_dim_identity,
     pin_paged_vs_torch,
     pin_paged_layout_invariance,
+    pin_varlen_vs_torch,
 ]
