@@ -51,6 +51,10 @@ class FaOptions(ctypes.Structure):
         ("dsinks", ctypes.c_void_p),
         ("deterministic", ctypes.c_int32),
         ("reserved", ctypes.c_int32),
+        ("cu_seqlens_q", ctypes.c_void_p),
+        ("cu_seqlens_k", ctypes.c_void_p),
+        ("total_q", ctypes.c_int32),
+        ("total_k", ctypes.c_int32),
     ]
 
 
@@ -213,7 +217,7 @@ def make_options(q, k, mask=None, window=(-1, -1), v=None, sinks=None, dsinks=No
     kl = k.shape[2]
     wl, wr = window if window is not None else (-1, -1)
     opt = FaOptions(int(wl), int(wr), FA_MASK_F32, 0, 0, 0, 0, None, None,
-                    1 if deterministic else 0, 0)
+                    1 if deterministic else 0, 0, None, None, 0, 0)
     if v is not None and v.shape[-1] != d:
         opt.value_dim = int(v.shape[-1])
     if mask is not None:
@@ -385,3 +389,53 @@ def paged_attention(q, k_cache, v_cache, block_table, lengths, *, scale, causal=
     lse = torch.empty((B, H, lq), dtype=torch.float32, device=q.device)
     fa_paged_attention(q, k_cache, v_cache, block_table, lengths, o, lse, params, stream)
     return o, lse
+
+
+def varlen_params_options(q, k, v, cu_q, cu_k, max_q, max_k, *, scale, causal, window=None,
+                          sinks=None, dsinks=None, deterministic=False):
+    """FaParams and FaOptions of a variable-length batch: q [H, total_q, d], k and v
+    [Hk, total_k, d(v)], cu_q / cu_k int32 CUDA tensors of batch + 1 offsets, max_q / max_k the
+    longest sequence."""
+    import torch
+
+    H, Tq, d = q.shape
+    Hk, Tk, _ = k.shape
+    for t, n in ((cu_q, "cu_q"), (cu_k, "cu_k")):
+        _check(t, torch.int32, n)
+    B = cu_q.numel() - 1
+    params = FaParams(B, H, Hk, int(max_q), int(max_k), d, float(scale), int(bool(causal)))
+    opt = make_options(q[None], k[None], None, window, v=v[None], sinks=sinks, dsinks=dsinks,
+                       deterministic=deterministic)
+    opt.cu_seqlens_q = cu_q.data_ptr()
+    opt.cu_seqlens_k = cu_k.data_ptr()
+    opt.total_q, opt.total_k = Tq, Tk
+    return params, opt
+
+
+def varlen_attention_fwd(q, k, v, cu_q, cu_k, max_q, max_k, *, scale, causal, window=None,
+                         sinks=None, stream=None):
+    """Forward of a variable-length batch (see varlen_params_options): returns (o, lse) with
+    o [H, total_q, dv] and lse [H, total_q]."""
+    import torch
+
+    H, Tq, _ = q.shape
+    o = torch.empty((H, Tq, v.shape[2]), dtype=q.dtype, device=q.device)
+    lse = torch.empty((H, Tq), dtype=torch.float32, device=q.device)
+    params, opt = varlen_params_options(q, k, v, cu_q, cu_k, max_q, max_k, scale=scale,
+                                        causal=causal, window=window, sinks=sinks)
+    fa_train_fwd_ex(q, k, v, None, o, lse, params, opt, stream)
+    return o, lse
+
+
+def varlen_attention_bwd(q, k, v, o, lse, dO, cu_q, cu_k, max_q, max_k, *, scale, causal,
+                         window=None, sinks=None, deterministic=False, stream=None):
+    """Backward of a variable-length batch: returns (dq, dk, dv) (+ dsinks with sinks)."""
+    import torch
+
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dsinks = None if sinks is None else torch.empty_like(sinks)
+    params, opt = varlen_params_options(q, k, v, cu_q, cu_k, max_q, max_k, scale=scale,
+                                        causal=causal, window=window, sinks=sinks,
+                                        dsinks=dsinks, deterministic=deterministic)
+    fa_train_bwd_ex(q, k, v, o, lse, dO, None, dq, dk, dv, params, opt, stream)
+    return (dq, dk, dv) if sinks is None else (dq, dk, dv, dsinks)

@@ -113,6 +113,10 @@ fa_options default_options(const fa_params* p) {
   o.dsinks = nullptr;
   o.deterministic = 0;
   o.reserved = 0;
+  o.cu_seqlens_q = nullptr;
+  o.cu_seqlens_k = nullptr;
+  o.total_q = 0;
+  o.total_k = 0;
   o.mask_stride_q = p->kl;
   o.mask_stride_h = (int64_t)p->ql * p->kl;
   o.mask_stride_b = (int64_t)p->n_heads * p->ql * p->kl;
@@ -125,6 +129,15 @@ int check_options(const fa_options* o, const void* mask, const fa_params* p, boo
   if (o->window_left < -1 || o->window_right < -1) return FA_ERR_INVALID;
   if (o->value_dim < 0) return FA_ERR_INVALID;
   if ((o->deterministic != 0 && o->deterministic != 1) || o->reserved != 0) return FA_ERR_INVALID;
+  if ((o->cu_seqlens_q == nullptr) != (o->cu_seqlens_k == nullptr)) return FA_ERR_INVALID;
+  if (o->cu_seqlens_q) {
+    if (!aligned(o->cu_seqlens_q, 4) || !aligned(o->cu_seqlens_k, 4)) return FA_ERR_INVALID;
+    if (o->total_q < 1 || o->total_k < 1) return FA_ERR_INVALID;
+    if ((int64_t)o->total_q * p->n_heads > INT32_MAX / 2 ||
+        (int64_t)o->total_k * p->n_kv_heads > INT32_MAX / 2)
+      return FA_ERR_INVALID;
+    if (mask) return FA_ERR_UNSUPPORTED;  // a dense mask has no shape for packed sequences
+  }
   if (o->sinks && !aligned(o->sinks, 4)) return FA_ERR_INVALID;
   if (bwd && o->dsinks && (!o->sinks || !aligned(o->dsinks, 4))) return FA_ERR_INVALID;
   if (o->mask_type != FA_MASK_F32 && o->mask_type != FA_MASK_BF16 && o->mask_type != FA_MASK_BOOL)
@@ -264,6 +277,10 @@ int fa_train_fwd_ex(const void* q, const void* k, const void* v, const void* mas
   a.mask_stride_h = op->mask_stride_h;
   a.mask_stride_q = op->mask_stride_q;
   a.sinks = op->sinks;
+  a.cu_q = op->cu_seqlens_q;
+  a.cu_k = op->cu_seqlens_k;
+  a.total_q = op->total_q;
+  a.total_k = op->total_k;
   a.o = o;
   a.lse = lse;
   if ((e = device_status_word(dev, &a.status)) != cudaSuccess) return cuda_fail(e, "status word");
@@ -281,9 +298,14 @@ int fa_train_fwd_ex(const void* q, const void* k, const void* v, const void* mas
   a.band = band.mode;
   fa::FwdMaps m;
   const int qrows = fa::fwd_q_box_rows(a.d), kvrows = fa::fwd_kv_box_rows(a.d);
-  if (!encode_bf16_3d(&m.q, q, a.B * a.H, a.ql, a.d, qrows) ||
-      !encode_bf16_3d(&m.k, k, a.B * a.Hk, a.kl, a.d, kvrows) ||
-      !encode_bf16_3d(&m.v, v, a.B * a.Hk, a.kl, a.dval, kvrows))
+  // tensor-map z and rows: (batch, head) slices of ql / kl rows, or for a variable-length
+  // batch the heads of total_q / total_k packed rows
+  const bool vl = a.cu_q != nullptr;
+  const int qz = vl ? a.H : a.B * a.H, kz = vl ? a.Hk : a.B * a.Hk;
+  const int qr = vl ? a.total_q : a.ql, kr = vl ? a.total_k : a.kl;
+  if (!encode_bf16_3d(&m.q, q, qz, qr, a.d, qrows) ||
+      !encode_bf16_3d(&m.k, k, kz, kr, a.d, kvrows) ||
+      !encode_bf16_3d(&m.v, v, kz, kr, a.dval, kvrows))
     return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
   e = fa::launch_fwd(a, m, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
@@ -325,6 +347,10 @@ static int prepare_bwd(const void* q, const void* k, const void* v, const void* 
   a->dsinks = op->dsinks;
   a->dsink_part = nullptr;  // set with the workspace
   a->deterministic = op->deterministic;
+  a->cu_q = op->cu_seqlens_q;
+  a->cu_k = op->cu_seqlens_k;
+  a->total_q = op->total_q;
+  a->total_k = op->total_k;
   a->dq = dq;
   a->dk = dk;
   a->dv = dv;
@@ -348,17 +374,20 @@ static int prepare_bwd(const void* q, const void* k, const void* v, const void* 
 
 static int encode_bwd_maps(const fa::BwdArgs& a, fa::BwdMaps* m) {
   const int qrows = fa::bwd_q_box_rows(a.d), kvrows = fa::bwd_kv_box_rows(a.d);
-  if (!encode_bf16_3d(&m->q, a.q, a.B * a.H, a.ql, a.d, qrows) ||
-      !encode_bf16_3d(&m->dO, a.dO, a.B * a.H, a.ql, a.dval, qrows) ||
-      !encode_bf16_3d(&m->k, a.k, a.B * a.Hk, a.kl, a.d, kvrows) ||
-      !encode_bf16_3d(&m->v, a.v, a.B * a.Hk, a.kl, a.dval, kvrows))
+  const bool vl = a.cu_q != nullptr;  // variable-length batch: heads of packed rows
+  const int qz = vl ? a.H : a.B * a.H, kz = vl ? a.Hk : a.B * a.Hk;
+  const int qr = vl ? a.total_q : a.ql, kr = vl ? a.total_k : a.kl;
+  if (!encode_bf16_3d(&m->q, a.q, qz, qr, a.d, qrows) ||
+      !encode_bf16_3d(&m->dO, a.dO, qz, qr, a.dval, qrows) ||
+      !encode_bf16_3d(&m->k, a.k, kz, kr, a.d, kvrows) ||
+      !encode_bf16_3d(&m->v, a.v, kz, kr, a.dval, kvrows))
     return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
   if (a.deterministic) {
     const int drows = fa::dq_det_box_rows();
-    if (!encode_bf16_3d(&m->det.q, a.q, a.B * a.H, a.ql, a.d, 128) ||
-        !encode_bf16_3d(&m->det.dO, a.dO, a.B * a.H, a.ql, a.dval, 128) ||
-        !encode_bf16_3d(&m->det.k, a.k, a.B * a.Hk, a.kl, a.d, drows) ||
-        !encode_bf16_3d(&m->det.v, a.v, a.B * a.Hk, a.kl, a.dval, drows))
+    if (!encode_bf16_3d(&m->det.q, a.q, qz, qr, a.d, 128) ||
+        !encode_bf16_3d(&m->det.dO, a.dO, qz, qr, a.dval, 128) ||
+        !encode_bf16_3d(&m->det.k, a.k, kz, kr, a.d, drows) ||
+        !encode_bf16_3d(&m->det.v, a.v, kz, kr, a.dval, drows))
       return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
   }
   return FA_OK;

@@ -126,6 +126,9 @@ struct BwdKParams {
   int H, Hk, ql, kl, ql_pad;
   int lo_off, hi_off;  // key j is visible to query row i iff q_abs + lo_off <= j <= q_abs + hi_off
   int skip_dq;         // 1: dQ comes from the deterministic dQ kernel; no dQ work here
+  const int32_t* cu_q;  // variable-length batch: sequence offsets (VARLEN kernels)
+  const int32_t* cu_k;
+  int total_q, total_k;
   float scale, scale_log2;
 };
 
@@ -153,7 +156,9 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
                                                        float* __restrict__ dqacc,
                                                        const float* __restrict__ sinks,
                                                        float* __restrict__ dsink_part, int BH,
-                                                       int H, int ql, int ql_pad, int zero_acc) {
+                                                       int H, int ql, int ql_pad, int zero_acc,
+                                                       const int32_t* __restrict__ cu_q,
+                                                       int total_q) {
   constexpr int TPR = DV / 8;            // threads per O / dO row (8 bf16 = 16 bytes each)
   constexpr int RPB = 256 / TPR;         // rows per pass of the block
   constexpr int ROWS = 4;                // passes per block
@@ -164,14 +169,22 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   const int i0 = blockIdx.x * RPB * ROWS;  // first row of the chunk (ql_pad is a multiple)
   const bool want_dsink = dsink_part != nullptr;
   for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
+    // rows of this (batch, head): fixed length, or sequence b of a variable-length batch
+    size_t rowbase = (size_t)bh * ql;
+    int qlen = ql;
+    if (cu_q != nullptr) {
+      int qs;
+      varlen_seq(cu_q, bh / H, total_q, ql, qs, qlen);
+      rowbase = (size_t)(bh % H) * total_q + qs;
+    }
     uint4 a[ROWS], g[ROWS];
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {
       const int i = i0 + r * RPB + threadIdx.x / TPR;
       a[r] = make_uint4(0, 0, 0, 0);
       g[r] = make_uint4(0, 0, 0, 0);
-      if (i < ql) {
-        const size_t base = ((size_t)bh * ql + i) * DV + sub * 8;
+      if (i < qlen) {
+        const size_t base = (rowbase + i) * DV + sub * 8;
         a[r] = *reinterpret_cast<const uint4*>(o + base);
         g[r] = *reinterpret_cast<const uint4*>(dO + base);
       }
@@ -190,15 +203,15 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
       if (sub == 0) {
         float nl2 = -INFINITY;  // padding rows and fully masked rows: P = exp2(s - inf) = 0
         float term = 0.0f;      // this row's share of dsinks[h]
-        if (i < ql) {
-          const float L = lse[(size_t)bh * ql + i];
+        if (i < qlen) {
+          const float L = lse[rowbase + i];
           if (L != -INFINITY) {
             nl2 = -L * kLog2eB;
             if (want_dsink) term = -expf(__ldg(sinks + bh % H) - L) * acc;
           }
         }
         lse2[(size_t)bh * ql_pad + i] = nl2;
-        dvec[(size_t)bh * ql_pad + i] = i < ql ? acc : 0.0f;
+        dvec[(size_t)bh * ql_pad + i] = i < qlen ? acc : 0.0f;
         if (want_dsink) sink_terms[r * RPB + threadIdx.x / TPR] = term;
       }
     }
@@ -235,7 +248,9 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
                                                      int ql, int ql_pad, float scale,
                                                      const float* __restrict__ dsink_part,
                                                      float* __restrict__ dsinks, int B, int H,
-                                                     int sink_chunks, int convert) {
+                                                     int sink_chunks, int convert,
+                                                     const int32_t* __restrict__ cu_q,
+                                                     int total_q) {
   if (dsinks != nullptr && blockIdx.x == 0) {  // block-uniform
     __shared__ float red[256];
     const int n = B * sink_chunks;
@@ -259,6 +274,13 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
   const int i = e / (HD / 8), c = (e % (HD / 8)) * 8;
   if (i >= ql) return;
   for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
+    size_t rowbase = (size_t)bh * ql;
+    if (cu_q != nullptr) {  // sequence b of a variable-length batch
+      int qs, qlen;
+      varlen_seq(cu_q, bh / H, total_q, ql, qs, qlen);
+      if (i >= qlen) continue;
+      rowbase = (size_t)(bh % H) * total_q + qs;
+    }
     const float4* src = reinterpret_cast<const float4*>(dqacc + ((size_t)bh * ql_pad + i) * HD + c);
     const float4 v0 = src[0], v1 = src[1];
     uint4 out;
@@ -266,7 +288,7 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
     out.y = pack_bf16(v0.z * scale, v0.w * scale);
     out.z = pack_bf16(v1.x * scale, v1.y * scale);
     out.w = pack_bf16(v1.z * scale, v1.w * scale);
-    *reinterpret_cast<uint4*>(dq + ((size_t)bh * ql + i) * HD + c) = out;
+    *reinterpret_cast<uint4*>(dq + (rowbase + i) * HD + c) = out;
   }
 }
 
@@ -275,23 +297,23 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
 // q_abs + lo_off <= j <= q_abs + hi_off for some j in the tile (q_abs = kl - ql + i). Under the
 // causal band alone, key n0 is visible to the rows from n0 - (kl - ql) on, and to the last row.
 template <int HD, int BAND>
-__device__ __forceinline__ void bwd_mtile_range(int n0, const BwdKParams& p, int& first,
-                                                int& last) {
+__device__ __forceinline__ void bwd_mtile_range(int n0, const BwdKParams& p, int ql, int kl,
+                                                int& first, int& last) {
   constexpr int BM = BwdTraits<HD>::BM;
-  const int n_mt = (p.ql + BM - 1) / BM;
+  const int n_mt = (ql + BM - 1) / BM;
   if (BAND != kBandWindow) {
     first = 0;
     if (BAND == kBandCausal) {
-      const int first_row = n0 - (p.kl - p.ql);
+      const int first_row = n0 - (kl - ql);
       first = first_row <= 0 ? 0 : first_row / BM;
     }
     last = n_mt - 1;
     return;
   }
-  const long long off = (long long)p.kl - p.ql;
-  const long long n1 = min(n0 + kBN, p.kl) - 1;
+  const long long off = (long long)kl - ql;
+  const long long n1 = min(n0 + kBN, kl) - 1;
   const long long imin = max(0LL, (long long)n0 - off - p.hi_off);
-  const long long imax = min((long long)p.ql - 1, n1 - off - p.lo_off);
+  const long long imax = min((long long)ql - 1, n1 - off - p.lo_off);
   if (imax < imin) {
     first = 0;
     last = -1;
@@ -316,7 +338,7 @@ __device__ __forceinline__ void st_swizzled(uint8_t* chunk, int j, int g, uint4 
   *reinterpret_cast<uint4*>(chunk + j * 128 + ((g ^ (j & 7)) << 4)) = val;
 }
 
-template <int HD, int DV, int BAND, int MASKT>
+template <int HD, int DV, int BAND, int MASKT, bool VARLEN>
 __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                     const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mDO,
@@ -343,9 +365,26 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
   const int b = bkh / p.Hk, kh = bkh % p.Hk;
   const int G = p.H / p.Hk;
   const int n0 = (int)blockIdx.y * kBN;
+  // the rows of this problem: one (batch, kv head) of fixed length, or in a variable-length
+  // batch sequence b's own rows of the packed heads (tensor-map z = head, rows offset)
+  int ql = p.ql, kl = p.kl;
+  int kz = bkh, qzb = b * p.H, krow0 = 0, qrow0 = 0;
+  size_t kvrow0 = (size_t)bkh * p.kl;  // dK / dV row of key 0
+  if constexpr (VARLEN) {
+    int qs, ks;
+    const bool bad = varlen_seq(p.cu_q, b, p.total_q, p.ql, qs, ql) |
+                     varlen_seq(p.cu_k, b, p.total_k, p.kl, ks, kl);
+    if (bad && threadIdx.x == 0 && p.status) atomicCAS(p.status, kStatusOk, kStatusBadInput);
+    kz = kh;
+    qzb = 0;
+    krow0 = ks;
+    qrow0 = qs;
+    kvrow0 = (size_t)kh * p.total_k + ks;
+  }
+  if (n0 >= kl) return;  // a kv tile past this sequence's keys (the whole CTA leaves)
   int m_first, m_last;
   constexpr bool WIN = BAND == kBandWindow;
-  bwd_mtile_range<HD, BAND>(n0, p, m_first, m_last);
+  bwd_mtile_range<HD, BAND>(n0, p, ql, kl, m_first, m_last);
   const int nm = m_last - m_first + 1;  // query tiles per head (0 if none)
   const int n_iter = G * nm;          // (head, query tile) pairs this CTA visits
 
@@ -393,9 +432,9 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
       for (int s = 0; s < ST; ++s) last_use[s] = -1;
       mbar_arrive_expect_tx(&kv_full, LY::K_BYTES + LY::V_BYTES);
       for (int c = 0; c < KCH; ++c)
-        tma_load_3d(smem + LY::OFF_K + c * kBN * 128, &mK, &kv_full, c * 64, n0, bkh);
+        tma_load_3d(smem + LY::OFF_K + c * kBN * 128, &mK, &kv_full, c * 64, krow0 + n0, kz);
       for (int c = 0; c < VCH; ++c)
-        tma_load_3d(smem + LY::OFF_V + c * kBN * 128, &mV, &kv_full, c * 64, n0, bkh);
+        tma_load_3d(smem + LY::OFF_V + c * kBN * 128, &mV, &kv_full, c * 64, krow0 + n0, kz);
       for (int it = 0; it < n_iter; ++it) {
         const int st = it % ST;
         const uint32_t use = it / ST;
@@ -406,10 +445,10 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
         mbar_arrive_expect_tx(&qdo_full[st], LY::QT_BYTES + LY::DOT_BYTES + 2 * BM * 4);
         for (int c = 0; c < KCH; ++c)
           tma_load_3d(smem + LY::OFF_Q + st * LY::QT_BYTES + c * BM * 128, &mQ, &qdo_full[st],
-                      c * 64, q0, bh);
+                      c * 64, qrow0 + q0, qzb + h);
         for (int c = 0; c < VCH; ++c)
           tma_load_3d(smem + LY::OFF_DO + st * LY::DOT_BYTES + c * BM * 128, &mDO,
-                      &qdo_full[st], c * 64, q0, bh);
+                      &qdo_full[st], c * 64, qrow0 + q0, qzb + h);
         bulk_load(smem + LY::OFF_L + st * BM * 4, p.lse2 + (size_t)bh * p.ql_pad + q0, BM * 4,
                   &qdo_full[st]);
         bulk_load(smem + LY::OFF_D + st * BM * 4, p.dvec + (size_t)bh * p.ql_pad + q0, BM * 4,
@@ -572,7 +611,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
     // ------------------------------------------------------------------ WG0: P^T, dQ drain
     const int j = warp * 32 + lane;  // kv row within the tile == TMEM lane
     const int kv = n0 + j;
-    const bool kv_live = kv < p.kl;
+    const bool kv_live = kv < kl;
     const uint32_t lane_base = tbase + ((uint32_t)(warp * 32) << 16);
     const float c2 = p.scale_log2;
     const uint64_t c2v = f2_pack(c2, c2);
@@ -586,7 +625,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
       const uint32_t colS = LY::COL_S0 + (it % NSB) * BM;
       // column q (row q0 + q) sees this key iff qlo <= q <= qhi (no upper limit without a
       // window)
-      const int off = p.kl - p.ql;
+      const int off = kl - ql;
       const int hi_off = WIN ? p.hi_off : 0;
       const int qlo = kv - off - hi_off - q0;
       const int qhi = WIN ? kv - off - p.lo_off - q0 : BM;
@@ -633,7 +672,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
               float m4[4];
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                m4[k] = (mcol != nullptr && q0 + q + k < p.ql)
+                m4[k] = (mcol != nullptr && q0 + q + k < ql)
                             ? mask_log2_b<MASKT>(mcol, (long long)(q + k) * p.msq)
                             : 0.0f;
               b01 = f2_add(b01, f2_pack(m4[0], m4[1]));
@@ -826,7 +865,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
       tc_fence_after();
       have = ok && n_iter > 0;
     }
-    const size_t kvrow = (size_t)bkh * p.kl + (kv < p.kl ? kv : 0);
+    const size_t kvrow = kvrow0 + (kv < kl ? kv : 0);
 #pragma unroll 1
     for (int which = 0; which < 2; ++which) {
       const uint32_t col = which == 0 ? LY::COL_DV : LY::COL_DK;
@@ -845,7 +884,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
         for (int e = 0; e < 16; ++e)
           pk[e] = have ? pack_bf16(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul)
                        : 0u;
-        if (kv < p.kl) {
+        if (kv < kl) {
           uint4* dst = reinterpret_cast<uint4*>(out + c);
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
@@ -885,10 +924,10 @@ void bwd_carve_workspace(void* base, int B, int H, int ql, int d, float** lse2, 
   *dsink_part = reinterpret_cast<float*>(p + 2 * align256(rows * 4) + align256(rows * d * 4));
 }
 
-template <int HD, int DV, int BAND, int MASKT>
+template <int HD, int DV, int BAND, int MASKT, bool VARLEN = false>
 static cudaError_t launch_main_t(const BwdArgs& a, const BwdMaps& m, cudaStream_t s) {
   using LY = BwdLayout<HD, DV>;
-  auto kern = bwd_main_kernel<HD, DV, BAND, MASKT>;
+  auto kern = bwd_main_kernel<HD, DV, BAND, MASKT, VARLEN>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
@@ -904,6 +943,10 @@ static cudaError_t launch_main_t(const BwdArgs& a, const BwdMaps& m, cudaStream_
   kp.lo_off = a.lo_off;
   kp.hi_off = a.hi_off;
   kp.skip_dq = a.deterministic ? 1 : 0;
+  kp.cu_q = a.cu_q;
+  kp.cu_k = a.cu_k;
+  kp.total_q = a.total_q;
+  kp.total_k = a.total_k;
   kp.lse2 = a.lse2;
   kp.dvec = a.dvec;
   kp.dqacc = a.dqacc;
@@ -927,6 +970,7 @@ static cudaError_t launch_main_t(const BwdArgs& a, const BwdMaps& m, cudaStream_
 
 template <int HD, int DV, int BAND>
 static cudaError_t launch_main_m(const BwdArgs& a, const BwdMaps& m, cudaStream_t s) {
+  if (a.cu_q) return launch_main_t<HD, DV, BAND, 0, true>(a, m, s);  // (no mask with varlen)
   if (!a.mask) return launch_main_t<HD, DV, BAND, 0>(a, m, s);
   switch (a.mask_type) {
     case 0: return launch_main_t<HD, DV, BAND, 1>(a, m, s);
@@ -947,7 +991,7 @@ static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t
     bwd_prep_kernel<HD, DV><<<grid, 256, 0, s>>>(
         reinterpret_cast<const __nv_bfloat16*>(a.o), reinterpret_cast<const __nv_bfloat16*>(a.dO),
         a.lse, a.lse2, a.dvec, a.dqacc, a.sinks, dsink_part, BH, a.H, a.ql, a.ql_pad,
-        a.deterministic ? 0 : 1);
+        a.deterministic ? 0 : 1, a.cu_q, a.total_q);
     cudaError_t e = cudaGetLastError();
     profile_mark(kKernBwdPrep, 1, s);
     if (e != cudaSuccess) return e;
@@ -963,7 +1007,7 @@ static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t
       profile_mark(kKernBwdDq, 0, s);
       bwd_dq_kernel<HD><<<dim3(1, a.H < 65535 ? a.H : 65535), 256, 0, s>>>(
           a.dqacc, reinterpret_cast<__nv_bfloat16*>(a.dq), BH, a.ql, a.ql_pad, a.scale,
-          dsink_part, a.dsinks, a.B, a.H, sink_chunks, 0);
+          dsink_part, a.dsinks, a.B, a.H, sink_chunks, 0, a.cu_q, a.total_q);
       profile_mark(kKernBwdDq, 1, s);
     }
     return cudaGetLastError();
@@ -974,7 +1018,7 @@ static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t
     profile_mark(kKernBwdDq, 0, s);
     bwd_dq_kernel<HD><<<grid, 256, 0, s>>>(a.dqacc, reinterpret_cast<__nv_bfloat16*>(a.dq), BH,
                                            a.ql, a.ql_pad, a.scale, dsink_part, a.dsinks, a.B,
-                                           a.H, sink_chunks, 1);
+                                           a.H, sink_chunks, 1, a.cu_q, a.total_q);
     profile_mark(kKernBwdDq, 1, s);
   }
   return cudaGetLastError();

@@ -81,6 +81,9 @@ struct DqKParams {
   const float* dvec;        // [B*H, ql_pad]: D
   __nv_bfloat16* dq;        // [B, H, ql, HD]
   int* status;
+  const int32_t* cu_q;  // variable-length batch: sequence offsets, or nullptr
+  const int32_t* cu_k;
+  int total_q, total_k;
   int H, Hk, ql, kl, ql_pad;
   int lo_off, hi_off;
   float scale, scale_log2;
@@ -117,9 +120,24 @@ __global__ void __launch_bounds__(DqLayout<HD, DV>::THREADS, 1)
   const int b = bh / p.H, h = bh % p.H;
   const int bkh = b * p.Hk + h / (p.H / p.Hk);
   const int m0 = (int)blockIdx.y * kQM;
-  const int r1 = min(m0 + kQM, p.ql) - 1;
+  // the rows of this problem: one (batch, head), or sequence b of a variable-length batch
+  int ql = p.ql, kl = p.kl;
+  int qz = bh, kz = bkh, qrow0 = 0, krow0 = 0;
+  size_t orow0 = (size_t)bh * p.ql;  // dQ row of query 0
+  if (p.cu_q != nullptr) {
+    int qs, ks;
+    varlen_seq(p.cu_q, b, p.total_q, p.ql, qs, ql);
+    varlen_seq(p.cu_k, b, p.total_k, p.kl, ks, kl);
+    qz = h;
+    kz = h / (p.H / p.Hk);
+    qrow0 = qs;
+    krow0 = ks;
+    orow0 = (size_t)h * p.total_q + qs;
+  }
+  if (m0 >= ql) return;  // a query tile past this sequence's rows (the whole CTA leaves)
+  const int r1 = min(m0 + kQM, ql) - 1;
   int J0, J1;
-  band_kv_tiles<kQN, BAND>(m0, r1, p.ql, p.kl, p.lo_off, p.hi_off, J0, J1);
+  band_kv_tiles<kQN, BAND>(m0, r1, ql, kl, p.lo_off, p.hi_off, J0, J1);
   if (J0 < 0) J0 = J1 = 0;
   const int ntt = J1 - J0;  // kv tiles this CTA visits
 
@@ -158,9 +176,9 @@ __global__ void __launch_bounds__(DqLayout<HD, DV>::THREADS, 1)
       for (int s = 0; s < STAGES; ++s) last[s] = -1;
       mbar_arrive_expect_tx(&q_full, LY::Q_BYTES + LY::DO_BYTES);
       for (int c = 0; c < KCH; ++c)
-        tma_load_3d(smem + LY::OFF_Q + c * kQM * 128, &mQ, &q_full, c * 64, m0, bh);
+        tma_load_3d(smem + LY::OFF_Q + c * kQM * 128, &mQ, &q_full, c * 64, qrow0 + m0, qz);
       for (int c = 0; c < VCH; ++c)
-        tma_load_3d(smem + LY::OFF_DO + c * kQM * 128, &mDO, &q_full, c * 64, m0, bh);
+        tma_load_3d(smem + LY::OFF_DO + c * kQM * 128, &mDO, &q_full, c * 64, qrow0 + m0, qz);
       const uint64_t pol = policy_evict_last();
       for (int jj = 0; jj < ntt; ++jj) {
         const int st = jj % STAGES;
@@ -170,10 +188,10 @@ __global__ void __launch_bounds__(DqLayout<HD, DV>::THREADS, 1)
         mbar_arrive_expect_tx(&kv_full[st], LY::K_BYTES + LY::V_BYTES);
         for (int c = 0; c < KCH; ++c)
           tma_load_3d_hint(smem + LY::OFF_K + st * LY::K_BYTES + c * kQN * 128, &mK, &kv_full[st],
-                           c * 64, n0, bkh, pol);
+                           c * 64, krow0 + n0, kz, pol);
         for (int c = 0; c < VCH; ++c)
           tma_load_3d_hint(smem + LY::OFF_V + st * LY::V_BYTES + c * kQN * 128, &mV, &kv_full[st],
-                           c * 64, n0, bkh, pol);
+                           c * 64, krow0 + n0, kz, pol);
         last[st] = jj;
       }
       mbar_wait_drain(&q_full, 0);
@@ -242,18 +260,18 @@ __global__ void __launch_bounds__(DqLayout<HD, DV>::THREADS, 1)
     const int r = warp * 32 + lane;  // query row within the tile == TMEM lane
     const int i = m0 + r;
     const uint32_t lane_base = tbase + ((uint32_t)(warp * 32) << 16);
-    const int off = p.kl - p.ql;
+    const int off = kl - ql;
     const int hi_off = WIN ? p.hi_off : 0;
     // visible keys of this row: [klo_row, khi_row]; the tile bounds decide interior tiles
     const int klo_row = WIN ? off + i + p.lo_off : 0;
-    const int khi_row = BAND != kBandNone ? min(p.kl - 1, off + i + hi_off) : p.kl - 1;
+    const int khi_row = BAND != kBandNone ? min(kl - 1, off + i + hi_off) : kl - 1;
     const int klo_tile = WIN ? off + r1 + p.lo_off : 0;
-    const int khi_tile = BAND != kBandNone ? min(p.kl - 1, off + m0 + hi_off) : p.kl - 1;
+    const int khi_tile = BAND != kBandNone ? min(kl - 1, off + m0 + hi_off) : kl - 1;
     const float nl2 = p.lse2[(size_t)bh * p.ql_pad + i];  // i < ql_pad: padding rows hold -inf
     const float Dr = p.dvec[(size_t)bh * p.ql_pad + i];
     const float c2 = p.scale_log2;
     const void* mrow = nullptr;
-    if (MASKT != 0 && i < p.ql) {
+    if (MASKT != 0 && i < ql) {
       const size_t es = MASKT == 1 ? 4 : MASKT == 2 ? 2 : 1;
       mrow = reinterpret_cast<const uint8_t*>(p.mask) +
              (b * p.msb + (long long)h * p.msh + (long long)i * p.msq) * es;
@@ -286,7 +304,7 @@ __global__ void __launch_bounds__(DqLayout<HD, DV>::THREADS, 1)
             const int c = c32 * 32 + 2 * e + u;
             float x = fmaf(__uint_as_float(rs[c32][2 * e + u]), c2, nl2);
             if (MASKT != 0)
-              x += (mrow != nullptr && n0 + c < p.kl) ? dq_mask_log2<MASKT>(mrow, n0 + c) : 0.0f;
+              x += (mrow != nullptr && n0 + c < kl) ? dq_mask_log2<MASKT>(mrow, n0 + c) : 0.0f;
             float pv = ex2(x);
             if (edge && ((WIN && c < lim_lo) || c > lim_hi)) pv = 0.0f;
             ds2[u] = pv * (__uint_as_float(rd[c32][2 * e + u]) - Dr);
@@ -306,7 +324,7 @@ __global__ void __launch_bounds__(DqLayout<HD, DV>::THREADS, 1)
       tc_fence_after();
       have = ok;
     }
-    __nv_bfloat16* out = p.dq + ((size_t)bh * p.ql + (i < p.ql ? i : 0)) * HD;
+    __nv_bfloat16* out = p.dq + (orow0 + (i < ql ? i : 0)) * HD;
 #pragma unroll 1
     for (int c = 0; c < HD; c += 32) {
       uint32_t rq[32];
@@ -320,7 +338,7 @@ __global__ void __launch_bounds__(DqLayout<HD, DV>::THREADS, 1)
         pk[e] = have ? pack_bf16(__uint_as_float(rq[2 * e]) * p.scale,
                                  __uint_as_float(rq[2 * e + 1]) * p.scale)
                      : 0u;
-      if (i < p.ql) {
+      if (i < ql) {
         uint4* dst = reinterpret_cast<uint4*>(out + c);
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4)
@@ -358,6 +376,10 @@ static cudaError_t launch_dq_det_t(const BwdArgs& a, const DqMaps& m, cudaStream
   kp.dvec = a.dvec;
   kp.dq = reinterpret_cast<__nv_bfloat16*>(a.dq);
   kp.status = a.status;
+  kp.cu_q = a.cu_q;
+  kp.cu_k = a.cu_k;
+  kp.total_q = a.total_q;
+  kp.total_k = a.total_k;
   kp.H = a.H;
   kp.Hk = a.Hk;
   kp.ql = a.ql;

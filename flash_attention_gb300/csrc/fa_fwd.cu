@@ -87,8 +87,11 @@ struct FwdKParams {
   __nv_bfloat16* o;
   float* lse;
   const float* sinks;  // [H] natural-log sink logits, or nullptr
+  const int32_t* cu_q;  // variable-length batch: sequence offsets, or nullptr
+  const int32_t* cu_k;
+  int total_q, total_k;
   int* status;
-  int H, Hk, ql, kl, n_mblk;
+  int H, Hk, ql, kl, n_mblk;  // ql, kl: the longest sequence in a variable-length batch
   int lo_off, hi_off;  // key j is visible to row i iff q_abs + lo_off <= j <= q_abs + hi_off
   float scale_log2;    // scale * log2(e)
 };
@@ -111,18 +114,18 @@ __device__ __forceinline__ float mask_log2(const void* mrow, long long j) {
 // and the caller places it at the end of the previous tile's range, so that the ranges of a
 // CTA's tiles stay ordered.
 template <int HD, int BAND>
-__device__ __forceinline__ void fwd_tile_range(int m0, int t, const FwdKParams& p, int& first,
-                                               int& last) {
+__device__ __forceinline__ void fwd_tile_range(int m0, int t, const FwdKParams& p, int ql,
+                                               int kl, int& first, int& last) {
   const int r0 = m0 + t * kBM;
-  if (BAND == kBandWindow && r0 >= p.ql) {  // a tile wholly past the last query row
+  if (BAND == kBandWindow && r0 >= ql) {  // a tile wholly past the last query row
     first = last = -1;
     return;
   }
-  const int r1 = min(m0 + (t + 1) * kBM, p.ql) - 1;  // last row of the tile (clamped)
-  band_kv_tiles<FwdTraits<HD>::BN, BAND>(r0, r1, p.ql, p.kl, p.lo_off, p.hi_off, first, last);
+  const int r1 = min(m0 + (t + 1) * kBM, ql) - 1;  // last row of the tile (clamped)
+  band_kv_tiles<FwdTraits<HD>::BN, BAND>(r0, r1, ql, kl, p.lo_off, p.hi_off, first, last);
 }
 
-template <int HD, int DV, int BAND, int MASKT>
+template <int HD, int DV, int BAND, int MASKT, bool VARLEN>
 __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                const __grid_constant__ CUtensorMap mV, const FwdKParams p) {
@@ -148,12 +151,29 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
   const int m0 = mblk * NQ * kBM;
   const int b = bh / p.H, h = bh % p.H;
   const int bkh = b * p.Hk + h / (p.H / p.Hk);
+  // the rows of this problem: one (batch, head) of fixed length, or in a variable-length
+  // batch sequence b's own rows of the packed head h (tensor-map z = head, rows offset)
+  int ql = p.ql, kl = p.kl;
+  int qz = bh, kz = bkh, qrow0 = 0, krow0 = 0;
+  size_t orow0 = (size_t)bh * p.ql;  // O / L row of query 0
+  if constexpr (VARLEN) {
+    int qs, ks;
+    const bool bad = varlen_seq(p.cu_q, b, p.total_q, p.ql, qs, ql) |
+                     varlen_seq(p.cu_k, b, p.total_k, p.kl, ks, kl);
+    if (bad && threadIdx.x == 0 && p.status) atomicCAS(p.status, kStatusOk, kStatusBadInput);
+    qz = h;
+    kz = h / (p.H / p.Hk);
+    qrow0 = qs;
+    krow0 = ks;
+    orow0 = (size_t)h * p.total_q + qs;
+  }
+  if (m0 >= ql) return;  // a query tile past this sequence's rows (the whole CTA leaves)
 
   // kv tile ranges of the query tiles, and their union [J0, J1)
   constexpr bool WIN = BAND == kBandWindow;
   int jt0[NQ], jt1[NQ];
 #pragma unroll
-  for (int t = 0; t < NQ; ++t) fwd_tile_range<HD, BAND>(m0, t, p, jt0[t], jt1[t]);
+  for (int t = 0; t < NQ; ++t) fwd_tile_range<HD, BAND>(m0, t, p, ql, kl, jt0[t], jt1[t]);
   int J0 = 0, J1 = 0;
   if (!WIN) {
 #pragma unroll
@@ -217,7 +237,7 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
       for (int t = 0; t < NQ; ++t)
         for (int c = 0; c < KCH; ++c)
           tma_load_3d(smem + LY::OFF_Q + t * LY::Q_TILE_BYTES + c * kBM * 128, &mQ, &q_full,
-                      c * 64, m0 + t * kBM, bh);
+                      c * 64, qrow0 + m0 + t * kBM, qz);
       for (int j = J0; j < J1; ++j) {
         const int st = (j - J0) % STAGES;
         const uint32_t use = (j - J0) / STAGES;
@@ -225,13 +245,13 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
         mbar_arrive_expect_tx(&k_full[st], LY::K_TILE_BYTES);
         for (int c = 0; c < KCH; ++c)
           tma_load_3d_hint(smem + LY::OFF_K + st * LY::K_TILE_BYTES + c * BN * 128, &mK,
-                           &k_full[st], c * 64, j * BN, bkh, pol_kv);
+                           &k_full[st], c * 64, krow0 + j * BN, kz, pol_kv);
         last_k[st] = j - J0;
         if (use > 0 && !mbar_wait(&v_empty[st], (use - 1) & 1, &abort_flag)) break;
         mbar_arrive_expect_tx(&v_full[st], LY::V_TILE_BYTES);
         for (int c = 0; c < VCH; ++c)
           tma_load_3d_hint(smem + LY::OFF_V + st * LY::V_TILE_BYTES + c * BN * 128, &mV,
-                           &v_full[st], c * 64, j * BN, bkh, pol_kv);
+                           &v_full[st], c * 64, krow0 + j * BN, kz, pol_kv);
         last_v[st] = j - J0;
       }
       // Let every copy this thread started land before the CTA can exit.
@@ -336,24 +356,24 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
     const int i = m0 + t * kBM + r;
     // kv tiles [kt0, kt0 + ntt) of this query tile (an empty window range gives ntt = 0)
     int kt0, kt1;
-    fwd_tile_range<HD, BAND>(m0, t, p, kt0, kt1);
+    fwd_tile_range<HD, BAND>(m0, t, p, ql, kl, kt0, kt1);
     const int ntt = kt1 - kt0;
-    const int off = p.kl - p.ql;
+    const int off = kl - ql;
     // visible keys of this row: [klo_row, khi_row] (the row band, clipped to the keys)
     const int hi_off = WIN ? p.hi_off : 0;
     const int klo_row = WIN ? off + i + p.lo_off : 0;
-    const int khi_row = BAND != kBandNone ? min(p.kl - 1, off + i + hi_off) : p.kl - 1;
+    const int khi_row = BAND != kBandNone ? min(kl - 1, off + i + hi_off) : kl - 1;
     // the same bounds at the tile's first and last rows decide whether a kv tile is interior
     const int tile_row0 = m0 + t * kBM;
-    const int tile_row1 = min(tile_row0 + kBM, p.ql) - 1;
+    const int tile_row1 = min(tile_row0 + kBM, ql) - 1;
     const int klo_tile = WIN ? off + tile_row1 + p.lo_off : 0;  // largest lo
     const int khi_tile =
-        BAND != kBandNone ? min(p.kl - 1, off + tile_row0 + hi_off) : p.kl - 1;  // smallest hi
+        BAND != kBandNone ? min(kl - 1, off + tile_row0 + hi_off) : kl - 1;  // smallest hi
     const float c2 = p.scale_log2;
     const uint32_t lane_base = tbase + ((uint32_t)(wl * 32) << 16);
     const uint32_t o_col = t * LY::TILE_COLS;
     const void* mrow = nullptr;
-    if (MASKT != 0 && i < p.ql) {
+    if (MASKT != 0 && i < ql) {
       const int b_ = bh / p.H, h_ = bh % p.H;
       const size_t es = MASKT == 1 ? 4 : MASKT == 2 ? 2 : 1;
       mrow = reinterpret_cast<const uint8_t*>(p.mask) +
@@ -391,7 +411,7 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
             const int c = c32 * 32 + e;
             float v = __uint_as_float(sr[c32][e]);
             if (MASKT != 0) {
-              const float mv = (mrow != nullptr && n0 + c < p.kl) ? mask_log2<MASKT>(mrow, n0 + c) : 0.0f;
+              const float mv = (mrow != nullptr && n0 + c < kl) ? mask_log2<MASKT>(mrow, n0 + c) : 0.0f;
               v = fmaf(v, c2, mv);
             }
             if ((WIN && c < lim_lo) || c > lim_hi) v = -INFINITY;
@@ -496,7 +516,7 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
         L = s2 * kLn2;  // a row that sees no key: O = 0, L = sink
       }
     }
-    __nv_bfloat16* orow = p.o + ((size_t)bh * p.ql + (i < p.ql ? i : 0)) * DV;
+    __nv_bfloat16* orow = p.o + (orow0 + (i < ql ? i : 0)) * DV;
 #pragma unroll 1
     for (int c = 0; c < DV; c += 32) {
       uint32_t orr[32];
@@ -511,7 +531,7 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
         float a1 = have_o ? __uint_as_float(orr[2 * e + 1]) * inv : 0.0f;
         packed[e] = pack_bf16(a0, a1);
       }
-      if (i < p.ql) {
+      if (i < ql) {
         uint4* dst = reinterpret_cast<uint4*>(orow + c);
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4)
@@ -519,7 +539,7 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
                                packed[4 * v4 + 3]);
       }
     }
-    if (i < p.ql) p.lse[(size_t)bh * p.ql + i] = L;
+    if (i < ql) p.lse[orow0 + i] = L;
   }
 
   tc_fence_before();
@@ -533,10 +553,10 @@ int fwd_kv_box_rows(int d) {
   return d == 64 ? FwdTraits<64>::BN : d == 128 ? FwdTraits<128>::BN : FwdTraits<256>::BN;
 }
 
-template <int HD, int DV, int BAND, int MASKT>
+template <int HD, int DV, int BAND, int MASKT, bool VARLEN = false>
 static cudaError_t launch_fwd_t(const FwdArgs& a, const FwdMaps& m, cudaStream_t stream) {
   using LY = FwdLayout<HD, DV>;
-  auto kern = fwd_kernel<HD, DV, BAND, MASKT>;
+  auto kern = fwd_kernel<HD, DV, BAND, MASKT, VARLEN>;
   static bool attr_set = false;  // per instantiation; the attribute is per device function
   if (!attr_set) {
     cudaError_t e =
@@ -552,6 +572,10 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, const FwdMaps& m, cudaStream_t
   kp.o = reinterpret_cast<__nv_bfloat16*>(a.o);
   kp.lse = a.lse;
   kp.sinks = a.sinks;
+  kp.cu_q = a.cu_q;
+  kp.cu_k = a.cu_k;
+  kp.total_q = a.total_q;
+  kp.total_k = a.total_k;
   kp.status = a.status;
   kp.H = a.H;
   kp.Hk = a.Hk;
@@ -571,6 +595,7 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, const FwdMaps& m, cudaStream_t
 
 template <int HD, int DV, int BAND>
 static cudaError_t launch_fwd_m(const FwdArgs& a, const FwdMaps& m, cudaStream_t s) {
+  if (a.cu_q) return launch_fwd_t<HD, DV, BAND, 0, true>(a, m, s);  // (no mask with varlen)
   if (!a.mask) return launch_fwd_t<HD, DV, BAND, 0>(a, m, s);
   switch (a.mask_type) {
     case 0: return launch_fwd_t<HD, DV, BAND, 1>(a, m, s);

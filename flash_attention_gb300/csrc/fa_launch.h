@@ -8,6 +8,19 @@
 
 namespace fa {
 
+// Bounds of sequence b of a variable-length batch from its offsets: start and length, clamped
+// to [0, total] and to `maxlen`. Returns true when the offsets were out of range.
+__device__ __forceinline__ bool varlen_seq(const int32_t* cu, int b, int total, int maxlen,
+                                           int& start, int& len) {
+  int s = cu[b], e = cu[b + 1];
+  const bool bad = s < 0 || e < s || e > total || e - s > maxlen;
+  s = s < 0 ? 0 : (s > total ? total : s);
+  e = e < s ? s : (e > total ? total : e);
+  start = s;
+  len = e - s < maxlen ? e - s : maxlen;
+  return bad;
+}
+
 // Device-side status codes, written into the per-device status word the kernels are given (a
 // device int owned by the library): kStatusTimeout when a bounded wait gave up (the kernel then
 // winds down), kStatusBadInput when a paged kernel met a length or block-table entry out of
@@ -64,8 +77,11 @@ struct FwdArgs {
   void* o;            // bf16 [B, H, ql, d]
   float* lse;         // [B, H, ql]
   const float* sinks; // [H] natural-log sink logits, or nullptr
+  const int32_t* cu_q;  // variable-length batch: [B + 1] row offsets of the sequences, or nullptr
+  const int32_t* cu_k;
+  int total_q, total_k;  // rows per head of the packed q / k (variable-length batch)
   int* status;        // device status word (nullable)
-  int B, H, Hk, ql, kl, d;
+  int B, H, Hk, ql, kl, d;  // ql, kl: the longest sequence in a variable-length batch
   int dval;           // value head dim (of v and o)
   float scale;
   int lo_off, hi_off;
@@ -103,6 +119,9 @@ struct BwdArgs {
   float* dvec;   // workspace [B*H, ql_pad]: D = rowsum(dO * O)
   float* dqacc;  // workspace [B*H, ql_pad, d] f32 dQ accumulator
   const float* sinks;  // [H] sink logits, or nullptr
+  const int32_t* cu_q;  // variable-length batch (see FwdArgs), or nullptr
+  const int32_t* cu_k;
+  int total_q, total_k;
   float* dsinks;       // [H] sink gradient output, or nullptr (then no sink partials)
   float* dsink_part;   // workspace [B*H, sink_chunks]: per-block partial sums of dsinks
   int* status;

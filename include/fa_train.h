@@ -121,7 +121,18 @@ typedef struct fa_params {
  * separate kernel that walks the kv tiles of each query tile in a fixed order, instead of
  * being added into an f32 accumulator by many CTAs at once. dK, dV and dsinks are always
  * reduced in a fixed order, so the whole backward then returns the same bits on every run.
- * It recomputes S and dP once more, which costs time. Ignored by the forward. */
+ * It recomputes S and dP once more, which costs time. Ignored by the forward.
+ *
+ * Variable-length batch (no counterpart on the pages; each sequence is the fixed-length problem
+ * above on its own rows): with cu_seqlens_q non-NULL, `batch` independent sequences are packed
+ * head-major without padding: q, o, dO, dQ are [n_heads, total_q, d] (o, dO with value_dim),
+ * k, v, dK, dV are [n_kv_heads, total_k, d], lse is [n_heads, total_q]. Sequence b owns rows
+ * cu_seqlens_q[b] .. cu_seqlens_q[b+1] of q and cu_seqlens_k[b] .. cu_seqlens_k[b+1] of k
+ * (int32 device arrays of batch + 1 entries, 0 first, non-decreasing, the last = total_q /
+ * total_k), and fa_params.ql / kl give the longest sequence (they size the grids). Causal and
+ * window bands align bottom-right within each sequence. A sequence with no keys gives O = 0
+ * and L = -inf (or its sink). Offsets out of range are clamped and reported by
+ * fa_device_status (FA_ERR_BAD_INPUT). No mask may be given (FA_ERR_UNSUPPORTED). */
 typedef struct fa_options {
   int32_t window_left;   /* -1, or >= 0 */
   int32_t window_right;  /* -1, or >= 0 */
@@ -134,6 +145,10 @@ typedef struct fa_options {
   float* dsinks;         /* backward only: NULL, or [n_heads] f32 output on the device */
   int32_t deterministic; /* 0 or 1 (backward only) */
   int32_t reserved;      /* must be 0 */
+  const int32_t* cu_seqlens_q; /* NULL, or the variable-length batch's query offsets [batch+1] */
+  const int32_t* cu_seqlens_k; /* its key offsets [batch+1]; both or neither */
+  int32_t total_q;       /* variable-length batch: rows per head of q (>= 1) */
+  int32_t total_k;       /* rows per head of k and v (>= 1) */
 } fa_options;
 
 /* 1 if this build has kernels for the (head_dim, value_dim) pair, else 0. */

@@ -133,7 +133,7 @@ def _bwd_ex(lib, params, opts, mask=None):
 def _opts(**kw):
     base = dict(window_left=-1, window_right=-1, mask_type=0, value_dim=0, mask_stride_b=0,
                 mask_stride_h=0, mask_stride_q=128, sinks=None, dsinks=None, deterministic=0,
-                reserved=0)
+                reserved=0, cu_seqlens_q=None, cu_seqlens_k=None, total_q=0, total_k=0)
     base.update(kw)
     return fa.FaOptions(**base)
 
@@ -142,6 +142,8 @@ BAD_OPTIONS = [
     dict(window_left=-2), dict(window_right=-5), dict(mask_type=3), dict(mask_type=-1),
     dict(value_dim=-1), dict(mask_stride_b=-1), dict(mask_stride_h=-4),
     dict(mask_stride_q=-128), dict(sinks=FAKE + 2), dict(deterministic=2), dict(reserved=1),
+    dict(cu_seqlens_q=FAKE), dict(cu_seqlens_q=FAKE, cu_seqlens_k=FAKE + 2, total_q=4, total_k=4),
+    dict(cu_seqlens_q=FAKE, cu_seqlens_k=FAKE, total_q=0, total_k=4),
 ]
 
 
@@ -186,8 +188,14 @@ def test_value_dim_without_kernels_is_unsupported(lib):
     assert _bwd_ex(lib, GOOD, _opts(value_dim=96)) == fa.FA_ERR_UNSUPPORTED
 
 
+def test_varlen_with_a_mask_is_unsupported(lib):
+    o = _opts(cu_seqlens_q=FAKE, cu_seqlens_k=FAKE, total_q=8, total_k=8)
+    assert _fwd_ex(lib, GOOD, o, mask=FAKE) == fa.FA_ERR_UNSUPPORTED
+
+
 def test_options_struct_layout():
-    assert ctypes.sizeof(fa.FaOptions) == 64
+    assert ctypes.sizeof(fa.FaOptions) == 88
+    assert fa.FaOptions.cu_seqlens_q.offset == 64 and fa.FaOptions.total_k.offset == 84
     assert fa.FaOptions.deterministic.offset == 56
     assert fa.FaOptions.mask_stride_b.offset == 16
     assert fa.FaOptions.sinks.offset == 40 and fa.FaOptions.dsinks.offset == 48
