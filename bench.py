@@ -75,7 +75,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(fa_inputs.BY_NAME) + sorted(fa_inputs.DECODE_BY_NAME))
+                    choices=sorted(fa_inputs.BY_NAME) + sorted(fa_inputs.DECODE_BY_NAME)
+                    + sorted(fa_inputs.VARLEN_BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ncu", action="store_true",
@@ -476,6 +477,197 @@ def run_paged(args, w):
         print(json.dumps(out), flush=True)
 
 
+# ------------------------------------------------------------------ variable-length batches
+def varlen_config(w, n):
+    return {"workload": w.name, "n_heads": w.n_heads, "n_kv_heads": w.n_kv_heads,
+            "head_dim": w.head_dim, "sequences": w.batch, "lengths": list(w.q_lens),
+            "total_tokens": int(sum(w.q_lens)), "causal": w.causal,
+            "flop_rule": "fwd 4d, bwd 10d per visible (query, key) pair of each sequence",
+            "l2": "inputs larger than L2 (no flush)",
+            "parallelism": "replicas" if n == 1 else f"{n} independent replicas"}
+
+
+def varlen_oracle_sample(w, x, budget_s, cores):
+    """The CPU oracle (fwd + bwd) on whole sequences, shortest first, for ~budget_s:
+    (FLOPs, seconds, sequences)."""
+    import oracle
+
+    q, k, v, do = x.widened()
+    order = sorted(range(w.batch), key=lambda b: w.q_lens[b])
+    spent, fl, n = 0.0, 0.0, 0
+    for b in order:
+        if spent >= budget_s:
+            break
+        qs, qe, ks, ke = x.cu_q[b], x.cu_q[b + 1], x.cu_k[b], x.cu_k[b + 1]
+        sub = fa_inputs.VarlenWorkload("s", w.n_heads, w.n_kv_heads, w.head_dim, (qe - qs,),
+                                       (ke - ks,), w.causal)
+        t0 = time.perf_counter()
+        oracle.fwd(q[None, :, qs:qe], k[None, :, ks:ke], v[None, :, ks:ke], None, scale=w.scale,
+                   causal=w.causal, nthreads=cores)
+        oracle.bwd(q[None, :, qs:qe], k[None, :, ks:ke], v[None, :, ks:ke], None,
+                   do[None, :, qs:qe], scale=w.scale, causal=w.causal, nthreads=cores)
+        spent += time.perf_counter() - t0
+        fl += sum(sub.flops())
+        n += 1
+    return fl, spent, n
+
+
+def run_varlen_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    x = fa_inputs.make_varlen_inputs(w, index=50 + fa_inputs.VARLEN_WORKLOADS.index(w))
+    cores = cpu_cores()
+    per_step = max(1.0, 120.0 / max(args.steps + args.warmup, 1))
+    for _ in range(args.warmup):
+        varlen_oracle_sample(w, x, min(per_step, 2.0), cores)
+    fl, sec = 0.0, 0.0
+    for _ in range(args.steps):
+        f_, s_, _ = varlen_oracle_sample(w, x, per_step, cores)
+        fl += f_
+        sec += s_
+    value = fl / sec / 1e12
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": sec / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": varlen_config(w, args.gpus),
+           "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                            "sample": f"per step: whole sequences, shortest first, ~{per_step:.0f} s"},
+           "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def run_varlen(args, w):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import flash_attention_gb300 as fa
+
+    fa.build()
+    fa.load_library()
+    x = fa_inputs.make_varlen_inputs(w, index=50 + fa_inputs.VARLEN_WORKLOADS.index(w),
+                                     seed_base=fa_inputs.SEED_BASE + 1_000_003 * rank)
+
+    def bf(bits):
+        return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16)
+
+    h_q, h_k, h_v, h_do = (bf(t).pin_memory() for t in (x.q, x.k, x.v, x.do))
+    q, k, v, do = (t.to(dev) for t in (h_q, h_k, h_v, h_do))
+    cq, ck = torch.from_numpy(x.cu_q).to(dev), torch.from_numpy(x.cu_k).to(dev)
+    mq, mk = max(w.q_lens), max(w.k_lens)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    params, opts = fa.varlen_params_options(q, k, v, cq, ck, mq, mk, scale=w.scale,
+                                            causal=w.causal)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.fa_train_fwd_ex(q, k, v, None, o, lse, params, opts, stream)
+        fa.fa_train_bwd_ex(q, k, v, o, lse, do, None, dq, dk, dv, params, opts, stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    if args.ncu:
+        for _ in range(args.warmup + args.steps):
+            step()
+        torch.cuda.synchronize()
+        print(f"ncu mode: {w.name}, status {fa.fa_device_status(True)}", flush=True)
+        return
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if fa.fa_device_status(True) != fa.FA_OK:
+        clocks.stop()
+        raise RuntimeError("a kernel reported an error during warm-up")
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fa.fa_profile_enable(True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    fa.fa_profile_enable(False)
+    clk = clocks.stop()
+    barrier()
+    prof = fa.fa_profile_read()
+    if fa.fa_device_status(True) != fa.FA_OK:
+        raise RuntimeError("a kernel reported an error during the timed steps")
+    tot_ms = reduce_max(e0.elapsed_time(e1) / args.steps, world, dev)
+    fwd_f, bwd_f = w.flops()
+    value = world * (fwd_f + bwd_f) / (tot_ms * 1e-3) / 1e12
+    peaks = load_peaks()
+    dom_name, (dom_ms, dom_n) = max(prof.items(), key=lambda kv: kv[1][0])
+    algo = {"fwd_kernel": fwd_f, "bwd_main_kernel": bwd_f}.get(dom_name, 0.0)
+    achieved = algo / (dom_ms / max(dom_n, 1) * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dom_name, "achieved": achieved,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"],
+                "traffic": recorded_traffic(dom_name, w.name),
+                "peak_source": f"bf16_tflops burst, {peaks['source']}",
+                "per_kernel_ms": {n: (t / max(c, 1)) for n, (t, c) in prof.items() if c}}
+    e2e = None
+    if not args.no_e2e:
+        h_dq, h_dk, h_dv = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv))
+
+        def e2e_step():
+            for d_, h_ in ((q, h_q), (k, h_k), (v, h_v), (do, h_do)):
+                d_.copy_(h_, non_blocking=True)
+            step()
+            for d_, h_ in ((dq, h_dq), (dk, h_dk), (dv, h_dv)):
+                h_.copy_(d_, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        f1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max(f0.elapsed_time(f1) / args.steps, world, dev)
+        e2e = {"value": world * (fwd_f + bwd_f) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_do)),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in (h_dq, h_dk, h_dv))}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cores = cpu_cores()
+        f_, s_, n_ = varlen_oracle_sample(w, x, 10.0, cores)
+        cpu = {"value": f_ / s_ / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"fwd+bwd of the {n_} shortest sequence(s), f64, {s_:.1f} s"}
+    if rank == 0:
+        out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms,
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+               "dtype": "bf16", "data": "synthetic", "config": varlen_config(w, world),
+               "pct_of_peak": 100.0 * value / (world * peaks["bf16_tflops"]),
+               "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+               "gpu_launches": int(sum(c for _, c in prof.values())), "clocks": clk}
+        print(json.dumps(out), flush=True)
+
+
 def config_of(w, n):
     return {"workload": w.name, "batch": w.batch, "n_heads": w.n_heads,
             "n_kv_heads": w.n_kv_heads, "ql": w.ql, "kl": w.kl, "head_dim": w.head_dim,
@@ -687,6 +879,13 @@ def run_ours(args, w):
 
 def main():
     args = parse()
+    if args.workload in fa_inputs.VARLEN_BY_NAME:
+        w = fa_inputs.VARLEN_BY_NAME[args.workload]
+        if args.impl == "reference":
+            run_varlen_reference(args, w)
+        else:
+            run_varlen(args, w)
+        return
     if args.workload in fa_inputs.DECODE_BY_NAME:
         w = fa_inputs.DECODE_BY_NAME[args.workload]
         if args.impl == "reference":

@@ -356,3 +356,13 @@ def make_varlen_inputs(w: VarlenWorkload, index: int = 33, seed_base: int | None
     v = normal_bf16(base + T_V, (w.n_kv_heads, tk, w.head_dim))
     do = normal_bf16(base + T_DO, (w.n_heads, tq, w.head_dim), w.do_std)
     return VarlenInputs(q, k, v, do, cu_q, cu_k)
+
+
+# Variable-length workloads of the benchmark (index = position + 50 in the seed formula).
+_MIX = (8192, 512, 3000, 1024, 6000, 256, 4096, 2048, 7000, 768, 1500, 5000, 300, 2500, 3500,
+        4500)
+VARLEN_WORKLOADS = [
+    # 16 causal sequences of 256 to 8192 tokens packed together, GQA 32:8, head_dim 128
+    VarlenWorkload("varlen_d128_mix", 32, 8, 128, _MIX, _MIX, True, do_std=0.1),
+]
+VARLEN_BY_NAME = {w.name: w for w in VARLEN_WORKLOADS}

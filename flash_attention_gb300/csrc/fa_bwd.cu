@@ -126,6 +126,7 @@ struct BwdKParams {
   int H, Hk, ql, kl, ql_pad;
   int lo_off, hi_off;  // key j is visible to query row i iff q_abs + lo_off <= j <= q_abs + hi_off
   int skip_dq;         // 1: dQ comes from the deterministic dQ kernel; no dQ work here
+  int tiles_fast;      // 1: blockIdx.x = kv tile, y = (batch, kv head, slice); 0: swapped
   const int32_t* cu_q;  // variable-length batch: sequence offsets (VARLEN kernels)
   const int32_t* cu_k;
   int total_q, total_k;
@@ -360,11 +361,17 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
   __shared__ int abort_flag;
 
   const int warp = warp_id(), lane = lane_id();
-  const int dh = (int)blockIdx.x % T::DSPLIT;
-  const int bkh = (int)blockIdx.x / T::DSPLIT;  // b * Hk + kh
+  // Launch order, heaviest (causal) kv tile first either way. Fixed length: tile-major, so
+  // that every group's heaviest tile starts in the first wave and the light ones fill the
+  // tail. Variable-length batch: the kv tiles of one (sequence, kv head) next to each other,
+  // so that the Q / dO tiles they all walk stay in L2 (measured: 7.6 -> 5.0 ms on a mix of
+  // 16 sequences, where tile-major order read ~48 GB from HBM per launch).
+  const int gidx = p.tiles_fast ? (int)blockIdx.y : (int)blockIdx.x;
+  const int dh = gidx % T::DSPLIT;
+  const int bkh = gidx / T::DSPLIT;  // b * Hk + kh
   const int b = bkh / p.Hk, kh = bkh % p.Hk;
   const int G = p.H / p.Hk;
-  const int n0 = (int)blockIdx.y * kBN;
+  const int n0 = (int)(p.tiles_fast ? blockIdx.x : blockIdx.y) * kBN;
   // the rows of this problem: one (batch, kv head) of fixed length, or in a variable-length
   // batch sequence b's own rows of the packed heads (tensor-map z = head, rows offset)
   int ql = p.ql, kl = p.kl;
@@ -960,7 +967,9 @@ static cudaError_t launch_main_t(const BwdArgs& a, const BwdMaps& m, cudaStream_
   kp.ql_pad = a.ql_pad;
   kp.scale = a.scale;
   kp.scale_log2 = a.scale * kLog2eB;
-  dim3 grid(a.B * a.Hk * BwdTraits<HD>::DSPLIT, (a.kl + kBN - 1) / kBN);
+  const int groups = a.B * a.Hk * BwdTraits<HD>::DSPLIT, ktiles = (a.kl + kBN - 1) / kBN;
+  kp.tiles_fast = a.cu_q != nullptr && groups <= 65535;  // (grid y limit)
+  dim3 grid(kp.tiles_fast ? ktiles : groups, kp.tiles_fast ? groups : ktiles);
   profile_mark(kKernBwdMain, 0, s);
   kern<<<grid, LY::THREADS, LY::SMEM_BYTES, s>>>(m.q, m.k, m.v, m.dO, kp);
   cudaError_t e = cudaGetLastError();

@@ -85,6 +85,7 @@ struct DqKParams {
   const int32_t* cu_k;
   int total_q, total_k;
   int H, Hk, ql, kl, ql_pad;
+  int tiles_fast;  // 1: blockIdx.x = query tile, y = (batch, head); 0: swapped
   int lo_off, hi_off;
   float scale, scale_log2;
 };
@@ -116,10 +117,11 @@ __global__ void __launch_bounds__(DqLayout<HD, DV>::THREADS, 1)
   __shared__ int abort_flag;
 
   const int warp = warp_id(), lane = lane_id();
-  const int bh = blockIdx.x;
+  // variable-length batch: the tiles of one (sequence, head) together (they share K, V in L2)
+  const int bh = p.tiles_fast ? (int)blockIdx.y : (int)blockIdx.x;
   const int b = bh / p.H, h = bh % p.H;
   const int bkh = b * p.Hk + h / (p.H / p.Hk);
-  const int m0 = (int)blockIdx.y * kQM;
+  const int m0 = (int)(p.tiles_fast ? blockIdx.x : blockIdx.y) * kQM;
   // the rows of this problem: one (batch, head), or sequence b of a variable-length batch
   int ql = p.ql, kl = p.kl;
   int qz = bh, kz = bkh, qrow0 = 0, krow0 = 0;
@@ -389,7 +391,9 @@ static cudaError_t launch_dq_det_t(const BwdArgs& a, const DqMaps& m, cudaStream
   kp.hi_off = a.hi_off;
   kp.scale = a.scale;
   kp.scale_log2 = a.scale * kLog2eQ;
-  dim3 grid(a.B * a.H, (a.ql + kQM - 1) / kQM);
+  kp.tiles_fast = a.cu_q != nullptr && a.B * a.H <= 65535;
+  const int mt = (a.ql + kQM - 1) / kQM;
+  dim3 grid(kp.tiles_fast ? mt : a.B * a.H, kp.tiles_fast ? a.B * a.H : mt);
   kern<<<grid, LY::THREADS, LY::SMEM_BYTES, s>>>(m.q, m.k, m.v, m.dO, kp);
   return cudaGetLastError();
 }

@@ -92,6 +92,7 @@ struct FwdKParams {
   int total_q, total_k;
   int* status;
   int H, Hk, ql, kl, n_mblk;  // ql, kl: the longest sequence in a variable-length batch
+  int tiles_fast;  // 1: blockIdx.x = query tile, y = (batch, head); 0: the other way round
   int lo_off, hi_off;  // key j is visible to row i iff q_abs + lo_off <= j <= q_abs + hi_off
   float scale_log2;    // scale * log2(e)
 };
@@ -146,8 +147,12 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
 
   const int warp = warp_id();
   const int lane = lane_id();
-  const int bh = blockIdx.x;                     // b * H + h
-  const int mblk = p.n_mblk - 1 - (int)blockIdx.y;  // heaviest (causal) first
+  // Launch order, heaviest (causal) query tile first either way. Fixed length: tile-major, so
+  // that every head's heaviest tile starts in the first wave and the light ones fill the tail.
+  // Variable-length batch: the tiles of one (sequence, head) next to each other, so that they
+  // share its K and V through L2 (tile-major, concurrent CTAs of every sequence thrash L2).
+  const int bh = p.tiles_fast ? (int)blockIdx.y : (int)blockIdx.x;  // b * H + h
+  const int mblk = p.n_mblk - 1 - (int)(p.tiles_fast ? blockIdx.x : blockIdx.y);
   const int m0 = mblk * NQ * kBM;
   const int b = bh / p.H, h = bh % p.H;
   const int bkh = b * p.Hk + h / (p.H / p.Hk);
@@ -585,7 +590,8 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, const FwdMaps& m, cudaStream_t
   kp.hi_off = a.hi_off;
   kp.n_mblk = (a.ql + FwdTraits<HD>::NQ * kBM - 1) / (FwdTraits<HD>::NQ * kBM);
   kp.scale_log2 = a.scale * kLog2e;
-  dim3 grid(a.B * a.H, kp.n_mblk);
+  kp.tiles_fast = a.cu_q != nullptr && a.B * a.H <= 65535;  // (grid y limit)
+  dim3 grid(kp.tiles_fast ? kp.n_mblk : a.B * a.H, kp.tiles_fast ? a.B * a.H : kp.n_mblk);
   profile_mark(kKernFwd, 0, stream);
   kern<<<grid, LY::THREADS, LY::SMEM_BYTES, stream>>>(m.q, m.k, m.v, kp);
   cudaError_t e = cudaGetLastError();
