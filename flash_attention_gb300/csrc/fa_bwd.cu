@@ -20,9 +20,11 @@
 //                    to TMEM as bf16; dV += P^T dO and dK += dS^T Q with the A operand read
 //                    from TMEM; dQ^T = K^T dS^T (head_dim >= 128) or dQ = dS K (head_dim 64)
 //                    with dS^T staged in swizzled shared memory; a second warpgroup drains dQ
-//                    from TMEM into the f32 accumulator with global reductions, and writes
-//                    dK, dV at the end
-//   bwd_dq_kernel    dQ = bf16(scale * accumulator)
+//                    from TMEM into the f32 accumulator with global reductions (head_dim 128:
+//                    one bulk reduction per tile, the tile kept transposed), and writes dK, dV
+//                    at the end
+//   bwd_dq_kernel    dQ = bf16(scale * accumulator); bwd_dq_tiles_kernel does the same from
+//                    the transposed tiles of the bulk path
 #include <float.h>
 
 #include <mutex>
@@ -48,24 +50,37 @@ struct BwdTraits;
 // DQ_BULK: the dQ tile is staged in shared memory ([q][d] f32, contiguous in the accumulator)
 // and added to the accumulator by one bulk reduction; otherwise each thread adds its values
 // with global reductions.
+// SPLIT_MMA: in the deterministic mode (no dQ MMAs here) two warps issue the MMAs, one S^T and
+// dP^T, the other dV and dK, so that neither stream waits behind the other's barrier waits and
+// the issuing thread is less often starved of issue slots by the busy compute warps that share
+// its scheduler (measured on the d128 causal workload: 572 -> 484 us). With dQ MMAs the single
+// issuer's order measured faster (661 vs 671 us).
 template <>
 struct BwdTraits<64> {
   static constexpr int BM = 128, DSPLIT = 1, ST = 3, NSB = 1;
   static constexpr bool DQT = false, LOOKAHEAD = true, DQ_BULK = false;  // dQ = dS K (M = BM)
+  static constexpr bool SPLIT_MMA = false;
 };
 template <>
 struct BwdTraits<128> {
   static constexpr int BM = 64, DSPLIT = 1, ST = 3, NSB = 2;
   // dQ^T = K^T dS^T (M = head-dim slice)
   static constexpr bool DQT = true, LOOKAHEAD = true, DQ_BULK = true;
+  static constexpr bool SPLIT_MMA = true;
 };
 template <>
 struct BwdTraits<256> {
   static constexpr int BM = 64, DSPLIT = 2, ST = 1, NSB = 2;
   static constexpr bool DQT = true, LOOKAHEAD = false, DQ_BULK = false;
+  static constexpr bool SPLIT_MMA = false;
 };
 
 constexpr int kBN = 128;  // kv rows per CTA (the M of the kv-major MMAs)
+
+// Bulk dQ path: the accumulator tile of one (batch, head, query tile) is stored transposed, as
+// head-dim rows of BM f32, with the 16-byte chunk c (query rows 4c .. 4c+3) of row d at chunk
+// position c ^ (d % kDqChunks).
+constexpr int kDqChunks = 16;  // 16-byte chunks per transposed row (BM = 64 query rows)
 
 // HD: head dim of Q, K (and dQ, dK); DV: head dim of V, O, dO (and dV).
 template <int HD, int DV>
@@ -101,15 +116,18 @@ struct BwdLayout {
   static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
   static constexpr int DQ_COLS = T::DQT ? BM : HD;
   // WG0 (warps 0-3): P^T; WG1 (warps 4-7): dS^T and the dK/dV epilogue; WG2 (warps 8-11):
-  // the dQ drain; warp 12: TMA; warp 13: MMA; warp 14: issues the bulk dQ reductions.
+  // the dQ drain; warp 12: TMA; warp 13: MMA (with SPLIT_MMA: S^T and dP^T only); warp 14:
+  // issues the bulk dQ reductions; warp 15 (SPLIT_MMA): the dV, dK and dQ MMAs.
   static constexpr int THREADS = 512;
-  static constexpr int TMA_WARP = 12, MMA_WARP = 13, BULK_WARP = 14;
+  static constexpr int TMA_WARP = 12, MMA_WARP = 13, BULK_WARP = 14, MMA2_WARP = 15;
   static_assert(TMEM_USED <= 512, "TMEM budget");
   static_assert(DQ_COLS <= BM, "dQ tile must fit in a dP^T buffer");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(T::DQT ? DH == 128 : BM == 128, "every MMA has M = 128");
   static_assert(T::LOOKAHEAD ? T::ST >= (T::NSB == 2 ? 3 : 2) : true, "ring too shallow");
-  static_assert(!T::DQ_BULK || (T::DQT && T::DSPLIT == 1), "bulk dQ needs whole [q][d] rows");
+  static_assert(!T::SPLIT_MMA || (T::NSB == 2 && T::LOOKAHEAD), "split issue order");
+  static_assert(!T::DQ_BULK || (T::DQT && T::DSPLIT == 1), "bulk dQ needs whole head-dim rows");
+  static_assert(!T::DQ_BULK || BM / 4 == kDqChunks, "transposed dQ tile layout");
   static_assert(T::DSPLIT == 1 || DV == HD, "a split head dim needs DV == HD");
   static_assert(DVH % 16 == 0 && DVH >= 16 && DVH <= 256, "dV MMA N");
 };
@@ -178,16 +196,26 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
       varlen_seq(cu_q, bh / H, total_q, ql, qs, qlen);
       rowbase = (size_t)(bh % H) * total_q + qs;
     }
+    if (zero_acc) {  // (the deterministic mode has no accumulator) stores first: they overlap
+                     // the loads below
+      float4* z = reinterpret_cast<float4*>(dqacc + ((size_t)bh * ql_pad + i0) * HD);
+#pragma unroll
+      for (int c = threadIdx.x; c < RPB * ROWS * HD / 4; c += 256)
+        z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     uint4 a[ROWS], g[ROWS];
+    float Lr[ROWS];  // L of the rows this thread reduces (read by the first thread of a row)
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {
       const int i = i0 + r * RPB + threadIdx.x / TPR;
       a[r] = make_uint4(0, 0, 0, 0);
       g[r] = make_uint4(0, 0, 0, 0);
+      Lr[r] = -INFINITY;
       if (i < qlen) {
         const size_t base = (rowbase + i) * DV + sub * 8;
         a[r] = *reinterpret_cast<const uint4*>(o + base);
         g[r] = *reinterpret_cast<const uint4*>(dO + base);
+        if (sub == 0) Lr[r] = lse[rowbase + i];
       }
     }
 #pragma unroll
@@ -205,7 +233,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
         float nl2 = -INFINITY;  // padding rows and fully masked rows: P = exp2(s - inf) = 0
         float term = 0.0f;      // this row's share of dsinks[h]
         if (i < qlen) {
-          const float L = lse[rowbase + i];
+          const float L = Lr[r];
           if (L != -INFINITY) {
             nl2 = -L * kLog2eB;
             if (want_dsink) term = -expf(__ldg(sinks + bh % H) - L) * acc;
@@ -215,12 +243,6 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
         dvec[(size_t)bh * ql_pad + i] = i < qlen ? acc : 0.0f;
         if (want_dsink) sink_terms[r * RPB + threadIdx.x / TPR] = term;
       }
-    }
-    if (zero_acc) {  // (the deterministic mode has no accumulator)
-      float4* z = reinterpret_cast<float4*>(dqacc + ((size_t)bh * ql_pad + i0) * HD);
-#pragma unroll 4
-      for (int c = threadIdx.x; c < RPB * ROWS * HD / 4; c += 256)
-        z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if (want_dsink) {  // block-uniform
       __syncthreads();
@@ -243,6 +265,29 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
 // Blocks with x == 0 also finish dsinks[h] for h = y, y + gridDim.y, ...: the sum, in a fixed
 // order, of the prep kernel's partials of every batch entry of head h. With convert = 0 (the
 // deterministic mode, where dQ is written by its own kernel) only that sum is done.
+// dsinks[h] for h = blockIdx.y, blockIdx.y + gridDim.y, ...: the prep kernel's partials of every
+// batch entry of head h, summed in a fixed order (256 threads).
+__device__ __forceinline__ void dsinks_sum(const float* __restrict__ dsink_part,
+                                           float* __restrict__ dsinks, int B, int H,
+                                           int sink_chunks) {
+  __shared__ float red[256];
+  const int n = B * sink_chunks;
+  for (int h = blockIdx.y; h < H; h += gridDim.y) {
+    float s = 0.0f;
+    for (int k = threadIdx.x; k < n; k += 256)
+      s += dsink_part[((size_t)(k / sink_chunks) * H + h) * sink_chunks + k % sink_chunks];
+    red[threadIdx.x] = s;
+    __syncthreads();
+#pragma unroll
+    for (int w = 128; w > 0; w >>= 1) {
+      if ((int)threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) dsinks[h] = red[0];
+    __syncthreads();  // red is reused by the next head
+  }
+}
+
 template <int HD>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ dqacc,
                                                      __nv_bfloat16* __restrict__ dq, int BH,
@@ -252,24 +297,7 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
                                                      int sink_chunks, int convert,
                                                      const int32_t* __restrict__ cu_q,
                                                      int total_q) {
-  if (dsinks != nullptr && blockIdx.x == 0) {  // block-uniform
-    __shared__ float red[256];
-    const int n = B * sink_chunks;
-    for (int h = blockIdx.y; h < H; h += gridDim.y) {
-      float s = 0.0f;
-      for (int k = threadIdx.x; k < n; k += 256)
-        s += dsink_part[((size_t)(k / sink_chunks) * H + h) * sink_chunks + k % sink_chunks];
-      red[threadIdx.x] = s;
-      __syncthreads();
-#pragma unroll
-      for (int w = 128; w > 0; w >>= 1) {
-        if ((int)threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
-        __syncthreads();
-      }
-      if (threadIdx.x == 0) dsinks[h] = red[0];
-      __syncthreads();  // red is reused by the next head
-    }
-  }
+  if (dsinks != nullptr && blockIdx.x == 0) dsinks_sum(dsink_part, dsinks, B, H, sink_chunks);
   if (!convert) return;
   const int e = blockIdx.x * 256 + threadIdx.x;  // index of the 8-value group within a head
   const int i = e / (HD / 8), c = (e % (HD / 8)) * 8;
@@ -290,6 +318,69 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
     out.z = pack_bf16(v1.x * scale, v1.y * scale);
     out.w = pack_bf16(v1.z * scale, v1.w * scale);
     *reinterpret_cast<uint4*>(dq + (rowbase + i) * HD + c) = out;
+  }
+}
+
+// dQ = bf16(scale * accumulator) from the transposed accumulator tiles of the bulk path.
+// Grid: x = (query tile of BM rows, half of the head dimension), y = (batch, head) (strided);
+// blocks with x == 0 also finish dsinks. A block reads its half tile (HD/2 rows of BM f32,
+// chunk-rotated) with all of its 16-byte loads in flight and transposes it through shared
+// memory into [q][d] (rows padded to HD/2 + 1 floats); then four consecutive threads write one
+// query row's 128 contiguous bytes of bf16.
+template <int HD, int BM>
+__global__ void __launch_bounds__(256) bwd_dq_tiles_kernel(const float* __restrict__ dqacc,
+                                                           __nv_bfloat16* __restrict__ dq,
+                                                           int BH, int ql, int ql_pad,
+                                                           float scale,
+                                                           const float* __restrict__ dsink_part,
+                                                           float* __restrict__ dsinks, int B,
+                                                           int H, int sink_chunks,
+                                                           const int32_t* __restrict__ cu_q,
+                                                           int total_q) {
+  constexpr int DR = HD / 2;                    // head-dim rows per block
+  constexpr int NV = DR * kDqChunks / 256;      // 16-byte loads per thread
+  static_assert(BM / 4 == kDqChunks && DR % kDqChunks == 0 && NV * 256 == DR * kDqChunks &&
+                    BM * (DR / 16) == 256,
+                "tile layout");
+  if (dsinks != nullptr && blockIdx.x == 0) dsinks_sum(dsink_part, dsinks, B, H, sink_chunks);
+  __shared__ float tile[BM][DR + 1];
+  const int q0 = (blockIdx.x / 2) * BM, d0 = (blockIdx.x % 2) * DR;
+  for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
+    size_t rowbase = (size_t)bh * ql;
+    int qlen = ql;
+    if (cu_q != nullptr) {  // sequence b of a variable-length batch
+      int qs;
+      varlen_seq(cu_q, bh / H, total_q, ql, qs, qlen);
+      rowbase = (size_t)(bh % H) * total_q + qs;
+    }
+    if (q0 >= qlen) continue;  // (block-uniform)
+    const float4* src =
+        reinterpret_cast<const float4*>(dqacc + ((size_t)bh * ql_pad + q0) * HD) + d0 * kDqChunks;
+    float4 v[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) v[k] = src[threadIdx.x + 256 * k];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int f = threadIdx.x + 256 * k;
+      const int d = f / kDqChunks;  // row within the half (d0 is a multiple of kDqChunks)
+      const int q = 4 * ((f % kDqChunks) ^ (d % kDqChunks));
+      tile[q][d] = v[k].x;
+      tile[q + 1][d] = v[k].y;
+      tile[q + 2][d] = v[k].z;
+      tile[q + 3][d] = v[k].w;
+    }
+    __syncthreads();
+    const int q = threadIdx.x / (DR / 16), c = (threadIdx.x % (DR / 16)) * 16;
+    if (q0 + q < qlen) {
+      uint32_t w[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        w[e] = pack_bf16(tile[q][c + 2 * e] * scale, tile[q][c + 2 * e + 1] * scale);
+      uint4* dst = reinterpret_cast<uint4*>(dq + (rowbase + q0 + q) * HD + d0 + c);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+    __syncthreads();  // the tile is rewritten for the next head
   }
 }
 
@@ -355,7 +446,8 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
   __shared__ uint64_t kv_full, qdo_full[ST], qdo_empty[ST];
   __shared__ uint64_t s_full[NSB], p_ready[NSB], p_consumed[NSB];
   __shared__ uint64_t dp_full[2], ds_ready[2], dq_full[2], dq_free[2];
-  __shared__ uint64_t acc_full, mma_drain;
+  __shared__ uint64_t acc_full, mma_drain, mma_drain2;
+  __shared__ uint64_t dv_done[NSB];  // SPLIT_MMA: dV(it) has read P^T(it) from its S^T buffer
   __shared__ uint64_t stg_full, stg_free;  // dQ staging handshake of the bulk drain
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
@@ -394,6 +486,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
   bwd_mtile_range<HD, BAND>(n0, p, ql, kl, m_first, m_last);
   const int nm = m_last - m_first + 1;  // query tiles per head (0 if none)
   const int n_iter = G * nm;          // (head, query tile) pairs this CTA visits
+  const bool split_mma = T::SPLIT_MMA && p.skip_dq;  // two MMA issuers (see BwdTraits)
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -415,6 +508,8 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
     }
     mbar_init(&acc_full, 1);
     mbar_init(&mma_drain, 1);
+    mbar_init(&mma_drain2, 1);
+    for (int s = 0; s < NSB; ++s) mbar_init(&dv_done[s], 1);
     mbar_init(&stg_full, 128);
     mbar_init(&stg_free, 1);
     fence_barrier_init();
@@ -466,8 +561,114 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
       for (int s = 0; s < ST; ++s)
         if (last_use[s] >= 0) mbar_wait_drain(&qdo_full[s], (last_use[s] / ST) & 1);
     }
+  } else if (split_mma && (warp == LY::MMA_WARP || warp == LY::MMA2_WARP)) {
+    // ------------------------------------------------------------------ MMA issuers (split)
+    // Warp 13 issues S^T(it) and dP^T(it); warp 15 issues dV(it), dK(it) and dQ(it). Each
+    // stream keeps the order the single issuer had, and the one hazard between them that the
+    // issue order used to cover (S^T(it) overwriting the score buffer that dV(it - NSB) reads
+    // P^T from) is covered by the dv_done barrier.
+    if constexpr (T::SPLIT_MMA) {
+      if (elect_one()) {
+        const uint32_t sK = smem_u32(smem + LY::OFF_K), sV = smem_u32(smem + LY::OFF_V);
+        const Desc kd = make_desc(sK, 16, 1024);          // K as a K-major operand
+        const Desc vd = make_desc(sV, 16, 1024);          // V as a K-major operand
+        const Desc kmn = make_desc(sK, kBN * 128, 1024);  // K as an MN-major operand
+        const uint32_t id_s = idesc_bf16(128, BM, 0, 0);      // S^T, dP^T: [kv x q]
+        const uint32_t id_dv = idesc_bf16(128, DVH, 0, 1);    // dV: A tmem, B MN-major
+        const uint32_t id_dk = idesc_bf16(128, DH, 0, 1);     // dK: A tmem, B MN-major
+        const uint32_t id_dq = idesc_bf16(DH, BM, 1, 1);      // dQ^T: [d x q]
+        const uint32_t tDV = tbase + LY::COL_DV, tDK = tbase + LY::COL_DK;
+        const uint32_t slice = (dh * DH / 64) * (BM * 128);
+        const uint32_t vslice = (dh * DVH / 64) * (BM * 128);
+        bool ok = mbar_wait(&kv_full, 0, &abort_flag);
+        if (warp == LY::MMA_WARP) {
+          for (int it = 0; it < n_iter && ok; ++it) {
+            const int st = it % ST;
+            ok = mbar_wait(&qdo_full[st], (it / ST) & 1, &abort_flag);
+            // S^T(it) = K Q^T, into the score buffer of it - NSB once WG1 and dV(it - NSB) have
+            // read P^T(it - NSB) from it
+            if (ok && it >= NSB) {
+              ok = mbar_wait(&p_consumed[it % NSB], ((it - NSB) / NSB) & 1, &abort_flag);
+              if (ok) ok = mbar_wait(&dv_done[it % NSB], ((it - NSB) / NSB) & 1, &abort_flag);
+            }
+            if (!ok) break;
+            tc_fence_after();
+            const Desc qd = make_desc(smem_u32(smem + LY::OFF_Q + st * LY::QT_BYTES), 16, 1024);
+            const uint32_t tS = tbase + LY::COL_S0 + (it % NSB) * BM;
+#pragma unroll
+            for (int ks = 0; ks < HD / 16; ++ks) {
+              const uint32_t ko = (ks / 4) * (kBN * 128) + (ks % 4) * 32;
+              const uint32_t qo = (ks / 4) * (BM * 128) + (ks % 4) * 32;
+              mma_ss2(tS, kd.at(ko), kd.hi, qd.at(qo), qd.hi, id_s, ks > 0 ? 1u : 0u);
+            }
+            mma_commit(&s_full[it % NSB]);
+            // dP^T(it) = V dO^T, into the buffer that dQ(it - 2) used, once WG2 has drained it
+            if (it >= 2) {
+              ok = mbar_wait(&dq_free[it % 2], ((it - 2) / 2) & 1, &abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            const Desc dod = make_desc(smem_u32(smem + LY::OFF_DO + st * LY::DOT_BYTES), 16, 1024);
+            const uint32_t tDP = tbase + LY::COL_DP0 + (it % 2) * BM;
+#pragma unroll
+            for (int ks = 0; ks < DV / 16; ++ks) {
+              const uint32_t ko = (ks / 4) * (kBN * 128) + (ks % 4) * 32;
+              const uint32_t qo = (ks / 4) * (BM * 128) + (ks % 4) * 32;
+              mma_ss2(tDP, vd.at(ko), vd.hi, dod.at(qo), dod.hi, id_s, ks > 0 ? 1u : 0u);
+            }
+            mma_commit(&dp_full[it % 2]);
+          }
+          mma_commit(&mma_drain2);
+          mbar_wait_drain(&mma_drain2, 0);
+        } else {
+          for (int it = 0; it < n_iter && ok; ++it) {
+            const int st = it % ST;
+            // (the stage barrier is observed for the tensor core's reads of Q and dO; its next
+            // phase needs dK(it) below, so it cannot have moved on)
+            ok = mbar_wait(&qdo_full[st], (it / ST) & 1, &abort_flag);
+            if (ok) ok = mbar_wait(&p_ready[it % NSB], (it / NSB) & 1, &abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            const Desc qmn = make_desc(smem_u32(smem + LY::OFF_Q + st * LY::QT_BYTES), BM * 128, 1024);
+            const Desc domn = make_desc(smem_u32(smem + LY::OFF_DO + st * LY::DOT_BYTES), BM * 128, 1024);
+            const uint32_t tS = tbase + LY::COL_S0 + (it % NSB) * BM;
+            const uint32_t tDP = tbase + LY::COL_DP0 + (it % 2) * BM;
+            const Desc dsd = make_desc(smem_u32(smem + LY::OFF_DS + (it % 2) * LY::DS_BYTES), kBN * 128, 1024);
+            // dV += P^T dO
+#pragma unroll
+            for (int ks = 0; ks < BM / 16; ++ks)
+              mma_ts2(tDV, tS + ks * 8, domn.at(vslice + ks * 2048), domn.hi, id_dv,
+                      (it > 0 || ks > 0) ? 1u : 0u);
+            mma_commit(&dv_done[it % NSB]);
+            // dK += dS^T Q
+            ok = mbar_wait(&ds_ready[it % 2], (it / 2) & 1, &abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < BM / 16; ++ks)
+              mma_ts2(tDK, tDP + ks * 8, qmn.at(slice + ks * 2048), qmn.hi, id_dk,
+                      (it > 0 || ks > 0) ? 1u : 0u);
+            mma_commit(&qdo_empty[st]);
+            // dQ^T[d, q] = sum_kv K[kv, d] dS^T[kv, q], into the dP^T buffer (its dS^T has just
+            // been read by dK); with skip_dq the commit still hands the buffers on
+            if (!p.skip_dq) {
+              const uint32_t kslice = (dh * DH / 64) * (kBN * 128);
+#pragma unroll
+              for (int ks = 0; ks < kBN / 16; ++ks)
+                mma_ss2(tDP, kmn.at(kslice + ks * 2048), kmn.hi, dsd.at(ks * 2048), dsd.hi, id_dq,
+                        ks > 0 ? 1u : 0u);
+            }
+            mma_commit(&dq_full[it % 2]);
+          }
+          mma_commit(&acc_full);
+          mma_commit(&mma_drain);
+          mbar_wait_drain(&mma_drain, 0);
+        }
+      }
+    }
   } else if (warp == LY::MMA_WARP) {
     // ------------------------------------------------------------------ MMA issuer
+    {
     if (elect_one()) {
       const uint32_t sK = smem_u32(smem + LY::OFF_K), sV = smem_u32(smem + LY::OFF_V);
       const Desc kd = make_desc(sK, 16, 1024);          // K as a K-major operand
@@ -595,6 +796,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
       mma_commit(&acc_full);
       mma_commit(&mma_drain);
       mbar_wait_drain(&mma_drain, 0);
+    }
     }
   } else if (warp == LY::BULK_WARP) {
     // ------------------------------------------------------------------ bulk dQ reductions
@@ -729,9 +931,12 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
         return;
       }
       if constexpr (T::DQ_BULK) {
-        // lane = head-dim index, column = query row: stage as [q][d] f32 (contiguous in the
-        // accumulator); the bulk warp adds the tile with one reduction. The staging buffer is
-        // handed over with mbarriers: stg_full once written, stg_free once read.
+        // lane = head-dim index d, column = query row: stage the tile transposed, as HD rows of
+        // BM f32 (the accumulator keeps this tile layout; the dQ convert kernel turns it back),
+        // with the 16-byte chunks of row d XOR-rotated by (d & 15) so that the 16-byte stores of
+        // any 8 consecutive lanes hit 8 distinct bank groups. The bulk warp adds the tile with
+        // one reduction; the buffer is handed over with mbarriers (stg_full once written,
+        // stg_free once read).
         float* stg = reinterpret_cast<float*>(smem + LY::OFF_STG);
         uint32_t rq[BM / 32][32];
 #pragma unroll
@@ -743,10 +948,13 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
           ok = __all_sync(0xffffffffu, mbar_wait(&stg_free, (it - 1) & 1, &abort_flag));
           if (!ok) return;
         }
+        float4* row = reinterpret_cast<float4*>(stg + j * BM);
 #pragma unroll
-        for (int c32 = 0; c32 < BM / 32; ++c32)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) stg[(c32 * 32 + e) * HD + j] = __uint_as_float(rq[c32][e]);
+        for (int c = 0; c < BM / 4; ++c) {  // chunk c: query rows 4c .. 4c+3
+          const uint32_t* r = &rq[c / 8][(c % 8) * 4];
+          row[c ^ (j & (kDqChunks - 1))] = make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]),
+                                                       __uint_as_float(r[2]), __uint_as_float(r[3]));
+        }
         fence_proxy_async();  // staging writes -> visible to the bulk copy
         mbar_arrive(&stg_full);
       } else if constexpr (T::DQT) {
@@ -1021,7 +1229,15 @@ static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t
     }
     return cudaGetLastError();
   }
-  {
+  if constexpr (BwdTraits<HD>::DQ_BULK) {  // transposed accumulator tiles
+    constexpr int BM = BwdTraits<HD>::BM;
+    dim3 grid((unsigned)((a.ql + BM - 1) / BM * 2), BH < 65535 ? BH : 65535);
+    profile_mark(kKernBwdDq, 0, s);
+    bwd_dq_tiles_kernel<HD, BM><<<grid, 256, 0, s>>>(
+        a.dqacc, reinterpret_cast<__nv_bfloat16*>(a.dq), BH, a.ql, a.ql_pad, a.scale, dsink_part,
+        a.dsinks, a.B, a.H, sink_chunks, a.cu_q, a.total_q);
+    profile_mark(kKernBwdDq, 1, s);
+  } else {
     const long long groups = (long long)a.ql * (HD / 8);  // 8-value groups per head
     dim3 grid((unsigned)((groups + 255) / 256), BH < 65535 ? BH : 65535);
     profile_mark(kKernBwdDq, 0, s);
