@@ -42,18 +42,26 @@ struct FwdTraits;
 // NQ query tiles per CTA, BN keys per kv tile, NS score buffers per query tile, STAGES-deep
 // K/V ring. POLY: one pair of exponentials in every POLY goes to the FMA-pipe polynomial
 // (0 = all on MUFU); the MUFU unit (16 exp2 per clock per SM) would otherwise be as slow as
-// the tensor core at head_dim 128 and the bottleneck at 64.
+// the tensor core at head_dim 128 and the bottleneck at 64. SPLIT: S = Q K^T and O += P V are
+// issued by two warps (a busy scheduler starves a lone issuing thread less often when the
+// two streams do not wait behind each other's barriers). S into a score buffer then waits for
+// the completion of the P V that read it, not just for its issue: with one score buffer per
+// tile (NS = 1) that wait is on the critical path (measured at head_dim 128: 230 -> 272 us on
+// the 4k causal GQA shape), with two it is hidden (head_dim 256: 125 -> 121 us).
 template <>
 struct FwdTraits<64> {
   static constexpr int NQ = 2, BN = 128, NS = 1, STAGES = 3, POLY = 4;
+  static constexpr bool SPLIT = false;
 };
 template <>
 struct FwdTraits<128> {
   static constexpr int NQ = 2, BN = 128, NS = 1, STAGES = 2, POLY = 8;
+  static constexpr bool SPLIT = false;
 };
 template <>
 struct FwdTraits<256> {
   static constexpr int NQ = 1, BN = 64, NS = 2, STAGES = 2, POLY = 0;
+  static constexpr bool SPLIT = true;
 };
 
 // HD: head dim of Q and K; DV: head dim of V and O (the value head dim).
@@ -74,9 +82,11 @@ struct FwdLayout {
   static constexpr int TILE_COLS = DV + T::NS * T::BN;
   static constexpr int TMEM_COLS_USED = T::NQ * TILE_COLS;
   static constexpr int TMEM_COLS = TMEM_COLS_USED <= 256 ? 256 : 512;
-  static constexpr int THREADS = T::NQ * 128 + 64;  // softmax warpgroups + TMA + MMA warps
+  // softmax warpgroups + TMA + MMA warps (with SPLIT: MMA_WARP issues S, MMA2_WARP P V)
+  static constexpr int THREADS = T::NQ * 128 + (T::SPLIT ? 96 : 64);
   static constexpr int TMA_WARP = T::NQ * 4;
   static constexpr int MMA_WARP = T::NQ * 4 + 1;
+  static constexpr int MMA2_WARP = T::NQ * 4 + 2;
   static_assert(TMEM_COLS_USED <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
@@ -141,7 +151,8 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
   __shared__ uint64_t q_full;
   __shared__ uint64_t k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
   __shared__ uint64_t s_full[NQ][NS], p_full[NQ][NS], o_done[NQ], o_final[NQ];
-  __shared__ uint64_t mma_drain;
+  __shared__ uint64_t pv_done[NQ][NS];  // SPLIT: P V of a score buffer has read its P
+  __shared__ uint64_t mma_drain, mma_drain2;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
 
@@ -213,11 +224,13 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
       for (int s = 0; s < NS; ++s) {
         mbar_init(&s_full[t][s], 1);
         mbar_init(&p_full[t][s], 128);
+        mbar_init(&pv_done[t][s], 1);
       }
       mbar_init(&o_done[t], 1);
       mbar_init(&o_final[t], 1);
     }
     mbar_init(&mma_drain, 1);
+    mbar_init(&mma_drain2, 1);
     fence_barrier_init();
   }
   if (warp == LY::MMA_WARP) {
@@ -266,8 +279,8 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
         if (last_v[s] >= 0) mbar_wait_drain(&v_full[s], (last_v[s] / STAGES) & 1);
       }
     }
-  } else if (warp == LY::MMA_WARP) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == LY::MMA_WARP || (T::SPLIT && warp == LY::MMA2_WARP)) {
+    // ------------------------------------------------------------------ MMA issuer(s)
     if (elect_one()) {
       const uint32_t idesc_s = idesc_bf16(kBM, BN, 0, 0);
       const uint32_t idesc_o = idesc_bf16(kBM, DV, 0, 1);
@@ -313,6 +326,61 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
         if (WIN ? --kleft[st] == 0 : t == NQ - 1) mma_commit(&k_empty[st]);
       };
 
+      if constexpr (T::SPLIT) {
+        if (warp == LY::MMA_WARP) {
+          // S of every (kv tile, query tile) in kv order; S(t, j) reuses the score buffer of
+          // iteration j - NS of tile t once P V there has read P
+          for (int j = J0; j < J1 && ok; ++j) {
+#pragma unroll
+            for (int t = 0; t < NQ; ++t) {
+              if (!ok) break;
+              if (j < jt0[t] || j >= jt1[t]) continue;
+              const int jj = j - jt0[t];
+              if (jj >= NS) {
+                ok = mbar_wait(&pv_done[t][jj % NS], ((jj - NS) / NS) & 1, &abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+              }
+              issue_s(t, j);
+            }
+          }
+          mma_commit(&mma_drain2);
+          mbar_wait_drain(&mma_drain2, 0);
+        } else {
+          for (int j = J0; j < J1 && ok; ++j) {
+            const int st = (j - J0) % STAGES;
+#pragma unroll
+            for (int t = 0; t < NQ; ++t) {
+              if (!ok) break;
+              if (j < jt0[t] || j >= jt1[t]) continue;
+              const int jj = j - jt0[t];
+              const int sb = jj % NS;
+              ok = mbar_wait(&p_full[t][sb], (jj / NS) & 1, &abort_flag);
+              if (!ok) break;
+              if (j > v_ready) {
+                ok = mbar_wait(&v_full[st], ((j - J0) / STAGES) & 1, &abort_flag);
+                if (!ok) break;
+                if (WIN) vleft[st] = users(j);
+                v_ready = j;
+              }
+              tc_fence_after();
+              const uint32_t o_tmem = tbase + t * LY::TILE_COLS;
+              const uint32_t p_tmem = o_tmem + DV + sb * BN;
+              const Desc vb = make_desc(sv + st * LY::V_TILE_BYTES, BN * 128, 1024);
+#pragma unroll
+              for (int ks = 0; ks < BN / 16; ++ks)
+                mma_ts2(o_tmem, p_tmem + ks * 8, vb.at(ks * 2048), vb.hi, idesc_o,
+                        (jj > 0 || ks > 0) ? 1u : 0u);
+              mma_commit(&o_done[t]);
+              mma_commit(&pv_done[t][sb]);
+              if (j == jt1[t] - 1) mma_commit(&o_final[t]);  // every PV of tile t issued
+              if (WIN ? --vleft[st] == 0 : t == NQ - 1) mma_commit(&v_empty[st]);
+            }
+          }
+          mma_commit(&mma_drain);
+          mbar_wait_drain(&mma_drain, 0);
+        }
+      } else {
       // prologue: the first NS score tiles of every query tile
       for (int s0 = 0; s0 < NS && ok; ++s0)
 #pragma unroll
@@ -352,6 +420,7 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
       // all MMAs complete before TMEM can be released
       mma_commit(&mma_drain);
       mbar_wait_drain(&mma_drain, 0);
+      }
     }
   } else if (warp < 4 * NQ) {
     // ------------------------------------------------------------------ softmax warpgroups
