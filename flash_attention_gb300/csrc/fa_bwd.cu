@@ -47,7 +47,7 @@ constexpr float kLog2eB = 1.4426950408889634f;
 // forms dV, dK and dQ.
 template <int HD>
 struct BwdTraits;
-// DQ_BULK: the dQ tile is staged in shared memory ([q][d] f32, contiguous in the accumulator)
+// DQ_BULK: the dQ tile is staged in shared memory (f32, in the accumulator's tile layout below)
 // and added to the accumulator by one bulk reduction; otherwise each thread adds its values
 // with global reductions.
 // SPLIT_MMA: in the deterministic mode (no dQ MMAs here) two warps issue the MMAs, one S^T and
@@ -57,8 +57,9 @@ struct BwdTraits;
 // issuer's order measured faster (661 vs 671 us).
 template <>
 struct BwdTraits<64> {
-  static constexpr int BM = 128, DSPLIT = 1, ST = 3, NSB = 1;
-  static constexpr bool DQT = false, LOOKAHEAD = true, DQ_BULK = false;  // dQ = dS K (M = BM)
+  // (a 2-deep Q/dO ring leaves room for the bulk dQ staging tile)
+  static constexpr int BM = 128, DSPLIT = 1, ST = 2, NSB = 1;
+  static constexpr bool DQT = false, LOOKAHEAD = true, DQ_BULK = true;  // dQ = dS K (M = BM)
   static constexpr bool SPLIT_MMA = false;
 };
 template <>
@@ -77,10 +78,12 @@ struct BwdTraits<256> {
 
 constexpr int kBN = 128;  // kv rows per CTA (the M of the kv-major MMAs)
 
-// Bulk dQ path: the accumulator tile of one (batch, head, query tile) is stored transposed, as
-// head-dim rows of BM f32, with the 16-byte chunk c (query rows 4c .. 4c+3) of row d at chunk
-// position c ^ (d % kDqChunks).
-constexpr int kDqChunks = 16;  // 16-byte chunks per transposed row (BM = 64 query rows)
+// Bulk dQ path: with dQ^T formed (head_dim 128) the accumulator tile of one (batch, head,
+// query tile) is stored transposed, as head-dim rows of BM f32, with the 16-byte chunk c (query
+// rows 4c .. 4c+3) of row d at chunk position c ^ (d % kDqChunks); with dQ formed (head_dim 64)
+// it keeps query rows of HD f32, the chunk c (head-dim 4c .. 4c+3) of row q at c ^ (q %
+// kDqChunks). Either way 8 consecutive staging lanes store to 8 distinct bank groups.
+constexpr int kDqChunks = 16;  // 16-byte chunks per staged row (64 f32)
 
 // HD: head dim of Q, K (and dQ, dK); DV: head dim of V, O, dO (and dV).
 template <int HD, int DV>
@@ -126,8 +129,8 @@ struct BwdLayout {
   static_assert(T::DQT ? DH == 128 : BM == 128, "every MMA has M = 128");
   static_assert(T::LOOKAHEAD ? T::ST >= (T::NSB == 2 ? 3 : 2) : true, "ring too shallow");
   static_assert(!T::SPLIT_MMA || (T::NSB == 2 && T::LOOKAHEAD), "split issue order");
-  static_assert(!T::DQ_BULK || (T::DQT && T::DSPLIT == 1), "bulk dQ needs whole head-dim rows");
-  static_assert(!T::DQ_BULK || BM / 4 == kDqChunks, "transposed dQ tile layout");
+  static_assert(!T::DQ_BULK || T::DSPLIT == 1, "bulk dQ needs whole head-dim rows");
+  static_assert(!T::DQ_BULK || (T::DQT ? BM : HD) / 4 == kDqChunks, "staged dQ tile layout");
   static_assert(T::DSPLIT == 1 || DV == HD, "a split head dim needs DV == HD");
   static_assert(DVH % 16 == 0 && DVH >= 16 && DVH <= 256, "dV MMA N");
 };
@@ -288,7 +291,9 @@ __device__ __forceinline__ void dsinks_sum(const float* __restrict__ dsink_part,
   }
 }
 
-template <int HD>
+// SWZ: rows of the accumulator hold their 16-byte chunks XOR-rotated by (row % kDqChunks)
+// (the bulk path at head_dim 64).
+template <int HD, bool SWZ>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ dqacc,
                                                      __nv_bfloat16* __restrict__ dq, int BH,
                                                      int ql, int ql_pad, float scale,
@@ -310,8 +315,9 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
       if (i >= qlen) continue;
       rowbase = (size_t)(bh % H) * total_q + qs;
     }
-    const float4* src = reinterpret_cast<const float4*>(dqacc + ((size_t)bh * ql_pad + i) * HD + c);
-    const float4 v0 = src[0], v1 = src[1];
+    const float4* srow = reinterpret_cast<const float4*>(dqacc + ((size_t)bh * ql_pad + i) * HD);
+    const int c4 = c / 4, rot = SWZ ? (i % kDqChunks) : 0;  // (query tiles start at multiples of 16)
+    const float4 v0 = srow[c4 ^ rot], v1 = srow[(c4 + 1) ^ rot];
     uint4 out;
     out.x = pack_bf16(v0.x * scale, v0.y * scale);
     out.y = pack_bf16(v0.z * scale, v0.w * scale);
@@ -930,7 +936,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
         mbar_arrive(&dq_free[it % 2]);
         return;
       }
-      if constexpr (T::DQ_BULK) {
+      if constexpr (T::DQ_BULK && T::DQT) {
         // lane = head-dim index d, column = query row: stage the tile transposed, as HD rows of
         // BM f32 (the accumulator keeps this tile layout; the dQ convert kernel turns it back),
         // with the 16-byte chunks of row d XOR-rotated by (d & 15) so that the 16-byte stores of
@@ -951,6 +957,29 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
         float4* row = reinterpret_cast<float4*>(stg + j * BM);
 #pragma unroll
         for (int c = 0; c < BM / 4; ++c) {  // chunk c: query rows 4c .. 4c+3
+          const uint32_t* r = &rq[c / 8][(c % 8) * 4];
+          row[c ^ (j & (kDqChunks - 1))] = make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]),
+                                                       __uint_as_float(r[2]), __uint_as_float(r[3]));
+        }
+        fence_proxy_async();  // staging writes -> visible to the bulk copy
+        mbar_arrive(&stg_full);
+      } else if constexpr (T::DQ_BULK) {
+        // lane = query row j, column = head-dim index: stage the row (HD f32) with its 16-byte
+        // chunks XOR-rotated by (j & 15); the bulk warp adds the tile with one reduction
+        float* stg = reinterpret_cast<float*>(smem + LY::OFF_STG);
+        uint32_t rq[HD / 32][32];
+#pragma unroll
+        for (int c32 = 0; c32 < HD / 32; ++c32) tmem_ld32(lane_base + colDQ + c32 * 32, rq[c32]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&dq_free[it % 2]);
+        if (it > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&stg_free, (it - 1) & 1, &abort_flag));
+          if (!ok) return;
+        }
+        float4* row = reinterpret_cast<float4*>(stg + j * HD);
+#pragma unroll
+        for (int c = 0; c < HD / 4; ++c) {  // chunk c: head-dim 4c .. 4c+3
           const uint32_t* r = &rq[c / 8][(c % 8) * 4];
           row[c ^ (j & (kDqChunks - 1))] = make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]),
                                                        __uint_as_float(r[2]), __uint_as_float(r[3]));
@@ -1222,14 +1251,14 @@ static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t
     if (e != cudaSuccess) return e;
     if (a.dsinks != nullptr) {  // the dsinks sum alone
       profile_mark(kKernBwdDq, 0, s);
-      bwd_dq_kernel<HD><<<dim3(1, a.H < 65535 ? a.H : 65535), 256, 0, s>>>(
+      bwd_dq_kernel<HD, false><<<dim3(1, a.H < 65535 ? a.H : 65535), 256, 0, s>>>(
           a.dqacc, reinterpret_cast<__nv_bfloat16*>(a.dq), BH, a.ql, a.ql_pad, a.scale,
           dsink_part, a.dsinks, a.B, a.H, sink_chunks, 0, a.cu_q, a.total_q);
       profile_mark(kKernBwdDq, 1, s);
     }
     return cudaGetLastError();
   }
-  if constexpr (BwdTraits<HD>::DQ_BULK) {  // transposed accumulator tiles
+  if constexpr (BwdTraits<HD>::DQ_BULK && BwdTraits<HD>::DQT) {  // transposed accumulator tiles
     constexpr int BM = BwdTraits<HD>::BM;
     dim3 grid((unsigned)((a.ql + BM - 1) / BM * 2), BH < 65535 ? BH : 65535);
     profile_mark(kKernBwdDq, 0, s);
@@ -1241,9 +1270,9 @@ static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t
     const long long groups = (long long)a.ql * (HD / 8);  // 8-value groups per head
     dim3 grid((unsigned)((groups + 255) / 256), BH < 65535 ? BH : 65535);
     profile_mark(kKernBwdDq, 0, s);
-    bwd_dq_kernel<HD><<<grid, 256, 0, s>>>(a.dqacc, reinterpret_cast<__nv_bfloat16*>(a.dq), BH,
-                                           a.ql, a.ql_pad, a.scale, dsink_part, a.dsinks, a.B,
-                                           a.H, sink_chunks, 1, a.cu_q, a.total_q);
+    bwd_dq_kernel<HD, BwdTraits<HD>::DQ_BULK><<<grid, 256, 0, s>>>(
+        a.dqacc, reinterpret_cast<__nv_bfloat16*>(a.dq), BH, a.ql, a.ql_pad, a.scale, dsink_part,
+        a.dsinks, a.B, a.H, sink_chunks, 1, a.cu_q, a.total_q);
     profile_mark(kKernBwdDq, 1, s);
   }
   return cudaGetLastError();
