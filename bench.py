@@ -69,6 +69,38 @@ def kernel_flops(w):
     return out
 
 
+# exp2 rate of the special-function (MUFU) unit of an sm_100-family SM: 4 per clock in each of
+# its four sub-partitions.
+MUFU_EX2_PER_SM_CLK = 16
+
+
+def kernel_exps(w):
+    """exp2 evaluations of one launch by the counting rule: one per (query, key) pair in the
+    forward (P) and again in the backward main pass (P recomputed from L); the deterministic dQ
+    kernel recomputes P once more."""
+    fwd_f, _ = w.flops()
+    pairs = fwd_f / (2.0 * (w.head_dim + w.dv))
+    out = {"fwd_kernel": pairs, "bwd_main_kernel": pairs}
+    if w.deterministic:
+        out["bwd_dq_det_kernel"] = pairs
+    return out
+
+
+def kernel_bounds(w, tensor_tflops, n_sm, sm_mhz):
+    """Two lower bounds on each tensor-core kernel's time: its FLOPs at the tensor peak, and
+    its exp2 count at the MUFU rate (every exponential on MUFU; the forward moves a share of
+    them to an FMA-pipe polynomial, so its own ceiling there is higher). The larger binds."""
+    fl, ex = kernel_flops(w), kernel_exps(w)
+    mufu = MUFU_EX2_PER_SM_CLK * n_sm * sm_mhz * 1e6
+    out = {}
+    for k in fl:
+        t_tc = fl[k] / (tensor_tflops * 1e12) * 1e6
+        t_ex = ex.get(k, 0.0) / mufu * 1e6
+        out[k] = {"tensor_us": t_tc, "exp2_mufu_us": t_ex,
+                  "binds": "tensor" if t_tc >= t_ex else "exp2"}
+    return {"exp2_per_s": mufu, "n_sm": n_sm, "sm_mhz": sm_mhz, "kernels": out}
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -804,6 +836,10 @@ def run_ours(args, w):
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"bf16_tflops burst, {peaks['source']}",
                 "per_kernel_ms": {n: (t / max(c, 1)) for n, (t, c) in prof.items()}}
+    # the secondary bound (exp2 on MUFU) beside the tensor bound, at the sampled maximum clock
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    clock = (clk or {}).get("sm_max_mhz") or (clk or {}).get("sm_mhz") or 2070.0
+    roofline["bounds"] = kernel_bounds(w, peak, n_sm, float(clock))
 
     # ---------------- end to end through the C ABI with host buffers
     e2e = None

@@ -50,3 +50,22 @@ def test_existing_seeds_unchanged():
     # appending workloads must not move the seeds of the existing ones
     names = [w.name for w in fa_inputs.WORKLOADS[:5]]
     assert names == ["tiny_gqa_d64", "masked_d256", "train_d64", "gqa_d128_4k", "rect_d256"]
+
+
+def test_exp2_bound_binds_the_d64_forward_only():
+    """The secondary (exp2 on MUFU) bound: at head_dim 64 the forward's exponentials outweigh its
+    tensor work, at 128 the tensor work dominates, and the backward (2.5x the forward's FLOPs
+    for the same exponentials) stays tensor-bound."""
+    import bench
+
+    peak, n_sm, mhz = 1945.3, 152, 2070.0
+    d64 = bench.kernel_bounds(fa_inputs.BY_NAME["train_d64"], peak, n_sm, mhz)["kernels"]
+    d128 = bench.kernel_bounds(fa_inputs.BY_NAME["gqa_d128_4k"], peak, n_sm, mhz)["kernels"]
+    assert d64["fwd_kernel"]["binds"] == "exp2"
+    assert d64["bwd_main_kernel"]["binds"] == "tensor"
+    assert d128["fwd_kernel"]["binds"] == "tensor" and d128["bwd_main_kernel"]["binds"] == "tensor"
+    # one exponential per visible pair: B*H*ql*kl/2 for causal
+    w = fa_inputs.BY_NAME["gqa_d128_4k"]
+    assert bench.kernel_exps(w)["fwd_kernel"] == w.batch * w.n_heads * w.ql * w.kl * 0.5
+    exp_us = d128["fwd_kernel"]["exp2_mufu_us"]
+    assert abs(exp_us - w.batch * w.n_heads * w.ql * w.kl * 0.5 / (16 * n_sm * mhz * 1e6) * 1e6) < 1e-6
