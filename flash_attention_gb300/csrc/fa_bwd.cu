@@ -20,11 +20,11 @@
 //                    to TMEM as bf16; dV += P^T dO and dK += dS^T Q with the A operand read
 //                    from TMEM; dQ^T = K^T dS^T (head_dim >= 128) or dQ = dS K (head_dim 64)
 //                    with dS^T staged in swizzled shared memory; a second warpgroup drains dQ
-//                    from TMEM into the f32 accumulator with global reductions (head_dim 128:
-//                    one bulk reduction per tile, the tile kept transposed), and writes dK, dV
-//                    at the end
+//                    from TMEM into the f32 accumulator with global reductions (head_dim 64
+//                    and 128: one bulk reduction per tile staged in shared memory, at 128 kept
+//                    transposed), and writes dK, dV at the end
 //   bwd_dq_kernel    dQ = bf16(scale * accumulator); bwd_dq_tiles_kernel does the same from
-//                    the transposed tiles of the bulk path
+//                    the transposed tiles of the head_dim-128 bulk path
 #include <float.h>
 
 #include <mutex>

@@ -69,3 +69,13 @@ def test_exp2_bound_binds_the_d64_forward_only():
     assert bench.kernel_exps(w)["fwd_kernel"] == w.batch * w.n_heads * w.ql * w.kl * 0.5
     exp_us = d128["fwd_kernel"]["exp2_mufu_us"]
     assert abs(exp_us - w.batch * w.n_heads * w.ql * w.kl * 0.5 / (16 * n_sm * mhz * 1e6) * 1e6) < 1e-6
+
+
+def test_source_hash_ignores_comments_only():
+    """A recorded capture stays valid across comment edits and is voided by code edits."""
+    import bench
+
+    code = "int f(int x) {  // doubles\n  /* the\n  body */ return 2 * x;\n}\n"
+    assert bench.code_only(code) == bench.code_only(code.replace("doubles", "twice x"))
+    assert bench.code_only(code) == bench.code_only(code + "\n\n// trailing note\n")
+    assert bench.code_only(code) != bench.code_only(code.replace("2 * x", "3 * x"))
