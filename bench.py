@@ -175,8 +175,8 @@ def code_only(text):
 def source_hash(files):
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, f)) as fh:
-            h.update(code_only(fh.read()).encode())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            h.update(code_only(fh.read()).encode("utf-8"))
     return h.hexdigest()[:16]
 
 
