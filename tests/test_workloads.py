@@ -79,3 +79,28 @@ def test_source_hash_ignores_comments_only():
     assert bench.code_only(code) == bench.code_only(code.replace("doubles", "twice x"))
     assert bench.code_only(code) == bench.code_only(code + "\n\n// trailing note\n")
     assert bench.code_only(code) != bench.code_only(code.replace("2 * x", "3 * x"))
+
+
+def test_reference_arm_json_line():
+    """`bench.py --impl reference` (the CPU oracle arm, runnable without a GPU) prints one JSON
+    line with the contract's keys."""
+    import json
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "0", "--workload", "tiny_gqa_d64"],
+                       capture_output=True, text=True, timeout=300, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["config"]["workload"] == "tiny_gqa_d64"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
