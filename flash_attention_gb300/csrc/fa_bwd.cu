@@ -1001,7 +1001,8 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
           for (int e = 0; e < 32; ++e)
             atomicAdd(dst + (size_t)(c32 * 32 + e) * HD, __uint_as_float(rq[c32][e]));
       } else {
-        // lane = query row, column = head-dim index
+        // lane = query row, column = head-dim index (dQ formed without a staging tile; no
+        // head dim selects this form at present: head_dim 64 stages its tile)
         float4* dst = reinterpret_cast<float4*>(p.dqacc + ((size_t)bh * p.ql_pad + q0 + j) * HD);
         uint32_t rq[HD / 32][32];
 #pragma unroll
