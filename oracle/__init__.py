@@ -47,7 +47,11 @@ MUTATIONS = {
     "v_stride_d": 16,
     "table_stride": 17,
     "decode_top_left": 18,
+    "bool_mask_inverted": 19,
 }
+# Codes above handled here in Python (the mask-form conversion), not in fa_oracle.c.
+_PY_MUTATION_BOOL_INVERTED = 19
+_py_mutation = 0
 
 
 def build(force: bool = False) -> str:
@@ -166,14 +170,19 @@ def dense_mask(mask, shape):
         return None
     m = np.asarray(mask)
     if m.dtype == np.bool_ or m.dtype == np.uint8:
-        m = np.where(m != 0, np.float32(0.0), np.float32(-np.inf))
+        visible = m != 0
+        if _py_mutation == _PY_MUTATION_BOOL_INVERTED:
+            visible = ~visible
+        m = np.where(visible, np.float32(0.0), np.float32(-np.inf))
     m = np.broadcast_to(m.astype(np.float32), shape)
     return np.ascontiguousarray(m)
 
 
 def set_mutation(name_or_code) -> None:
     """Plant one known mistake in the oracle (tests only); 0 or None removes it."""
+    global _py_mutation
     code = MUTATIONS.get(name_or_code, name_or_code) if name_or_code else 0
+    _py_mutation = int(code)
     _load().fa_oracle_set_mutation(int(code))
 
 

@@ -731,6 +731,69 @@ def pin_varlen_vs_torch():
     return fails
 
 
+def pin_mask_forms_vs_torch():
+    """The mask forms the CUDA path accepts, through `oracle.dense_mask`, against torch given the
+    same mask in its own form (page "nuvec-core tests/fast.rs",
+    `attention_kernels_match_the_fallback`: bool [lq, lk] masks and additive [1, Hq, Lq, Lk]
+    masks). torch's scaled_dot_product_attention reads a bool `attn_mask` as True = the key takes
+    part, and broadcasts a mask of shape [ql, kl], [B, 1, ql, kl] or [1, H, ql, kl] itself; an
+    additive bf16 mask is widened to f64 by torch. O, dQ, dK and dV come from torch's math kernel
+    and autograd (f64); L from torch.logsumexp over torch's masked scores. A row that the mask
+    hides entirely must give O = 0 (torch's math kernel returns zeros there), L = -inf and zero
+    gradients."""
+    out = []
+    B, H, Hk, ql, kl, d = 2, 4, 2, 9, 13, 8
+    q, k, v, do, _ = _problem(71, B, H, Hk, ql, kl, d)
+    rng = np.random.default_rng(72)
+    scale = 0.35
+    m_2d = rng.random((ql, kl)) > 0.3
+    m_2d[3, :] = False  # one row hidden entirely
+    m_b1 = rng.random((B, 1, ql, kl)) > 0.3
+    m_bf = rng.uniform(-2.0, 0.5, size=(1, H, ql, kl)).astype(np.float32)
+    m_bf[rng.random(m_bf.shape) < 0.1] = -np.inf
+    m_bf = _bf16_exact(m_bf)
+    cases = [("bool [ql,kl]", m_2d, False), ("bool [B,1,ql,kl] causal", m_b1, True),
+             ("bf16 [1,H,ql,kl]", m_bf, False)]
+    G = H // Hk
+    for name, m_np, causal in cases:
+        dm = oracle.dense_mask(m_np, (B, H, ql, kl))
+        o, lse = oracle.fwd(q, k, v, dm, scale=scale, causal=causal)
+        dq, dk, dv = oracle.bwd(q, k, v, dm, do, scale=scale, causal=causal)
+        if m_np.dtype == np.bool_:
+            tm = torch.from_numpy(m_np)
+            if causal:
+                tm = tm & causal_lower_right(ql, kl)._materialize(device="cpu")
+        else:  # (the additive case runs without causal)
+            tm = torch.from_numpy(m_np).to(torch.bfloat16).double()
+        qt = torch.from_numpy(q).double().requires_grad_()
+        kt = torch.from_numpy(k).double().requires_grad_()
+        vt = torch.from_numpy(v).double().requires_grad_()
+        with torch.nn.attention.sdpa_kernel(torch.nn.attention.SDPBackend.MATH):
+            ot = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=tm, scale=scale,
+                                                enable_gqa=True)
+        (ot * torch.from_numpy(do).double()).sum().backward()
+        _cmp(f"mask {name} O", o, ot.detach().numpy(), out=out)
+        _cmp(f"mask {name} dQ", dq, qt.grad.numpy(), out=out)
+        _cmp(f"mask {name} dK", dk, kt.grad.numpy(), out=out)
+        _cmp(f"mask {name} dV", dv, vt.grad.numpy(), out=out)
+        with torch.no_grad():
+            s = scale * torch.from_numpy(q).double() @ torch.from_numpy(k).double() \
+                .repeat_interleave(G, dim=1).transpose(-1, -2)
+            if tm.dtype == torch.bool:
+                s = s.masked_fill(~tm, float("-inf"))
+            else:
+                s = s + tm
+            lt = torch.logsumexp(s, dim=-1).numpy()
+        _cmp(f"mask {name} L", lse, lt, out=out)
+    # the hidden row of the [ql, kl] bool mask: O = 0, L = -inf, dQ = 0 in every batch and head
+    dm = oracle.dense_mask(m_2d, (B, H, ql, kl))
+    o, lse = oracle.fwd(q, k, v, dm, scale=scale, causal=False)
+    dq, _, _ = oracle.bwd(q, k, v, dm, do, scale=scale, causal=False)
+    if not (np.all(o[:, :, 3] == 0) and np.all(np.isneginf(lse[:, :, 3])) and np.all(dq[:, :, 3] == 0)):
+        out.append("mask: a row hidden by the bool mask must give O = 0, L = -inf, dQ = 0")
+    return out
+
+
 ALL_PINS = [
     pin_fwd_vs_torch_cpu_flash,
     pin_bwd_vs_torch_autograd,
@@ -749,4 +812,5 @@ ALL_PINS = [
     pin_paged_vs_torch,
     pin_paged_layout_invariance,
     pin_varlen_vs_torch,
+    pin_mask_forms_vs_torch,
 ]
