@@ -141,6 +141,16 @@ def load_library():
             lib.fa_profile_read.restype = ctypes.c_int
             lib.fa_kernel_name.argtypes = [ctypes.c_int]
             lib.fa_kernel_name.restype = ctypes.c_char_p
+            lib.fa_train_bwd_noalloc.argtypes = [vp, vp, vp, vp, fp, vp, fp, vp, vp, vp, pp, vp]
+            lib.fa_train_bwd_noalloc.restype = ctypes.c_int
+            lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+            lib.fa_set_wait_limit_ns.restype = ctypes.c_int
+            lib.fa_get_wait_limit_ns.argtypes = []
+            lib.fa_get_wait_limit_ns.restype = ctypes.c_uint64
+            lib.fa_debug_ex2.argtypes = [vp, vp, vp, vp, ctypes.c_int64, vp]
+            lib.fa_debug_ex2.restype = ctypes.c_int
+            lib.fa_debug_wait_timeout.argtypes = [vp, vp]
+            lib.fa_debug_wait_timeout.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -301,6 +311,62 @@ def fa_error_string(code: int) -> str:
 
 def fa_version() -> str:
     return load_library().fa_version().decode()
+
+
+def fa_train_bwd_noalloc(q, k, v, o, lse, dO, mask, dq, dk, dv, params: FaParams,
+                         stream=None) -> None:
+    """C call `fa_train_bwd_noalloc` (the backward with its scratch in the library's fixed
+    device array; no allocation)."""
+    import torch
+
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO"), (dq, "dq"), (dk, "dk"),
+                 (dv, "dv")):
+        _check(t, torch.bfloat16, n)
+    _check(lse, torch.float32, "lse")
+    if mask is not None:
+        _check(mask, torch.float32, "mask")
+    rc = load_library().fa_train_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                             _ptr(dO), _ptr(mask), _ptr(dq), _ptr(dk), _ptr(dv),
+                                             ctypes.byref(params), _stream_handle(stream))
+    if rc:
+        raise FaError(rc, "fa_train_bwd_noalloc")
+
+
+def fa_set_wait_limit_ns(ns: int) -> None:
+    """Limit of one barrier wait in the kernels launched from now on (0: the default 2 s)."""
+    rc = load_library().fa_set_wait_limit_ns(int(ns))
+    if rc:
+        raise FaError(rc, "fa_set_wait_limit_ns")
+
+
+def fa_get_wait_limit_ns() -> int:
+    return int(load_library().fa_get_wait_limit_ns())
+
+
+def fa_debug_ex2(x, stream=None):
+    """The softmax's two exp2 forms and CUDA's exp2f on a CUDA float32 tensor:
+    (polynomial, hardware approximation, exp2f)."""
+    import torch
+
+    _check(x, torch.float32, "x")
+    outs = [torch.empty_like(x) for _ in range(3)]
+    rc = load_library().fa_debug_ex2(_ptr(x), *(_ptr(t) for t in outs), x.numel(),
+                                     _stream_handle(stream))
+    if rc:
+        raise FaError(rc, "fa_debug_ex2")
+    return tuple(outs)
+
+
+def fa_debug_wait_timeout(stream=None):
+    """Launches the kernel that waits on a barrier nothing completes; returns a CUDA int64
+    tensor that receives how long it waited (ns)."""
+    import torch
+
+    waited = torch.zeros(1, dtype=torch.int64, device="cuda")
+    rc = load_library().fa_debug_wait_timeout(_ptr(waited), _stream_handle(stream))
+    if rc:
+        raise FaError(rc, "fa_debug_wait_timeout")
+    return waited
 
 
 def _plain_call(q, k, v, mask, window, sinks):

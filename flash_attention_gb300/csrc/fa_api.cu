@@ -80,6 +80,15 @@ cudaError_t device_status_word(int dev, int** out) {
   return cudaSuccess;
 }
 
+// ---------------------------------------------------------------- bounded waits
+// Limit of one barrier wait in the kernels launched from now on (fa_set_wait_limit_ns).
+std::atomic<uint64_t> g_wait_limit_ns{fa::kWaitLimitNs};
+constexpr uint64_t kMaxWaitLimitNs = 60ull * 1000000000ull;  // 60 s
+
+// Devices on which fa_train_bwd_noalloc has been called (their fixed array's status word is
+// then read by fa_device_status too).
+std::atomic<uint64_t> g_noalloc_used{0};
+
 // ---------------------------------------------------------------- argument checks
 constexpr int kMaxLen = 1 << 22;  // keeps every grid dimension within its limit
 constexpr int kPagedMaxRows = 128 * 65535;  // query rows per kv head (grid z of 128-row tiles)
@@ -156,10 +165,13 @@ int check_device() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  int major = 0;
+  int major = 0, minor = 0;
   e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-  if (major != 10) return FA_ERR_UNSUPPORTED;
+  // the library holds sm_103a code only: any other device (sm_100 included) would fail at the
+  // first launch with "no kernel image"
+  if (major != 10 || minor != 3) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 
@@ -284,6 +296,7 @@ int fa_train_fwd_ex(const void* q, const void* k, const void* v, const void* mas
   a.o = o;
   a.lse = lse;
   if ((e = device_status_word(dev, &a.status)) != cudaSuccess) return cuda_fail(e, "status word");
+  a.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   a.B = p->batch;
   a.H = p->n_heads;
   a.Hk = p->n_kv_heads;
@@ -368,6 +381,7 @@ static int prepare_bwd(const void* q, const void* k, const void* v, const void* 
   a->hi_off = band.hi_off;
   a->band = band.mode;
   a->status = nullptr;
+  a->wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   (void)m;
   return FA_OK;
 }
@@ -438,21 +452,28 @@ int fa_train_bwd_noalloc(const void* q, const void* k, const void* v, const void
   int rc = prepare_bwd(q, k, v, o, lse, dO, mask, dq, dk, dv, p, nullptr, &a, &m);
   if (rc) return rc;
   const size_t ws_bytes = fa::bwd_workspace_bytes(a.B, a.H, a.ql, a.d);
-  if (ws_bytes > fa::kNoAllocScratchBytes) {
+  const size_t ws_max = fa::kNoAllocScratchBytes - fa::kNoAllocStatusBytes;
+  if (ws_bytes > ws_max) {
     snprintf(g_last_cuda_error, sizeof(g_last_cuda_error),
              "fa_train_bwd_noalloc: needs %zu bytes of scratch, the fixed array holds %zu",
-             ws_bytes, fa::kNoAllocScratchBytes);
+             ws_bytes, ws_max);
     return FA_ERR_TOO_LARGE;
   }
   if ((rc = check_device())) return rc;
   cudaError_t e = get_encoder();
   if (e != cudaSuccess) return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
-  void* ws = nullptr;
-  if ((e = fa::noalloc_scratch(&ws)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
-  a.status = nullptr;  // the status word is allocated; this path records no timeout
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  void* base = nullptr;
+  if ((e = fa::noalloc_scratch(&base)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
   if ((rc = encode_bwd_maps(a, &m))) return rc;
-  // the pre-pass rewrites L*log2(e) and D and zeroes the dQ accumulator for every row the
-  // main pass reads, so the array's previous contents never reach a result
+  // the array's first bytes are this path's status word (a bounded wait that runs out is
+  // recorded there, and fa_device_status reads it); the workspace follows. The pre-pass
+  // rewrites L*log2(e) and D and zeroes the dQ accumulator for every row the main pass reads,
+  // so the array's previous contents never reach a result
+  a.status = static_cast<int*>(base);
+  void* ws = static_cast<uint8_t*>(base) + fa::kNoAllocStatusBytes;
+  if (dev >= 0 && dev < 64) g_noalloc_used.fetch_or(uint64_t(1) << dev);
   fa::bwd_carve_workspace(ws, a.B, a.H, a.ql, a.d, &a.lse2, &a.dvec, &a.dqacc,
                           &a.dsink_part);
   e = fa::launch_bwd(a, m, static_cast<cudaStream_t>(stream));
@@ -497,6 +518,7 @@ int fa_paged_attention(const void* q, const void* k_cache, const void* v_cache,
   a.o = o;
   a.lse = lse;
   if ((e = device_status_word(dev, &a.status)) != cudaSuccess) return cuda_fail(e, "status word");
+  a.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   a.B = p->batch;
   a.H = p->n_heads;
   a.Hk = p->n_kv_heads;
@@ -542,8 +564,50 @@ int fa_device_status(int clear) {
   if (clear && v) {
     if ((e = cudaMemset(w, 0, sizeof(int))) != cudaSuccess) return cuda_fail(e, "cudaMemset");
   }
+  if (dev < 64 && ((g_noalloc_used.load() >> dev) & 1u)) {  // the no-allocation path's word
+    int v2 = 0;
+    if ((e = fa::noalloc_status(clear, &v2)) != cudaSuccess)
+      return cuda_fail(e, "no-allocation status word");
+    if (v2 && (!v || v2 == fa::kStatusTimeout)) v = v2;
+  }
   if (!v) return FA_OK;
   return v == fa::kStatusBadInput ? FA_ERR_BAD_INPUT : FA_ERR_DEVICE_TIMEOUT;
+}
+
+int fa_set_wait_limit_ns(uint64_t ns) {
+  if (ns > kMaxWaitLimitNs) return FA_ERR_INVALID;
+  g_wait_limit_ns.store(ns == 0 ? fa::kWaitLimitNs : ns);
+  return FA_OK;
+}
+
+uint64_t fa_get_wait_limit_ns(void) { return g_wait_limit_ns.load(); }
+
+int fa_debug_ex2(const float* x, float* y_poly, float* y_mufu, float* y_ref, int64_t n,
+                 void* stream) {
+  if (n < 0) return FA_ERR_INVALID;
+  if (n > 0 && (!x || !y_poly || !y_mufu || !y_ref || !aligned(x, 4) || !aligned(y_poly, 4) ||
+                !aligned(y_mufu, 4) || !aligned(y_ref, 4)))
+    return FA_ERR_INVALID;
+  int rc;
+  if ((rc = check_device())) return rc;
+  cudaError_t e = fa::launch_ex2_probe(x, y_poly, y_mufu, y_ref, (long long)n,
+                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e, "exp2 probe launch");
+}
+
+int fa_debug_wait_timeout(uint64_t* waited_ns, void* stream) {
+  if (waited_ns && !aligned(waited_ns, 8)) return FA_ERR_INVALID;
+  int rc;
+  if ((rc = check_device())) return rc;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int* status = nullptr;
+  if ((e = device_status_word(dev, &status)) != cudaSuccess) return cuda_fail(e, "status word");
+  e = fa::launch_wait_probe(status, g_wait_limit_ns.load(),
+                            reinterpret_cast<unsigned long long*>(waited_ns),
+                            static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e, "wait probe launch");
 }
 
 const char* fa_error_string(int code) {
@@ -552,7 +616,8 @@ const char* fa_error_string(int code) {
     case FA_ERR_INVALID: return "invalid argument (parameter, null or misaligned pointer)";
     case FA_ERR_CUDA: return "CUDA call or kernel launch failed";
     case FA_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait on the device";
-    case FA_ERR_UNSUPPORTED: return "device is not an sm_100-family GPU (needs sm_103a)";
+    case FA_ERR_UNSUPPORTED:
+      return "unsupported: the device is not compute capability 10.3 (the library holds sm_103a code only), or no kernel exists for this head-dim pair";
     case FA_ERR_TOO_LARGE: return "problem needs more scratch than the fixed no-allocation array holds";
     case FA_ERR_BAD_INPUT:
       return "a paged call met a sequence length or block-table entry out of range";

@@ -27,8 +27,6 @@
 //                    the transposed tiles of the head_dim-128 bulk path
 #include <float.h>
 
-#include <mutex>
-
 #include "fa_common.cuh"
 #include "fa_launch.h"
 
@@ -152,6 +150,7 @@ struct BwdKParams {
   const int32_t* cu_k;
   int total_q, total_k;
   float scale, scale_log2;
+  unsigned long long wait_limit_ns;  // limit of one barrier wait
 };
 
 // ------------------------------------------------------------------------ prep kernel
@@ -456,7 +455,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
   __shared__ uint64_t dv_done[NSB];  // SPLIT_MMA: dV(it) has read P^T(it) from its S^T buffer
   __shared__ uint64_t stg_full, stg_free;  // dQ staging handshake of the bulk drain
   __shared__ uint32_t tmem_base_s;
-  __shared__ int abort_flag;
+  __shared__ WaitCtl wctl;
 
   const int warp = warp_id(), lane = lane_id();
   // Launch order, heaviest (causal) kv tile first either way. Fixed length: tile-major, so
@@ -495,7 +494,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
   const bool split_mma = T::SPLIT_MMA && p.skip_dq;  // two MMA issuers (see BwdTraits)
 
   if (threadIdx.x == 0) {
-    abort_flag = 0;
+    wait_ctl_init(&wctl, p.wait_limit_ns);
     mbar_init(&kv_full, 1);
     for (int s = 0; s < ST; ++s) {
       mbar_init(&qdo_full[s], 1);
@@ -546,7 +545,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
       for (int it = 0; it < n_iter; ++it) {
         const int st = it % ST;
         const uint32_t use = it / ST;
-        if (it >= ST && !mbar_wait(&qdo_empty[st], (use - 1) & 1, &abort_flag)) break;
+        if (it >= ST && !mbar_wait(&qdo_empty[st], (use - 1) & 1, &wctl)) break;
         const int h = kh * G + it / nm;
         const int q0 = (m_first + it % nm) * BM;
         const int bh = b * p.H + h;
@@ -586,16 +585,16 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
         const uint32_t tDV = tbase + LY::COL_DV, tDK = tbase + LY::COL_DK;
         const uint32_t slice = (dh * DH / 64) * (BM * 128);
         const uint32_t vslice = (dh * DVH / 64) * (BM * 128);
-        bool ok = mbar_wait(&kv_full, 0, &abort_flag);
+        bool ok = mbar_wait(&kv_full, 0, &wctl);
         if (warp == LY::MMA_WARP) {
           for (int it = 0; it < n_iter && ok; ++it) {
             const int st = it % ST;
-            ok = mbar_wait(&qdo_full[st], (it / ST) & 1, &abort_flag);
+            ok = mbar_wait(&qdo_full[st], (it / ST) & 1, &wctl);
             // S^T(it) = K Q^T, into the score buffer of it - NSB once WG1 and dV(it - NSB) have
             // read P^T(it - NSB) from it
             if (ok && it >= NSB) {
-              ok = mbar_wait(&p_consumed[it % NSB], ((it - NSB) / NSB) & 1, &abort_flag);
-              if (ok) ok = mbar_wait(&dv_done[it % NSB], ((it - NSB) / NSB) & 1, &abort_flag);
+              ok = mbar_wait(&p_consumed[it % NSB], ((it - NSB) / NSB) & 1, &wctl);
+              if (ok) ok = mbar_wait(&dv_done[it % NSB], ((it - NSB) / NSB) & 1, &wctl);
             }
             if (!ok) break;
             tc_fence_after();
@@ -610,7 +609,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
             mma_commit(&s_full[it % NSB]);
             // dP^T(it) = V dO^T, into the buffer that dQ(it - 2) used, once WG2 has drained it
             if (it >= 2) {
-              ok = mbar_wait(&dq_free[it % 2], ((it - 2) / 2) & 1, &abort_flag);
+              ok = mbar_wait(&dq_free[it % 2], ((it - 2) / 2) & 1, &wctl);
               if (!ok) break;
               tc_fence_after();
             }
@@ -631,8 +630,8 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
             const int st = it % ST;
             // (the stage barrier is observed for the tensor core's reads of Q and dO; its next
             // phase needs dK(it) below, so it cannot have moved on)
-            ok = mbar_wait(&qdo_full[st], (it / ST) & 1, &abort_flag);
-            if (ok) ok = mbar_wait(&p_ready[it % NSB], (it / NSB) & 1, &abort_flag);
+            ok = mbar_wait(&qdo_full[st], (it / ST) & 1, &wctl);
+            if (ok) ok = mbar_wait(&p_ready[it % NSB], (it / NSB) & 1, &wctl);
             if (!ok) break;
             tc_fence_after();
             const Desc qmn = make_desc(smem_u32(smem + LY::OFF_Q + st * LY::QT_BYTES), BM * 128, 1024);
@@ -647,7 +646,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
                       (it > 0 || ks > 0) ? 1u : 0u);
             mma_commit(&dv_done[it % NSB]);
             // dK += dS^T Q
-            ok = mbar_wait(&ds_ready[it % 2], (it / 2) & 1, &abort_flag);
+            ok = mbar_wait(&ds_ready[it % 2], (it / 2) & 1, &wctl);
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
@@ -688,12 +687,12 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
       // head-dim slices of Q (for dK, N = DH) and dO (for dV, N = DVH): MN-major B operands
       const uint32_t slice = (dh * DH / 64) * (BM * 128);
       const uint32_t vslice = (dh * DVH / 64) * (BM * 128);
-      bool ok = mbar_wait(&kv_full, 0, &abort_flag);
+      bool ok = mbar_wait(&kv_full, 0, &wctl);
       int q_ready = -1;  // highest iteration whose Q/dO stage wait is done
 
       auto stage_ready = [&](int it) {
         if (it > q_ready) {
-          ok = ok && mbar_wait(&qdo_full[it % ST], (it / ST) & 1, &abort_flag);
+          ok = ok && mbar_wait(&qdo_full[it % ST], (it / ST) & 1, &wctl);
           q_ready = it;
           tc_fence_after();
         }
@@ -714,7 +713,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
       auto issue_dp = [&](int it) {  // dP^T(it) = V dO^T, into the buffer dQ(it-2) used
         stage_ready(it);
         if (ok && it >= 2) {
-          ok = mbar_wait(&dq_free[it % 2], ((it - 2) / 2) & 1, &abort_flag);
+          ok = mbar_wait(&dq_free[it % 2], ((it - 2) / 2) & 1, &wctl);
           tc_fence_after();
         }
         if (!ok) return;
@@ -742,7 +741,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
         const uint32_t tDP = tbase + LY::COL_DP0 + (it % 2) * BM;
         const Desc dsd = make_desc(smem_u32(smem + LY::OFF_DS + (it % 2) * LY::DS_BYTES), kBN * 128, 1024);
         // dV += P^T dO
-        ok = mbar_wait(&p_ready[it % NSB], (it / NSB) & 1, &abort_flag);
+        ok = mbar_wait(&p_ready[it % NSB], (it / NSB) & 1, &wctl);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -757,7 +756,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
           // the next S^T into this tile's score buffer, as soon as the dS warpgroup has read
           // P^T(it) from it (dV(it), issued above, reads it first: same-thread MMAs run in order)
           if (it + NSB < n_iter) {
-            ok = mbar_wait(&p_consumed[it % NSB], (it / NSB) & 1, &abort_flag);
+            ok = mbar_wait(&p_consumed[it % NSB], (it / NSB) & 1, &wctl);
             if (!ok) break;
             tc_fence_after();
             issue_s(it + NSB);
@@ -765,7 +764,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
           }
         }
         // dK += dS^T Q
-        ok = mbar_wait(&ds_ready[it % 2], (it / 2) & 1, &abort_flag);
+        ok = mbar_wait(&ds_ready[it % 2], (it / 2) & 1, &wctl);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -810,7 +809,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
       if (!p.skip_dq && elect_one()) {
         const float* stg = reinterpret_cast<const float*>(smem + LY::OFF_STG);
         for (int it = 0; it < n_iter; ++it) {
-          if (!mbar_wait(&stg_full, it & 1, &abort_flag)) break;
+          if (!mbar_wait(&stg_full, it & 1, &wctl)) break;
           const int h = kh * G + it / nm;
           const int q0 = (m_first + it % nm) * BM;
           const int bh = b * p.H + h;
@@ -862,8 +861,8 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
 
       // the stage's L rows came with the Q/dO copies; observe that barrier here too (its
       // next phase needs this tile's dK MMA, so it cannot have moved on)
-      ok = __all_sync(0xffffffffu, mbar_wait(&qdo_full[st], (it / ST) & 1, &abort_flag));
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[it % NSB], (it / NSB) & 1, &abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(&qdo_full[st], (it / ST) & 1, &wctl));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[it % NSB], (it / NSB) & 1, &wctl));
       if (!ok) break;
       tc_fence_after();
       const float4* sL4 = reinterpret_cast<const float4*>(sL);  // -L*log2(e) per query
@@ -928,7 +927,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
       const int q0 = (m_first + it % nm) * BM;
       const int bh = b * p.H + h;
       const uint32_t colDQ = LY::COL_DP0 + (it % 2) * BM;
-      ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[it % 2], (it / 2) & 1, &abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[it % 2], (it / 2) & 1, &wctl));
       if (!ok) return;
       tc_fence_after();
       if (p.skip_dq) {  // nothing to drain: hand the buffer straight back
@@ -951,7 +950,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
         tc_fence_before();
         mbar_arrive(&dq_free[it % 2]);
         if (it > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&stg_free, (it - 1) & 1, &abort_flag));
+          ok = __all_sync(0xffffffffu, mbar_wait(&stg_free, (it - 1) & 1, &wctl));
           if (!ok) return;
         }
         float4* row = reinterpret_cast<float4*>(stg + j * BM);
@@ -974,7 +973,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
         tc_fence_before();
         mbar_arrive(&dq_free[it % 2]);
         if (it > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&stg_free, (it - 1) & 1, &abort_flag));
+          ok = __all_sync(0xffffffffu, mbar_wait(&stg_free, (it - 1) & 1, &wctl));
           if (!ok) return;
         }
         float4* row = reinterpret_cast<float4*>(stg + j * HD);
@@ -1034,13 +1033,13 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
       const float* sD = reinterpret_cast<const float*>(smem + LY::OFF_D + st * BM * 4);
       const uint32_t colS = LY::COL_S0 + (it % NSB) * BM;
       const uint32_t colDP = LY::COL_DP0 + (it % 2) * BM;
-      ok = __all_sync(0xffffffffu, mbar_wait(&dp_full[it % 2], (it / 2) & 1, &abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(&dp_full[it % 2], (it / 2) & 1, &wctl));
       // (p_ready also makes the stage's D rows visible: the P warpgroup observed the Q/dO stage
       // barrier before it arrived on p_ready)
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&p_ready[it % NSB], (it / NSB) & 1, &abort_flag));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&p_ready[it % NSB], (it / NSB) & 1, &wctl));
       // the dQ MMA of tile it-2 must be done reading this dS^T buffer
       if (ok && it >= 2)
-        ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[it % 2], ((it - 2) / 2) & 1, &abort_flag));
+        ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[it % 2], ((it - 2) / 2) & 1, &wctl));
       if (!ok) break;
       tc_fence_after();
       uint8_t* sds = smem + LY::OFF_DS + (it % 2) * LY::DS_BYTES;
@@ -1106,7 +1105,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
     // ---------------------------------------------------------------- dK, dV epilogue
     bool have = false;
     if (ok) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&acc_full, 0, &abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(&acc_full, 0, &wctl));
       tc_fence_after();
       have = ok && n_iter > 0;
     }
@@ -1142,7 +1141,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == LY::MMA_WARP) tmem_dealloc(tbase, LY::TMEM_COLS);
-  if (threadIdx.x == 0) report_abort(&abort_flag, p.status);
+  if (threadIdx.x == 0) report_abort(&wctl, p.status);
 }
 
 // ------------------------------------------------------------------------ host side
@@ -1173,12 +1172,10 @@ template <int HD, int DV, int BAND, int MASKT, bool VARLEN = false>
 static cudaError_t launch_main_t(const BwdArgs& a, const BwdMaps& m, cudaStream_t s) {
   using LY = BwdLayout<HD, DV>;
   auto kern = bwd_main_kernel<HD, DV, BAND, MASKT, VARLEN>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM_BYTES);
+  static OncePerKey<> smem_attr;  // per instantiation and device
+  {
+    const cudaError_t e = set_smem_once(smem_attr, kern, LY::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   BwdKParams kp;
   kp.mask = a.mask;
@@ -1198,6 +1195,7 @@ static cudaError_t launch_main_t(const BwdArgs& a, const BwdMaps& m, cudaStream_
   kp.dk = reinterpret_cast<__nv_bfloat16*>(a.dk);
   kp.dv = reinterpret_cast<__nv_bfloat16*>(a.dv);
   kp.status = a.status;
+  kp.wait_limit_ns = a.wait_limit_ns;
   kp.H = a.H;
   kp.Hk = a.Hk;
   kp.ql = a.ql;
@@ -1281,31 +1279,20 @@ static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t
 
 // ------------------------------------------------------------------------ fixed scratch
 // Backward scratch for callers that must not allocate device memory (fa_train_bwd_noalloc).
-// A file-scope device array: every GPU that loads this library holds these bytes until the
-// process exits. Host code cannot use the array's name as a device address, so its address
-// is looked up once per device with cudaGetSymbolAddress (below) and passed to the kernels.
+// A file-scope device array: CUDA creates it when it loads this file's device code on a GPU
+// (at context creation with eager module loading, else at the first use of one of its
+// kernels or symbols), and it stays until the process exits. Host code cannot use the array's
+// name as a device address, so the address is looked up with cudaGetSymbolAddress, on the
+// current device, at every call (nothing cached: nothing goes stale across a device reset).
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-namespace {
-constexpr int kMaxNoAllocDevices = 64;
-void* g_noalloc_ptr[kMaxNoAllocDevices] = {nullptr};
-std::mutex g_noalloc_mu;
-}  // namespace
+cudaError_t noalloc_scratch(void** ptr) { return cudaGetSymbolAddress(ptr, g_noalloc_scratch); }
 
-cudaError_t noalloc_scratch(void** ptr) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxNoAllocDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // with `dev` current
-    if (e != cudaSuccess) return e;
-    g_noalloc_ptr[dev] = p;
-  }
-  *ptr = g_noalloc_ptr[dev];
-  return cudaSuccess;
+cudaError_t noalloc_status(int clear, int* value) {
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_noalloc_scratch, sizeof(int));
+  if (e != cudaSuccess || !clear || *value == 0) return e;
+  const int zero = 0;
+  return cudaMemcpyToSymbol(g_noalloc_scratch, &zero, sizeof(int));
 }
 
 cudaError_t launch_bwd(const BwdArgs& a, const BwdMaps& m, cudaStream_t stream) {

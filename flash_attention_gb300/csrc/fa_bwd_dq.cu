@@ -88,6 +88,7 @@ struct DqKParams {
   int tiles_fast;  // 1: blockIdx.x = query tile, y = (batch, head); 0: swapped
   int lo_off, hi_off;
   float scale, scale_log2;
+  unsigned long long wait_limit_ns;  // limit of one barrier wait
 };
 
 template <int MASKT>
@@ -114,7 +115,7 @@ __global__ void __launch_bounds__(DqLayout<HD, DV>::THREADS, 1)
   __shared__ uint64_t q_full, kv_full[STAGES], kv_empty[STAGES];
   __shared__ uint64_t sdp_full[2], ds_ready[2], dq_final, mma_drain;
   __shared__ uint32_t tmem_base_s;
-  __shared__ int abort_flag;
+  __shared__ WaitCtl wctl;
 
   const int warp = warp_id(), lane = lane_id();
   // variable-length batch: the tiles of one (sequence, head) together (they share K, V in L2)
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(DqLayout<HD, DV>::THREADS, 1)
   const int ntt = J1 - J0;  // kv tiles this CTA visits
 
   if (threadIdx.x == 0) {
-    abort_flag = 0;
+    wait_ctl_init(&wctl, p.wait_limit_ns);
     mbar_init(&q_full, 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&kv_full[s], 1);
@@ -185,7 +186,7 @@ __global__ void __launch_bounds__(DqLayout<HD, DV>::THREADS, 1)
       for (int jj = 0; jj < ntt; ++jj) {
         const int st = jj % STAGES;
         const uint32_t use = jj / STAGES;
-        if (use > 0 && !mbar_wait(&kv_empty[st], (use - 1) & 1, &abort_flag)) break;
+        if (use > 0 && !mbar_wait(&kv_empty[st], (use - 1) & 1, &wctl)) break;
         const int n0 = (J0 + jj) * kQN;
         mbar_arrive_expect_tx(&kv_full[st], LY::K_BYTES + LY::V_BYTES);
         for (int c = 0; c < KCH; ++c)
@@ -210,12 +211,12 @@ __global__ void __launch_bounds__(DqLayout<HD, DV>::THREADS, 1)
       const uint32_t id_s = idesc_bf16(kQM, kQN, 0, 0);  // S, dP: [q x kv]
       const uint32_t id_dq = idesc_bf16(kQM, HD, 0, 1);  // dQ: A = dS (tmem), B = K MN-major
       const uint32_t tDQ = tbase + LY::COL_DQ;
-      bool ok = mbar_wait(&q_full, 0, &abort_flag);
+      bool ok = mbar_wait(&q_full, 0, &wctl);
       tc_fence_after();
 
       auto issue_sdp = [&](int jj) {  // S(jj) = Q K^T, dP(jj) = dO V^T into buffer jj % 2
         const int st = jj % STAGES;
-        ok = ok && mbar_wait(&kv_full[st], (jj / STAGES) & 1, &abort_flag);
+        ok = ok && mbar_wait(&kv_full[st], (jj / STAGES) & 1, &wctl);
         if (!ok) return;
         tc_fence_after();
         const uint32_t tS = tbase + LY::COL_S0 + (jj % 2) * kQN;
@@ -242,7 +243,7 @@ __global__ void __launch_bounds__(DqLayout<HD, DV>::THREADS, 1)
           issue_sdp(jj + 1);
           if (!ok) break;
         }
-        ok = mbar_wait(&ds_ready[jj % 2], (jj / 2) & 1, &abort_flag);
+        ok = mbar_wait(&ds_ready[jj % 2], (jj / 2) & 1, &wctl);
         if (!ok) break;
         tc_fence_after();
         const uint32_t tS = tbase + LY::COL_S0 + (jj % 2) * kQN;
@@ -282,7 +283,7 @@ __global__ void __launch_bounds__(DqLayout<HD, DV>::THREADS, 1)
     for (int jj = 0; jj < ntt; ++jj) {
       const uint32_t colS = LY::COL_S0 + (jj % 2) * kQN;
       const uint32_t colDP = LY::COL_DP0 + (jj % 2) * kQN;
-      ok = __all_sync(0xffffffffu, mbar_wait(&sdp_full[jj % 2], (jj / 2) & 1, &abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(&sdp_full[jj % 2], (jj / 2) & 1, &wctl));
       if (!ok) break;
       tc_fence_after();
       uint32_t rs[2][32], rd[2][32];
@@ -322,7 +323,7 @@ __global__ void __launch_bounds__(DqLayout<HD, DV>::THREADS, 1)
     // ---------------------------------------------------------------- epilogue
     bool have = false;
     if (ok && ntt > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&dq_final, 0, &abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(&dq_final, 0, &wctl));
       tc_fence_after();
       have = ok;
     }
@@ -352,7 +353,7 @@ __global__ void __launch_bounds__(DqLayout<HD, DV>::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == LY::MMA_WARP) tmem_dealloc(tbase, LY::TMEM_COLS);
-  if (threadIdx.x == 0) report_abort(&abort_flag, p.status);
+  if (threadIdx.x == 0) report_abort(&wctl, p.status);
 }
 
 // ------------------------------------------------------------------------ host side
@@ -362,12 +363,10 @@ template <int HD, int DV, int BAND, int MASKT>
 static cudaError_t launch_dq_det_t(const BwdArgs& a, const DqMaps& m, cudaStream_t s) {
   using LY = DqLayout<HD, DV>;
   auto kern = bwd_dq_det_kernel<HD, DV, BAND, MASKT>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM_BYTES);
+  static OncePerKey<> smem_attr;  // per instantiation and device
+  {
+    const cudaError_t e = set_smem_once(smem_attr, kern, LY::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   DqKParams kp;
   kp.mask = a.mask;
@@ -378,6 +377,7 @@ static cudaError_t launch_dq_det_t(const BwdArgs& a, const DqMaps& m, cudaStream
   kp.dvec = a.dvec;
   kp.dq = reinterpret_cast<__nv_bfloat16*>(a.dq);
   kp.status = a.status;
+  kp.wait_limit_ns = a.wait_limit_ns;
   kp.cu_q = a.cu_q;
   kp.cu_k = a.cu_k;
   kp.total_q = a.total_q;

@@ -15,10 +15,13 @@
 
 namespace fa {
 
-// Limit of one mbarrier wait, in ns of %globaltimer. A legitimate wait in these kernels lasts
-// microseconds; reaching this means a pipeline bug, and the kernel then winds down instead of
-// hanging the GPU.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// Bounded-wait state of one CTA, in shared memory: the abort flag that the first wait to run
+// out raises, and the limit every wait of the CTA uses.
+struct WaitCtl {
+  int abort;
+  int pad_;
+  uint64_t limit_ns;
+};
 
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
@@ -72,22 +75,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait until the phase with the given parity has completed. Bounded: after kWaitLimitNs the
-// wait raises the CTA's abort flag (a shared int) and returns false. Once the flag is up every
+// Called by one thread before the CTA's first wait (followed by a CTA-wide barrier).
+__device__ __forceinline__ void wait_ctl_init(WaitCtl* w, uint64_t limit_ns) {
+  w->abort = 0;
+  w->limit_ns = limit_ns;
+}
+
+// Wait until the phase with the given parity has completed. Bounded: once the wait has lasted
+// the CTA's limit it raises the CTA's abort flag and returns false. Once the flag is up every
 // later wait returns false soon after, so all roles of the CTA reach the end of the kernel,
 // where the flag is turned into kStatusTimeout in the status word.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort_flag) {
+// The clock is read every 256 polls, or on every poll when the limit is below 100 us (a limit
+// that short exists to make waits run out in tests).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, WaitCtl* w) {
   if (mbar_try_wait(bar, parity)) return true;
+  volatile int* abort_flag = &w->abort;
+  const bool every_poll = w->limit_ns < 100000ull;
   uint64_t t0 = 0;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
+    if ((it & 255u) == 0 || every_poll) {
       if (*abort_flag) return false;
       uint64_t now = globaltimer();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > kWaitLimitNs) {
+      } else if (now - t0 > w->limit_ns) {
         *abort_flag = 1;
         return false;
       }
@@ -361,8 +373,9 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 }
 
 // Called by one thread at the very end of a kernel.
-__device__ __forceinline__ void report_abort(const volatile int* abort_flag, int* status) {
-  if (*abort_flag && status) atomicExch(status, kStatusTimeout);
+__device__ __forceinline__ void report_abort(const WaitCtl* w, int* status) {
+  if (*reinterpret_cast<const volatile int*>(&w->abort) && status)
+    atomicExch(status, kStatusTimeout);
 }
 
 // ----------------------------------------------------------------------------- math
@@ -408,7 +421,9 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
 // magic-number addition, f in [-0.5, 0.5]; 2^f by a degree-3 polynomial whose coefficients are
 // this project's own relative-error minimax (Remez) fit on [-0.5, 0.5] (max relative error
 // 7.5e-5, far below the 2^-9 half-ulp of the bf16 P it feeds); 2^n is added to the exponent
-// field. Inputs below -126 return 0 (the softmax never needs values under 2^-126).
+// field. Inputs below -126 return 0 (the softmax never needs values under 2^-126); on
+// [-126, -125) the result can land in the denormal encoding and is then only accurate to
+// about 2^-138 absolute (it joins a row sum of at least 1 and rounds to 0 in bf16).
 __device__ __forceinline__ float ex2_poly(float x) {
   constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
   constexpr float c0 = 0.99992806f, c1 = 0.69326097f, c2 = 0.24261113f, c3 = 0.05517167f;

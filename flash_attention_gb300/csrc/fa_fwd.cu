@@ -105,6 +105,7 @@ struct FwdKParams {
   int tiles_fast;  // 1: blockIdx.x = query tile, y = (batch, head); 0: the other way round
   int lo_off, hi_off;  // key j is visible to row i iff q_abs + lo_off <= j <= q_abs + hi_off
   float scale_log2;    // scale * log2(e)
+  unsigned long long wait_limit_ns;  // limit of one barrier wait
 };
 
 // Mask value of key column `j` for the row whose mask row starts at `mrow`, as a base-2
@@ -154,7 +155,7 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
   __shared__ uint64_t pv_done[NQ][NS];  // SPLIT: P V of a score buffer has read its P
   __shared__ uint64_t mma_drain, mma_drain2;
   __shared__ uint32_t tmem_base_s;
-  __shared__ int abort_flag;
+  __shared__ WaitCtl wctl;
 
   const int warp = warp_id();
   const int lane = lane_id();
@@ -212,7 +213,7 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
   }
 
   if (threadIdx.x == 0) {
-    abort_flag = 0;
+    wait_ctl_init(&wctl, p.wait_limit_ns);
     mbar_init(&q_full, 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&k_full[s], 1);
@@ -259,13 +260,13 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
       for (int j = J0; j < J1; ++j) {
         const int st = (j - J0) % STAGES;
         const uint32_t use = (j - J0) / STAGES;
-        if (use > 0 && !mbar_wait(&k_empty[st], (use - 1) & 1, &abort_flag)) break;
+        if (use > 0 && !mbar_wait(&k_empty[st], (use - 1) & 1, &wctl)) break;
         mbar_arrive_expect_tx(&k_full[st], LY::K_TILE_BYTES);
         for (int c = 0; c < KCH; ++c)
           tma_load_3d_hint(smem + LY::OFF_K + st * LY::K_TILE_BYTES + c * BN * 128, &mK,
                            &k_full[st], c * 64, krow0 + j * BN, kz, pol_kv);
         last_k[st] = j - J0;
-        if (use > 0 && !mbar_wait(&v_empty[st], (use - 1) & 1, &abort_flag)) break;
+        if (use > 0 && !mbar_wait(&v_empty[st], (use - 1) & 1, &wctl)) break;
         mbar_arrive_expect_tx(&v_full[st], LY::V_TILE_BYTES);
         for (int c = 0; c < VCH; ++c)
           tma_load_3d_hint(smem + LY::OFF_V + st * LY::V_TILE_BYTES + c * BN * 128, &mV,
@@ -300,7 +301,7 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
         for (int t = 0; t < NQ; ++t) n += (j >= jt0[t] && j < jt1[t]) ? 1 : 0;
         return n;
       };
-      bool ok = mbar_wait(&q_full, 0, &abort_flag);
+      bool ok = mbar_wait(&q_full, 0, &wctl);
       tc_fence_after();
 
       auto issue_s = [&](int t, int j) {
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
         // wait the K tiles in order (without a window the next one is always j itself)
         while (ok && j > k_ready) {
           const int jw = WIN ? k_ready + 1 : j;
-          ok = mbar_wait(&k_full[(jw - J0) % STAGES], ((jw - J0) / STAGES) & 1, &abort_flag);
+          ok = mbar_wait(&k_full[(jw - J0) % STAGES], ((jw - J0) / STAGES) & 1, &wctl);
           if (WIN) kleft[(jw - J0) % STAGES] = users(jw);
           k_ready = jw;
           tc_fence_after();
@@ -337,7 +338,7 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
               if (j < jt0[t] || j >= jt1[t]) continue;
               const int jj = j - jt0[t];
               if (jj >= NS) {
-                ok = mbar_wait(&pv_done[t][jj % NS], ((jj - NS) / NS) & 1, &abort_flag);
+                ok = mbar_wait(&pv_done[t][jj % NS], ((jj - NS) / NS) & 1, &wctl);
                 if (!ok) break;
                 tc_fence_after();
               }
@@ -355,10 +356,10 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
               if (j < jt0[t] || j >= jt1[t]) continue;
               const int jj = j - jt0[t];
               const int sb = jj % NS;
-              ok = mbar_wait(&p_full[t][sb], (jj / NS) & 1, &abort_flag);
+              ok = mbar_wait(&p_full[t][sb], (jj / NS) & 1, &wctl);
               if (!ok) break;
               if (j > v_ready) {
-                ok = mbar_wait(&v_full[st], ((j - J0) / STAGES) & 1, &abort_flag);
+                ok = mbar_wait(&v_full[st], ((j - J0) / STAGES) & 1, &wctl);
                 if (!ok) break;
                 if (WIN) vleft[st] = users(j);
                 v_ready = j;
@@ -395,10 +396,10 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
           if (j < jt0[t] || j >= jt1[t]) continue;
           const int jj = j - jt0[t];  // iteration of this query tile
           const int sb = jj % NS;
-          ok = mbar_wait(&p_full[t][sb], (jj / NS) & 1, &abort_flag);
+          ok = mbar_wait(&p_full[t][sb], (jj / NS) & 1, &wctl);
           if (!ok) break;
           if (j > v_ready) {
-            ok = mbar_wait(&v_full[st], ((j - J0) / STAGES) & 1, &abort_flag);
+            ok = mbar_wait(&v_full[st], ((j - J0) / STAGES) & 1, &wctl);
             if (!ok) break;
             if (WIN) vleft[st] = users(j);
             v_ready = j;
@@ -462,7 +463,7 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
 
     for (int j = 0; j < ntt; ++j) {  // j: iteration of this query tile (kv tile kt0 + j)
       const int sb = j % NS;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t][sb], (j / NS) & 1, &abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t][sb], (j / NS) & 1, &wctl));
       if (!ok) break;
       tc_fence_after();
       const uint32_t s_addr = lane_base + o_col + DV + sb * BN;
@@ -510,7 +511,7 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
           // O holds PV of tiles < j: wait for the last of them, then scale the row in place.
           // (S of tile j was committed after PV of tile j-NS, so at most NS-1 <= 1 phase of
           // o_done is outstanding here and the parity wait is exact.)
-          ok = __all_sync(0xffffffffu, mbar_wait(&o_done[t], (j - 1) & 1, &abort_flag));
+          ok = __all_sync(0xffffffffu, mbar_wait(&o_done[t], (j - 1) & 1, &wctl));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
@@ -567,7 +568,7 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
     // may be anywhere between NS phases behind and done here, which a parity wait cannot
     // tell apart).
     if (ok && ntt > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&o_final[t], 0, &abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(&o_final[t], 0, &wctl));
       tc_fence_after();
     }
     // O = O_acc * inv and L from the keys' normaliser l * 2^m_used. A sink adds 2^s2 to the
@@ -619,7 +620,7 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == LY::MMA_WARP) tmem_dealloc(tbase, LY::TMEM_COLS);
-  if (threadIdx.x == 0) report_abort(&abort_flag, p.status);
+  if (threadIdx.x == 0) report_abort(&wctl, p.status);
 }
 
 int fwd_q_box_rows(int) { return kBM; }
@@ -631,12 +632,10 @@ template <int HD, int DV, int BAND, int MASKT, bool VARLEN = false>
 static cudaError_t launch_fwd_t(const FwdArgs& a, const FwdMaps& m, cudaStream_t stream) {
   using LY = FwdLayout<HD, DV>;
   auto kern = fwd_kernel<HD, DV, BAND, MASKT, VARLEN>;
-  static bool attr_set = false;  // per instantiation; the attribute is per device function
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM_BYTES);
+  static OncePerKey<> smem_attr;  // per instantiation and device
+  {
+    const cudaError_t e = set_smem_once(smem_attr, kern, LY::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   FwdKParams kp;
   kp.mask = a.mask;
@@ -651,6 +650,7 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, const FwdMaps& m, cudaStream_t
   kp.total_q = a.total_q;
   kp.total_k = a.total_k;
   kp.status = a.status;
+  kp.wait_limit_ns = a.wait_limit_ns;
   kp.H = a.H;
   kp.Hk = a.Hk;
   kp.ql = a.ql;

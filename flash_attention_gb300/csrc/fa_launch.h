@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "fa_once.h"
+
 namespace fa {
 
 // Bounds of sequence b of a variable-length batch from its offsets: start and length, clamped
@@ -27,6 +29,12 @@ __device__ __forceinline__ bool varlen_seq(const int32_t* cu, int b, int total, 
 // range.
 enum : int { kStatusOk = 0, kStatusTimeout = 1, kStatusBadInput = 2 };
 
+// Default limit of one mbarrier wait in the kernels, in ns of %globaltimer. A legitimate wait
+// lasts microseconds; reaching this means a pipeline bug, and the kernel then winds down
+// instead of hanging the GPU. The host can set another limit (fa_set_wait_limit_ns); it reaches
+// every kernel as a launch parameter.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
 // Kernel ids of the timing facility (same values as FA_KERNEL_* in the public header).
 enum KernelId {
   kKernFwd = 0,
@@ -42,6 +50,19 @@ enum KernelId {
 // Records a timing event before (end = 0) or after (end = 1) a launch on `s` when timing is
 // enabled; does nothing otherwise. Defined in fa_api.cu.
 void profile_mark(int kernel, int end, cudaStream_t s);
+
+// Sets a kernel's dynamic shared-memory limit on the current device, once per device and
+// thread-safely (the attribute belongs to a device context, so a process that drives several
+// GPUs sets it on each).
+template <class K>
+inline cudaError_t set_smem_once(OncePerKey<>& once, K kern, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  return once.run(dev, [&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  });
+}
 
 // Visibility band of a row: key j is visible to query row i iff
 //   q_abs + lo_off <= j <= q_abs + hi_off,  q_abs = kl - ql + i
@@ -81,6 +102,7 @@ struct FwdArgs {
   const int32_t* cu_k;
   int total_q, total_k;  // rows per head of the packed q / k (variable-length batch)
   int* status;        // device status word (nullable)
+  uint64_t wait_limit_ns;  // limit of one barrier wait in the kernels (fa_set_wait_limit_ns)
   int B, H, Hk, ql, kl, d;  // ql, kl: the longest sequence in a variable-length batch
   int dval;           // value head dim (of v and o)
   float scale;
@@ -125,6 +147,7 @@ struct BwdArgs {
   float* dsinks;       // [H] sink gradient output, or nullptr (then no sink partials)
   float* dsink_part;   // workspace [B*H, sink_chunks]: per-block partial sums of dsinks
   int* status;
+  uint64_t wait_limit_ns;
   int B, H, Hk, ql, kl, d, ql_pad;
   int dval;  // value head dim (of v, o, dO, dV)
   int deterministic;  // 1: dQ from the query-tile-major kernel (no cross-CTA additions)
@@ -159,10 +182,23 @@ cudaError_t launch_bwd(const BwdArgs& a, const BwdMaps& m, cudaStream_t stream);
 int dq_det_box_rows();
 cudaError_t launch_dq_det(const BwdArgs& a, const DqMaps& m, cudaStream_t stream);
 
-// Fixed-size device scratch of fa_train_bwd_noalloc (defined in fa_bwd.cu). The first call on a
-// device looks up the array's device address; later calls return the cached address.
+// Fixed-size device scratch of fa_train_bwd_noalloc (defined in fa_bwd.cu): the first
+// kNoAllocStatusBytes hold the status word of the calls that use it, the rest the backward's
+// workspace. noalloc_scratch looks up the array's address on the current device (every call:
+// nothing is cached, so nothing goes stale across a device reset); noalloc_status reads (and
+// with clear != 0 zeroes) its status word, synchronously.
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
+constexpr size_t kNoAllocStatusBytes = 256;
 cudaError_t noalloc_scratch(void** ptr);
+cudaError_t noalloc_status(int clear, int* value);
+
+// Diagnostics (fa_diag.cu): the softmax's exp2 forms on an array, and one bounded wait on a
+// barrier that nothing completes (it runs out after `limit_ns`, records kStatusTimeout in
+// `status` and writes the time it waited to `waited_ns` when that is not null).
+cudaError_t launch_ex2_probe(const float* x, float* y_poly, float* y_mufu, float* y_ref,
+                             long long n, cudaStream_t s);
+cudaError_t launch_wait_probe(int* status, uint64_t limit_ns, unsigned long long* waited_ns,
+                              cudaStream_t s);
 
 // Paged key/value cache attention (fa_paged.cu).
 struct PagedArgs {
@@ -171,6 +207,7 @@ struct PagedArgs {
   void* o;               // bf16 [B, H, lq, d]
   float* lse;            // [B, H, lq] or nullptr
   int* status;
+  uint64_t wait_limit_ns;
   int B, H, Hk, G, lq, d, bs, max_pages, num_pages, causal, num_splits;
   float scale;
 };

@@ -82,6 +82,7 @@ struct PagedKParams {
   int* status;
   int H, Hk, G, lq, rows, bs, max_pages, num_pages, kps, n_splits;
   float scale_log2;
+  unsigned long long wait_limit_ns;  // limit of one barrier wait
 };
 
 template <int HD, bool CAUSAL>
@@ -97,7 +98,8 @@ __global__ void __launch_bounds__(PagedLayout<HD>::THREADS, 1)
   __shared__ uint64_t q_full, k_full[ST], v_full[ST], k_empty[ST], v_empty[ST];
   __shared__ uint64_t s_full[2], p_full[2], pv_done[2], o_done, o_final, drain_s, drain_pv;
   __shared__ uint32_t tmem_base_s;
-  __shared__ int abort_flag, bad_input;
+  __shared__ WaitCtl wctl;
+  __shared__ int bad_input;
   __shared__ int page_s[kPageChunk];  // block-table entries [chunk_base, chunk_base + 512)
 
   const int warp = warp_id(), lane = lane_id();
@@ -116,7 +118,7 @@ __global__ void __launch_bounds__(PagedLayout<HD>::THREADS, 1)
   const int live_warps = min(4, (min(p.rows - r0, kPM) + 31) / 32);
 
   if (threadIdx.x == 0) {
-    abort_flag = 0;
+    wait_ctl_init(&wctl, p.wait_limit_ns);
     bad_input = raw_len != len;
     mbar_init(&q_full, 1);
     for (int s = 0; s < ST; ++s) {
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(PagedLayout<HD>::THREADS, 1)
       uint64_t* full = which == 0 ? &k_full[st] : &v_full[st];
       bool ok = true;
       if (leader) {
-        if (use > 0) ok = mbar_wait(empty, (use - 1) & 1, &abort_flag);
+        if (use > 0) ok = mbar_wait(empty, (use - 1) & 1, &wctl);
         if (ok) mbar_arrive_expect_tx(full, LY::KV_BYTES);
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
@@ -248,12 +250,12 @@ __global__ void __launch_bounds__(PagedLayout<HD>::THREADS, 1)
       const uint32_t sq = smem_u32(smem + LY::OFF_Q), sk = smem_u32(smem + LY::OFF_K);
       const uint32_t id_s = idesc_bf16(kPM, kPN, 0, 0);
       const Desc qa = make_desc(sq, 16, 1024);
-      bool ok = ntt == 0 || mbar_wait(&q_full, 0, &abort_flag);
+      bool ok = ntt == 0 || mbar_wait(&q_full, 0, &wctl);
       tc_fence_after();
       for (int jj = 0; jj < ntt && ok; ++jj) {
         const int st = jj % ST;
-        ok = mbar_wait(&k_full[st], (jj / ST) & 1, &abort_flag);
-        if (ok && jj >= 2) ok = mbar_wait(&pv_done[jj % 2], ((jj - 2) / 2) & 1, &abort_flag);
+        ok = mbar_wait(&k_full[st], (jj / ST) & 1, &wctl);
+        if (ok && jj >= 2) ok = mbar_wait(&pv_done[jj % 2], ((jj - 2) / 2) & 1, &wctl);
         if (!ok) break;
         tc_fence_after();
         const uint32_t tS = tbase + LY::COL_S0 + (jj % 2) * kPN;
@@ -279,8 +281,8 @@ __global__ void __launch_bounds__(PagedLayout<HD>::THREADS, 1)
     for (int jj = 0; jj < ntt && ok; ++jj) {
       const int st = jj % ST;
       const int n0 = k0 + jj * kPN;
-      ok = __all_sync(0xffffffffu, mbar_wait(&p_full[jj % 2], (jj / 2) & 1, &abort_flag));
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&v_full[st], (jj / ST) & 1, &abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(&p_full[jj % 2], (jj / 2) & 1, &wctl));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&v_full[st], (jj / ST) & 1, &wctl));
       if (!ok) break;
       if (n0 + kPN > len) {
         // rows len - n0 .. kPN - 1 of this V tile hold no key of the sequence (the rest of the
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(PagedLayout<HD>::THREADS, 1)
     bool ok = true;
     for (int jj = 0; jj < ntt; ++jj) {
       const uint32_t colS = LY::COL_S0 + (jj % 2) * kPN;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[jj % 2], (jj / 2) & 1, &abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[jj % 2], (jj / 2) & 1, &wctl));
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[2][32];
@@ -363,7 +365,7 @@ __global__ void __launch_bounds__(PagedLayout<HD>::THREADS, 1)
         if (jj > 0) {
           // O holds P V of tiles < jj; S(jj) was issued after P V(jj - 2), so only the last
           // P V can be outstanding and the parity wait is exact
-          ok = __all_sync(0xffffffffu, mbar_wait(&o_done, (jj - 1) & 1, &abort_flag));
+          ok = __all_sync(0xffffffffu, mbar_wait(&o_done, (jj - 1) & 1, &wctl));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
@@ -399,7 +401,7 @@ __global__ void __launch_bounds__(PagedLayout<HD>::THREADS, 1)
     }
     // ---------------------------------------------------------------- epilogue
     if (ok && ntt > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&o_final, 0, &abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(&o_final, 0, &wctl));
       tc_fence_after();
     }
     const bool have_o = ok && ntt > 0 && l > 0.0f;
@@ -451,7 +453,7 @@ __global__ void __launch_bounds__(PagedLayout<HD>::THREADS, 1)
   __syncthreads();
   if (warp == LY::S_WARP) tmem_dealloc(tbase, LY::TMEM_COLS);
   if (threadIdx.x == 0) {
-    report_abort(&abort_flag, p.status);
+    report_abort(&wctl, p.status);
     if (bad_input && p.status) atomicCAS(p.status, kStatusOk, kStatusBadInput);
   }
 }
@@ -530,12 +532,10 @@ static cudaError_t launch_paged_t(const PagedArgs& a, const PagedMaps& m, int sp
                                   cudaStream_t s) {
   using LY = PagedLayout<HD>;
   auto kern = paged_attn_kernel<HD, CAUSAL>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM_BYTES);
+  static OncePerKey<> smem_attr;  // per instantiation and device
+  {
+    const cudaError_t e = set_smem_once(smem_attr, kern, LY::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   const long long cap = (long long)a.max_pages * a.bs;
   const long long per = (cap + splits - 1) / splits;
@@ -550,6 +550,7 @@ static cudaError_t launch_paged_t(const PagedArgs& a, const PagedMaps& m, int sp
                                                     ((size_t)splits * rows_all * HD * 4 + 255) / 256 * 256)
                          : nullptr;
   kp.status = a.status;
+  kp.wait_limit_ns = a.wait_limit_ns;
   kp.H = a.H;
   kp.Hk = a.Hk;
   kp.G = a.G;

@@ -42,8 +42,14 @@
  * Errors: a synchronous return code. Arguments are checked before anything is enqueued, so an
  * FA_ERR_INVALID call has no effect. FA_ERR_CUDA means a CUDA call or launch failed (the text
  * of the last such error is kept per thread, see fa_last_cuda_error). Kernel-side pipeline
- * stalls are bounded: a kernel that waited more than 2 s on one of its own barriers gives up,
- * returns, and leaves FA_ERR_DEVICE_TIMEOUT for fa_device_status to report.
+ * stalls are bounded: a kernel that waited more than 2 s (see fa_set_wait_limit_ns) on one of
+ * its own barriers gives up, returns, and leaves FA_ERR_DEVICE_TIMEOUT for fa_device_status to
+ * report.
+ *
+ * Devices: the library holds sm_103a code only; every compute call first checks that the
+ * current device has compute capability 10.3 (FA_ERR_UNSUPPORTED otherwise). Per-device state
+ * (kernel attributes, the status word) is set up on each device at its first use, so one
+ * process may drive several GPUs, from several host threads.
  */
 #ifndef FA_TRAIN_H_
 #define FA_TRAIN_H_
@@ -72,7 +78,8 @@ typedef struct fa_params {
 #define FA_ERR_INVALID 1        /* bad parameter, null or misaligned pointer */
 #define FA_ERR_CUDA 2           /* a CUDA runtime/driver call or a launch failed */
 #define FA_ERR_DEVICE_TIMEOUT 3 /* a kernel gave up a bounded wait (see fa_device_status) */
-#define FA_ERR_UNSUPPORTED 4    /* the device is not sm_103 or sm_100 family */
+#define FA_ERR_UNSUPPORTED 4    /* the device is not compute capability 10.3, or no kernel
+                                   exists for the requested option */
 #define FA_ERR_TOO_LARGE 5      /* the problem needs more scratch than fa_train_bwd_noalloc has */
 #define FA_ERR_BAD_INPUT 6      /* (fa_device_status) a paged call met a sequence length or a
                                    block-table entry out of range; those keys were read as 0 */
@@ -229,17 +236,26 @@ int fa_train_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
  * routine; the caller still provides every input and output.
  *
  * Limits and rules:
- *  - the scratch holds 64 MiB per GPU, held from the moment the library is loaded on that GPU
- *    until the process exits; a problem whose scratch, 4*B*H*ceil128(ql)*(head_dim + 2) bytes
- *    plus alignment, exceeds it returns FA_ERR_TOO_LARGE without touching the device;
+ *  - the array holds 64 MiB per GPU: its first 256 bytes are the status word of these calls (a
+ *    bounded wait that runs out is recorded there and reported by fa_device_status, as for the
+ *    other entry points), the rest is the backward's scratch. A problem whose scratch,
+ *    4*B*H*ceil128(ql)*(head_dim + 2) bytes plus alignment, exceeds 64 MiB - 256 bytes returns
+ *    FA_ERR_TOO_LARGE without touching the device;
+ *  - the array is part of the library's device code, and CUDA creates it on a GPU when it
+ *    loads that code there. With CUDA's default lazy loading this happens at the first call on
+ *    that GPU of this entry point or of any backward entry point of the library, and that load
+ *    does allocate device memory. So make one call (a warm-up) on each GPU before a pool
+ *    allocator reserves the device, or run with CUDA_MODULE_LOADING=EAGER, which creates the
+ *    array with the CUDA context. From then on the array stays until the process exits (or a
+ *    cudaDeviceReset, after which the next call loads it again, as the first one did);
+ *  - the first call on each GPU also sets the kernels' shared-memory attributes; make it
+ *    before any stream capture;
+ *  - every call looks up the array's address on the current device (cudaGetSymbolAddress,
+ *    which allocates nothing once the array exists); nothing is cached between calls;
  *  - every call on a GPU shares that one array, and the array keeps the previous call's
- *    contents (each call rewrites what it reads, so that does not leak into results); calls
- *    that overlap on the GPU (for example on two streams) race on it and give wrong results:
- *    serialise them;
- *  - the first call on each GPU looks up the array's device address (one runtime call, made
- *    with that GPU current); make that first call before any stream capture;
- *  - a bounded wait that runs out in one of its kernels is not recorded for fa_device_status
- *    (the kernel still ends). */
+ *    contents (each call rewrites or zeroes what it reads, so that does not leak into
+ *    results); calls that overlap on the GPU (for example on two streams) race on it and give
+ *    wrong results: serialise them. */
 int fa_train_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                          const float* lse, const void* dO, const float* mask, void* dq, void* dk,
                          void* dv, const fa_params* p, void* stream);
@@ -289,6 +305,30 @@ typedef struct fa_paged_params {
 int fa_paged_attention(const void* q, const void* k_cache, const void* v_cache,
                        const int32_t* block_table, const int32_t* lengths, void* o, float* lse,
                        const fa_paged_params* p, void* stream);
+
+/* ------------------------------------------------------------------ bounded waits, diagnostics
+ * Sets the limit of one barrier wait inside the kernels launched after this call, from any
+ * thread (default 2 s; ns = 0 restores it; more than 60 s gives FA_ERR_INVALID). A wait that
+ * lasts longer makes its kernel give up and return, with its outputs left undefined, and
+ * fa_device_status then reports FA_ERR_DEVICE_TIMEOUT. A short limit makes legitimate waits
+ * run out: it exists to test that path, not for normal use. No counterpart on the pages. */
+int fa_set_wait_limit_ns(uint64_t ns);
+/* The current limit, in ns. */
+uint64_t fa_get_wait_limit_ns(void);
+
+/* Test aid (no counterpart on the pages): evaluates, for the n floats of x (device), the two
+ * base-2 exponentials the softmax uses -- the FMA-pipe polynomial into y_poly and the hardware
+ * approximation into y_mufu -- and CUDA's exp2f into y_ref (device arrays of n floats, 4-byte
+ * aligned). Asynchronous on `stream`. */
+int fa_debug_ex2(const float* x, float* y_poly, float* y_mufu, float* y_ref, int64_t n,
+                 void* stream);
+
+/* Test aid (no counterpart on the pages): one kernel waits on a barrier that nothing ever
+ * completes, using the current wait limit. The wait runs out, the kernel records
+ * FA_ERR_DEVICE_TIMEOUT for fa_device_status and returns; with waited_ns non-NULL (device,
+ * 8-byte aligned) it writes how long it waited, in ns. Asynchronous on `stream`. Set a short
+ * limit first (fa_set_wait_limit_ns): with the default the kernel takes 2 s. */
+int fa_debug_wait_timeout(uint64_t* waited_ns, void* stream);
 
 /* Synchronises the current device, then returns FA_OK, FA_ERR_DEVICE_TIMEOUT if any kernel of
  * this library on it gave up a bounded wait, or FA_ERR_BAD_INPUT if a paged call met a length

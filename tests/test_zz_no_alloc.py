@@ -5,11 +5,13 @@ memory belongs to a pool allocator that has already reserved it, or a step loop 
 allocation is not allowed to block or fail. Those callers hand in every input and output, and
 the library takes its scratch from a fixed array that is part of the library itself.
 
-This test calls it through the C ABI and checks that, on two calls in a row, it gives what the
-ordinary allocating entry point fa_train_bwd gives, within the gradient tolerance of the parity
-tests (max |difference| <= 2e-2 * max |gradient|). It also checks that a problem too large for
-the fixed array is refused before anything runs. It is self-contained, so it passes alone in a
-fresh process as well as after the other tests; the file name makes pytest collect it last.
+The test calls it through the C ABI. For each shape it first runs a call of another shape, so
+that the fixed array holds that call's leftovers, then makes two calls in a row and checks
+both against the CPU oracle (the gradient tolerance of the parity tests: max |difference| <=
+2e-2 * max |gradient| + 1e-4) and against the ordinary allocating entry point fa_train_bwd.
+It also checks that a problem too large for the fixed array is refused before anything runs.
+It is self-contained, so it passes alone in a fresh process as well as after the other tests;
+the file name makes pytest collect it last.
 """
 import ctypes
 
@@ -17,6 +19,7 @@ import numpy as np
 import pytest
 
 import fa_inputs
+import oracle
 from tests import parity
 
 pytestmark = pytest.mark.gpu
@@ -27,6 +30,13 @@ SHAPES = [
     fa_inputs.Workload("noalloc_masked_d256", 1, 4, 2, 200, 330, 256, 1.0 / 16, False,
                        masked=True),
 ]
+# runs first in each case: other head dim, other row counts, so the array holds its leftovers
+POISON = {
+    "noalloc_gqa_d128": fa_inputs.Workload("poison_d64", 1, 4, 4, 700, 900, 64, 0.125, False,
+                                           masked=True),
+    "noalloc_masked_d256": fa_inputs.Workload("poison_d128", 2, 4, 1, 300, 300, 128, 0.09,
+                                              True),
+}
 
 
 @pytest.fixture(scope="module")
@@ -37,6 +47,7 @@ def lib():
     import flash_attention_gb300 as fa
 
     fa.build()
+    oracle.build()
     lib = fa.load_library()
     vp = ctypes.c_void_p
     lib.fa_train_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
@@ -49,41 +60,68 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-@pytest.mark.parametrize("w", SHAPES, ids=lambda w: w.name)
-def test_noalloc_backward_matches_allocating_backward(lib, w):
+def _noalloc(lib, w, d, o, lse):
+    """One fa_train_bwd_noalloc call through the C ABI; outputs start as 7.0 everywhere."""
     import torch
 
     import flash_attention_gb300 as fa
 
-    inp = fa_inputs.make_inputs(w, index=11)
-    d = parity.to_device(inp)
     q, k, v, do, mask = d["q"], d["k"], d["v"], d["do"], d["mask"]
-    o, lse = fa.attention_fwd(q, k, v, scale=w.scale, causal=w.causal, mask=mask)
-    dq_ref, dk_ref, dv_ref = fa.attention_bwd(q, k, v, o, lse, do, scale=w.scale,
-                                              causal=w.causal, mask=mask)
-    torch.cuda.synchronize()
-    ref = {n: t.float().cpu().numpy() for n, t in (("dq", dq_ref), ("dk", dk_ref), ("dv", dv_ref))}
     params = fa.make_params(q, k, scale=w.scale, causal=w.causal)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    dq, dk, dv = torch.full_like(q, 7.0), torch.full_like(k, 7.0), torch.full_like(v, 7.0)
+    rc = lib.fa_train_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                  _ptr(mask), _ptr(dq), _ptr(dk), _ptr(dv),
+                                  ctypes.byref(params), stream)
+    assert rc == fa.FA_OK, fa.fa_error_string(rc)
+    torch.cuda.synchronize()
+    return {n: t.float().cpu().numpy().astype(np.float64)
+            for n, t in (("dq", dq), ("dk", dk), ("dv", dv))}
+
+
+def _forward(w, index):
+    import flash_attention_gb300 as fa
+
+    inp = fa_inputs.make_inputs(w, index=index)
+    d = parity.to_device(inp)
+    o, lse = fa.attention_fwd(d["q"], d["k"], d["v"], scale=w.scale, causal=w.causal,
+                              mask=d["mask"])
+    return inp, d, o, lse
+
+
+@pytest.mark.parametrize("w", SHAPES, ids=lambda w: w.name)
+def test_noalloc_backward_matches_oracle_and_allocating_backward(lib, w):
+    import torch
+
+    import flash_attention_gb300 as fa
+
+    pw = POISON[w.name]
+    _, pd, po, plse = _forward(pw, 12)
+    _noalloc(lib, pw, pd, po, plse)  # leaves this shape's rows in the fixed array
+
+    inp, d, o, lse = _forward(w, 11)
+    dq_a, dk_a, dv_a = fa.attention_bwd(d["q"], d["k"], d["v"], o, lse, d["do"], scale=w.scale,
+                                        causal=w.causal, mask=d["mask"])
+    torch.cuda.synchronize()
+    alloc = {n: t.float().cpu().numpy().astype(np.float64)
+             for n, t in (("dq", dq_a), ("dk", dk_a), ("dv", dv_a))}
+    q, k, v, do = inp.widened()
+    dq_r, dk_r, dv_r = oracle.bwd(q, k, v, inp.mask, do, scale=w.scale, causal=w.causal)
+    ref = {"dq": dq_r, "dk": dk_r, "dv": dv_r}
     for call in range(2):
-        dq, dk, dv = torch.full_like(q, 7.0), torch.full_like(k, 7.0), torch.full_like(v, 7.0)
-        rc = lib.fa_train_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
-                                      _ptr(mask), _ptr(dq), _ptr(dk), _ptr(dv),
-                                      ctypes.byref(params), stream)
-        assert rc == fa.FA_OK, fa.fa_error_string(rc)
-        torch.cuda.synchronize()
-        for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
-            got = t.float().cpu().numpy()
-            assert not np.isnan(got).any()
-            bound = parity.G_REL * float(np.abs(ref[name]).max())
-            err = float(np.abs(got - ref[name]).max())
-            assert err <= bound, f"call {call}: {name} differs by {err:.3e} > {bound:.3e}"
+        got = _noalloc(lib, w, d, o, lse)
+        for name in ("dq", "dk", "dv"):
+            parity.check_grad(got[name], ref[name], name, f"{w.name} call {call} vs oracle")
+            parity.check_grad(got[name], alloc[name], name,
+                              f"{w.name} call {call} vs fa_train_bwd")
+    assert fa.fa_device_status(True) == fa.FA_OK
 
 
 def test_noalloc_refuses_a_problem_beyond_its_scratch(lib):
     import flash_attention_gb300 as fa
 
-    # 4 * 64 * 4096 * (128 + 2) bytes of scratch > 64 MiB; nothing is dereferenced or launched
+    # 4 * 64 * 4096 * (128 + 2) bytes of scratch > 64 MiB - 256; nothing is dereferenced or
+    # launched
     p = fa.FaParams(2, 32, 8, 4096, 4096, 128, 0.088, 1)
     fake = ctypes.c_void_p(0x100000)
     rc = lib.fa_train_bwd_noalloc(fake, fake, fake, fake, fake, fake, None, fake, fake, fake,
