@@ -46,13 +46,23 @@ def check_o(o_gpu, o_ref, label=""):
     err = np.abs(o_gpu - o_ref)
     tol = O_ATOL + 0.5 * bf16_ulp(o_ref)
     bad = err > tol
-    strict = np.abs(o_gpu - round_bf16(o_ref)) > O_ATOL
+    o_ref_bf = round_bf16(o_ref)
+    strict = np.abs(o_gpu - o_ref_bf) > O_ATOL
     stats = {"o_max_err": float(err.max(initial=0.0)),
-             "o_strict_one_ulp_flips": int(strict.sum())}
+             "o_strict_misses": int(strict.sum()),
+             "o_elements": int(o_ref.size)}
     if bad.any():
         i = np.unravel_index(np.argmax(np.where(bad, err - tol, -1)), err.shape)
         raise AssertionError(f"{label}: O error {err[i]:.3e} > {tol[i]:.3e} at {i} "
                              f"(gpu {o_gpu[i]!r}, ref {o_ref[i]!r}); {int(bad.sum())} bad")
+    if strict.any():
+        # every miss of the strict rule must be the neighbouring bf16 value of bf16(O_ref): a
+        # rounding flip of a correct f32 result, nothing larger
+        gb = fa_inputs.f32_to_bf16_bits(o_gpu[strict].astype(np.float32)).astype(np.int64)
+        rb = fa_inputs.f32_to_bf16_bits(o_ref_bf[strict].astype(np.float32)).astype(np.int64)
+        dist = np.abs(gb - rb)
+        assert (dist == 1).all(), (f"{label}: {int((dist != 1).sum())} strict-rule misses are "
+                                   f"not one bf16 ulp (largest distance {int(dist.max())} ulps)")
     return stats
 
 
