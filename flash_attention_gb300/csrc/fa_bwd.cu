@@ -27,61 +27,11 @@
 //                    the transposed tiles of the head_dim-128 bulk path
 #include <float.h>
 
+#include "fa_bwd_common.cuh"
 #include "fa_common.cuh"
 #include "fa_launch.h"
 
 namespace fa {
-
-namespace {
-constexpr float kLog2eB = 1.4426950408889634f;
-}
-
-// ------------------------------------------------------------------------ traits / layout
-// BM query rows per tile; DSPLIT: slices of the head dimension (one CTA per slice);
-// ST: depth of the Q/dO ring; NSB: score buffers (S^T) in TMEM; DQT: dQ formed transposed.
-// Two dP^T buffers are always used; the dQ tile of iteration `it` is written into the dP^T
-// buffer of `it` once dK has consumed the dS^T stored there. LOOKAHEAD: issue the next tile's
-// dP^T before this tile's dK (needs ST >= 2), so the dS warpgroup is fed while the tensor core
-// forms dV, dK and dQ.
-template <int HD>
-struct BwdTraits;
-// DQ_BULK: the dQ tile is staged in shared memory (f32, in the accumulator's tile layout below)
-// and added to the accumulator by one bulk reduction; otherwise each thread adds its values
-// with global reductions.
-// SPLIT_MMA: in the deterministic mode (no dQ MMAs here) two warps issue the MMAs, one S^T and
-// dP^T, the other dV and dK, so that neither stream waits behind the other's barrier waits and
-// the issuing thread is less often starved of issue slots by the busy compute warps that share
-// its scheduler (measured on the d128 causal workload: 572 -> 484 us). With dQ MMAs the single
-// issuer's order measured faster (661 vs 671 us).
-template <>
-struct BwdTraits<64> {
-  // (a 2-deep Q/dO ring leaves room for the bulk dQ staging tile)
-  static constexpr int BM = 128, DSPLIT = 1, ST = 2, NSB = 1;
-  static constexpr bool DQT = false, LOOKAHEAD = true, DQ_BULK = true;  // dQ = dS K (M = BM)
-  static constexpr bool SPLIT_MMA = false;
-};
-template <>
-struct BwdTraits<128> {
-  static constexpr int BM = 64, DSPLIT = 1, ST = 3, NSB = 2;
-  // dQ^T = K^T dS^T (M = head-dim slice)
-  static constexpr bool DQT = true, LOOKAHEAD = true, DQ_BULK = true;
-  static constexpr bool SPLIT_MMA = true;
-};
-template <>
-struct BwdTraits<256> {
-  static constexpr int BM = 64, DSPLIT = 2, ST = 1, NSB = 2;
-  static constexpr bool DQT = true, LOOKAHEAD = false, DQ_BULK = false;
-  static constexpr bool SPLIT_MMA = false;
-};
-
-constexpr int kBN = 128;  // kv rows per CTA (the M of the kv-major MMAs)
-
-// Bulk dQ path: with dQ^T formed (head_dim 128) the accumulator tile of one (batch, head,
-// query tile) is stored transposed, as head-dim rows of BM f32, with the 16-byte chunk c (query
-// rows 4c .. 4c+3) of row d at chunk position c ^ (d % kDqChunks); with dQ formed (head_dim 64)
-// it keeps query rows of HD f32, the chunk c (head-dim 4c .. 4c+3) of row q at c ^ (q %
-// kDqChunks). Either way 8 consecutive staging lanes store to 8 distinct bank groups.
-constexpr int kDqChunks = 16;  // 16-byte chunks per staged row (64 f32)
 
 // HD: head dim of Q, K (and dQ, dK); DV: head dim of V, O, dO (and dV).
 template <int HD, int DV>
@@ -131,26 +81,6 @@ struct BwdLayout {
   static_assert(!T::DQ_BULK || (T::DQT ? BM : HD) / 4 == kDqChunks, "staged dQ tile layout");
   static_assert(T::DSPLIT == 1 || DV == HD, "a split head dim needs DV == HD");
   static_assert(DVH % 16 == 0 && DVH >= 16 && DVH <= 256, "dV MMA N");
-};
-
-struct BwdKParams {
-  const void* mask;         // additive f32 / bf16, or bool (uint8), addressed with the strides
-  long long msb, msh, msq;  // mask strides (elements) of batch, head, query row
-  const float* lse2;
-  const float* dvec;
-  float* dqacc;
-  __nv_bfloat16* dk;
-  __nv_bfloat16* dv;
-  int* status;
-  int H, Hk, ql, kl, ql_pad;
-  int lo_off, hi_off;  // key j is visible to query row i iff q_abs + lo_off <= j <= q_abs + hi_off
-  int skip_dq;         // 1: dQ comes from the deterministic dQ kernel; no dQ work here
-  int tiles_fast;      // 1: blockIdx.x = kv tile, y = (batch, kv head, slice); 0: swapped
-  const int32_t* cu_q;  // variable-length batch: sequence offsets (VARLEN kernels)
-  const int32_t* cu_k;
-  int total_q, total_k;
-  float scale, scale_log2;
-  unsigned long long wait_limit_ns;  // limit of one barrier wait
 };
 
 // ------------------------------------------------------------------------ prep kernel
@@ -326,12 +256,12 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
   }
 }
 
-// dQ = bf16(scale * accumulator) from the transposed accumulator tiles of the bulk path.
-// Grid: x = (query tile of BM rows, half of the head dimension), y = (batch, head) (strided);
-// blocks with x == 0 also finish dsinks. A block reads its half tile (HD/2 rows of BM f32,
-// chunk-rotated) with all of its 16-byte loads in flight and transposes it through shared
-// memory into [q][d] (rows padded to HD/2 + 1 floats); then four consecutive threads write one
-// query row's 128 contiguous bytes of bf16.
+// dQ = bf16(scale * accumulator) from the transposed accumulator tiles of the bulk path
+// (head_dim 128 and 256). Grid: x = (query tile of BM rows, 64-row slice of the head
+// dimension), y = (batch, head) (strided); blocks with x == 0 also finish dsinks. A block reads
+// its slice (64 head-dim rows of BM f32, chunk-rotated) with all of its 16-byte loads in flight
+// and transposes it through shared memory into [q][d] (rows padded to 65 floats); then four
+// consecutive threads write one query row's 128 contiguous bytes of bf16.
 template <int HD, int BM>
 __global__ void __launch_bounds__(256) bwd_dq_tiles_kernel(const float* __restrict__ dqacc,
                                                            __nv_bfloat16* __restrict__ dq,
@@ -342,14 +272,15 @@ __global__ void __launch_bounds__(256) bwd_dq_tiles_kernel(const float* __restri
                                                            int H, int sink_chunks,
                                                            const int32_t* __restrict__ cu_q,
                                                            int total_q) {
-  constexpr int DR = HD / 2;                    // head-dim rows per block
+  constexpr int DR = 64;                        // head-dim rows per block
+  constexpr int NB = HD / DR;                   // blocks per query tile
   constexpr int NV = DR * kDqChunks / 256;      // 16-byte loads per thread
   static_assert(BM / 4 == kDqChunks && DR % kDqChunks == 0 && NV * 256 == DR * kDqChunks &&
                     BM * (DR / 16) == 256,
                 "tile layout");
   if (dsinks != nullptr && blockIdx.x == 0) dsinks_sum(dsink_part, dsinks, B, H, sink_chunks);
   __shared__ float tile[BM][DR + 1];
-  const int q0 = (blockIdx.x / 2) * BM, d0 = (blockIdx.x % 2) * DR;
+  const int q0 = (blockIdx.x / NB) * BM, d0 = (blockIdx.x % NB) * DR;
   for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
     size_t rowbase = (size_t)bh * ql;
     int qlen = ql;
@@ -390,51 +321,6 @@ __global__ void __launch_bounds__(256) bwd_dq_tiles_kernel(const float* __restri
 }
 
 // ------------------------------------------------------------------------ main kernel
-// Query tiles [first, last] whose rows see some key of the kv tile starting at n0: rows i with
-// q_abs + lo_off <= j <= q_abs + hi_off for some j in the tile (q_abs = kl - ql + i). Under the
-// causal band alone, key n0 is visible to the rows from n0 - (kl - ql) on, and to the last row.
-template <int HD, int BAND>
-__device__ __forceinline__ void bwd_mtile_range(int n0, const BwdKParams& p, int ql, int kl,
-                                                int& first, int& last) {
-  constexpr int BM = BwdTraits<HD>::BM;
-  const int n_mt = (ql + BM - 1) / BM;
-  if (BAND != kBandWindow) {
-    first = 0;
-    if (BAND == kBandCausal) {
-      const int first_row = n0 - (kl - ql);
-      first = first_row <= 0 ? 0 : first_row / BM;
-    }
-    last = n_mt - 1;
-    return;
-  }
-  const long long off = (long long)kl - ql;
-  const long long n1 = min(n0 + kBN, kl) - 1;
-  const long long imin = max(0LL, (long long)n0 - off - p.hi_off);
-  const long long imax = min((long long)ql - 1, n1 - off - p.lo_off);
-  if (imax < imin) {
-    first = 0;
-    last = -1;
-    return;
-  }
-  first = (int)(imin / BM);
-  last = (int)(imax / BM);
-}
-
-// Mask value at element offset `e` from `base`, as a base-2 additive term.
-template <int MASKT>
-__device__ __forceinline__ float mask_log2_b(const void* base, long long e) {
-  if constexpr (MASKT == 1) return reinterpret_cast<const float*>(base)[e] * kLog2eB;
-  if constexpr (MASKT == 2)
-    return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[e]) * kLog2eB;
-  if constexpr (MASKT == 3) return reinterpret_cast<const uint8_t*>(base)[e] ? 0.0f : -INFINITY;
-  return 0.0f;
-}
-
-// Writes 8 bf16 (one 16-byte granule g of row j) into a 128-byte-swizzled tile chunk.
-__device__ __forceinline__ void st_swizzled(uint8_t* chunk, int j, int g, uint4 val) {
-  *reinterpret_cast<uint4*>(chunk + j * 128 + ((g ^ (j & 7)) << 4)) = val;
-}
-
 template <int HD, int DV, int BAND, int MASKT, bool VARLEN>
 __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
@@ -1177,32 +1063,7 @@ static cudaError_t launch_main_t(const BwdArgs& a, const BwdMaps& m, cudaStream_
     const cudaError_t e = set_smem_once(smem_attr, kern, LY::SMEM_BYTES);
     if (e != cudaSuccess) return e;
   }
-  BwdKParams kp;
-  kp.mask = a.mask;
-  kp.msb = a.mask_stride_b;
-  kp.msh = a.mask_stride_h;
-  kp.msq = a.mask_stride_q;
-  kp.lo_off = a.lo_off;
-  kp.hi_off = a.hi_off;
-  kp.skip_dq = a.deterministic ? 1 : 0;
-  kp.cu_q = a.cu_q;
-  kp.cu_k = a.cu_k;
-  kp.total_q = a.total_q;
-  kp.total_k = a.total_k;
-  kp.lse2 = a.lse2;
-  kp.dvec = a.dvec;
-  kp.dqacc = a.dqacc;
-  kp.dk = reinterpret_cast<__nv_bfloat16*>(a.dk);
-  kp.dv = reinterpret_cast<__nv_bfloat16*>(a.dv);
-  kp.status = a.status;
-  kp.wait_limit_ns = a.wait_limit_ns;
-  kp.H = a.H;
-  kp.Hk = a.Hk;
-  kp.ql = a.ql;
-  kp.kl = a.kl;
-  kp.ql_pad = a.ql_pad;
-  kp.scale = a.scale;
-  kp.scale_log2 = a.scale * kLog2eB;
+  BwdKParams kp = make_bwd_kparams(a);
   const int groups = a.B * a.Hk * BwdTraits<HD>::DSPLIT, ktiles = (a.kl + kBN - 1) / kBN;
   kp.tiles_fast = a.cu_q != nullptr && groups <= 65535;  // (grid y limit)
   dim3 grid(kp.tiles_fast ? ktiles : groups, kp.tiles_fast ? groups : ktiles);
@@ -1241,9 +1102,14 @@ static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t
     profile_mark(kKernBwdPrep, 1, s);
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = a.band == kBandNone     ? launch_main_m<HD, DV, kBandNone>(a, m, s)
-                  : a.band == kBandCausal ? launch_main_m<HD, DV, kBandCausal>(a, m, s)
-                                          : launch_main_m<HD, DV, kBandWindow>(a, m, s);
+  cudaError_t e;
+  if constexpr (HD == 256) {
+    e = launch_bwd_pair(a, m, s);  // CTA pairs (fa_bwd_pair.cu)
+  } else {
+    e = a.band == kBandNone     ? launch_main_m<HD, DV, kBandNone>(a, m, s)
+        : a.band == kBandCausal ? launch_main_m<HD, DV, kBandCausal>(a, m, s)
+                                : launch_main_m<HD, DV, kBandWindow>(a, m, s);
+  }
   if (e != cudaSuccess) return e;
   if (a.deterministic) {
     e = launch_dq_det(a, m.det, s);
@@ -1259,7 +1125,7 @@ static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t
   }
   if constexpr (BwdTraits<HD>::DQ_BULK && BwdTraits<HD>::DQT) {  // transposed accumulator tiles
     constexpr int BM = BwdTraits<HD>::BM;
-    dim3 grid((unsigned)((a.ql + BM - 1) / BM * 2), BH < 65535 ? BH : 65535);
+    dim3 grid((unsigned)((a.ql + BM - 1) / BM * (HD / 64)), BH < 65535 ? BH : 65535);
     profile_mark(kKernBwdDq, 0, s);
     bwd_dq_tiles_kernel<HD, BM><<<grid, 256, 0, s>>>(
         a.dqacc, reinterpret_cast<__nv_bfloat16*>(a.dq), BH, a.ql, a.ql_pad, a.scale, dsink_part,

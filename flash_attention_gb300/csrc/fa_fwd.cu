@@ -87,6 +87,8 @@ struct FwdLayout {
   static constexpr int TMA_WARP = T::NQ * 4;
   static constexpr int MMA_WARP = T::NQ * 4 + 1;
   static constexpr int MMA2_WARP = T::NQ * 4 + 2;
+  // two CTAs per SM when both fit (TMEM and shared memory), else one
+  static constexpr int MIN_BLOCKS = (TMEM_COLS <= 256 && SMEM_BYTES <= 113 * 1024) ? 2 : 1;
   static_assert(TMEM_COLS_USED <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
@@ -121,16 +123,16 @@ __device__ __forceinline__ float mask_log2(const void* mrow, long long j) {
 
 // Kv tiles [first, last) that query tile t of the CTA at row m0 must visit: the tiles holding a
 // key inside the row band [q_abs + lo_off, q_abs + hi_off] of any of its rows (q_abs = kl - ql +
-// row). Without a window every range starts at tile 0 (an empty range is [0, 0)). With one, a
-// tile wholly past the last query row, or whose band misses every key, gets first = last = -1
-// and the caller places it at the end of the previous tile's range, so that the ranges of a
-// CTA's tiles stay ordered.
+// row). Without a window every range starts at tile 0 (an empty range is [0, 0), as for a tile
+// wholly past the last query row). With one, a tile wholly past the last query row, or whose
+// band misses every key, gets first = last = -1 and the caller places it at the end of the
+// previous tile's range, so that the ranges of a CTA's tiles stay ordered.
 template <int HD, int BAND>
 __device__ __forceinline__ void fwd_tile_range(int m0, int t, const FwdKParams& p, int ql,
                                                int kl, int& first, int& last) {
   const int r0 = m0 + t * kBM;
-  if (BAND == kBandWindow && r0 >= ql) {  // a tile wholly past the last query row
-    first = last = -1;
+  if (r0 >= ql) {  // a tile wholly past the last query row: nothing to visit
+    first = last = BAND == kBandWindow ? -1 : 0;
     return;
   }
   const int r1 = min(m0 + (t + 1) * kBM, ql) - 1;  // last row of the tile (clamped)
@@ -138,7 +140,7 @@ __device__ __forceinline__ void fwd_tile_range(int m0, int t, const FwdKParams& 
 }
 
 template <int HD, int DV, int BAND, int MASKT, bool VARLEN>
-__global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
+__global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, FwdLayout<HD, DV>::MIN_BLOCKS)
     fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                const __grid_constant__ CUtensorMap mV, const FwdKParams p) {
   using T = FwdTraits<HD>;
@@ -290,10 +292,12 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
       const uint32_t sv = smem_u32(smem + LY::OFF_V);
       // K / V of kv tile j sit in stage (j - J0) % STAGES. A stage is released once every query
       // tile that uses the kv tile has issued its MMA on it. Without a window the last query
-      // tile uses every kv tile of the CTA (its range is the widest and all start at 0), so it
-      // releases; with one, kleft / vleft count the users still to come (set when the tile's
-      // full barrier is waited, in kv order).
+      // tile with rows uses every kv tile of the CTA (its range is the widest and all start at
+      // 0), so it releases; with one, kleft / vleft count the users still to come (set when the
+      // tile's full barrier is waited, in kv order).
       int k_ready = J0 - 1, v_ready = J0 - 1;  // highest kv tile whose K / V wait is done
+      // without a window the last query tile that has rows uses every kv tile of the CTA
+      const int t_rel = min(NQ - 1, (ql - 1 - m0) / kBM);
       int kleft[STAGES], vleft[STAGES];
       auto users = [&](int j) {
         int n = 0;
@@ -324,7 +328,7 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
           mma_ss2(d_tmem, qa.at((ks / 4) * (kBM * 128) + (ks % 4) * 32), qa.hi,
                   kb.at((ks / 4) * (BN * 128) + (ks % 4) * 32), kb.hi, idesc_s, ks > 0 ? 1u : 0u);
         mma_commit(&s_full[t][jj % NS]);
-        if (WIN ? --kleft[st] == 0 : t == NQ - 1) mma_commit(&k_empty[st]);
+        if (WIN ? --kleft[st] == 0 : t == t_rel) mma_commit(&k_empty[st]);
       };
 
       if constexpr (T::SPLIT) {
@@ -375,7 +379,7 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
               mma_commit(&o_done[t]);
               mma_commit(&pv_done[t][sb]);
               if (j == jt1[t] - 1) mma_commit(&o_final[t]);  // every PV of tile t issued
-              if (WIN ? --vleft[st] == 0 : t == NQ - 1) mma_commit(&v_empty[st]);
+              if (WIN ? --vleft[st] == 0 : t == t_rel) mma_commit(&v_empty[st]);
             }
           }
           mma_commit(&mma_drain);
@@ -414,7 +418,7 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, 1)
                     (jj > 0 || ks > 0) ? 1u : 0u);
           mma_commit(&o_done[t]);
           if (j == jt1[t] - 1) mma_commit(&o_final[t]);  // every PV of tile t issued
-          if (WIN ? --vleft[st] == 0 : t == NQ - 1) mma_commit(&v_empty[st]);
+          if (WIN ? --vleft[st] == 0 : t == t_rel) mma_commit(&v_empty[st]);
           if (j + NS < jt1[t]) issue_s(t, j + NS);
         }
       }

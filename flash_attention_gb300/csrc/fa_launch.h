@@ -178,6 +178,10 @@ void bwd_carve_workspace(void* base, int B, int H, int ql, int d, float** lse2, 
 
 cudaError_t launch_bwd(const BwdArgs& a, const BwdMaps& m, cudaStream_t stream);
 
+// Backward main pass at head_dim 256 on CTA pairs (fa_bwd_pair.cu); needs the pre-pass's
+// lse2, dvec (and the zeroed dQ accumulator unless deterministic).
+cudaError_t launch_bwd_pair(const BwdArgs& a, const BwdMaps& m, cudaStream_t stream);
+
 // Deterministic dQ (fa_bwd_dq.cu): needs lse2 and dvec from the pre-pass; writes a.dq (bf16).
 int dq_det_box_rows();
 cudaError_t launch_dq_det(const BwdArgs& a, const DqMaps& m, cudaStream_t stream);
