@@ -10,26 +10,27 @@
 //   dV += P^T dO,  dK += dS^T Q,  dQ^T += K^T dS^T  (f32, across CTAs).
 //
 // Why a pair: at head_dim 256 the f32 dK and dV of a 128-key tile fill all 512 TMEM columns of
-// one CTA, so each CTA can own only one 128-wide half of them. Two CTAs that each computed S^T
-// and dP^T for their half would repeat 2 of the 5 contractions, and K, V, Q and dO would fill
-// their shared memory. Here the two CTAs of a cluster split the work instead:
-//   rank 0 holds K, computes S^T and P^T, dV and dK for head-dim columns 0-127, and all of dQ;
-//   rank 1 holds V, computes dP^T and dS^T, dV and dK for columns 128-255.
-// Each CTA stages the bf16 tile it produced (P^T from rank 0, dS^T from rank 1) in its own shared
-// memory and sends it to the other CTA with one bulk copy (cp.async.bulk shared::cta to
-// shared::cluster) that completes a transaction on the other CTA's barrier; its own copy also
-// goes to TMEM as the A operand of its own dV (rank 0) or dK (rank 1) MMA. (128 threads storing
-// their rows into the other CTA directly measured 1.3-2 us per tile, most of an iteration.) Every contraction is done once, and each CTA holds only what it multiplies: a two-stage
-// Q/dO ring fits next to K or V, the exchange buffers and (rank 0) a dQ staging tile for bulk
-// reductions.
+// one CTA. Two CTAs that each owned one half of the head dimension would both have to form S^T
+// and dP^T (2 of the 5 contractions twice), with K, V, Q and dO filling their shared memory.
+// Here the two CTAs of a cluster split the work by what they multiply:
+//   rank 0 holds K: S^T, P^T, all of dV (A = its own P^T in TMEM) and all of dQ^T;
+//   rank 1 holds V: dP^T, dS^T and all of dK (A = its own dS^T in TMEM).
+// The two tiles each rank needs from the other travel through shared memory: rank 0 stages
+// P^T in its exchange buffer and sends it with one bulk copy (cp.async.bulk shared::cta to
+// shared::cluster) that completes a transaction on rank 1's barrier; rank 1 computes dS^T,
+// writes it over P^T in the same buffer and sends it back the same way. (128 threads storing
+// their rows into the other CTA directly measured 1.3-2 us per tile.) Each rank's Q/dO stage is
+// read only by its own MMAs, so rank 0 frees it once dV is issued, without waiting for rank 1.
+// Buffer reuse follows from the order of the exchange: rank 0 stages P^T(it + 2) in its buffer
+// only after its dQ MMAs have read dS^T(it) there, which also means rank 1's copy of dS^T(it)
+// (and so rank 1's use of its own buffer) is complete before P^T(it + 2) can arrive.
 //
 // Roles (384 threads): warps 0-3 compute P^T (rank 0) or dS^T (rank 1), one kv row per thread
-// (= TMEM lane), and write that CTA's dK/dV half at the end; warps 4-7 (rank 0) drain dQ^T from
-// TMEM into a staging tile; warp 8 issues the TMA loads; warp 9 issues the MMAs, polling the
-// barriers of the three MMA groups of its rank so that whichever is ready goes first; warp 10
-// (rank 0) adds the staged dQ^T tiles into the f32 accumulator with bulk reductions; warp 11
-// sends the staged tile to the other CTA; on rank 1, warp 10 tells rank 0 when rank 1's exchange
-// buffer may be rewritten. Every wait is bounded.
+// (= TMEM lane), and write that rank's dV or dK at the end; warps 4-7 (rank 0) stage dQ^T from
+// TMEM for warp 11, which adds it to the f32 accumulator with bulk reductions; warp 8 issues
+// the TMA loads (one lane per ring); warp 9 issues the MMAs, polling the barriers of its rank's
+// MMA groups so that whichever is ready goes first; warp 10 sends the staged tiles. Every wait
+// is bounded.
 #include "fa_bwd_common.cuh"
 
 namespace fa {
@@ -42,31 +43,33 @@ constexpr int kPST = 2;   // depth of the Q / dO ring
 
 // One shared-memory layout for both ranks; what a region holds depends on the rank.
 struct PairLayout {
-  static constexpr int KV_BYTES = kBN * kPD * 2;          // K (rank 0) or V (rank 1), 64 KB
-  static constexpr int FULL_BYTES = kPM * kPD * 2;        // Q (rank 0) or dO (rank 1), 32 KB
-  static constexpr int HALF_BYTES = kPM * (kPD / 2) * 2;  // dO[:, 0:128] (0) / Q[:, 128:256] (1)
-  static constexpr int STAGE_BYTES = FULL_BYTES + HALF_BYTES;
-  static constexpr int X_BYTES = kBN * kPM * 2;           // a [kv][q] bf16 tile, 16 KB
-  static constexpr int STG_BYTES = 128 * kPM * 4;         // rank 0: 128 head-dim rows x 64 f32
+  static constexpr int KV_BYTES = kBN * kPD * 2;    // K (rank 0) or V (rank 1), 64 KB
+  static constexpr int TILE_BYTES = kPM * kPD * 2;  // one 64 x 256 bf16 tile, 32 KB
+  static constexpr int X_BYTES = kBN * kPM * 2;     // a [kv][q] bf16 exchange tile, 16 KB
+  static constexpr int STG_BYTES = 128 * kPM * 4;   // rank 0: half a dQ^T tile in f32, 32 KB
+  // Two rings with the lifetimes of their operands: F holds the tile that only S^T / dP^T read
+  // (rank 0: Q; rank 1: dO), freed as soon as that MMA completes, so one stage suffices; R
+  // holds the tile that dV / dK read (rank 0: dO; rank 1: Q) and the row vector the P^T / dS^T
+  // warps read (-L log2(e) or D), freed after dV / dK, two stages.
   static constexpr int OFF_KV = 0;
-  static constexpr int OFF_ST = OFF_KV + KV_BYTES;            // kPST stages
-  static constexpr int OFF_X = OFF_ST + kPST * STAGE_BYTES;   // 2 exchange buffers
-  static constexpr int OFF_STG = OFF_X + 2 * X_BYTES;  // rank 0: dQ^T staging; 1: dS^T out
-  static constexpr int OFF_L = OFF_STG + STG_BYTES;           // kPST x kPM f32: -L log2(e)
-  static constexpr int OFF_D = OFF_L + kPST * kPM * 4;        // kPST x kPM f32: D
-  static constexpr int OFF_END = OFF_D + kPST * kPM * 4;
+  static constexpr int OFF_F = OFF_KV + KV_BYTES;           // 1 stage
+  static constexpr int OFF_R = OFF_F + TILE_BYTES;          // kPST stages
+  static constexpr int OFF_X = OFF_R + kPST * TILE_BYTES;   // 2 exchange buffers
+  static constexpr int OFF_STG = OFF_X + 2 * X_BYTES;       // rank 0: dQ^T staging
+  static constexpr int OFF_LD = OFF_STG + STG_BYTES;        // kPST x kPM f32 (ring R)
+  static constexpr int OFF_END = OFF_LD + kPST * kPM * 4;
   static constexpr int SMEM_BYTES = OFF_END + 1024;
   // TMEM columns: two 64-column buffers (rank 0: S^T then P^T as bf16; rank 1: dP^T then dS^T),
-  // rank 0's dQ^T (two 128-row halves of 64 columns), and the dV and dK halves.
+  // rank 0's dQ^T (two 128-row halves of 64 columns), and the 256-column accumulator (rank 0:
+  // dV; rank 1: dK).
   static constexpr int COL_X0 = 0;
   static constexpr int COL_DQ = 128;
-  static constexpr int COL_DV = 256;
-  static constexpr int COL_DK = 384;
+  static constexpr int COL_ACC = 256;
   static constexpr int TMEM_COLS = 512;
   static constexpr int THREADS = 384;
-  static constexpr int TMA_WARP = 8, MMA_WARP = 9, BULK_WARP = 10, LINK_WARP = 11;
+  static constexpr int TMA_WARP = 8, MMA_WARP = 9, LINK_WARP = 10, BULK_WARP = 11;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-  static_assert(kPM / 4 == kDqChunks, "staged dQ^T tile layout");
+  static_assert(kPM / 4 == kDqChunks, "dQ^T tile layout of the accumulator");
 };
 
 template <int BAND, int MASKT, bool VARLEN>
@@ -81,15 +84,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  __shared__ uint64_t kv_full, qdo_full[ST], qdo_empty[ST];
-  __shared__ uint64_t mine_full[2];  // rank 0: S^T(it) in TMEM; rank 1: dP^T(it)
-  __shared__ uint64_t own_ready[2];  // 128 arrivals: P^T (0) / dS^T (1) written to TMEM as bf16
-  __shared__ uint64_t x_ready[2];    // the peer's tile has landed in x buffer (bulk-copy bytes)
-  __shared__ uint64_t x_free[2];     // rank 0: rank 1's x buffer may be rewritten (remote)
-  __shared__ uint64_t x_done[2];     // MMA commit: this CTA's MMAs have read its x buffer
-  __shared__ uint64_t out_staged[2]; // 128 arrivals: this CTA's outgoing tile is staged
-  __shared__ uint32_t n_sent;        // tiles sent to the peer (read by the peer at the end)
+  __shared__ uint64_t kv_full, f_full, f_empty, r_full[ST], r_empty[ST];
+  __shared__ uint64_t mine_full[2];   // rank 0: S^T(it) in TMEM; rank 1: dP^T(it)
+  __shared__ uint64_t own_ready[2];   // 128 arrivals: P^T (0) / dS^T (1) written to TMEM as bf16
+  __shared__ uint64_t x_ready[2];     // the peer's tile has landed in x buffer (bulk-copy bytes)
+  __shared__ uint64_t x_done[2];      // rank 0: its dQ MMAs have read dS^T in x buffer
+  __shared__ uint64_t out_staged[2];  // 128 arrivals: this rank's outgoing tile is in x buffer
   __shared__ uint64_t dq_full, dq_free, stg_full, stg_free, acc_full, mma_drain;
+  __shared__ uint32_t n_sent;         // tiles sent to the peer (read by the peer at the end)
   __shared__ uint32_t tmem_base_s;
   __shared__ WaitCtl wctl;
 
@@ -128,27 +130,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
   if (threadIdx.x == 0) {
     wait_ctl_init(&wctl, p.wait_limit_ns);
     mbar_init(&kv_full, 1);
+    mbar_init(&f_full, 1);
+    mbar_init(&f_empty, 1);
     for (int s = 0; s < ST; ++s) {
-      mbar_init(&qdo_full[s], 1);
-      mbar_init(&qdo_empty[s], 1);
+      mbar_init(&r_full[s], 1);
+      mbar_init(&r_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&mine_full[s], 1);
       mbar_init(&own_ready[s], 128);
       mbar_init(&x_ready[s], 1);
-      mbar_init(&x_free[s], 1);
       mbar_init(&x_done[s], 1);
       mbar_init(&out_staged[s], 128);
     }
-    n_sent = 0;
     mbar_init(&dq_full, 1);
     mbar_init(&dq_free, 128);
     mbar_init(&stg_full, 128);
     mbar_init(&stg_free, 1);
     mbar_init(&acc_full, 1);
     mbar_init(&mma_drain, 1);
-    // rank 1 receives P^T(0) and P^T(1) into armed phases (later phases are armed as buffers
-    // free up; rank 0 arms each phase before it sends the P^T the peer answers with dS^T)
+    n_sent = 0;
+    // every phase of x_ready expects one tile; it is armed before that tile can be sent: rank 1
+    // arms P^T(0), P^T(1) here and P^T(it + 2) before it sends dS^T(it); rank 0 arms dS^T(it)
+    // before it sends P^T(it)
     if (rank == 1)
       for (int s = 0; s < 2 && s < n_iter; ++s) mbar_arrive_expect_tx(&x_ready[s], LY::X_BYTES);
     fence_barrier_init();
@@ -160,128 +164,111 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync_all();  // the peer's barriers are initialised before any remote arrive
+  cluster_sync_all();  // the peer's barriers are initialised before any copy reaches them
   const uint32_t tbase = tmem_base_s;
   const uint32_t x_local = smem_u32(smem + LY::OFF_X);
 
   if (warp == LY::TMA_WARP) {
-    // ------------------------------------------------------------------ TMA producer
-    if (elect_one()) {
+    // ------------------------------------------------------------------ TMA producers
+    // lane 0: K or V, then ring F; lane 1: ring R (each waits only on its own ring)
+    const CUtensorMap* mkv = rank == 0 ? &mK : &mV;
+    const CUtensorMap* mfirst = rank == 0 ? &mQ : &mDO;   // read by S^T / dP^T (ring F)
+    const CUtensorMap* msecond = rank == 0 ? &mDO : &mQ;  // read by dV / dK (ring R)
+    const float* ld_src = rank == 0 ? p.lse2 : p.dvec;    // -L log2(e) (P^T) or D (dS^T)
+    if (lane == 0) {
       tma_prefetch_desc(&mQ);
       tma_prefetch_desc(&mK);
       tma_prefetch_desc(&mV);
       tma_prefetch_desc(&mDO);
-      int last_use[ST];
-      for (int s = 0; s < ST; ++s) last_use[s] = -1;
-      const CUtensorMap* mkv = rank == 0 ? &mK : &mV;
-      const CUtensorMap* mfull = rank == 0 ? &mQ : &mDO;  // the tile this rank needs whole
-      const CUtensorMap* mhalf = rank == 0 ? &mDO : &mQ;  // ... and the half it needs
-      const int half_c0 = rank == 0 ? 0 : 2;              // first 64-column chunk of that half
       mbar_arrive_expect_tx(&kv_full, LY::KV_BYTES);
       for (int c = 0; c < HD / 64; ++c)
         tma_load_3d(smem + LY::OFF_KV + c * kBN * 128, mkv, &kv_full, c * 64, krow0 + n0, kz);
+      int loaded = 0;
+      for (int it = 0; it < n_iter; ++it) {
+        if (it >= 1 && !mbar_wait(&f_empty, (it - 1) & 1, &wctl)) break;
+        const int h = kh * G + it / nm;
+        const int q0 = (m_first + it % nm) * BM;
+        mbar_arrive_expect_tx(&f_full, LY::TILE_BYTES);
+        for (int c = 0; c < HD / 64; ++c)
+          tma_load_3d(smem + LY::OFF_F + c * BM * 128, mfirst, &f_full, c * 64, qrow0 + q0,
+                      qzb + h);
+        loaded = it + 1;
+      }
+      mbar_wait_drain(&kv_full, 0);
+      if (loaded > 0) mbar_wait_drain(&f_full, (loaded - 1) & 1);
+    } else if (lane == 1) {
+      int last_use[ST];
+      for (int s = 0; s < ST; ++s) last_use[s] = -1;
       for (int it = 0; it < n_iter; ++it) {
         const int st = it % ST;
         const uint32_t use = it / ST;
-        if (it >= ST && !mbar_wait(&qdo_empty[st], (use - 1) & 1, &wctl)) break;
+        if (it >= ST && !mbar_wait(&r_empty[st], (use - 1) & 1, &wctl)) break;
         const int h = kh * G + it / nm;
         const int q0 = (m_first + it % nm) * BM;
         const int bh = b * p.H + h;
-        uint8_t* sbase = smem + LY::OFF_ST + st * LY::STAGE_BYTES;
-        mbar_arrive_expect_tx(&qdo_full[st], LY::STAGE_BYTES + 2 * BM * 4);
+        mbar_arrive_expect_tx(&r_full[st], LY::TILE_BYTES + BM * 4);
         for (int c = 0; c < HD / 64; ++c)
-          tma_load_3d(sbase + c * BM * 128, mfull, &qdo_full[st], c * 64, qrow0 + q0, qzb + h);
-        for (int c = 0; c < 2; ++c)
-          tma_load_3d(sbase + LY::FULL_BYTES + c * BM * 128, mhalf, &qdo_full[st],
-                      (half_c0 + c) * 64, qrow0 + q0, qzb + h);
-        bulk_load(smem + LY::OFF_L + st * BM * 4, p.lse2 + (size_t)bh * p.ql_pad + q0, BM * 4,
-                  &qdo_full[st]);
-        bulk_load(smem + LY::OFF_D + st * BM * 4, p.dvec + (size_t)bh * p.ql_pad + q0, BM * 4,
-                  &qdo_full[st]);
+          tma_load_3d(smem + LY::OFF_R + st * LY::TILE_BYTES + c * BM * 128, msecond, &r_full[st],
+                      c * 64, qrow0 + q0, qzb + h);
+        bulk_load(smem + LY::OFF_LD + st * BM * 4, ld_src + (size_t)bh * p.ql_pad + q0, BM * 4,
+                  &r_full[st]);
         last_use[st] = it;
       }
-      mbar_wait_drain(&kv_full, 0);
       for (int s = 0; s < ST; ++s)
-        if (last_use[s] >= 0) mbar_wait_drain(&qdo_full[s], (last_use[s] / ST) & 1);
+        if (last_use[s] >= 0) mbar_wait_drain(&r_full[s], (last_use[s] / ST) & 1);
     }
   } else if (warp == LY::MMA_WARP) {
     // ------------------------------------------------------------------ MMA issuer
-    // Three groups per iteration it, issued in dependence order but interleaved across
-    // iterations by polling: X(it) = S^T (rank 0) or dP^T (rank 1) into TMEM buffer it % 2;
-    // V(it) = dV half (rank 0: A = P^T in TMEM; rank 1: A = P^T in the exchange buffer);
-    // K(it) = dK half (rank 0: A = dS^T in the exchange buffer; rank 1: A = dS^T in TMEM) and,
-    // on rank 0, dQ^T. Conditions: X(i) needs its Q/dO stage and its TMEM buffer free (rank 0:
-    // V(i-2) issued; rank 1: K(i-2) issued: MMAs of one thread run in issue order); V(i) needs
-    // X(i) issued and P^T(i); K(i) needs V(i) issued (so that the stage-release commit after it
-    // covers every reader of the stage) and dS^T(i), and dQ(i) the drain of dQ(i-1).
+    // Groups of iteration it: X(it) = S^T (rank 0) or dP^T (rank 1) into TMEM buffer it % 2;
+    // A(it) = dV += P^T dO (rank 0) or dK += dS^T Q (rank 1), A from this rank's TMEM; on rank 0
+    // Q(it) = dQ^T from dS^T in the exchange buffer. X(i) needs its stage and its TMEM buffer
+    // (A(i - 2) issued: MMAs of one thread run in issue order); A(i) needs X(i) issued and this
+    // rank's P^T / dS^T(i), and releases the stage; Q(i) needs dS^T(i) and the drain of Q(i-1).
     if (elect_one()) {
       const uint32_t sKV = smem_u32(smem + LY::OFF_KV);
       const Desc akv = make_desc(sKV, 16, 1024);          // K or V as a K-major operand
       const Desc kmn = make_desc(sKV, kBN * 128, 1024);   // K as an MN-major operand (dQ^T)
       const uint32_t id_x = idesc_bf16(128, BM, 0, 0);    // S^T, dP^T: [kv x q]
-      const uint32_t id_acc = idesc_bf16(128, 128, 0, 1); // dV, dK halves: B MN-major
+      const uint32_t id_acc = idesc_bf16(128, HD, 0, 1);  // dV, dK: A tmem, B MN-major, N = 256
       const uint32_t id_dq = idesc_bf16(128, BM, 1, 1);   // dQ^T half: [d x q]
-      const uint32_t tDV = tbase + LY::COL_DV, tDK = tbase + LY::COL_DK;
+      const uint32_t tACC = tbase + LY::COL_ACC;
       bool ok = mbar_wait(&kv_full, 0, &wctl);
-      int nx = 0, nv = 0, nk = 0;
+      // (rank 0 runs the Q group in the deterministic mode too, without dQ MMAs: its commit
+      // still tells the P^T warps that the exchange buffer has been read back)
+      int nx = 0, na = 0, nq = rank == 0 ? 0 : n_iter;
       const bool every_poll = wctl.limit_ns < 100000ull;
       uint64_t t_idle = 0;
       uint32_t spins = 0;
-      while (ok && nk < n_iter) {
+      while (ok && (na < n_iter || nq < n_iter)) {
         bool progressed = false;
-        // ---- K(nk): dK half (+ dQ^T on rank 0)
-        if (nk < nv) {
-          const int bb = nk & 1;
-          const uint32_t ph = (nk >> 1) & 1;
-          bool ready = rank == 0 ? mbar_test_wait_cluster(&x_ready[bb], ph)
-                                 : mbar_test_wait(&own_ready[bb], ph);
-          if (ready && do_dq && nk > 0) ready = mbar_test_wait(&dq_free, (nk - 1) & 1);
+        // ---- Q(nq) (rank 0): dQ^T = K^T dS^T, two 128-row halves of d
+        if (nq < n_iter && nq < na) {
+          const int bb = nq & 1;
+          bool ready = mbar_test_wait_cluster(&x_ready[bb], (nq >> 1) & 1);
+          if (ready && do_dq && nq > 0) ready = mbar_test_wait(&dq_free, (nq - 1) & 1);
           if (ready) {
             tc_fence_after();
             fence_proxy_async();
-            const int st = nk % ST;
-            const uint32_t sst = smem_u32(smem + LY::OFF_ST + st * LY::STAGE_BYTES);
-            if (rank == 0) {
-              // dK[:, 0:128] += dS^T Q[:, 0:128]: A = dS^T (exchange buffer, K-major), B = Q
-              // half (MN-major: the first two chunks of the stage's Q tile)
-              const Desc dsk = make_desc(x_local + bb * LY::X_BYTES, 16, 1024);
-              const Desc qmn = make_desc(sst, BM * 128, 1024);
-#pragma unroll
-              for (int ks = 0; ks < BM / 16; ++ks)
-                mma_ss2(tDK, dsk.at(ks * 32), dsk.hi, qmn.at(ks * 2048), qmn.hi, id_acc,
-                        (nk > 0 || ks > 0) ? 1u : 0u);
-            } else {
-              // dK[:, 128:256] += dS^T Q[:, 128:256]: A = dS^T (TMEM), B = the stage's Q half
-              const Desc qmn = make_desc(sst + LY::FULL_BYTES, BM * 128, 1024);
-              const uint32_t tX = tbase + LY::COL_X0 + bb * BM;
-#pragma unroll
-              for (int ks = 0; ks < BM / 16; ++ks)
-                mma_ts2(tDK, tX + ks * 8, qmn.at(ks * 2048), qmn.hi, id_acc,
-                        (nk > 0 || ks > 0) ? 1u : 0u);
-            }
-            mma_commit(&qdo_empty[st]);
             if (do_dq) {
-              // dQ^T[d, q] = sum_kv K[kv, d] dS^T[kv, q], two 128-row halves of d
               const Desc dsn = make_desc(x_local + bb * LY::X_BYTES, kBN * 128, 1024);
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
                 for (int ks = 0; ks < kBN / 16; ++ks)
-                  mma_ss2(tbase + LY::COL_DQ + hh * BM, kmn.at(2 * hh * (kBN * 128) + ks * 2048),
-                          kmn.hi, dsn.at(ks * 2048), dsn.hi, id_dq, ks > 0 ? 1u : 0u);
+                  mma_ss2(tbase + LY::COL_DQ + hh * BM,
+                          kmn.at(2 * hh * (kBN * 128) + ks * 2048), kmn.hi, dsn.at(ks * 2048),
+                          dsn.hi, id_dq, ks > 0 ? 1u : 0u);
               mma_commit(&dq_full);
             }
             mma_commit(&x_done[bb]);
-            ++nk;
+            ++nq;
             progressed = true;
           }
         }
         // ---- X(nx): S^T (rank 0) or dP^T (rank 1)
-        if (nx < n_iter && nx <= (rank == 0 ? nv : nk) + 1 &&
-            mbar_test_wait(&qdo_full[nx % ST], (nx / ST) & 1)) {
+        if (nx < n_iter && nx <= na + 1 && mbar_test_wait(&f_full, nx & 1)) {
           tc_fence_after();
-          const Desc bd = make_desc(smem_u32(smem + LY::OFF_ST + (nx % ST) * LY::STAGE_BYTES), 16,
-                                    1024);  // Q (rank 0) or dO (rank 1), K-major
+          const Desc bd = make_desc(smem_u32(smem + LY::OFF_F), 16, 1024);  // Q or dO, K-major
           const uint32_t tX = tbase + LY::COL_X0 + (nx & 1) * BM;
 #pragma unroll
           for (int ks = 0; ks < HD / 16; ++ks) {
@@ -290,41 +277,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
             mma_ss2(tX, akv.at(ko), akv.hi, bd.at(qo), bd.hi, id_x, ks > 0 ? 1u : 0u);
           }
           mma_commit(&mine_full[nx & 1]);
+          mma_commit(&f_empty);  // ring F is free once this MMA has read it
           ++nx;
           progressed = true;
         }
-        // ---- V(nv): dV half
-        if (nv < nx) {
-          const int bb = nv & 1;
-          const uint32_t ph = (nv >> 1) & 1;
-          const bool ready = rank == 0 ? mbar_test_wait(&own_ready[bb], ph)
-                                       : mbar_test_wait_cluster(&x_ready[bb], ph);
-          if (ready) {
-            tc_fence_after();
-            fence_proxy_async();
-            const int st = nv % ST;
-            const uint32_t sst = smem_u32(smem + LY::OFF_ST + st * LY::STAGE_BYTES);
-            if (rank == 0) {
-              // dV[:, 0:128] += P^T dO[:, 0:128]: A = P^T (TMEM), B = the stage's dO half
-              const Desc dmn = make_desc(sst + LY::FULL_BYTES, BM * 128, 1024);
-              const uint32_t tX = tbase + LY::COL_X0 + bb * BM;
+        // ---- A(na): dV (rank 0) or dK (rank 1), accumulated over every iteration
+        if (na < nx && mbar_test_wait(&own_ready[na & 1], (na >> 1) & 1) &&
+            mbar_test_wait(&r_full[na % ST], (na / ST) & 1)) {
+          tc_fence_after();
+          const int st = na % ST;
+          // B = dO (rank 0) or Q (rank 1) from ring R, MN-major, N = 256
+          const Desc bmn = make_desc(smem_u32(smem + LY::OFF_R + st * LY::TILE_BYTES), BM * 128,
+                                     1024);
+          const uint32_t tX = tbase + LY::COL_X0 + (na & 1) * BM;
 #pragma unroll
-              for (int ks = 0; ks < BM / 16; ++ks)
-                mma_ts2(tDV, tX + ks * 8, dmn.at(ks * 2048), dmn.hi, id_acc,
-                        (nv > 0 || ks > 0) ? 1u : 0u);
-            } else {
-              // dV[:, 128:256] += P^T dO[:, 128:256]: A = P^T (exchange buffer, K-major),
-              // B = chunks 2, 3 of the stage's dO tile (MN-major)
-              const Desc pk = make_desc(x_local + bb * LY::X_BYTES, 16, 1024);
-              const Desc dmn = make_desc(sst + 2 * (BM * 128), BM * 128, 1024);
-#pragma unroll
-              for (int ks = 0; ks < BM / 16; ++ks)
-                mma_ss2(tDV, pk.at(ks * 32), pk.hi, dmn.at(ks * 2048), dmn.hi, id_acc,
-                        (nv > 0 || ks > 0) ? 1u : 0u);
-            }
-            ++nv;
-            progressed = true;
-          }
+          for (int ks = 0; ks < BM / 16; ++ks)
+            mma_ts2(tACC, tX + ks * 8, bmn.at(ks * 2048), bmn.hi, id_acc,
+                    (na > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(&r_empty[st]);  // ring R's last reader on this rank
+          ++na;
+          progressed = true;
         }
         if (progressed) {
           spins = 0;
@@ -347,62 +319,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
       mma_commit(&mma_drain);
       mbar_wait_drain(&mma_drain, 0);
     }
-  } else if (warp == LY::BULK_WARP && rank == 1) {
-    // ------------------------------------------------------------------ rank 1: releases
-    // Once rank 1's MMAs of iteration it have read its exchange buffer it % 2 (P^T(it), for dV),
-    // the buffer may receive P^T(it + 2): arm that phase, then tell rank 0.
-    if (elect_one()) {
-      const uint32_t free_peer = mapa_shared(smem_u32(&x_free[0]), peer);
-      for (int it = 0; it + 2 < n_iter; ++it) {
-        if (!mbar_wait(&x_done[it & 1], (it >> 1) & 1, &wctl)) break;
-        mbar_arrive_expect_tx(&x_ready[it & 1], LY::X_BYTES);
-        mbar_arrive_remote(free_peer + (it & 1) * 8);
-      }
-    }
-  } else if (warp == LY::BULK_WARP) {
-    // ------------------------------------------------------------------ bulk dQ reductions
-    if (do_dq && elect_one()) {
-      const float* stg = reinterpret_cast<const float*>(smem + LY::OFF_STG);
-      for (int it = 0; it < n_iter; ++it) {
-        const int h = kh * G + it / nm;
-        const int q0 = (m_first + it % nm) * BM;
-        const int bh = b * p.H + h;
-        bool ok = true;
-        for (int hh = 0; hh < 2 && ok; ++hh) {
-          const int k = 2 * it + hh;
-          ok = mbar_wait(&stg_full, k & 1, &wctl);
-          if (!ok) break;
-          bulk_reduce_add_f32(p.dqacc + ((size_t)bh * p.ql_pad + q0) * HD + hh * 128 * BM, stg,
-                              128 * BM * 4);
-          bulk_commit();
-          bulk_wait_read<0>();  // the staging tile has been read
-          mbar_arrive(&stg_free);
-        }
-        if (!ok) break;
-      }
-      bulk_wait<0>();  // every reduction has landed before the CTA exits
-    }
   } else if (warp == LY::LINK_WARP) {
     // ------------------------------------------------------------------ sending staged tiles
-    // Rank 0 sends P^T(it) from its exchange buffer it % 2 (dS^T(it) from rank 1 lands there
-    // afterwards: rank 1 answers only once P^T(it) has arrived) into rank 1's buffer, once rank 1
-    // has freed it, after arming its own phase for the answer. Rank 1 sends dS^T(it) from its
-    // staging tile; rank 0 has armed the phase before it sent P^T(it), and the staging tile is
-    // not rewritten before rank 0 has consumed this one (rank 1 rewrites it only after P^T(it+2)
-    // arrives, which rank 0 sends only after its MMAs have read dS^T(it)).
     if (elect_one()) {
       const uint32_t x_peer = mapa_shared(x_local, peer);
       const uint32_t ready_peer = mapa_shared(smem_u32(&x_ready[0]), peer);
-      const uint8_t* src0 = smem + (rank == 0 ? LY::OFF_X : LY::OFF_STG);
       for (int it = 0; it < n_iter; ++it) {
         const int bb = it & 1;
         if (!mbar_wait(&out_staged[bb], (it >> 1) & 1, &wctl)) break;
-        if (rank == 0) {
-          if (it >= 2 && !mbar_wait_cluster(&x_free[bb], ((it - 2) >> 1) & 1, &wctl)) break;
-          mbar_arrive_expect_tx(&x_ready[bb], LY::X_BYTES);  // for dS^T(it)
-        }
-        bulk_copy_to_peer(x_peer + bb * LY::X_BYTES, src0 + bb * LY::X_BYTES, LY::X_BYTES,
-                          ready_peer + bb * 8);
+        if (rank == 0)
+          mbar_arrive_expect_tx(&x_ready[bb], LY::X_BYTES);  // dS^T(it) will come back
+        else if (it + 2 < n_iter)
+          mbar_arrive_expect_tx(&x_ready[bb], LY::X_BYTES);  // P^T(it + 2) may follow
+        bulk_copy_to_peer(x_peer + bb * LY::X_BYTES, smem + LY::OFF_X + bb * LY::X_BYTES,
+                          LY::X_BYTES, ready_peer + bb * 8);
         *reinterpret_cast<volatile uint32_t*>(&n_sent) = it + 1;
       }
     }
@@ -417,8 +347,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
       const int st = it % ST;
       const int bb = it & 1;
       const uint32_t colX = LY::COL_X0 + bb * BM;
+      uint8_t* xrow = smem + LY::OFF_X + bb * LY::X_BYTES + j * 128;
       uint32_t pk[BM / 2];  // this row's 64 bf16 results as packed pairs
-      ok = __all_sync(0xffffffffu, mbar_wait(&qdo_full[st], (it / ST) & 1, &wctl));
+      ok = __all_sync(0xffffffffu, mbar_wait(&r_full[st], (it / ST) & 1, &wctl));
       if (ok)
         ok = __all_sync(0xffffffffu, mbar_wait(&mine_full[bb], (it >> 1) & 1, &wctl));
       if (rank == 0) {
@@ -442,7 +373,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
         }
         if (!ok) break;
         tc_fence_after();
-        const float4* sL4 = reinterpret_cast<const float4*>(smem + LY::OFF_L + st * BM * 4);
+        const float4* sL4 = reinterpret_cast<const float4*>(smem + LY::OFF_LD + st * BM * 4);
         const float c2 = p.scale_log2;
         const uint64_t c2v = f2_pack(c2, c2);
         uint32_t rs[2][32];
@@ -485,17 +416,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
             pk[c32 * 16 + 2 * e4 + 1] = pack_bf16(p2, p3);
           }
         }
+        // P^T to TMEM first (this rank's dV and the release of its stage need only that),
+        // then to the exchange buffer, which holds dS^T(it - 2) until the dQ MMAs have read it
+        tmem_st16(lane_base + colX, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+        tmem_st16(lane_base + colX + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&own_ready[bb]);
+        if (it >= 2) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&x_done[bb], ((it - 2) >> 1) & 1, &wctl));
+          if (!ok) break;
+        }
       } else {
         // dS^T(it) = P^T(it) o (dP^T(it) - D): P^T from the exchange buffer (written by rank 0)
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(&x_ready[bb], (it >> 1) & 1, &wctl));
         if (!ok) break;
         tc_fence_after();
-        const float4* sD4 = reinterpret_cast<const float4*>(smem + LY::OFF_D + st * BM * 4);
+        const float4* sD4 = reinterpret_cast<const float4*>(smem + LY::OFF_LD + st * BM * 4);
         uint32_t rd[2][32];
         tmem_ld32(lane_base + colX, rd[0]);
         tmem_ld32(lane_base + colX + 32, rd[1]);
         uint32_t rp[BM / 2];  // P^T bf16 pairs of this row
-        const uint8_t* xrow = smem + LY::OFF_X + bb * LY::X_BYTES + j * 128;
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           const uint4 v = *reinterpret_cast<const uint4*>(xrow + ((g ^ (j & 7)) << 4));
@@ -533,29 +474,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
           }
         }
       }
-      // stage row j of the outgoing tile (rank 0: into its exchange buffer bb, once its MMAs
-      // have read dS^T(it - 2) there; rank 1: into its staging tile bb) for the link warp
-      if (rank == 0 && it >= 2) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&x_done[bb], ((it - 2) >> 1) & 1, &wctl));
-        if (!ok) break;
-      }
-      uint8_t* orow = smem + (rank == 0 ? LY::OFF_X : LY::OFF_STG) + bb * LY::X_BYTES + j * 128;
+      // the outgoing tile: row j of the exchange buffer (rank 1: over its own P^T(it) row,
+      // already read), sent by the link warp
 #pragma unroll
       for (int g = 0; g < 8; ++g)
-        *reinterpret_cast<uint4*>(orow + ((g ^ (j & 7)) << 4)) =
+        *reinterpret_cast<uint4*>(xrow + ((g ^ (j & 7)) << 4)) =
             make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
       fence_proxy_async();  // generic writes -> visible to the bulk copy
       mbar_arrive(&out_staged[bb]);
-      // this CTA's own copy as bf16 over the fp32 tile in TMEM: A operand of its dV (rank 0)
-      // or dK (rank 1) MMA
-      tmem_st16(lane_base + colX, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
-      tmem_st16(lane_base + colX + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&own_ready[bb]);
+      if (rank == 1) {
+        // dS^T as bf16 over dP^T in TMEM: A operand of this rank's dK MMA
+        tmem_st16(lane_base + colX, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+        tmem_st16(lane_base + colX + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&own_ready[bb]);
+      }
     }
 
-    // ---------------------------------------------------------------- dK, dV epilogue
+    // ---------------------------------------------------------------- dV (0) / dK (1) epilogue
     bool have = false;
     if (ok) {
       ok = __all_sync(0xffffffffu, mbar_wait(&acc_full, 0, &wctl));
@@ -563,38 +500,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
       have = ok && n_iter > 0;
     }
     const size_t kvrow = kvrow0 + (kv < kl ? kv : 0);
+    const float mul = rank == 0 ? 1.0f : p.scale;
+    __nv_bfloat16* out = (rank == 0 ? p.dv : p.dk) + kvrow * HD;
 #pragma unroll 1
-    for (int which = 0; which < 2; ++which) {
-      const uint32_t col = which == 0 ? LY::COL_DV : LY::COL_DK;
-      const float mul = which == 0 ? 1.0f : p.scale;
-      __nv_bfloat16* out =
-          (which == 0 ? p.dv : p.dk) + kvrow * HD + rank * (HD / 2);  // this rank's half
-#pragma unroll 1
-      for (int c = 0; c < HD / 2; c += 32) {
-        uint32_t r[32];
-        if (have) {
-          tmem_ld32(lane_base + col + c, r);
-          tmem_wait_ld();
-        }
-        uint32_t pkk[16];
+    for (int c = 0; c < HD; c += 32) {
+      uint32_t r[32];
+      if (have) {
+        tmem_ld32(lane_base + LY::COL_ACC + c, r);
+        tmem_wait_ld();
+      }
+      uint32_t pkk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pkk[e] = have ? pack_bf16(__uint_as_float(r[2 * e]) * mul,
-                                    __uint_as_float(r[2 * e + 1]) * mul)
-                        : 0u;
-        if (kv < kl) {
-          uint4* dst = reinterpret_cast<uint4*>(out + c);
+      for (int e = 0; e < 16; ++e)
+        pkk[e] = have ? pack_bf16(__uint_as_float(r[2 * e]) * mul,
+                                  __uint_as_float(r[2 * e + 1]) * mul)
+                      : 0u;
+      if (kv < kl) {
+        uint4* dst = reinterpret_cast<uint4*>(out + c);
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(pkk[4 * v4], pkk[4 * v4 + 1], pkk[4 * v4 + 2], pkk[4 * v4 + 3]);
-        }
+        for (int v4 = 0; v4 < 4; ++v4)
+          dst[v4] = make_uint4(pkk[4 * v4], pkk[4 * v4 + 1], pkk[4 * v4 + 2], pkk[4 * v4 + 3]);
       }
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------------ rank 0: dQ^T drain
-    // lane = head-dim row within a 128-row half, column = query row. Each half is staged as
-    // 128 rows of 64 f32 with the 16-byte chunks of row d XOR-rotated by (d & 15), the
-    // accumulator's tile layout; the bulk warp adds it with one reduction.
+    // lane = head-dim row d within a 128-row half, column = query row. Each half is staged as
+    // 128 rows of 64 f32 with the 16-byte chunk c (query rows 4c .. 4c+3) of row d at chunk
+    // position c ^ (d & 15) -- the accumulator's tile layout, which the dQ convert kernel reads
+    // -- and the bulk warp adds it with one reduction. (One 16-byte vector reduction per chunk
+    // from every thread instead measured ~2.3 us per tile, the slowest step of an iteration.)
     if (do_dq) {
       const int j = (warp - 4) * 32 + lane;
       const uint32_t lane_base = tbase + ((uint32_t)((warp - 4) * 32) << 16);
@@ -610,7 +544,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
           tmem_ld32(lane_base + LY::COL_DQ + hh * BM, rq[0]);
           tmem_ld32(lane_base + LY::COL_DQ + hh * BM + 32, rq[1]);
           tmem_wait_ld();
-          if (hh == 1) {  // both halves are in registers: the TMEM tile is free
+          if (hh == 1) {  // both halves read: the TMEM tile is free for the next dQ^T
             tc_fence_before();
             mbar_arrive(&dq_free);
           }
@@ -620,7 +554,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
           }
           float4* row = reinterpret_cast<float4*>(stg + j * BM);
 #pragma unroll
-          for (int c = 0; c < BM / 4; ++c) {  // chunk c: query rows 4c .. 4c+3
+          for (int c = 0; c < BM / 4; ++c) {
             const uint32_t* r = &rq[c / 8][(c % 8) * 4];
             row[c ^ (j & (kDqChunks - 1))] =
                 make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]),
@@ -630,6 +564,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
           mbar_arrive(&stg_full);
         }
       }
+    }
+  } else if (warp == LY::BULK_WARP) {
+    // ------------------------------------------------------------------ rank 0: dQ reductions
+    if (do_dq && elect_one()) {
+      const float* stg = reinterpret_cast<const float*>(smem + LY::OFF_STG);
+      for (int it = 0; it < n_iter; ++it) {
+        const int h = kh * G + it / nm;
+        const int q0 = (m_first + it % nm) * BM;
+        const int bh = b * p.H + h;
+        bool ok = true;
+        for (int hh = 0; hh < 2 && ok; ++hh) {
+          ok = mbar_wait(&stg_full, (2 * it + hh) & 1, &wctl);
+          if (!ok) break;
+          bulk_reduce_add_f32(p.dqacc + ((size_t)bh * p.ql_pad + q0) * HD + hh * 128 * BM, stg,
+                              128 * BM * 4);
+          bulk_commit();
+          bulk_wait_read<0>();  // the staging tile has been read
+          mbar_arrive(&stg_free);
+        }
+        if (!ok) break;
+      }
+      bulk_wait<0>();  // every reduction has landed before the CTA exits
     }
   }
 
