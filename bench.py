@@ -54,6 +54,18 @@ KERNEL_SOURCES = {
     "paged_attn_kernel": ["flash_attention_gb300/csrc/fa_paged.cu",
                           "flash_attention_gb300/csrc/fa_common.cuh"],
 }
+# at head_dim 256 the backward main pass is the CTA-pair kernel (timed under the same name)
+PAIR_SOURCES = ["flash_attention_gb300/csrc/fa_bwd_pair.cu",
+                "flash_attention_gb300/csrc/fa_bwd_common.cuh",
+                "flash_attention_gb300/csrc/fa_common.cuh"]
+
+
+def kernel_sources(kernel, workload):
+    """Source files whose hash dates a traffic figure of `kernel` on `workload`."""
+    w = fa_inputs.BY_NAME.get(workload)
+    if kernel == "bwd_main_kernel" and w is not None and w.head_dim == 256:
+        return PAIR_SOURCES
+    return KERNEL_SOURCES.get(kernel, [])
 
 
 def kernel_flops(w):
@@ -189,7 +201,7 @@ def recorded_traffic(kernel, workload):
     with open(path) as f:
         rec = json.load(f)
     e = rec.get(kernel, {}).get(workload)
-    if not e or e.get("source_hash") != source_hash(KERNEL_SOURCES.get(kernel, [])):
+    if not e or e.get("source_hash") != source_hash(kernel_sources(kernel, workload)):
         return None
     return e.get("dram_bytes_per_launch")
 
