@@ -13,8 +13,14 @@
 // one CTA. Two CTAs that each owned one half of the head dimension would both have to form S^T
 // and dP^T (2 of the 5 contractions twice), with K, V, Q and dO filling their shared memory.
 // Here the two CTAs of a cluster split the work by what they multiply:
-//   rank 0 holds K: S^T, P^T, all of dV (A = its own P^T in TMEM) and all of dQ^T;
-//   rank 1 holds V: dP^T, dS^T and all of dK (A = its own dS^T in TMEM).
+//   rank 0 holds K: S^T, P^T, all of dV (A = its own P^T in TMEM) and head-dim rows 0-127
+//   of dQ^T;
+//   rank 1 holds V and the upper half of K: dP^T, dS^T, all of dK (A = its own dS^T in TMEM)
+//   and head-dim rows 128-255 of dQ^T.
+// The dQ^T split matters because one SM pushes only ~30-50 GB/s of f32 reductions towards L2
+// (measured on a GB300 with 38, 76 and 152 SMs pushing at once: the rate per SM is the same).
+// With all 64 KB of a step's dQ^T on rank 0, that push, not the tensor core, set the step
+// time.
 // The two tiles each rank needs from the other travel through shared memory: rank 0 stages
 // P^T in its exchange buffer and sends it with one bulk copy (cp.async.bulk shared::cta to
 // shared::cluster) that completes a transaction on rank 1's barrier; rank 1 computes dS^T,
@@ -22,15 +28,17 @@
 // their rows into the other CTA directly measured 1.3-2 us per tile.) Each rank's Q/dO stage is
 // read only by its own MMAs, so rank 0 frees it once dV is issued, without waiting for rank 1.
 // Buffer reuse follows from the order of the exchange: rank 0 stages P^T(it + 2) in its buffer
-// only after its dQ MMAs have read dS^T(it) there, which also means rank 1's copy of dS^T(it)
-// (and so rank 1's use of its own buffer) is complete before P^T(it + 2) can arrive.
+// only after its dQ MMAs have read dS^T(it) there. Rank 1 sends dS^T(it) only after its own dQ
+// MMAs have read it from its buffer. So both of rank 1's uses of the buffer are complete
+// before P^T(it + 2) can arrive.
 //
 // Roles (384 threads): warps 0-3 compute P^T (rank 0) or dS^T (rank 1), one kv row per thread
-// (= TMEM lane), and write that rank's dV or dK at the end; warps 4-7 (rank 0) stage dQ^T from
-// TMEM for warp 11, which adds it to the f32 accumulator with bulk reductions; warp 8 issues
-// the TMA loads (one lane per ring); warp 9 issues the MMAs, polling the barriers of its rank's
-// MMA groups so that whichever is ready goes first; warp 10 sends the staged tiles. Every wait
-// is bounded.
+// (= TMEM lane), and write that rank's dV or dK at the end. Warps 4-7 drain this rank's half of
+// dQ^T from TMEM. On rank 0 they stage it for warp 11, which adds it to the f32 accumulator
+// with a bulk reduction. On rank 1, whose shared memory holds the K half instead of a staging
+// tile, they add it with 16-byte vector reductions. Warp 8 issues the TMA loads (one lane per
+// ring). Warp 9 issues the MMAs, polling the barriers of its rank's MMA groups so that
+// whichever is ready goes first. Warp 10 sends the staged tiles. Every wait is bounded.
 #include "fa_bwd_common.cuh"
 
 namespace fa {
@@ -47,6 +55,7 @@ struct PairLayout {
   static constexpr int TILE_BYTES = kPM * kPD * 2;  // one 64 x 256 bf16 tile, 32 KB
   static constexpr int X_BYTES = kBN * kPM * 2;     // a [kv][q] bf16 exchange tile, 16 KB
   static constexpr int STG_BYTES = 128 * kPM * 4;   // rank 0: half a dQ^T tile in f32, 32 KB
+  static constexpr int KH_BYTES = kBN * 128 * 2;     // rank 1: K columns 128-255, 32 KB
   // Two rings with the lifetimes of their operands: F holds the tile that only S^T / dP^T read
   // (rank 0: Q; rank 1: dO), freed as soon as that MMA completes, so one stage suffices; R
   // holds the tile that dV / dK read (rank 0: dO; rank 1: Q) and the row vector the P^T / dS^T
@@ -55,13 +64,13 @@ struct PairLayout {
   static constexpr int OFF_F = OFF_KV + KV_BYTES;           // 1 stage
   static constexpr int OFF_R = OFF_F + TILE_BYTES;          // kPST stages
   static constexpr int OFF_X = OFF_R + kPST * TILE_BYTES;   // 2 exchange buffers
-  static constexpr int OFF_STG = OFF_X + 2 * X_BYTES;       // rank 0: dQ^T staging
+  static constexpr int OFF_STG = OFF_X + 2 * X_BYTES;       // rank 0: dQ^T staging; rank 1: K half
   static constexpr int OFF_LD = OFF_STG + STG_BYTES;        // kPST x kPM f32 (ring R)
   static constexpr int OFF_END = OFF_LD + kPST * kPM * 4;
   static constexpr int SMEM_BYTES = OFF_END + 1024;
   // TMEM columns: two 64-column buffers (rank 0: S^T then P^T as bf16; rank 1: dP^T then dS^T),
-  // rank 0's dQ^T (two 128-row halves of 64 columns), and the 256-column accumulator (rank 0:
-  // dV; rank 1: dK).
+  // two 64-column buffers for this rank's 128-row half of dQ^T (one per step parity), and the
+  // 256-column accumulator (rank 0: dV; rank 1: dK).
   static constexpr int COL_X0 = 0;
   static constexpr int COL_DQ = 128;
   static constexpr int COL_ACC = 256;
@@ -69,6 +78,7 @@ struct PairLayout {
   static constexpr int THREADS = 384;
   static constexpr int TMA_WARP = 8, MMA_WARP = 9, LINK_WARP = 10, BULK_WARP = 11;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static_assert(KH_BYTES == STG_BYTES, "rank 1 keeps its K half where rank 0 stages dQ^T");
   static_assert(kPM / 4 == kDqChunks, "dQ^T tile layout of the accumulator");
 };
 
@@ -90,7 +100,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
   __shared__ uint64_t x_ready[2];     // the peer's tile has landed in x buffer (bulk-copy bytes)
   __shared__ uint64_t x_done[2];      // rank 0: its dQ MMAs have read dS^T in x buffer
   __shared__ uint64_t out_staged[2];  // 128 arrivals: this rank's outgoing tile is in x buffer
-  __shared__ uint64_t dq_full, dq_free, stg_full, stg_free, acc_full, mma_drain;
+  __shared__ uint64_t dq_full[2], dq_free[2];  // this rank's dQ^T half in TMEM buffer it % 2
+  __shared__ uint64_t x1_read[2];              // rank 1: its dQ MMAs have read dS^T in x buffer
+  __shared__ uint64_t stg_full, stg_free, acc_full, mma_drain;
   __shared__ uint32_t n_sent;         // tiles sent to the peer (read by the peer at the end)
   __shared__ uint32_t tmem_base_s;
   __shared__ WaitCtl wctl;
@@ -125,7 +137,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
   bwd_mtile_range<HD, BAND>(n0, p, ql, kl, m_first, m_last);
   const int nm = m_last - m_first + 1;  // query tiles per head (0 if none)
   const int n_iter = G * nm;            // (head, query tile) pairs this pair of CTAs visits
-  const bool do_dq = rank == 0 && !p.skip_dq;
+  const bool do_dq = !p.skip_dq;  // both ranks form and add a half of dQ^T
 
   if (threadIdx.x == 0) {
     wait_ctl_init(&wctl, p.wait_limit_ns);
@@ -143,8 +155,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
       mbar_init(&x_done[s], 1);
       mbar_init(&out_staged[s], 128);
     }
-    mbar_init(&dq_full, 1);
-    mbar_init(&dq_free, 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&dq_full[s], 1);
+      mbar_init(&dq_free[s], 128);
+      mbar_init(&x1_read[s], 1);
+    }
     mbar_init(&stg_full, 128);
     mbar_init(&stg_free, 1);
     mbar_init(&acc_full, 1);
@@ -180,9 +195,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
       tma_prefetch_desc(&mK);
       tma_prefetch_desc(&mV);
       tma_prefetch_desc(&mDO);
-      mbar_arrive_expect_tx(&kv_full, LY::KV_BYTES);
+      const bool k_half = rank == 1 && do_dq;  // rank 1's dQ^T rows need K columns 128-255
+      mbar_arrive_expect_tx(&kv_full, LY::KV_BYTES + (k_half ? LY::KH_BYTES : 0));
       for (int c = 0; c < HD / 64; ++c)
         tma_load_3d(smem + LY::OFF_KV + c * kBN * 128, mkv, &kv_full, c * 64, krow0 + n0, kz);
+      if (k_half)
+        for (int c = 2; c < HD / 64; ++c)
+          tma_load_3d(smem + LY::OFF_STG + (c - 2) * kBN * 128, &mK, &kv_full, c * 64,
+                      krow0 + n0, kz);
       int loaded = 0;
       for (int it = 0; it < n_iter; ++it) {
         if (it >= 1 && !mbar_wait(&f_empty, (it - 1) & 1, &wctl)) break;
@@ -220,47 +240,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
   } else if (warp == LY::MMA_WARP) {
     // ------------------------------------------------------------------ MMA issuer
     // Groups of iteration it: X(it) = S^T (rank 0) or dP^T (rank 1) into TMEM buffer it % 2;
-    // A(it) = dV += P^T dO (rank 0) or dK += dS^T Q (rank 1), A from this rank's TMEM; on rank 0
-    // Q(it) = dQ^T from dS^T in the exchange buffer. X(i) needs its stage and its TMEM buffer
-    // (A(i - 2) issued: MMAs of one thread run in issue order); A(i) needs X(i) issued and this
-    // rank's P^T / dS^T(i), and releases the stage; Q(i) needs dS^T(i) and the drain of Q(i-1).
+    // A(it) = dV += P^T dO (rank 0) or dK += dS^T Q (rank 1), A from this rank's TMEM;
+    // Q(it) = this rank's 128-row half of dQ^T from dS^T in exchange buffer it % 2 (rank 0: as
+    // received from rank 1; rank 1: its own, once staged). X(i) needs its stage and its TMEM
+    // buffer (A(i - 2) issued: MMAs of one thread run in issue order); A(i) needs X(i) issued
+    // and this rank's P^T / dS^T(i), and releases the stage; Q(i) needs dS^T(i) and the drain
+    // of Q(i - 2), which used the same TMEM buffer.
     if (elect_one()) {
       const uint32_t sKV = smem_u32(smem + LY::OFF_KV);
       const Desc akv = make_desc(sKV, 16, 1024);          // K or V as a K-major operand
-      const Desc kmn = make_desc(sKV, kBN * 128, 1024);   // K as an MN-major operand (dQ^T)
+      // K columns 0-127 (rank 0) or 128-255 (rank 1) as the MN-major A operand of dQ^T
+      const Desc kq = make_desc(rank == 0 ? sKV : smem_u32(smem + LY::OFF_STG), kBN * 128, 1024);
       const uint32_t id_x = idesc_bf16(128, BM, 0, 0);    // S^T, dP^T: [kv x q]
       const uint32_t id_acc = idesc_bf16(128, HD, 0, 1);  // dV, dK: A tmem, B MN-major, N = 256
-      const uint32_t id_dq = idesc_bf16(128, BM, 1, 1);   // dQ^T half: [d x q]
+      const uint32_t id_dq = idesc_bf16(128, BM, 1, 1);   // dQ^T half: [d x q], K = kv
       const uint32_t tACC = tbase + LY::COL_ACC;
       bool ok = mbar_wait(&kv_full, 0, &wctl);
       // (rank 0 runs the Q group in the deterministic mode too, without dQ MMAs: its commit
       // still tells the P^T warps that the exchange buffer has been read back)
-      int nx = 0, na = 0, nq = rank == 0 ? 0 : n_iter;
+      int nx = 0, na = 0, nq = (rank == 0 || do_dq) ? 0 : n_iter;
       const bool every_poll = wctl.limit_ns < 100000ull;
       uint64_t t_idle = 0;
       uint32_t spins = 0;
       while (ok && (na < n_iter || nq < n_iter)) {
         bool progressed = false;
-        // ---- Q(nq) (rank 0): dQ^T = K^T dS^T, two 128-row halves of d
-        if (nq < n_iter && nq < na) {
+        // ---- Q(nq): dQ^T rows of this rank's half = K^T dS^T
+        if (nq < n_iter && (rank == 1 || nq < na)) {
           const int bb = nq & 1;
-          bool ready = mbar_test_wait_cluster(&x_ready[bb], (nq >> 1) & 1);
-          if (ready && do_dq && nq > 0) ready = mbar_test_wait(&dq_free, (nq - 1) & 1);
+          bool ready = rank == 0 ? mbar_test_wait_cluster(&x_ready[bb], (nq >> 1) & 1)
+                                 : mbar_test_wait(&out_staged[bb], (nq >> 1) & 1);
+          if (ready && do_dq && nq >= 2)
+            ready = mbar_test_wait(&dq_free[bb], ((nq - 2) >> 1) & 1);
           if (ready) {
             tc_fence_after();
             fence_proxy_async();
             if (do_dq) {
               const Desc dsn = make_desc(x_local + bb * LY::X_BYTES, kBN * 128, 1024);
 #pragma unroll
-              for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                for (int ks = 0; ks < kBN / 16; ++ks)
-                  mma_ss2(tbase + LY::COL_DQ + hh * BM,
-                          kmn.at(2 * hh * (kBN * 128) + ks * 2048), kmn.hi, dsn.at(ks * 2048),
-                          dsn.hi, id_dq, ks > 0 ? 1u : 0u);
-              mma_commit(&dq_full);
+              for (int ks = 0; ks < kBN / 16; ++ks)
+                mma_ss2(tbase + LY::COL_DQ + bb * BM, kq.at(ks * 2048), kq.hi, dsn.at(ks * 2048),
+                        dsn.hi, id_dq, ks > 0 ? 1u : 0u);
+              mma_commit(&dq_full[bb]);
             }
-            mma_commit(&x_done[bb]);
+            // rank 0: the P^T warps may stage P^T(nq + 2) in this buffer; rank 1: the link
+            // warp may send dS^T(nq), after which P^T(nq + 2) can arrive in it
+            mma_commit(rank == 0 ? &x_done[bb] : &x1_read[bb]);
             ++nq;
             progressed = true;
           }
@@ -327,6 +351,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
       for (int it = 0; it < n_iter; ++it) {
         const int bb = it & 1;
         if (!mbar_wait(&out_staged[bb], (it >> 1) & 1, &wctl)) break;
+        // rank 1 reads dS^T(it) from this buffer for its own dQ MMAs: send it only once they
+        // have, so that P^T(it + 2), which rank 0 sends after receiving it, lands on a free
+        // buffer
+        if (rank == 1 && do_dq && !mbar_wait(&x1_read[bb], (it >> 1) & 1, &wctl)) break;
         if (rank == 0)
           mbar_arrive_expect_tx(&x_ready[bb], LY::X_BYTES);  // dS^T(it) will come back
         else if (it + 2 < n_iter)
@@ -523,33 +551,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
       }
     }
   } else if (warp < 8) {
-    // ------------------------------------------------------------------ rank 0: dQ^T drain
-    // lane = head-dim row d within a 128-row half, column = query row. Each half is staged as
-    // 128 rows of 64 f32 with the 16-byte chunk c (query rows 4c .. 4c+3) of row d at chunk
-    // position c ^ (d & 15) -- the accumulator's tile layout, which the dQ convert kernel reads
-    // -- and the bulk warp adds it with one reduction. (One 16-byte vector reduction per chunk
-    // from every thread instead measured ~2.3 us per tile, the slowest step of an iteration.)
+    // ------------------------------------------------------------------ dQ^T drain
+    // lane = head-dim row d within this rank's 128-row half, column = query row. The
+    // accumulator keeps each (head, query tile) as 256 rows of 64 f32, with the 16-byte chunk c
+    // (query rows 4c .. 4c+3) of row d at chunk position c ^ (d & 15); the dQ convert kernel
+    // reads that layout. Rank 0 stages its half in that layout and the bulk warp adds it with
+    // one reduction. Rank 1 has no staging tile (its shared memory holds the K half) and adds
+    // each chunk with a 16-byte vector reduction.
     if (do_dq) {
       const int j = (warp - 4) * 32 + lane;
       const uint32_t lane_base = tbase + ((uint32_t)((warp - 4) * 32) << 16);
       float* stg = reinterpret_cast<float*>(smem + LY::OFF_STG);
       bool ok = true;
       for (int it = 0; it < n_iter && ok; ++it) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&dq_full, it & 1, &wctl));
+        const int bb = it & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[bb], (it >> 1) & 1, &wctl));
         if (!ok) break;
         tc_fence_after();
-        for (int hh = 0; hh < 2; ++hh) {
-          const int k = 2 * it + hh;  // use of the staging tile
-          uint32_t rq[2][32];
-          tmem_ld32(lane_base + LY::COL_DQ + hh * BM, rq[0]);
-          tmem_ld32(lane_base + LY::COL_DQ + hh * BM + 32, rq[1]);
-          tmem_wait_ld();
-          if (hh == 1) {  // both halves read: the TMEM tile is free for the next dQ^T
-            tc_fence_before();
-            mbar_arrive(&dq_free);
-          }
-          if (k > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&stg_free, (k - 1) & 1, &wctl));
+        uint32_t rq[2][32];
+        tmem_ld32(lane_base + LY::COL_DQ + bb * BM, rq[0]);
+        tmem_ld32(lane_base + LY::COL_DQ + bb * BM + 32, rq[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&dq_free[bb]);  // the TMEM buffer may take dQ^T(it + 2)
+        if (rank == 0) {
+          if (it > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&stg_free, (it - 1) & 1, &wctl));
             if (!ok) break;
           }
           float4* row = reinterpret_cast<float4*>(stg + j * BM);
@@ -562,28 +589,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
           }
           fence_proxy_async();  // staging writes -> visible to the bulk copy
           mbar_arrive(&stg_full);
+        } else {
+          const int h = kh * G + it / nm;
+          const int q0 = (m_first + it % nm) * BM;
+          const int bh = b * p.H + h;
+          float4* arow = reinterpret_cast<float4*>(p.dqacc + ((size_t)bh * p.ql_pad + q0) * HD +
+                                                   (size_t)(128 + j) * BM);
+#pragma unroll
+          for (int c = 0; c < BM / 4; ++c) {
+            const uint32_t* r = &rq[c / 8][(c % 8) * 4];
+            atomicAdd(arow + (c ^ (j & (kDqChunks - 1))),
+                      make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]),
+                                  __uint_as_float(r[2]), __uint_as_float(r[3])));
+          }
         }
       }
     }
   } else if (warp == LY::BULK_WARP) {
     // ------------------------------------------------------------------ rank 0: dQ reductions
-    if (do_dq && elect_one()) {
+    if (rank == 0 && do_dq && elect_one()) {
       const float* stg = reinterpret_cast<const float*>(smem + LY::OFF_STG);
       for (int it = 0; it < n_iter; ++it) {
         const int h = kh * G + it / nm;
         const int q0 = (m_first + it % nm) * BM;
         const int bh = b * p.H + h;
-        bool ok = true;
-        for (int hh = 0; hh < 2 && ok; ++hh) {
-          ok = mbar_wait(&stg_full, (2 * it + hh) & 1, &wctl);
-          if (!ok) break;
-          bulk_reduce_add_f32(p.dqacc + ((size_t)bh * p.ql_pad + q0) * HD + hh * 128 * BM, stg,
-                              128 * BM * 4);
-          bulk_commit();
-          bulk_wait_read<0>();  // the staging tile has been read
-          mbar_arrive(&stg_free);
-        }
-        if (!ok) break;
+        if (!mbar_wait(&stg_full, it & 1, &wctl)) break;
+        bulk_reduce_add_f32(p.dqacc + ((size_t)bh * p.ql_pad + q0) * HD, stg, 128 * BM * 4);
+        bulk_commit();
+        bulk_wait_read<0>();  // the staging tile has been read
+        mbar_arrive(&stg_free);
       }
       bulk_wait<0>();  // every reduction has landed before the CTA exits
     }
