@@ -553,11 +553,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
   } else if (warp < 8) {
     // ------------------------------------------------------------------ dQ^T drain
     // lane = head-dim row d within this rank's 128-row half, column = query row. The
-    // accumulator keeps each (head, query tile) as 256 rows of 64 f32, with the 16-byte chunk c
-    // (query rows 4c .. 4c+3) of row d at chunk position c ^ (d & 15); the dQ convert kernel
-    // reads that layout. Rank 0 stages its half in that layout and the bulk warp adds it with
-    // one reduction. Rank 1 has no staging tile (its shared memory holds the K half) and adds
-    // each chunk with a 16-byte vector reduction.
+    // accumulator keeps each (head, query tile) as two chunk-major halves: the 16-byte chunk c
+    // (query rows 4c .. 4c+3) of row d at position (d / 128) * 2048 + c * 128 + d % 128, which
+    // the dQ convert kernel reads. Rank 0 stages its half in that layout (32 consecutive lanes
+    // store 512 contiguous bytes) and the bulk warp adds it with one reduction. Rank 1 has no
+    // staging tile (its shared memory holds the K half) and adds each chunk with a 16-byte
+    // vector reduction, a warp covering 512 contiguous bytes per instruction.
     if (do_dq) {
       const int j = (warp - 4) * 32 + lane;
       const uint32_t lane_base = tbase + ((uint32_t)((warp - 4) * 32) << 16);
@@ -579,13 +580,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
             ok = __all_sync(0xffffffffu, mbar_wait(&stg_free, (it - 1) & 1, &wctl));
             if (!ok) break;
           }
-          float4* row = reinterpret_cast<float4*>(stg + j * BM);
+          float4* s4 = reinterpret_cast<float4*>(stg);
 #pragma unroll
           for (int c = 0; c < BM / 4; ++c) {
             const uint32_t* r = &rq[c / 8][(c % 8) * 4];
-            row[c ^ (j & (kDqChunks - 1))] =
-                make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]),
-                            __uint_as_float(r[3]));
+            s4[c * 128 + j] = make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]),
+                                          __uint_as_float(r[2]), __uint_as_float(r[3]));
           }
           fence_proxy_async();  // staging writes -> visible to the bulk copy
           mbar_arrive(&stg_full);
@@ -593,12 +593,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
           const int h = kh * G + it / nm;
           const int q0 = (m_first + it % nm) * BM;
           const int bh = b * p.H + h;
-          float4* arow = reinterpret_cast<float4*>(p.dqacc + ((size_t)bh * p.ql_pad + q0) * HD +
-                                                   (size_t)(128 + j) * BM);
+          float4* half1 = reinterpret_cast<float4*>(p.dqacc + ((size_t)bh * p.ql_pad + q0) * HD) +
+                          128 * kDqChunks;
 #pragma unroll
           for (int c = 0; c < BM / 4; ++c) {
             const uint32_t* r = &rq[c / 8][(c % 8) * 4];
-            atomicAdd(arow + (c ^ (j & (kDqChunks - 1))),
+            atomicAdd(half1 + c * 128 + j,
                       make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]),
                                   __uint_as_float(r[2]), __uint_as_float(r[3])));
           }
