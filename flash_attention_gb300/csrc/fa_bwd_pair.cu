@@ -27,10 +27,10 @@
 // writes it over P^T in the same buffer and sends it back the same way. (128 threads storing
 // their rows into the other CTA directly measured 1.3-2 us per tile.) Each rank's Q/dO stage is
 // read only by its own MMAs, so rank 0 frees it once dV is issued, without waiting for rank 1.
-// Buffer reuse follows from the order of the exchange: rank 0 stages P^T(it + 2) in its buffer
-// only after its dQ MMAs have read dS^T(it) there. Rank 1 sends dS^T(it) only after its own dQ
-// MMAs have read it from its buffer. So both of rank 1's uses of the buffer are complete
-// before P^T(it + 2) can arrive.
+// Buffer reuse: rank 0 stages P^T(it + 2) in its buffer only after its dQ MMAs have read
+// dS^T(it) there. Rank 0 sends P^T(it + 2) into rank 1's buffer only after rank 1's dQ MMAs
+// have read dS^T(it) from it: rank 1 tells it with a remote arrive once they complete. Rank 1
+// read P^T(it) there before writing dS^T(it) over it, so the buffer is free.
 //
 // Roles (384 threads): warps 0-3 compute P^T (rank 0) or dS^T (rank 1), one kv row per thread
 // (= TMEM lane), and write that rank's dV or dK at the end. Warps 4-7 drain this rank's half of
@@ -101,7 +101,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
   __shared__ uint64_t x_done[2];      // rank 0: its dQ MMAs have read dS^T in x buffer
   __shared__ uint64_t out_staged[2];  // 128 arrivals: this rank's outgoing tile is in x buffer
   __shared__ uint64_t dq_full[2], dq_free[2];  // this rank's dQ^T half in TMEM buffer it % 2
-  __shared__ uint64_t x1_read[2];              // rank 1: its dQ MMAs have read dS^T in x buffer
+  __shared__ uint64_t peer_read[2];  // rank 0: rank 1's dQ MMAs have read dS^T in its x buffer
   __shared__ uint64_t stg_full, stg_free, acc_full, mma_drain;
   __shared__ uint32_t n_sent;         // tiles sent to the peer (read by the peer at the end)
   __shared__ uint32_t tmem_base_s;
@@ -158,7 +158,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
     for (int s = 0; s < 2; ++s) {
       mbar_init(&dq_full[s], 1);
       mbar_init(&dq_free[s], 128);
-      mbar_init(&x1_read[s], 1);
+      mbar_init(&peer_read[s], 1);
     }
     mbar_init(&stg_full, 128);
     mbar_init(&stg_free, 1);
@@ -282,9 +282,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
                         dsn.hi, id_dq, ks > 0 ? 1u : 0u);
               mma_commit(&dq_full[bb]);
             }
-            // rank 0: the P^T warps may stage P^T(nq + 2) in this buffer; rank 1: the link
-            // warp may send dS^T(nq), after which P^T(nq + 2) can arrive in it
-            mma_commit(rank == 0 ? &x_done[bb] : &x1_read[bb]);
+            // rank 0: the P^T warps may stage P^T(nq + 2) in this buffer (rank 1 learns that
+            // its buffer has been read from its drain warps, which wait for dq_full)
+            if (rank == 0) mma_commit(&x_done[bb]);
             ++nq;
             progressed = true;
           }
@@ -351,10 +351,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
       for (int it = 0; it < n_iter; ++it) {
         const int bb = it & 1;
         if (!mbar_wait(&out_staged[bb], (it >> 1) & 1, &wctl)) break;
-        // rank 1 reads dS^T(it) from this buffer for its own dQ MMAs: send it only once they
-        // have, so that P^T(it + 2), which rank 0 sends after receiving it, lands on a free
-        // buffer
-        if (rank == 1 && do_dq && !mbar_wait(&x1_read[bb], (it >> 1) & 1, &wctl)) break;
+        // rank 1 reads dS^T(it - 2) from the buffer P^T(it) lands in, for its own dQ MMAs
+        if (rank == 0 && do_dq && it >= 2 &&
+            !mbar_wait_cluster(&peer_read[bb], ((it - 2) >> 1) & 1, &wctl))
+          break;
         if (rank == 0)
           mbar_arrive_expect_tx(&x_ready[bb], LY::X_BYTES);  // dS^T(it) will come back
         else if (it + 2 < n_iter)
@@ -568,6 +568,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
         const int bb = it & 1;
         ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[bb], (it >> 1) & 1, &wctl));
         if (!ok) break;
+        // rank 1: its dQ MMAs have read dS^T(it) from its exchange buffer; rank 0 may send
+        // P^T(it + 2) into it
+        if (rank == 1 && threadIdx.x == 128)
+          mbar_arrive_remote(mapa_shared(smem_u32(&peer_read[bb]), 0));
         tc_fence_after();
         uint32_t rq[2][32];
         tmem_ld32(lane_base + LY::COL_DQ + bb * BM, rq[0]);
