@@ -61,23 +61,14 @@ bool encode_bf16_3d(CUtensorMap* m, const void* base, int bh, int rows, int d, i
 }
 
 // ---------------------------------------------------------------- per-device status word
-constexpr int kMaxDevices = 64;
-int* g_status[kMaxDevices] = {nullptr};
-std::mutex g_status_mu;
+// One int in this file's device code: CUDA creates it, zeroed, with the module on each device,
+// and again after a device reset. Its address is looked up on every call (cheap once the
+// module is loaded, and nothing to go stale), as the no-allocation scratch's is.
+__device__ int g_status_word;
 
 cudaError_t device_status_word(int dev, int** out) {
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lk(g_status_mu);
-  if (!g_status[dev]) {
-    int* p = nullptr;
-    cudaError_t e = cudaMalloc(&p, sizeof(int));
-    if (e != cudaSuccess) return e;
-    e = cudaMemset(p, 0, sizeof(int));
-    if (e != cudaSuccess) return e;
-    g_status[dev] = p;
-  }
-  *out = g_status[dev];
-  return cudaSuccess;
+  if (dev < 0) return cudaErrorInvalidDevice;
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(out), g_status_word);
 }
 
 // ---------------------------------------------------------------- bounded waits
