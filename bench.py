@@ -46,7 +46,8 @@ DEFAULT_WORKLOAD = "gqa_d128_4k"
 KERNEL_SOURCES = {
     "fwd_kernel": ["flash_attention_gb300/csrc/fa_fwd.cu", "flash_attention_gb300/csrc/fa_common.cuh",
                    "flash_attention_gb300/csrc/fa_band.cuh"],
-    "bwd_main_kernel": ["flash_attention_gb300/csrc/fa_bwd.cu",
+    "bwd_main_kernel": ["flash_attention_gb300/csrc/fa_bwd_main.cuh",
+                        "flash_attention_gb300/csrc/fa_bwd_common.cuh",
                         "flash_attention_gb300/csrc/fa_common.cuh"],
     "bwd_dq_det_kernel": ["flash_attention_gb300/csrc/fa_bwd_dq.cu",
                           "flash_attention_gb300/csrc/fa_common.cuh",

@@ -34,6 +34,8 @@ FA_ERR_BAD_INPUT = 6
 FA_MASK_F32 = 0
 FA_MASK_BF16 = 1
 FA_MASK_BOOL = 2
+FA_LAYOUT_Q_BSHD = 1   # q, o, dO, dq as [batch, seq, heads, dim] in memory
+FA_LAYOUT_KV_BSHD = 2  # k, v, dk, dv as [batch, seq, kv_heads, dim] in memory
 
 
 class FaOptions(ctypes.Structure):
@@ -50,7 +52,7 @@ class FaOptions(ctypes.Structure):
         ("sinks", ctypes.c_void_p),
         ("dsinks", ctypes.c_void_p),
         ("deterministic", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("layout", ctypes.c_int32),
         ("cu_seqlens_q", ctypes.c_void_p),
         ("cu_seqlens_k", ctypes.c_void_p),
         ("total_q", ctypes.c_int32),
@@ -183,6 +185,37 @@ def _check(t, dtype, name):
         raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
 
 
+def _layout_bit(t) -> int:
+    """0 if `t` ([..., heads, rows, dim]) is contiguous, 1 if it is the transposed view of a
+    contiguous [..., rows, heads, dim] tensor (the memory layout the FA_LAYOUT_* flags name)."""
+    if t.is_contiguous():
+        return 0
+    if t.transpose(-3, -2).is_contiguous():
+        return 1
+    raise ValueError("a [.., heads, rows, dim] tensor must be contiguous or a transposed view of "
+                     "a contiguous [.., rows, heads, dim] tensor")
+
+
+def _check_bf16(t, bshd, name):
+    import torch
+
+    if t.dtype != torch.bfloat16 or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA bfloat16 tensor")
+    ok = t.transpose(-3, -2).is_contiguous() if bshd else t.is_contiguous()
+    if not ok:
+        raise ValueError(f"{name} must be laid out as " +
+                         ("[.., rows, heads, dim]" if bshd else "[.., heads, rows, dim]"))
+
+
+def _check_sides(options, q_side, kv_side):
+    """Checks the q-side (q, o, dO, dq) and kv-side (k, v, dk, dv) tensors against the layout
+    flags of `options`."""
+    for t, n in q_side:
+        _check_bf16(t, options.layout & FA_LAYOUT_Q_BSHD, n)
+    for t, n in kv_side:
+        _check_bf16(t, options.layout & FA_LAYOUT_KV_BSHD, n)
+
+
 def fa_train_fwd(q, k, v, mask, o, lse, params: FaParams, stream=None) -> None:
     """C call `fa_train_fwd` on torch tensors (q, k, v, o bf16; mask, lse f32)."""
     import torch
@@ -219,15 +252,17 @@ def make_options(q, k, mask=None, window=(-1, -1), v=None, sinks=None, dsinks=No
                  deterministic=False) -> FaOptions:
     """fa_options for a mask tensor of any supported dtype (float32, bfloat16, bool) whose shape
     broadcasts to [B, H, ql, kl] with the keys contiguous, a (left, right) window, the value
-    head dim of `v` (when it differs from q's), float32 [H] sinks / dsinks tensors, and the
-    deterministic backward."""
+    head dim of `v` (when it differs from q's), float32 [H] sinks / dsinks tensors, the
+    deterministic backward, and the memory layouts of q and k (contiguous, or transposed views
+    of [B, seq, heads, dim] tensors)."""
     import torch
 
     B, H, ql, d = q.shape
     kl = k.shape[2]
     wl, wr = window if window is not None else (-1, -1)
+    layout = FA_LAYOUT_Q_BSHD * _layout_bit(q) | FA_LAYOUT_KV_BSHD * _layout_bit(k)
     opt = FaOptions(int(wl), int(wr), FA_MASK_F32, 0, 0, 0, 0, None, None,
-                    1 if deterministic else 0, 0, None, None, 0, 0)
+                    1 if deterministic else 0, layout, None, None, 0, 0)
     if v is not None and v.shape[-1] != d:
         opt.value_dim = int(v.shape[-1])
     if mask is not None:
@@ -256,8 +291,7 @@ def fa_train_fwd_ex(q, k, v, mask, o, lse, params: FaParams, options: FaOptions,
     """C call `fa_train_fwd_ex` (window, mask type and broadcast in `options`)."""
     import torch
 
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
-        _check(t, torch.bfloat16, n)
+    _check_sides(options, ((q, "q"), (o, "o")), ((k, "k"), (v, "v")))
     _check(lse, torch.float32, "lse")
     rc = load_library().fa_train_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(o), _ptr(lse),
                                         ctypes.byref(params), ctypes.byref(options),
@@ -271,9 +305,8 @@ def fa_train_bwd_ex(q, k, v, o, lse, dO, mask, dq, dk, dv, params: FaParams, opt
     """C call `fa_train_bwd_ex`."""
     import torch
 
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO"), (dq, "dq"), (dk, "dk"),
-                 (dv, "dv")):
-        _check(t, torch.bfloat16, n)
+    _check_sides(options, ((q, "q"), (o, "o"), (dO, "dO"), (dq, "dq")),
+                 ((k, "k"), (v, "v"), (dk, "dk"), (dv, "dv")))
     _check(lse, torch.float32, "lse")
     rc = load_library().fa_train_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
                                         _ptr(mask), _ptr(dq), _ptr(dk), _ptr(dv),
@@ -378,7 +411,8 @@ def _plain_call(q, k, v, mask, window, sinks):
     dense = mask is None or (mask.dtype == torch.float32 and mask.dim() == 4
                              and mask.is_contiguous()
                              and tuple(mask.shape) == (B, H, ql, k.shape[2]))
-    return dense and window is None and sinks is None and v.shape[-1] == d
+    contiguous = q.is_contiguous() and k.is_contiguous() and v.is_contiguous()
+    return dense and contiguous and window is None and sinks is None and v.shape[-1] == d
 
 
 def attention_fwd(q, k, v, *, scale, causal, mask=None, window=None, sinks=None, stream=None):
@@ -389,7 +423,10 @@ def attention_fwd(q, k, v, *, scale, causal, mask=None, window=None, sinks=None,
     import torch
 
     B, H, ql, d = q.shape
-    o = torch.empty((B, H, ql, v.shape[-1]), dtype=q.dtype, device=q.device)
+    if _layout_bit(q):  # o in q's layout
+        o = torch.empty((B, ql, H, v.shape[-1]), dtype=q.dtype, device=q.device).transpose(1, 2)
+    else:
+        o = torch.empty((B, H, ql, v.shape[-1]), dtype=q.dtype, device=q.device)
     lse = torch.empty((B, H, ql), dtype=torch.float32, device=q.device)
     params = make_params(q, k, scale=scale, causal=causal)
     if _plain_call(q, k, v, mask, window, sinks):
@@ -485,7 +522,10 @@ def varlen_attention_fwd(q, k, v, cu_q, cu_k, max_q, max_k, *, scale, causal, wi
     import torch
 
     H, Tq, _ = q.shape
-    o = torch.empty((H, Tq, v.shape[2]), dtype=q.dtype, device=q.device)
+    if _layout_bit(q):  # o in q's layout: [total_q, H, dv] memory
+        o = torch.empty((Tq, H, v.shape[2]), dtype=q.dtype, device=q.device).transpose(0, 1)
+    else:
+        o = torch.empty((H, Tq, v.shape[2]), dtype=q.dtype, device=q.device)
     lse = torch.empty((H, Tq), dtype=torch.float32, device=q.device)
     params, opt = varlen_params_options(q, k, v, cu_q, cu_k, max_q, max_k, scale=scale,
                                         causal=causal, window=window, sinks=sinks)

@@ -46,8 +46,34 @@ cudaError_t get_encoder() {
   return g_encode_err;
 }
 
+// 4-D bf16 tensor map (d, rows, heads, batch) over a [batch, heads, rows, d] tensor stored as
+// such or, with bshd, as [batch, rows, heads, d]; box (64, box_rows, 1, 1), 128-byte swizzle;
+// reads outside [0, rows) fill with zeros.
+bool encode_bf16_4d(CUtensorMap* m, const void* base, int d, int rows, int heads, int batch,
+                    bool bshd, int box_rows) {
+  const cuuint64_t row_b = (cuuint64_t)d * 2;
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads, (cuuint64_t)batch};
+  cuuint64_t strides[3];
+  if (bshd) {
+    strides[0] = row_b * heads;                    // next row
+    strides[1] = row_b;                            // next head
+    strides[2] = row_b * heads * (cuuint64_t)rows; // next batch
+  } else {
+    strides[0] = row_b;
+    strides[1] = row_b * rows;
+    strides[2] = row_b * rows * (cuuint64_t)heads;
+  }
+  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 3-D bf16 tensor map over a contiguous [bh, rows, d] tensor, box (64, box_rows, 1), 128-byte
-// swizzle; reads outside [0, rows) fill with zeros.
+// swizzle; reads outside [0, rows) fill with zeros (the paged caches and queries).
 bool encode_bf16_3d(CUtensorMap* m, const void* base, int bh, int rows, int d, int box_rows) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)bh};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * (cuuint64_t)d * 2};
@@ -58,6 +84,14 @@ bool encode_bf16_3d(CUtensorMap* m, const void* base, int bh, int rows, int d, i
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// The tile map of a q-side or kv-side tensor: 3-D (d, rows, batch * heads) in the default
+// layout, 4-D in the bshd layout (the kernels issue the matching load form).
+bool encode_bf16_map(CUtensorMap* m, const void* base, int d, int rows, int heads, int batch,
+                     bool bshd, int box_rows) {
+  return bshd ? encode_bf16_4d(m, base, d, rows, heads, batch, true, box_rows)
+              : encode_bf16_3d(m, base, heads * batch, rows, d, box_rows);
 }
 
 // ---------------------------------------------------------------- per-device status word
@@ -112,7 +146,7 @@ fa_options default_options(const fa_params* p) {
   o.sinks = nullptr;
   o.dsinks = nullptr;
   o.deterministic = 0;
-  o.reserved = 0;
+  o.layout = 0;
   o.cu_seqlens_q = nullptr;
   o.cu_seqlens_k = nullptr;
   o.total_q = 0;
@@ -128,7 +162,8 @@ fa_options default_options(const fa_params* p) {
 int check_options(const fa_options* o, const void* mask, const fa_params* p, bool bwd) {
   if (o->window_left < -1 || o->window_right < -1) return FA_ERR_INVALID;
   if (o->value_dim < 0) return FA_ERR_INVALID;
-  if ((o->deterministic != 0 && o->deterministic != 1) || o->reserved != 0) return FA_ERR_INVALID;
+  if (o->deterministic != 0 && o->deterministic != 1) return FA_ERR_INVALID;
+  if (o->layout & ~(FA_LAYOUT_Q_BSHD | FA_LAYOUT_KV_BSHD)) return FA_ERR_INVALID;
   if ((o->cu_seqlens_q == nullptr) != (o->cu_seqlens_k == nullptr)) return FA_ERR_INVALID;
   if (o->cu_seqlens_q) {
     if (!aligned(o->cu_seqlens_q, 4) || !aligned(o->cu_seqlens_k, 4)) return FA_ERR_INVALID;
@@ -284,6 +319,8 @@ int fa_train_fwd_ex(const void* q, const void* k, const void* v, const void* mas
   a.cu_k = op->cu_seqlens_k;
   a.total_q = op->total_q;
   a.total_k = op->total_k;
+  a.q_bshd = (op->layout & FA_LAYOUT_Q_BSHD) != 0;
+  a.kv_bshd = (op->layout & FA_LAYOUT_KV_BSHD) != 0;
   a.o = o;
   a.lse = lse;
   if ((e = device_status_word(dev, &a.status)) != cudaSuccess) return cuda_fail(e, "status word");
@@ -305,11 +342,11 @@ int fa_train_fwd_ex(const void* q, const void* k, const void* v, const void* mas
   // tensor-map z and rows: (batch, head) slices of ql / kl rows, or for a variable-length
   // batch the heads of total_q / total_k packed rows
   const bool vl = a.cu_q != nullptr;
-  const int qz = vl ? a.H : a.B * a.H, kz = vl ? a.Hk : a.B * a.Hk;
+  const int nb = vl ? 1 : a.B;
   const int qr = vl ? a.total_q : a.ql, kr = vl ? a.total_k : a.kl;
-  if (!encode_bf16_3d(&m.q, q, qz, qr, a.d, qrows) ||
-      !encode_bf16_3d(&m.k, k, kz, kr, a.d, kvrows) ||
-      !encode_bf16_3d(&m.v, v, kz, kr, a.dval, kvrows))
+  if (!encode_bf16_map(&m.q, q, a.d, qr, a.H, nb, a.q_bshd, qrows) ||
+      !encode_bf16_map(&m.k, k, a.d, kr, a.Hk, nb, a.kv_bshd, kvrows) ||
+      !encode_bf16_map(&m.v, v, a.dval, kr, a.Hk, nb, a.kv_bshd, kvrows))
     return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
   e = fa::launch_fwd(a, m, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
@@ -355,6 +392,8 @@ static int prepare_bwd(const void* q, const void* k, const void* v, const void* 
   a->cu_k = op->cu_seqlens_k;
   a->total_q = op->total_q;
   a->total_k = op->total_k;
+  a->q_bshd = (op->layout & FA_LAYOUT_Q_BSHD) != 0;
+  a->kv_bshd = (op->layout & FA_LAYOUT_KV_BSHD) != 0;
   a->dq = dq;
   a->dk = dk;
   a->dv = dv;
@@ -379,20 +418,21 @@ static int prepare_bwd(const void* q, const void* k, const void* v, const void* 
 
 static int encode_bwd_maps(const fa::BwdArgs& a, fa::BwdMaps* m) {
   const int qrows = fa::bwd_q_box_rows(a.d), kvrows = fa::bwd_kv_box_rows(a.d);
-  const bool vl = a.cu_q != nullptr;  // variable-length batch: heads of packed rows
-  const int qz = vl ? a.H : a.B * a.H, kz = vl ? a.Hk : a.B * a.Hk;
+  const bool vl = a.cu_q != nullptr;  // variable-length batch: one batch of packed rows
+  const int nb = vl ? 1 : a.B;
   const int qr = vl ? a.total_q : a.ql, kr = vl ? a.total_k : a.kl;
-  if (!encode_bf16_3d(&m->q, a.q, qz, qr, a.d, qrows) ||
-      !encode_bf16_3d(&m->dO, a.dO, qz, qr, a.dval, qrows) ||
-      !encode_bf16_3d(&m->k, a.k, kz, kr, a.d, kvrows) ||
-      !encode_bf16_3d(&m->v, a.v, kz, kr, a.dval, kvrows))
+  const bool qs = a.q_bshd, ks = a.kv_bshd;
+  if (!encode_bf16_map(&m->q, a.q, a.d, qr, a.H, nb, qs, qrows) ||
+      !encode_bf16_map(&m->dO, a.dO, a.dval, qr, a.H, nb, qs, qrows) ||
+      !encode_bf16_map(&m->k, a.k, a.d, kr, a.Hk, nb, ks, kvrows) ||
+      !encode_bf16_map(&m->v, a.v, a.dval, kr, a.Hk, nb, ks, kvrows))
     return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
   if (a.deterministic) {
     const int drows = fa::dq_det_box_rows();
-    if (!encode_bf16_3d(&m->det.q, a.q, qz, qr, a.d, 128) ||
-        !encode_bf16_3d(&m->det.dO, a.dO, qz, qr, a.dval, 128) ||
-        !encode_bf16_3d(&m->det.k, a.k, kz, kr, a.d, drows) ||
-        !encode_bf16_3d(&m->det.v, a.v, kz, kr, a.dval, drows))
+    if (!encode_bf16_map(&m->det.q, a.q, a.d, qr, a.H, nb, qs, 128) ||
+        !encode_bf16_map(&m->det.dO, a.dO, a.dval, qr, a.H, nb, qs, 128) ||
+        !encode_bf16_map(&m->det.k, a.k, a.d, kr, a.Hk, nb, ks, drows) ||
+        !encode_bf16_map(&m->det.v, a.v, a.dval, kr, a.Hk, nb, ks, drows))
       return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
   }
   return FA_OK;

@@ -82,6 +82,7 @@ struct BwdKParams {
   const int32_t* cu_q;  // variable-length batch: sequence offsets (VARLEN kernels)
   const int32_t* cu_k;
   int total_q, total_k;
+  int q_bshd, kv_bshd;  // 1: dq / dk, dv are [batch, rows, heads, d] (else [batch, heads, rows, d])
   float scale, scale_log2;
   unsigned long long wait_limit_ns;  // limit of one barrier wait
 };
@@ -100,6 +101,8 @@ inline BwdKParams make_bwd_kparams(const BwdArgs& a) {
   kp.cu_k = a.cu_k;
   kp.total_q = a.total_q;
   kp.total_k = a.total_k;
+  kp.q_bshd = a.q_bshd;
+  kp.kv_bshd = a.kv_bshd;
   kp.lse2 = a.lse2;
   kp.dvec = a.dvec;
   kp.dqacc = a.dqacc;

@@ -84,6 +84,7 @@ struct DqKParams {
   const int32_t* cu_q;  // variable-length batch: sequence offsets, or nullptr
   const int32_t* cu_k;
   int total_q, total_k;
+  int q_bshd, kv_bshd;  // 1: q, dO, dq / k, v are [batch, rows, heads, d] (tile maps 4-D)
   int H, Hk, ql, kl, ql_pad;
   int tiles_fast;  // 1: blockIdx.x = query tile, y = (batch, head); 0: swapped
   int lo_off, hi_off;
@@ -121,21 +122,22 @@ __global__ void __launch_bounds__(DqLayout<HD, DV>::THREADS, 1)
   // variable-length batch: the tiles of one (sequence, head) together (they share K, V in L2)
   const int bh = p.tiles_fast ? (int)blockIdx.y : (int)blockIdx.x;
   const int b = bh / p.H, h = bh % p.H;
-  const int bkh = b * p.Hk + h / (p.H / p.Hk);
   const int m0 = (int)(p.tiles_fast ? blockIdx.x : blockIdx.y) * kQM;
   // the rows of this problem: one (batch, head), or sequence b of a variable-length batch
   int ql = p.ql, kl = p.kl;
-  int qz = bh, kz = bkh, qrow0 = 0, krow0 = 0;
-  size_t orow0 = (size_t)bh * p.ql;  // dQ row of query 0
+  const int kh = h / (p.H / p.Hk);
+  int tb = b, qrow0 = 0, krow0 = 0;  // tb: batch coordinate of the tile loads
+  int ob = bh / p.H, or0 = 0, orows = p.ql;  // dQ: batch, first row and rows of this problem
   if (p.cu_q != nullptr) {
     int qs, ks;
     varlen_seq(p.cu_q, b, p.total_q, p.ql, qs, ql);
     varlen_seq(p.cu_k, b, p.total_k, p.kl, ks, kl);
-    qz = h;
-    kz = h / (p.H / p.Hk);
+    tb = 0;
     qrow0 = qs;
     krow0 = ks;
-    orow0 = (size_t)h * p.total_q + qs;
+    ob = 0;
+    or0 = qs;
+    orows = p.total_q;
   }
   if (m0 >= ql) return;  // a query tile past this sequence's rows (the whole CTA leaves)
   const int r1 = min(m0 + kQM, ql) - 1;
@@ -179,9 +181,11 @@ __global__ void __launch_bounds__(DqLayout<HD, DV>::THREADS, 1)
       for (int s = 0; s < STAGES; ++s) last[s] = -1;
       mbar_arrive_expect_tx(&q_full, LY::Q_BYTES + LY::DO_BYTES);
       for (int c = 0; c < KCH; ++c)
-        tma_load_3d(smem + LY::OFF_Q + c * kQM * 128, &mQ, &q_full, c * 64, qrow0 + m0, qz);
+        tma_load_bh(smem + LY::OFF_Q + c * kQM * 128, &mQ, &q_full, c * 64, qrow0 + m0, h, tb,
+                    p.H, p.q_bshd != 0);
       for (int c = 0; c < VCH; ++c)
-        tma_load_3d(smem + LY::OFF_DO + c * kQM * 128, &mDO, &q_full, c * 64, qrow0 + m0, qz);
+        tma_load_bh(smem + LY::OFF_DO + c * kQM * 128, &mDO, &q_full, c * 64, qrow0 + m0, h, tb,
+                    p.H, p.q_bshd != 0);
       const uint64_t pol = policy_evict_last();
       for (int jj = 0; jj < ntt; ++jj) {
         const int st = jj % STAGES;
@@ -190,11 +194,11 @@ __global__ void __launch_bounds__(DqLayout<HD, DV>::THREADS, 1)
         const int n0 = (J0 + jj) * kQN;
         mbar_arrive_expect_tx(&kv_full[st], LY::K_BYTES + LY::V_BYTES);
         for (int c = 0; c < KCH; ++c)
-          tma_load_3d_hint(smem + LY::OFF_K + st * LY::K_BYTES + c * kQN * 128, &mK, &kv_full[st],
-                           c * 64, krow0 + n0, kz, pol);
+          tma_load_bh_hint(smem + LY::OFF_K + st * LY::K_BYTES + c * kQN * 128, &mK, &kv_full[st],
+                           c * 64, krow0 + n0, kh, tb, p.Hk, p.kv_bshd != 0, pol);
         for (int c = 0; c < VCH; ++c)
-          tma_load_3d_hint(smem + LY::OFF_V + st * LY::V_BYTES + c * kQN * 128, &mV, &kv_full[st],
-                           c * 64, krow0 + n0, kz, pol);
+          tma_load_bh_hint(smem + LY::OFF_V + st * LY::V_BYTES + c * kQN * 128, &mV, &kv_full[st],
+                           c * 64, krow0 + n0, kh, tb, p.Hk, p.kv_bshd != 0, pol);
         last[st] = jj;
       }
       mbar_wait_drain(&q_full, 0);
@@ -327,7 +331,8 @@ __global__ void __launch_bounds__(DqLayout<HD, DV>::THREADS, 1)
       tc_fence_after();
       have = ok;
     }
-    __nv_bfloat16* out = p.dq + (orow0 + (i < ql ? i : 0)) * HD;
+    __nv_bfloat16* out =
+        p.dq + bhsd_offset(ob, bh % p.H, or0 + (i < ql ? i : 0), p.H, orows, HD, p.q_bshd != 0);
 #pragma unroll 1
     for (int c = 0; c < HD; c += 32) {
       uint32_t rq[32];
@@ -376,6 +381,8 @@ static cudaError_t launch_dq_det_t(const BwdArgs& a, const DqMaps& m, cudaStream
   kp.lse2 = a.lse2;
   kp.dvec = a.dvec;
   kp.dq = reinterpret_cast<__nv_bfloat16*>(a.dq);
+  kp.q_bshd = a.q_bshd;
+  kp.kv_bshd = a.kv_bshd;
   kp.status = a.status;
   kp.wait_limit_ns = a.wait_limit_ns;
   kp.cu_q = a.cu_q;

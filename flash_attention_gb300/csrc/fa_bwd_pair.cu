@@ -118,19 +118,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
   const int G = p.H / p.Hk;
   const int n0 = (int)(p.tiles_fast ? (blockIdx.x >> 1) : blockIdx.y) * kBN;
   int ql = p.ql, kl = p.kl;
-  int kz = bkh, qzb = b * p.H, krow0 = 0, qrow0 = 0;
-  size_t kvrow0 = (size_t)bkh * p.kl;  // dK / dV row of key 0
+  int krow0 = 0, qrow0 = 0;
+  int kb = b, krows = p.kl;  // dK / dV: batch and rows of this problem (row of key 0: krow0)
   if constexpr (VARLEN) {
     int qs, ks;
     const bool bad = varlen_seq(p.cu_q, b, p.total_q, p.ql, qs, ql) |
                      varlen_seq(p.cu_k, b, p.total_k, p.kl, ks, kl);
     if (bad && threadIdx.x == 0 && rank == 0 && p.status)
       atomicCAS(p.status, kStatusOk, kStatusBadInput);
-    kz = kh;
-    qzb = 0;
     krow0 = ks;
     qrow0 = qs;
-    kvrow0 = (size_t)kh * p.total_k + ks;
+    kb = 0;
+    krows = p.total_k;
   }
   if (n0 >= kl) return;  // a kv tile past this sequence's keys: both CTAs of the pair leave
   int m_first, m_last;
@@ -198,11 +197,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
       const bool k_half = rank == 1 && do_dq;  // rank 1's dQ^T rows need K columns 128-255
       mbar_arrive_expect_tx(&kv_full, LY::KV_BYTES + (k_half ? LY::KH_BYTES : 0));
       for (int c = 0; c < HD / 64; ++c)
-        tma_load_3d(smem + LY::OFF_KV + c * kBN * 128, mkv, &kv_full, c * 64, krow0 + n0, kz);
+        tma_load_bh(smem + LY::OFF_KV + c * kBN * 128, mkv, &kv_full, c * 64, krow0 + n0, kh, kb,
+                    p.Hk, p.kv_bshd != 0);
       if (k_half)
         for (int c = 2; c < HD / 64; ++c)
-          tma_load_3d(smem + LY::OFF_STG + (c - 2) * kBN * 128, &mK, &kv_full, c * 64,
-                      krow0 + n0, kz);
+          tma_load_bh(smem + LY::OFF_STG + (c - 2) * kBN * 128, &mK, &kv_full, c * 64,
+                      krow0 + n0, kh, kb, p.Hk, p.kv_bshd != 0);
       int loaded = 0;
       for (int it = 0; it < n_iter; ++it) {
         if (it >= 1 && !mbar_wait(&f_empty, (it - 1) & 1, &wctl)) break;
@@ -210,8 +210,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
         const int q0 = (m_first + it % nm) * BM;
         mbar_arrive_expect_tx(&f_full, LY::TILE_BYTES);
         for (int c = 0; c < HD / 64; ++c)
-          tma_load_3d(smem + LY::OFF_F + c * BM * 128, mfirst, &f_full, c * 64, qrow0 + q0,
-                      qzb + h);
+          tma_load_bh(smem + LY::OFF_F + c * BM * 128, mfirst, &f_full, c * 64, qrow0 + q0, h,
+                      kb, p.H, p.q_bshd != 0);
         loaded = it + 1;
       }
       mbar_wait_drain(&kv_full, 0);
@@ -228,8 +228,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
         const int bh = b * p.H + h;
         mbar_arrive_expect_tx(&r_full[st], LY::TILE_BYTES + BM * 4);
         for (int c = 0; c < HD / 64; ++c)
-          tma_load_3d(smem + LY::OFF_R + st * LY::TILE_BYTES + c * BM * 128, msecond, &r_full[st],
-                      c * 64, qrow0 + q0, qzb + h);
+          tma_load_bh(smem + LY::OFF_R + st * LY::TILE_BYTES + c * BM * 128, msecond, &r_full[st],
+                      c * 64, qrow0 + q0, h, kb, p.H, p.q_bshd != 0);
         bulk_load(smem + LY::OFF_LD + st * BM * 4, ld_src + (size_t)bh * p.ql_pad + q0, BM * 4,
                   &r_full[st]);
         last_use[st] = it;
@@ -527,9 +527,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairLayout::THREADS,
       tc_fence_after();
       have = ok && n_iter > 0;
     }
-    const size_t kvrow = kvrow0 + (kv < kl ? kv : 0);
+    const long long kvr = krow0 + (kv < kl ? kv : 0);  // row of this key in dK / dV
     const float mul = rank == 0 ? 1.0f : p.scale;
-    __nv_bfloat16* out = (rank == 0 ? p.dv : p.dk) + kvrow * HD;
+    __nv_bfloat16* out =
+        (rank == 0 ? p.dv : p.dk) + bhsd_offset(kb, kh, kvr, p.Hk, krows, HD, p.kv_bshd != 0);
 #pragma unroll 1
     for (int c = 0; c < HD; c += 32) {
       uint32_t r[32];

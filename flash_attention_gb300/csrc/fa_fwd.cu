@@ -102,6 +102,7 @@ struct FwdKParams {
   const int32_t* cu_q;  // variable-length batch: sequence offsets, or nullptr
   const int32_t* cu_k;
   int total_q, total_k;
+  int q_bshd, kv_bshd;  // 1: q, o / k, v are [batch, rows, heads, d] (else [b, heads, rows, d])
   int* status;
   int H, Hk, ql, kl, n_mblk;  // ql, kl: the longest sequence in a variable-length batch
   int tiles_fast;  // 1: blockIdx.x = query tile, y = (batch, head); 0: the other way round
@@ -169,22 +170,26 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, FwdLayout<HD, DV>:
   const int mblk = p.n_mblk - 1 - (int)(p.tiles_fast ? blockIdx.x : blockIdx.y);
   const int m0 = mblk * NQ * kBM;
   const int b = bh / p.H, h = bh % p.H;
-  const int bkh = b * p.Hk + h / (p.H / p.Hk);
   // the rows of this problem: one (batch, head) of fixed length, or in a variable-length
   // batch sequence b's own rows of the packed head h (tensor-map z = head, rows offset)
   int ql = p.ql, kl = p.kl;
-  int qz = bh, kz = bkh, qrow0 = 0, krow0 = 0;
-  size_t orow0 = (size_t)bh * p.ql;  // O / L row of query 0
+  int qrow0 = 0, krow0 = 0;
+  size_t orow0 = (size_t)bh * p.ql;  // L row of query 0
+  int ob = b, or0 = 0, orows = p.ql;  // O: batch, first row and rows of this problem
+  const int kh = h / (p.H / p.Hk);
+  int tb = b;  // batch coordinate of the tile loads (0 in a packed batch)
   if constexpr (VARLEN) {
     int qs, ks;
     const bool bad = varlen_seq(p.cu_q, b, p.total_q, p.ql, qs, ql) |
                      varlen_seq(p.cu_k, b, p.total_k, p.kl, ks, kl);
     if (bad && threadIdx.x == 0 && p.status) atomicCAS(p.status, kStatusOk, kStatusBadInput);
-    qz = h;
-    kz = h / (p.H / p.Hk);
     qrow0 = qs;
     krow0 = ks;
     orow0 = (size_t)h * p.total_q + qs;
+    ob = 0;
+    tb = 0;
+    or0 = qs;
+    orows = p.total_q;
   }
   if (m0 >= ql) return;  // a query tile past this sequence's rows (the whole CTA leaves)
 
@@ -257,22 +262,24 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, FwdLayout<HD, DV>:
       mbar_arrive_expect_tx(&q_full, NQ * LY::Q_TILE_BYTES);
       for (int t = 0; t < NQ; ++t)
         for (int c = 0; c < KCH; ++c)
-          tma_load_3d(smem + LY::OFF_Q + t * LY::Q_TILE_BYTES + c * kBM * 128, &mQ, &q_full,
-                      c * 64, qrow0 + m0 + t * kBM, qz);
+          tma_load_bh(smem + LY::OFF_Q + t * LY::Q_TILE_BYTES + c * kBM * 128, &mQ, &q_full,
+                      c * 64, qrow0 + m0 + t * kBM, h, tb, p.H, p.q_bshd != 0);
       for (int j = J0; j < J1; ++j) {
         const int st = (j - J0) % STAGES;
         const uint32_t use = (j - J0) / STAGES;
         if (use > 0 && !mbar_wait(&k_empty[st], (use - 1) & 1, &wctl)) break;
         mbar_arrive_expect_tx(&k_full[st], LY::K_TILE_BYTES);
         for (int c = 0; c < KCH; ++c)
-          tma_load_3d_hint(smem + LY::OFF_K + st * LY::K_TILE_BYTES + c * BN * 128, &mK,
-                           &k_full[st], c * 64, krow0 + j * BN, kz, pol_kv);
+          tma_load_bh_hint(smem + LY::OFF_K + st * LY::K_TILE_BYTES + c * BN * 128, &mK,
+                           &k_full[st], c * 64, krow0 + j * BN, kh, tb, p.Hk, p.kv_bshd != 0,
+                           pol_kv);
         last_k[st] = j - J0;
         if (use > 0 && !mbar_wait(&v_empty[st], (use - 1) & 1, &wctl)) break;
         mbar_arrive_expect_tx(&v_full[st], LY::V_TILE_BYTES);
         for (int c = 0; c < VCH; ++c)
-          tma_load_3d_hint(smem + LY::OFF_V + st * LY::V_TILE_BYTES + c * BN * 128, &mV,
-                           &v_full[st], c * 64, krow0 + j * BN, kz, pol_kv);
+          tma_load_bh_hint(smem + LY::OFF_V + st * LY::V_TILE_BYTES + c * BN * 128, &mV,
+                           &v_full[st], c * 64, krow0 + j * BN, kh, tb, p.Hk, p.kv_bshd != 0,
+                           pol_kv);
         last_v[st] = j - J0;
       }
       // Let every copy this thread started land before the CTA can exit.
@@ -595,7 +602,8 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, FwdLayout<HD, DV>:
         L = s2 * kLn2;  // a row that sees no key: O = 0, L = sink
       }
     }
-    __nv_bfloat16* orow = p.o + (orow0 + (i < ql ? i : 0)) * DV;
+    __nv_bfloat16* orow =
+        p.o + bhsd_offset(ob, h, or0 + (i < ql ? i : 0), p.H, orows, DV, p.q_bshd != 0);
 #pragma unroll 1
     for (int c = 0; c < DV; c += 32) {
       uint32_t orr[32];
@@ -652,6 +660,8 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, const FwdMaps& m, cudaStream_t
   kp.cu_q = a.cu_q;
   kp.cu_k = a.cu_k;
   kp.total_q = a.total_q;
+  kp.q_bshd = a.q_bshd;
+  kp.kv_bshd = a.kv_bshd;
   kp.total_k = a.total_k;
   kp.status = a.status;
   kp.wait_limit_ns = a.wait_limit_ns;

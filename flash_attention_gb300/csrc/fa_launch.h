@@ -95,12 +95,13 @@ struct FwdArgs {
   const void* mask;   // nullptr, or the mask in mask_type's element type
   int mask_type;      // 0 f32 additive, 1 bf16 additive, 2 bool (uint8, nonzero = visible)
   long long mask_stride_b, mask_stride_h, mask_stride_q;  // elements; keys contiguous
-  void* o;            // bf16 [B, H, ql, d]
+  void* o;            // bf16 [B, H, ql, dval] (see q_bshd)
   float* lse;         // [B, H, ql]
   const float* sinks; // [H] natural-log sink logits, or nullptr
   const int32_t* cu_q;  // variable-length batch: [B + 1] row offsets of the sequences, or nullptr
   const int32_t* cu_k;
   int total_q, total_k;  // rows per head of the packed q / k (variable-length batch)
+  int q_bshd, kv_bshd;   // 1: q, o (and dO, dq) / k, v (and dk, dv) are [batch, rows, heads, d]
   int* status;        // device status word (nullable)
   uint64_t wait_limit_ns;  // limit of one barrier wait in the kernels (fa_set_wait_limit_ns)
   int B, H, Hk, ql, kl, d;  // ql, kl: the longest sequence in a variable-length batch
@@ -110,8 +111,8 @@ struct FwdArgs {
   int band;  // BandMode
 };
 
-// Tensor maps of a forward launch (3-D, innermost first: d, rows, batch*heads; 128-byte
-// swizzle; box of 64 columns).
+// Tensor maps of a forward launch (innermost first: d, rows, batch * heads, or 4-D d, rows,
+// heads, batch for the bshd layout; 128-byte swizzle; box of 64 columns).
 struct FwdMaps {
   CUtensorMap q, k, v;
 };
@@ -144,6 +145,7 @@ struct BwdArgs {
   const int32_t* cu_q;  // variable-length batch (see FwdArgs), or nullptr
   const int32_t* cu_k;
   int total_q, total_k;
+  int q_bshd, kv_bshd;  // layouts, as in FwdArgs
   float* dsinks;       // [H] sink gradient output, or nullptr (then no sink partials)
   float* dsink_part;   // workspace [B*H, sink_chunks]: per-block partial sums of dsinks
   int* status;

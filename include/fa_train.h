@@ -139,7 +139,17 @@ typedef struct fa_params {
  * total_k), and fa_params.ql / kl give the longest sequence (they size the grids). Causal and
  * window bands align bottom-right within each sequence. A sequence with no keys gives O = 0
  * and L = -inf (or its sink). Offsets out of range are clamped and reported by
- * fa_device_status (FA_ERR_BAD_INPUT). No mask may be given (FA_ERR_UNSUPPORTED). */
+ * fa_device_status (FA_ERR_BAD_INPUT). No mask may be given (FA_ERR_UNSUPPORTED).
+ *
+ * Layouts (page "nuvec-core tests/fast.rs", `attention_kernels_match_the_fallback`, passes K
+ * and V as transposed views): by default every bf16 tensor is [batch, heads, rows, dim] in
+ * memory. FA_LAYOUT_Q_BSHD makes q, o, dO and dQ [batch, ql, n_heads, dim] in memory, and
+ * FA_LAYOUT_KV_BSHD makes k, v, dK and dV [batch, kl, n_kv_heads, dim]; a [batch, heads, rows,
+ * dim] view of such a tensor is its transpose of dims 1 and 2. In a variable-length batch the
+ * flags make them [total_q, n_heads, dim] / [total_k, n_kv_heads, dim]. The dim is contiguous
+ * either way; lse keeps its layout. Outputs are written in the layout of their inputs. */
+#define FA_LAYOUT_Q_BSHD 1  /* q, o, dO, dQ as [batch, ql, n_heads, dim] */
+#define FA_LAYOUT_KV_BSHD 2 /* k, v, dK, dV as [batch, kl, n_kv_heads, dim] */
 typedef struct fa_options {
   int32_t window_left;   /* -1, or >= 0 */
   int32_t window_right;  /* -1, or >= 0 */
@@ -151,7 +161,7 @@ typedef struct fa_options {
   const float* sinks;    /* NULL, or [n_heads] f32 on the device, 4-byte aligned */
   float* dsinks;         /* backward only: NULL, or [n_heads] f32 output on the device */
   int32_t deterministic; /* 0 or 1 (backward only) */
-  int32_t reserved;      /* must be 0 */
+  int32_t layout;        /* 0, or FA_LAYOUT_* flags */
   const int32_t* cu_seqlens_q; /* NULL, or the variable-length batch's query offsets [batch+1] */
   const int32_t* cu_seqlens_k; /* its key offsets [batch+1]; both or neither */
   int32_t total_q;       /* variable-length batch: rows per head of q (>= 1) */
@@ -176,9 +186,10 @@ int fa_train_fwd(const void* q, const void* k, const void* v, const float* mask,
 /* Forward with options (window, mask type and broadcast). opt == NULL gives the base
  * behaviour (no window; a mask, if any, dense [B, H, ql, kl] f32). Rows whose window and mask
  * leave no key give O = 0 and L = -inf. Errors as fa_train_fwd; FA_ERR_INVALID also for
- * window values below -1, an unknown mask type, a negative value_dim, negative strides, a
- * mask not aligned to its element size or a misaligned sinks pointer; FA_ERR_UNSUPPORTED for
- * a (head_dim, value_dim) pair without kernels. The forward ignores dsinks. */
+ * window values below -1, an unknown mask type, unknown layout flags, a negative value_dim,
+ * negative strides, a mask not aligned to its element size or a misaligned sinks pointer;
+ * FA_ERR_UNSUPPORTED for a (head_dim, value_dim) pair without kernels. The forward ignores
+ * dsinks. */
 int fa_train_fwd_ex(const void* q, const void* k, const void* v, const void* mask, void* o,
                     float* lse, const fa_params* p, const fa_options* opt, void* stream);
 

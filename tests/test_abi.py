@@ -133,7 +133,7 @@ def _bwd_ex(lib, params, opts, mask=None):
 def _opts(**kw):
     base = dict(window_left=-1, window_right=-1, mask_type=0, value_dim=0, mask_stride_b=0,
                 mask_stride_h=0, mask_stride_q=128, sinks=None, dsinks=None, deterministic=0,
-                reserved=0, cu_seqlens_q=None, cu_seqlens_k=None, total_q=0, total_k=0)
+                layout=0, cu_seqlens_q=None, cu_seqlens_k=None, total_q=0, total_k=0)
     base.update(kw)
     return fa.FaOptions(**base)
 
@@ -141,7 +141,7 @@ def _opts(**kw):
 BAD_OPTIONS = [
     dict(window_left=-2), dict(window_right=-5), dict(mask_type=3), dict(mask_type=-1),
     dict(value_dim=-1), dict(mask_stride_b=-1), dict(mask_stride_h=-4),
-    dict(mask_stride_q=-128), dict(sinks=FAKE + 2), dict(deterministic=2), dict(reserved=1),
+    dict(mask_stride_q=-128), dict(sinks=FAKE + 2), dict(deterministic=2), dict(layout=4), dict(layout=-1),
     dict(cu_seqlens_q=FAKE), dict(cu_seqlens_q=FAKE, cu_seqlens_k=FAKE + 2, total_q=4, total_k=4),
     dict(cu_seqlens_q=FAKE, cu_seqlens_k=FAKE, total_q=0, total_k=4),
 ]

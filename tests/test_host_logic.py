@@ -48,3 +48,22 @@ def test_debug_entry_points_check_arguments():
     assert lib.fa_debug_ex2(fake + 2, fake, fake, fake, 8, None) == fa.FA_ERR_INVALID
     assert lib.fa_debug_ex2(None, fake, fake, fake, 8, None) == fa.FA_ERR_INVALID
     assert lib.fa_debug_wait_timeout(fake + 4, None) == fa.FA_ERR_INVALID
+
+
+def test_layout_detection_of_the_binding():
+    """The binding names a tensor's memory layout for the FA_LAYOUT_* flags: contiguous
+    [B, H, L, D] is 0, a transposed view of a contiguous [B, L, H, D] tensor is 1, anything else
+    is refused rather than copied."""
+    torch = pytest.importorskip("torch")
+    t = torch.zeros(2, 4, 8, 64)
+    assert fa._layout_bit(t) == 0
+    assert fa._layout_bit(torch.zeros(2, 8, 4, 64).transpose(1, 2)) == 1
+    assert fa._layout_bit(torch.zeros(8, 4, 64).transpose(0, 1)) == 1  # packed [total, H, D]
+    with pytest.raises(ValueError):
+        fa._layout_bit(t[..., ::2])  # dim not contiguous
+    with pytest.raises(ValueError):
+        fa._layout_bit(t.transpose(0, 1))  # [H, B, L, D] memory
+    opt = fa.make_options(torch.zeros(2, 8, 4, 64).transpose(1, 2), t)
+    assert opt.layout == fa.FA_LAYOUT_Q_BSHD
+    opt = fa.make_options(t, torch.zeros(2, 8, 4, 64).transpose(1, 2))
+    assert opt.layout == fa.FA_LAYOUT_KV_BSHD
