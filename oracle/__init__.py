@@ -48,9 +48,12 @@ MUTATIONS = {
     "table_stride": 17,
     "decode_top_left": 18,
     "bool_mask_inverted": 19,
+    "paged_grad_slot": 20,
 }
-# Codes above handled here in Python (the mask-form conversion), not in fa_oracle.c.
+# Codes above handled here in Python (the mask-form conversion, the paged gradient's slot
+# mapping), not in fa_oracle.c.
 _PY_MUTATION_BOOL_INVERTED = 19
+_PY_MUTATION_PAGED_SLOT = 20
 _py_mutation = 0
 
 
@@ -299,6 +302,41 @@ def paged_fwd(q, k_cache, v_cache, block_table, lengths, *, scale, causal, nthre
     if rc:
         raise ValueError(f"oracle paged_fwd failed ({rc})")
     return o, lse
+
+
+def paged_bwd(q, k_cache, v_cache, block_table, lengths, do, *, scale, causal, nthreads=None):
+    """Gradients of sum(O * dO) for `paged_fwd` with respect to q [B, H, lq, d] and to both
+    caches [num_pages, Hk, page_size, d], in f64: (dQ, dK_cache, dV_cache).
+
+    Page "nuvec-core tests/fast.rs", `paged_attention_equals_contiguous_attention`, takes the
+    gradients of the paged attention for q and the caches ("paged grads"). Each sequence is the
+    fixed-length problem on the keys its table names (logical key j in page
+    block_table[b, j // page_size], slot j % page_size), so its gradients are `bwd` on those
+    gathered keys. A cache slot's gradient is the sum over every (sequence, key) that reads it
+    (a page named by two sequences gets both contributions); slots no sequence reads get 0."""
+    q, kc, vc, do = _f32(q), _f32(k_cache), _f32(v_cache), _f32(do)
+    table = np.asarray(block_table, np.int64)
+    lens = np.asarray(lengths, np.int64)
+    B, H, lq, d = q.shape
+    _, Hk, bs, _ = kc.shape
+    dq = np.zeros(q.shape, np.float64)
+    dkc = np.zeros(kc.shape, np.float64)
+    dvc = np.zeros(vc.shape, np.float64)
+    for b in range(B):
+        n = int(lens[b])
+        if n == 0:
+            continue
+        j = np.arange(n)
+        pages = table[b, j // bs]
+        slots = (j + 1) % bs if _py_mutation == _PY_MUTATION_PAGED_SLOT else j % bs
+        kb = kc[pages, :, slots, :].transpose(1, 0, 2)[None]  # [1, Hk, n, d]
+        vb = vc[pages, :, slots, :].transpose(1, 0, 2)[None]
+        g = bwd(q[b:b + 1], kb, vb, None, do[b:b + 1], scale=scale, causal=causal,
+                nthreads=nthreads)
+        dq[b] = g[0][0]
+        np.add.at(dkc, (pages, slice(None), slots, slice(None)), g[1][0].transpose(1, 0, 2))
+        np.add.at(dvc, (pages, slice(None), slots, slice(None)), g[2][0].transpose(1, 0, 2))
+    return dq, dkc, dvc
 
 
 # ------------------------------------------------------------------ variable-length batches

@@ -678,6 +678,79 @@ def pin_paged_layout_invariance():
     return fails
 
 
+def _torch_paged_loss(q, kc, vc, table, lens, do, scale, causal, G):
+    """sum(O * dO) of the paged attention, composed from torch ops on the whole caches (the
+    keys of each sequence gathered by advanced indexing), so that autograd differentiates the
+    page lookup itself."""
+    B, H, lq, d = q.shape
+    bs = kc.shape[2]
+    loss = q.new_zeros(())
+    for b in range(B):
+        n = int(lens[b])
+        if n == 0:
+            continue
+        j = torch.arange(n)
+        pages = torch.as_tensor(table[b], dtype=torch.long)[j // bs]
+        kb = kc[pages, :, j % bs, :].permute(1, 0, 2).repeat_interleave(G, 0)  # [H, n, d]
+        vb = vc[pages, :, j % bs, :].permute(1, 0, 2).repeat_interleave(G, 0)
+        s_ = q[b] @ kb.transpose(1, 2) * scale  # [H, lq, n]
+        if causal:
+            i = torch.arange(lq)[:, None]
+            hidden = j[None, :] > n - lq + i  # bottom-right: query i is position n - lq + i
+        else:
+            hidden = torch.zeros(lq, n, dtype=torch.bool)
+        dead = hidden.all(dim=1)  # rows that see no key: O = 0
+        s_ = s_.masked_fill(hidden[None], float("-inf"))
+        s_ = torch.where(dead[None, :, None], torch.zeros_like(s_), s_)  # finite softmax input
+        p_ = torch.softmax(s_, dim=-1)
+        p_ = torch.where(dead[None, :, None], torch.zeros_like(p_), p_)
+        loss = loss + ((p_ @ vb) * do[b]).sum()
+    return loss
+
+
+PAGED_BWD_CASES = [
+    # (B, H, Hk, lq, d, page_size, lengths, causal, shared): shared names one page twice
+    (2, 4, 2, 1, 8, 4, (6, 11), False, False),
+    (2, 4, 1, 3, 8, 4, (9, 2), True, False),    # lq > len for the short sequence
+    (3, 2, 2, 2, 4, 8, (17, 0, 8), True, False),  # an empty sequence
+    (2, 4, 2, 2, 8, 4, (8, 8), True, True),     # a page read by both sequences
+]
+
+
+def pin_paged_bwd_vs_torch_autograd():
+    """The paged gradients (dQ and both cache gradients) against torch autograd in f64 through
+    a paged forward built from torch ops on the whole caches: unused slots and pages get
+    exactly 0, and a page named by two sequences gets the sum of both."""
+    import fa_inputs
+
+    fails = []
+    for n, (B, H, Hk, lq, d, bs, lens, causal, shared) in enumerate(PAGED_BWD_CASES):
+        G = H // Hk
+        per = max(-(-L // bs) for L in lens) if max(lens) else 1
+        P = B * per + 3  # three pages nobody uses
+        rng = np.random.default_rng(500 + n)
+        order = rng.permutation(P)
+        table = order[:B * per].reshape(B, per).astype(np.int32)
+        if shared:
+            table[1, 0] = table[0, 0]
+        q = fa_inputs.bf16_bits_to_f32(fa_inputs.normal_bf16(900 + 4 * n, (B, H, lq, d)))
+        kc = fa_inputs.bf16_bits_to_f32(fa_inputs.normal_bf16(901 + 4 * n, (P, Hk, bs, d)))
+        vc = fa_inputs.bf16_bits_to_f32(fa_inputs.normal_bf16(902 + 4 * n, (P, Hk, bs, d)))
+        do = fa_inputs.bf16_bits_to_f32(fa_inputs.normal_bf16(903 + 4 * n, (B, H, lq, d)))
+        lens_a = np.asarray(lens, np.int32)
+        dq, dk, dv = oracle.paged_bwd(q, kc, vc, table, lens_a, do, scale=0.35, causal=causal)
+        tq, tk, tv = (torch.from_numpy(x).double().requires_grad_() for x in (q, kc, vc))
+        _torch_paged_loss(tq, tk, tv, table, lens_a, torch.from_numpy(do).double(), 0.35,
+                          causal, G).backward()
+        _cmp(f"paged bwd case{n} dQ", dq, tq.grad.numpy(), out=fails)
+        _cmp(f"paged bwd case{n} dK cache", dk, tk.grad.numpy(), out=fails)
+        _cmp(f"paged bwd case{n} dV cache", dv, tv.grad.numpy(), out=fails)
+        unused = np.setdiff1d(np.arange(P), table.ravel())
+        if np.abs(dk[unused]).max(initial=0) != 0 or np.abs(dv[unused]).max(initial=0) != 0:
+            fails.append(f"paged bwd case{n}: an unused page got a gradient")
+    return fails
+
+
 # ------------------------------------------------------------------ variable-length batches
 VARLEN_CASES = [
     # (H, Hk, d, q_lens, k_lens, causal)
@@ -811,6 +884,7 @@ ALL_PINS = [
     pin_value_dim_identity,
     pin_paged_vs_torch,
     pin_paged_layout_invariance,
+    pin_paged_bwd_vs_torch_autograd,
     pin_varlen_vs_torch,
     pin_mask_forms_vs_torch,
 ]
