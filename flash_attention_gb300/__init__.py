@@ -18,7 +18,7 @@ __all__ = [
     "fa_version", "fa_profile_enable", "fa_profile_read", "attention_fwd", "attention_bwd", "load_library", "build", "LIB_PATH",
     "FA_OK", "FA_ERR_INVALID", "FA_ERR_CUDA", "FA_ERR_DEVICE_TIMEOUT", "FA_ERR_UNSUPPORTED",
     "FA_ERR_TOO_LARGE", "FA_ERR_BAD_INPUT", "FaOptions", "FaPagedParams", "paged_attention",
-    "fa_paged_attention", "fa_train_fwd_ex", "fa_train_bwd_ex", "make_options",
+    "fa_paged_attention", "fa_paged_attention_bwd", "fa_train_fwd_ex", "fa_train_bwd_ex", "make_options",
     "FA_MASK_F32", "FA_MASK_BF16", "FA_MASK_BOOL",
 ]
 
@@ -130,6 +130,9 @@ def load_library():
             lib.fa_train_bwd_ex.restype = ctypes.c_int
             lib.fa_paged_attention.argtypes = [vp, vp, vp, vp, vp, vp, fp, vp, vp]
             lib.fa_paged_attention.restype = ctypes.c_int
+            lib.fa_paged_attention_bwd.argtypes = [vp, vp, vp, vp, vp, vp, fp, vp, vp, vp, vp,
+                                                   vp, vp]
+            lib.fa_paged_attention_bwd.restype = ctypes.c_int
             lib.fa_device_status.argtypes = [ctypes.c_int]
             lib.fa_device_status.restype = ctypes.c_int
             lib.fa_error_string.argtypes = [ctypes.c_int]
@@ -492,6 +495,43 @@ def paged_attention(q, k_cache, v_cache, block_table, lengths, *, scale, causal=
     lse = torch.empty((B, H, lq), dtype=torch.float32, device=q.device)
     fa_paged_attention(q, k_cache, v_cache, block_table, lengths, o, lse, params, stream)
     return o, lse
+
+
+def fa_paged_attention_bwd(q, k_cache, v_cache, block_table, lengths, o, lse, dO, dq, dk_cache,
+                           dv_cache, params: FaPagedParams, stream=None) -> None:
+    """C call `fa_paged_attention_bwd` (gradients for q and both caches)."""
+    import torch
+
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (o, "o"), (dO, "dO"),
+                 (dq, "dq"), (dk_cache, "dk_cache"), (dv_cache, "dv_cache")):
+        _check(t, torch.bfloat16, n)
+    _check(block_table, torch.int32, "block_table")
+    _check(lengths, torch.int32, "lengths")
+    _check(lse, torch.float32, "lse")
+    rc = load_library().fa_paged_attention_bwd(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(lengths), _ptr(o),
+        _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk_cache), _ptr(dv_cache), ctypes.byref(params),
+        _stream_handle(stream))
+    if rc:
+        raise FaError(rc, "fa_paged_attention_bwd")
+
+
+def paged_attention_bwd(q, k_cache, v_cache, block_table, lengths, o, lse, dO, *, scale,
+                        causal=True, stream=None):
+    """Gradients of paged_attention: returns (dq, dk_cache, dv_cache), the cache gradients
+    shaped like the caches (0 in every slot no sequence reads)."""
+    import torch
+
+    B, H, lq, d = q.shape
+    P, Hk, bs, _ = k_cache.shape
+    params = FaPagedParams(B, H, Hk, lq, d, bs, block_table.shape[1], P, float(scale),
+                           int(bool(causal)), 0, 0)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k_cache)
+    dv = torch.empty_like(v_cache)
+    fa_paged_attention_bwd(q, k_cache, v_cache, block_table, lengths, o, lse, dO, dq, dk, dv,
+                           params, stream)
+    return dq, dk, dv
 
 
 def varlen_params_options(q, k, v, cu_q, cu_k, max_q, max_k, *, scale, causal, window=None,

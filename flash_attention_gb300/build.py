@@ -17,7 +17,7 @@ INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libfa_gb300.so")
 SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_bwd_strided.cu", "fa_bwd_pair.cu",
-           "fa_bwd_dq.cu", "fa_paged.cu", "fa_diag.cu"]
+           "fa_bwd_dq.cu", "fa_paged.cu", "fa_paged_bwd.cu", "fa_diag.cu"]
 HEADERS = ["fa_common.cuh", "fa_launch.h", "fa_band.cuh", "fa_once.h", "fa_bwd_common.cuh",
            "fa_bwd_main.cuh"]
 

@@ -512,9 +512,9 @@ int fa_train_bwd_noalloc(const void* q, const void* k, const void* v, const void
   return FA_OK;
 }
 
-int fa_paged_attention(const void* q, const void* k_cache, const void* v_cache,
-                       const int32_t* block_table, const int32_t* lengths, void* o, float* lse,
-                       const fa_paged_params* p, void* stream) {
+// Parameter and pointer checks shared by the paged forward and backward.
+static int check_paged(const fa_paged_params* p, const void* q, const void* k_cache,
+                       const void* v_cache, const int32_t* block_table, const int32_t* lengths) {
   if (!p) return FA_ERR_INVALID;
   const int ps = p->page_size;
   if (p->batch <= 0 || p->n_heads <= 0 || p->n_kv_heads <= 0 || p->q_len <= 0 ||
@@ -531,11 +531,21 @@ int fa_paged_attention(const void* q, const void* k_cache, const void* v_cache,
   if (G * p->q_len > (int64_t)kPagedMaxRows) return FA_ERR_INVALID;
   if ((int64_t)p->batch * p->n_kv_heads > 65535) return FA_ERR_INVALID;  // grid y
   int rc;
-  if ((rc = check_bf16(q)) || (rc = check_bf16(k_cache)) || (rc = check_bf16(v_cache)) ||
-      (rc = check_bf16(o)))
-    return rc;
+  if ((rc = check_bf16(q)) || (rc = check_bf16(k_cache)) || (rc = check_bf16(v_cache))) return rc;
   if (!block_table || !lengths || !aligned(block_table, 4) || !aligned(lengths, 4))
     return FA_ERR_INVALID;
+  return FA_OK;
+}
+
+int fa_paged_attention(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_table, const int32_t* lengths, void* o, float* lse,
+                       const fa_paged_params* p, void* stream) {
+  if (!p) return FA_ERR_INVALID;
+  const int ps = p->page_size;
+  const int64_t G = p->n_heads > 0 && p->n_kv_heads > 0 ? p->n_heads / p->n_kv_heads : 0;
+  int rc;
+  if ((rc = check_paged(p, q, k_cache, v_cache, block_table, lengths)) || (rc = check_bf16(o)))
+    return rc;
   if (lse && !aligned(lse, 4)) return FA_ERR_INVALID;
   if ((rc = check_device())) return rc;
   cudaError_t e = get_encoder();
@@ -579,6 +589,104 @@ int fa_paged_attention(const void* q, const void* k_cache, const void* v_cache,
   cudaError_t e2 = ws ? cudaFreeAsync(ws, s) : cudaSuccess;
   if (e != cudaSuccess) return cuda_fail(e, "paged attention launch");
   if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync (paged workspace)");
+  return FA_OK;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int fa_paged_attention_bwd(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_table, const int32_t* lengths, const void* o,
+                           const float* lse, const void* dO, void* dq, void* dk_cache,
+                           void* dv_cache, const fa_paged_params* p, void* stream) {
+  int rc;
+  if ((rc = check_paged(p, q, k_cache, v_cache, block_table, lengths))) return rc;
+  if ((rc = check_bf16(o)) || (rc = check_bf16(dO)) || (rc = check_bf16(dq)) ||
+      (rc = check_bf16(dk_cache)) || (rc = check_bf16(dv_cache)) || (rc = check_f32(lse)))
+    return rc;
+  if ((int64_t)p->batch * p->q_len > 65535) return FA_ERR_INVALID;  // grid y of the mask
+  if ((rc = check_device())) return rc;
+  cudaError_t e = get_encoder();
+  if (e != cudaSuccess) return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int B = p->batch, H = p->n_heads, Hk = p->n_kv_heads, lq = p->q_len, d = p->head_dim;
+  const int64_t cap = (int64_t)p->max_pages * p->page_size;
+  // the flat problem: B sequences of lq queries over `cap` key slots, masked
+  fa_params fp;
+  fp.batch = B;
+  fp.n_heads = H;
+  fp.n_kv_heads = Hk;
+  fp.ql = lq;
+  fp.kl = (int32_t)cap;
+  fp.head_dim = d;
+  fp.scale = p->scale;
+  fp.causal = 0;
+  fa_options fo = default_options(&fp);
+  fo.mask_type = FA_MASK_BOOL;
+  fo.mask_stride_b = (int64_t)lq * cap;
+  fo.mask_stride_h = 0;
+  fo.mask_stride_q = cap;
+  const size_t flat = align256((size_t)B * Hk * cap * d * 2);
+  const size_t mask_bytes = align256((size_t)B * lq * cap);
+  const size_t uses_bytes = align256((size_t)p->num_pages * 4);
+  const size_t bwd_bytes = fa::bwd_workspace_bytes(B, H, lq, d);
+  void* ws = nullptr;
+  e = cudaMallocAsync(&ws, 4 * flat + mask_bytes + uses_bytes + bwd_bytes, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync (paged backward workspace)");
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  fa::PagedGradArgs g;
+  g.k_cache = k_cache;
+  g.v_cache = v_cache;
+  g.table = block_table;
+  g.lens = lengths;
+  g.k_flat = w;
+  g.v_flat = w + flat;
+  g.dk_flat = w + 2 * flat;
+  g.dv_flat = w + 3 * flat;
+  g.dk_cache = dk_cache;
+  g.dv_cache = dv_cache;
+  g.mask = w + 4 * flat;
+  g.uses = reinterpret_cast<int*>(w + 4 * flat + mask_bytes);
+  g.B = B;
+  g.Hk = Hk;
+  g.lq = lq;
+  g.d = d;
+  g.ps = p->page_size;
+  g.max_pages = p->max_pages;
+  g.num_pages = p->num_pages;
+  g.causal = p->causal;
+  void* bwd_ws = w + 4 * flat + mask_bytes + uses_bytes;
+  const size_t cache_bytes = (size_t)p->num_pages * Hk * p->page_size * d * 2;
+  fa::BwdArgs a;
+  fa::BwdMaps m;
+  if ((e = device_status_word(dev, &g.status)) != cudaSuccess ||
+      (e = cudaMemsetAsync(dk_cache, 0, cache_bytes, s)) != cudaSuccess ||
+      (e = cudaMemsetAsync(dv_cache, 0, cache_bytes, s)) != cudaSuccess ||
+      (e = cudaMemsetAsync(g.uses, 0, (size_t)p->num_pages * 4, s)) != cudaSuccess ||
+      (e = fa::launch_paged_gather(g, s)) != cudaSuccess) {
+    cudaFreeAsync(ws, s);
+    return cuda_fail(e, "paged backward: gather");
+  }
+  rc = prepare_bwd(q, g.k_flat, g.v_flat, o, lse, dO, g.mask, dq, const_cast<void*>(g.dk_flat),
+                   const_cast<void*>(g.dv_flat), &fp, &fo, &a, &m);
+  if (!rc) {
+    a.status = g.status;
+    rc = encode_bwd_maps(a, &m);
+  }
+  if (rc) {
+    cudaFreeAsync(ws, s);
+    return rc;
+  }
+  fa::bwd_carve_workspace(bwd_ws, a.B, a.H, a.ql, a.d, &a.lse2, &a.dvec, &a.dqacc,
+                          &a.dsink_part);
+  if ((e = fa::launch_bwd(a, m, s)) != cudaSuccess ||
+      (e = fa::launch_paged_scatter(g, s)) != cudaSuccess) {
+    cudaFreeAsync(ws, s);
+    return cuda_fail(e, "paged backward launch");
+  }
+  if ((e = cudaFreeAsync(ws, s)) != cudaSuccess)
+    return cuda_fail(e, "cudaFreeAsync (paged backward workspace)");
   return FA_OK;
 }
 

@@ -227,4 +227,26 @@ size_t paged_workspace_bytes(const PagedArgs& a, int splits);
 cudaError_t launch_paged(const PagedArgs& a, const PagedMaps& m, int splits, void* ws,
                          cudaStream_t stream);
 
+// Gradients through the paged cache (fa_paged_bwd.cu): the gather of each sequence's keys and
+// values into contiguous [B, Hk, capacity, d] tensors plus the bool mask of the flat problem,
+// and the scatter of its dK, dV back into the pages.
+struct PagedGradArgs {
+  const void* k_cache;   // bf16 [num_pages, Hk, page_size, d]
+  const void* v_cache;
+  const int32_t* table;  // [B, max_pages]
+  const int32_t* lens;   // [B]
+  void* k_flat;          // bf16 [B, Hk, capacity, d] (capacity = max_pages * page_size)
+  void* v_flat;
+  const void* dk_flat;   // the flat problem's dK, dV
+  const void* dv_flat;
+  void* dk_cache;        // outputs, zeroed before the scatter
+  void* dv_cache;
+  uint8_t* mask;         // [B, lq, capacity], 1 = visible
+  int* uses;             // [num_pages]: how many (sequence, slot) name each page; zeroed
+  int* status;
+  int B, Hk, lq, d, ps, max_pages, num_pages, causal;
+};
+cudaError_t launch_paged_gather(const PagedGradArgs& a, cudaStream_t stream);
+cudaError_t launch_paged_scatter(const PagedGradArgs& a, cudaStream_t stream);
+
 }  // namespace fa

@@ -282,7 +282,7 @@ int fa_train_bwd_noalloc(const void* q, const void* k, const void* v, const void
  * block_table[b * max_pages + j / page_size], slot j % page_size. The q_len queries are the
  * sequence's last positions: with causal = 1, query i sees key j iff
  * j <= lengths[b] - q_len + i. O = softmax(scale * q k^T) v; L = natural-log logsumexp. A query
- * that sees no key gets O = 0 and L = -inf. Forward only (no gradient). */
+ * that sees no key gets O = 0 and L = -inf. Gradients: fa_paged_attention_bwd below. */
 typedef struct fa_paged_params {
   int32_t batch;       /* sequences, >= 1 */
   int32_t n_heads;     /* query heads, a multiple of n_kv_heads */
@@ -316,6 +316,30 @@ typedef struct fa_paged_params {
 int fa_paged_attention(const void* q, const void* k_cache, const void* v_cache,
                        const int32_t* block_table, const int32_t* lengths, void* o, float* lse,
                        const fa_paged_params* p, void* stream);
+
+/* Gradients through the paged cache: dQ and the gradients of both caches for the attention of
+ * fa_paged_attention. Page "nuvec-core tests/fast.rs",
+ * `paged_attention_equals_contiguous_attention`, checks the gradients for q and the caches
+ * ("paged grads").
+ *   q, k_cache, v_cache, block_table, lengths, p : as given to fa_paged_attention
+ *   o, lse     : that call's outputs (lse required: f32 [batch, n_heads, q_len], 16-byte
+ *                aligned)
+ *   dO         : bf16 [batch, n_heads, q_len, head_dim], the gradient of the loss for o
+ *   dq         : output, bf16 like q
+ *   dk_cache, dv_cache : outputs, bf16 like the caches: every element is written; a slot
+ *                that no (sequence, query) reads gets 0.
+ * Each page may hold keys of one sequence only: a page named twice among the used table
+ * entries (its gradient would be a sum) gets no gradient written and makes fa_device_status
+ * return FA_ERR_BAD_INPUT, as do lengths and table entries out of range (read as in the
+ * forward). The call gathers every sequence's keys and values into contiguous tensors and
+ * runs the training backward on them (scratch: 4 * batch * n_kv_heads * max_pages *
+ * page_size * head_dim * 2 bytes plus the backward's own, taken with cudaMallocAsync on
+ * `stream`). p->num_splits is ignored. Returns FA_OK, FA_ERR_INVALID (parameters, pointers,
+ * batch * q_len above 65535), FA_ERR_UNSUPPORTED or FA_ERR_CUDA. */
+int fa_paged_attention_bwd(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_table, const int32_t* lengths, const void* o,
+                           const float* lse, const void* dO, void* dq, void* dk_cache,
+                           void* dv_cache, const fa_paged_params* p, void* stream);
 
 /* ------------------------------------------------------------------ bounded waits, diagnostics
  * Sets the limit of one barrier wait inside the kernels launched after this call, from any

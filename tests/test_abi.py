@@ -231,6 +231,27 @@ def test_paged_bad_pointers_rejected(lib):
     assert _paged(lib, PAGED_GOOD, q=FAKE + 8) == fa.FA_ERR_INVALID
 
 
+def _paged_bwd(lib, params, lse=FAKE, dk=FAKE, q=FAKE):
+    p = fa.FaPagedParams(**params)
+    return lib.fa_paged_attention_bwd(q, FAKE, FAKE, FAKE, FAKE, FAKE, lse, FAKE, FAKE, dk, FAKE,
+                                      ctypes.byref(p), None)
+
+
+@pytest.mark.parametrize("field,value", BAD_PAGED)
+def test_paged_bwd_bad_params_rejected(lib, field, value):
+    assert _paged_bwd(lib, dict(PAGED_GOOD, **{field: value})) == fa.FA_ERR_INVALID
+
+
+def test_paged_bwd_bad_pointers_rejected(lib):
+    assert _paged_bwd(lib, PAGED_GOOD, lse=None) == fa.FA_ERR_INVALID  # lse is required
+    assert _paged_bwd(lib, PAGED_GOOD, lse=FAKE + 4) == fa.FA_ERR_INVALID
+    assert _paged_bwd(lib, PAGED_GOOD, dk=FAKE + 2) == fa.FA_ERR_INVALID
+    assert _paged_bwd(lib, PAGED_GOOD, q=None) == fa.FA_ERR_INVALID
+    # the mask of the flat problem has batch * q_len rows of grid y
+    assert _paged_bwd(lib, dict(PAGED_GOOD, batch=300, n_heads=2, n_kv_heads=2, q_len=256)) == \
+        fa.FA_ERR_INVALID
+
+
 def test_paged_params_struct_layout():
     assert ctypes.sizeof(fa.FaPagedParams) == 48
     assert fa.FaPagedParams.scale.offset == 32
