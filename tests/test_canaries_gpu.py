@@ -1,10 +1,11 @@
 """Guard bands around every output: the kernels must write exactly their outputs.
 
 Each output (O, L, dQ, dK, dV, dsinks; the packed tensors of a variable-length batch; the
-paged attention's O and L) is placed in the middle of a larger device buffer whose two guard
-bands of 4096 elements hold a sentinel bit pattern. After ragged tiles, ql > kl, windows,
-masks, sinks, a value head dim below the q/k one, the deterministic backward, packed
-sequences and paged calls, the guard bands must hold the sentinel bit for bit (nothing was
+paged attention's O and L and its gradients dQ, dK cache, dV cache) is placed in the middle of
+a larger device buffer whose two guard bands of 4096 elements hold a sentinel bit pattern.
+After ragged tiles, ql > kl, windows, masks, sinks, a value head dim below the q/k one, the
+deterministic backward, packed sequences, outputs written as transposed views and paged
+calls, the guard bands must hold the sentinel bit for bit (nothing was
 written outside an output), and no sentinel may be left inside (every output element was
 written). The guarded results must also equal the same calls on plain allocations: bit for bit
 for O, L, dK, dV (their order of operations is fixed) and within the gradient tolerance for dQ,
@@ -213,3 +214,54 @@ def test_paged_outputs_stay_inside_their_buffers(q_len, splits):
                                   num_splits=splits)
     torch.cuda.synchronize()
     assert torch.equal(o.t, o2) and torch.equal(lse.t, lse2)
+    # the gradients through the cache: dQ and both cache gradients
+    do = bf(fa_inputs.normal_bf16(4000 + q_len, tuple(q.shape)))
+    dq = Guarded(tuple(q.shape), torch.bfloat16)
+    dkc, dvc = Guarded(tuple(kc.shape), torch.bfloat16), Guarded(tuple(vc.shape), torch.bfloat16)
+    fa.fa_paged_attention_bwd(q, kc, vc, table, lens, o.t, lse.t, do, dq.t, dkc.t, dvc.t, params)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(True) == fa.FA_OK
+    for name, gd in (("dQ", dq), ("dK cache", dkc), ("dV cache", dvc)):
+        gd.check(name)
+    g2 = fa.paged_attention_bwd(q, kc, vc, table, lens, o2, lse2, do, scale=d ** -0.5,
+                                causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(dkc.t, g2[1]) and torch.equal(dvc.t, g2[2])
+    _grad_close(dq.t, g2[0], "dq")
+
+
+@pytest.mark.parametrize("layout", [1, 2, 3], ids=["q_side", "kv_side", "both"])
+def test_transposed_views_stay_inside_their_buffers(layout):
+    """Outputs written as [B, seq, heads, dim] memory (transposed views) stay in their buffers."""
+    import torch
+
+    import flash_attention_gb300 as fa
+
+    B, H, Hk, ql, kl, d = 2, 4, 2, 130, 190, 128
+    g = torch.Generator(device="cpu").manual_seed(77 + layout)
+
+    def rnd(*shape, bshd, std=1.0):  # logical [B, heads, rows, d]
+        t = (torch.randn(*shape, generator=g) * std).to(torch.bfloat16).cuda()
+        return t.transpose(1, 2).contiguous().transpose(1, 2) if bshd else t
+
+    qs, ks = bool(layout & 1), bool(layout & 2)
+    q, do = rnd(B, H, ql, d, bshd=qs), rnd(B, H, ql, d, bshd=qs, std=0.1)
+    k, v = rnd(B, Hk, kl, d, bshd=ks), rnd(B, Hk, kl, d, bshd=ks)
+
+    def out(shape, bshd):  # a guarded output with the layout of its side
+        if not bshd:
+            return Guarded(shape, torch.bfloat16), lambda gd: gd.t
+        b_, h_, r_, d_ = shape
+        return Guarded((b_, r_, h_, d_), torch.bfloat16), lambda gd: gd.t.transpose(1, 2)
+
+    params = fa.make_params(q, k, scale=d ** -0.5, causal=True)
+    (o, ov), lse = out((B, H, ql, d), qs), Guarded((B, H, ql), torch.float32)
+    (dq, dqv), (dk, dkv), (dv, dvv) = out((B, H, ql, d), qs), out((B, Hk, kl, d), ks), \
+        out((B, Hk, kl, d), ks)
+    opt = fa.make_options(q, k, v=v)
+    fa.fa_train_fwd_ex(q, k, v, None, ov(o), lse.t, params, opt)
+    fa.fa_train_bwd_ex(q, k, v, ov(o), lse.t, do, None, dqv(dq), dkv(dk), dvv(dv), params, opt)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(True) == fa.FA_OK
+    for name, gd in (("O", o), ("L", lse), ("dQ", dq), ("dK", dk), ("dV", dv)):
+        gd.check(name)
