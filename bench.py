@@ -123,6 +123,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=sorted(fa_inputs.BY_NAME) + sorted(fa_inputs.DECODE_BY_NAME)
+                    + sorted(PAGED_GRAD)
                     + sorted(fa_inputs.VARLEN_BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -338,6 +339,34 @@ def run_reference(args, w):
 
 # ------------------------------------------------------------------ paged key/value cache
 PAGED_METRIC = "paged attention: key/value bytes read per second (bf16 cache) at 1 GB300"
+PAGED_GRAD_METRIC = ("paged attention forward + gradients for q and the caches: bytes moved per "
+                     "second (bf16 cache) at 1 GB300")
+# Gradient workloads: the forward and fa_paged_attention_bwd on a decode workload's caches.
+PAGED_GRAD = {"paged_decode_d128_grad": "paged_decode_d128",
+              "paged_prefill4_d128_grad": "paged_prefill4_d128"}
+
+
+def paged_grad_bytes(w, x):
+    """Algorithmic bytes of one forward + gradient step, and of each gradient kernel.
+    The step: the forward's, then the gradients' least traffic (q, O, dO in and dq out; the
+    keys and values each sequence reads; both cache gradients written whole, since slots no
+    sequence reads get 0). Per kernel, what its own interface makes it move: the gather (used
+    keys and values in, the flat [B, Hk, capacity, d] copies out), the backward main pass on
+    the flat problem (flat K, V in and dK, dV out; q and dO in) and the scatter (flat dK, dV
+    in; the rows of the used pages out)."""
+    el = w.head_dim * 2
+    bs = w.page_size
+    lens = x.lengths.astype(np.int64)
+    used = int(lens.sum()) * w.n_kv_heads * el
+    used_pages = int(((lens + bs - 1) // bs * bs).sum()) * w.n_kv_heads * el
+    flat = w.batch * w.n_kv_heads * x.block_table.shape[1] * bs * el
+    cache = x.k_cache.shape[0] * w.n_kv_heads * bs * el
+    qbytes = w.batch * w.n_heads * w.q_len * el
+    step = paged_bytes(w, x) + 4 * qbytes + 2 * used + 2 * cache
+    per = {"paged_gather_kernel": 2 * used + 2 * flat,
+           "bwd_main_kernel": 4 * flat + 2 * qbytes,
+           "paged_scatter_kernel": 2 * flat + 2 * used_pages}
+    return step, per
 
 
 def paged_bytes(w, x):
@@ -374,6 +403,36 @@ def paged_oracle_sample(w, x, budget_s=10.0, cores=None):
     return nbytes, spent, n
 
 
+def paged_grad_oracle_sample(w, x, do_bits, total_bytes, budget_s=10.0, cores=None):
+    """The CPU oracle's paged forward and gradients on whole sequences, taken in turn until
+    ~budget_s. Each sequence runs on a cache of just its own pages (copied outside the timed
+    part). Returns (bytes, seconds, n): the sequences' share of the step's algorithmic bytes,
+    by key count."""
+    import oracle
+
+    q, kc, vc = x.widened()
+    do = fa_inputs.bf16_bits_to_f32(do_bits)
+    bs = w.page_size
+    total_keys = max(int(x.lengths.astype(np.int64).sum()), 1)
+    spent, nbytes, n = 0.0, 0, 0
+    while spent < budget_s and n < w.batch:
+        L = int(x.lengths[n])
+        pages = x.block_table[n, :-(-L // bs)]
+        sub_k, sub_v = kc[pages], vc[pages]
+        table = np.arange(len(pages), dtype=np.int32)[None]
+        lens = x.lengths[n:n + 1]
+        t0 = time.perf_counter()
+        o = oracle.paged_fwd(q[n:n + 1], sub_k, sub_v, table, lens, scale=w.scale,
+                             causal=w.causal, nthreads=cores)
+        oracle.paged_bwd(q[n:n + 1], sub_k, sub_v, table, lens, do[n:n + 1], scale=w.scale,
+                         causal=w.causal, nthreads=cores)
+        spent += time.perf_counter() - t0
+        del o
+        nbytes += total_bytes * L // total_keys
+        n += 1
+    return nbytes, spent, n
+
+
 def run_paged_reference(args, w):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -405,7 +464,7 @@ def run_paged_reference(args, w):
     print(json.dumps(out), flush=True)
 
 
-def run_paged(args, w):
+def run_paged(args, w, grad=False):
     import torch
 
     rank, world, local = dist_env()
@@ -436,9 +495,17 @@ def run_paged(args, w):
                               w.page_size, x.block_table.shape[1], x.k_cache.shape[0],
                               w.scale, int(w.causal), 0, 0)
     stream = torch.cuda.current_stream(dev)
+    if grad:
+        h_do = bf(fa_inputs.normal_bf16(fa_inputs.SEED_BASE + 77 + rank, tuple(x.q.shape),
+                                        0.1)).pin_memory()
+        do = h_do.to(dev)
+        dq, dkc, dvc = torch.empty_like(q), torch.empty_like(kc), torch.empty_like(vc)
 
     def step():
         fa.fa_paged_attention(q, kc, vc, tb, ln, o, lse, params, stream)
+        if grad:
+            fa.fa_paged_attention_bwd(q, kc, vc, tb, ln, o, lse, do, dq, dkc, dvc, params,
+                                      stream)
 
     def barrier():
         if world > 1:
@@ -481,29 +548,42 @@ def run_paged(args, w):
         raise RuntimeError("paged kernel reported an error during the timed steps")
     tot_ms = reduce_max(e0.elapsed_time(e1) / args.steps, world, dev)
     nbytes = paged_bytes(w, x)
+    kern_bytes = {"paged_attn_kernel": nbytes}
+    if grad:
+        nbytes, per = paged_grad_bytes(w, x)
+        kern_bytes.update(per)
     value = world * nbytes / (tot_ms * 1e-3) / 1e9
     peaks = load_peaks()
     hbm = peaks["hbm_gbs"]
-    ms, n = prof["paged_attn_kernel"]
+    # the dominant kernel by device time, against the bytes it must move
+    dom = max(kern_bytes, key=lambda k: prof[k][0])
+    ms, n = prof[dom]
     kern_ms = ms / max(n, 1)
-    roofline = {"bound": "hbm", "kernel": "paged_attn_kernel",
-                "achieved": nbytes / (kern_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
-                "frac": nbytes / (kern_ms * 1e-3) / 1e9 / hbm,
-                "traffic": recorded_traffic("paged_attn_kernel", w.name),
+    roofline = {"bound": "hbm", "kernel": dom,
+                "achieved": kern_bytes[dom] / (kern_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                "frac": kern_bytes[dom] / (kern_ms * 1e-3) / 1e9 / hbm,
+                "traffic": recorded_traffic(dom, w.name) if not grad else None,
                 "peak_source": f"hbm_gbs, {peaks['source']}",
                 "per_kernel_ms": {k: (t / max(c, 1)) for k, (t, c) in prof.items() if c}}
     launches = sum(c for _, c in prof.values())
+    if grad:  # the gather's timed region holds two launches (gather and mask)
+        launches += prof["paged_gather_kernel"][1]
 
     e2e = None
     if not args.no_e2e:
         h_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        h_dq = torch.empty(q.shape, dtype=q.dtype).pin_memory() if grad else None
 
         def e2e_step():  # new queries, table and lengths in; the attention output back
             q.copy_(h_q, non_blocking=True)
             tb.copy_(h_tb, non_blocking=True)
             ln.copy_(h_ln, non_blocking=True)
+            if grad:
+                do.copy_(h_do, non_blocking=True)
             step()
             h_o.copy_(o, non_blocking=True)
+            if grad:
+                h_dq.copy_(dq, non_blocking=True)
 
         for _ in range(2):
             e2e_step()
@@ -516,24 +596,37 @@ def run_paged(args, w):
         f1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = reduce_max(f0.elapsed_time(f1) / args.steps, world, dev)
-        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_tb, h_ln))
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_tb, h_ln) + ((h_do,) if grad else ()))
         e2e = {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": h_o.numel() * h_o.element_size(),
-               "note": "the key/value cache stays resident on the GPU, as in serving"}
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size()
+                                         for t in (h_o,) + ((h_dq,) if grad else ())),
+               "note": "the key/value cache stays resident on the GPU, as in serving"
+                       + ("; its gradients stay on the GPU, dq comes back" if grad else "")}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = cpu_cores()
-        b_, s_, n_ = paged_oracle_sample(w, x, 10.0, cores)
+        if grad:
+            b_, s_, n_ = paged_grad_oracle_sample(w, x, h_do.view(torch.int16).numpy()
+                                                  .view(np.uint16), nbytes, 10.0, cores)
+            what = "forward + gradients"
+        else:
+            b_, s_, n_ = paged_oracle_sample(w, x, 10.0, cores)
+            what = "forward"
         cpu = {"value": b_ / s_ / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-               "sample": f"{n_} whole sequence(s) of {w.batch}, f64, {s_:.1f} s"}
+               "sample": f"{what} of {n_} whole sequence(s) of {w.batch}, f64, {s_:.1f} s"}
 
     if rank == 0:
-        out = {"metric": PAGED_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        cfg = paged_config(w, world)
+        if grad:
+            cfg["workload"] = w.name + "_grad"
+            cfg["step"] = "fa_paged_attention + fa_paged_attention_bwd (dO ~ N(0, 0.01))"
+        out = {"metric": PAGED_GRAD_METRIC if grad else PAGED_METRIC, "value": value,
+               "unit": "GB/s", "n_gpus": world,
                "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms,
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-               "dtype": "bf16", "data": "synthetic", "config": paged_config(w, world),
+               "dtype": "bf16", "data": "synthetic", "config": cfg,
                "bytes_per_step": nbytes, "roofline": roofline, "cpu_baseline": cpu,
                "e2e": e2e, "gpu_launches": int(launches), "clocks": clk}
         print(json.dumps(out), flush=True)
@@ -1045,6 +1138,14 @@ def main():
             run_varlen_reference(args, w)
         else:
             run_varlen(args, w)
+        return
+    if args.workload in PAGED_GRAD:
+        w = fa_inputs.DECODE_BY_NAME[PAGED_GRAD[args.workload]]
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times "
+                              "the oracle's paged forward only"}), flush=True)
+        else:
+            run_paged(args, w, grad=True)
         return
     if args.workload in fa_inputs.DECODE_BY_NAME:
         w = fa_inputs.DECODE_BY_NAME[args.workload]

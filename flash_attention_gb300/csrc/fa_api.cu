@@ -287,6 +287,8 @@ const char* fa_kernel_name(int id) {
     case FA_KERNEL_BWD_DQ_DET: return "bwd_dq_det_kernel";
     case FA_KERNEL_PAGED: return "paged_attn_kernel";
     case FA_KERNEL_PAGED_COMBINE: return "paged_combine_kernel";
+    case FA_KERNEL_PAGED_GATHER: return "paged_gather_kernel";
+    case FA_KERNEL_PAGED_SCATTER: return "paged_scatter_kernel";
     case FA_KERNEL_BWD_MAIN: return "bwd_main_kernel";
     case FA_KERNEL_BWD_DQ: return "bwd_dq_kernel";
     default: return "unknown";

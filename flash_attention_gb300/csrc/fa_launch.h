@@ -44,7 +44,9 @@ enum KernelId {
   kKernBwdDqDet = 4,
   kKernPaged = 5,
   kKernPagedCombine = 6,
-  kNumKernels = 7
+  kKernPagedGather = 7,
+  kKernPagedScatter = 8,
+  kNumKernels = 9
 };
 
 // Records a timing event before (end = 0) or after (end = 1) a launch on `s` when timing is

@@ -103,18 +103,25 @@ __global__ void __launch_bounds__(256) paged_scatter_kernel(PagedGradArgs a) {
 cudaError_t launch_paged_gather(const PagedGradArgs& a, cudaStream_t s) {
   const long long cap = (long long)a.max_pages * a.ps;
   const long long chunks = cap * (a.d / 8);
+  profile_mark(kKernPagedGather, 0, s);
   paged_gather_kernel<<<dim3((unsigned)((chunks + 255) / 256), a.B * a.Hk), 256, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  paged_mask_kernel<<<dim3((unsigned)((cap + 255) / 256), a.B * a.lq), 256, 0, s>>>(a);
-  return cudaGetLastError();
+  if (e == cudaSuccess) {
+    paged_mask_kernel<<<dim3((unsigned)((cap + 255) / 256), a.B * a.lq), 256, 0, s>>>(a);
+    e = cudaGetLastError();
+  }
+  profile_mark(kKernPagedGather, 1, s);
+  return e;
 }
 
 cudaError_t launch_paged_scatter(const PagedGradArgs& a, cudaStream_t s) {
   const long long cap = (long long)a.max_pages * a.ps;
   const long long chunks = cap * (a.d / 8);
+  profile_mark(kKernPagedScatter, 0, s);
   paged_scatter_kernel<<<dim3((unsigned)((chunks + 255) / 256), a.B * a.Hk), 256, 0, s>>>(a);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  profile_mark(kKernPagedScatter, 1, s);
+  return e;
 }
 
 }  // namespace fa

@@ -217,7 +217,9 @@ int fa_train_bwd(const void* q, const void* k, const void* v, const void* o, con
 #define FA_KERNEL_BWD_DQ_DET 4 /* deterministic mode: query-tile-major dQ */
 #define FA_KERNEL_PAGED 5      /* paged key/value cache attention */
 #define FA_KERNEL_PAGED_COMBINE 6 /* merge of the key splits of fa_paged_attention */
-#define FA_NUM_KERNELS 7
+#define FA_KERNEL_PAGED_GATHER 7  /* fa_paged_attention_bwd: pages -> contiguous K, V and mask */
+#define FA_KERNEL_PAGED_SCATTER 8 /* fa_paged_attention_bwd: dK, dV back into the pages */
+#define FA_NUM_KERNELS 9
 
 /* Turns timing on (1) or off (0). Returns FA_OK. */
 int fa_profile_enable(int on);

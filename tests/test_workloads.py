@@ -104,3 +104,45 @@ def test_reference_arm_json_line():
     assert d["impl"] == "reference" and d["value"] > 0 and d["config"]["workload"] == "tiny_gqa_d64"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_paged_grad_bytes_and_oracle_sample():
+    """The paged-gradient bench counts: brute-force byte counts on a small cache, and the
+    oracle sample (forward + gradients per sequence on its own pages) covers whole sequences
+    and matches the oracle on the full cache for the first one."""
+    import os
+    import sys
+
+    import numpy as np
+
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    import oracle
+
+    w = fa_inputs.DecodeWorkload("tiny_paged_grad", 3, 4, 2, 1, 64, 8, 5, 30)
+    x = fa_inputs.make_paged_inputs(w, index=7)
+    step, per = bench.paged_grad_bytes(w, x)
+    el = 64 * 2
+    used_keys = sum(int(n) for n in x.lengths)
+    used_slots = sum(-(-int(n) // 8) * 8 for n in x.lengths)
+    flat = 3 * 2 * x.block_table.shape[1] * 8 * el
+    assert per["paged_gather_kernel"] == 2 * used_keys * 2 * el + 2 * flat
+    assert per["paged_scatter_kernel"] == 2 * flat + 2 * used_slots * 2 * el
+    qb = 3 * 4 * 1 * el
+    assert step == (bench.paged_bytes(w, x) + 4 * qb + 2 * used_keys * 2 * el
+                    + 2 * x.k_cache.size * 2)
+
+    do = fa_inputs.normal_bf16(5, tuple(x.q.shape), 0.1)
+    b_, s_, n_ = bench.paged_grad_oracle_sample(w, x, do, step, budget_s=1e-9)
+    assert n_ == 1 and 0 < b_ < step and s_ > 0
+    # the per-sequence copy of its own pages gives the full cache's gradients
+    q, kc, vc = x.widened()
+    dof = fa_inputs.bf16_bits_to_f32(do)
+    L = int(x.lengths[0])
+    pages = x.block_table[0, :-(-L // 8)]
+    sub = oracle.paged_bwd(q[:1], kc[pages], vc[pages], np.arange(len(pages))[None],
+                           x.lengths[:1], dof[:1], scale=w.scale, causal=True)
+    full = oracle.paged_bwd(q[:1], np.nan_to_num(kc), np.nan_to_num(vc), x.block_table[:1],
+                            x.lengths[:1], dof[:1], scale=w.scale, causal=True)
+    np.testing.assert_allclose(sub[0], full[0], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(np.nan_to_num(sub[1]), full[1][pages], rtol=1e-12, atol=1e-14)
