@@ -351,21 +351,18 @@ def paged_grad_bytes(w, x):
     The step: the forward's, then the gradients' least traffic (q, O, dO in and dq out; the
     keys and values each sequence reads; both cache gradients written whole, since slots no
     sequence reads get 0). Per kernel, what its own interface makes it move: the gather (used
-    keys and values in, the flat [B, Hk, capacity, d] copies out), the backward main pass on
-    the flat problem (flat K, V in and dK, dV out; q and dO in) and the scatter (flat dK, dV
-    in; the rows of the used pages out)."""
+    keys and values in and out, packed; q, O, dO in and out, packed), the backward main pass on
+    the packed problem (K, V in and dK, dV out; q and dO in) and the scatter (packed dK, dV in;
+    both cache gradients out; dq in and out)."""
     el = w.head_dim * 2
-    bs = w.page_size
     lens = x.lengths.astype(np.int64)
     used = int(lens.sum()) * w.n_kv_heads * el
-    used_pages = int(((lens + bs - 1) // bs * bs).sum()) * w.n_kv_heads * el
-    flat = w.batch * w.n_kv_heads * x.block_table.shape[1] * bs * el
-    cache = x.k_cache.shape[0] * w.n_kv_heads * bs * el
+    cache = x.k_cache.shape[0] * w.n_kv_heads * w.page_size * el
     qbytes = w.batch * w.n_heads * w.q_len * el
     step = paged_bytes(w, x) + 4 * qbytes + 2 * used + 2 * cache
-    per = {"paged_gather_kernel": 2 * used + 2 * flat,
-           "bwd_main_kernel": 4 * flat + 2 * qbytes,
-           "paged_scatter_kernel": 2 * flat + 2 * used_pages}
+    per = {"paged_gather_kernel": 4 * used + 6 * qbytes,
+           "bwd_main_kernel": 4 * used + 2 * qbytes,
+           "paged_scatter_kernel": 2 * used + 2 * cache + 2 * qbytes}
     return step, per
 
 

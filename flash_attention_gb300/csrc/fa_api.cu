@@ -605,73 +605,104 @@ int fa_paged_attention_bwd(const void* q, const void* k_cache, const void* v_cac
   if ((rc = check_bf16(o)) || (rc = check_bf16(dO)) || (rc = check_bf16(dq)) ||
       (rc = check_bf16(dk_cache)) || (rc = check_bf16(dv_cache)) || (rc = check_f32(lse)))
     return rc;
-  if ((int64_t)p->batch * p->q_len > 65535) return FA_ERR_INVALID;  // grid y of the mask
+  const int B = p->batch, H = p->n_heads, Hk = p->n_kv_heads, lq = p->q_len, d = p->head_dim;
+  const int G = H / Hk;
+  const int64_t cap = (int64_t)p->max_pages * p->page_size;
+  // the packed problem: a variable-length batch of B sequences, one per sequence's used keys;
+  // with `pack` the G query heads of a kv head are its G * lq rows (no row's keys depend on
+  // its position: decode, or no causal rule)
+  const bool pack = lq == 1 || !p->causal;
+  const int Hq = pack ? Hk : H;
+  const int64_t rq = pack ? (int64_t)G * lq : lq;
+  const int64_t total_q = B * rq, total_k = B * cap;
+  if (rq > kMaxLen || total_q * Hq > INT32_MAX / 2 || total_k * Hk > INT32_MAX / 2)
+    return FA_ERR_INVALID;
+  const int64_t chunks = d / 8;  // 16-byte chunks per row: grid x of the gather kernels
+  if ((int64_t)p->num_pages * p->page_size * chunks / 256 >= INT32_MAX ||
+      (int64_t)B * H * lq * chunks / 256 >= INT32_MAX)
+    return FA_ERR_INVALID;
   if ((rc = check_device())) return rc;
   cudaError_t e = get_encoder();
   if (e != cudaSuccess) return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
   int dev = 0;
   cudaGetDevice(&dev);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int B = p->batch, H = p->n_heads, Hk = p->n_kv_heads, lq = p->q_len, d = p->head_dim;
-  const int64_t cap = (int64_t)p->max_pages * p->page_size;
-  // the flat problem: B sequences of lq queries over `cap` key slots, masked
   fa_params fp;
   fp.batch = B;
-  fp.n_heads = H;
+  fp.n_heads = Hq;
   fp.n_kv_heads = Hk;
-  fp.ql = lq;
+  fp.ql = (int32_t)rq;
   fp.kl = (int32_t)cap;
   fp.head_dim = d;
   fp.scale = p->scale;
-  fp.causal = 0;
+  fp.causal = pack ? 0 : 1;  // (bottom-right: query i of a sequence sees keys <= len - lq + i)
   fa_options fo = default_options(&fp);
-  fo.mask_type = FA_MASK_BOOL;
-  fo.mask_stride_b = (int64_t)lq * cap;
-  fo.mask_stride_h = 0;
-  fo.mask_stride_q = cap;
-  const size_t flat = align256((size_t)B * Hk * cap * d * 2);
-  const size_t mask_bytes = align256((size_t)B * lq * cap);
-  const size_t uses_bytes = align256((size_t)p->num_pages * 4);
-  const size_t bwd_bytes = fa::bwd_workspace_bytes(B, H, lq, d);
+  fo.total_q = (int32_t)total_q;
+  fo.total_k = (int32_t)total_k;  // an upper bound: the keys used are cu_k[B] <= B * capacity
+  const size_t kv_bytes = align256((size_t)Hk * total_k * d * 2);
+  const size_t q_bytes = align256((size_t)B * H * lq * d * 2);
+  const size_t lse_bytes = align256((size_t)B * H * lq * 4);
+  const size_t cu_bytes = align256((size_t)(B + 1) * 4);
+  const size_t owner_bytes = align256((size_t)p->num_pages * 4);
+  const size_t bwd_bytes = fa::bwd_workspace_bytes(B, Hq, (int)rq, d);
+  const size_t total =
+      4 * kv_bytes + 4 * q_bytes + lse_bytes + 2 * cu_bytes + owner_bytes + bwd_bytes;
   void* ws = nullptr;
-  e = cudaMallocAsync(&ws, 4 * flat + mask_bytes + uses_bytes + bwd_bytes, s);
+  e = cudaMallocAsync(&ws, total, s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync (paged backward workspace)");
   uint8_t* w = static_cast<uint8_t*>(ws);
+  auto take = [&w](size_t n) {
+    uint8_t* r = w;
+    w += n;
+    return r;
+  };
   fa::PagedGradArgs g;
   g.k_cache = k_cache;
   g.v_cache = v_cache;
   g.table = block_table;
   g.lens = lengths;
-  g.k_flat = w;
-  g.v_flat = w + flat;
-  g.dk_flat = w + 2 * flat;
-  g.dv_flat = w + 3 * flat;
+  g.q = q;
+  g.o = o;
+  g.dO = dO;
+  g.lse = lse;
+  g.dq = dq;
   g.dk_cache = dk_cache;
   g.dv_cache = dv_cache;
-  g.mask = w + 4 * flat;
-  g.uses = reinterpret_cast<int*>(w + 4 * flat + mask_bytes);
+  g.k_pack = take(kv_bytes);
+  g.v_pack = take(kv_bytes);
+  g.dk_pack = take(kv_bytes);
+  g.dv_pack = take(kv_bytes);
+  g.q_pack = take(q_bytes);
+  g.o_pack = take(q_bytes);
+  g.do_pack = take(q_bytes);
+  g.dq_pack = take(q_bytes);
+  g.lse_pack = reinterpret_cast<float*>(take(lse_bytes));
+  g.cu_q = reinterpret_cast<int32_t*>(take(cu_bytes));
+  g.cu_k = reinterpret_cast<int32_t*>(take(cu_bytes));
+  g.owner = reinterpret_cast<int32_t*>(take(owner_bytes));
+  void* bwd_ws = take(bwd_bytes);
   g.B = B;
+  g.H = H;
   g.Hk = Hk;
   g.lq = lq;
   g.d = d;
   g.ps = p->page_size;
   g.max_pages = p->max_pages;
   g.num_pages = p->num_pages;
-  g.causal = p->causal;
-  void* bwd_ws = w + 4 * flat + mask_bytes + uses_bytes;
-  const size_t cache_bytes = (size_t)p->num_pages * Hk * p->page_size * d * 2;
+  g.pack = pack ? 1 : 0;
+  fo.cu_seqlens_q = g.cu_q;
+  fo.cu_seqlens_k = g.cu_k;
   fa::BwdArgs a;
   fa::BwdMaps m;
   if ((e = device_status_word(dev, &g.status)) != cudaSuccess ||
-      (e = cudaMemsetAsync(dk_cache, 0, cache_bytes, s)) != cudaSuccess ||
-      (e = cudaMemsetAsync(dv_cache, 0, cache_bytes, s)) != cudaSuccess ||
-      (e = cudaMemsetAsync(g.uses, 0, (size_t)p->num_pages * 4, s)) != cudaSuccess ||
+      (e = cudaMemsetAsync(g.owner, 0xFF, (size_t)p->num_pages * 4, s)) != cudaSuccess ||
       (e = fa::launch_paged_gather(g, s)) != cudaSuccess) {
     cudaFreeAsync(ws, s);
     return cuda_fail(e, "paged backward: gather");
   }
-  rc = prepare_bwd(q, g.k_flat, g.v_flat, o, lse, dO, g.mask, dq, const_cast<void*>(g.dk_flat),
-                   const_cast<void*>(g.dv_flat), &fp, &fo, &a, &m);
+  rc = prepare_bwd(g.q_pack, g.k_pack, g.v_pack, g.o_pack, g.lse_pack, g.do_pack, nullptr,
+                   const_cast<void*>(g.dq_pack), const_cast<void*>(g.dk_pack),
+                   const_cast<void*>(g.dv_pack), &fp, &fo, &a, &m);
   if (!rc) {
     a.status = g.status;
     rc = encode_bwd_maps(a, &m);

@@ -229,26 +229,42 @@ size_t paged_workspace_bytes(const PagedArgs& a, int splits);
 cudaError_t launch_paged(const PagedArgs& a, const PagedMaps& m, int splits, void* ws,
                          cudaStream_t stream);
 
-// Gradients through the paged cache (fa_paged_bwd.cu): the gather of each sequence's keys and
-// values into contiguous [B, Hk, capacity, d] tensors plus the bool mask of the flat problem,
-// and the scatter of its dK, dV back into the pages.
+// Gradients through the paged cache (fa_paged_bwd.cu): the paged problem is turned into a
+// variable-length batch (sequence b = its used keys, packed head-major without padding) for
+// the training backward, and its gradients are put back into the pages and the [B, H, lq, d]
+// layout. With `pack`, the G query heads of a kv head are one sequence's G * lq query rows
+// (row g * lq + i), which the backward then treats as one head.
 struct PagedGradArgs {
   const void* k_cache;   // bf16 [num_pages, Hk, page_size, d]
   const void* v_cache;
   const int32_t* table;  // [B, max_pages]
   const int32_t* lens;   // [B]
-  void* k_flat;          // bf16 [B, Hk, capacity, d] (capacity = max_pages * page_size)
-  void* v_flat;
-  const void* dk_flat;   // the flat problem's dK, dV
-  const void* dv_flat;
-  void* dk_cache;        // outputs, zeroed before the scatter
+  const void* q;         // bf16 [B, H, lq, d]
+  const void* o;
+  const void* dO;
+  const float* lse;      // f32 [B, H, lq]
+  void* dq;              // output, bf16 [B, H, lq, d]
+  void* dk_cache;        // outputs, bf16 like the caches, every element written
   void* dv_cache;
-  uint8_t* mask;         // [B, lq, capacity], 1 = visible
-  int* uses;             // [num_pages]: how many (sequence, slot) name each page; zeroed
+  void* k_pack;          // bf16 [Hk, B * capacity, d]: sequence b's keys at rows cu_k[b] ..
+  void* v_pack;
+  const void* dk_pack;   // the packed problem's dK, dV
+  const void* dv_pack;
+  void* q_pack;          // bf16 [Hq, B * rq, d] (Hq = Hk with pack, else H; rq = rows per
+  void* o_pack;          // sequence, G * lq with pack, else lq)
+  void* do_pack;
+  const void* dq_pack;
+  float* lse_pack;       // f32 [Hq, B * rq]
+  int32_t* cu_q;         // [B + 1]: b * rq
+  int32_t* cu_k;         // [B + 1]: prefix sums of the (clamped) lengths
+  int32_t* owner;        // [num_pages]: b * max_pages + slot of the one table entry that uses
+                         // the page; -1 (set before the gather) none, -2 two or more
   int* status;
-  int B, Hk, lq, d, ps, max_pages, num_pages, causal;
+  int B, H, Hk, lq, d, ps, max_pages, num_pages, pack;
 };
+// The offsets, the packed K, V (and the owner of every used page), the packed q-side tensors.
 cudaError_t launch_paged_gather(const PagedGradArgs& a, cudaStream_t stream);
+// Both cache gradients whole (zero where no sequence reads) and dq.
 cudaError_t launch_paged_scatter(const PagedGradArgs& a, cudaStream_t stream);
 
 }  // namespace fa

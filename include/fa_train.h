@@ -217,8 +217,8 @@ int fa_train_bwd(const void* q, const void* k, const void* v, const void* o, con
 #define FA_KERNEL_BWD_DQ_DET 4 /* deterministic mode: query-tile-major dQ */
 #define FA_KERNEL_PAGED 5      /* paged key/value cache attention */
 #define FA_KERNEL_PAGED_COMBINE 6 /* merge of the key splits of fa_paged_attention */
-#define FA_KERNEL_PAGED_GATHER 7  /* fa_paged_attention_bwd: pages -> contiguous K, V and mask */
-#define FA_KERNEL_PAGED_SCATTER 8 /* fa_paged_attention_bwd: dK, dV back into the pages */
+#define FA_KERNEL_PAGED_GATHER 7  /* fa_paged_attention_bwd: pages -> packed K, V, q side */
+#define FA_KERNEL_PAGED_SCATTER 8 /* fa_paged_attention_bwd: gradients back into the pages, dq */
 #define FA_NUM_KERNELS 9
 
 /* Turns timing on (1) or off (0). Returns FA_OK. */
@@ -331,13 +331,17 @@ int fa_paged_attention(const void* q, const void* k_cache, const void* v_cache,
  *   dk_cache, dv_cache : outputs, bf16 like the caches: every element is written; a slot
  *                that no (sequence, query) reads gets 0.
  * Each page may hold keys of one sequence only: a page named twice among the used table
- * entries (its gradient would be a sum) gets no gradient written and makes fa_device_status
- * return FA_ERR_BAD_INPUT, as do lengths and table entries out of range (read as in the
- * forward). The call gathers every sequence's keys and values into contiguous tensors and
- * runs the training backward on them (scratch: 4 * batch * n_kv_heads * max_pages *
- * page_size * head_dim * 2 bytes plus the backward's own, taken with cudaMallocAsync on
- * `stream`). p->num_splits is ignored. Returns FA_OK, FA_ERR_INVALID (parameters, pointers,
- * batch * q_len above 65535), FA_ERR_UNSUPPORTED or FA_ERR_CUDA. */
+ * entries (its gradient would be a sum) gets a zero gradient and makes fa_device_status return
+ * FA_ERR_BAD_INPUT, as do lengths and table entries out of range (read as in the forward).
+ * The call turns the batch into a variable-length batch of each sequence's used keys, packed
+ * without padding, runs the training backward on it and writes the gradients back; for decode
+ * (q_len = 1) or without the causal rule it takes the n_heads / n_kv_heads query heads of a kv
+ * head as one sequence's rows. Scratch, taken with cudaMallocAsync on `stream`: 4 * batch *
+ * n_kv_heads * max_pages * page_size * head_dim * 2 bytes for the keys, 4 * batch * n_heads *
+ * q_len * (2 * head_dim + 1) bytes for the query side, plus the backward's own.
+ * p->num_splits is ignored. Returns FA_OK, FA_ERR_INVALID (parameters, pointers, a packed
+ * problem past the size limits: batch * max_pages * page_size * n_kv_heads or
+ * batch * n_heads * q_len at 2^30 or more), FA_ERR_UNSUPPORTED or FA_ERR_CUDA. */
 int fa_paged_attention_bwd(const void* q, const void* k_cache, const void* v_cache,
                            const int32_t* block_table, const int32_t* lengths, const void* o,
                            const float* lse, const void* dO, void* dq, void* dk_cache,

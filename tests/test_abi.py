@@ -247,9 +247,9 @@ def test_paged_bwd_bad_pointers_rejected(lib):
     assert _paged_bwd(lib, PAGED_GOOD, lse=FAKE + 4) == fa.FA_ERR_INVALID
     assert _paged_bwd(lib, PAGED_GOOD, dk=FAKE + 2) == fa.FA_ERR_INVALID
     assert _paged_bwd(lib, PAGED_GOOD, q=None) == fa.FA_ERR_INVALID
-    # the mask of the flat problem has batch * q_len rows of grid y
-    assert _paged_bwd(lib, dict(PAGED_GOOD, batch=300, n_heads=2, n_kv_heads=2, q_len=256)) == \
-        fa.FA_ERR_INVALID
+    # the packed keys, batch * capacity rows per kv head, must stay within the tensor maps
+    assert _paged_bwd(lib, dict(PAGED_GOOD, batch=600, n_heads=8, n_kv_heads=8,
+                                max_pages=65536, num_pages=1000)) == fa.FA_ERR_INVALID
 
 
 def test_paged_params_struct_layout():

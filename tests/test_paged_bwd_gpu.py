@@ -1,7 +1,8 @@
 """Gradients through the paged cache on the GPU (fa_paged_attention_bwd) against the CPU oracle
 (oracle.paged_bwd), for the shapes of page "nuvec-core tests/fast.rs",
 `paged_attention_equals_contiguous_attention` ("paged grads"): decode and causal multi-query
-steps, GQA, head dims 64 / 128 / 256, page sizes 8 to 64, short and long (two-pass) caches.
+steps, GQA, head dims 64 / 128 / 256, page sizes 8 to 64, short and long (two-pass) caches,
+a non-causal multi-query step and 8 query heads per kv head.
 
 The caches hold the keys in shuffled pages with three pages nobody uses. Every slot that holds
 no key is NaN, so a read outside the keys would show. dQ and both cache gradients are compared
@@ -27,6 +28,8 @@ CASES = [
     (1, 8, 2, 4, 128, 64, (2100,)),
     (1, 4, 2, 1, 256, 16, (1100,)),
     (3, 4, 2, 3, 128, 16, (0, 2, 40)),  # an empty sequence and one shorter than q_len
+    (2, 4, 2, 3, 128, 16, (30, 77), False),  # no causal rule: the query heads packed as rows
+    (2, 16, 2, 1, 64, 8, (104, 64)),  # 8 query heads per kv head; a sequence at capacity
 ]
 
 
@@ -45,7 +48,8 @@ def _gpu():
 
 
 def _problem(n, case, shared=False):
-    B, H, Hk, lq, d, bs, lens = case
+    B, H, Hk, lq, d, bs, lens = case[:7]
+    causal = case[7] if len(case) > 7 else lq > 1
     per = max(1, max(-(-L // bs) for L in lens))
     P = B * per + 3
     rng = np.random.default_rng(2100 + n)
@@ -65,7 +69,7 @@ def _problem(n, case, shared=False):
     for c in (kc, vc):
         c.transpose(0, 2, 1, 3)[~used] = nan  # [P, bs, Hk, d] view: every head of the slot
     return dict(B=B, H=H, Hk=Hk, lq=lq, d=d, bs=bs, P=P, lens=np.asarray(lens, np.int32),
-                table=table, q=q, kc=kc, vc=vc, do=do, used=used, causal=lq > 1,
+                table=table, q=q, kc=kc, vc=vc, do=do, used=used, causal=causal,
                 scale=d ** -0.5)
 
 
@@ -87,7 +91,7 @@ def _run(x):
     return dq, dk, dv
 
 
-@pytest.mark.parametrize("n", range(len(CASES)), ids=[str(c[:6] + (c[6][:2],)) for c in CASES])
+@pytest.mark.parametrize("n", range(len(CASES)), ids=[str(c[:6] + (c[6][:2],) + c[7:]) for c in CASES])
 def test_paged_gradients_match_oracle(n):
     import flash_attention_gb300 as fa
 

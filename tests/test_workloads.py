@@ -124,13 +124,12 @@ def test_paged_grad_bytes_and_oracle_sample():
     step, per = bench.paged_grad_bytes(w, x)
     el = 64 * 2
     used_keys = sum(int(n) for n in x.lengths)
-    used_slots = sum(-(-int(n) // 8) * 8 for n in x.lengths)
-    flat = 3 * 2 * x.block_table.shape[1] * 8 * el
-    assert per["paged_gather_kernel"] == 2 * used_keys * 2 * el + 2 * flat
-    assert per["paged_scatter_kernel"] == 2 * flat + 2 * used_slots * 2 * el
     qb = 3 * 4 * 1 * el
-    assert step == (bench.paged_bytes(w, x) + 4 * qb + 2 * used_keys * 2 * el
-                    + 2 * x.k_cache.size * 2)
+    cache = x.k_cache.size * 2
+    assert per["paged_gather_kernel"] == 4 * used_keys * 2 * el + 6 * qb
+    assert per["bwd_main_kernel"] == 4 * used_keys * 2 * el + 2 * qb
+    assert per["paged_scatter_kernel"] == 2 * used_keys * 2 * el + 2 * cache + 2 * qb
+    assert step == bench.paged_bytes(w, x) + 4 * qb + 2 * used_keys * 2 * el + 2 * cache
 
     do = fa_inputs.normal_bf16(5, tuple(x.q.shape), 0.1)
     b_, s_, n_ = bench.paged_grad_oracle_sample(w, x, do, step, budget_s=1e-9)
