@@ -40,9 +40,10 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest p before O is 
 template <int HD>
 struct FwdTraits;
 // NQ query tiles per CTA, BN keys per kv tile, NS score buffers per query tile, STAGES-deep
-// K/V ring. POLY: one pair of exponentials in every POLY goes to the FMA-pipe polynomial
-// (0 = all on MUFU); the MUFU unit (16 exp2 per clock per SM) would otherwise be as slow as
-// the tensor core at head_dim 128 and the bottleneck at 64. SPLIT: S = Q K^T and O += P V are
+// K/V ring. POLY: pair e of each 16-pair group of exponentials goes to the FMA-pipe
+// polynomial when e % POLY == 0 (0 = all on MUFU, 16 or more = one pair in 16). A small share
+// relieves the MUFU queue (16 exp2 per clock per SM); a larger one costs the softmax warps
+// issue slots (measured best: 16 at head_dim 64 and 128). SPLIT: S = Q K^T and O += P V are
 // issued by two warps (a busy scheduler starves a lone issuing thread less often when the
 // two streams do not wait behind each other's barriers). S into a score buffer then waits for
 // the completion of the P V that read it, not just for its issue: with one score buffer per
@@ -50,12 +51,12 @@ struct FwdTraits;
 // the 4k causal GQA shape), with two it is hidden (head_dim 256: 125 -> 121 us).
 template <>
 struct FwdTraits<64> {
-  static constexpr int NQ = 2, BN = 128, NS = 1, STAGES = 3, POLY = 4;
+  static constexpr int NQ = 2, BN = 128, NS = 1, STAGES = 3, POLY = 16;
   static constexpr bool SPLIT = false;
 };
 template <>
 struct FwdTraits<128> {
-  static constexpr int NQ = 2, BN = 128, NS = 1, STAGES = 2, POLY = 8;
+  static constexpr int NQ = 2, BN = 128, NS = 1, STAGES = 2, POLY = 16;
   static constexpr bool SPLIT = false;
 };
 template <>
