@@ -202,14 +202,14 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
     }
     const float4* srow = reinterpret_cast<const float4*>(dqacc + ((size_t)bh * ql_pad + i) * HD);
     const int c4 = c / 4, rot = SWZ ? (i % kDqChunks) : 0;  // (query tiles start at multiples of 16)
-    const float4 v0 = srow[c4 ^ rot], v1 = srow[(c4 + 1) ^ rot];
+    const float4 v0 = __ldcs(srow + (c4 ^ rot)), v1 = __ldcs(srow + ((c4 + 1) ^ rot));
     uint4 out;
     out.x = pack_bf16(v0.x * scale, v0.y * scale);
     out.y = pack_bf16(v0.z * scale, v0.w * scale);
     out.z = pack_bf16(v1.x * scale, v1.y * scale);
     out.w = pack_bf16(v1.z * scale, v1.w * scale);
-    *reinterpret_cast<uint4*>(dq + bhsd_offset(ob, bh % H, or0 + i, H, orows, HD, q_bshd != 0) +
-                              c) = out;
+    __stcs(reinterpret_cast<uint4*>(dq + bhsd_offset(ob, bh % H, or0 + i, H, orows, HD,
+                                                      q_bshd != 0) + c), out);
   }
 }
 
@@ -219,7 +219,8 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
 // x == 0 also finish dsinks. A block reads its slice (64 head-dim rows of BM f32) with all of
 // its 16-byte loads in flight and transposes it through shared memory into [q][d] (rows padded
 // to 65 floats); then four consecutive threads write one query row's 128 contiguous bytes of
-// bf16.
+// bf16. Both sides are touched once, so loads and stores are marked evict-first (35.1 against
+// 37.6 us on the 4k GQA shape).
 template <int HD, int BM>
 __global__ void __launch_bounds__(256) bwd_dq_tiles_kernel(const float* __restrict__ dqacc,
                                                            __nv_bfloat16* __restrict__ dq,
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(256) bwd_dq_tiles_kernel(const float* __restri
 #pragma unroll
       for (int k = 0; k < NV; ++k) {
         const int f = threadIdx.x + 256 * k;
-        v[k] = src[(f / DR) * 128 + f % DR];
+        v[k] = __ldcs(src + (f / DR) * 128 + f % DR);
       }
 #pragma unroll
       for (int k = 0; k < NV; ++k) {
@@ -271,7 +272,7 @@ __global__ void __launch_bounds__(256) bwd_dq_tiles_kernel(const float* __restri
     } else {
       const float4* src = tile4 + d0 * kDqChunks;
 #pragma unroll
-      for (int k = 0; k < NV; ++k) v[k] = src[threadIdx.x + 256 * k];
+      for (int k = 0; k < NV; ++k) v[k] = __ldcs(src + threadIdx.x + 256 * k);
 #pragma unroll
       for (int k = 0; k < NV; ++k) {
         const int f = threadIdx.x + 256 * k;
@@ -292,8 +293,8 @@ __global__ void __launch_bounds__(256) bwd_dq_tiles_kernel(const float* __restri
         w[e] = pack_bf16(tile[q][c + 2 * e] * scale, tile[q][c + 2 * e + 1] * scale);
       uint4* dst = reinterpret_cast<uint4*>(
           dq + bhsd_offset(ob, bh % H, or0 + q0 + q, H, orows, HD, q_bshd != 0) + d0 + c);
-      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      __stcs(dst, make_uint4(w[0], w[1], w[2], w[3]));
+      __stcs(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
     }
     __syncthreads();  // the tile is rewritten for the next head
   }
