@@ -213,10 +213,9 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
   }
 }
 
-// dQ = bf16(scale * accumulator) from the transposed accumulator tiles of the bulk path
-// (head_dim 128: chunk-rotated rows; head_dim 256: chunk-major halves). Grid: x = (query tile
-// of BM rows, 64-row slice of the head dimension), y = (batch, head) (strided); blocks with
-// x == 0 also finish dsinks. A block reads its slice (64 head-dim rows of BM f32) with all of
+// dQ = bf16(scale * accumulator) from the transposed, chunk-major accumulator tiles of the
+// bulk path. Grid: x = (query tile of BM rows, 64-row slice of the head dimension), y =
+// (batch, head) (strided); blocks with x == 0 also finish dsinks. A block reads its slice (64 head-dim rows of BM f32) with all of
 // its 16-byte loads in flight and transposes it through shared memory into [q][d] (rows padded
 // to 65 floats); then four consecutive threads write one query row's 128 contiguous bytes of
 // bf16. Both sides are touched once, so loads and stores are marked evict-first (35.1 against
@@ -252,8 +251,8 @@ __global__ void __launch_bounds__(256) bwd_dq_tiles_kernel(const float* __restri
     if (q0 >= qlen) continue;  // (block-uniform)
     const float4* tile4 = reinterpret_cast<const float4*>(dqacc + ((size_t)bh * ql_pad + q0) * HD);
     float4 v[NV];
-    if constexpr (HD == 256) {
-      // chunk-major halves: chunk c of row d at (d / 128) * 128 * kDqChunks + c * 128 + d % 128
+    {
+      // chunk-major (halves): chunk c of row d at (d / 128) * 128 * kDqChunks + c * 128 + d % 128
       const float4* src = tile4 + (d0 / 128) * 128 * kDqChunks + d0 % 128;
 #pragma unroll
       for (int k = 0; k < NV; ++k) {
@@ -264,20 +263,6 @@ __global__ void __launch_bounds__(256) bwd_dq_tiles_kernel(const float* __restri
       for (int k = 0; k < NV; ++k) {
         const int f = threadIdx.x + 256 * k;
         const int d = f % DR, q = 4 * (f / DR);
-        tile[q][d] = v[k].x;
-        tile[q + 1][d] = v[k].y;
-        tile[q + 2][d] = v[k].z;
-        tile[q + 3][d] = v[k].w;
-      }
-    } else {
-      const float4* src = tile4 + d0 * kDqChunks;
-#pragma unroll
-      for (int k = 0; k < NV; ++k) v[k] = __ldcs(src + threadIdx.x + 256 * k);
-#pragma unroll
-      for (int k = 0; k < NV; ++k) {
-        const int f = threadIdx.x + 256 * k;
-        const int d = f / kDqChunks;  // row within the half (d0 is a multiple of kDqChunks)
-        const int q = 4 * ((f % kDqChunks) ^ (d % kDqChunks));
         tile[q][d] = v[k].x;
         tile[q + 1][d] = v[k].y;
         tile[q + 2][d] = v[k].z;
@@ -361,7 +346,7 @@ static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t
     }
     return cudaGetLastError();
   }
-  if constexpr (BwdTraits<HD>::DQ_BULK && BwdTraits<HD>::DQT) {  // transposed accumulator tiles
+  if constexpr (BwdTraits<HD>::DQT) {  // transposed accumulator tiles
     constexpr int BM = BwdTraits<HD>::BM;
     dim3 grid((unsigned)((a.ql + BM - 1) / BM * (HD / 64)), BH < 65535 ? BH : 65535);
     profile_mark(kKernBwdDq, 0, s);

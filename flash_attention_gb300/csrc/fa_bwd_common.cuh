@@ -55,15 +55,14 @@ struct BwdTraits<256> {
 
 constexpr int kBN = 128;  // kv rows per CTA (the M of the kv-major MMAs)
 
-// Bulk dQ path: with dQ^T formed (head_dim 128) the accumulator tile of one (batch, head,
-// query tile) is stored transposed, as head-dim rows of BM f32, with the 16-byte chunk c (query
-// rows 4c .. 4c+3) of row d at chunk position c ^ (d % kDqChunks); with dQ formed (head_dim 64)
-// it keeps query rows of HD f32, the chunk c (head-dim 4c .. 4c+3) of row q at c ^ (q %
-// kDqChunks). Either way 8 consecutive staging lanes store to 8 distinct bank groups.
-// head_dim 256 (the CTA-pair kernel, each CTA adding one 128-row half of dQ^T) stores each half
-// chunk-major instead: the chunk c of row d at 16-byte position (d / 128) * 128 * kDqChunks +
-// c * 128 + d % 128, so that 32 consecutive lanes (rows) write 512 contiguous bytes, whether
-// they stage the half for a bulk reduction or add it with vector reductions.
+// Bulk dQ path: with dQ^T formed (head_dim 128 and 256) the accumulator tile of one (batch,
+// head, query tile) is stored transposed and chunk-major: the 16-byte chunk c (query rows
+// 4c .. 4c+3) of head-dim row d at 16-byte position (d / 128) * 128 * kDqChunks + c * 128 +
+// d % 128, so that 32 consecutive lanes (rows) write 512 contiguous bytes, whether they stage
+// the tile for a bulk reduction or add it with vector reductions (at head_dim 256 each CTA of
+// the pair adds one 128-row half). With dQ formed (head_dim 64) the tile keeps query rows of
+// HD f32, the chunk c (head-dim 4c .. 4c+3) of row q at c ^ (q % kDqChunks), so that 8
+// consecutive staging lanes store to 8 distinct bank groups.
 constexpr int kDqChunks = 16;  // 16-byte chunks per staged row (64 f32)
 
 struct BwdKParams {

@@ -586,12 +586,12 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
         return;
       }
       if constexpr (T::DQ_BULK && T::DQT) {
-        // lane = head-dim index d, column = query row: stage the tile transposed, as HD rows of
-        // BM f32 (the accumulator keeps this tile layout; the dQ convert kernel turns it back),
-        // with the 16-byte chunks of row d XOR-rotated by (d & 15) so that the 16-byte stores of
-        // any 8 consecutive lanes hit 8 distinct bank groups. The bulk warp adds the tile with
-        // one reduction; the buffer is handed over with mbarriers (stg_full once written,
-        // stg_free once read).
+        // lane = head-dim index d, column = query row: stage the tile transposed and
+        // chunk-major (chunk c = query rows 4c .. 4c+3 of row d at float4 position c * HD + d;
+        // the accumulator keeps this tile layout and the dQ convert kernel turns it back), so
+        // that the 16-byte stores of a warp cover 512 contiguous bytes. The bulk warp adds the
+        // tile with one reduction; the buffer is handed over with mbarriers (stg_full once
+        // written, stg_free once read).
         float* stg = reinterpret_cast<float*>(smem + LY::OFF_STG);
         uint32_t rq[BM / 32][32];
 #pragma unroll
@@ -603,12 +603,13 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
           ok = __all_sync(0xffffffffu, mbar_wait(&stg_free, (it - 1) & 1, &wctl));
           if (!ok) return;
         }
-        float4* row = reinterpret_cast<float4*>(stg + j * BM);
+        static_assert(BM / 4 == kDqChunks, "chunk-major dQ tile");
+        float4* st4 = reinterpret_cast<float4*>(stg) + j;
 #pragma unroll
         for (int c = 0; c < BM / 4; ++c) {  // chunk c: query rows 4c .. 4c+3
           const uint32_t* r = &rq[c / 8][(c % 8) * 4];
-          row[c ^ (j & (kDqChunks - 1))] = make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]),
-                                                       __uint_as_float(r[2]), __uint_as_float(r[3]));
+          st4[c * HD] = make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]),
+                                    __uint_as_float(r[2]), __uint_as_float(r[3]));
         }
         fence_proxy_async();  // staging writes -> visible to the bulk copy
         mbar_arrive(&stg_full);
@@ -636,8 +637,12 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
         fence_proxy_async();  // staging writes -> visible to the bulk copy
         mbar_arrive(&stg_full);
       } else if constexpr (T::DQT) {
-        // lane = head-dim index within the slice, column = query row
-        float* dst = p.dqacc + ((size_t)bh * p.ql_pad + q0) * HD + dh * DH + j;
+        // lane = head-dim index d, column = query row: add the tile straight from registers
+        // with 16-byte vector reductions in the chunk-major tile layout. No head dim selects
+        // this form at present: at head_dim 128 it measured slower than the staged bulk
+        // reduction (main pass 721 against 641 us on the 4k GQA shape).
+        static_assert(T::DSPLIT == 1 && BM / 4 == kDqChunks, "chunk-major dQ tile");
+        float4* dst = reinterpret_cast<float4*>(p.dqacc + ((size_t)bh * p.ql_pad + q0) * HD) + j;
         uint32_t rq[BM / 32][32];
 #pragma unroll
         for (int c32 = 0; c32 < BM / 32; ++c32) tmem_ld32(lane_base + colDQ + c32 * 32, rq[c32]);
@@ -645,10 +650,11 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
         tc_fence_before();
         mbar_arrive(&dq_free[it % 2]);
 #pragma unroll
-        for (int c32 = 0; c32 < BM / 32; ++c32)
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            atomicAdd(dst + (size_t)(c32 * 32 + e) * HD, __uint_as_float(rq[c32][e]));
+        for (int c = 0; c < BM / 4; ++c) {
+          const uint32_t* r = &rq[c / 8][(c % 8) * 4];
+          atomicAdd(dst + c * HD, make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]),
+                                              __uint_as_float(r[2]), __uint_as_float(r[3])));
+        }
       } else {
         // lane = query row, column = head-dim index (dQ formed without a staging tile; no
         // head dim selects this form at present: head_dim 64 stages its tile)
