@@ -350,19 +350,26 @@ def paged_grad_bytes(w, x):
     """Algorithmic bytes of one forward + gradient step, and of each gradient kernel.
     The step: the forward's, then the gradients' least traffic (q, O, dO in and dq out; the
     keys and values each sequence reads; both cache gradients written whole, since slots no
-    sequence reads get 0). Per kernel, what its own interface makes it move: the gather (used
-    keys and values in and out, packed; q, O, dO in and out, packed), the backward main pass on
-    the packed problem (K, V in and dK, dV out; q and dO in) and the scatter (packed dK, dV in;
-    both cache gradients out; dq in and out)."""
+    sequence reads get 0). Per kernel, what its own interface makes it move. With G * q_len
+    <= 8 query rows per kv head (the decode path): the gradient kernel (used keys and values
+    in, their dK, dV rows out; q, O, dO in) and the fill (every other cache-gradient row out,
+    dq in f32 and out). Otherwise (the packed path): the gather (used keys and values in and
+    out, packed; q, O, dO in and out, packed), the backward main pass on the packed problem
+    (K, V in and dK, dV out; q and dO in) and the scatter (packed dK, dV in; both cache
+    gradients out; dq in and out)."""
     el = w.head_dim * 2
     lens = x.lengths.astype(np.int64)
     used = int(lens.sum()) * w.n_kv_heads * el
     cache = x.k_cache.shape[0] * w.n_kv_heads * w.page_size * el
     qbytes = w.batch * w.n_heads * w.q_len * el
     step = paged_bytes(w, x) + 4 * qbytes + 2 * used + 2 * cache
-    per = {"paged_gather_kernel": 4 * used + 6 * qbytes,
-           "bwd_main_kernel": 4 * used + 2 * qbytes,
-           "paged_scatter_kernel": 2 * used + 2 * cache + 2 * qbytes}
+    if (w.n_heads // w.n_kv_heads) * w.q_len <= 8:
+        per = {"paged_decode_bwd_kernel": 4 * used + 3 * qbytes,
+               "paged_scatter_kernel": 2 * (cache - used) + 3 * qbytes}
+    else:
+        per = {"paged_gather_kernel": 4 * used + 6 * qbytes,
+               "bwd_main_kernel": 4 * used + 2 * qbytes,
+               "paged_scatter_kernel": 2 * used + 2 * cache + 2 * qbytes}
     return step, per
 
 
@@ -581,7 +588,9 @@ def run_paged(args, w, grad=False):
                 "peak_source": f"hbm_gbs, {peaks['source']}",
                 "per_kernel_ms": {k: (t / max(c, 1)) for k, (t, c) in prof.items() if c}}
     launches = sum(c for _, c in prof.values())
-    if grad:  # timed regions of several launches: gather (index, gather, tail, q side), scatter
+    if grad and prof.get("paged_decode_bwd_kernel", (0, 0))[1]:
+        launches += prof["paged_scatter_kernel"][1]  # (fill and dq convert in one region)
+    elif grad:  # timed regions of several launches: gather (index, gather, tail, q side), scatter
         launches += 3 * prof["paged_gather_kernel"][1] + prof["paged_scatter_kernel"][1]
 
     e2e = None

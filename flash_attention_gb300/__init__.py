@@ -323,7 +323,7 @@ def fa_device_status(clear: bool = True) -> int:
     return load_library().fa_device_status(int(bool(clear)))
 
 
-FA_NUM_KERNELS = 9
+FA_NUM_KERNELS = 10
 
 
 def fa_profile_enable(on: bool) -> None:

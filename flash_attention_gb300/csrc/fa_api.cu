@@ -289,6 +289,7 @@ const char* fa_kernel_name(int id) {
     case FA_KERNEL_PAGED_COMBINE: return "paged_combine_kernel";
     case FA_KERNEL_PAGED_GATHER: return "paged_gather_kernel";
     case FA_KERNEL_PAGED_SCATTER: return "paged_scatter_kernel";
+    case FA_KERNEL_PAGED_DECODE_BWD: return "paged_decode_bwd_kernel";
     case FA_KERNEL_BWD_MAIN: return "bwd_main_kernel";
     case FA_KERNEL_BWD_DQ: return "bwd_dq_kernel";
     default: return "unknown";
@@ -608,6 +609,55 @@ int fa_paged_attention_bwd(const void* q, const void* k_cache, const void* v_cac
   const int B = p->batch, H = p->n_heads, Hk = p->n_kv_heads, lq = p->q_len, d = p->head_dim;
   const int G = H / Hk;
   const int64_t cap = (int64_t)p->max_pages * p->page_size;
+  const int64_t chunks = d / 8;  // 16-byte chunks per row: grid x of the row kernels
+  if ((int64_t)p->num_pages * p->page_size * chunks / 256 >= INT32_MAX ||
+      (int64_t)B * H * lq * chunks / 256 >= INT32_MAX)
+    return FA_ERR_INVALID;
+  fa::PagedGradArgs g;
+  g.k_cache = k_cache;
+  g.v_cache = v_cache;
+  g.table = block_table;
+  g.lens = lengths;
+  g.q = q;
+  g.o = o;
+  g.dO = dO;
+  g.lse = lse;
+  g.dq = dq;
+  g.dk_cache = dk_cache;
+  g.dv_cache = dv_cache;
+  g.B = B;
+  g.H = H;
+  g.Hk = Hk;
+  g.lq = lq;
+  g.d = d;
+  g.ps = p->page_size;
+  g.max_pages = p->max_pages;
+  g.num_pages = p->num_pages;
+  g.causal = p->causal;
+  if (fa::paged_decode_path(G, lq)) {
+    // few query rows per kv head: the CUDA-core kernels read the pages directly
+    if ((rc = check_device())) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t owner_bytes = align256((size_t)p->num_pages * 4);
+    const size_t acc_bytes = align256((size_t)B * H * lq * d * 4);
+    void* ws = nullptr;
+    cudaError_t e = cudaMallocAsync(&ws, owner_bytes + acc_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync (paged backward workspace)");
+    g.owner = static_cast<int32_t*>(ws);
+    float* dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + owner_bytes);
+    if ((e = device_status_word(dev, &g.status)) != cudaSuccess ||
+        (e = cudaMemsetAsync(g.owner, 0xFF, (size_t)p->num_pages * 4, s)) != cudaSuccess ||
+        (e = cudaMemsetAsync(dq_acc, 0, (size_t)B * H * lq * d * 4, s)) != cudaSuccess ||
+        (e = fa::launch_paged_decode_bwd(g, dq_acc, p->scale, s)) != cudaSuccess) {
+      cudaFreeAsync(ws, s);
+      return cuda_fail(e, "paged backward (decode path)");
+    }
+    if ((e = cudaFreeAsync(ws, s)) != cudaSuccess)
+      return cuda_fail(e, "cudaFreeAsync (paged backward workspace)");
+    return FA_OK;
+  }
   // the packed problem: a variable-length batch of B sequences, one per sequence's used keys;
   // with `pack` the G query heads of a kv head are its G * lq rows (no row's keys depend on
   // its position: decode, or no causal rule)
@@ -616,10 +666,6 @@ int fa_paged_attention_bwd(const void* q, const void* k_cache, const void* v_cac
   const int64_t rq = pack ? (int64_t)G * lq : lq;
   const int64_t total_q = B * rq, total_k = B * cap;
   if (rq > kMaxLen || total_q * Hq > INT32_MAX / 2 || total_k * Hk > INT32_MAX / 2)
-    return FA_ERR_INVALID;
-  const int64_t chunks = d / 8;  // 16-byte chunks per row: grid x of the gather kernels
-  if ((int64_t)p->num_pages * p->page_size * chunks / 256 >= INT32_MAX ||
-      (int64_t)B * H * lq * chunks / 256 >= INT32_MAX)
     return FA_ERR_INVALID;
   if ((rc = check_device())) return rc;
   cudaError_t e = get_encoder();
@@ -656,18 +702,6 @@ int fa_paged_attention_bwd(const void* q, const void* k_cache, const void* v_cac
     w += n;
     return r;
   };
-  fa::PagedGradArgs g;
-  g.k_cache = k_cache;
-  g.v_cache = v_cache;
-  g.table = block_table;
-  g.lens = lengths;
-  g.q = q;
-  g.o = o;
-  g.dO = dO;
-  g.lse = lse;
-  g.dq = dq;
-  g.dk_cache = dk_cache;
-  g.dv_cache = dv_cache;
   g.k_pack = take(kv_bytes);
   g.v_pack = take(kv_bytes);
   g.dk_pack = take(kv_bytes);
@@ -681,14 +715,6 @@ int fa_paged_attention_bwd(const void* q, const void* k_cache, const void* v_cac
   g.cu_k = reinterpret_cast<int32_t*>(take(cu_bytes));
   g.owner = reinterpret_cast<int32_t*>(take(owner_bytes));
   void* bwd_ws = take(bwd_bytes);
-  g.B = B;
-  g.H = H;
-  g.Hk = Hk;
-  g.lq = lq;
-  g.d = d;
-  g.ps = p->page_size;
-  g.max_pages = p->max_pages;
-  g.num_pages = p->num_pages;
   g.pack = pack ? 1 : 0;
   fo.cu_seqlens_q = g.cu_q;
   fo.cu_seqlens_k = g.cu_k;

@@ -46,7 +46,8 @@ enum KernelId {
   kKernPagedCombine = 6,
   kKernPagedGather = 7,
   kKernPagedScatter = 8,
-  kNumKernels = 9
+  kKernPagedDecodeBwd = 9,
+  kNumKernels = 10
 };
 
 // Records a timing event before (end = 0) or after (end = 1) a launch on `s` when timing is
@@ -260,11 +261,18 @@ struct PagedGradArgs {
   int32_t* owner;        // [num_pages]: b * max_pages + slot of the one table entry that uses
                          // the page; -1 (set before the gather) none, -2 two or more
   int* status;
-  int B, H, Hk, lq, d, ps, max_pages, num_pages, pack;
+  int B, H, Hk, lq, d, ps, max_pages, num_pages, pack, causal;
 };
 // The offsets, the packed K, V (and the owner of every used page), the packed q-side tensors.
 cudaError_t launch_paged_gather(const PagedGradArgs& a, cudaStream_t stream);
 // Both cache gradients whole (zero where no sequence reads) and dq.
 cudaError_t launch_paged_scatter(const PagedGradArgs& a, cudaStream_t stream);
+// The decode path (G * q_len small: no packing, no training backward): page owners, the
+// CUDA-core gradient kernel writing dK, dV into the cache gradients and f32 dQ sums into
+// dq_acc (zeroed, [B, H, lq, d]), the zero fill of unread slots and dq. Uses q, o, dO, lse,
+// dq, the caches, their gradients, table, lens, owner (set to -1) and status of `a`.
+bool paged_decode_path(int G, int lq);
+cudaError_t launch_paged_decode_bwd(const PagedGradArgs& a, float* dq_acc, float scale,
+                                    cudaStream_t stream);
 
 }  // namespace fa

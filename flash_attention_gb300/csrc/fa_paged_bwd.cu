@@ -17,7 +17,8 @@
 //   4. scatter: every cache slot gets its gradient from the packed dK, dV through its page's
 //      owner, or 0 when no sequence reads it; dq goes back to [B, H, q_len, d].
 // A page used by two sequences (or twice by one) would need the contributions summed; it gets
-// a zero gradient and FA_ERR_BAD_INPUT is reported.
+// a zero gradient and FA_ERR_BAD_INPUT is reported. With few query rows per kv head the
+// decode path below replaces steps 1-4.
 #include "fa_common.cuh"
 #include "fa_launch.h"
 
@@ -198,6 +199,262 @@ __global__ void __launch_bounds__(256) paged_scatter_kernel(PagedGradArgs a) {
   reinterpret_cast<uint4*>(a.dv_cache)[dst] = gv;
 }
 
+// ---------------------------------------------------------------- decode path
+// With few query rows per kv head (G * q_len <= kDecRows: decode, short cached prefills) the
+// gradients are HBM-bound: every used key and value is read once and its two gradient rows
+// written once, against 5 * 2 * G * q_len FLOPs per key and head dim element. A tensor-core
+// tile would hold at most kDecRows live rows of its 64 or 128, so these kernels run on the
+// CUDA cores instead, read the keys through the block table, and write dK, dV straight into
+// the cache gradients:
+//   paged_owner_kernel     every used page records its (sequence, table slot);
+//   paged_decode_bwd_kernel per (sequence, kv head, 256-key chunk): P, dP, dS for the rows of
+//                          the kv head's G query heads, dK and dV of each key, dQ partial sums;
+//   paged_fill_kernel      zeros in every cache-gradient slot no sequence reads (and in pages
+//                          used twice), then dq = bf16 of the f32 partial sums.
+constexpr int kDecRows = 8;    // query rows per kv head of the decode path (G * q_len)
+constexpr int kDecKeys = 256;  // keys per block of the decode kernel
+
+namespace {
+__device__ __forceinline__ int clamped_len(const PagedGradArgs& a, int b) {
+  const int len = a.lens[b];
+  const long long cap = paged_cap(a);
+  return len < 0 ? 0 : (len > cap ? (int)cap : len);
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+}  // namespace
+
+// Grid (ceil(max_pages / 256), B): table slot `slot` of sequence b, if it holds keys, claims
+// its page (owner = b * max_pages + slot; -2 when the page is claimed twice).
+__global__ void __launch_bounds__(256) paged_owner_kernel(PagedGradArgs a) {
+  const int b = blockIdx.y;
+  const int slot = blockIdx.x * 256 + threadIdx.x;
+  const int len = a.lens[b];
+  if (slot == 0 && (len < 0 || len > paged_cap(a))) report_bad(a.status);
+  if (slot >= a.max_pages || (long long)slot * a.ps >= clamped_len(a, b)) return;
+  const int page = a.table[(size_t)b * a.max_pages + slot];
+  if (page < 0 || page >= a.num_pages) {
+    report_bad(a.status);  // read as zero keys, no gradient written
+    return;
+  }
+  if (atomicCAS(a.owner + page, -1, b * a.max_pages + slot) != -1) {
+    atomicExch(a.owner + page, -2);
+    report_bad(a.status);
+  }
+}
+
+// Grid (ceil(capacity / kDecKeys), B * Hk), kDecThreads threads. Row r of a kv head is query
+// head kh * G + r / q_len, query r % q_len; it sees keys j < length, and under the causal rule
+// j <= length - q_len + r % q_len. A key row is LPK = D / 8 lanes (16 bytes, 8 elements
+// each); a warp step takes KPW = 32 / LPK keys. A lane always holds the same 8 columns, so it
+// keeps those columns of every row's q and dO in registers for the whole block. Dot products
+// over the key row are summed across its lanes with shuffles. RMAX: the row bound the
+// registers are sized for (4 or kDecRows). The kernel is bound by latency and issue, not by
+// HBM: measured on the 16-sequence decode workload (d=128, 4 rows), 128-thread blocks at 3 per
+// SM with q/dO in f32 registers took 369 us; 256 threads at 1 per SM 573 us; q/dO read from
+// shared memory at each key (256 threads, 2 per SM) 677 us; bf16 q/dO pairs at 4 blocks of 128
+// per SM (spilling) 427 us.
+constexpr int kDecThreads = 128;
+template <int D, int RMAX>
+__global__ void __launch_bounds__(kDecThreads, RMAX <= 4 ? 3 : 1) paged_decode_bwd_kernel(
+    PagedGradArgs a, float* dq_acc, float scale, float scale_log2) {
+  constexpr int LPK = D / 8, KPW = 32 / LPK, NW = kDecThreads / 32;
+  __shared__ __align__(16) float sq[RMAX][D];   // q rows
+  __shared__ __align__(16) float sdo[RMAX][D];  // dO rows
+  __shared__ __align__(16) float sdq[RMAX][D];  // the block's dQ sums (unscaled)
+  __shared__ float sl2[RMAX], sdd[RMAX];        // L * log2(e) (-inf: no key), D = <dO, O>
+  __shared__ int shi[RMAX];                     // keys j < shi[r] are visible to row r
+  const int bkh = blockIdx.y, b = bkh / a.Hk, kh = bkh % a.Hk;
+  const int G = a.H / a.Hk, R = G * a.lq;
+  const int len = clamped_len(a, b);
+  const int c0 = blockIdx.x * kDecKeys;
+  if (c0 >= len) return;  // (block-uniform)
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
+  const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(a.o);
+  const __nv_bfloat16* dO = static_cast<const __nv_bfloat16*>(a.dO);
+  const size_t row0 = ((size_t)b * a.H + (size_t)kh * G) * a.lq;  // [B, H, lq] row of r = 0
+  for (int x = tid; x < RMAX * D; x += kDecThreads) {
+    const int r = x / D, e = x % D;
+    float qv = 0.0f, dv = 0.0f;
+    if (r < R) {
+      qv = __bfloat162float(q[(row0 + r) * D + e]);
+      dv = __bfloat162float(dO[(row0 + r) * D + e]);
+    }
+    sq[r][e] = qv;
+    sdo[r][e] = dv;
+    sdq[r][e] = 0.0f;
+  }
+  for (int r = warp; r < RMAX; r += NW) {  // one warp per row: D = <dO, O>, L, visibility
+    float acc = 0.0f;
+    if (r < R)
+      for (int e = lane; e < D; e += 32)
+        acc += __bfloat162float(o[(row0 + r) * D + e]) * __bfloat162float(dO[(row0 + r) * D + e]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) {
+      const float L = r < R ? a.lse[row0 + r] : -INFINITY;
+      sdd[r] = acc;
+      sl2[r] = L * 1.4426950408889634f;  // -inf stays -inf
+      const int hi = a.causal ? len - a.lq + r % a.lq + 1 : len;
+      shi[r] = r < R ? (hi < 0 ? 0 : hi) : 0;
+    }
+  }
+  __syncthreads();
+
+  const int sub = lane % LPK;  // 16-byte chunk of the key row: elements 8 * sub .. + 7
+  const int kk = lane / LPK;   // key within the warp step
+  const int e0 = sub * 8;
+  const int c1 = min(c0 + kDecKeys, len);
+  const long long total_kv = (long long)a.num_pages * a.Hk * a.ps;  // rows of each cache
+  const uint4* K4 = static_cast<const uint4*>(a.k_cache);
+  const uint4* V4 = static_cast<const uint4*>(a.v_cache);
+  float dq[RMAX][8];
+  float qr[RMAX][8], gr[RMAX][8];  // this lane's columns of q and dO
+#pragma unroll
+  for (int r = 0; r < RMAX; ++r)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      dq[r][e] = 0.0f;
+      qr[r][e] = sq[r][e0 + e];
+      gr[r][e] = sdo[r][e0 + e];
+    }
+
+  // key j's cache row (page * Hk + kh) * ps + j % ps, or -1 (past the end / outside the cache)
+  auto key_row = [&](int j, int& slot, int& page) -> long long {
+    slot = j / a.ps;
+    page = j < c1 ? a.table[(size_t)b * a.max_pages + slot] : -1;
+    if (page < 0 || page >= a.num_pages) return -1;
+    return ((long long)page * a.Hk + kh) * a.ps + j % a.ps;
+  };
+  const int step = NW * KPW;
+  int j = c0 + warp * KPW + kk;
+  int slot, page;
+  long long kr = key_row(j, slot, page);
+  uint4 kn = make_uint4(0, 0, 0, 0), vn = kn;
+  if (kr >= 0 && kr < total_kv) {
+    kn = K4[kr * LPK + sub];
+    vn = V4[kr * LPK + sub];
+  }
+#pragma unroll 1
+  for (int base = c0 + warp * KPW; base < c1; base += step) {  // (warp-uniform)
+    const uint4 kc = kn, vc = vn;
+    const int jc = j, slot_c = slot, page_c = page;
+    const long long kr_c = kr;
+    // the next step's loads go out before this step's arithmetic
+    j += step;
+    kr = key_row(j, slot, page);
+    kn = make_uint4(0, 0, 0, 0);
+    vn = kn;
+    if (kr >= 0 && kr < total_kv) {
+      kn = K4[kr * LPK + sub];
+      vn = V4[kr * LPK + sub];
+    }
+    const bool live = jc < c1;
+    const float kf[8] = {bf_lo(kc.x), bf_hi(kc.x), bf_lo(kc.y), bf_hi(kc.y),
+                         bf_lo(kc.z), bf_hi(kc.z), bf_lo(kc.w), bf_hi(kc.w)};
+    const float vf[8] = {bf_lo(vc.x), bf_hi(vc.x), bf_lo(vc.y), bf_hi(vc.y),
+                         bf_lo(vc.z), bf_hi(vc.z), bf_lo(vc.w), bf_hi(vc.w)};
+    float sv[RMAX], dpv[RMAX];
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) {
+      float s0 = 0.0f, d0 = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        s0 += qr[r][e] * kf[e];
+        d0 += gr[r][e] * vf[e];
+      }
+      sv[r] = s0;
+      dpv[r] = d0;
+    }
+#pragma unroll
+    for (int off = LPK / 2; off > 0; off >>= 1)
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r) {
+        sv[r] += __shfl_xor_sync(0xffffffffu, sv[r], off);
+        dpv[r] += __shfl_xor_sync(0xffffffffu, dpv[r], off);
+      }
+    float dk[8], dv[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) dk[e] = dv[e] = 0.0f;
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) {
+      const float l2 = sl2[r];
+      const bool vis = live && r < R && jc < shi[r] && l2 != -INFINITY;
+      const float pr = vis ? exp2f(sv[r] * scale_log2 - l2) : 0.0f;
+      const float ds = pr * (dpv[r] - sdd[r]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        dk[e] += ds * qr[r][e];
+        dv[e] += pr * gr[r][e];
+        dq[r][e] += ds * kf[e];
+      }
+    }
+    // this sequence's own page only: a page claimed twice (or none) is zero-filled later
+    if (kr_c >= 0 && kr_c < total_kv && a.owner[page_c] == b * a.max_pages + slot_c) {
+      const uint4 wk = make_uint4(pack_bf16(dk[0] * scale, dk[1] * scale),
+                                  pack_bf16(dk[2] * scale, dk[3] * scale),
+                                  pack_bf16(dk[4] * scale, dk[5] * scale),
+                                  pack_bf16(dk[6] * scale, dk[7] * scale));
+      const uint4 wv = make_uint4(pack_bf16(dv[0], dv[1]), pack_bf16(dv[2], dv[3]),
+                                  pack_bf16(dv[4], dv[5]), pack_bf16(dv[6], dv[7]));
+      reinterpret_cast<uint4*>(a.dk_cache)[kr_c * LPK + sub] = wk;
+      reinterpret_cast<uint4*>(a.dv_cache)[kr_c * LPK + sub] = wv;
+    }
+  }
+  // dQ: the warp's keys (lanes of one chunk, different kk) summed, then the block's warps
+  // in shared memory, then one global f32 sum per element
+#pragma unroll
+  for (int off = LPK; off < 32; off <<= 1)
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) dq[r][e] += __shfl_xor_sync(0xffffffffu, dq[r][e], off);
+  if (kk == 0) {
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r)
+      if (r < R)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) atomicAdd(&sdq[r][e0 + e], dq[r][e]);
+  }
+  __syncthreads();
+  for (int x = tid; x < R * D; x += kDecThreads) {
+    const int r = x / D, e = x % D;
+    atomicAdd(dq_acc + (row0 + r) * D + e, sdq[r][e] * scale);
+  }
+}
+
+// Grid (ceil(num_pages * page_size * d / 8 / 256), Hk): zeros in every cache-gradient chunk
+// whose slot holds no key of its page's one owner (the decode kernel wrote the others).
+__global__ void __launch_bounds__(256) paged_fill_kernel(PagedGradArgs a) {
+  const int kh = blockIdx.y;
+  const int cpr = a.d / 8;
+  const long long e = (long long)blockIdx.x * 256 + threadIdx.x;
+  if (e >= (long long)a.num_pages * a.ps * cpr) return;
+  const long long prow = e / cpr;
+  const int c = (int)(e % cpr);
+  const int page = (int)(prow / a.ps), s = (int)(prow % a.ps);
+  const int own = a.owner[page];
+  if (own >= 0 && (long long)(own % a.max_pages) * a.ps + s < clamped_len(a, own / a.max_pages))
+    return;
+  const size_t dst = (((size_t)page * a.Hk + kh) * a.ps + s) * cpr + c;
+  reinterpret_cast<uint4*>(a.dk_cache)[dst] = make_uint4(0, 0, 0, 0);
+  reinterpret_cast<uint4*>(a.dv_cache)[dst] = make_uint4(0, 0, 0, 0);
+}
+
+// Grid (ceil(B * H * lq * d / 8 / 256)): dq = bf16 of the f32 sums, 8 elements per thread.
+__global__ void __launch_bounds__(256) paged_dq_convert_kernel(PagedGradArgs a,
+                                                               const float* dq_acc) {
+  const long long e = (long long)blockIdx.x * 256 + threadIdx.x;
+  if (e >= (long long)a.B * a.H * a.lq * a.d / 8) return;
+  const float4 x0 = reinterpret_cast<const float4*>(dq_acc)[2 * e];
+  const float4 x1 = reinterpret_cast<const float4*>(dq_acc)[2 * e + 1];
+  reinterpret_cast<uint4*>(a.dq)[e] =
+      make_uint4(pack_bf16(x0.x, x0.y), pack_bf16(x0.z, x0.w), pack_bf16(x1.x, x1.y),
+                 pack_bf16(x1.z, x1.w));
+}
+
 namespace {
 unsigned blocks_of(long long n) { return (unsigned)((n + 255) / 256); }
 }  // namespace
@@ -232,6 +489,50 @@ cudaError_t launch_paged_scatter(const PagedGradArgs& a, cudaStream_t s) {
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) {
     paged_qside_kernel<false><<<blocks_of((long long)a.B * a.H * a.lq * cpr), 256, 0, s>>>(a);
+    e = cudaGetLastError();
+  }
+  profile_mark(kKernPagedScatter, 1, s);
+  return e;
+}
+
+bool paged_decode_path(int G, int lq) { return (long long)G * lq <= kDecRows; }
+
+cudaError_t launch_paged_decode_bwd(const PagedGradArgs& a, float* dq_acc, float scale,
+                                    cudaStream_t s) {
+  const long long cap = (long long)a.max_pages * a.ps;
+  const int cpr = a.d / 8;
+  const int R = (a.H / a.Hk) * a.lq;
+  profile_mark(kKernPagedGather, 0, s);
+  paged_owner_kernel<<<dim3(blocks_of(a.max_pages), a.B), 256, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  profile_mark(kKernPagedGather, 1, s);
+  if (e != cudaSuccess) return e;
+  profile_mark(kKernPagedDecodeBwd, 0, s);
+  const dim3 grid((unsigned)((cap + kDecKeys - 1) / kDecKeys), a.B * a.Hk);
+  const float sl2 = scale * 1.4426950408889634f;
+#define FA_DEC(DD)                                                                   \
+  if (R <= 4)                                                                        \
+    paged_decode_bwd_kernel<DD, 4><<<grid, kDecThreads, 0, s>>>(a, dq_acc, scale, sl2); \
+  else                                                                               \
+    paged_decode_bwd_kernel<DD, kDecRows><<<grid, kDecThreads, 0, s>>>(a, dq_acc, scale, sl2);
+  if (a.d == 64) {
+    FA_DEC(64)
+  } else if (a.d == 128) {
+    FA_DEC(128)
+  } else {
+    FA_DEC(256)
+  }
+#undef FA_DEC
+  e = cudaGetLastError();
+  profile_mark(kKernPagedDecodeBwd, 1, s);
+  if (e != cudaSuccess) return e;
+  profile_mark(kKernPagedScatter, 0, s);
+  paged_fill_kernel<<<dim3(blocks_of((long long)a.num_pages * a.ps * cpr), a.Hk), 256, 0, s>>>(
+      a);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) {
+    paged_dq_convert_kernel<<<blocks_of((long long)a.B * a.H * a.lq * cpr), 256, 0, s>>>(
+        a, dq_acc);
     e = cudaGetLastError();
   }
   profile_mark(kKernPagedScatter, 1, s);

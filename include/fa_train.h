@@ -217,9 +217,10 @@ int fa_train_bwd(const void* q, const void* k, const void* v, const void* o, con
 #define FA_KERNEL_BWD_DQ_DET 4 /* deterministic mode: query-tile-major dQ */
 #define FA_KERNEL_PAGED 5      /* paged key/value cache attention */
 #define FA_KERNEL_PAGED_COMBINE 6 /* merge of the key splits of fa_paged_attention */
-#define FA_KERNEL_PAGED_GATHER 7  /* fa_paged_attention_bwd: pages -> packed K, V, q side */
-#define FA_KERNEL_PAGED_SCATTER 8 /* fa_paged_attention_bwd: gradients back into the pages, dq */
-#define FA_NUM_KERNELS 9
+#define FA_KERNEL_PAGED_GATHER 7  /* fa_paged_attention_bwd: packed K, V, q side / page owners */
+#define FA_KERNEL_PAGED_SCATTER 8 /* fa_paged_attention_bwd: cache gradients completed, dq */
+#define FA_KERNEL_PAGED_DECODE_BWD 9 /* fa_paged_attention_bwd, few rows: the gradient kernel */
+#define FA_NUM_KERNELS 10
 
 /* Turns timing on (1) or off (0). Returns FA_OK. */
 int fa_profile_enable(int on);
@@ -333,12 +334,16 @@ int fa_paged_attention(const void* q, const void* k_cache, const void* v_cache,
  * Each page may hold keys of one sequence only: a page named twice among the used table
  * entries (its gradient would be a sum) gets a zero gradient and makes fa_device_status return
  * FA_ERR_BAD_INPUT, as do lengths and table entries out of range (read as in the forward).
- * The call turns the batch into a variable-length batch of each sequence's used keys, packed
- * without padding, runs the training backward on it and writes the gradients back; for decode
- * (q_len = 1) or without the causal rule it takes the n_heads / n_kv_heads query heads of a kv
- * head as one sequence's rows. Scratch, taken with cudaMallocAsync on `stream`: 4 * batch *
- * n_kv_heads * max_pages * page_size * head_dim * 2 bytes for the keys, 4 * batch * n_heads *
- * q_len * (2 * head_dim + 1) bytes for the query side, plus the backward's own.
+ * With at most 8 query rows per kv head ((n_heads / n_kv_heads) * q_len <= 8: decode and short
+ * cached prefills) CUDA-core kernels read the keys through the block table and write dK, dV
+ * into the cache gradients directly (scratch: num_pages * 4 + batch * n_heads * q_len *
+ * head_dim * 4 bytes). Otherwise the call turns the batch into a variable-length batch of
+ * each sequence's used keys, packed without padding, runs the training backward on it and
+ * writes the gradients back; without the causal rule it takes the n_heads / n_kv_heads query
+ * heads of a kv head as one sequence's rows (scratch: 4 * batch * n_kv_heads * max_pages *
+ * page_size * head_dim * 2 bytes for the keys, 4 * batch * n_heads * q_len * (2 * head_dim +
+ * 1) bytes for the query side, plus the backward's own). Scratch is taken with
+ * cudaMallocAsync on `stream`.
  * p->num_splits is ignored. Returns FA_OK, FA_ERR_INVALID (parameters, pointers, a packed
  * problem past the size limits: batch * max_pages * page_size * n_kv_heads or
  * batch * n_heads * q_len at 2^30 or more), FA_ERR_UNSUPPORTED or FA_ERR_CUDA. */

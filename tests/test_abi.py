@@ -247,8 +247,9 @@ def test_paged_bwd_bad_pointers_rejected(lib):
     assert _paged_bwd(lib, PAGED_GOOD, lse=FAKE + 4) == fa.FA_ERR_INVALID
     assert _paged_bwd(lib, PAGED_GOOD, dk=FAKE + 2) == fa.FA_ERR_INVALID
     assert _paged_bwd(lib, PAGED_GOOD, q=None) == fa.FA_ERR_INVALID
-    # the packed keys, batch * capacity rows per kv head, must stay within the tensor maps
-    assert _paged_bwd(lib, dict(PAGED_GOOD, batch=600, n_heads=8, n_kv_heads=8,
+    # more than 8 query rows per kv head take the packed path, whose batch * capacity rows
+    # per kv head must stay within the tensor maps
+    assert _paged_bwd(lib, dict(PAGED_GOOD, batch=600, n_heads=16, n_kv_heads=8, q_len=8,
                                 max_pages=65536, num_pages=1000)) == fa.FA_ERR_INVALID
 
 

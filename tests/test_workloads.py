@@ -126,10 +126,17 @@ def test_paged_grad_bytes_and_oracle_sample():
     used_keys = sum(int(n) for n in x.lengths)
     qb = 3 * 4 * 1 * el
     cache = x.k_cache.size * 2
-    assert per["paged_gather_kernel"] == 4 * used_keys * 2 * el + 6 * qb
-    assert per["bwd_main_kernel"] == 4 * used_keys * 2 * el + 2 * qb
-    assert per["paged_scatter_kernel"] == 2 * used_keys * 2 * el + 2 * cache + 2 * qb
+    # 2 query rows per kv head: the decode path
+    assert per["paged_decode_bwd_kernel"] == 4 * used_keys * 2 * el + 3 * qb
+    assert per["paged_scatter_kernel"] == 2 * (cache - used_keys * 2 * el) + 3 * qb
     assert step == bench.paged_bytes(w, x) + 4 * qb + 2 * used_keys * 2 * el + 2 * cache
+    wide = fa_inputs.DecodeWorkload("tiny_paged_grad_wide", 3, 8, 2, 3, 64, 8, 5, 30)
+    xw = fa_inputs.make_paged_inputs(wide, index=8)
+    _, perw = bench.paged_grad_bytes(wide, xw)
+    used_w = sum(int(n) for n in xw.lengths) * 2 * el
+    qw = 3 * 8 * 3 * el
+    assert perw["bwd_main_kernel"] == 4 * used_w + 2 * qw
+    assert perw["paged_scatter_kernel"] == 2 * used_w + 2 * xw.k_cache.size * 2 + 2 * qw
 
     do = fa_inputs.normal_bf16(5, tuple(x.q.shape), 0.1)
     b_, s_, n_ = bench.paged_grad_oracle_sample(w, x, do, step, budget_s=1e-9)
