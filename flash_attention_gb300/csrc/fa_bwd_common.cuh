@@ -23,8 +23,9 @@ constexpr float kLog2eB = 1.4426950408889634f;
 template <int HD>
 struct BwdTraits;
 // DQ_BULK: the dQ tile is staged in shared memory (f32, in the accumulator's tile layout below)
-// and added to the accumulator by one bulk reduction; otherwise each thread adds its values
-// with global reductions.
+// and added to the accumulator by one bulk reduction (every head dim of the main pass does so:
+// at head_dim 128, adding the tile from registers with 16-byte vector reductions measured 721
+// against 641 us on the 4k causal GQA shape, and at 64 scattered reductions 189 against 171 us).
 // SPLIT_MMA: in the deterministic mode (no dQ MMAs here) two warps issue the MMAs, one S^T and
 // dP^T, the other dV and dK, so that neither stream waits behind the other's barrier waits and
 // the issuing thread is less often starved of issue slots by the busy compute warps that share

@@ -55,7 +55,7 @@ struct BwdLayout {
   static_assert(T::DQT ? DH == 128 : BM == 128, "every MMA has M = 128");
   static_assert(T::LOOKAHEAD ? T::ST >= (T::NSB == 2 ? 3 : 2) : true, "ring too shallow");
   static_assert(!T::SPLIT_MMA || (T::NSB == 2 && T::LOOKAHEAD), "split issue order");
-  static_assert(!T::DQ_BULK || T::DSPLIT == 1, "bulk dQ needs whole head-dim rows");
+  static_assert(T::DQ_BULK && T::DSPLIT == 1, "the dQ drain stages whole head-dim rows");
   static_assert(!T::DQ_BULK || (T::DQT ? BM : HD) / 4 == kDqChunks, "staged dQ tile layout");
   static_assert(T::DSPLIT == 1 || DV == HD, "a split head dim needs DV == HD");
   static_assert(DVH % 16 == 0 && DVH >= 16 && DVH <= 256, "dV MMA N");
@@ -613,7 +613,7 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
         }
         fence_proxy_async();  // staging writes -> visible to the bulk copy
         mbar_arrive(&stg_full);
-      } else if constexpr (T::DQ_BULK) {
+      } else {
         // lane = query row j, column = head-dim index: stage the row (HD f32) with its 16-byte
         // chunks XOR-rotated by (j & 15); the bulk warp adds the tile with one reduction
         float* stg = reinterpret_cast<float*>(smem + LY::OFF_STG);
@@ -636,43 +636,6 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
         }
         fence_proxy_async();  // staging writes -> visible to the bulk copy
         mbar_arrive(&stg_full);
-      } else if constexpr (T::DQT) {
-        // lane = head-dim index d, column = query row: add the tile straight from registers
-        // with 16-byte vector reductions in the chunk-major tile layout. No head dim selects
-        // this form at present: at head_dim 128 it measured slower than the staged bulk
-        // reduction (main pass 721 against 641 us on the 4k GQA shape).
-        static_assert(T::DSPLIT == 1 && BM / 4 == kDqChunks, "chunk-major dQ tile");
-        float4* dst = reinterpret_cast<float4*>(p.dqacc + ((size_t)bh * p.ql_pad + q0) * HD) + j;
-        uint32_t rq[BM / 32][32];
-#pragma unroll
-        for (int c32 = 0; c32 < BM / 32; ++c32) tmem_ld32(lane_base + colDQ + c32 * 32, rq[c32]);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&dq_free[it % 2]);
-#pragma unroll
-        for (int c = 0; c < BM / 4; ++c) {
-          const uint32_t* r = &rq[c / 8][(c % 8) * 4];
-          atomicAdd(dst + c * HD, make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]),
-                                              __uint_as_float(r[2]), __uint_as_float(r[3])));
-        }
-      } else {
-        // lane = query row, column = head-dim index (dQ formed without a staging tile; no
-        // head dim selects this form at present: head_dim 64 stages its tile)
-        float4* dst = reinterpret_cast<float4*>(p.dqacc + ((size_t)bh * p.ql_pad + q0 + j) * HD);
-        uint32_t rq[HD / 32][32];
-#pragma unroll
-        for (int c32 = 0; c32 < HD / 32; ++c32) tmem_ld32(lane_base + colDQ + c32 * 32, rq[c32]);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&dq_free[it % 2]);
-#pragma unroll
-        for (int c32 = 0; c32 < HD / 32; ++c32)
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            atomicAdd(dst + c32 * 8 + e,
-                      make_float4(__uint_as_float(rq[c32][4 * e]), __uint_as_float(rq[c32][4 * e + 1]),
-                                  __uint_as_float(rq[c32][4 * e + 2]),
-                                  __uint_as_float(rq[c32][4 * e + 3])));
       }
     };
 

@@ -120,3 +120,20 @@ def test_shared_page_is_reported():
     x = _problem(90, (2, 4, 2, 1, 128, 16, (40, 40)), shared=True)
     _run(x)
     assert fa.fa_device_status(True) == fa.FA_ERR_BAD_INPUT
+
+
+@pytest.mark.parametrize("lq", [1, 4], ids=["decode_path", "packed_path"])
+def test_table_entry_outside_the_cache_is_reported(lq):
+    """A used table entry past the cache reads as zero keys in both passes, writes no gradient
+    outside the caches and makes fa_device_status return FA_ERR_BAD_INPUT; the outputs stay
+    finite."""
+    import torch
+
+    import flash_attention_gb300 as fa
+
+    x = _problem(91, (2, 8, 2, lq, 128, 16, (40, 40)))
+    x["table"][1, 1] = x["P"] + 5  # (slot 1 holds keys 16 .. 31 of sequence 1)
+    dq, dk, dv = _run(x)
+    assert fa.fa_device_status(True) == fa.FA_ERR_BAD_INPUT
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        assert torch.isfinite(t.float()).all(), name
