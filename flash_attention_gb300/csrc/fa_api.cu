@@ -634,6 +634,9 @@ int fa_paged_attention_bwd(const void* q, const void* k_cache, const void* v_cac
   g.max_pages = p->max_pages;
   g.num_pages = p->num_pages;
   g.causal = p->causal;
+  g.ps_shift = 0;
+  while ((1 << g.ps_shift) < p->page_size) ++g.ps_shift;
+  g.cpr_shift = d == 64 ? 3 : d == 128 ? 4 : 5;
   if (fa::paged_decode_path(G, lq)) {
     // few query rows per kv head: the CUDA-core kernels read the pages directly
     if ((rc = check_device())) return rc;

@@ -262,6 +262,7 @@ struct PagedGradArgs {
                          // the page; -1 (set before the gather) none, -2 two or more
   int* status;
   int B, H, Hk, lq, d, ps, max_pages, num_pages, pack, causal;
+  int ps_shift, cpr_shift;  // log2 of page_size and of d / 8 (both powers of two)
 };
 // The offsets, the packed K, V (and the owner of every used page), the packed q-side tensors.
 cudaError_t launch_paged_gather(const PagedGradArgs& a, cudaStream_t stream);

@@ -99,17 +99,18 @@ __global__ void __launch_bounds__(256) paged_gather_kernel(PagedGradArgs a) {
   const int bkh = blockIdx.y, b = bkh / a.Hk, kh = bkh % a.Hk;
   const int cpr = a.d / 8;  // 16-byte chunks per row
   const long long e = (long long)blockIdx.x * 256 + threadIdx.x;
-  const long long r = e / cpr;
-  const int c = (int)(e % cpr);
+  const long long r = e >> a.cpr_shift;
+  const int c = (int)(e & (cpr - 1));
   const int k0 = a.cu_k[b], len = a.cu_k[b + 1] - k0;
   if (r >= len) return;
   const long long total_k = (long long)a.B * paged_cap(a);  // rows per head of k_pack
-  const int slot = (int)(r / a.ps);
+  const int slot = (int)(r >> a.ps_shift);
+  const int in_page = (int)(r & (a.ps - 1));
   const int page = a.table[(size_t)b * a.max_pages + slot];
-  const bool lead = kh == 0 && c == 0 && r % a.ps == 0;
+  const bool lead = kh == 0 && c == 0 && in_page == 0;
   uint4 kv = make_uint4(0, 0, 0, 0), vv = kv;
   if (page >= 0 && page < a.num_pages) {
-    const size_t src = (((size_t)page * a.Hk + kh) * a.ps + r % a.ps) * cpr + c;
+    const size_t src = (((size_t)page * a.Hk + kh) * a.ps + in_page) * cpr + c;
     kv = reinterpret_cast<const uint4*>(a.k_cache)[src];
     vv = reinterpret_cast<const uint4*>(a.v_cache)[src];
     if (lead && atomicCAS(a.owner + page, -1, b * a.max_pages + slot) != -1) {
@@ -178,9 +179,9 @@ __global__ void __launch_bounds__(256) paged_scatter_kernel(PagedGradArgs a) {
   const int cpr = a.d / 8;
   const long long e = (long long)blockIdx.x * 256 + threadIdx.x;
   if (e >= (long long)a.num_pages * a.ps * cpr) return;
-  const long long prow = e / cpr;  // page * ps + slot within the page
-  const int c = (int)(e % cpr);
-  const int page = (int)(prow / a.ps), s = (int)(prow % a.ps);
+  const long long prow = e >> a.cpr_shift;  // page * ps + slot within the page
+  const int c = (int)(e & (cpr - 1));
+  const int page = (int)(prow >> a.ps_shift), s = (int)(prow & (a.ps - 1));
   uint4 gk = make_uint4(0, 0, 0, 0), gv = gk;
   const int own = a.owner[page];
   if (own >= 0) {
@@ -219,6 +220,52 @@ __device__ __forceinline__ int clamped_len(const PagedGradArgs& a, int b) {
   const int len = a.lens[b];
   const long long cap = paged_cap(a);
   return len < 0 ? 0 : (len > cap ? (int)cap : len);
+}
+
+// Recursive halving of N sums over the lanes of a 2*O-lane group: at each level (offsets O,
+// O/2, ..., 1) a lane keeps the half of its C values that its lane bit selects and adds its
+// partner's copy of that half, sending the other; once one value is left the remaining levels
+// add the partner's value. The lane ends with halved_count values, those of indices idx0 ..
+__device__ __host__ constexpr int halved_count(int lanes, int n) {
+  while (lanes > 1 && n > 1) {
+    lanes /= 2;
+    n /= 2;
+  }
+  return n;
+}
+
+// The lane (within its group) that ends with the sum of value index r (< n / 2).
+__device__ __host__ constexpr int halved_holder(int r, int lanes, int n) {
+  const int cf = halved_count(lanes, n);
+  int rem = r - r % cf, holder = 0;
+  for (int k = 1; (n >> (k + 1)) >= cf && (lanes >> (k + 1)) >= 1; ++k) {
+    const int w = n >> (k + 1);  // the kept upper half at level k starts w values on
+    if (rem >= w) {
+      rem -= w;
+      holder |= lanes >> (k + 1);
+    }
+  }
+  return holder;
+}
+
+template <int O, int C, int N>
+__device__ __forceinline__ void halve_sums(float (&v)[N], int lane, int& idx0) {
+  if constexpr (O >= 1) {
+    if constexpr (C > 1) {
+      const bool up = (lane & O) != 0;
+#pragma unroll
+      for (int i = 0; i < C / 2; ++i) {
+        const float send = up ? v[i] : v[C / 2 + i];
+        const float keep = up ? v[C / 2 + i] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+      }
+      if (up) idx0 += C / 2;
+      halve_sums<O / 2, C / 2, N>(v, lane, idx0);
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+      halve_sums<O / 2, 1, N>(v, lane, idx0);
+    }
+  }
 }
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -323,10 +370,10 @@ __global__ void __launch_bounds__(kDecThreads, RMAX <= 4 ? 3 : 1) paged_decode_b
 
   // key j's cache row (page * Hk + kh) * ps + j % ps, or -1 (past the end / outside the cache)
   auto key_row = [&](int j, int& slot, int& page) -> long long {
-    slot = j / a.ps;
+    slot = j >> a.ps_shift;
     page = j < c1 ? a.table[(size_t)b * a.max_pages + slot] : -1;
     if (page < 0 || page >= a.num_pages) return -1;
-    return ((long long)page * a.Hk + kh) * a.ps + j % a.ps;
+    return ((long long)page * a.Hk + kh) * a.ps + (j & (a.ps - 1));
   };
   const int step = NW * KPW;
   int j = c0 + warp * KPW + kk;
@@ -368,27 +415,50 @@ __global__ void __launch_bounds__(kDecThreads, RMAX <= 4 ? 3 : 1) paged_decode_b
       sv[r] = s0;
       dpv[r] = d0;
     }
+    // the 2 * RMAX sums over the key row's LPK lanes by recursive halving: each lane ends with
+    // CF of them (s or dP of rows idx0 .. idx0 + CF - 1 of its half), P and dS are formed once
+    // per row, then every lane of the row gets all of them
+    float hv[2 * RMAX];
 #pragma unroll
-    for (int off = LPK / 2; off > 0; off >>= 1)
+    for (int r = 0; r < RMAX; ++r) {
+      hv[r] = sv[r];
+      hv[RMAX + r] = dpv[r];
+    }
+    int idx0 = 0;
+    halve_sums<LPK / 2, 2 * RMAX, 2 * RMAX>(hv, lane, idx0);
+    constexpr int CF = halved_count(LPK, 2 * RMAX);
+    const bool dp_lane = (lane & (LPK / 2)) != 0;  // lanes of the upper half hold the dP sums
+    const int r0 = dp_lane ? idx0 - RMAX : idx0;
+    float p_own[CF], ds_own[CF];
 #pragma unroll
-      for (int r = 0; r < RMAX; ++r) {
-        sv[r] += __shfl_xor_sync(0xffffffffu, sv[r], off);
-        dpv[r] += __shfl_xor_sync(0xffffffffu, dpv[r], off);
-      }
+    for (int i = 0; i < CF; ++i) {
+      const float other = __shfl_xor_sync(0xffffffffu, hv[i], LPK / 2);
+      const float s_r = dp_lane ? other : hv[i], dp_r = dp_lane ? hv[i] : other;
+      const int r = r0 + i;
+      const float l2 = sl2[r];
+      const bool vis = live && r < R && jc < shi[r] && l2 != -INFINITY;
+      p_own[i] = vis ? ex2(s_r * scale_log2 - l2) : 0.0f;
+      ds_own[i] = p_own[i] * (dp_r - sdd[r]);
+    }
+    const int group = lane & ~(LPK - 1);
+    float pr[RMAX], dsr[RMAX];
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) {
+      constexpr int cf = CF;
+      const int src = group + halved_holder(r, LPK, 2 * RMAX);
+      pr[r] = __shfl_sync(0xffffffffu, p_own[r % cf], src);
+      dsr[r] = __shfl_sync(0xffffffffu, ds_own[r % cf], src);
+    }
     float dk[8], dv[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) dk[e] = dv[e] = 0.0f;
 #pragma unroll
     for (int r = 0; r < RMAX; ++r) {
-      const float l2 = sl2[r];
-      const bool vis = live && r < R && jc < shi[r] && l2 != -INFINITY;
-      const float pr = vis ? exp2f(sv[r] * scale_log2 - l2) : 0.0f;
-      const float ds = pr * (dpv[r] - sdd[r]);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        dk[e] += ds * qr[r][e];
-        dv[e] += pr * gr[r][e];
-        dq[r][e] += ds * kf[e];
+        dk[e] += dsr[r] * qr[r][e];
+        dv[e] += pr[r] * gr[r][e];
+        dq[r][e] += dsr[r] * kf[e];
       }
     }
     // this sequence's own page only: a page claimed twice (or none) is zero-filled later
@@ -432,9 +502,9 @@ __global__ void __launch_bounds__(256) paged_fill_kernel(PagedGradArgs a) {
   const int cpr = a.d / 8;
   const long long e = (long long)blockIdx.x * 256 + threadIdx.x;
   if (e >= (long long)a.num_pages * a.ps * cpr) return;
-  const long long prow = e / cpr;
-  const int c = (int)(e % cpr);
-  const int page = (int)(prow / a.ps), s = (int)(prow % a.ps);
+  const long long prow = e >> a.cpr_shift;
+  const int c = (int)(e & (cpr - 1));
+  const int page = (int)(prow >> a.ps_shift), s = (int)(prow & (a.ps - 1));
   const int own = a.owner[page];
   if (own >= 0 && (long long)(own % a.max_pages) * a.ps + s < clamped_len(a, own / a.max_pages))
     return;
