@@ -54,6 +54,8 @@ KERNEL_SOURCES = {
                           "flash_attention_gb300/csrc/fa_band.cuh"],
     "paged_attn_kernel": ["flash_attention_gb300/csrc/fa_paged.cu",
                           "flash_attention_gb300/csrc/fa_common.cuh"],
+    "paged_decode_bwd_kernel": ["flash_attention_gb300/csrc/fa_paged_bwd.cu",
+                                "flash_attention_gb300/csrc/fa_common.cuh"],
 }
 # at head_dim 256 the backward main pass is the CTA-pair kernel (timed under the same name)
 PAIR_SOURCES = ["flash_attention_gb300/csrc/fa_bwd_pair.cu",
@@ -584,7 +586,7 @@ def run_paged(args, w, grad=False):
     roofline = {"bound": "hbm", "kernel": dom,
                 "achieved": kern_bytes[dom] / (kern_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
                 "frac": kern_bytes[dom] / (kern_ms * 1e-3) / 1e9 / hbm,
-                "traffic": recorded_traffic(dom, w.name) if not grad else None,
+                "traffic": recorded_traffic(dom, w.name + ("_grad" if grad else "")),
                 "peak_source": f"hbm_gbs, {peaks['source']}",
                 "per_kernel_ms": {k: (t / max(c, 1)) for k, (t, c) in prof.items() if c}}
     launches = sum(c for _, c in prof.values())
