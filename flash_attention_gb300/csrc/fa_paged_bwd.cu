@@ -225,7 +225,8 @@ __device__ __forceinline__ int clamped_len(const PagedGradArgs& a, int b) {
 // Recursive halving of N sums over the lanes of a 2*O-lane group: at each level (offsets O,
 // O/2, ..., 1) a lane keeps the half of its C values that its lane bit selects and adds its
 // partner's copy of that half, sending the other; once one value is left the remaining levels
-// add the partner's value. The lane ends with halved_count values, those of indices idx0 ..
+// add the partner's value. The lane ends with halved_count(2*O, N) sums, those of value
+// indices idx0 .. idx0 + halved_count - 1 (idx0 accumulates the kept halves' offsets).
 __device__ __host__ constexpr int halved_count(int lanes, int n) {
   while (lanes > 1 && n > 1) {
     lanes /= 2;
@@ -295,14 +296,14 @@ __global__ void __launch_bounds__(256) paged_owner_kernel(PagedGradArgs a) {
 // head kh * G + r / q_len, query r % q_len; it sees keys j < length, and under the causal rule
 // j <= length - q_len + r % q_len. A key row is LPK = D / 8 lanes (16 bytes, 8 elements
 // each); a warp step takes KPW = 32 / LPK keys. A lane always holds the same 8 columns, so it
-// keeps those columns of every row's q and dO in registers for the whole block. Dot products
-// over the key row are summed across its lanes with shuffles. RMAX: the row bound the
-// registers are sized for (4 or kDecRows). The kernel is bound by latency and issue, not by
-// HBM: measured on the 16-sequence decode workload (d=128, 4 rows), 128-thread blocks at 3 per
-// SM with q/dO in f32 registers took 369 us (325 us once the row sums were halved instead of
-// butterflied); 256 threads at 1 per SM 573 us; q/dO read from shared memory at each key (256
-// threads, 2 per SM) 677 us; bf16 q/dO pairs at 4 blocks of 128 per SM (spilling) 427 us; two
-// key steps in flight per warp instead of one 354 us.
+// keeps those columns of every row's q and dO in registers for the whole block. The dot
+// products over a key row are summed across its lanes by recursive halving. RMAX: the row
+// bound the registers are sized for (4 or kDecRows). The kernel is bound by latency and issue,
+// not by HBM. Measured on the 16-sequence decode workload (d=128, 4 rows): 128-thread blocks
+// at 3 per SM with q/dO in f32 registers took 369 us (325 us once the row sums were halved
+// instead of butterflied); 256 threads at 1 per SM 573 us; q/dO read from shared memory at
+// each key (256 threads, 2 per SM) 677 us; bf16 q/dO pairs at 4 blocks of 128 per SM
+// (spilling) 427 us; two key steps in flight per warp instead of one 354 us.
 constexpr int kDecThreads = 128;
 template <int D, int RMAX>
 __global__ void __launch_bounds__(kDecThreads, RMAX <= 4 ? 3 : 1) paged_decode_bwd_kernel(
