@@ -215,11 +215,12 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
 
 // dQ = bf16(scale * accumulator) from the transposed, chunk-major accumulator tiles of the
 // bulk path. Grid: x = (query tile of BM rows, 64-row slice of the head dimension), y =
-// (batch, head) (strided); blocks with x == 0 also finish dsinks. A block reads its slice (64 head-dim rows of BM f32) with all of
-// its 16-byte loads in flight and transposes it through shared memory into [q][d] (rows padded
-// to 65 floats); then four consecutive threads write one query row's 128 contiguous bytes of
-// bf16. Both sides are touched once, so loads and stores are marked evict-first (35.1 against
-// 37.6 us on the 4k GQA shape).
+// (batch, head) (strided); blocks with x == 0 also finish dsinks. A block reads its slice (64
+// head-dim rows of BM f32) with all of its 16-byte loads in flight and transposes it through
+// shared memory into [q][d] (rows padded to 65 floats, written conflict-free since a warp's
+// loads cover one chunk of 32 consecutive rows); then four consecutive threads write one
+// query row's 128 contiguous bytes of bf16. Both sides are touched once, so loads and stores
+// are marked evict-first (35.1 against 37.6 us on the 4k GQA shape).
 template <int HD, int BM>
 __global__ void __launch_bounds__(256) bwd_dq_tiles_kernel(const float* __restrict__ dqacc,
                                                            __nv_bfloat16* __restrict__ dq,
