@@ -67,6 +67,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   static_assert(RPB * ROWS == prep_rows_per_block<DV>(), "prep chunk");
   static_assert(RPB * ROWS >= kPrepRowsMin && RPB * ROWS <= 256, "sink partial layout");
   __shared__ float sink_terms[RPB * ROWS];
+  grid_dep_wait();  // (launched to overlap the previous kernel's tail: O may be its output)
+  grid_dep_trigger();
   const int sub = threadIdx.x % TPR;
   const int i0 = blockIdx.x * RPB * ROWS;  // first row of the chunk (ql_pad is a multiple)
   const bool want_dsink = dsink_part != nullptr;
@@ -185,6 +187,7 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
                                                      int sink_chunks, int convert,
                                                      const int32_t* __restrict__ cu_q,
                                                      int total_q, int q_bshd) {
+  grid_dep_wait();  // the accumulator and the dsinks partials are the previous kernels' output
   if (dsinks != nullptr && blockIdx.x == 0) dsinks_sum(dsink_part, dsinks, B, H, sink_chunks);
   if (!convert) return;
   const int e = blockIdx.x * 256 + threadIdx.x;  // index of the 8-value group within a head
@@ -237,6 +240,7 @@ __global__ void __launch_bounds__(256) bwd_dq_tiles_kernel(const float* __restri
   static_assert(BM / 4 == kDqChunks && DR % kDqChunks == 0 && NV * 256 == DR * kDqChunks &&
                     BM * (DR / 16) == 256,
                 "tile layout");
+  grid_dep_wait();  // the accumulator and the dsinks partials are the previous kernels' output
   if (dsinks != nullptr && blockIdx.x == 0) dsinks_sum(dsink_part, dsinks, B, H, sink_chunks);
   __shared__ float tile[BM][DR + 1];
   const int q0 = (blockIdx.x / NB) * BM, d0 = (blockIdx.x % NB) * DR;
@@ -319,11 +323,11 @@ static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t
   {
     dim3 grid(sink_chunks, BH < 65535 ? BH : 65535);
     profile_mark(kKernBwdPrep, 0, s);
-    bwd_prep_kernel<HD, DV><<<grid, 256, 0, s>>>(
+    cudaError_t e = launch_pdl(
+        bwd_prep_kernel<HD, DV>, grid, dim3(256), 0, s,
         reinterpret_cast<const __nv_bfloat16*>(a.o), reinterpret_cast<const __nv_bfloat16*>(a.dO),
         a.lse, a.lse2, a.dvec, a.dqacc, a.sinks, dsink_part, BH, a.H, a.ql, a.ql_pad,
         a.deterministic ? 0 : 1, a.cu_q, a.total_q, a.q_bshd);
-    cudaError_t e = cudaGetLastError();
     profile_mark(kKernBwdPrep, 1, s);
     if (e != cudaSuccess) return e;
   }
@@ -351,18 +355,21 @@ static cudaError_t launch_bwd_d(const BwdArgs& a, const BwdMaps& m, cudaStream_t
     constexpr int BM = BwdTraits<HD>::BM;
     dim3 grid((unsigned)((a.ql + BM - 1) / BM * (HD / 64)), BH < 65535 ? BH : 65535);
     profile_mark(kKernBwdDq, 0, s);
-    bwd_dq_tiles_kernel<HD, BM><<<grid, 256, 0, s>>>(
-        a.dqacc, reinterpret_cast<__nv_bfloat16*>(a.dq), BH, a.ql, a.ql_pad, a.scale, dsink_part,
-        a.dsinks, a.B, a.H, sink_chunks, a.cu_q, a.total_q, a.q_bshd);
+    e = launch_pdl(bwd_dq_tiles_kernel<HD, BM>, grid, dim3(256), 0, s, a.dqacc,
+                   reinterpret_cast<__nv_bfloat16*>(a.dq), BH, a.ql, a.ql_pad, a.scale,
+                   dsink_part, a.dsinks, a.B, a.H, sink_chunks, a.cu_q, a.total_q, a.q_bshd);
     profile_mark(kKernBwdDq, 1, s);
+    if (e != cudaSuccess) return e;
   } else {
     const long long groups = (long long)a.ql * (HD / 8);  // 8-value groups per head
     dim3 grid((unsigned)((groups + 255) / 256), BH < 65535 ? BH : 65535);
     profile_mark(kKernBwdDq, 0, s);
-    bwd_dq_kernel<HD, BwdTraits<HD>::DQ_BULK><<<grid, 256, 0, s>>>(
-        a.dqacc, reinterpret_cast<__nv_bfloat16*>(a.dq), BH, a.ql, a.ql_pad, a.scale, dsink_part,
-        a.dsinks, a.B, a.H, sink_chunks, 1, a.cu_q, a.total_q, a.q_bshd);
+    e = launch_pdl(bwd_dq_kernel<HD, BwdTraits<HD>::DQ_BULK>, grid, dim3(256), 0, s, a.dqacc,
+                   reinterpret_cast<__nv_bfloat16*>(a.dq), BH, a.ql, a.ql_pad, a.scale,
+                   dsink_part, a.dsinks, a.B, a.H, sink_chunks, 1, a.cu_q, a.total_q,
+                   a.q_bshd);
     profile_mark(kKernBwdDq, 1, s);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

@@ -158,6 +158,10 @@ __global__ void __launch_bounds__(BwdLayout<HD, DV>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_base_s;
+  // the prologue above overlaps the pre-pass's tail; L, D and the zeroed accumulator are its
+  // output
+  grid_dep_wait();
+  grid_dep_trigger();
 
   if (warp == LY::TMA_WARP) {
     // ------------------------------------------------------------------ TMA producer
@@ -779,8 +783,8 @@ static cudaError_t launch_main_t(const BwdArgs& a, const BwdMaps& m, cudaStream_
   kp.tiles_fast = a.cu_q != nullptr && groups <= 65535;  // (grid y limit)
   dim3 grid(kp.tiles_fast ? ktiles : groups, kp.tiles_fast ? groups : ktiles);
   profile_mark(kKernBwdMain, 0, s);
-  kern<<<grid, LY::THREADS, LY::SMEM_BYTES, s>>>(m.q, m.k, m.v, m.dO, kp);
-  cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_pdl(kern, grid, dim3(LY::THREADS), LY::SMEM_BYTES, s, m.q, m.k,
+                                   m.v, m.dO, kp);
   profile_mark(kKernBwdMain, 1, s);
   return e;
 }

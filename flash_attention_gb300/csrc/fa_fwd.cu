@@ -250,6 +250,9 @@ __global__ void __launch_bounds__(FwdLayout<HD, DV>::THREADS, FwdLayout<HD, DV>:
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_base_s;
+  // a following kernel launched with programmatic serialisation (the backward's pre-pass) may
+  // be scheduled once every CTA of this grid is resident; it waits for this grid's completion
+  grid_dep_trigger();
 
   if (warp == LY::TMA_WARP) {
     // ------------------------------------------------------------------ TMA producer

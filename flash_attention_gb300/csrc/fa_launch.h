@@ -54,6 +54,25 @@ enum KernelId {
 // enabled; does nothing otherwise. Defined in fa_api.cu.
 void profile_mark(int kernel, int end, cudaStream_t s);
 
+// Launches `kernel` with programmatic stream serialisation: it may be scheduled before the
+// previous kernel of `s` completes and must call grid_dep_wait() before it touches memory that
+// kernel writes or reads.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Sets a kernel's dynamic shared-memory limit on the current device, once per device and
 // thread-safely (the attribute belongs to a device context, so a process that drives several
 // GPUs sets it on each).
