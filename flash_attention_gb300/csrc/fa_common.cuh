@@ -44,18 +44,6 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
-// ----------------------------------------------------------- programmatic dependent launch
-// A kernel launched with programmatic stream serialisation may start while the previous
-// kernel of its stream still runs; grid_dep_wait() returns once that kernel has completed and
-// its memory is visible (at once for a kernel launched without it). grid_dep_trigger() lets
-// the next such kernel be scheduled once every CTA of this grid has issued it or exited.
-__device__ __forceinline__ void grid_dep_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void grid_dep_trigger() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 // ----------------------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));

@@ -54,6 +54,17 @@ enum KernelId {
 // enabled; does nothing otherwise. Defined in fa_api.cu.
 void profile_mark(int kernel, int end, cudaStream_t s);
 
+// A kernel launched with programmatic stream serialisation may start while the previous
+// kernel of its stream still runs; grid_dep_wait() returns once that kernel has completed and
+// its memory is visible (at once for a kernel launched without it). grid_dep_trigger() lets
+// the next such kernel be scheduled once every CTA of this grid has issued it or exited.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Launches `kernel` with programmatic stream serialisation: it may be scheduled before the
 // previous kernel of `s` completes and must call grid_dep_wait() before it touches memory that
 // kernel writes or reads.
