@@ -751,6 +751,46 @@ def pin_paged_bwd_vs_torch_autograd():
     return fails
 
 
+def pin_paged_bwd_vs_finite_differences():
+    """The paged gradients against f64 central differences (Richardson-extrapolated, steps
+    2^-8 and 2^-9, exact for bf16-valued inputs) of loss = sum(O * dO) through the oracle's
+    paged forward, for every element of q and of both caches on a tiny causal multi-query
+    problem with shuffled pages, a partly filled last page and a page nobody uses."""
+    import fa_inputs
+
+    fails = []
+    B, H, Hk, lq, d, bs, lens = 2, 2, 1, 2, 4, 4, (5, 3)
+    P = 2 * 2 + 1
+    table = np.array([[3, 0], [4, 2]], np.int32)  # page 1 unused; sequence 1 uses one page
+    q = fa_inputs.bf16_bits_to_f32(fa_inputs.normal_bf16(950, (B, H, lq, d)))
+    kc = fa_inputs.bf16_bits_to_f32(fa_inputs.normal_bf16(951, (P, Hk, bs, d)))
+    vc = fa_inputs.bf16_bits_to_f32(fa_inputs.normal_bf16(952, (P, Hk, bs, d)))
+    do = fa_inputs.bf16_bits_to_f32(fa_inputs.normal_bf16(953, (B, H, lq, d)))
+    lens_a = np.asarray(lens, np.int32)
+    scale = 0.45
+    dq, dk, dv = oracle.paged_bwd(q, kc, vc, table, lens_a, do, scale=scale, causal=True)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.paged_fwd(qq, kk, vv, table, lens_a, scale=scale, causal=True)
+        return float((o * do.astype(np.float64)).sum())
+
+    for name, arr, grad in (("q", q, dq), ("k cache", kc, dk), ("v cache", vc, dv)):
+        num = np.zeros(arr.shape)
+        for idx in np.ndindex(arr.shape):
+            ests = []
+            for h in (2.0 ** -8, 2.0 ** -9):
+                plus, minus = arr.copy(), arr.copy()
+                plus[idx] += np.float32(h)
+                minus[idx] -= np.float32(h)
+                args_p = {"q": (plus, kc, vc), "k cache": (q, plus, vc), "v cache": (q, kc, plus)}
+                args_m = {"q": (minus, kc, vc), "k cache": (q, minus, vc),
+                          "v cache": (q, kc, minus)}
+                ests.append((loss(*args_p[name]) - loss(*args_m[name])) / (2 * h))
+            num[idx] = (4 * ests[1] - ests[0]) / 3
+        _cmp(f"paged FD d{name}", grad, num, tol=2e-7, out=fails)
+    return fails
+
+
 # ------------------------------------------------------------------ variable-length batches
 VARLEN_CASES = [
     # (H, Hk, d, q_lens, k_lens, causal)
@@ -885,6 +925,7 @@ ALL_PINS = [
     pin_paged_vs_torch,
     pin_paged_layout_invariance,
     pin_paged_bwd_vs_torch_autograd,
+    pin_paged_bwd_vs_finite_differences,
     pin_varlen_vs_torch,
     pin_mask_forms_vs_torch,
 ]
