@@ -439,7 +439,7 @@ def paged_grad_oracle_sample(w, x, do_bits, total_bytes, budget_s=10.0, cores=No
     return nbytes, spent, n
 
 
-def run_paged_reference(args, w):
+def run_paged_reference(args, w, grad=False):
     rank, world, _ = dist_env()
     if rank != 0:
         return
@@ -449,22 +449,35 @@ def run_paged_reference(args, w):
     x = fa_inputs.make_paged_inputs(w)
     cores = cpu_cores()
     per_step = max(1.0, 120.0 / max(args.steps + args.warmup, 1))
+    if grad:
+        do_bits = fa_inputs.normal_bf16(fa_inputs.SEED_BASE + 77, tuple(x.q.shape), 0.1)
+        step_bytes = paged_grad_bytes(w, x)[0]
+
+        def sample(budget):
+            return paged_grad_oracle_sample(w, x, do_bits, step_bytes, budget, cores)
+    else:
+        def sample(budget):
+            return paged_oracle_sample(w, x, budget, cores)
     for _ in range(args.warmup):
-        paged_oracle_sample(w, x, min(per_step, 2.0), cores)
+        sample(min(per_step, 2.0))
     tot_b, tot_s = 0, 0.0
     for _ in range(args.steps):
-        b_, s_, _ = paged_oracle_sample(w, x, per_step, cores)
+        b_, s_, _ = sample(per_step)
         tot_b += b_
         tot_s += s_
     value = tot_b / tot_s / 1e9
-    out = {"impl": "reference", "metric": PAGED_METRIC, "value": value, "unit": "GB/s",
+    cfg = paged_config(w, args.gpus)
+    if grad:
+        cfg["workload"] = w.name + "_grad"
+    out = {"impl": "reference", "metric": PAGED_GRAD_METRIC if grad else PAGED_METRIC,
+           "value": value, "unit": "GB/s",
            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": tot_s / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
-           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": paged_config(w, args.gpus),
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                             "sample": "per step: whole sequences in turn for ~"
-                                      f"{per_step:.0f} s of the CPU oracle"},
+                                      f"{per_step:.0f} s of the CPU oracle"
+                                      + (" (forward + gradients)" if grad else "")},
            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
@@ -1168,8 +1181,7 @@ def main():
     if args.workload in PAGED_GRAD:
         w = fa_inputs.DECODE_BY_NAME[PAGED_GRAD[args.workload]]
         if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times "
-                              "the oracle's paged forward only"}), flush=True)
+            run_paged_reference(args, w, grad=True)
         else:
             run_paged(args, w, grad=True)
         return
