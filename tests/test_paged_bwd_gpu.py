@@ -30,6 +30,8 @@ CASES = [
     (3, 4, 2, 3, 128, 16, (0, 2, 40)),  # an empty sequence and one shorter than q_len
     (2, 4, 2, 3, 128, 16, (30, 77), False),  # no causal rule: the query heads packed as rows
     (2, 16, 2, 1, 64, 8, (104, 64)),  # 8 query heads per kv head; a sequence at capacity
+    (2, 8, 2, 2, 256, 16, (40, 900)),  # 8 rows per kv head at head dim 256 (causal, 2 queries)
+    (2, 4, 1, 1, 64, 16, (700, 33)),   # 4 rows per kv head at head dim 64, several key blocks
 ]
 
 
