@@ -308,7 +308,10 @@ __global__ void __launch_bounds__(256) paged_owner_kernel(PagedGradArgs a) {
 // each key (256 threads, 2 per SM) 677 us; bf16 q/dO pairs at 4 blocks of 128 per SM
 // (spilling) 427 us; two key steps in flight per warp instead of one 354 us; the block's
 // page numbers and owners read into shared memory up front instead of the table at each key
-// 333 against 320 us.
+// 333 against 320 us; keys streamed through a 4-stage cp.async ring in shared memory (each
+// lane copying and reading back its own chunks) 296.8 against 299.7 us at 512 keys per block,
+// not worth its code: the kernel is issue-bound once a step's loads overlap the previous
+// step's arithmetic.
 constexpr int kDecThreads = 128;
 template <int D, int RMAX>
 __global__ void __launch_bounds__(kDecThreads, RMAX <= 4 ? 3 : 1) paged_decode_bwd_kernel(
